@@ -1,0 +1,344 @@
+// ORACLE — test infrastructure only.
+//
+// A plain, slow, obviously-correct CPU model of the importance-aware,
+// budgeted KV-cache decode step.  Only the tests, the smoke check and the
+// benchmark's CPU-baseline leg may load it.  It shares no code, header or
+// constant with the CUDA library.
+//
+// Data are fp32 (bf16 inputs widened exactly); every reduction is in double.
+// Per unit (layer, batch, KV head) it keeps a list of entries sorted by
+// original position; physical order is irrelevant because attention is
+// invariant to permuting (k, v) pairs (Kelle summary, sec. 2.2, eq. 1-2).
+//
+// Step by step, with the passage each follows:
+//  * attention      P = softmax(s), s_j = scale * <q_h, k_j>, o_h = sum_j p_hj v_j
+//                   (HiKV sec. II-A; Kelle summary sec. 2.2 eq. 1-2).  The scale
+//                   is 1/sqrt(d) unless the caller gives one (the pages write
+//                   softmax(QK^T) without it; the standard scaled dot product is
+//                   the reading taken).
+//  * importance     imp_j += sum over the G query heads of the KV group of p_hj
+//                   (H2O cumulative score, KV cache compression blog sec. 3
+//                   "H2O"; pooled over the query heads sharing a KV head, blog
+//                   sec. 5.2; per-head score, Kelle summary sec. 4.1 eq. 3).
+//                   The head sum is formed in double and rounded once to
+//                   float; the running score is a float32 add.
+//  * window score   prefill importance = the attention columns of the last nq
+//                   prompt queries, causally masked, summed (HiKV sec. III-D;
+//                   SnapKV observation window, blog sec. 3).  Queries are
+//                   applied in position order.
+//  * eviction       when n > B: sinks (pos < S) and the recent window
+//                   (pos > t - W) are always kept; of the rest keep the
+//                   B - S - W with the largest importance, ties by lowest
+//                   position; the others are evicted (blog sec. 3 "H2O",
+//                   StreamingLLM sinks + window; budget per head, HeadKV
+//                   summary sec. 3.2).  Survivors keep their scores.
+//  * outputs        rounded once from double to the output type (fp32 or bf16
+//                   round-to-nearest-even).
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <thread>
+#include <vector>
+
+namespace {
+
+struct Entry {
+    int32_t pos;
+    float imp;
+    std::vector<float> k, v;
+};
+
+struct Unit {
+    std::vector<Entry> e;            // retained, ascending pos
+    std::vector<Entry> last_evicted; // entries removed by the latest evict
+    int32_t next_pos = 0;            // positions appended so far
+    double evicted_mass = 0.0;       // sum of imp of every evicted entry
+};
+
+struct Oracle {
+    int L, B, Hq, Hkv, d, G, S, W;
+    double scale;
+    int out_bf16;
+    int nthreads;
+    std::vector<int32_t> budget;     // [L * Hkv]
+    std::vector<Unit> units;         // [L][B][Hkv]
+    int unit_index(int l, int b, int g) const { return (l * B + b) * Hkv + g; }
+    int budget_of(int u) const {
+        int g = u % Hkv;
+        int l = u / (B * Hkv);
+        return budget[l * Hkv + g];
+    }
+};
+
+// Round a double to the nearest bf16 value (ties to even) and return it as float.
+float round_bf16(double x) {
+    if (x == 0.0 || !std::isfinite(x)) return (float)x;
+    int e;
+    double m = std::frexp(x, &e);          // x = m * 2^e, 0.5 <= |m| < 1
+    double scaled = m * 256.0;             // 8 significant bits
+    double r = std::nearbyint(scaled);     // default mode: ties to even
+    return (float)std::ldexp(r / 256.0, e);
+}
+
+template <class F>
+void parallel_units(int nthreads, int n, F f) {
+    if (nthreads <= 1 || n <= 1) {
+        for (int i = 0; i < n; ++i) f(i);
+        return;
+    }
+    int t = std::min(nthreads, n);
+    std::vector<std::thread> th;
+    for (int w = 0; w < t; ++w)
+        th.emplace_back([&, w] {
+            for (int i = w; i < n; i += t) f(i);
+        });
+    for (auto& x : th) x.join();
+}
+
+// softmax weights of one query over the entries `e` whose pos <= max_pos.
+// Returns p (0 for masked entries) and writes the unnormalised output sum.
+void attend(const Oracle& O, const std::vector<Entry>& e, const float* q,
+            int32_t max_pos, std::vector<double>& p, double* o /* [d] or null */) {
+    size_t n = e.size();
+    p.assign(n, 0.0);
+    std::vector<double> s(n, 0.0);
+    double m = -INFINITY;
+    for (size_t j = 0; j < n; ++j) {
+        if (e[j].pos > max_pos) continue;
+        double acc = 0.0;
+        for (int c = 0; c < O.d; ++c) acc += (double)q[c] * (double)e[j].k[c];
+        s[j] = O.scale * acc;
+        m = std::max(m, s[j]);
+    }
+    double l = 0.0;
+    for (size_t j = 0; j < n; ++j)
+        if (e[j].pos <= max_pos) l += std::exp(s[j] - m);
+    for (size_t j = 0; j < n; ++j)
+        if (e[j].pos <= max_pos) p[j] = std::exp(s[j] - m) / l;
+    if (o) {
+        for (int c = 0; c < O.d; ++c) o[c] = 0.0;
+        for (size_t j = 0; j < n; ++j) {
+            if (p[j] == 0.0) continue;
+            for (int c = 0; c < O.d; ++c) o[c] += p[j] * (double)e[j].v[c];
+        }
+    }
+}
+
+bool range_ok(const Oracle* O, int layer0, int nl) {
+    return O && layer0 >= 0 && nl >= 0 && layer0 + nl <= O->L;
+}
+
+}  // namespace
+
+extern "C" {
+
+void* ora_create(int L, int B, int Hq, int Hkv, int d, int S, int W,
+                 const int32_t* budgets, double scale, int out_bf16, int nthreads) {
+    if (L <= 0 || B <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv) return nullptr;
+    Oracle* O = new Oracle();
+    O->L = L; O->B = B; O->Hq = Hq; O->Hkv = Hkv; O->d = d; O->G = Hq / Hkv;
+    O->S = S; O->W = W;
+    O->scale = scale > 0 ? scale : 1.0 / std::sqrt((double)d);
+    O->out_bf16 = out_bf16;
+    O->nthreads = nthreads > 0 ? nthreads : 1;
+    O->budget.assign(budgets, budgets + L * Hkv);
+    O->units.resize((size_t)L * B * Hkv);
+    return O;
+}
+
+void ora_destroy(void* h) { delete (Oracle*)h; }
+
+int ora_num_threads(void* h, int n) {
+    Oracle* O = (Oracle*)h;
+    if (n > 0) O->nthreads = n;
+    return O->nthreads;
+}
+
+// k, v: [nl][B][Hkv][ntok][d] fp32.  New entries get imp = 0 and the next
+// positions of their unit.
+int ora_append(void* h, int layer0, int nl, int ntok, const float* k, const float* v) {
+    Oracle* O = (Oracle*)h;
+    if (!range_ok(O, layer0, nl) || ntok < 0) return 1;
+    int per_layer = O->B * O->Hkv;
+    parallel_units(O->nthreads, nl * per_layer, [&](int i) {
+        int u = layer0 * per_layer + i;
+        Unit& U = O->units[u];
+        const float* kb = k + (size_t)i * ntok * O->d;
+        const float* vb = v + (size_t)i * ntok * O->d;
+        for (int t = 0; t < ntok; ++t) {
+            Entry en;
+            en.pos = U.next_pos++;
+            en.imp = 0.0f;
+            en.k.assign(kb + (size_t)t * O->d, kb + (size_t)(t + 1) * O->d);
+            en.v.assign(vb + (size_t)t * O->d, vb + (size_t)(t + 1) * O->d);
+            U.e.push_back(std::move(en));
+        }
+        U.last_evicted.clear();
+    });
+    return 0;
+}
+
+// Prefill importance: q [nl][B][Hq][nq][d] are the queries of the last nq
+// appended positions.  Query i (position t-nq+1+i) sees entries with
+// pos <= its own position.  Applied in position order.
+int ora_score_window(void* h, int layer0, int nl, int nq, const float* q) {
+    Oracle* O = (Oracle*)h;
+    if (!range_ok(O, layer0, nl) || nq < 0) return 1;
+    int per_layer = O->B * O->Hkv;
+    parallel_units(O->nthreads, nl * per_layer, [&](int i) {
+        int u = layer0 * per_layer + i;
+        Unit& U = O->units[u];
+        int li = i / per_layer, b = (i / O->Hkv) % O->B, g = i % O->Hkv;
+        int32_t t = U.next_pos - 1;
+        std::vector<double> p, colsum;
+        for (int qi = 0; qi < nq; ++qi) {
+            int32_t qpos = t - nq + 1 + qi;
+            colsum.assign(U.e.size(), 0.0);
+            for (int hh = 0; hh < O->G; ++hh) {
+                int head = g * O->G + hh;
+                const float* qv = q + ((((size_t)li * O->B + b) * O->Hq + head) * nq + qi) * O->d;
+                attend(*O, U.e, qv, qpos, p, nullptr);
+                for (size_t j = 0; j < U.e.size(); ++j) colsum[j] += p[j];
+            }
+            for (size_t j = 0; j < U.e.size(); ++j) {
+                float inc = (float)colsum[j];
+                U.e[j].imp = U.e[j].imp + inc;
+            }
+        }
+    });
+    return 0;
+}
+
+// One decode step: q [nl][B][Hq][d] -> out [nl][B][Hq][d] (float values,
+// rounded to the output type).  Every retained entry is attended,
+// including the one appended for this step.
+int ora_decode(void* h, int layer0, int nl, const float* q, float* out) {
+    Oracle* O = (Oracle*)h;
+    if (!range_ok(O, layer0, nl)) return 1;
+    int per_layer = O->B * O->Hkv;
+    for (int i = 0; i < nl * per_layer; ++i)
+        if (O->units[layer0 * per_layer + i].e.empty()) return 2;
+    parallel_units(O->nthreads, nl * per_layer, [&](int i) {
+        int u = layer0 * per_layer + i;
+        Unit& U = O->units[u];
+        int li = i / per_layer, b = (i / O->Hkv) % O->B, g = i % O->Hkv;
+        std::vector<double> p, colsum(U.e.size(), 0.0), o(O->d);
+        for (int hh = 0; hh < O->G; ++hh) {
+            int head = g * O->G + hh;
+            size_t row = (((size_t)li * O->B + b) * O->Hq + head) * O->d;
+            attend(*O, U.e, q + row, INT32_MAX, p, o.data());
+            for (size_t j = 0; j < U.e.size(); ++j) colsum[j] += p[j];
+            for (int c = 0; c < O->d; ++c)
+                out[row + c] = O->out_bf16 ? round_bf16(o[c]) : (float)o[c];
+        }
+        for (size_t j = 0; j < U.e.size(); ++j) {
+            float inc = (float)colsum[j];
+            U.e[j].imp = U.e[j].imp + inc;
+        }
+    });
+    return 0;
+}
+
+// Cut every unit of the range with n > B to exactly B entries.
+int ora_evict(void* h, int layer0, int nl) {
+    Oracle* O = (Oracle*)h;
+    if (!range_ok(O, layer0, nl)) return 1;
+    int per_layer = O->B * O->Hkv;
+    parallel_units(O->nthreads, nl * per_layer, [&](int i) {
+        int u = layer0 * per_layer + i;
+        Unit& U = O->units[u];
+        U.last_evicted.clear();
+        int Bu = O->budget_of(u);
+        int n = (int)U.e.size();
+        if (n <= Bu) return;
+        int32_t t = U.next_pos - 1;
+        std::vector<Entry> keep, cand;
+        for (auto& en : U.e) {
+            bool prot = en.pos < O->S || en.pos > t - O->W;
+            if (prot) keep.push_back(std::move(en));
+            else cand.push_back(std::move(en));
+        }
+        std::sort(cand.begin(), cand.end(), [](const Entry& a, const Entry& b) {
+            if (a.imp != b.imp) return a.imp > b.imp;
+            return a.pos < b.pos;
+        });
+        int kmid = Bu - (int)keep.size();
+        if (kmid < 0) kmid = 0;
+        if (kmid > (int)cand.size()) kmid = (int)cand.size();
+        for (int j = 0; j < (int)cand.size(); ++j) {
+            if (j < kmid) keep.push_back(std::move(cand[j]));
+            else {
+                U.evicted_mass += cand[j].imp;
+                U.last_evicted.push_back(std::move(cand[j]));
+            }
+        }
+        std::sort(keep.begin(), keep.end(),
+                  [](const Entry& a, const Entry& b) { return a.pos < b.pos; });
+        U.e = std::move(keep);
+    });
+    return 0;
+}
+
+int ora_len(void* h, int u) { return (int)((Oracle*)h)->units[u].e.size(); }
+int ora_next_pos(void* h, int u) { return ((Oracle*)h)->units[u].next_pos; }
+int ora_num_evicted(void* h, int u) { return (int)((Oracle*)h)->units[u].last_evicted.size(); }
+double ora_evicted_mass(void* h, int u) { return ((Oracle*)h)->units[u].evicted_mass; }
+
+// Retained entries of unit u in ascending position.  k/v may be null.
+int ora_state(void* h, int u, int32_t* pos, float* imp, float* k, float* v) {
+    Oracle* O = (Oracle*)h;
+    const Unit& U = O->units[u];
+    for (size_t j = 0; j < U.e.size(); ++j) {
+        if (pos) pos[j] = U.e[j].pos;
+        if (imp) imp[j] = U.e[j].imp;
+        if (k) std::memcpy(k + j * O->d, U.e[j].k.data(), sizeof(float) * O->d);
+        if (v) std::memcpy(v + j * O->d, U.e[j].v.data(), sizeof(float) * O->d);
+    }
+    return (int)U.e.size();
+}
+
+// Entries removed by the latest evict of unit u.
+int ora_evicted(void* h, int u, int32_t* pos, float* imp) {
+    const Unit& U = ((Oracle*)h)->units[u];
+    for (size_t j = 0; j < U.last_evicted.size(); ++j) {
+        pos[j] = U.last_evicted[j].pos;
+        imp[j] = U.last_evicted[j].imp;
+    }
+    return (int)U.last_evicted.size();
+}
+
+// Make the retained set of unit u equal to `pos` (n entries), which must be a
+// subset of retained + last evicted.  Moves entries between the two lists and
+// keeps every score; the evicted-mass total follows the move.  Returns 0 on
+// success and leaves the unit unchanged on failure.
+int ora_resync(void* h, int u, int n, const int32_t* pos) {
+    Oracle* O = (Oracle*)h;
+    Unit& U = O->units[u];
+    std::vector<int32_t> want(pos, pos + n);
+    std::sort(want.begin(), want.end());
+    if (std::adjacent_find(want.begin(), want.end()) != want.end()) return 1;
+    int found = 0;
+    for (auto* list : {&U.e, &U.last_evicted})
+        for (auto& en : *list)
+            found += std::binary_search(want.begin(), want.end(), en.pos) ? 1 : 0;
+    if (found != n) return 1;
+    double old_mass = 0.0;
+    for (auto& en : U.last_evicted) old_mass += en.imp;
+    std::vector<Entry> keep, out;
+    for (auto* list : {&U.e, &U.last_evicted})
+        for (auto& en : *list) {
+            if (std::binary_search(want.begin(), want.end(), en.pos)) keep.push_back(std::move(en));
+            else out.push_back(std::move(en));
+        }
+    std::sort(keep.begin(), keep.end(),
+              [](const Entry& a, const Entry& b) { return a.pos < b.pos; });
+    double new_mass = 0.0;
+    for (auto& en : out) new_mass += en.imp;
+    U.evicted_mass += new_mass - old_mass;
+    U.e = std::move(keep);
+    U.last_evicted = std::move(out);
+    return 0;
+}
+
+}  // extern "C"

@@ -1,0 +1,314 @@
+"""Pins of the CPU oracle to things other than itself.
+
+Each test ties one part of the oracle to a library routine, a closed form, an
+invariant or a brute force, chosen so that a plausible slip (a dropped scale,
+a wrong head-to-group map, a transposed operand, a wrong tie order, a missing
+increment) fails at least one of them.
+"""
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rand(rng, *shape):
+    return rng.standard_normal(shape).astype(np.float32)
+
+
+def _sdpa_ref(q, k, v, G, scale=None):
+    """Textbook attention via torch SDPA in float64; kv head of query head h is h // G."""
+    qt = torch.from_numpy(q.astype(np.float64))            # [Hq, 1, d]
+    kt = torch.from_numpy(k.astype(np.float64)).repeat_interleave(G, dim=0)  # [Hq, n, d]
+    vt = torch.from_numpy(v.astype(np.float64)).repeat_interleave(G, dim=0)
+    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=scale)
+    return o.numpy()
+
+
+# --------------------------------------------------------------------------
+# attention: budget >= context means no eviction, so the decode output is
+# plain full attention (library SDPA).
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("out_bf16", [False, True])
+def test_full_attention_equals_library_sdpa(out_bf16):
+    rng = np.random.default_rng(11)
+    L, B, Hq, Hkv, d = 2, 2, 8, 2, 32
+    G = Hq // Hkv
+    prompt, steps = 40, 5
+    O = oracle.Oracle(L, B, Hq, Hkv, d, 4, 8, np.full(L * Hkv, 10_000), out_bf16=out_bf16)
+    K = _rand(rng, L, B, Hkv, prompt + steps, d)
+    V = _rand(rng, L, B, Hkv, prompt + steps, d)
+    O.append(0, K[:, :, :, :prompt], V[:, :, :, :prompt])
+    for s in range(steps):
+        t = prompt + s
+        O.append(0, K[:, :, :, t:t + 1], V[:, :, :, t:t + 1])
+        q = _rand(rng, L, B, Hq, d)
+        out = O.decode(0, q)
+        O.evict(0, L)  # budget far above n: must be a no-op
+        for l in range(L):
+            for b in range(B):
+                ref = _sdpa_ref(q[l, b][:, None, :], K[l, b, :, :t + 1], V[l, b, :, :t + 1], G)[:, 0]
+                got = out[l, b]
+                if not out_bf16:
+                    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-6 * np.abs(ref).max())
+                else:
+                    # bf16: representable, and within half an ulp of the exact value
+                    bits = got.view(np.uint32)
+                    assert np.all(bits & 0xFFFF == 0)
+                    e = np.floor(np.log2(np.abs(ref)))
+                    half_ulp = 2.0 ** (e - 8)
+                    assert np.all(np.abs(got - ref) <= half_ulp * (1 + 1e-9))
+    for u in range(O.units):
+        assert O.length(u) == prompt + steps
+
+
+def test_scale_override_is_used():
+    rng = np.random.default_rng(3)
+    O = oracle.Oracle(1, 1, 2, 1, 16, 0, 0, [100], scale=0.5)
+    K, V = _rand(rng, 1, 1, 1, 9, 16), _rand(rng, 1, 1, 1, 9, 16)
+    O.append(0, K, V)
+    q = _rand(rng, 1, 1, 2, 16)
+    ref = _sdpa_ref(q[0, 0][:, None], K[0, 0], V[0, 0], 2, scale=0.5)[:, 0]
+    np.testing.assert_allclose(O.decode(0, q)[0, 0], ref, rtol=0, atol=1e-6 * np.abs(ref).max())
+
+
+# --------------------------------------------------------------------------
+# importance: equals the attention columns summed over the group's heads,
+# with the window queries causally masked (brute force on tiny inputs).
+# --------------------------------------------------------------------------
+def test_importance_equals_summed_attention_columns():
+    rng = np.random.default_rng(5)
+    L, B, Hq, Hkv, d = 1, 2, 4, 2, 8
+    G = Hq // Hkv
+    prompt, nq, steps = 12, 3, 4
+    O = oracle.Oracle(L, B, Hq, Hkv, d, 1, 2, np.full(Hkv, 1000))
+    K = _rand(rng, L, B, Hkv, prompt + steps, d) * 2
+    V = _rand(rng, L, B, Hkv, prompt + steps, d)
+    Qw = _rand(rng, L, B, Hq, nq, d) * 2
+    O.append(0, K[:, :, :, :prompt], V[:, :, :, :prompt])
+    O.score_window(0, Qw)
+    expect = np.zeros((B, Hkv, prompt + steps))
+    for b in range(B):
+        for g in range(Hkv):
+            for i in range(nq):
+                qpos = prompt - nq + i
+                for hh in range(G):
+                    s = Qw[0, b, g * G + hh, i].astype(np.float64) @ K[0, b, g, :qpos + 1].T.astype(np.float64)
+                    p = torch.softmax(torch.from_numpy(s / np.sqrt(d)), 0).numpy()
+                    expect[b, g, :qpos + 1] += p
+    for s_ in range(steps):
+        t = prompt + s_
+        O.append(0, K[:, :, :, t:t + 1], V[:, :, :, t:t + 1])
+        q = _rand(rng, L, B, Hq, d)
+        O.decode(0, q)
+        for b in range(B):
+            for g in range(Hkv):
+                for hh in range(G):
+                    s = q[0, b, g * G + hh].astype(np.float64) @ K[0, b, g, :t + 1].T.astype(np.float64)
+                    expect[b, g, :t + 1] += torch.softmax(torch.from_numpy(s / np.sqrt(d)), 0).numpy()
+    for b in range(B):
+        for g in range(Hkv):
+            pos, imp = O.state(O.unit(0, b, g))
+            np.testing.assert_array_equal(pos, np.arange(prompt + steps))
+            np.testing.assert_allclose(imp, expect[b, g], rtol=2e-6, atol=1e-7)
+
+
+# --------------------------------------------------------------------------
+# softmax sums to one, so every scored query adds exactly G to the unit's
+# total importance: retained + evicted mass = G * (nq + steps).
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("evict", [False, True])
+def test_importance_mass_conservation(evict):
+    rng = np.random.default_rng(7)
+    L, B, Hq, Hkv, d = 2, 1, 6, 2, 16
+    G = Hq // Hkv
+    prompt, nq, steps, S, Wn = 64, 8, 20, 2, 6
+    budget = np.array([24, 30, 20, 28]) if evict else np.full(L * Hkv, 500)
+    O = oracle.Oracle(L, B, Hq, Hkv, d, S, Wn, budget)
+    O.append(0, _rand(rng, L, B, Hkv, prompt, d), _rand(rng, L, B, Hkv, prompt, d))
+    O.score_window(0, _rand(rng, L, B, Hq, nq, d))
+    O.evict(0, L)
+    for _ in range(steps):
+        O.append(0, _rand(rng, L, B, Hkv, 1, d), _rand(rng, L, B, Hkv, 1, d))
+        O.decode(0, _rand(rng, L, B, Hq, d))
+        O.evict(0, L)
+    for u in range(O.units):
+        pos, imp = O.state(u)
+        total = float(imp.astype(np.float64).sum()) + O.evicted_mass(u)
+        assert abs(total - G * (nq + steps)) < 1e-5 * G * (nq + steps)
+        if evict:
+            assert len(pos) == min(prompt + steps, O.budget_of(u))
+
+
+# --------------------------------------------------------------------------
+# eviction rule
+# --------------------------------------------------------------------------
+def _h2o_keep(pos, imp, capacity, sink, window):
+    """Keep set of the H2O eviction listing (KV cache compression blog, sec. 3
+    "H2O"), restated: entries in position order; the first `sink` and the last
+    `window` are protected; of the rest the `capacity - sink - window` with
+    the largest scores (torch.topk) are kept."""
+    order = np.argsort(pos)
+    pos, imp = pos[order], imp[order]
+    n = len(pos)
+    if n <= capacity:
+        return set(pos.tolist())
+    cand = torch.ones(n, dtype=torch.bool)
+    cand[:sink] = False
+    if window:
+        cand[n - window:] = False
+    ci = torch.nonzero(cand).squeeze(1)
+    _, top = torch.topk(torch.from_numpy(imp)[ci], k=capacity - sink - window, largest=True)
+    kept = set(pos[:sink].tolist()) | set(pos[n - window:].tolist() if window else [])
+    kept |= set(pos[ci[top].numpy()].tolist())
+    return kept
+
+
+def test_evict_matches_h2o_topk_on_distinct_scores():
+    rng = np.random.default_rng(13)
+    L, B, Hq, Hkv, d = 1, 2, 4, 2, 16
+    S, Wn = 3, 5
+    budget = np.array([20, 26])
+    O = oracle.Oracle(L, B, Hq, Hkv, d, S, Wn, budget)
+    O.append(0, _rand(rng, L, B, Hkv, 48, d) * 2, _rand(rng, L, B, Hkv, 48, d))
+    O.score_window(0, _rand(rng, L, B, Hq, 6, d) * 2)
+    checked = 0
+    for step in range(30):
+        if step:
+            O.append(0, _rand(rng, L, B, Hkv, 1, d) * 2, _rand(rng, L, B, Hkv, 1, d))
+            O.decode(0, _rand(rng, L, B, Hq, d) * 2)
+        before = [O.state(u) for u in range(O.units)]
+        O.evict(0, L)
+        for u in range(O.units):
+            pos, imp = before[u]
+            t = O.next_pos(u) - 1
+            mid = (pos >= S) & (pos <= t - Wn)
+            assert len(np.unique(imp[mid])) == mid.sum(), "scores must be distinct here"
+            want = _h2o_keep(pos, imp, O.budget_of(u), S, Wn)
+            got, _ = O.state(u)
+            assert set(got.tolist()) == want
+            assert len(got) == min(len(pos), O.budget_of(u))
+            assert len(np.unique(got)) == len(got)
+            assert set(range(S)) <= set(got.tolist())
+            assert set(range(t - Wn + 1, t + 1)) <= set(got.tolist())
+            checked += 1
+    assert checked == 30 * O.units
+
+
+def test_budget_equal_sinks_plus_window_is_streaming_llm():
+    """B = S + W leaves exactly {t_1..t_S} U {t_{i-W+1}..t_i} (StreamingLLM,
+    KV cache compression blog sec. 3)."""
+    rng = np.random.default_rng(17)
+    S, Wn = 4, 12
+    O = oracle.Oracle(1, 1, 2, 1, 8, S, Wn, [S + Wn])
+    O.append(0, _rand(rng, 1, 1, 1, 40, 8), _rand(rng, 1, 1, 1, 40, 8))
+    O.score_window(0, _rand(rng, 1, 1, 2, 4, 8))
+    for step in range(25):
+        if step:
+            O.append(0, _rand(rng, 1, 1, 1, 1, 8), _rand(rng, 1, 1, 1, 1, 8))
+            O.decode(0, _rand(rng, 1, 1, 2, 8))
+        O.evict(0, 1)
+        t = O.next_pos(0) - 1
+        pos, _ = O.state(0)
+        assert pos.tolist() == list(range(S)) + list(range(t - Wn + 1, t + 1))
+
+
+def _exact_uniform_keep(history, S, Wn, B, G):
+    """Brute force with exact rationals for all-zero keys (uniform softmax).
+
+    history: list of ("window", nq) / ("decode",) / ("append", n) / ("evict",)
+    Returns the retained position set after replaying it.
+    """
+    imp = {}
+    nxt = 0
+    for ev in history:
+        if ev[0] == "append":
+            for _ in range(ev[1]):
+                imp[nxt] = Fraction(0)
+                nxt += 1
+        elif ev[0] == "window":
+            nq = ev[1]
+            t = nxt - 1
+            for i in range(nq):
+                qpos = t - nq + 1 + i
+                vis = [p for p in imp if p <= qpos]
+                for p in vis:
+                    imp[p] += Fraction(G, len(vis))
+        elif ev[0] == "decode":
+            n = len(imp)
+            for p in imp:
+                imp[p] += Fraction(G, n)
+        elif ev[0] == "evict":
+            if len(imp) <= B:
+                continue
+            t = nxt - 1
+            prot = [p for p in imp if p < S or p > t - Wn]
+            cand = sorted((p for p in imp if not (p < S or p > t - Wn)),
+                          key=lambda p: (-imp[p], p))
+            keep = set(prot) | set(cand[:B - len(prot)])
+            imp = {p: imp[p] for p in keep}
+    return set(imp)
+
+
+def test_zero_keys_uniform_softmax_tie_rule():
+    """All-zero keys make every softmax uniform, so scores are closed forms
+    and whole classes of tokens tie exactly; ties must keep the lowest
+    positions."""
+    S, Wn, Bu, G, d = 2, 5, 14, 2, 8
+    prompt, nq = 40, 6
+    rng = np.random.default_rng(19)
+    O = oracle.Oracle(1, 1, G, 1, d, S, Wn, [Bu])
+    zk = np.zeros((1, 1, 1, prompt, d), np.float32)
+    O.append(0, zk, _rand(rng, 1, 1, 1, prompt, d))
+    O.score_window(0, _rand(rng, 1, 1, G, nq, d))
+    O.evict(0, 1)
+    hist = [("append", prompt), ("window", nq), ("evict",)]
+    assert set(O.state(0)[0].tolist()) == _exact_uniform_keep(hist, S, Wn, Bu, G)
+    # the cut keeps the lowest candidate positions among the tied prompt class
+    assert set(O.state(0)[0].tolist()) == set(range(Bu - Wn)) | set(range(prompt - Wn, prompt))
+    for _ in range(12):
+        O.append(0, np.zeros((1, 1, 1, 1, d), np.float32), _rand(rng, 1, 1, 1, 1, d))
+        O.decode(0, _rand(rng, 1, 1, G, d))
+        O.evict(0, 1)
+        hist += [("append", 1), ("decode",), ("evict",)]
+        assert set(O.state(0)[0].tolist()) == _exact_uniform_keep(hist, S, Wn, Bu, G)
+
+
+def test_resync_moves_entries_and_mass():
+    rng = np.random.default_rng(23)
+    O = oracle.Oracle(1, 1, 2, 1, 8, 1, 2, [6])
+    O.append(0, _rand(rng, 1, 1, 1, 10, 8), _rand(rng, 1, 1, 1, 10, 8))
+    O.score_window(0, _rand(rng, 1, 1, 2, 3, 8))
+    total_before = O.state(0)[1].astype(np.float64).sum()
+    O.evict(0, 1)
+    pos, _ = O.state(0)
+    epos, _ = O.last_evicted(0)
+    swapped = np.concatenate([pos[pos != pos[1]], epos[:1]])
+    O.resync(0, swapped)
+    assert set(O.state(0)[0].tolist()) == set(swapped.tolist())
+    total = O.state(0)[1].astype(np.float64).sum() + O.evicted_mass(0)
+    assert abs(total - total_before) < 1e-6
+    with pytest.raises(RuntimeError):
+        O.resync(0, np.array([99, 100]))
+
+
+# --------------------------------------------------------------------------
+# byte accounting used by the roofline: the page's worked KV-size example
+# --------------------------------------------------------------------------
+def test_kv_size_worked_example():
+    vals = {}
+    with open(os.path.join(GOLDEN, "kv_size_llama3_70b_128k.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            k, v = line.split()
+            vals[k] = float(v)
+    m = W.kv_bytes(int(vals["batch"]), int(vals["length"]), int(vals["layers"]),
+                   int(vals["kv_heads"]), int(vals["head_dim"]), int(vals["elem_bytes"]))
+    assert round(m / 1e9, 1) == vals["gigabytes"]
