@@ -1,0 +1,361 @@
+"""Benchmark of the budgeted, importance-aware KV-cache decode step on GB300.
+
+One step = the whole hot path for one decode token of every unit:
+hikv_append (new k, v) -> hikv_decode_step (fused attention + importance +
+victim argmin) -> hikv_evict (back to budget).  Workload: the Llama-3-8B-shaped
+layer (batch 8, 32 query / 8 KV heads, d 128, bf16 K/V, 8192-token prompt,
+budget 1024, 4 sinks, 64-token window, eviction every step), seeded synthetic
+inputs resident in HBM before timing.  The retained set (34 MB) fits in L2,
+so L2 is flushed (256 MB write) between timed steps, outside the timed events.
+
+Prints one JSON line.  `--impl reference` times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "decode steps/s and achieved HBM GB/s (fraction of ~8 TB/s) at 1 GB300"
+WORKLOAD_INDEX = 1
+KERNEL_SOURCES = ["importance_aware_kv_gb300/csrc/k_decode.cuh",
+                  "importance_aware_kv_gb300/csrc/hikv_internal.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "k_decode_llama3_8b_traffic.json")
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.proc = None
+        self.out = os.path.join("/tmp", f"hikv_clocks_{os.getpid()}.csv")
+        try:
+            self.f = open(self.out, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_id}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.out) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    mx.append(float(p[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, p[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.out)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_id_for(dev_index: int) -> str:
+    import torch
+    try:
+        bus = torch.cuda.get_device_properties(dev_index).pci_bus_id
+        if bus:
+            return str(bus)
+    except Exception:
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    if vis and "," not in vis and vis.strip().isdigit():
+        return vis.strip()
+    return str(dev_index)
+
+
+# --------------------------------------------------------------------------
+def step_bytes(w, n: int):
+    """Algorithmic bytes of one decode step of one unit holding n tokens during
+    attention: K/V rows, importance read+write, positions, q in, out, plus the
+    appended row; the decode kernel alone moves all but the append."""
+    e = w.elem_bytes
+    kv = 2 * n * w.d * e
+    meta = 12 * n
+    qo = 2 * w.group * w.d * e
+    app = 2 * w.d * e
+    return kv, meta, qo, app
+
+
+def run_cpu_oracle(w, seed, steps, warmup, budget_s=20.0):
+    """Time the oracle's decode loop (append -> decode -> evict, every unit)."""
+    import oracle
+    import workloads as W
+    threads = os.cpu_count() or 1
+    O = oracle.Oracle(w.layers, w.batch, w.hq, w.hkv, w.d, w.sink, w.window, W.budgets(w, seed),
+                      out_bf16=(w.dtype == "bf16"), threads=threads)
+    k, v = W.gen_kv(w, 0, w.layers, 0, w.prompt, seed)
+    O.append(0, W.to_f32(k), W.to_f32(v))
+    del k, v
+    O.score_window(0, W.to_f32(W.gen_q(w, 0, w.layers, w.prompt - w.nq, w.nq, seed)))
+    O.evict(0, w.layers)
+    total = warmup + steps
+    ks, vs = W.gen_kv(w, 0, w.layers, w.prompt, total, seed)
+    qs = W.gen_q(w, 0, w.layers, w.prompt, total, seed)
+    done, t_used = 0, 0.0
+    for s in range(total):
+        t0 = time.perf_counter()
+        O.append(0, W.to_f32(ks[:, :, :, s:s + 1]), W.to_f32(vs[:, :, :, s:s + 1]))
+        O.decode(0, W.to_f32(qs[:, :, :, s]))
+        O.evict(0, w.layers)
+        dt = time.perf_counter() - t0
+        if s >= warmup:
+            t_used += dt
+            done += 1
+            if t_used > budget_s:
+                break
+    return done / t_used, threads, done
+
+
+def bench_reference(args):
+    import workloads as W
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w = W.WORKLOADS[WORKLOAD_INDEX]
+    val, cores, done = run_cpu_oracle(w, w.index, args.steps, args.warmup, budget_s=120.0)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "steps/s", "n_gpus": 0,
+        "steps": done, "warmup": args.warmup, "ms_per_step": 1e3 / val, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": w.name, "units": w.units, "budget": w.budget, "sink": w.sink,
+                   "window": w.window, "evict_every": w.evict_every},
+        "cpu_baseline": {"value": val, "unit": "steps/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{done} decode steps of the full workload after prefill"},
+        "e2e": {"value": val, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
+def bench_gpu(args):
+    import torch
+    import torch.distributed as dist
+    import importance_aware_kv_gb300 as hk
+    import workloads as W
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = W.WORKLOADS[WORKLOAD_INDEX]
+    seed = w.index + 1000 * rank          # every rank decodes its own batch
+    K, Wu, Ke = args.steps, args.warmup, args.e2e_steps
+    total_steps = Wu + K + Ke
+    budgets = W.budgets(w, seed)
+    cache = hk.Cache(hk.CacheConfig(w.layers, w.batch, w.hq, w.hkv, w.d, w.dtype, w.sink, w.window,
+                                    budgets, w.prompt + total_steps + 1))
+    # ---- setup (untimed): prompt, window scoring, cut to budget ----
+    k, v = W.gen_kv(w, 0, w.layers, 0, w.prompt, seed)
+    cache.append(W.to_torch(k).to(dev), W.to_torch(v).to(dev))
+    del k, v
+    cache.score_window(W.to_torch(W.gen_q(w, 0, w.layers, w.prompt - w.nq, w.nq, seed)).to(dev))
+    cache.evict()
+    ks, vs = W.gen_kv(w, 0, w.layers, w.prompt, total_steps, seed)
+    qs = W.gen_q(w, 0, w.layers, w.prompt, total_steps, seed)
+    ks = np.ascontiguousarray(np.moveaxis(ks, 3, 0)[:, :, :, :, None, :])
+    vs = np.ascontiguousarray(np.moveaxis(vs, 3, 0)[:, :, :, :, None, :])
+    qs = np.ascontiguousarray(np.moveaxis(qs, 3, 0))
+    dks, dvs, dqs = (W.to_torch(x).to(dev) for x in (ks, vs, qs))
+    out = torch.empty_like(dqs[0])
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(s):
+        cache.append(dks[s], dvs[s])
+        cache.decode_step(dqs[s], out)
+        cache.evict()
+
+    for s in range(Wu):
+        flush.fill_(float(s))
+        step(s)
+    torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    sampler = ClockSampler(gpu_id_for(local))
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(K):
+        s = Wu + i
+        flush.fill_(float(i))
+        e0, e1, e2, e3 = ev[i]
+        e0.record(stream)
+        cache.append(dks[s], dvs[s])
+        e1.record(stream)
+        cache.decode_step(dqs[s], out)
+        e2.record(stream)
+        cache.evict()
+        e3.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    step_ms = [e0.elapsed_time(e3) for (e0, e1, e2, e3) in ev]
+    dec_ms = [e1.elapsed_time(e2) for (e0, e1, e2, e3) in ev]
+    t_total = sum(step_ms) / 1e3
+    if world > 1:
+        t = torch.tensor([t_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_total = float(t.item())
+
+    # ---- e2e through the C ABI with pinned host buffers ----
+    hk_s = stream
+    hk_k = torch.from_numpy(ks.view(np.int16)).pin_memory()
+    hk_v = torch.from_numpy(vs.view(np.int16)).pin_memory()
+    hk_q = torch.from_numpy(qs.view(np.int16)).pin_memory()
+    k_dev = torch.empty(ks.shape[1:], dtype=torch.int16, device=dev)
+    v_dev = torch.empty_like(k_dev)
+    q_dev = torch.empty(qs.shape[1:], dtype=torch.int16, device=dev)
+    out_host = torch.empty(tuple(out.shape), dtype=torch.bfloat16).pin_memory()
+    torch.cuda.synchronize()
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    e2e_ms = 0.0
+    for i in range(Ke):
+        s = Wu + K + i
+        flush.fill_(float(i))
+        e_start.record(hk_s)
+        k_dev.copy_(hk_k[s], non_blocking=True)
+        v_dev.copy_(hk_v[s], non_blocking=True)
+        q_dev.copy_(hk_q[s], non_blocking=True)
+        kb, vb, qb = k_dev.view(torch.bfloat16), v_dev.view(torch.bfloat16), q_dev.view(torch.bfloat16)
+        cache.append(kb, vb)
+        cache.decode_step(qb, out)
+        cache.evict()
+        out_host.copy_(out, non_blocking=True)
+        e_end.record(hk_s)
+        e_end.synchronize()
+        e2e_ms += e_start.elapsed_time(e_end)
+    h2d = (ks[0].nbytes + vs[0].nbytes + qs[0].nbytes)
+    d2h = out_host.numel() * 2
+    cache.device_status()
+    n_ret = int(cache.lengths().max()) + 1      # tokens attended per unit per step
+    cache.close()
+
+    # ---- numbers ----
+    kv, meta, qo, app = step_bytes(w, n_ret)
+    units = w.units
+    dec_bytes = units * (kv + meta + qo)
+    step_bytes_all = units * (kv + meta + qo + app)
+    dec_avg_s = (sum(dec_ms) / len(dec_ms)) / 1e3
+    peaks, src = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    achieved = dec_bytes / dec_avg_s / 1e9
+    traffic = None
+    try:
+        with open(TRAFFIC_FILE) as f:
+            tr = json.load(f)
+        if tr.get("kernel_sha") == kernel_sha():
+            traffic = tr.get("dram_bytes_per_launch")
+    except (OSError, ValueError):
+        pass
+    value = world * K / t_total
+    line = {
+        "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": K,
+        "warmup": Wu, "ms_per_step": t_total * 1e3 / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded)",
+        "config": {"workload": w.name, "layers": w.layers, "batch": w.batch, "q_heads": w.hq,
+                   "kv_heads": w.hkv, "head_dim": w.d, "kv_dtype": w.dtype, "prompt": w.prompt,
+                   "budget": w.budget, "sink": w.sink, "window": w.window,
+                   "evict_every": w.evict_every, "tokens_attended_per_unit": n_ret,
+                   "l2": "flushed between timed steps (256 MB write, outside the timed events)",
+                   "parallelism": f"replicas x{world} (units sharded by rank, no collective)"},
+        "hbm_gbs_step": step_bytes_all * world * K / t_total / 1e9,
+        "retained_kv_gbs": units * kv * world * K / t_total / 1e9,
+        "roofline": {"kernel": "k_decode (fused attention + importance + argmin)", "bound": "hbm",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": f"{src} hbm_gbs", "traffic": traffic,
+                     "bytes_per_launch": dec_bytes, "avg_launch_us": dec_avg_s * 1e6},
+        "e2e": {"value": Ke / (e2e_ms / 1e3), "unit": "steps/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "steps": Ke},
+        "gpu_launches": 3 * K,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        val, cores, done = run_cpu_oracle(w, seed, min(64, w.steps), 2, budget_s=20.0)
+        line["cpu_baseline"] = {"value": val, "unit": "steps/s", "cores": cores, "kind": "oracle",
+                                "sample": f"{done} decode steps (all {units} units) after prefill"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--e2e-steps", type=int, default=40)
+    ap.add_argument("--impl", default="hikv", choices=["hikv", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

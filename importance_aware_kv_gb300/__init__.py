@@ -1,0 +1,238 @@
+"""Python binding of libhikv, the importance-aware budgeted KV-cache decode step.
+
+Argument marshalling only: every function below takes torch CUDA tensors,
+checks their dtype/shape/contiguity, and passes raw device pointers and the
+current CUDA stream to the C ABI declared in ``include/hikv.h``.  All
+arithmetic of the step runs in the library's CUDA kernels; there is no CPU
+or PyTorch fallback, and importing this package fails loudly when
+``libhikv.so`` has not been built (``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libhikv.so")
+
+HIKV_OK, HIKV_ERR_INVALID_ARG, HIKV_ERR_OUT_OF_MEMORY, HIKV_ERR_CAPACITY = 0, 1, 2, 3
+HIKV_ERR_CUDA, HIKV_ERR_TIMEOUT, HIKV_ERR_STATE, HIKV_ERR_UNSUPPORTED = 4, 5, 6, 7
+STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "OUT_OF_MEMORY", 3: "CAPACITY", 4: "CUDA",
+                5: "TIMEOUT", 6: "STATE", 7: "UNSUPPORTED"}
+HIKV_F32, HIKV_BF16 = 0, 1
+
+# every entry point of include/hikv.h
+ABI_FUNCTIONS = ("hikv_create_cache", "hikv_destroy_cache", "hikv_append", "hikv_score_window",
+                 "hikv_decode_step", "hikv_evict", "hikv_gather_retained", "hikv_get_lengths",
+                 "hikv_device_status", "hikv_last_error")
+
+
+class HikvError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"hikv {STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+class hikv_config(ctypes.Structure):
+    _fields_ = [("num_layers", ctypes.c_int32), ("batch", ctypes.c_int32),
+                ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("num_sink", ctypes.c_int32), ("recent_window", ctypes.c_int32),
+                ("budgets", ctypes.POINTER(ctypes.c_int32)), ("max_tokens", ctypes.c_int32),
+                ("page_tokens", ctypes.c_int32), ("pool_pages", ctypes.c_int64),
+                ("max_window_queries", ctypes.c_int32), ("scale", ctypes.c_float)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build the CUDA library first "
+                          "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I32, I64, S = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int
+    sig = {
+        "hikv_create_cache": ([ctypes.POINTER(hikv_config), ctypes.POINTER(P)], S),
+        "hikv_destroy_cache": ([P], S),
+        "hikv_append": ([P, I32, I32, I32, P, P, P], S),
+        "hikv_score_window": ([P, I32, I32, I32, P, P], S),
+        "hikv_decode_step": ([P, I32, I32, P, P, P], S),
+        "hikv_evict": ([P, I32, I32, P], S),
+        "hikv_gather_retained": ([P, I32, I32, I32, P, P, P, P, P, P], S),
+        "hikv_get_lengths": ([P, I32, I32, P], S),
+        "hikv_device_status": ([P], S),
+        "hikv_last_error": ([], ctypes.c_char_p),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    return lib
+
+
+_lib = _load()
+
+
+def _check(status: int):
+    if status != HIKV_OK:
+        raise HikvError(status, _lib.hikv_last_error().decode())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dev(t, name, dtype=None, shape=None):
+    import torch
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+@dataclass
+class CacheConfig:
+    num_layers: int
+    batch: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    dtype: str                     # "f32" | "bf16"
+    num_sink: int
+    recent_window: int
+    budgets: Sequence[int]         # [num_layers * num_kv_heads]
+    max_tokens: int
+    page_tokens: int = 64
+    pool_pages: int = 0
+    max_window_queries: int = 0
+    scale: float = 0.0
+
+
+def hikv_create_cache(cfg: CacheConfig) -> ctypes.c_void_p:
+    b = np.ascontiguousarray(np.asarray(cfg.budgets, dtype=np.int32))
+    c = hikv_config(cfg.num_layers, cfg.batch, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim,
+                    HIKV_BF16 if cfg.dtype == "bf16" else HIKV_F32, cfg.num_sink,
+                    cfg.recent_window, b.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                    cfg.max_tokens, cfg.page_tokens, cfg.pool_pages, cfg.max_window_queries,
+                    cfg.scale)
+    h = ctypes.c_void_p()
+    _check(_lib.hikv_create_cache(ctypes.byref(c), ctypes.byref(h)))
+    return h
+
+
+def hikv_destroy_cache(h) -> None:
+    _check(_lib.hikv_destroy_cache(h))
+
+
+def hikv_append(h, layer0: int, k, v, stream=None) -> None:
+    nl, ntok = k.shape[0], k.shape[3]
+    _check(_lib.hikv_append(h, layer0, nl, ntok, _dev(k, "k"), _dev(v, "v", k.dtype, k.shape),
+                            _stream(stream)))
+
+
+def hikv_score_window(h, layer0: int, q, stream=None) -> None:
+    _check(_lib.hikv_score_window(h, layer0, q.shape[0], q.shape[3], _dev(q, "q"), _stream(stream)))
+
+
+def hikv_decode_step(h, layer0: int, q, out, stream=None) -> None:
+    _check(_lib.hikv_decode_step(h, layer0, q.shape[0], _dev(q, "q"),
+                                 _dev(out, "out", q.dtype, q.shape), _stream(stream)))
+
+
+def hikv_evict(h, layer0: int, nlayers: int, stream=None) -> None:
+    _check(_lib.hikv_evict(h, layer0, nlayers, _stream(stream)))
+
+
+def hikv_gather_retained(h, layer0: int, nlayers: int, cap: int, lengths, positions, importance,
+                         k_out=None, v_out=None, stream=None) -> None:
+    import torch
+    _check(_lib.hikv_gather_retained(
+        h, layer0, nlayers, cap, _dev(lengths, "lengths", torch.int32),
+        _dev(positions, "positions", torch.int32), _dev(importance, "importance", torch.float32),
+        _dev(k_out, "k_out"), _dev(v_out, "v_out"), _stream(stream)))
+
+
+def hikv_get_lengths(h, layer0: int, nlayers: int, units_per_layer: int) -> np.ndarray:
+    out = np.empty(nlayers * units_per_layer, dtype=np.int32)
+    _check(_lib.hikv_get_lengths(h, layer0, nlayers, out.ctypes.data))
+    return out
+
+
+def hikv_device_status(h) -> None:
+    _check(_lib.hikv_device_status(h))
+
+
+def hikv_last_error() -> str:
+    return _lib.hikv_last_error().decode()
+
+
+class Cache:
+    """Owning wrapper: one hikv cache on the current CUDA device."""
+
+    def __init__(self, cfg: CacheConfig):
+        self.cfg = cfg
+        self.units_per_layer = cfg.batch * cfg.num_kv_heads
+        self.units = cfg.num_layers * self.units_per_layer
+        self.h = hikv_create_cache(cfg)
+
+    def close(self):
+        if getattr(self, "h", None) is not None and self.h.value:
+            hikv_destroy_cache(self.h)
+        self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def append(self, k, v, layer0=0, stream=None):
+        hikv_append(self.h, layer0, k, v, stream)
+
+    def score_window(self, q, layer0=0, stream=None):
+        hikv_score_window(self.h, layer0, q, stream)
+
+    def decode_step(self, q, out, layer0=0, stream=None):
+        hikv_decode_step(self.h, layer0, q, out, stream)
+
+    def evict(self, layer0=0, nlayers=None, stream=None):
+        hikv_evict(self.h, layer0, self.cfg.num_layers if nlayers is None else nlayers, stream)
+
+    def lengths(self, layer0=0, nlayers=None) -> np.ndarray:
+        nl = self.cfg.num_layers - layer0 if nlayers is None else nlayers
+        return hikv_get_lengths(self.h, layer0, nl, self.units_per_layer)
+
+    def gather(self, layer0=0, nlayers=None, cap=None, with_kv=False, stream=None):
+        """Retained state of the layers as CUDA tensors (positions ascending)."""
+        import torch
+        nl = self.cfg.num_layers - layer0 if nlayers is None else nlayers
+        nu = nl * self.units_per_layer
+        if cap is None:
+            cap = max(1, int(self.lengths(layer0, nl).max()))
+        dev = torch.device("cuda", torch.cuda.current_device())
+        lengths = torch.empty(nu, dtype=torch.int32, device=dev)
+        positions = torch.empty(nu, cap, dtype=torch.int32, device=dev)
+        importance = torch.empty(nu, cap, dtype=torch.float32, device=dev)
+        k_out = v_out = None
+        if with_kv:
+            dt = torch.bfloat16 if self.cfg.dtype == "bf16" else torch.float32
+            k_out = torch.empty(nu, cap, self.cfg.head_dim, dtype=dt, device=dev)
+            v_out = torch.empty_like(k_out)
+        hikv_gather_retained(self.h, layer0, nl, cap, lengths, positions, importance, k_out, v_out,
+                             stream)
+        return lengths, positions, importance, k_out, v_out
+
+    def device_status(self):
+        hikv_device_status(self.h)

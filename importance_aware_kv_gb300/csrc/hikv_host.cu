@@ -1,0 +1,481 @@
+// Host side of the hikv C ABI: argument checks, the exact host mirror of each
+// unit's length and mapped pages, device allocation, and kernel launches.
+// Nothing here synchronises the device except create/destroy/device_status.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <numeric>
+#include <string>
+#include <vector>
+
+#include "../../include/hikv.h"
+#include "hikv_internal.cuh"
+
+namespace hikv {
+size_t window_smem_bytes(int d, int nqv);
+}
+
+using namespace hikv;
+
+namespace {
+
+thread_local std::string g_err;
+
+hikv_status fail(hikv_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return s;
+}
+
+hikv_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(HIKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int kWindowChunk = 1024;   // tokens per CTA of the window-scoring kernels
+
+}  // namespace
+
+struct hikv_cache {
+    // configuration
+    int L = 0, B = 0, Hq = 0, Hkv = 0, G = 0, d = 0, dtype = 0, esz = 0;
+    int S = 0, W = 0, cap = 0, P = 0, page_shift = 0, max_pages = 0, max_wq = 0;
+    int units = 0, per_layer = 0;
+    int64_t pool_pages = 0;
+    float scale = 0.f;
+    std::vector<int32_t> budget_unit;   // [units]
+    // device
+    int device = 0, sm_count = 0;
+    size_t smem_optin = 0;
+    int max_smem_chunk = 0;             // decode smem path limit (tokens per CTA)
+    View v{};
+    int32_t* d_append_base = nullptr;
+    float* d_logits = nullptr;          // long-chunk decode logits (may be null)
+    unsigned long long* d_cand = nullptr;
+    int32_t* d_cand_slot = nullptr;
+    int32_t* d_holes = nullptr;
+    int64_t* d_hole_off = nullptr;
+    float* d_wpart = nullptr;
+    int wchunks = 0;
+    int32_t* d_order_all = nullptr;
+    int32_t* d_order_layer = nullptr;
+    std::vector<void*> allocs;
+    // host mirror
+    std::vector<int32_t> len, next_pos, mapped;
+    std::vector<uint8_t> fresh;         // decode ran since the last state change
+    int64_t pages_in_use = 0;
+    int cs_override = 0;                // HIKV_DECODE_CS (tuning)
+};
+
+namespace {
+
+template <class T>
+cudaError_t dalloc(hikv_cache* c, T** p, size_t count) {
+    *p = nullptr;
+    if (count == 0) count = 1;
+    cudaError_t e = cudaMalloc((void**)p, count * sizeof(T));
+    if (e == cudaSuccess) c->allocs.push_back(*p);
+    return e;
+}
+
+void free_all(hikv_cache* c) {
+    for (void* p : c->allocs) cudaFree(p);
+    c->allocs.clear();
+}
+
+bool range_ok(const hikv_cache* c, int32_t layer0, int32_t nl) {
+    return c && layer0 >= 0 && nl > 0 && layer0 + nl <= c->L;
+}
+
+int ilog2(int x) {
+    int r = 0;
+    while ((1 << r) < x) ++r;
+    return r;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* hikv_last_error(void) { return g_err.c_str(); }
+
+hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
+    g_err.clear();
+    if (!cfg || !out) return fail(HIKV_ERR_INVALID_ARG, "create: null config or out pointer");
+    *out = nullptr;
+    const hikv_config& f = *cfg;
+    if (f.num_layers <= 0 || f.batch <= 0 || f.num_q_heads <= 0 || f.num_kv_heads <= 0 ||
+        f.head_dim <= 0 || f.max_tokens <= 0)
+        return fail(HIKV_ERR_INVALID_ARG, "create: sizes must be positive");
+    if (f.num_q_heads % f.num_kv_heads)
+        return fail(HIKV_ERR_INVALID_ARG, "create: num_q_heads must be a multiple of num_kv_heads");
+    const int G = f.num_q_heads / f.num_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8)
+        return fail(HIKV_ERR_UNSUPPORTED, "create: group size %d not in {1,2,4,8}", G);
+    if (f.head_dim != 64 && f.head_dim != 128)
+        return fail(HIKV_ERR_UNSUPPORTED, "create: head_dim %d not in {64,128}", f.head_dim);
+    if (f.dtype != HIKV_F32 && f.dtype != HIKV_BF16)
+        return fail(HIKV_ERR_UNSUPPORTED, "create: dtype %d", f.dtype);
+    if (f.num_sink < 0 || f.recent_window < 0)
+        return fail(HIKV_ERR_INVALID_ARG, "create: negative sink or window");
+    if (!f.budgets) return fail(HIKV_ERR_INVALID_ARG, "create: budgets is NULL");
+    const int P = f.page_tokens ? f.page_tokens : 64;
+    if (P < 16 || (P & (P - 1)))
+        return fail(HIKV_ERR_INVALID_ARG, "create: page_tokens %d must be a power of two >= 16", P);
+    if (f.pool_pages < 0) return fail(HIKV_ERR_INVALID_ARG, "create: negative pool_pages");
+    if (f.max_window_queries < 0) return fail(HIKV_ERR_INVALID_ARG, "create: negative max_window_queries");
+    if (!(f.scale >= 0.f) || !std::isfinite(f.scale)) return fail(HIKV_ERR_INVALID_ARG, "create: bad scale");
+    const int64_t units64 = (int64_t)f.num_layers * f.batch * f.num_kv_heads;
+    if (units64 > 65535) return fail(HIKV_ERR_UNSUPPORTED, "create: %lld units > 65535", (long long)units64);
+    for (int i = 0; i < f.num_layers * f.num_kv_heads; ++i) {
+        const int32_t b = f.budgets[i];
+        if (b < 1 || b < f.num_sink + f.recent_window)
+            return fail(HIKV_ERR_INVALID_ARG, "create: budget[%d]=%d must be >= max(1, S+W=%d)", i, b,
+                        f.num_sink + f.recent_window);
+    }
+
+    hikv_cache* c = new hikv_cache();
+    c->L = f.num_layers; c->B = f.batch; c->Hq = f.num_q_heads; c->Hkv = f.num_kv_heads;
+    c->G = G; c->d = f.head_dim; c->dtype = f.dtype; c->esz = f.dtype == HIKV_BF16 ? 2 : 4;
+    c->S = f.num_sink; c->W = f.recent_window; c->cap = f.max_tokens;
+    c->P = P; c->page_shift = ilog2(P);
+    c->max_pages = ceil_div(c->cap, P);
+    c->max_wq = f.max_window_queries ? f.max_window_queries : 32;
+    c->units = (int)units64;
+    c->per_layer = c->B * c->Hkv;
+    c->pool_pages = f.pool_pages ? f.pool_pages : (int64_t)c->units * c->max_pages;
+    if (c->pool_pages > INT32_MAX) {
+        delete c;
+        return fail(HIKV_ERR_UNSUPPORTED, "create: pool of %lld pages too large", (long long)f.pool_pages);
+    }
+    c->scale = f.scale > 0.f ? f.scale : 1.0f / std::sqrt((float)c->d);
+    c->budget_unit.resize(c->units);
+    for (int u = 0; u < c->units; ++u)
+        c->budget_unit[u] = f.budgets[(u / c->per_layer) * c->Hkv + u % c->Hkv];
+    if (const char* e = std::getenv("HIKV_DECODE_CS")) c->cs_override = std::atoi(e);
+
+    cudaError_t e = cudaGetDevice(&c->device);
+    if (e != cudaSuccess) { delete c; return cuda_fail(e, "create: cudaGetDevice"); }
+    cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, c->device);
+    int optin = 0;
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device);
+    c->smem_optin = (size_t)optin;
+    c->max_smem_chunk = decode_max_smem_chunk(c->dtype, c->d, c->G, std::min<size_t>(c->smem_optin, 160 * 1024));
+
+    View& v = c->v;
+    const int row_bytes = c->d * c->esz;
+    v.row_bytes = row_bytes;
+    v.page_bytes = 2LL * P * row_bytes;
+    v.page_tokens = P; v.page_shift = c->page_shift; v.max_pages = c->max_pages; v.cap = c->cap;
+    v.pool_pages = (int32_t)c->pool_pages; v.units = c->units;
+    v.batch = c->B; v.hq = c->Hq; v.hkv = c->Hkv; v.group = G; v.d = c->d;
+    v.sink = c->S; v.window = c->W;
+
+    const size_t U = (size_t)c->units;
+    // hole lists: a unit cut from n <= cap to B leaves at most min(B, cap - B) holes
+    std::vector<int64_t> hole_off(U);
+    int64_t holes_total = 0;
+    for (size_t u = 0; u < U; ++u) {
+        hole_off[u] = holes_total;
+        holes_total += std::max(0, std::min(c->budget_unit[u], c->cap - c->budget_unit[u]));
+    }
+    c->wchunks = ceil_div(c->cap, kWindowChunk);
+    const bool need_logits = ceil_div(c->cap, kMaxCS) > c->max_smem_chunk;
+
+#define ALLOC(ptr, n)                                                       \
+    if ((e = dalloc(c, &(ptr), (n))) != cudaSuccess) {                      \
+        free_all(c);                                                        \
+        delete c;                                                           \
+        cudaGetLastError();                                                 \
+        return fail(HIKV_ERR_OUT_OF_MEMORY, "create: cudaMalloc of " #ptr " failed: %s", cudaGetErrorString(e)); \
+    }
+    ALLOC(v.pool, (size_t)c->pool_pages * (size_t)v.page_bytes);
+    ALLOC(v.page_table, U * c->max_pages);
+    ALLOC(v.imp, U * c->cap);
+    ALLOC(v.pos, U * c->cap);
+    ALLOC(v.len, U);
+    ALLOC(v.next_pos, U);
+    ALLOC(v.mapped, U);
+    ALLOC(v.victim, U);
+    ALLOC(v.budget, U);
+    ALLOC(v.free_stack, (size_t)c->pool_pages);
+    ALLOC(v.free_top, 1);
+    ALLOC(v.err, 1);
+    ALLOC(c->d_append_base, U);
+    ALLOC(c->d_cand, U * kMaxCS);
+    ALLOC(c->d_cand_slot, U * kMaxCS);
+    ALLOC(c->d_holes, (size_t)holes_total);
+    ALLOC(c->d_hole_off, U);
+    ALLOC(c->d_wpart, U * c->wchunks * (size_t)c->max_wq * G * 2);
+    ALLOC(c->d_order_all, U);
+    ALLOC(c->d_order_layer, U);
+    if (need_logits) ALLOC(c->d_logits, U * (size_t)c->cap * G);
+#undef ALLOC
+
+    // initial device state
+    std::vector<int32_t> stack((size_t)c->pool_pages);
+    std::iota(stack.begin(), stack.end(), 0);
+    std::vector<int32_t> order_all(U), order_layer(U);
+    std::iota(order_all.begin(), order_all.end(), 0);
+    std::stable_sort(order_all.begin(), order_all.end(),
+                     [&](int a, int b) { return c->budget_unit[a] > c->budget_unit[b]; });
+    for (int l = 0; l < c->L; ++l) {
+        auto first = order_layer.begin() + (size_t)l * c->per_layer;
+        std::iota(first, first + c->per_layer, l * c->per_layer);
+        std::stable_sort(first, first + c->per_layer,
+                         [&](int a, int b) { return c->budget_unit[a] > c->budget_unit[b]; });
+    }
+    const int32_t top = (int32_t)c->pool_pages;
+    const int32_t minus1 = -1;
+    (void)minus1;
+    bool ok = cudaMemset(v.page_table, 0xFF, U * c->max_pages * 4) == cudaSuccess &&
+              cudaMemset(v.imp, 0, U * c->cap * 4) == cudaSuccess &&
+              cudaMemset(v.pos, 0xFF, U * c->cap * 4) == cudaSuccess &&
+              cudaMemset(v.len, 0, U * 4) == cudaSuccess &&
+              cudaMemset(v.next_pos, 0, U * 4) == cudaSuccess &&
+              cudaMemset(v.mapped, 0, U * 4) == cudaSuccess &&
+              cudaMemset(v.victim, 0xFF, U * 4) == cudaSuccess &&
+              cudaMemset(v.err, 0, 4) == cudaSuccess &&
+              cudaMemcpy(v.budget, c->budget_unit.data(), U * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
+              cudaMemcpy(v.free_stack, stack.data(), stack.size() * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
+              cudaMemcpy(v.free_top, &top, 4, cudaMemcpyHostToDevice) == cudaSuccess &&
+              cudaMemcpy(c->d_hole_off, hole_off.data(), U * 8, cudaMemcpyHostToDevice) == cudaSuccess &&
+              cudaMemcpy(c->d_order_all, order_all.data(), U * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
+              cudaMemcpy(c->d_order_layer, order_layer.data(), U * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
+              cudaDeviceSynchronize() == cudaSuccess;
+    if (!ok) {
+        e = cudaGetLastError();
+        free_all(c);
+        delete c;
+        return cuda_fail(e, "create: initialisation");
+    }
+    c->len.assign(U, 0);
+    c->next_pos.assign(U, 0);
+    c->mapped.assign(U, 0);
+    c->fresh.assign(U, 0);
+    *out = c;
+    return HIKV_OK;
+}
+
+hikv_status hikv_destroy_cache(hikv_cache* c) {
+    g_err.clear();
+    if (!c) return HIKV_OK;
+    cudaError_t e = cudaDeviceSynchronize();
+    free_all(c);
+    delete c;
+    if (e != cudaSuccess) return cuda_fail(e, "destroy: synchronize");
+    return HIKV_OK;
+}
+
+hikv_status hikv_append(hikv_cache* c, int32_t layer0, int32_t nl, int32_t ntok, const void* k,
+                        const void* vv, hikv_stream_t stream) {
+    g_err.clear();
+    if (!range_ok(c, layer0, nl)) return fail(HIKV_ERR_INVALID_ARG, "append: bad cache or layer range");
+    if (ntok < 0) return fail(HIKV_ERR_INVALID_ARG, "append: ntok < 0");
+    if (ntok == 0) return HIKV_OK;
+    if (!k || !vv) return fail(HIKV_ERR_INVALID_ARG, "append: null k or v");
+    const int u0 = layer0 * c->per_layer, nu = nl * c->per_layer;
+    int64_t new_pages = 0;
+    for (int u = u0; u < u0 + nu; ++u) {
+        if ((int64_t)c->len[u] + ntok > c->cap)
+            return fail(HIKV_ERR_CAPACITY, "append: unit %d would hold %lld > max_tokens %d", u,
+                        (long long)c->len[u] + ntok, c->cap);
+        if ((int64_t)c->next_pos[u] + ntok > INT32_MAX)
+            return fail(HIKV_ERR_CAPACITY, "append: positions of unit %d overflow int32", u);
+        new_pages += std::max(0, ceil_div(c->len[u] + ntok, c->P) - c->mapped[u]);
+    }
+    if (c->pages_in_use + new_pages > c->pool_pages)
+        return fail(HIKV_ERR_CAPACITY, "append: page pool exhausted (%lld in use + %lld > %lld)",
+                    (long long)c->pages_in_use, (long long)new_pages, (long long)c->pool_pages);
+    AppendArgs a{};
+    a.v = c->v;
+    a.u0 = u0;
+    a.nunits = nu;
+    a.ntok = ntok;
+    a.k = (const uint8_t*)k;
+    a.vv = (const uint8_t*)vv;
+    a.base = c->d_append_base;
+    cudaError_t e = launch_append(a, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "append: launch");
+    for (int u = u0; u < u0 + nu; ++u) {
+        c->len[u] += ntok;
+        c->next_pos[u] += ntok;
+        c->mapped[u] = std::max(c->mapped[u], ceil_div(c->len[u], c->P));
+        c->fresh[u] = 0;
+    }
+    c->pages_in_use += new_pages;
+    return HIKV_OK;
+}
+
+hikv_status hikv_score_window(hikv_cache* c, int32_t layer0, int32_t nl, int32_t nq, const void* q,
+                              hikv_stream_t stream) {
+    g_err.clear();
+    if (!range_ok(c, layer0, nl)) return fail(HIKV_ERR_INVALID_ARG, "score_window: bad cache or layer range");
+    if (nq < 1 || nq > c->max_wq)
+        return fail(HIKV_ERR_INVALID_ARG, "score_window: nq=%d not in [1, %d]", nq, c->max_wq);
+    if (!q) return fail(HIKV_ERR_INVALID_ARG, "score_window: null q");
+    if (window_smem_bytes(c->d, nq * c->G) > c->smem_optin)
+        return fail(HIKV_ERR_UNSUPPORTED, "score_window: nq*G=%d query vectors exceed shared memory", nq * c->G);
+    const int u0 = layer0 * c->per_layer, nu = nl * c->per_layer;
+    int maxn = 0;
+    for (int u = u0; u < u0 + nu; ++u) {
+        if (c->next_pos[u] < nq || c->len[u] < 1)
+            return fail(HIKV_ERR_STATE, "score_window: unit %d has fewer than nq=%d positions", u, nq);
+        maxn = std::max(maxn, c->len[u]);
+    }
+    WindowArgs a{};
+    a.v = c->v;
+    a.u0 = u0;
+    a.nunits = nu;
+    a.layer0 = layer0;
+    a.nq = nq;
+    a.q = (const uint8_t*)q;
+    a.qscale = c->scale * 1.4426950408889634f;
+    a.part = c->d_wpart;
+    a.nchunks_max = c->wchunks;
+    a.nchunks_grid = ceil_div(maxn, kWindowChunk);
+    a.chunk = kWindowChunk;
+    cudaError_t e = launch_window(a, c->dtype, c->d, c->G, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "score_window: launch");
+    for (int u = u0; u < u0 + nu; ++u) c->fresh[u] = 0;
+    return HIKV_OK;
+}
+
+hikv_status hikv_decode_step(hikv_cache* c, int32_t layer0, int32_t nl, const void* q, void* out,
+                             hikv_stream_t stream) {
+    g_err.clear();
+    if (!range_ok(c, layer0, nl)) return fail(HIKV_ERR_INVALID_ARG, "decode_step: bad cache or layer range");
+    if (!q || !out) return fail(HIKV_ERR_INVALID_ARG, "decode_step: null q or out");
+    if (q == out) return fail(HIKV_ERR_INVALID_ARG, "decode_step: out aliases q");
+    const int u0 = layer0 * c->per_layer, nu = nl * c->per_layer;
+    int maxn = 0;
+    for (int u = u0; u < u0 + nu; ++u) {
+        if (c->len[u] < 1) return fail(HIKV_ERR_STATE, "decode_step: unit %d is empty", u);
+        maxn = std::max(maxn, c->len[u]);
+    }
+    // CTAs per unit: enough clusters to fill the GPU ~3 deep, within 1..8
+    int cs = 1;
+    if (c->cs_override > 0) {
+        cs = std::min(c->cs_override, kMaxCS);
+    } else {
+        const int target = 3 * c->sm_count;
+        while (cs < 8 && (int64_t)nu * cs < target) cs *= 2;
+        while (cs < 8 && ceil_div(maxn, cs) > c->max_smem_chunk) cs *= 2;
+    }
+    cs = std::min(cs, std::max(1, maxn));
+    const int chunk = ceil_div(maxn, cs);
+    const bool smem_path = chunk <= c->max_smem_chunk;
+    if (!smem_path && !c->d_logits)
+        return fail(HIKV_ERR_UNSUPPORTED, "decode_step: %d tokens per CTA exceed shared memory", chunk);
+    DecodeArgs a{};
+    a.v = c->v;
+    a.order = (nl == c->L) ? c->d_order_all : c->d_order_layer + u0;
+    a.n_units = nu;
+    a.layer0 = layer0;
+    a.q = (const uint8_t*)q;
+    a.out = (uint8_t*)out;
+    a.qscale = c->scale * 1.4426950408889634f;
+    a.logits = c->d_logits;
+    a.cand = c->d_cand;
+    a.cand_slot = c->d_cand_slot;
+    a.cs = cs;
+    a.chunk_cap = smem_path ? chunk : 0;
+    const size_t smem = decode_smem_bytes(c->dtype, c->d, c->G, smem_path, a.chunk_cap);
+    cudaError_t e = launch_decode(a, c->dtype, c->d, c->G, smem_path, smem, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decode_step: launch");
+    for (int u = u0; u < u0 + nu; ++u) c->fresh[u] = 1;
+    return HIKV_OK;
+}
+
+hikv_status hikv_evict(hikv_cache* c, int32_t layer0, int32_t nl, hikv_stream_t stream) {
+    g_err.clear();
+    if (!range_ok(c, layer0, nl)) return fail(HIKV_ERR_INVALID_ARG, "evict: bad cache or layer range");
+    const int u0 = layer0 * c->per_layer, nu = nl * c->per_layer;
+    bool any = false, fast = true;
+    for (int u = u0; u < u0 + nu; ++u) {
+        const int over = c->len[u] - c->budget_unit[u];
+        if (over <= 0) continue;
+        any = true;
+        if (over > 1 || !c->fresh[u]) fast = false;
+    }
+    if (!any) return HIKV_OK;
+    EvictArgs a{};
+    a.v = c->v;
+    a.u0 = u0;
+    a.nunits = nu;
+    a.holes = c->d_holes;
+    a.hole_off = c->d_hole_off;
+    cudaError_t e = fast ? launch_evict_fast(a, (cudaStream_t)stream) : launch_evict_general(a, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "evict: launch");
+    for (int u = u0; u < u0 + nu; ++u) {
+        const int Bu = c->budget_unit[u];
+        if (c->len[u] > Bu) {
+            c->len[u] = Bu;
+            const int keep = std::min(ceil_div(Bu + 1, c->P), c->max_pages);
+            if (c->mapped[u] > keep) {
+                c->pages_in_use -= c->mapped[u] - keep;
+                c->mapped[u] = keep;
+            }
+        }
+        c->fresh[u] = 0;
+    }
+    return HIKV_OK;
+}
+
+hikv_status hikv_gather_retained(hikv_cache* c, int32_t layer0, int32_t nl, int32_t cap, int32_t* lengths,
+                                 int32_t* positions, float* importance, void* k_out, void* v_out,
+                                 hikv_stream_t stream) {
+    g_err.clear();
+    if (!range_ok(c, layer0, nl)) return fail(HIKV_ERR_INVALID_ARG, "gather: bad cache or layer range");
+    if (!lengths || !positions || !importance) return fail(HIKV_ERR_INVALID_ARG, "gather: null output");
+    const int u0 = layer0 * c->per_layer, nu = nl * c->per_layer;
+    for (int u = u0; u < u0 + nu; ++u)
+        if (c->len[u] > cap) return fail(HIKV_ERR_INVALID_ARG, "gather: cap %d < length %d of unit %d", cap, c->len[u], u);
+    GatherArgs a{};
+    a.v = c->v;
+    a.u0 = u0;
+    a.nunits = nu;
+    a.cap = cap;
+    a.lengths = lengths;
+    a.positions = positions;
+    a.importance = importance;
+    a.k_out = (uint8_t*)k_out;
+    a.v_out = (uint8_t*)v_out;
+    cudaError_t e = launch_gather(a, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "gather: launch");
+    return HIKV_OK;
+}
+
+hikv_status hikv_get_lengths(const hikv_cache* c, int32_t layer0, int32_t nl, int32_t* lengths_host) {
+    g_err.clear();
+    if (!range_ok(c, layer0, nl) || !lengths_host) return fail(HIKV_ERR_INVALID_ARG, "get_lengths: bad arguments");
+    std::memcpy(lengths_host, c->len.data() + (size_t)layer0 * c->per_layer, sizeof(int32_t) * nl * c->per_layer);
+    return HIKV_OK;
+}
+
+hikv_status hikv_device_status(hikv_cache* c) {
+    g_err.clear();
+    if (!c) return fail(HIKV_ERR_INVALID_ARG, "device_status: null cache");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "device_status: synchronize");
+    uint32_t w = 0;
+    e = cudaMemcpy(&w, c->v.err, 4, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "device_status: read");
+    if (w) {
+        cudaMemset(c->v.err, 0, 4);
+        cudaDeviceSynchronize();
+    }
+    if (w & DEVERR_TIMEOUT) return fail(HIKV_ERR_TIMEOUT, "device: a bounded wait gave up (bits 0x%x)", w);
+    if (w) return fail(HIKV_ERR_STATE, "device: inconsistent state recorded (bits 0x%x)", w);
+    return HIKV_OK;
+}
+
+}  // extern "C"

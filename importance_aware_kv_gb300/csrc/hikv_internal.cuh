@@ -1,0 +1,279 @@
+// Internal definitions shared by the hikv kernels and the host cache manager.
+//
+// Memory layout in HBM (one cache):
+//   pool        [pool_pages] pages; a page holds P consecutive slots of one
+//               unit: K rows [P][d] then V rows [P][d], row = d * elem bytes.
+//   page_table  [units][max_pages] int32 page ids (-1 = unmapped); slot s of
+//               unit u lives in page page_table[u][s / P], row s % P.
+//   imp, pos    [units][cap] fp32 importance and int32 original position of
+//               every slot; slots [0, len[u]) are live, densely packed.
+//   len, next_pos, mapped, victim   [units] int32 per-unit state.
+//   free_stack  [pool_pages] ids of free pages, free_stack[0, *free_top).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace hikv {
+
+// device error word bits
+enum : uint32_t {
+    DEVERR_TIMEOUT = 1u,     // a bounded mbarrier wait gave up
+    DEVERR_PAGE = 2u,        // page id out of range / unmapped page touched
+    DEVERR_POOL = 4u,        // free stack under/overflow
+    DEVERR_STATE = 8u,       // inconsistent per-unit state
+};
+
+struct View {
+    uint8_t* pool;
+    int32_t* page_table;
+    float* imp;
+    int32_t* pos;
+    int32_t* len;
+    int32_t* next_pos;
+    int32_t* mapped;
+    int32_t* victim;
+    int32_t* budget;      // [units]
+    int32_t* free_stack;
+    int32_t* free_top;
+    uint32_t* err;
+    int64_t page_bytes;   // 2 * P * row_bytes
+    int32_t row_bytes;    // d * elem
+    int32_t page_tokens;  // P (power of two)
+    int32_t page_shift;   // log2(P)
+    int32_t max_pages;    // per unit
+    int32_t cap;          // slots per unit (metadata row stride)
+    int32_t pool_pages;
+    int32_t units;
+    int32_t batch, hq, hkv, group, d;
+    int32_t sink, window;
+};
+
+constexpr int kMaxCS = 16;   // most CTAs (cluster size) per unit in the decode kernel
+
+__host__ __device__ inline int32_t ceil_div(int32_t a, int32_t b) { return (a + b - 1) / b; }
+
+// Address of the K (or V) row of slot s of unit u; nullptr if the page is bad.
+__device__ __forceinline__ uint8_t* row_ptr(const View& v, int32_t u, int32_t s, bool is_v) {
+    int32_t pg = v.page_table[(int64_t)u * v.max_pages + (s >> v.page_shift)];
+    if (pg < 0 || pg >= v.pool_pages) {
+        atomicOr(v.err, DEVERR_PAGE);
+        return nullptr;
+    }
+    int32_t r = s & (v.page_tokens - 1);
+    return v.pool + (int64_t)pg * v.page_bytes +
+           ((is_v ? (int64_t)v.page_tokens : 0) + r) * v.row_bytes;
+}
+
+// ---------------------------------------------------------------------------
+// PTX wrappers (sm_90+ mbarrier / bulk copy / cluster; used on sm_103a)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: gives up after ~2^22 polls with back-off (well over a second
+// on a stalled barrier), records DEVERR_TIMEOUT and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t* err) {
+    for (uint32_t i = 0; i < (1u << 22); ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (i > 32) __nanosleep(256);
+    }
+    atomicOr(err, DEVERR_TIMEOUT);
+    return false;
+}
+
+// 1-D bulk copy global -> shared (TMA engine), completion counted on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// shared::cluster address of `p` in CTA `rank` of this cluster
+__device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// element conversion
+// ---------------------------------------------------------------------------
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+    __device__ __forceinline__ static float to_f(float x) { return x; }
+    __device__ __forceinline__ static float from_f(float x) { return x; }
+};
+template <> struct Elem<__nv_bfloat16> {
+    __device__ __forceinline__ static float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+    __device__ __forceinline__ static __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
+};
+
+// widen EPL consecutive elements held in raw registers
+template <typename T, int EPL> struct Widen;
+template <> struct Widen<__nv_bfloat16, 4> {   // 8 bytes
+    __device__ __forceinline__ static void run(const uint2 r, float* f) {
+        f[0] = __uint_as_float(r.x << 16);
+        f[1] = __uint_as_float(r.x & 0xFFFF0000u);
+        f[2] = __uint_as_float(r.y << 16);
+        f[3] = __uint_as_float(r.y & 0xFFFF0000u);
+    }
+};
+template <> struct Widen<__nv_bfloat16, 2> {   // 4 bytes
+    __device__ __forceinline__ static void run(const uint32_t r, float* f) {
+        f[0] = __uint_as_float(r << 16);
+        f[1] = __uint_as_float(r & 0xFFFF0000u);
+    }
+};
+template <> struct Widen<float, 2> {           // 8 bytes
+    __device__ __forceinline__ static void run(const uint2 r, float* f) {
+        f[0] = __uint_as_float(r.x);
+        f[1] = __uint_as_float(r.y);
+    }
+};
+template <> struct Widen<float, 4> {           // 16 bytes
+    __device__ __forceinline__ static void run(const uint4 r, float* f) {
+        f[0] = __uint_as_float(r.x);
+        f[1] = __uint_as_float(r.y);
+        f[2] = __uint_as_float(r.z);
+        f[3] = __uint_as_float(r.w);
+    }
+};
+
+// raw lane vector type: EPL * sizeof(T) bytes
+template <int BYTES> struct RawVec;
+template <> struct RawVec<4> { using type = uint32_t; };
+template <> struct RawVec<8> { using type = uint2; };
+template <> struct RawVec<16> { using type = uint4; };
+
+// ---------------------------------------------------------------------------
+// launchers (defined in the kernel files)
+// ---------------------------------------------------------------------------
+struct AppendArgs {
+    View v;
+    int32_t u0, nunits, ntok;
+    const uint8_t* k;
+    const uint8_t* vv;
+    int32_t* base;   // scratch [units]: first slot of this append per unit
+};
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
+
+struct DecodeArgs {
+    View v;
+    const int32_t* order;   // [n_units] absolute unit ids, launch order
+    int32_t n_units;
+    int32_t layer0;
+    const uint8_t* q;
+    uint8_t* out;
+    float qscale;           // scale * log2(e)
+    float* logits;          // global logit scratch [units][cap][G] (long path) or null
+    unsigned long long* cand; // [units][16] local argmin keys
+    int32_t* cand_slot;     // [units][16]
+    int32_t cs;             // CTAs per unit (cluster size)
+    int32_t chunk_cap;      // max tokens per CTA handled by the smem path
+};
+cudaError_t launch_decode(const DecodeArgs& a, int dtype, int d, int group, bool smem_path,
+                          size_t smem_bytes, cudaStream_t s);
+size_t decode_smem_bytes(int dtype, int d, int group, bool smem_path, int chunk_cap);
+int decode_max_smem_chunk(int dtype, int d, int group, size_t smem_limit);
+
+struct EvictArgs {
+    View v;
+    int32_t u0, nunits;
+    int32_t* holes;          // scratch: per unit hole lists
+    const int64_t* hole_off; // [units] offset of each unit's hole list
+};
+cudaError_t launch_evict_fast(const EvictArgs& a, cudaStream_t s);
+cudaError_t launch_evict_general(const EvictArgs& a, cudaStream_t s);
+
+struct WindowArgs {
+    View v;
+    int32_t u0, nunits, layer0, nq;
+    const uint8_t* q;
+    float qscale;
+    float* part;        // [units][nchunks_max][G*nq][2] partial (m, l)
+    int32_t nchunks_max; // per-unit stride of `part` in chunks
+    int32_t nchunks_grid;// chunks launched (covers the longest unit of the call)
+    int32_t chunk;      // tokens per CTA
+};
+cudaError_t launch_window(const WindowArgs& a, int dtype, int d, int group, cudaStream_t s);
+
+struct GatherArgs {
+    View v;
+    int32_t u0, nunits, cap;
+    int32_t* lengths;
+    int32_t* positions;
+    float* importance;
+    uint8_t* k_out;
+    uint8_t* v_out;
+};
+cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s);
+
+}  // namespace hikv

@@ -1,0 +1,221 @@
+// Eviction: cut a unit holding n > B tokens to exactly B and compact it.
+//
+// Keep rule (blog sec. 3 "H2O" with StreamingLLM's sinks and window; per-head
+// budgets B_u, HeadKV summary sec. 3.2): positions < S and > t - W are always
+// kept; of the other "candidate" tokens keep the B - S - W with the largest
+// (importance, -position), i.e. ties keep the lower position.
+//
+// Two kernels:
+//   k_evict_fast     n == B + 1 right after a decode step: the decode kernel
+//                    already found the single victim (fused argmin); the
+//                    token in the last slot moves into the victim's slot.
+//   k_evict_general  any n > B: a per-unit radix select over 64-bit keys
+//                    (importance bits << 32 | ~position; importance >= 0 so
+//                    the float bits order like the values) finds the
+//                    (B-S-W)-th largest candidate key T; survivors are the
+//                    protected tokens and candidates with key >= T (keys are
+//                    unique, so exactly B survive).  Survivors sitting in
+//                    slots >= B move into the dead slots < B, k-th with k-th
+//                    in slot order, and whole pages past the unit's need go
+//                    back to the pool (blog sec. 5.1: a compaction kernel
+//                    coalescing survivors into dense blocks frees pages).
+// HiKV's sorter and Kelle's systolic evictor do this selection in custom
+// silicon; here it is a radix select in shared memory.
+#include "hikv_internal.cuh"
+
+namespace hikv {
+namespace {
+
+__device__ __forceinline__ unsigned long long mk_key(float imp, int32_t pos) {
+    return ((unsigned long long)__float_as_uint(imp) << 32) | (unsigned long long)(~(uint32_t)pos);
+}
+
+__device__ void move_slot(const View& v, int32_t u, int32_t src, int32_t dst, int lane, int nlanes) {
+    const int32_t vec = v.row_bytes / 16;
+    for (int32_t i = lane; i < 2 * vec; i += nlanes) {
+        const bool isv = i >= vec;
+        const int32_t c = isv ? i - vec : i;
+        const uint8_t* s = row_ptr(v, u, src, isv);
+        uint8_t* d = row_ptr(v, u, dst, isv);
+        if (!s || !d) continue;
+        reinterpret_cast<uint4*>(d)[c] = reinterpret_cast<const uint4*>(s)[c];
+    }
+    if (lane == 0) {
+        const int64_t b = (int64_t)u * v.cap;
+        v.imp[b + dst] = v.imp[b + src];
+        v.pos[b + dst] = v.pos[b + src];
+    }
+}
+
+// warp per unit
+__global__ void k_evict_fast(EvictArgs a) {
+    const int32_t w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (w >= a.nunits) return;
+    const View& v = a.v;
+    const int32_t u = a.u0 + w;
+    const int32_t n = v.len[u];
+    const int32_t B = v.budget[u];
+    if (n <= B) return;
+    const int32_t vs = v.victim[u];
+    if (n != B + 1 || vs < 0 || vs >= n) {
+        if (lane == 0) atomicOr(v.err, DEVERR_STATE);
+        return;
+    }
+    if (vs != n - 1) move_slot(v, u, n - 1, vs, lane, 32);
+    __syncwarp();
+    if (lane == 0) {
+        v.len[u] = B;
+        v.victim[u] = -1;
+    }
+}
+
+constexpr int kEvThreads = 256;
+constexpr int kEvWarps = kEvThreads / 32;
+
+// exclusive block scan of one flag per thread; returns this thread's rank,
+// writes the block total to *total (all threads).
+__device__ int32_t block_rank(bool flag, int32_t* wsum, int32_t* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const unsigned m = __ballot_sync(0xffffffffu, flag);
+    const int32_t in_warp = __popc(m & ((1u << lane) - 1u));
+    if (lane == 0) wsum[warp] = __popc(m);
+    __syncthreads();
+    int32_t before = 0, all = 0;
+    for (int i = 0; i < kEvWarps; ++i) {
+        const int32_t x = wsum[i];
+        before += i < warp ? x : 0;
+        all += x;
+    }
+    __syncthreads();
+    *total = all;
+    return before + in_warp;
+}
+
+__global__ void __launch_bounds__(kEvThreads) k_evict_general(EvictArgs a) {
+    const View& v = a.v;
+    const int32_t u = a.u0 + blockIdx.x;
+    const int32_t n = v.len[u];
+    const int32_t B = v.budget[u];
+    if (n <= B) return;
+    const int32_t t = v.next_pos[u] - 1;
+    const int32_t lo = v.sink, hi = t - v.window;
+    const int32_t kmid = B - v.sink - v.window;
+    const float* imp = v.imp + (int64_t)u * v.cap;
+    const int32_t* pos = v.pos + (int64_t)u * v.cap;
+
+    __shared__ uint32_t hist[256];
+    __shared__ unsigned long long s_prefix, s_mask;
+    __shared__ int32_t s_rem;
+    __shared__ int32_t wsum[kEvWarps];
+
+    // --- radix select of the kmid-th largest candidate key ---
+    if (threadIdx.x == 0) {
+        s_prefix = 0ull;
+        s_mask = 0ull;
+        s_rem = kmid;
+    }
+    __syncthreads();
+    if (kmid > 0) {
+        for (int pass = 0; pass < 8; ++pass) {
+            const int shift = 56 - 8 * pass;
+            for (int i = threadIdx.x; i < 256; i += kEvThreads) hist[i] = 0;
+            __syncthreads();
+            const unsigned long long prefix = s_prefix, mask = s_mask;
+            for (int32_t s = threadIdx.x; s < n; s += kEvThreads) {
+                const int32_t p = pos[s];
+                if (p < lo || p > hi) continue;
+                const unsigned long long key = mk_key(imp[s], p);
+                if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+            }
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                int32_t rem = s_rem, cum = 0, sel = 0;
+                for (int bin = 255; bin >= 0; --bin) {
+                    const int32_t h = (int32_t)hist[bin];
+                    if (cum + h >= rem) {
+                        sel = bin;
+                        rem -= cum;
+                        break;
+                    }
+                    cum += h;
+                }
+                s_rem = rem;
+                s_prefix = prefix | ((unsigned long long)sel << shift);
+                s_mask = mask | (255ull << shift);
+            }
+            __syncthreads();
+        }
+    }
+    const unsigned long long T = s_prefix;
+    auto survives = [&](int32_t s) -> bool {
+        const int32_t p = pos[s];
+        if (p < lo || p > hi) return true;
+        return kmid > 0 && mk_key(imp[s], p) >= T;
+    };
+
+    // --- holes: dead slots in [0, B), ascending ---
+    int32_t* holes = a.holes + a.hole_off[u];
+    int32_t base = 0;
+    for (int32_t s0 = 0; s0 < B; s0 += kEvThreads) {
+        const int32_t s = s0 + threadIdx.x;
+        const bool f = s < B && !survives(s);
+        int32_t tot;
+        const int32_t r = block_rank(f, wsum, &tot);
+        if (f) holes[base + r] = s;
+        base += tot;
+    }
+    __syncthreads();
+    const int32_t nholes = base;
+
+    // --- movers: survivors in [B, n), ascending; k-th mover -> k-th hole ---
+    base = 0;
+    for (int32_t s0 = B; s0 < n; s0 += kEvThreads) {
+        const int32_t s = s0 + threadIdx.x;
+        const bool f = s < n && survives(s);
+        int32_t tot;
+        const int32_t r = block_rank(f, wsum, &tot);
+        if (f) {
+            if (base + r < nholes) move_slot(v, u, s, holes[base + r], 0, 1);
+            else atomicOr(v.err, DEVERR_STATE);
+        }
+        base += tot;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        if (base != nholes) atomicOr(v.err, DEVERR_STATE);
+        v.len[u] = B;
+        v.victim[u] = -1;
+        // return whole pages past slot B (one spare slot kept for the next append)
+        const int32_t keep = min(ceil_div(B + 1, v.page_tokens), v.max_pages);
+        const int32_t m = v.mapped[u];
+        if (m > keep) {
+            const int32_t cnt = m - keep;
+            const int32_t old = atomicAdd(v.free_top, cnt);
+            if (old + cnt > v.pool_pages) atomicOr(v.err, DEVERR_POOL);
+            for (int32_t i = 0; i < cnt; ++i) {
+                const int64_t e = (int64_t)u * v.max_pages + keep + i;
+                if (old + i < v.pool_pages) v.free_stack[old + i] = v.page_table[e];
+                v.page_table[e] = -1;
+            }
+            v.mapped[u] = keep;
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_evict_fast(const EvictArgs& a, cudaStream_t s) {
+    if (a.nunits <= 0) return cudaSuccess;
+    const int threads = 128;
+    k_evict_fast<<<ceil_div(a.nunits * 32, threads), threads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_evict_general(const EvictArgs& a, cudaStream_t s) {
+    if (a.nunits <= 0) return cudaSuccess;
+    k_evict_general<<<a.nunits, kEvThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace hikv

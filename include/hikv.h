@@ -1,0 +1,158 @@
+/*
+ * hikv — importance-aware, budgeted KV-cache decode step on one GPU (sm_103a).
+ *
+ * C ABI.  Every tensor argument is a plain pointer plus sizes; no C++ or torch
+ * types cross this boundary.  All tensor pointers are DEVICE pointers owned
+ * by the caller (contiguous, row-major, 16-byte aligned), unless a comment
+ * says "host".  The cache owns its page pool and metadata and frees them in
+ * hikv_destroy_cache.
+ *
+ * Method (citations name the page and its section):
+ *   - decode attention o_h = softmax(q_h K^T * scale) V over the retained
+ *     tokens of each (layer, batch, KV head) "unit"; query head h uses KV head
+ *     h / G (HiKV paper, sec. II-A; Kelle summary, sec. 2.2 eq. 1-2);
+ *   - each retained token's importance accumulates the softmax mass it
+ *     receives, summed over the G query heads of its KV group (KV cache
+ *     compression blog, sec. 3 "H2O" and sec. 5.2 on GQA; Kelle summary,
+ *     sec. 4.1 eq. 3);
+ *   - when a unit holds more than its budget B_u, it keeps the S sink tokens,
+ *     the W most recent tokens and the B_u - S - W most important others
+ *     (ties: lowest position kept), and compacts the survivors into its first
+ *     pages (blog sec. 3 "H2O" and "StreamingLLM"; per-head budgets, HeadKV
+ *     summary sec. 3.2; compaction, blog sec. 5.1).
+ *
+ * Streams and ordering: every call enqueues work on `stream` and returns
+ * without waiting for the GPU (create/destroy excepted).  Calls on one cache
+ * must be ordered on one stream (or ordered by the caller); overlapping calls
+ * on one cache race.  Argument and capacity errors are detected on the host,
+ * before anything is enqueued, from an exact host mirror of every unit's
+ * length; they leave the cache unchanged.  Launch failures return
+ * HIKV_ERR_CUDA.  hikv_last_error() gives a message for the calling thread.
+ *
+ * Units are numbered u = (layer * batch + b) * num_kv_heads + g.  A call on
+ * layers [layer0, layer0 + nlayers) touches exactly those units.
+ */
+#ifndef HIKV_H_
+#define HIKV_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;                    /* same type as cudaStream_t */
+typedef struct CUstream_st* hikv_stream_t;
+
+typedef struct hikv_cache hikv_cache;  /* opaque, library-owned */
+
+typedef enum {
+    HIKV_OK = 0,
+    HIKV_ERR_INVALID_ARG = 1,     /* bad pointer, size, range or config */
+    HIKV_ERR_OUT_OF_MEMORY = 2,   /* device allocation failed at create */
+    HIKV_ERR_CAPACITY = 3,        /* append past max_tokens or past the page pool */
+    HIKV_ERR_CUDA = 4,            /* a CUDA call or kernel launch failed */
+    HIKV_ERR_TIMEOUT = 5,         /* a bounded device-side wait gave up */
+    HIKV_ERR_STATE = 6,           /* call not valid in the cache's state (e.g. decode on an empty unit) */
+    HIKV_ERR_UNSUPPORTED = 7      /* shape outside the compiled kernel set */
+} hikv_status;
+
+typedef enum { HIKV_F32 = 0, HIKV_BF16 = 1 } hikv_dtype;
+
+typedef struct {
+    int32_t num_layers;     /* > 0 */
+    int32_t batch;          /* > 0 */
+    int32_t num_q_heads;    /* Hq, multiple of num_kv_heads */
+    int32_t num_kv_heads;   /* Hkv; group size G = Hq / Hkv in {1, 2, 4, 8} */
+    int32_t head_dim;       /* d in {64, 128} */
+    int32_t dtype;          /* hikv_dtype of K, V, q and out; accumulation is fp32 */
+    int32_t num_sink;       /* S >= 0: positions < S are never evicted */
+    int32_t recent_window;  /* W >= 0: the W newest positions are never evicted */
+    const int32_t* budgets; /* HOST [num_layers * num_kv_heads], B_u per (layer, KV
+                               head), shared by all batch rows; each >= S + W and >= 1.
+                               Copied at create. */
+    int32_t max_tokens;     /* slots per unit: a unit never holds more tokens */
+    int32_t page_tokens;    /* tokens per KV page: power of two, multiple of 16 (0 => 64) */
+    int64_t pool_pages;     /* pages in the shared pool (0 => every unit can reach
+                               max_tokens at once) */
+    int32_t max_window_queries; /* largest nq for hikv_score_window (0 => 32) */
+    float scale;            /* logit scale; 0 => 1/sqrt(head_dim) */
+} hikv_config;
+
+/* Create a cache: allocates the page pool, page tables, per-slot importance
+ * (fp32) and position (int32) arrays, and the work buffers, with cudaMalloc
+ * on the current device.  Synchronous.  On success *out owns all of it.
+ * Errors: INVALID_ARG (config), UNSUPPORTED (G or d or dtype), OUT_OF_MEMORY. */
+hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out);
+
+/* Free everything the cache owns (synchronises the device first).  NULL is a no-op. */
+hikv_status hikv_destroy_cache(hikv_cache* cache);
+
+/* Append ntok tokens to every unit of the layer range (HiKV Algorithm 1,
+ * last step: the new token's (k, v) enter the cache; Kelle summary sec. 8.4:
+ * a new token may reuse any free slot).  k, v: [nlayers][batch][Hkv][ntok][d]
+ * in the cache dtype.  New tokens get importance 0 and the next positions of
+ * their unit (positions count every token ever appended, from 0).
+ * Errors: INVALID_ARG, CAPACITY (a unit would exceed max_tokens, or the pool
+ * would run out of pages). */
+hikv_status hikv_append(hikv_cache* cache, int32_t layer0, int32_t nlayers, int32_t ntok,
+                        const void* k, const void* v, hikv_stream_t stream);
+
+/* Prefill importance: score the cached tokens with the queries of the last
+ * nq appended positions, causally (query i, at position t - nq + 1 + i, sees
+ * tokens at positions <= its own), adding each query's softmax mass summed
+ * over the group's heads to the tokens' importance, queries in position
+ * order (HiKV sec. III-D; SnapKV observation window, blog sec. 3).  No
+ * attention output.  q: [nlayers][batch][Hq][nq][d], 1 <= nq <=
+ * max_window_queries.  Errors: INVALID_ARG, STATE (a unit holds fewer than
+ * nq positions). */
+hikv_status hikv_score_window(hikv_cache* cache, int32_t layer0, int32_t nlayers, int32_t nq,
+                              const void* q, hikv_stream_t stream);
+
+/* One decode step of attention over every retained token (including any
+ * appended since the last step), plus the importance update.  q and out:
+ * [nlayers][batch][Hq][d] in the cache dtype; out may not alias q.
+ * Also records, for each unit holding more than its budget, its single
+ * least-important evictable token, which a following hikv_evict uses when it
+ * needs to drop exactly one token.  Errors: INVALID_ARG, STATE (an empty unit). */
+hikv_status hikv_decode_step(hikv_cache* cache, int32_t layer0, int32_t nlayers,
+                             const void* q, void* out, hikv_stream_t stream);
+
+/* Cut every unit of the range holding n > B_u tokens to exactly B_u:
+ * keep sinks, recent window and the B_u - S - W highest-importance others
+ * (ties keep the lower position), compact the survivors into slots
+ * [0, B_u) and return whole pages beyond the unit's need to the pool.
+ * Survivors keep their importance.  No-op for units with n <= B_u.  The
+ * caller picks the interval: after every step, every E steps, or once after
+ * prefill.  Errors: INVALID_ARG. */
+hikv_status hikv_evict(hikv_cache* cache, int32_t layer0, int32_t nlayers, hikv_stream_t stream);
+
+/* Export the retained state of every unit of the range, positions
+ * ascending.  lengths: [units]; positions (int32), importance (fp32):
+ * [units][cap]; k_out, v_out: [units][cap][d] in the cache dtype, or NULL to
+ * skip.  Rows past a unit's length hold position -1, importance 0 and zero
+ * K/V.  cap must be >= every unit's length.  lengths is written on the
+ * stream (read it after the stream synchronises).  Errors: INVALID_ARG. */
+hikv_status hikv_gather_retained(hikv_cache* cache, int32_t layer0, int32_t nlayers, int32_t cap,
+                                 int32_t* lengths, int32_t* positions, float* importance,
+                                 void* k_out, void* v_out, hikv_stream_t stream);
+
+/* HOST copy of the host mirror of each unit's length (no device access):
+ * lengths_host: [nlayers * batch * Hkv].  Errors: INVALID_ARG. */
+hikv_status hikv_get_lengths(const hikv_cache* cache, int32_t layer0, int32_t nlayers,
+                             int32_t* lengths_host);
+
+/* Synchronise the device and report device-side errors recorded by the
+ * kernels (a bounded wait that gave up, a page id out of range); clears them.
+ * Returns TIMEOUT or STATE for a recorded error, CUDA for a sticky CUDA
+ * error, else OK. */
+hikv_status hikv_device_status(hikv_cache* cache);
+
+/* Message for the last failing call on this thread ("" if none). */
+const char* hikv_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HIKV_H_ */

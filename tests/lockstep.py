@@ -1,0 +1,236 @@
+"""Lockstep parity harness: CUDA library vs CPU oracle on the same seeded inputs.
+
+The GPU cache runs the whole workload in the launch configuration the
+benchmark uses (all layers per call).  The oracle runs a sample of layers
+(all of them for small workloads) on the same inputs.  After every eviction
+the retained position sets of the sampled units are compared: they must be
+equal, except that a swap is accepted when the oracle's own scores of the
+swapped tokens lie within 1e-6 relative of each other (near-ties); the oracle
+is then resynced to the GPU's set so a near-tie cannot cascade.  Importance
+and attention outputs are compared with the tolerances of the method's
+statement: importance |d| <= 1e-4 |imp| + 1e-6 max|imp|; fp32 outputs per
+(unit, head) row ||d||_inf <= 1e-5 max(||o||_inf, 1e-3); bf16 outputs
+|d| <= 2e-2 elementwise.
+"""
+from __future__ import annotations
+
+import os
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+import oracle
+import workloads as W
+
+TIE_REL = 1e-6
+IMP_REL, IMP_ABS_FRAC = 1e-4, 1e-6
+OUT_F32_REL, OUT_BF16_ABS = 1e-5, 2e-2
+
+
+@dataclass
+class Report:
+    evictions_checked: int = 0
+    near_tie_swaps: int = 0
+    outputs_checked: int = 0
+    importance_checked: int = 0
+    max_out_err: float = 0.0
+    max_imp_err_rel: float = 0.0
+    notes: list = field(default_factory=list)
+
+
+def _to_dev(a: np.ndarray, dev):
+    return W.to_torch(np.ascontiguousarray(a)).to(dev, non_blocking=False)
+
+
+def _out_np(t: torch.Tensor) -> np.ndarray:
+    return t.float().cpu().numpy()
+
+
+class Lockstep:
+    def __init__(self, w: W.Workload, seed=None, sample_layers=None, cs=None, budgets=None,
+                 device="cuda", layer_chunk=None, full_cache=False, page_tokens=64,
+                 check_kv=True):
+        import importance_aware_kv_gb300 as hk
+        self.hk = hk
+        self.w = w
+        self.seed = w.index if seed is None else seed
+        self.dev = torch.device(device)
+        self.budgets = W.budgets(w, self.seed) if budgets is None else np.asarray(budgets, np.int32)
+        if full_cache:
+            self.budgets = np.full_like(self.budgets, w.total_positions)
+        self.sample = list(range(w.layers)) if sample_layers is None else list(sample_layers)
+        self.layer_chunk = layer_chunk or max(1, min(w.layers, int(2e9 // max(1, W.kv_bytes(
+            w.batch, w.prompt, 1, w.hkv, w.d, w.elem_bytes)))))
+        self.check_kv = check_kv
+        if cs is not None:
+            os.environ["HIKV_DECODE_CS"] = str(cs)
+        try:
+            self.cache = hk.Cache(hk.CacheConfig(
+                w.layers, w.batch, w.hq, w.hkv, w.d, w.dtype, w.sink, w.window,
+                self.budgets, w.total_positions, page_tokens=page_tokens,
+                max_window_queries=max(32, w.nq)))
+        finally:
+            if cs is not None:
+                os.environ.pop("HIKV_DECODE_CS", None)
+        bs = np.concatenate([self.budgets[l * w.hkv:(l + 1) * w.hkv] for l in self.sample])
+        self.ora = oracle.Oracle(len(self.sample), w.batch, w.hq, w.hkv, w.d, w.sink, w.window, bs,
+                                 out_bf16=(w.dtype == "bf16"), threads=os.cpu_count() or 1)
+        self.rep = Report()
+        self.upl = w.batch * w.hkv
+
+    # ------------------------------------------------------------------
+    def prefill(self):
+        w = self.w
+        for l0 in range(0, w.layers, self.layer_chunk):
+            nl = min(self.layer_chunk, w.layers - l0)
+            k, v = W.gen_kv(w, l0, nl, 0, w.prompt, self.seed)
+            self.cache.append(_to_dev(k, self.dev), _to_dev(v, self.dev), layer0=l0)
+            for si, l in enumerate(self.sample):
+                if l0 <= l < l0 + nl:
+                    self.ora.append(si, W.to_f32(k[l - l0:l - l0 + 1]), W.to_f32(v[l - l0:l - l0 + 1]))
+            del k, v
+        torch.cuda.synchronize()
+        q = W.gen_q(w, 0, w.layers, w.prompt - w.nq, w.nq, self.seed)
+        self.cache.score_window(_to_dev(q, self.dev))
+        for si, l in enumerate(self.sample):
+            self.ora.score_window(si, W.to_f32(q[l:l + 1]))
+        self.compare_state(after_evict=False)
+        self.cache.evict()
+        for si in range(len(self.sample)):
+            self.ora.evict(si, 1)
+        self.compare_state(after_evict=True, kv=True)
+
+    def _decode_inputs(self):
+        w = self.w
+        k, v = W.gen_kv(w, 0, w.layers, w.prompt, w.steps, self.seed)
+        q = W.gen_q(w, 0, w.layers, w.prompt, w.steps, self.seed)
+        # per-step contiguous slices: [steps][L][B][H][1][d] and [steps][L][B][Hq][d]
+        ks = np.ascontiguousarray(np.moveaxis(k, 3, 0)[:, :, :, :, None, :])
+        vs = np.ascontiguousarray(np.moveaxis(v, 3, 0)[:, :, :, :, None, :])
+        qs = np.ascontiguousarray(np.moveaxis(q, 3, 0))
+        return ks, vs, qs
+
+    def decode(self, steps=None, compare_every=1):
+        w = self.w
+        steps = w.steps if steps is None else steps
+        ks, vs, qs = self._decode_inputs()
+        dks, dvs, dqs = _to_dev(ks, self.dev), _to_dev(vs, self.dev), _to_dev(qs, self.dev)
+        out = torch.empty_like(dqs[0])
+        for s in range(steps):
+            self.cache.append(dks[s], dvs[s])
+            self.cache.decode_step(dqs[s], out)
+            evict_now = (s + 1) % w.evict_every == 0
+            if evict_now:
+                self.cache.evict()
+            for si, l in enumerate(self.sample):
+                self.ora.append(si, W.to_f32(ks[s, l:l + 1]), W.to_f32(vs[s, l:l + 1]))
+            ora_out = [self.ora.decode(si, W.to_f32(qs[s, l:l + 1])) for si, l in enumerate(self.sample)]
+            if evict_now:
+                for si in range(len(self.sample)):
+                    self.ora.evict(si, 1)
+            if (s % compare_every == 0) or s == steps - 1:
+                got = _out_np(out)
+                for si, l in enumerate(self.sample):
+                    self.compare_out(got[l], ora_out[si][0], s)
+            if evict_now:
+                self.compare_state(after_evict=True)
+        self.compare_state(after_evict=False, kv=True)
+        self.cache.device_status()
+        return self.rep
+
+    # ------------------------------------------------------------------
+    def compare_out(self, got, want, step):
+        w = self.w
+        if w.dtype == "f32":
+            rows_got = got.reshape(-1, w.d)
+            rows_want = want.reshape(-1, w.d)
+            err = np.abs(rows_got - rows_want).max(axis=1)
+            bound = OUT_F32_REL * np.maximum(np.abs(rows_want).max(axis=1), 1e-3)
+            bad = err > bound
+            if bad.any():
+                i = int(np.argmax(err / bound))
+                raise AssertionError(f"step {step}: fp32 output row {i} err {err[i]:.3e} > {bound[i]:.3e}")
+            self.rep.max_out_err = max(self.rep.max_out_err, float((err / bound).max()))
+        else:
+            err = np.abs(got - want)
+            m = float(err.max())
+            if m > OUT_BF16_ABS:
+                raise AssertionError(f"step {step}: bf16 output err {m:.3e} > {OUT_BF16_ABS}")
+            self.rep.max_out_err = max(self.rep.max_out_err, m)
+        self.rep.outputs_checked += got.size
+
+    def compare_state(self, after_evict: bool, kv: bool = False):
+        w = self.w
+        lens_host = self.cache.lengths()
+        for si, l in enumerate(self.sample):
+            lengths, positions, importance, kk, vv = self.cache.gather(
+                l, 1, with_kv=kv and self.check_kv and si == 0)
+            lengths = lengths.cpu().numpy()
+            positions = positions.cpu().numpy()
+            importance = importance.cpu().numpy()
+            for j in range(self.upl):
+                ou = si * self.upl + j
+                gu = l * self.upl + j
+                n = int(lengths[j])
+                assert n == int(lens_host[gu]), f"unit {gu}: device length {n} != host mirror {lens_host[gu]}"
+                gp = positions[j, :n]
+                gi = importance[j, :n]
+                assert np.all(np.diff(gp) > 0), f"unit {gu}: positions not strictly ascending"
+                op, oi = self.ora.state(ou)
+                if after_evict:
+                    self._compare_sets(ou, gu, gp, op, oi)
+                    op, oi = self.ora.state(ou)
+                assert np.array_equal(gp, op), f"unit {gu}: retained positions differ"
+                tol = IMP_REL * np.abs(oi) + IMP_ABS_FRAC * (np.abs(oi).max() if n else 0.0)
+                err = np.abs(gi - oi)
+                if np.any(err > tol):
+                    i = int(np.argmax(err - tol))
+                    raise AssertionError(f"unit {gu}: importance at pos {gp[i]}: gpu {gi[i]!r} oracle {oi[i]!r}")
+                rel = err / np.maximum(np.abs(oi), 1e-30)
+                self.rep.max_imp_err_rel = max(self.rep.max_imp_err_rel, float(rel.max()) if n else 0.0)
+                self.rep.importance_checked += n
+                if kk is not None and si == 0 and j in (0, self.upl - 1):
+                    self._check_kv(l, j, gp, kk[j, :n], vv[j, :n])
+            if after_evict:
+                self.rep.evictions_checked += self.upl
+
+    def _check_kv(self, layer, j, positions, kk, vv):
+        """Retained K/V rows must be byte-identical to the generated inputs."""
+        w = self.w
+        b, g = j // w.hkv, j % w.hkv
+        ka, va = W.gen_kv_unit(w, layer, b, g, 0, w.total_positions, self.seed)
+        want_k = ka[positions]
+        want_v = va[positions]
+        got_k = kk.cpu()
+        got_v = vv.cpu()
+        if w.dtype == "bf16":
+            got_k = got_k.view(torch.int16).numpy().view(np.uint16)
+            got_v = got_v.view(torch.int16).numpy().view(np.uint16)
+        else:
+            got_k, got_v = got_k.numpy(), got_v.numpy()
+        assert np.array_equal(got_k, want_k), f"layer {layer} unit {j}: K rows corrupted"
+        assert np.array_equal(got_v, want_v), f"layer {layer} unit {j}: V rows corrupted"
+
+    def _compare_sets(self, ou, gu, gp, op, oi):
+        gs, os_ = set(gp.tolist()), set(op.tolist())
+        if gs == os_:
+            return
+        gpu_only = np.array(sorted(gs - os_), dtype=np.int32)
+        ora_only = np.array(sorted(os_ - gs), dtype=np.int32)
+        assert len(gpu_only) == len(ora_only), f"unit {gu}: retained sizes differ"
+        ep, ei = self.ora.last_evicted(ou)
+        emap = dict(zip(ep.tolist(), ei.tolist()))
+        rmap = dict(zip(op.tolist(), oi.tolist()))
+        missing = [p for p in gpu_only.tolist() if p not in emap]
+        assert not missing, f"unit {gu}: GPU kept positions {missing[:5]} the oracle never had"
+        a = np.array([emap[p] for p in gpu_only.tolist()], dtype=np.float64)   # oracle evicted
+        b = np.array([rmap[p] for p in ora_only.tolist()], dtype=np.float64)   # oracle kept
+        hi = max(a.max(), b.max())
+        spread = b.max() - a.min()
+        if spread > TIE_REL * hi:
+            raise AssertionError(
+                f"unit {gu}: retained sets differ beyond near-ties: GPU kept {gpu_only[:4].tolist()} "
+                f"(oracle imp {a[:4].tolist()}), oracle kept {ora_only[:4].tolist()} (imp {b[:4].tolist()})")
+        self.rep.near_tie_swaps += len(gpu_only)
+        self.ora.resync(ou, gp)

@@ -1,0 +1,73 @@
+"""The C-ABI library loads here (no GPU) and exports every declared entry
+point; host-side argument checks answer before any CUDA call."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def hk():
+    from importance_aware_kv_gb300 import _build
+    _build.build()
+    import importance_aware_kv_gb300 as hk
+    return hk
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "hikv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(hikv_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(hk):
+    names = header_functions()
+    assert len(names) >= 10
+    lib = ctypes.CDLL(hk.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/hikv.h but not exported"
+    assert sorted(hk.ABI_FUNCTIONS) == names
+
+
+def _cfg(hk, **kw):
+    base = dict(num_layers=1, batch=1, num_q_heads=4, num_kv_heads=2, head_dim=64, dtype="f32",
+                num_sink=4, recent_window=8, budgets=[32, 32], max_tokens=128)
+    base.update(kw)
+    return hk.CacheConfig(**base)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(num_q_heads=6, num_kv_heads=4, budgets=[32] * 4), 1),   # Hq % Hkv
+    (dict(num_q_heads=12, num_kv_heads=4, budgets=[32] * 4), 7),  # G = 3
+    (dict(head_dim=96), 7),
+    (dict(budgets=[8, 32]), 1),                                   # budget < S + W
+    (dict(page_tokens=48), 1),
+    (dict(max_tokens=0), 1),
+    (dict(num_sink=-1), 1),
+])
+def test_create_rejects_bad_config_on_host(hk, kw, status):
+    with pytest.raises(hk.HikvError) as ei:
+        hk.hikv_create_cache(_cfg(hk, **kw))
+    assert ei.value.status == status
+
+
+def test_null_and_range_errors_need_no_device(hk):
+    lib = hk._lib
+    assert lib.hikv_append(None, 0, 1, 1, None, None, None) == hk.HIKV_ERR_INVALID_ARG
+    assert lib.hikv_decode_step(None, 0, 1, None, None, None) == hk.HIKV_ERR_INVALID_ARG
+    assert lib.hikv_evict(None, 0, 1, None) == hk.HIKV_ERR_INVALID_ARG
+    assert lib.hikv_destroy_cache(None) == hk.HIKV_OK
+    assert "layer range" in hk.hikv_last_error() or hk.hikv_last_error() == ""
+
+
+def test_create_without_device_reports_cuda(hk):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    with pytest.raises(hk.HikvError) as ei:
+        hk.hikv_create_cache(_cfg(hk))
+    assert ei.value.status == hk.HIKV_ERR_CUDA

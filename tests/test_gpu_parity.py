@@ -1,0 +1,147 @@
+"""GPU parity: the CUDA path against the CPU oracle, through the C ABI.
+
+Small workloads run every unit and every step in lockstep with the oracle;
+edge cases cover cluster splits, ragged tails, degenerate sink/window
+settings, group sizes, dtypes, the long-chunk (global logits) path, the
+exact tie rule, and host-detected errors.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from importance_aware_kv_gb300 import _build
+    _build.build()
+    import oracle
+    oracle._load()
+    W._load()
+
+
+def _ls(w, **kw):
+    from tests.lockstep import Lockstep
+    return Lockstep(w, **kw)
+
+
+def _run(w, **kw):
+    ls = _ls(w, **kw)
+    ls.prefill()
+    rep = ls.decode()
+    ls.cache.close()
+    return rep
+
+
+def test_tiny_fp32_workload_full_lockstep():
+    rep = _run(W.WORKLOADS[0])
+    assert rep.evictions_checked == 2 * (1 + 64)
+    assert rep.max_out_err <= 1.0
+
+
+def test_llama3_8b_layer_full_lockstep():
+    rep = _run(W.WORKLOADS[1])
+    assert rep.evictions_checked == 64 * (1 + 256)
+    print("near-tie swaps", rep.near_tie_swaps, "max bf16 err", rep.max_out_err,
+          "max imp rel err", rep.max_imp_err_rel)
+
+
+SMALL = W.Workload(100, "small", 2, 2, 8, 2, 128, "bf16", 300, 40, 96, 4, 16, 1, "bernoulli5x3")
+
+
+@pytest.mark.parametrize("cs", [1, 2, 4, 8, 16])
+def test_cluster_split_sizes(cs):
+    _run(SMALL, cs=cs)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(sink=0, window=0, budget=40),
+    dict(sink=0, window=12, budget=12),          # budget = S + W (StreamingLLM)
+    dict(sink=3, window=0, budget=3),
+    dict(sink=4, window=16, budget=20),
+    dict(sink=1, window=5, budget=77),           # ragged tile tails
+])
+def test_degenerate_sink_window(kw):
+    _run(SMALL.with_(**kw))
+
+
+@pytest.mark.parametrize("shape", [
+    dict(hq=2, hkv=2, d=64, dtype="f32"),        # G = 1
+    dict(hq=16, hkv=2, d=128, dtype="bf16"),     # G = 8
+    dict(hq=8, hkv=2, d=128, dtype="f32"),
+    dict(hq=8, hkv=2, d=64, dtype="bf16"),
+])
+def test_group_sizes_and_dtypes(shape):
+    _run(SMALL.with_(**shape))
+
+
+def test_evict_every_16_batched_select():
+    _run(SMALL.with_(evict_every=16, steps=48, budget=120, window=20))
+
+
+def test_ragged_budgets():
+    b = np.array([40, 96, 17 + 16, 200], dtype=np.int32)
+    _run(SMALL.with_(sink=1, window=16), budgets=b)
+
+
+def test_page_size_variants():
+    _run(SMALL, page_tokens=16)
+    _run(SMALL, page_tokens=256)
+
+
+def test_long_chunk_global_logits_path():
+    # 24k tokens in one unit: a CTA's chunk exceeds the shared-memory logits
+    w = W.Workload(101, "long", 1, 1, 8, 1, 128, "bf16", 24000, 6, 30000, 4, 64, 1, "zipf1.1")
+    _run(w, cs=2)
+
+
+def test_zero_keys_tie_rule_exact():
+    """All-zero keys: uniform softmax, whole classes of tokens tie exactly; the
+    GPU must keep the lowest positions, with no near-tie allowance."""
+    from tests.lockstep import Lockstep
+    w = W.Workload(102, "zero", 1, 1, 4, 1, 64, "f32", 200, 24, 60, 4, 16, 1, None)
+    ls = Lockstep(w, check_kv=False)
+    orig = W.gen_kv
+
+    def zero_keys(*a, **k):
+        kk, vv = orig(*a, **k)
+        return np.zeros_like(kk), vv
+    W.gen_kv = zero_keys
+    try:
+        ls.prefill()
+        ls.decode()
+    finally:
+        W.gen_kv = orig
+    assert ls.rep.near_tie_swaps == 0
+
+
+def test_host_errors_leave_cache_usable():
+    import importance_aware_kv_gb300 as hk
+    cfg = hk.CacheConfig(1, 1, 4, 2, 64, "f32", 2, 4, [16, 16], 40, page_tokens=16, pool_pages=4)
+    c = hk.Cache(cfg)
+    dev = torch.device("cuda")
+    q = torch.randn(1, 1, 4, 64, device=dev)
+    out = torch.empty_like(q)
+    with pytest.raises(hk.HikvError) as ei:
+        c.decode_step(q, out)                       # empty units
+    assert ei.value.status == hk.HIKV_ERR_STATE
+    k = torch.randn(1, 1, 2, 33, 64, device=dev)
+    with pytest.raises(hk.HikvError) as ei:
+        c.append(k, k.clone())                      # 2 units x 3 pages > pool of 4
+    assert ei.value.status == hk.HIKV_ERR_CAPACITY
+    k = torch.randn(1, 1, 2, 20, 64, device=dev)
+    c.append(k, k.clone())
+    with pytest.raises(hk.HikvError) as ei:
+        c.append(torch.randn(1, 1, 2, 21, 64, device=dev), torch.randn(1, 1, 2, 21, 64, device=dev))
+    assert ei.value.status == hk.HIKV_ERR_CAPACITY  # 41 > max_tokens
+    assert list(c.lengths()) == [20, 20]
+    c.decode_step(q, out)
+    c.evict()
+    assert list(c.lengths()) == [16, 16]
+    c.device_status()
+    c.close()

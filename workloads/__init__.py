@@ -228,6 +228,21 @@ def gen_kv(w: Workload, layer0: int, nlayers: int, pos0: int, npos: int,
     return k, v
 
 
+def gen_kv_unit(w: Workload, layer: int, batch: int, g: int, pos0: int, npos: int,
+                seed: Optional[int] = None):
+    """K and V rows [npos][d] of one (layer, batch, KV head) stream."""
+    seed = w.index if seed is None else seed
+    bf = w.dtype == "bf16"
+    dt = np.uint16 if bf else np.float32
+    k = np.empty((npos, w.d), dtype=dt)
+    v = np.empty_like(k)
+    hs = heavy_scale(w, seed, layer, batch)
+    sc = None if hs is None else np.ascontiguousarray(hs[pos0: pos0 + npos])
+    _fill_streams([(seed, T_KEY, layer, batch, g, pos0, npos, sc, k),
+                   (seed, T_VALUE, layer, batch, g, pos0, npos, None, v)], w.d, bf)
+    return k, v
+
+
 def gen_q(w: Workload, layer0: int, nlayers: int, pos0: int, npos: int,
           seed: Optional[int] = None):
     """Queries for positions [pos0, pos0+npos): [nlayers][batch][hq][npos][d]."""
