@@ -156,17 +156,21 @@ __global__ void __launch_bounds__(kEvThreads) k_evict_general(EvictArgs a) {
 
     // --- holes: dead slots in [0, B), ascending ---
     int32_t* holes = a.holes + a.hole_off[u];
+    const int32_t hole_cap = max(0, min(B, v.cap - B));   // size of this unit's hole list
     int32_t base = 0;
     for (int32_t s0 = 0; s0 < B; s0 += kEvThreads) {
         const int32_t s = s0 + threadIdx.x;
         const bool f = s < B && !survives(s);
         int32_t tot;
         const int32_t r = block_rank(f, wsum, &tot);
-        if (f) holes[base + r] = s;
+        if (f) {
+            if (base + r < hole_cap) holes[base + r] = s;
+            else atomicOr(v.err, DEVERR_STATE);
+        }
         base += tot;
     }
     __syncthreads();
-    const int32_t nholes = base;
+    const int32_t nholes = min(base, hole_cap);
 
     // --- movers: survivors in [B, n), ascending; k-th mover -> k-th hole ---
     base = 0;
