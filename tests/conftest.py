@@ -8,6 +8,16 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
+def build_native():
+    """Build libhikv.so in place if stale (loads the build script by path)."""
+    import importlib.util
+    path = os.path.join(ROOT, "importance_aware_kv_gb300", "_build.py")
+    spec = importlib.util.spec_from_file_location("hikv_native_build", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod.build()
+
+
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
     config.addinivalue_line("markers", "slow: full-size workload checks")

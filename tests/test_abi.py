@@ -12,8 +12,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def hk():
-    from importance_aware_kv_gb300 import _build
-    _build.build()
+    from tests.conftest import build_native
+    build_native()
     import importance_aware_kv_gb300 as hk
     return hk
 

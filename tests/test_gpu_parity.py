@@ -18,8 +18,8 @@ pytestmark = pytest.mark.gpu
 
 @pytest.fixture(scope="module", autouse=True)
 def built():
-    from importance_aware_kv_gb300 import _build
-    _build.build()
+    from tests.conftest import build_native
+    build_native()
     import oracle
     oracle._load()
     W._load()
