@@ -368,7 +368,7 @@ hikv_status hikv_decode_step(hikv_cache* c, int32_t layer0, int32_t nl, const vo
     } else {
         const int target = 3 * c->sm_count;
         while (cs < 8 && (int64_t)nu * cs < target) cs *= 2;
-        while (cs < 8 && ceil_div(maxn, cs) > c->max_smem_chunk) cs *= 2;
+        while (cs < kMaxCS && ceil_div(maxn, cs) > c->max_smem_chunk) cs *= 2;
     }
     cs = std::min(cs, std::max(1, maxn));
     const int chunk = ceil_div(maxn, cs);

@@ -95,9 +95,10 @@ def test_page_size_variants():
 
 
 def test_long_chunk_global_logits_path():
-    # 24k tokens in one unit: a CTA's chunk exceeds the shared-memory logits
-    w = W.Workload(101, "long", 1, 1, 8, 1, 128, "bf16", 24000, 6, 30000, 4, 64, 1, "zipf1.1")
-    _run(w, cs=2)
+    # 50k tokens in one unit at G = 8: even 16 CTAs leave chunks whose logits
+    # exceed shared memory, so the kernel keeps them in the global buffer
+    w = W.Workload(101, "long", 1, 1, 8, 1, 128, "bf16", 50000, 6, 60000, 4, 64, 1, "zipf1.1")
+    _run(w)
 
 
 def test_zero_keys_tie_rule_exact():
