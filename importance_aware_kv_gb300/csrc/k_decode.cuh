@@ -2,21 +2,23 @@
 //
 // One thread-block cluster per unit (layer, batch, KV head); its CS CTAs split
 // the unit's n live slots into equal chunks.  Per CTA:
-//   producer warp  streams the chunk's K rows, then its V rows, 16-row tiles,
-//                  HBM -> shared memory with 1-D TMA bulk copies into an
-//                  NSTAGE ring (mbarrier full/empty pairs, bounded waits);
-//   4 consumer warps
-//     phase A  logits s'_hj = <q_h * scale * log2 e, k_j> for the G query heads
-//              of the group; a lane holds d/32 elements of a row, and a
-//              warp-level reduce-scatter leaves one (row, head) sum per lane;
-//              logits stay in shared memory (or an L2-resident global buffer
-//              for very long chunks);
-//     max/exp  chunk max m_c per head, P_c = exp2(s' - m_c) in place, l_c;
-//     phase B  O_c[h] = sum_j P_c[j][h] v_j (lane-per-dims, no shuffles).
-//   cluster merge (DSMEM): m = max_c m_c, l = sum_c l_c 2^(m_c - m),
-//     beta_c = 2^(m_c - m) / l; out_h = sum_c beta_c O_c[h]; importance
-//     imp_j += sum_h P_c[j][h] beta_c[h] (fp32 add, heads ascending), and the
-//     eligible slot with the smallest (imp, -pos) is the step's victim.
+//   producer warp  streams the chunk in 16-row tiles, each tile's K rows and
+//                  V rows together, HBM -> shared memory with 1-D TMA bulk
+//                  copies into an NSTAGE ring (mbarrier full/empty pairs,
+//                  bounded waits);
+//   4 consumer warps, each owning every 4th row of a tile, keep a private
+//   online softmax (running max m_w, sum l_w, unnormalised O_w):
+//     logits s'_hj = <q_h * scale * log2 e, k_j> for the G query heads of the
+//     group -- a lane holds d/32 elements of a row, a warp reduce-scatter
+//     leaves one (row, head) sum per lane; logits are kept (shared memory, or
+//     an L2-resident global buffer for very long chunks) for the importance
+//     update; then p = 2^(s' - m_w), O_w += p v_j for the same tile's V rows.
+//   CTA merge of the 4 warp states, then a cluster merge by remote stores
+//   into shared memory (DSMEM) before one cluster barrier:
+//     m = max_c m_c, l = sum_c l_c 2^(m_c - m); out_h = sum_c O_c[h] 2^(m_c - m) / l;
+//     importance imp_j += sum_h 2^(s'_hj - m_h) / l_h (fp32 add, heads
+//     ascending), and the eligible slot with the smallest (imp, -pos) is the
+//     step's victim, gathered in CTA 0 by a second remote store + barrier.
 //
 // Method: decode attention P = softmax(q K^T), O = P V (HiKV sec. II-A; Kelle
 // summary sec. 2.2); importance accumulates P summed over the group's heads
@@ -34,7 +36,7 @@ namespace hikv {
 constexpr int kDecNCW = 4;                       // consumer warps
 constexpr int kDecThreads = (kDecNCW + 1) * 32;  // + producer warp
 constexpr int kDecTR = 16;                       // rows per tile
-constexpr int kDecStages = 8;
+constexpr int kDecStages = 4;
 
 // reduce-scatter of N0 per-lane values over the warp.  Stage k exchanges half
 // of the remaining values with the lane 16 >> k away; afterwards lane l holds
@@ -69,26 +71,28 @@ __device__ __forceinline__ float warp_reduce_scatter_full(float (&v)[N], int lan
 
 struct DecSmem {
     // byte offsets into dynamic shared memory
-    uint32_t ring, bars, red, small, S, simp, spos, total;
+    uint32_t ring, bars, ws, recv, small, S, simp, spos, total;
 };
 
 template <typename T, int D, int G>
 __host__ __device__ constexpr uint32_t dec_ring_bytes() {
-    return (uint32_t)kDecStages * kDecTR * D * sizeof(T);
+    return (uint32_t)kDecStages * 2 * kDecTR * D * sizeof(T);
 }
 
 template <typename T, int D, int G>
 __host__ __device__ inline DecSmem dec_layout(bool smem_s, int chunk_cap) {
     DecSmem L{};
     uint32_t off = 0;
-    L.ring = off;
+    L.ring = off;                                 // also the warp-partial O buffer after streaming
     off += dec_ring_bytes<T, D, G>();
     L.bars = off;
     off += 2 * kDecStages * 8;
-    L.red = off;
-    off += kDecNCW * G * D * 4;
+    L.ws = off;                                   // [NCW][2][32] per-warp broadcast scratch
+    off += kDecNCW * 2 * 32 * 4;
+    L.recv = off;                                 // O slices from every CTA: G*D + kMaxCS floats
+    off += (G * D + kMaxCS) * 4;
     L.small = off;
-    off += 4096;  // scalars (see k_decode)
+    off += 4096;
     L.S = off;
     if (smem_s) {
         off += (uint32_t)chunk_cap * G * 4;
@@ -105,12 +109,14 @@ __host__ __device__ inline DecSmem dec_layout(bool smem_s, int chunk_cap) {
 }
 
 template <typename T, int D, int G, bool SMEM_S>
-__global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
+__global__ void __launch_bounds__(kDecThreads, (G <= 4 ? 4 : 2)) k_decode(const DecodeArgs a) {
     constexpr int RB = D * (int)sizeof(T);   // row bytes
+    constexpr int TB = kDecTR * RB;          // tile bytes (K or V)
     constexpr int EPL = D / 32;              // elements per lane
     constexpr int LB = EPL * (int)sizeof(T); // bytes per lane
     constexpr int RPW = kDecTR / kDecNCW;    // rows per warp per tile
     constexpr int NV = RPW * G;              // logits per warp per tile
+    constexpr int NCT = kDecNCW * 32;        // consumer threads
     static_assert(NV <= 32 && (NV & (NV - 1)) == 0, "group size");
     using Raw = typename RawVec<LB>::type;
 
@@ -123,18 +129,23 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
     uint8_t* ring = smem + L.ring;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
     uint64_t* empty = full + kDecStages;
-    float* red = reinterpret_cast<float*>(smem + L.red);  // [NCW][G][D]; O_c = red[0..G*D)
+    float* ws = reinterpret_cast<float*>(smem + L.ws);        // [NCW][2][32]
+    float* orecv = reinterpret_cast<float*>(smem + L.recv);   // [CS][per]
     float* sm = reinterpret_cast<float*>(smem + L.small);
-    float* m_c = sm;                 // [G]
-    float* l_c = sm + 8;             // [G]
-    float* wred = sm + 16;           // [NCW][G]
-    float* pm = sm + 64;             // [kMaxCS][G]
-    float* pl = pm + kMaxCS * 8;     // [kMaxCS][G]
-    float* beta = pl + kMaxCS * 8;   // [kMaxCS][G]
-    float* mfin = beta + kMaxCS * 8; // [G]
-    float* linv = mfin + 8;          // [G]
-    unsigned long long* wkey = reinterpret_cast<unsigned long long*>(linv + 8 + 8);  // [NCW]
-    int32_t* wslot = reinterpret_cast<int32_t*>(wkey + kDecNCW);                        // [NCW]
+    float* m_recv = sm;                        // [kMaxCS][G]  (128)
+    float* l_recv = sm + 128;                  // [kMaxCS][G]  (128)
+    float* beta = sm + 256;                    // [kMaxCS][G]  (128)
+    float* mw_s = sm + 384;                    // [NCW][G]     (32)
+    float* lw_s = sm + 416;                    // [NCW][G]     (32)
+    float* wsc = sm + 448;                     // [NCW][G]     (32)
+    float* m_c = sm + 480;                     // [G]
+    float* l_c = sm + 488;                     // [G]
+    float* mfin = sm + 496;                    // [G]
+    float* linv = sm + 504;                    // [G]
+    unsigned long long* akey = reinterpret_cast<unsigned long long*>(sm + 512);  // [kMaxCS]
+    int32_t* aslot = reinterpret_cast<int32_t*>(akey + kMaxCS);                  // [kMaxCS]
+    unsigned long long* wkey = reinterpret_cast<unsigned long long*>(aslot + kMaxCS);  // [NCW]
+    int32_t* wslot = reinterpret_cast<int32_t*>(wkey + kDecNCW);                     // [NCW]
     volatile int32_t* abort_flag = wslot + kDecNCW;
     float* S_smem = reinterpret_cast<float*>(smem + L.S);
     float* simp = reinterpret_cast<float*>(smem + L.simp);
@@ -163,6 +174,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
     const int32_t first_blk = t0 / kDecTR;
     const int32_t nt = cnt > 0 ? (t1 - 1) / kDecTR - first_blk + 1 : 0;
     const int64_t qbase = (((int64_t)li * v.batch + b) * v.hq + (int64_t)g * G) * D;
+    const int32_t per = ceil_div(G * D, CS);   // output elements finalised per CTA
 
     float* Sb = SMEM_S ? S_smem : a.logits + ((int64_t)u * v.cap) * G;
     const int32_t s_off = SMEM_S ? t0 : 0;   // S index of slot s = (s - s_off) * G
@@ -181,7 +193,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
         // ---------------- producer ----------------
         if (lane == 0) {
             int it = 0;
-            for (; it < 2 * nt; ++it) {
+            for (; it < nt; ++it) {
                 if (*abort_flag) break;
                 const int st = it % kDecStages;
                 const uint32_t round = (uint32_t)(it / kDecStages);
@@ -189,19 +201,20 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
                     *abort_flag = 1;
                     break;
                 }
-                const int i = it < nt ? it : it - nt;
-                const int32_t s0 = max(t0, (first_blk + i) * kDecTR);
-                const int32_t s1 = min(t1, (first_blk + i + 1) * kDecTR);
-                const uint8_t* src = row_ptr(v, u, s0, it >= nt);
+                const int32_t s0 = max(t0, (first_blk + it) * kDecTR);
+                const int32_t s1 = min(t1, (first_blk + it + 1) * kDecTR);
+                const uint8_t* ksrc = row_ptr(v, u, s0, false);
+                const uint8_t* vsrc = row_ptr(v, u, s0, true);
                 const uint32_t bytes = (uint32_t)(s1 - s0) * RB;
-                if (src == nullptr) {
+                if (ksrc == nullptr || vsrc == nullptr) {
                     // unmapped page: complete the stage without data
                     *abort_flag = 1;
                     mbar_arrive(&full[st]);
                     break;
                 }
-                mbar_arrive_expect_tx(&full[st], bytes);
-                bulk_g2s(ring + st * (kDecTR * RB), src, bytes, &full[st]);
+                mbar_arrive_expect_tx(&full[st], 2 * bytes);
+                bulk_g2s(ring + st * 2 * TB, ksrc, bytes, &full[st]);
+                bulk_g2s(ring + st * 2 * TB + TB, vsrc, bytes, &full[st]);
             }
             if (*abort_flag) {
                 // let copies already in flight land before the CTA can exit
@@ -220,18 +233,34 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
     float qr[G][EPL];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-        const T* qp = reinterpret_cast<const T*>(a.q) + qbase + (int64_t)h * D + lane * EPL;
+        const Raw raw = *reinterpret_cast<const Raw*>(reinterpret_cast<const T*>(a.q) + qbase +
+                                                      (int64_t)h * D + lane * EPL);
+        Widen<T, EPL>::run(raw, qr[h]);
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) qr[h][e] = Elem<T>::to_f(qp[e]) * a.qscale;
+        for (int e = 0; e < EPL; ++e) qr[h][e] *= a.qscale;
     }
     if (SMEM_S) {
-        for (int j = ctid; j < cnt; j += kDecNCW * 32) {
+        for (int j = ctid; j < cnt; j += NCT) {
             simp[j] = v.imp[(int64_t)u * v.cap + t0 + j];
             spos[j] = v.pos[(int64_t)u * v.cap + t0 + j];
         }
     }
 
-    // phase A: logits
+    float* ws_s = ws + warp * 64;        // this warp's logits of the tile, [k*G + h]
+    float* ws_p = ws_s + 32;             // this warp's probabilities of the tile
+    float m_w[G], l_w[G], o[G][EPL];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        m_w[h] = -INFINITY;
+        l_w[h] = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) o[h][e] = 0.f;
+    }
+    constexpr int stride = 32 / NV;
+    const int vi = lane / stride;             // (row, head) value this lane ends up with
+    const int vk = vi / G, vh = vi % G;
+    const bool writer = (lane & (stride - 1)) == 0;
+
     for (int i = 0; i < nt; ++i) {
         if (*abort_flag) break;
         const int st = i % kDecStages;
@@ -241,14 +270,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
         }
         const int32_t s0 = max(t0, (first_blk + i) * kDecTR);
         const int32_t rows = min(t1, (first_blk + i + 1) * kDecTR) - s0;
-        const uint8_t* tile = ring + st * (kDecTR * RB);
+        const uint8_t* ktile = ring + st * 2 * TB;
+        const uint8_t* vtile = ktile + TB;
+        // logits of this warp's rows
         float acc[NV];
 #pragma unroll
         for (int k = 0; k < RPW; ++k) {
             const int r = warp + kDecNCW * k;
             float x[EPL];
             if (r < rows) {
-                Raw raw = *reinterpret_cast<const Raw*>(tile + r * RB + lane * LB);
+                Raw raw = *reinterpret_cast<const Raw*>(ktile + r * RB + lane * LB);
                 Widen<T, EPL>::run(raw, x);
             } else {
 #pragma unroll
@@ -262,175 +293,156 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
                 acc[k * G + h] = sacc;
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
         const float val = warp_reduce_scatter_full<NV>(acc, lane);
-        constexpr int stride = 32 / NV;
-        if ((lane & (stride - 1)) == 0) {
-            const int vi = lane / stride;
-            const int k = vi / G, h = vi % G;
-            const int r = warp + kDecNCW * k;
-            if (r < rows) Sb[(int64_t)(s0 + r - s_off) * G + h] = val;
+        const int vr = warp + kDecNCW * vk;       // tile row of this lane's value
+        if (writer) {
+            ws_s[vi] = (vr < rows) ? val : -INFINITY;
+            if (vr < rows) Sb[(int64_t)(s0 + vr - s_off) * G + vh] = val;
         }
-    }
-    named_bar_sync(1, kDecNCW * 32);
-
-    // chunk max per head
-    {
-        float mloc[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h) mloc[h] = -INFINITY;
-        for (int j = ctid; j < cnt; j += kDecNCW * 32) {
-#pragma unroll
-            for (int h = 0; h < G; ++h) mloc[h] = fmaxf(mloc[h], Sb[(int64_t)(t0 + j - s_off) * G + h]);
-        }
+        __syncwarp();
+        // tile max per head over this warp's valid rows; new running max
+        float m_new[G], scl[G];
+        bool rescale = false;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
+            float tm = -INFINITY;
 #pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) mloc[h] = fmaxf(mloc[h], __shfl_xor_sync(0xffffffffu, mloc[h], o));
-            if (lane == 0) wred[warp * G + h] = mloc[h];
+            for (int k = 0; k < RPW; ++k) tm = fmaxf(tm, ws_s[k * G + h]);
+            m_new[h] = fmaxf(m_w[h], tm);
+            scl[h] = (m_new[h] == m_w[h]) ? 1.f : exp2f(m_w[h] - m_new[h]);   // m_w = -inf -> 0
+            rescale |= (m_new[h] != m_w[h]);
         }
-        named_bar_sync(1, kDecNCW * 32);
-        if (ctid < G) {
-            float m = -INFINITY;
-            for (int w = 0; w < kDecNCW; ++w) m = fmaxf(m, wred[w * G + ctid]);
-            m_c[ctid] = m;
-        }
-        named_bar_sync(1, kDecNCW * 32);
-    }
-    // P_c = exp2(s' - m_c) in place, l_c
-    {
-        float mh[G], lsum[G];
+        if (writer) {
+            float mh = m_new[0];
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-            mh[h] = m_c[h];
-            lsum[h] = 0.f;
+            for (int h = 1; h < G; ++h)
+                if (vh == h) mh = m_new[h];
+            ws_p[vi] = (vr < rows) ? exp2f(val - mh) : 0.f;
         }
-        for (int j = ctid; j < cnt; j += kDecNCW * 32) {
-            float* row = Sb + (int64_t)(t0 + j - s_off) * G;
+        __syncwarp();
+        if (rescale) {
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                const float p = exp2f(row[h] - mh[h]);
-                row[h] = p;
-                lsum[h] += p;
+                l_w[h] *= scl[h];
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) o[h][e] *= scl[h];
             }
         }
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) lsum[h] += __shfl_xor_sync(0xffffffffu, lsum[h], o);
-        }
-        // wred reuse: every consumer passed the barrier after reading it
-        if (lane == 0) {
-#pragma unroll
-            for (int h = 0; h < G; ++h) wred[warp * G + h] = lsum[h];
-        }
-        named_bar_sync(1, kDecNCW * 32);
-        if (ctid < G) {
-            float l = 0.f;
-            for (int w = 0; w < kDecNCW; ++w) l += wred[w * G + ctid];
-            l_c[ctid] = l;
-        }
-        // the barrier below also publishes the P values written above
-    }
-    named_bar_sync(1, kDecNCW * 32);
-
-    // phase B: O_c = sum_j P_c[j] v_j
-    float o[G][EPL];
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) o[h][e] = 0.f;
-    for (int i = 0; i < nt; ++i) {
-        if (*abort_flag) break;
-        const int it = nt + i;
-        const int st = it % kDecStages;
-        if (!mbar_wait_bounded(&full[st], (uint32_t)(it / kDecStages) & 1u, v.err)) {
-            *abort_flag = 1;
-            break;
-        }
-        const int32_t s0 = max(t0, (first_blk + i) * kDecTR);
-        const int32_t rows = min(t1, (first_blk + i + 1) * kDecTR) - s0;
-        const uint8_t* tile = ring + st * (kDecTR * RB);
+        for (int h = 0; h < G; ++h) m_w[h] = m_new[h];
 #pragma unroll
         for (int k = 0; k < RPW; ++k) {
             const int r = warp + kDecNCW * k;
             if (r < rows) {
-                Raw raw = *reinterpret_cast<const Raw*>(tile + r * RB + lane * LB);
+                float p[G];
+#pragma unroll
+                for (int h = 0; h < G; ++h) p[h] = ws_p[k * G + h];
+                Raw raw = *reinterpret_cast<const Raw*>(vtile + r * RB + lane * LB);
                 float x[EPL];
                 Widen<T, EPL>::run(raw, x);
-                const float* prow = Sb + (int64_t)(s0 + r - s_off) * G;
-                float p[G];
-                if constexpr (G % 4 == 0) {
 #pragma unroll
-                    for (int h = 0; h < G; h += 4) {
-                        float4 t4 = *reinterpret_cast<const float4*>(prow + h);
-                        p[h] = t4.x; p[h + 1] = t4.y; p[h + 2] = t4.z; p[h + 3] = t4.w;
-                    }
-                } else {
-#pragma unroll
-                    for (int h = 0; h < G; ++h) p[h] = prow[h];
-                }
-#pragma unroll
-                for (int h = 0; h < G; ++h)
+                for (int h = 0; h < G; ++h) {
+                    l_w[h] += p[h];
 #pragma unroll
                     for (int e = 0; e < EPL; ++e) o[h][e] = fmaf(p[h], x[e], o[h][e]);
+                }
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
     }
+
+    // ---- CTA merge of the 4 warp states (ring reused for the O partials) ----
+    if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            mw_s[warp * G + h] = m_w[h];
+            lw_s[warp * G + h] = l_w[h];
+        }
+    }
+    named_bar_sync(1, NCT);   // every warp is done with the ring
+    float* red = reinterpret_cast<float*>(ring);   // [NCW][G][D]
 #pragma unroll
     for (int h = 0; h < G; ++h)
 #pragma unroll
         for (int e = 0; e < EPL; ++e) red[(warp * G + h) * D + lane * EPL + e] = o[h][e];
-    named_bar_sync(1, kDecNCW * 32);
-    for (int idx = ctid; idx < G * D; idx += kDecNCW * 32) {
-        float s = red[idx];
-        for (int w = 1; w < kDecNCW; ++w) s += red[w * G * D + idx];
-        red[idx] = s;  // O_c
+    if (ctid < G) {
+        float m = -INFINITY;
+        for (int w = 0; w < kDecNCW; ++w) m = fmaxf(m, mw_s[w * G + ctid]);
+        float l = 0.f;
+        for (int w = 0; w < kDecNCW; ++w) {
+            const float mw = mw_s[w * G + ctid];
+            const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - m);
+            wsc[w * G + ctid] = f;
+            l += lw_s[w * G + ctid] * f;
+        }
+        m_c[ctid] = m;
+        l_c[ctid] = l;
+    }
+    named_bar_sync(1, NCT);
+    // push (m_c, l_c) to every CTA of the cluster and O_c slices to their owners
+    if (ctid < CS * G) {
+        const int cc = ctid / G, h = ctid % G;
+        dsmem_st_f32(dsmem_addr(&m_recv[c * G + h], (uint32_t)cc), m_c[h]);
+        dsmem_st_f32(dsmem_addr(&l_recv[c * G + h], (uint32_t)cc), l_c[h]);
+    }
+    for (int idx = ctid; idx < G * D; idx += NCT) {
+        const int h = idx / D;
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < kDecNCW; ++w) s += red[w * G * D + idx] * wsc[w * G + h];
+        const int owner = idx / per, loc = idx - owner * per;
+        dsmem_st_f32(dsmem_addr(&orecv[c * per + loc], (uint32_t)owner), s);
     }
 
     __syncwarp();
-    cluster_sync_all();  // #1: m_c, l_c, O_c of every CTA are visible
+    cluster_sync_all();  // #1: every CTA's (m_c, l_c) and O slices are in place
 
-    if (ctid < CS * G) {
-        const int cc = ctid / G, h = ctid % G;
-        pm[cc * G + h] = dsmem_ld_f32(dsmem_addr(&m_c[h], (uint32_t)cc));
-        pl[cc * G + h] = dsmem_ld_f32(dsmem_addr(&l_c[h], (uint32_t)cc));
-    }
-    named_bar_sync(1, kDecNCW * 32);
     if (ctid < G) {
         float m = -INFINITY;
-        for (int cc = 0; cc < CS; ++cc) m = fmaxf(m, pm[cc * G + ctid]);
+        for (int cc = 0; cc < CS; ++cc) m = fmaxf(m, m_recv[cc * G + ctid]);
         float l = 0.f;
         for (int cc = 0; cc < CS; ++cc)
-            if (pl[cc * G + ctid] > 0.f) l += pl[cc * G + ctid] * exp2f(pm[cc * G + ctid] - m);
+            if (l_recv[cc * G + ctid] > 0.f) l += l_recv[cc * G + ctid] * exp2f(m_recv[cc * G + ctid] - m);
         mfin[ctid] = m;
         linv[ctid] = 1.0f / l;
     }
-    named_bar_sync(1, kDecNCW * 32);
+    named_bar_sync(1, NCT);
     if (ctid < CS * G) {
         const int h = ctid % G;
-        const float pmv = pm[ctid];
-        beta[ctid] = (pl[ctid] > 0.f) ? exp2f(pmv - mfin[h]) * linv[h] : 0.f;
+        beta[ctid] = (l_recv[ctid] > 0.f) ? exp2f(m_recv[ctid] - mfin[h]) * linv[h] : 0.f;
     }
-    named_bar_sync(1, kDecNCW * 32);
+    named_bar_sync(1, NCT);
 
+    // output slice owned by this CTA
+    {
+        T* outp = reinterpret_cast<T*>(a.out) + qbase;
+        for (int loc = ctid; loc < per; loc += NCT) {
+            const int idx = c * per + loc;
+            if (idx >= G * D) break;
+            const int h = idx / D;
+            float s = 0.f;
+            for (int cc = 0; cc < CS; ++cc) s += orecv[cc * per + loc] * beta[cc * G + h];
+            outp[idx] = Elem<T>::from_f(s);
+        }
+    }
     // importance update + local victim
     {
-        float bc[G];
+        float mf[G], li_[G];
 #pragma unroll
-        for (int h = 0; h < G; ++h) bc[h] = beta[c * G + h];
+        for (int h = 0; h < G; ++h) {
+            mf[h] = mfin[h];
+            li_[h] = linv[h];
+        }
         unsigned long long kmin = ~0ull;
         int32_t smin = -1;
         const int32_t lo = v.sink, hi = tnew - v.window;
-        for (int j = ctid; j < cnt; j += kDecNCW * 32) {
+        for (int j = ctid; j < cnt; j += NCT) {
             const int32_t slot = t0 + j;
-            const float* prow = Sb + (int64_t)(slot - s_off) * G;
+            const float* srow = Sb + (int64_t)(slot - s_off) * G;
             float inc = 0.f;
 #pragma unroll
-            for (int h = 0; h < G; ++h) inc += prow[h] * bc[h];
+            for (int h = 0; h < G; ++h) inc += exp2f(srow[h] - mf[h]) * li_[h];
             const int64_t mi = (int64_t)u * v.cap + slot;
             const float old = SMEM_S ? simp[j] : v.imp[mi];
             const float nw = old + inc;
@@ -463,19 +475,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
             }
         }
     }
-    // output slice of this CTA
-    {
-        const int32_t per = ceil_div(G * D, CS);
-        const int32_t e0 = c * per, e1 = min(G * D, e0 + per);
-        T* outp = reinterpret_cast<T*>(a.out) + qbase;
-        for (int idx = e0 + ctid; idx < e1; idx += kDecNCW * 32) {
-            const int h = idx / D;
-            float s = 0.f;
-            for (int cc = 0; cc < CS; ++cc) s += dsmem_ld_f32(dsmem_addr(&red[idx], (uint32_t)cc)) * beta[cc * G + h];
-            outp[idx] = Elem<T>::from_f(s);
-        }
-    }
-    named_bar_sync(1, kDecNCW * 32);
+    named_bar_sync(1, NCT);
     if (ctid == 0 && need_victim) {
         unsigned long long k = ~0ull;
         int32_t s = -1;
@@ -484,24 +484,22 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(const DecodeArgs a) {
                 k = wkey[w];
                 s = wslot[w];
             }
-        a.cand[(int64_t)u * kMaxCS + c] = k;
-        a.cand_slot[(int64_t)u * kMaxCS + c] = s;
+        dsmem_st_u64(dsmem_addr(&akey[c], 0u), k);
+        dsmem_st_s32(dsmem_addr(&aslot[c], 0u), s);
     }
 
     __syncwarp();
-    cluster_sync_all();  // #2: peers done reading this CTA's shared memory; cand visible
+    cluster_sync_all();  // #2: every CTA's local victim is in CTA 0
 
     if (c == 0 && ctid == 0) {
         int32_t vs = -1;
         if (need_victim) {
             unsigned long long k = ~0ull;
-            for (int cc = 0; cc < CS; ++cc) {
-                const unsigned long long kk = a.cand[(int64_t)u * kMaxCS + cc];
-                if (kk < k) {
-                    k = kk;
-                    vs = a.cand_slot[(int64_t)u * kMaxCS + cc];
+            for (int cc = 0; cc < CS; ++cc)
+                if (akey[cc] < k) {
+                    k = akey[cc];
+                    vs = aslot[cc];
                 }
-            }
         }
         v.victim[u] = vs;
     }
