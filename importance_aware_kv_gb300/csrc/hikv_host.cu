@@ -1,6 +1,8 @@
 // Host side of the hikv C ABI: argument checks, the exact host mirror of each
 // unit's length and mapped pages, device allocation, and kernel launches.
 // Nothing here synchronises the device except create/destroy/device_status.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -42,6 +44,21 @@ hikv_status cuda_fail(cudaError_t e, const char* what) {
 
 constexpr int kWindowChunk = 1024;   // tokens per CTA of the window-scoring kernels
 
+// cuTensorMapEncodeTiled from the driver, found through the runtime (no
+// link-time dependency on libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
 }  // namespace
 
 struct hikv_cache {
@@ -67,6 +84,7 @@ struct hikv_cache {
     int wchunks = 0;
     int32_t* d_order_all = nullptr;
     int32_t* d_order_layer = nullptr;
+    CUtensorMap tmap;                   // the pool as rows of d elements, 16 x 128-byte swizzled boxes
     std::vector<void*> allocs;
     // host mirror
     std::vector<int32_t> len, next_pos, mapped;
@@ -219,6 +237,32 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
     ALLOC(c->d_order_layer, U);
     if (need_logits) ALLOC(c->d_logits, U * (size_t)c->cap * G);
 #undef ALLOC
+
+    // TMA descriptor of the pool: [pool_pages * 2P rows][d elements], boxes of
+    // 16 rows x 128 bytes with the 128-byte swizzle the decode kernel reads
+    {
+        const uint64_t rows = (uint64_t)c->pool_pages * 2 * P;
+        auto enc = tensor_map_encoder();
+        if (!enc || rows > 0xFFFFFFFFull) {
+            free_all(c);
+            delete c;
+            return fail(enc ? HIKV_ERR_UNSUPPORTED : HIKV_ERR_CUDA,
+                        enc ? "create: pool too large for one tensor map" : "create: cuTensorMapEncodeTiled unavailable");
+        }
+        cuuint64_t dims[2] = {(cuuint64_t)c->d, (cuuint64_t)rows};
+        cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+        cuuint32_t box[2] = {(cuuint32_t)(128 / c->esz), 16u};
+        cuuint32_t estr[2] = {1u, 1u};
+        CUresult r = enc(&c->tmap, c->dtype == HIKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                         2, v.pool, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) {
+            free_all(c);
+            delete c;
+            return fail(HIKV_ERR_CUDA, "create: cuTensorMapEncodeTiled failed (%d)", (int)r);
+        }
+    }
 
     // initial device state
     std::vector<int32_t> stack((size_t)c->pool_pages);
@@ -389,7 +433,7 @@ hikv_status hikv_decode_step(hikv_cache* c, int32_t layer0, int32_t nl, const vo
     a.cs = cs;
     a.chunk_cap = smem_path ? chunk : 0;
     const size_t smem = decode_smem_bytes(c->dtype, c->d, c->G, smem_path, a.chunk_cap);
-    cudaError_t e = launch_decode(a, c->dtype, c->d, c->G, smem_path, smem, (cudaStream_t)stream);
+    cudaError_t e = launch_decode(a, c->tmap, c->dtype, c->d, c->G, smem_path, smem, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode_step: launch");
     for (int u = u0; u < u0 + nu; ++u) c->fresh[u] = 1;
     return HIKV_OK;

@@ -11,6 +11,7 @@
 //   free_stack  [pool_pages] ids of free pages, free_stack[0, *free_top).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -108,15 +109,49 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait: gives up after ~2^22 polls with back-off (well over a second
-// on a stalled barrier), records DEVERR_TIMEOUT and returns false.
+// try_wait with a suspend-time hint: the thread may sleep up to `ns` inside
+// the instruction until the phase completes, instead of spinning.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: gives up after 2^21 tries of at most ~1 us each (about two
+// seconds on a stalled barrier), records DEVERR_TIMEOUT and returns false.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t* err) {
-    for (uint32_t i = 0; i < (1u << 22); ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (i > 32) __nanosleep(256);
+    for (uint32_t i = 0; i < (1u << 21); ++i) {
+        if (mbar_try_wait_hint(bar, parity, 1000u)) return true;
     }
     atomicOr(err, DEVERR_TIMEOUT);
     return false;
+}
+
+// 2-D tiled TMA load of box {x, y} of `tmap` into shared memory.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tmap, int32_t x, int32_t y,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// packed fp32 pair FMA (two lanes of a float2 at once)
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(*reinterpret_cast<unsigned long long*>(&d))
+        : "l"(*reinterpret_cast<const unsigned long long*>(&a)),
+          "l"(*reinterpret_cast<const unsigned long long*>(&b)),
+          "l"(*reinterpret_cast<const unsigned long long*>(&c)));
+    return d;
 }
 
 // 1-D bulk copy global -> shared (TMA engine), completion counted on `bar`.
@@ -204,6 +239,18 @@ template <> struct Widen<__nv_bfloat16, 4> {   // 8 bytes
         f[3] = __uint_as_float(r.y & 0xFFFF0000u);
     }
 };
+template <> struct Widen<__nv_bfloat16, 8> {   // 16 bytes
+    __device__ __forceinline__ static void run(const uint4 r, float* f) {
+        f[0] = __uint_as_float(r.x << 16);
+        f[1] = __uint_as_float(r.x & 0xFFFF0000u);
+        f[2] = __uint_as_float(r.y << 16);
+        f[3] = __uint_as_float(r.y & 0xFFFF0000u);
+        f[4] = __uint_as_float(r.z << 16);
+        f[5] = __uint_as_float(r.z & 0xFFFF0000u);
+        f[6] = __uint_as_float(r.w << 16);
+        f[7] = __uint_as_float(r.w & 0xFFFF0000u);
+    }
+};
 template <> struct Widen<__nv_bfloat16, 2> {   // 4 bytes
     __device__ __forceinline__ static void run(const uint32_t r, float* f) {
         f[0] = __uint_as_float(r << 16);
@@ -257,8 +304,8 @@ struct DecodeArgs {
     int32_t cs;             // CTAs per unit (cluster size)
     int32_t chunk_cap;      // max tokens per CTA handled by the smem path
 };
-cudaError_t launch_decode(const DecodeArgs& a, int dtype, int d, int group, bool smem_path,
-                          size_t smem_bytes, cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmap, int dtype, int d, int group,
+                          bool smem_path, size_t smem_bytes, cudaStream_t s);
 size_t decode_smem_bytes(int dtype, int d, int group, bool smem_path, int chunk_cap);
 int decode_max_smem_chunk(int dtype, int d, int group, size_t smem_limit);
 

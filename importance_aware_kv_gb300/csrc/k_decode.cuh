@@ -1,32 +1,35 @@
 // Fused decode attention + importance update + victim argmin.
 //
-// One thread-block cluster per unit (layer, batch, KV head); its CS CTAs split
-// the unit's n live slots into equal chunks.  Per CTA:
-//   producer warp  streams the chunk in 16-row tiles, each tile's K rows and
-//                  V rows together, HBM -> shared memory with 1-D TMA bulk
-//                  copies into an NSTAGE ring (mbarrier full/empty pairs,
-//                  bounded waits);
-//   4 consumer warps, each owning every 4th row of a tile, keep a private
-//   online softmax (running max m_w, sum l_w, unnormalised O_w):
-//     logits s'_hj = <q_h * scale * log2 e, k_j> for the G query heads of the
-//     group -- a lane holds d/32 elements of a row, a warp reduce-scatter
-//     leaves one (row, head) sum per lane; logits are kept (shared memory, or
-//     an L2-resident global buffer for very long chunks) for the importance
-//     update; then p = 2^(s' - m_w), O_w += p v_j for the same tile's V rows.
-//   CTA merge of the 4 warp states, then a cluster merge by remote stores
-//   into shared memory (DSMEM) before one cluster barrier:
-//     m = max_c m_c, l = sum_c l_c 2^(m_c - m); out_h = sum_c O_c[h] 2^(m_c - m) / l;
-//     importance imp_j += sum_h 2^(s'_hj - m_h) / l_h (fp32 add, heads
-//     ascending), and the eligible slot with the smallest (imp, -pos) is the
-//     step's victim, gathered in CTA 0 by a second remote store + barrier.
-//
-// Method: decode attention P = softmax(q K^T), O = P V (HiKV sec. II-A; Kelle
-// summary sec. 2.2); importance accumulates P summed over the group's heads
+// Method: decode attention P = softmax(q K^T), O = P V over the retained
+// tokens (HiKV sec. II-A; Kelle summary sec. 2.2); every retained token's
+// importance accumulates P summed over the G query heads of its KV group
 // (blog sec. 3 "H2O", sec. 5.2); the victim is the least important token that
 // is neither a sink nor in the recent window, ties evicting the higher
-// position (blog sec. 3 "H2O"/"StreamingLLM").  The argmin stands in for the
-// min-search that Kelle's systolic evictor runs alongside attention (Kelle
-// summary sec. 5.3) and HiKV's min-heap (sec. III-B).
+// position (blog sec. 3 "H2O"/"StreamingLLM").  The fused argmin plays the
+// role of the min-search that Kelle's systolic evictor runs alongside
+// attention (Kelle summary sec. 5.3) and of HiKV's min-heap (sec. III-B).
+//
+// One thread-block cluster per unit (layer, batch, KV head); its CS CTAs split
+// the unit's n live slots into equal chunks.  Per CTA:
+//   producer warp   loads the page ids of the chunk, then streams it in
+//                   16-slot tiles: the tile's K rows and V rows arrive with
+//                   2-D TMA tensor copies (128-byte swizzle) into an NSTAGE
+//                   ring (mbarrier full/empty pairs, bounded waits).
+//   consumer warps  tile i belongs to warp i % 4, which keeps a private
+//                   online softmax (running max m_w, sum l_w, unnormalised
+//                   O_w) over its tiles:
+//     q.k   lane (row = lane % 16, half = lane / 16) owns half a K row: the
+//           swizzle makes those 16-byte reads conflict-free and lets q be a
+//           shared-memory broadcast; packed f32x2 FMAs, one shuffle joins the
+//           halves; logits (scaled by log2 e) are kept for the importance pass;
+//     p.v   lane owns d/32 output elements, packed f32x2 FMAs over the tile's
+//           V rows with p broadcast from shared memory.
+//   CTA merge of the warp states, then a cluster merge by remote stores into
+//   shared memory (DSMEM) before one cluster barrier:
+//     m = max_c m_c, l = sum_c l_c 2^(m_c - m); out_h = sum_c O_c[h] 2^(m_c - m) / l;
+//     importance imp_j += sum_h 2^(s'_hj - m_h) / l_h (fp32 add, heads
+//     ascending); the eligible slot with the smallest (imp, -pos) is the
+//     step's victim, gathered in CTA 0 by a second remote store + barrier.
 #pragma once
 
 #include "hikv_internal.cuh"
@@ -35,64 +38,34 @@ namespace hikv {
 
 constexpr int kDecNCW = 4;                       // consumer warps
 constexpr int kDecThreads = (kDecNCW + 1) * 32;  // + producer warp
-constexpr int kDecTR = 16;                       // rows per tile
-constexpr int kDecStages = 4;
-
-// reduce-scatter of N0 per-lane values over the warp.  Stage k exchanges half
-// of the remaining values with the lane 16 >> k away; afterwards lane l holds
-// the sum over 32 / N0 lanes of value index l / (32 / N0), and the butterfly
-// in warp_reduce_scatter_full completes it to the full warp sum.
-template <int N, int N0>
-__device__ __forceinline__ float warp_reduce_scatter(float (&v)[N], int lane) {
-    if constexpr (N == 1) {
-        return v[0];
-    } else {
-        constexpr int H = N / 2;
-        constexpr int off = 16 * N / N0;
-        const bool upper = (lane & off) != 0;
-        float nv[H];
-#pragma unroll
-        for (int i = 0; i < H; ++i) {
-            float send = upper ? v[i] : v[i + H];
-            float keep = upper ? v[i + H] : v[i];
-            nv[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-        }
-        return warp_reduce_scatter<H, N0>(nv, lane);
-    }
-}
-
-template <int N>
-__device__ __forceinline__ float warp_reduce_scatter_full(float (&v)[N], int lane) {
-    float r = warp_reduce_scatter<N, N>(v, lane);
-#pragma unroll
-    for (int o = 16 / N; o >= 1; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
-    return r;
-}
+constexpr int kDecTR = 16;                       // slots per tile
+constexpr int kDecStages = 4;                    // ring depth (tiles)
+constexpr int kDecMaxPg = 256;                   // page ids cached in shared memory
 
 struct DecSmem {
-    // byte offsets into dynamic shared memory
-    uint32_t ring, bars, ws, recv, small, S, simp, spos, total;
+    // byte offsets into dynamic shared memory, from a 1024-aligned base
+    uint32_t ring, bars, q, ps, recv, small, pg, S, simp, spos, total;
 };
 
 template <typename T, int D, int G>
-__host__ __device__ constexpr uint32_t dec_ring_bytes() {
-    return (uint32_t)kDecStages * 2 * kDecTR * D * sizeof(T);
-}
-
-template <typename T, int D, int G>
 __host__ __device__ inline DecSmem dec_layout(bool smem_s, int chunk_cap) {
+    constexpr uint32_t RB = D * sizeof(T);
     DecSmem L{};
     uint32_t off = 0;
-    L.ring = off;                                 // also the warp-partial O buffer after streaming
-    off += dec_ring_bytes<T, D, G>();
+    L.ring = off;                                 // K,V tiles; warp O partials after streaming
+    off += kDecStages * 2 * kDecTR * RB;
     L.bars = off;
     off += 2 * kDecStages * 8;
-    L.ws = off;                                   // [NCW][2][32] per-warp broadcast scratch
-    off += kDecNCW * 2 * 32 * 4;
+    L.q = off;                                    // q * scale * log2 e, fp32 [G][D]
+    off += G * D * 4;
+    L.ps = off;                                   // per-warp p of the tile, duplicated pairs [NCW][16][G][2]
+    off += kDecNCW * kDecTR * G * 8;
     L.recv = off;                                 // O slices from every CTA: G*D + kMaxCS floats
     off += (G * D + kMaxCS) * 4;
     L.small = off;
     off += 4096;
+    L.pg = off;                                   // page ids of the chunk
+    off += kDecMaxPg * 4;
     L.S = off;
     if (smem_s) {
         off += (uint32_t)chunk_cap * G * 4;
@@ -104,23 +77,34 @@ __host__ __device__ inline DecSmem dec_layout(bool smem_s, int chunk_cap) {
     } else {
         L.simp = L.spos = off;
     }
-    L.total = (off + 127) & ~127u;
+    L.total = ((off + 127) & ~127u) + 1024;       // + slack to align the base to 1024
     return L;
 }
 
+// byte offset of 16-byte chunk c of tile row r in a tile laid out as 128-byte
+// swizzled boxes [c / 8][r][(c % 8) ^ (r % 8)]
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+    return (uint32_t)((c >> 3) * (kDecTR * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
 template <typename T, int D, int G, bool SMEM_S>
-__global__ void __launch_bounds__(kDecThreads, (G <= 4 ? 4 : 2)) k_decode(const DecodeArgs a) {
-    constexpr int RB = D * (int)sizeof(T);   // row bytes
-    constexpr int TB = kDecTR * RB;          // tile bytes (K or V)
-    constexpr int EPL = D / 32;              // elements per lane
-    constexpr int LB = EPL * (int)sizeof(T); // bytes per lane
-    constexpr int RPW = kDecTR / kDecNCW;    // rows per warp per tile
-    constexpr int NV = RPW * G;              // logits per warp per tile
+__global__ void __launch_bounds__(kDecThreads, (G <= 4 ? 4 : 2))
+    k_decode(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap) {
+    constexpr int ESZ = (int)sizeof(T);
+    constexpr int RB = D * ESZ;              // row bytes: 128, 256 or 512
+    constexpr int NBOX = RB / 128;           // 128-byte TMA boxes per row
+    constexpr int TB = kDecTR * RB;          // K (or V) tile bytes
+    constexpr int CPR = RB / 16;             // 16-byte chunks per row
+    constexpr int CPL = CPR / 2;             // q.k: chunks per lane (half a row)
+    constexpr int EPC = 16 / ESZ;            // elements per chunk
+    constexpr int EPL = D / 32;              // p.v: elements per lane
+    constexpr int LB = EPL * ESZ;            // p.v: bytes per lane
     constexpr int NCT = kDecNCW * 32;        // consumer threads
-    static_assert(NV <= 32 && (NV & (NV - 1)) == 0, "group size");
+    static_assert(EPL % 2 == 0 && EPC % 2 == 0, "pairs");
     using Raw = typename RawVec<LB>::type;
 
-    extern __shared__ __align__(128) uint8_t smem[];
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const View& v = a.v;
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -129,7 +113,8 @@ __global__ void __launch_bounds__(kDecThreads, (G <= 4 ? 4 : 2)) k_decode(const 
     uint8_t* ring = smem + L.ring;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
     uint64_t* empty = full + kDecStages;
-    float* ws = reinterpret_cast<float*>(smem + L.ws);        // [NCW][2][32]
+    float* q_s = reinterpret_cast<float*>(smem + L.q);
+    float2* ps_all = reinterpret_cast<float2*>(smem + L.ps);
     float* orecv = reinterpret_cast<float*>(smem + L.recv);   // [CS][per]
     float* sm = reinterpret_cast<float*>(smem + L.small);
     float* m_recv = sm;                        // [kMaxCS][G]  (128)
@@ -147,6 +132,7 @@ __global__ void __launch_bounds__(kDecThreads, (G <= 4 ? 4 : 2)) k_decode(const 
     unsigned long long* wkey = reinterpret_cast<unsigned long long*>(aslot + kMaxCS);  // [NCW]
     int32_t* wslot = reinterpret_cast<int32_t*>(wkey + kDecNCW);                     // [NCW]
     volatile int32_t* abort_flag = wslot + kDecNCW;
+    int32_t* pg_s = reinterpret_cast<int32_t*>(smem + L.pg);
     float* S_smem = reinterpret_cast<float*>(smem + L.S);
     float* simp = reinterpret_cast<float*>(smem + L.simp);
     int32_t* spos = reinterpret_cast<int32_t*>(smem + L.spos);
@@ -173,6 +159,8 @@ __global__ void __launch_bounds__(kDecThreads, (G <= 4 ? 4 : 2)) k_decode(const 
     }
     const int32_t first_blk = t0 / kDecTR;
     const int32_t nt = cnt > 0 ? (t1 - 1) / kDecTR - first_blk + 1 : 0;
+    const int32_t pg0 = t0 >> v.page_shift;                     // first page of the chunk
+    const int32_t npg = cnt > 0 ? ((t1 - 1) >> v.page_shift) - pg0 + 1 : 0;
     const int64_t qbase = (((int64_t)li * v.batch + b) * v.hq + (int64_t)g * G) * D;
     const int32_t per = ceil_div(G * D, CS);   // output elements finalised per CTA
 
@@ -182,7 +170,7 @@ __global__ void __launch_bounds__(kDecThreads, (G <= 4 ? 4 : 2)) k_decode(const 
     if (tid == 0) {
         for (int s = 0; s < kDecStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kDecNCW);
+            mbar_init(&empty[s], 1);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -191,6 +179,9 @@ __global__ void __launch_bounds__(kDecThreads, (G <= 4 ? 4 : 2)) k_decode(const 
 
     if (warp == kDecNCW) {
         // ---------------- producer ----------------
+        const int32_t* ptab = v.page_table + (int64_t)u * v.max_pages;
+        for (int k = lane; k < min(npg, kDecMaxPg); k += 32) pg_s[k] = ptab[pg0 + k];
+        __syncwarp();
         if (lane == 0) {
             int it = 0;
             for (; it < nt; ++it) {
@@ -201,20 +192,24 @@ __global__ void __launch_bounds__(kDecThreads, (G <= 4 ? 4 : 2)) k_decode(const 
                     *abort_flag = 1;
                     break;
                 }
-                const int32_t s0 = max(t0, (first_blk + it) * kDecTR);
-                const int32_t s1 = min(t1, (first_blk + it + 1) * kDecTR);
-                const uint8_t* ksrc = row_ptr(v, u, s0, false);
-                const uint8_t* vsrc = row_ptr(v, u, s0, true);
-                const uint32_t bytes = (uint32_t)(s1 - s0) * RB;
-                if (ksrc == nullptr || vsrc == nullptr) {
-                    // unmapped page: complete the stage without data
+                const int32_t s0 = (first_blk + it) * kDecTR;       // 16-aligned: never crosses a page
+                const int32_t pk = (s0 >> v.page_shift) - pg0;
+                const int32_t pg = pk < kDecMaxPg ? pg_s[pk] : ptab[pg0 + pk];
+                if (pg < 0 || pg >= v.pool_pages) {
+                    atomicOr(v.err, DEVERR_PAGE);
                     *abort_flag = 1;
-                    mbar_arrive(&full[st]);
+                    mbar_arrive(&full[st]);   // complete the stage without data
                     break;
                 }
-                mbar_arrive_expect_tx(&full[st], 2 * bytes);
-                bulk_g2s(ring + st * 2 * TB, ksrc, bytes, &full[st]);
-                bulk_g2s(ring + st * 2 * TB + TB, vsrc, bytes, &full[st]);
+                const int32_t yk = pg * 2 * v.page_tokens + (s0 & (v.page_tokens - 1));
+                uint8_t* dst = ring + st * 2 * TB;
+                mbar_arrive_expect_tx(&full[st], 2 * TB);
+#pragma unroll
+                for (int bx = 0; bx < NBOX; ++bx) {
+                    tma_load_2d(dst + bx * (kDecTR * 128), &tmap, bx * (128 / ESZ), yk, &full[st]);
+                    tma_load_2d(dst + TB + bx * (kDecTR * 128), &tmap, bx * (128 / ESZ), yk + v.page_tokens,
+                                &full[st]);
+                }
             }
             if (*abort_flag) {
                 // let copies already in flight land before the CTA can exit
@@ -230,129 +225,127 @@ __global__ void __launch_bounds__(kDecThreads, (G <= 4 ? 4 : 2)) k_decode(const 
 
     // ---------------- consumers ----------------
     const int ctid = tid;  // 0..127
-    float qr[G][EPL];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-        const Raw raw = *reinterpret_cast<const Raw*>(reinterpret_cast<const T*>(a.q) + qbase +
-                                                      (int64_t)h * D + lane * EPL);
-        Widen<T, EPL>::run(raw, qr[h]);
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) qr[h][e] *= a.qscale;
-    }
+    for (int i = ctid; i < G * D; i += NCT)
+        q_s[i] = Elem<T>::to_f(reinterpret_cast<const T*>(a.q)[qbase + i]) * a.qscale;
     if (SMEM_S) {
         for (int j = ctid; j < cnt; j += NCT) {
             simp[j] = v.imp[(int64_t)u * v.cap + t0 + j];
             spos[j] = v.pos[(int64_t)u * v.cap + t0 + j];
         }
     }
+    named_bar_sync(1, NCT);
 
-    float* ws_s = ws + warp * 64;        // this warp's logits of the tile, [k*G + h]
-    float* ws_p = ws_s + 32;             // this warp's probabilities of the tile
-    float m_w[G], l_w[G], o[G][EPL];
+    float2* ps = ps_all + warp * (kDecTR * G);     // [16][G] duplicated p pairs
+    float m_w[G], l_w[G];
+    float2 o2[G][EPL / 2];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
         m_w[h] = -INFINITY;
         l_w[h] = 0.f;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) o[h][e] = 0.f;
+        for (int e = 0; e < EPL / 2; ++e) o2[h][e] = make_float2(0.f, 0.f);
     }
-    constexpr int stride = 32 / NV;
-    const int vi = lane / stride;             // (row, head) value this lane ends up with
-    const int vk = vi / G, vh = vi % G;
-    const bool writer = (lane & (stride - 1)) == 0;
+    const int qr = lane & 15;           // q.k: tile row of this lane
+    const int qh = lane >> 4;           // q.k: half of the row
+    const int pv_chunk = (lane * LB) >> 4, pv_in = (lane * LB) & 15;
 
-    for (int i = 0; i < nt; ++i) {
+    for (int i = warp; i < nt; i += kDecNCW) {
         if (*abort_flag) break;
         const int st = i % kDecStages;
         if (!mbar_wait_bounded(&full[st], (uint32_t)(i / kDecStages) & 1u, v.err)) {
             *abort_flag = 1;
             break;
         }
-        const int32_t s0 = max(t0, (first_blk + i) * kDecTR);
-        const int32_t rows = min(t1, (first_blk + i + 1) * kDecTR) - s0;
+        const int32_t s0 = (first_blk + i) * kDecTR;
         const uint8_t* ktile = ring + st * 2 * TB;
         const uint8_t* vtile = ktile + TB;
-        // logits of this warp's rows
-        float acc[NV];
+        const int32_t lo_r = max(0, t0 - s0), hi_r = min(kDecTR, t1 - s0);   // valid rows [lo_r, hi_r)
+
+        // ---- q.k: this lane's half row ----
+        float2 acc[G];
 #pragma unroll
-        for (int k = 0; k < RPW; ++k) {
-            const int r = warp + kDecNCW * k;
-            float x[EPL];
-            if (r < rows) {
-                Raw raw = *reinterpret_cast<const Raw*>(ktile + r * RB + lane * LB);
-                Widen<T, EPL>::run(raw, x);
-            } else {
+        for (int h = 0; h < G; ++h) acc[h] = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) x[e] = 0.f;
-            }
+        for (int j = 0; j < CPL; ++j) {
+            const int cidx = qh * CPL + j;
+            const uint4 raw = *reinterpret_cast<const uint4*>(ktile + swz(qr, cidx));
+            float x[EPC];
+            Widen<T, EPC>::run(raw, x);
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                float sacc = 0.f;
+                const float* qp = q_s + h * D + cidx * EPC;
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) sacc = fmaf(x[e], qr[h][e], sacc);
-                acc[k * G + h] = sacc;
+                for (int e = 0; e < EPC; e += 4) {
+                    const float4 q4 = *reinterpret_cast<const float4*>(qp + e);
+                    acc[h] = ffma2(make_float2(x[e], x[e + 1]), make_float2(q4.x, q4.y), acc[h]);
+                    acc[h] = ffma2(make_float2(x[e + 2], x[e + 3]), make_float2(q4.z, q4.w), acc[h]);
+                }
             }
         }
-        const float val = warp_reduce_scatter_full<NV>(acc, lane);
-        const int vr = warp + kDecNCW * vk;       // tile row of this lane's value
-        if (writer) {
-            ws_s[vi] = (vr < rows) ? val : -INFINITY;
-            if (vr < rows) Sb[(int64_t)(s0 + vr - s_off) * G + vh] = val;
+        const bool rv = qr >= lo_r && qr < hi_r;
+        float s[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            float t = acc[h].x + acc[h].y;
+            t += __shfl_xor_sync(0xffffffffu, t, 16);
+            s[h] = rv ? t : -INFINITY;
         }
-        __syncwarp();
-        // tile max per head over this warp's valid rows; new running max
-        float m_new[G], scl[G];
+        // ---- online softmax over this tile ----
+        float scl[G], p[G];
         bool rescale = false;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-            float tm = -INFINITY;
+            float mt = s[h];
 #pragma unroll
-            for (int k = 0; k < RPW; ++k) tm = fmaxf(tm, ws_s[k * G + h]);
-            m_new[h] = fmaxf(m_w[h], tm);
-            scl[h] = (m_new[h] == m_w[h]) ? 1.f : exp2f(m_w[h] - m_new[h]);   // m_w = -inf -> 0
-            rescale |= (m_new[h] != m_w[h]);
+            for (int o = 8; o >= 1; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+            const float mn = fmaxf(m_w[h], mt);
+            scl[h] = (mn == m_w[h]) ? 1.f : exp2f(m_w[h] - mn);
+            rescale |= (mn != m_w[h]);
+            m_w[h] = mn;
+            p[h] = rv ? exp2f(s[h] - mn) : 0.f;
+            float ls = p[h];
+#pragma unroll
+            for (int o = 8; o >= 1; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+            l_w[h] = l_w[h] * scl[h] + ls;
         }
-        if (writer) {
-            float mh = m_new[0];
+        if (qh == 0) {
 #pragma unroll
-            for (int h = 1; h < G; ++h)
-                if (vh == h) mh = m_new[h];
-            ws_p[vi] = (vr < rows) ? exp2f(val - mh) : 0.f;
-        }
-        __syncwarp();
-        if (rescale) {
+            for (int h = 0; h < G; ++h) ps[qr * G + h] = make_float2(p[h], p[h]);
+            if (rv) {
+                float* srow = Sb + (int64_t)(s0 + qr - s_off) * G;
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                l_w[h] *= scl[h];
-#pragma unroll
-                for (int e = 0; e < EPL; ++e) o[h][e] *= scl[h];
+                for (int h = 0; h < G; ++h) srow[h] = s[h];
             }
         }
+        if (rescale) {
 #pragma unroll
-        for (int h = 0; h < G; ++h) m_w[h] = m_new[h];
+            for (int h = 0; h < G; ++h)
 #pragma unroll
-        for (int k = 0; k < RPW; ++k) {
-            const int r = warp + kDecNCW * k;
-            if (r < rows) {
-                float p[G];
-#pragma unroll
-                for (int h = 0; h < G; ++h) p[h] = ws_p[k * G + h];
-                Raw raw = *reinterpret_cast<const Raw*>(vtile + r * RB + lane * LB);
-                float x[EPL];
-                Widen<T, EPL>::run(raw, x);
-#pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    l_w[h] += p[h];
-#pragma unroll
-                    for (int e = 0; e < EPL; ++e) o[h][e] = fmaf(p[h], x[e], o[h][e]);
+                for (int e = 0; e < EPL / 2; ++e) {
+                    o2[h][e].x *= scl[h];
+                    o2[h][e].y *= scl[h];
                 }
+        }
+        __syncwarp();
+        // ---- p.v over the tile's valid rows ----
+        for (int r = lo_r; r < hi_r; ++r) {
+            const Raw raw = *reinterpret_cast<const Raw*>(vtile + swz(r, pv_chunk) + pv_in);
+            float x[EPL];
+            Widen<T, EPL>::run(raw, x);
+            const float2* pr = ps + r * G;
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float2 pp = pr[h];
+#pragma unroll
+                for (int e = 0; e < EPL / 2; ++e)
+                    o2[h][e] = ffma2(make_float2(x[2 * e], x[2 * e + 1]), pp, o2[h][e]);
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
     }
 
-    // ---- CTA merge of the 4 warp states (ring reused for the O partials) ----
+    // ---- CTA merge of the warp states (ring reused for the O partials) ----
     if (lane == 0) {
 #pragma unroll
         for (int h = 0; h < G; ++h) {
@@ -365,7 +358,8 @@ __global__ void __launch_bounds__(kDecThreads, (G <= 4 ? 4 : 2)) k_decode(const 
 #pragma unroll
     for (int h = 0; h < G; ++h)
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) red[(warp * G + h) * D + lane * EPL + e] = o[h][e];
+        for (int e = 0; e < EPL / 2; ++e)
+            *reinterpret_cast<float2*>(&red[(warp * G + h) * D + lane * EPL + 2 * e]) = o2[h][e];
     if (ctid < G) {
         float m = -INFINITY;
         for (int w = 0; w < kDecNCW; ++w) m = fmaxf(m, mw_s[w * G + ctid]);
@@ -388,11 +382,11 @@ __global__ void __launch_bounds__(kDecThreads, (G <= 4 ? 4 : 2)) k_decode(const 
     }
     for (int idx = ctid; idx < G * D; idx += NCT) {
         const int h = idx / D;
-        float s = 0.f;
+        float sum = 0.f;
 #pragma unroll
-        for (int w = 0; w < kDecNCW; ++w) s += red[w * G * D + idx] * wsc[w * G + h];
+        for (int w = 0; w < kDecNCW; ++w) sum += red[w * G * D + idx] * wsc[w * G + h];
         const int owner = idx / per, loc = idx - owner * per;
-        dsmem_st_f32(dsmem_addr(&orecv[c * per + loc], (uint32_t)owner), s);
+        dsmem_st_f32(dsmem_addr(&orecv[c * per + loc], (uint32_t)owner), sum);
     }
 
     __syncwarp();
@@ -421,9 +415,9 @@ __global__ void __launch_bounds__(kDecThreads, (G <= 4 ? 4 : 2)) k_decode(const 
             const int idx = c * per + loc;
             if (idx >= G * D) break;
             const int h = idx / D;
-            float s = 0.f;
-            for (int cc = 0; cc < CS; ++cc) s += orecv[cc * per + loc] * beta[cc * G + h];
-            outp[idx] = Elem<T>::from_f(s);
+            float sum = 0.f;
+            for (int cc = 0; cc < CS; ++cc) sum += orecv[cc * per + loc] * beta[cc * G + h];
+            outp[idx] = Elem<T>::from_f(sum);
         }
     }
     // importance update + local victim
@@ -448,10 +442,10 @@ __global__ void __launch_bounds__(kDecThreads, (G <= 4 ? 4 : 2)) k_decode(const 
             const float nw = old + inc;
             v.imp[mi] = nw;
             if (need_victim) {
-                const int32_t p = SMEM_S ? spos[j] : v.pos[mi];
-                if (p >= lo && p <= hi) {
+                const int32_t ps_ = SMEM_S ? spos[j] : v.pos[mi];
+                if (ps_ >= lo && ps_ <= hi) {
                     const unsigned long long key =
-                        ((unsigned long long)__float_as_uint(nw) << 32) | (unsigned long long)(~(uint32_t)p);
+                        ((unsigned long long)__float_as_uint(nw) << 32) | (unsigned long long)(~(uint32_t)ps_);
                     if (key < kmin) {
                         kmin = key;
                         smin = slot;
@@ -461,9 +455,9 @@ __global__ void __launch_bounds__(kDecThreads, (G <= 4 ? 4 : 2)) k_decode(const 
         }
         if (need_victim) {
 #pragma unroll
-            for (int o2 = 16; o2 >= 1; o2 >>= 1) {
-                const unsigned long long ok = __shfl_xor_sync(0xffffffffu, kmin, o2);
-                const int32_t os = __shfl_xor_sync(0xffffffffu, smin, o2);
+            for (int o2i = 16; o2i >= 1; o2i >>= 1) {
+                const unsigned long long ok = __shfl_xor_sync(0xffffffffu, kmin, o2i);
+                const int32_t os = __shfl_xor_sync(0xffffffffu, smin, o2i);
                 if (ok < kmin) {
                     kmin = ok;
                     smin = os;
@@ -478,14 +472,14 @@ __global__ void __launch_bounds__(kDecThreads, (G <= 4 ? 4 : 2)) k_decode(const 
     named_bar_sync(1, NCT);
     if (ctid == 0 && need_victim) {
         unsigned long long k = ~0ull;
-        int32_t s = -1;
+        int32_t sl = -1;
         for (int w = 0; w < kDecNCW; ++w)
             if (wkey[w] < k) {
                 k = wkey[w];
-                s = wslot[w];
+                sl = wslot[w];
             }
         dsmem_st_u64(dsmem_addr(&akey[c], 0u), k);
-        dsmem_st_s32(dsmem_addr(&aslot[c], 0u), s);
+        dsmem_st_s32(dsmem_addr(&aslot[c], 0u), sl);
     }
 
     __syncwarp();
@@ -505,12 +499,8 @@ __global__ void __launch_bounds__(kDecThreads, (G <= 4 ? 4 : 2)) k_decode(const 
     }
 }
 
-}  // namespace hikv
-
-namespace hikv {
-
 template <typename T, int D, int G, bool SM>
-cudaError_t decode_launch_one(const DecodeArgs& a, size_t smem, cudaStream_t s) {
+cudaError_t decode_launch_one(const DecodeArgs& a, const CUtensorMap& tmap, size_t smem, cudaStream_t s) {
     auto kern = k_decode<T, D, G, SM>;
     static size_t smem_set = 0;  // largest dynamic smem opted into so far
     if (smem > smem_set) {
@@ -532,16 +522,17 @@ cudaError_t decode_launch_one(const DecodeArgs& a, size_t smem, cudaStream_t s) 
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a);
+    return cudaLaunchKernelEx(&cfg, kern, a, tmap);
 }
 
 template <typename T, int D, bool SM>
-cudaError_t decode_launch_g(const DecodeArgs& a, int group, size_t smem, cudaStream_t s) {
+cudaError_t decode_launch_g(const DecodeArgs& a, const CUtensorMap& tmap, int group, size_t smem,
+                            cudaStream_t s) {
     switch (group) {
-        case 1: return decode_launch_one<T, D, 1, SM>(a, smem, s);
-        case 2: return decode_launch_one<T, D, 2, SM>(a, smem, s);
-        case 4: return decode_launch_one<T, D, 4, SM>(a, smem, s);
-        case 8: return decode_launch_one<T, D, 8, SM>(a, smem, s);
+        case 1: return decode_launch_one<T, D, 1, SM>(a, tmap, smem, s);
+        case 2: return decode_launch_one<T, D, 2, SM>(a, tmap, smem, s);
+        case 4: return decode_launch_one<T, D, 4, SM>(a, tmap, smem, s);
+        case 8: return decode_launch_one<T, D, 8, SM>(a, tmap, smem, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -561,10 +552,10 @@ size_t decode_smem_t(int group, bool smem_path, int chunk_cap) {
 
 #define HIKV_DECODE_INSTANTIATE(T, D, NAME)                                                         \
     namespace hikv {                                                                                \
-    cudaError_t decode_launch_##NAME(const DecodeArgs& a, int group, bool smem_path, size_t smem,   \
-                                     cudaStream_t s) {                                              \
-        return smem_path ? decode_launch_g<T, D, true>(a, group, smem, s)                           \
-                         : decode_launch_g<T, D, false>(a, group, smem, s);                         \
+    cudaError_t decode_launch_##NAME(const DecodeArgs& a, const CUtensorMap& tmap, int group,       \
+                                     bool smem_path, size_t smem, cudaStream_t s) {                 \
+        return smem_path ? decode_launch_g<T, D, true>(a, tmap, group, smem, s)                     \
+                         : decode_launch_g<T, D, false>(a, tmap, group, smem, s);                   \
     }                                                                                               \
     size_t decode_smem_##NAME(int group, bool smem_path, int chunk_cap) {                           \
         return decode_smem_t<T, D>(group, smem_path, chunk_cap);                                    \

@@ -4,7 +4,7 @@
 namespace hikv {
 
 #define HIKV_DECL(NAME)                                                                            \
-    cudaError_t decode_launch_##NAME(const DecodeArgs&, int, bool, size_t, cudaStream_t);          \
+    cudaError_t decode_launch_##NAME(const DecodeArgs&, const CUtensorMap&, int, bool, size_t, cudaStream_t); \
     size_t decode_smem_##NAME(int, bool, int);
 HIKV_DECL(f32_64)
 HIKV_DECL(f32_128)
@@ -12,12 +12,12 @@ HIKV_DECL(bf16_64)
 HIKV_DECL(bf16_128)
 #undef HIKV_DECL
 
-cudaError_t launch_decode(const DecodeArgs& a, int dtype, int d, int group, bool smem_path,
-                          size_t smem_bytes, cudaStream_t s) {
-    if (dtype == 0 && d == 64) return decode_launch_f32_64(a, group, smem_path, smem_bytes, s);
-    if (dtype == 0 && d == 128) return decode_launch_f32_128(a, group, smem_path, smem_bytes, s);
-    if (dtype == 1 && d == 64) return decode_launch_bf16_64(a, group, smem_path, smem_bytes, s);
-    if (dtype == 1 && d == 128) return decode_launch_bf16_128(a, group, smem_path, smem_bytes, s);
+cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmap, int dtype, int d, int group,
+                          bool smem_path, size_t smem_bytes, cudaStream_t s) {
+    if (dtype == 0 && d == 64) return decode_launch_f32_64(a, tmap, group, smem_path, smem_bytes, s);
+    if (dtype == 0 && d == 128) return decode_launch_f32_128(a, tmap, group, smem_path, smem_bytes, s);
+    if (dtype == 1 && d == 64) return decode_launch_bf16_64(a, tmap, group, smem_path, smem_bytes, s);
+    if (dtype == 1 && d == 128) return decode_launch_bf16_128(a, tmap, group, smem_path, smem_bytes, s);
     return cudaErrorInvalidValue;
 }
 
