@@ -28,7 +28,7 @@ HIKV_F32, HIKV_BF16 = 0, 1
 # every entry point of include/hikv.h
 ABI_FUNCTIONS = ("hikv_create_cache", "hikv_destroy_cache", "hikv_append", "hikv_score_window",
                  "hikv_decode_step", "hikv_evict", "hikv_gather_retained", "hikv_get_lengths",
-                 "hikv_device_status", "hikv_last_error")
+                 "hikv_device_status", "hikv_last_error", "hikv_score_window_noalloc")
 
 
 class HikvError(RuntimeError):
@@ -64,6 +64,7 @@ def _load():
         "hikv_get_lengths": ([P, I32, I32, P], S),
         "hikv_device_status": ([P], S),
         "hikv_last_error": ([], ctypes.c_char_p),
+        "hikv_score_window_noalloc": ([I32] * 8 + [ctypes.c_float, P, P, P, P], S),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -172,6 +173,22 @@ def hikv_get_lengths(h, layer0: int, nlayers: int, units_per_layer: int) -> np.n
 
 def hikv_device_status(h) -> None:
     _check(_lib.hikv_device_status(h))
+
+
+def hikv_score_window_noalloc(k, q, importance, num_q_heads: int, scale: float = 0.0,
+                              stream=None) -> None:
+    """Stateless prompt importance on caller-owned buffers (no allocation).
+
+    k: [nl][B][Hkv][ntok][d], q: [nl][B][Hq][nq][d], importance: [nl][B][Hkv][ntok] fp32.
+    """
+    import torch
+    nl, b, hkv, ntok, d = k.shape
+    nq = q.shape[3]
+    dt = HIKV_BF16 if k.dtype == torch.bfloat16 else HIKV_F32
+    _check(_lib.hikv_score_window_noalloc(
+        nl, b, num_q_heads, hkv, d, dt, ntok, nq, scale, _dev(k, "k"),
+        _dev(q, "q", k.dtype, (nl, b, num_q_heads, nq, d)),
+        _dev(importance, "importance", torch.float32, (nl, b, hkv, ntok)), _stream(stream)))
 
 
 def hikv_last_error() -> str:

@@ -28,6 +28,15 @@ namespace {
 
 thread_local std::string g_err;
 
+}  // namespace
+
+namespace hikv {
+// lets other translation units of the library report through hikv_last_error()
+void set_last_error(const char* msg) { g_err = msg; }
+}  // namespace hikv
+
+namespace {
+
 hikv_status fail(hikv_status s, const char* fmt, ...) {
     char buf[512];
     va_list ap;

@@ -148,6 +148,37 @@ hikv_status hikv_get_lengths(const hikv_cache* cache, int32_t layer0, int32_t nl
  * error, else OK. */
 hikv_status hikv_device_status(hikv_cache* cache);
 
+/* Prompt importance for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart of this entry point; it exists for callers
+ * that may not call cudaMalloc: a plugin inside an inference engine that owns
+ * every device allocation and forbids allocating while it runs, or a
+ * real-time path where an allocation, and the synchronisation it can cause,
+ * is not allowed.  Such a caller cannot create a cache (hikv_create_cache
+ * allocates), so this call is stateless: it computes, for a prompt of ntok
+ * tokens (positions 0..ntok-1) per unit, what hikv_append + hikv_score_window
+ * would leave as importance in a fresh cache, from buffers the caller owns.
+ *
+ * k: [nlayers][batch][Hkv][ntok][d], q: [nlayers][batch][Hq][nq][d] (queries
+ * of positions ntok-nq..ntok-1), both in `dtype`; importance:
+ * [nlayers][batch][Hkv][ntok] fp32, overwritten.  Device pointers, 16-byte
+ * aligned.  scale 0 => 1/sqrt(head_dim).
+ *
+ * It allocates nothing.  Its scratch is a file-scope static device array of
+ * 2^20 floats (4 MiB) that every GPU loading the library holds until the
+ * process exits; calls needing more -- nlayers*batch*Hkv * ceil(ntok/1024) *
+ * G*nq * 2 floats -- are rejected with HIKV_ERR_INVALID_ARG and a message.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Every call shares the one array: calls that overlap on the GPU (other
+ * streams, other threads) race and must be serialised by the caller.
+ * Errors: INVALID_ARG, UNSUPPORTED (head_dim, dtype or too many query
+ * vectors for shared memory), CUDA (launch). */
+hikv_status hikv_score_window_noalloc(int32_t nlayers, int32_t batch, int32_t num_q_heads,
+                                      int32_t num_kv_heads, int32_t head_dim, int32_t dtype,
+                                      int32_t ntok, int32_t nq, float scale, const void* k,
+                                      const void* q, float* importance, hikv_stream_t stream);
+
 /* Message for the last failing call on this thread ("" if none). */
 const char* hikv_last_error(void);
 
