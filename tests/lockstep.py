@@ -50,7 +50,7 @@ def _out_np(t: torch.Tensor) -> np.ndarray:
 class Lockstep:
     def __init__(self, w: W.Workload, seed=None, sample_layers=None, cs=None, budgets=None,
                  device="cuda", layer_chunk=None, full_cache=False, page_tokens=64,
-                 check_kv=True):
+                 check_kv=True, full_twin_layers=None):
         import importance_aware_kv_gb300 as hk
         self.hk = hk
         self.w = w
@@ -78,6 +78,21 @@ class Lockstep:
                                  out_bf16=(w.dtype == "bf16"), threads=os.cpu_count() or 1)
         self.rep = Report()
         self.upl = w.batch * w.hkv
+        # optional twin: a no-eviction cache fed the same inputs, checked on
+        # `full_twin_layers` against an oracle whose budget exceeds the context
+        self.twin = None
+        if full_twin_layers is not None:
+            self.twin = Lockstep.__new__(Lockstep)
+            self.twin.__dict__.update(dict(hk=hk, w=w, seed=self.seed, dev=self.dev,
+                                           budgets=np.full_like(self.budgets, w.total_positions),
+                                           sample=list(full_twin_layers), layer_chunk=self.layer_chunk,
+                                           check_kv=False, rep=Report(), upl=self.upl, twin=None))
+            self.twin.cache = hk.Cache(hk.CacheConfig(
+                w.layers, w.batch, w.hq, w.hkv, w.d, w.dtype, w.sink, w.window, self.twin.budgets,
+                w.total_positions, page_tokens=page_tokens, max_window_queries=max(32, w.nq)))
+            self.twin.ora = oracle.Oracle(len(self.twin.sample), w.batch, w.hq, w.hkv, w.d, w.sink,
+                                          w.window, np.full(len(self.twin.sample) * w.hkv, w.total_positions),
+                                          out_bf16=(w.dtype == "bf16"), threads=os.cpu_count() or 1)
 
     # ------------------------------------------------------------------
     def prefill(self):
@@ -85,21 +100,28 @@ class Lockstep:
         for l0 in range(0, w.layers, self.layer_chunk):
             nl = min(self.layer_chunk, w.layers - l0)
             k, v = W.gen_kv(w, l0, nl, 0, w.prompt, self.seed)
-            self.cache.append(_to_dev(k, self.dev), _to_dev(v, self.dev), layer0=l0)
-            for si, l in enumerate(self.sample):
-                if l0 <= l < l0 + nl:
-                    self.ora.append(si, W.to_f32(k[l - l0:l - l0 + 1]), W.to_f32(v[l - l0:l - l0 + 1]))
-            del k, v
+            dk, dv = _to_dev(k, self.dev), _to_dev(v, self.dev)
+            for ls in self._all():
+                ls.cache.append(dk, dv, layer0=l0)
+                for si, l in enumerate(ls.sample):
+                    if l0 <= l < l0 + nl:
+                        ls.ora.append(si, W.to_f32(k[l - l0:l - l0 + 1]), W.to_f32(v[l - l0:l - l0 + 1]))
+            del k, v, dk, dv
         torch.cuda.synchronize()
         q = W.gen_q(w, 0, w.layers, w.prompt - w.nq, w.nq, self.seed)
-        self.cache.score_window(_to_dev(q, self.dev))
-        for si, l in enumerate(self.sample):
-            self.ora.score_window(si, W.to_f32(q[l:l + 1]))
-        self.compare_state(after_evict=False)
-        self.cache.evict()
-        for si in range(len(self.sample)):
-            self.ora.evict(si, 1)
-        self.compare_state(after_evict=True, kv=True)
+        dq = _to_dev(q, self.dev)
+        for ls in self._all():
+            ls.cache.score_window(dq)
+            for si, l in enumerate(ls.sample):
+                ls.ora.score_window(si, W.to_f32(q[l:l + 1]))
+            ls.compare_state(after_evict=False)
+            ls.cache.evict()
+            for si in range(len(ls.sample)):
+                ls.ora.evict(si, 1)
+            ls.compare_state(after_evict=True, kv=True)
+
+    def _all(self):
+        return [self] + ([self.twin] if self.twin is not None else [])
 
     def _decode_inputs(self):
         w = self.w
@@ -118,25 +140,27 @@ class Lockstep:
         dks, dvs, dqs = _to_dev(ks, self.dev), _to_dev(vs, self.dev), _to_dev(qs, self.dev)
         out = torch.empty_like(dqs[0])
         for s in range(steps):
-            self.cache.append(dks[s], dvs[s])
-            self.cache.decode_step(dqs[s], out)
             evict_now = (s + 1) % w.evict_every == 0
-            if evict_now:
-                self.cache.evict()
-            for si, l in enumerate(self.sample):
-                self.ora.append(si, W.to_f32(ks[s, l:l + 1]), W.to_f32(vs[s, l:l + 1]))
-            ora_out = [self.ora.decode(si, W.to_f32(qs[s, l:l + 1])) for si, l in enumerate(self.sample)]
-            if evict_now:
-                for si in range(len(self.sample)):
-                    self.ora.evict(si, 1)
-            if (s % compare_every == 0) or s == steps - 1:
-                got = _out_np(out)
-                for si, l in enumerate(self.sample):
-                    self.compare_out(got[l], ora_out[si][0], s)
-            if evict_now:
-                self.compare_state(after_evict=True)
-        self.compare_state(after_evict=False, kv=True)
-        self.cache.device_status()
+            for ls in self._all():
+                ls.cache.append(dks[s], dvs[s])
+                ls.cache.decode_step(dqs[s], out)
+                if evict_now:
+                    ls.cache.evict()
+                for si, l in enumerate(ls.sample):
+                    ls.ora.append(si, W.to_f32(ks[s, l:l + 1]), W.to_f32(vs[s, l:l + 1]))
+                ora_out = [ls.ora.decode(si, W.to_f32(qs[s, l:l + 1])) for si, l in enumerate(ls.sample)]
+                if evict_now:
+                    for si in range(len(ls.sample)):
+                        ls.ora.evict(si, 1)
+                if (s % compare_every == 0) or s == steps - 1:
+                    got = _out_np(out)
+                    for si, l in enumerate(ls.sample):
+                        ls.compare_out(got[l], ora_out[si][0], s)
+                if evict_now:
+                    ls.compare_state(after_evict=True)
+        for ls in self._all():
+            ls.compare_state(after_evict=False, kv=True)
+            ls.cache.device_status()
         return self.rep
 
     # ------------------------------------------------------------------
