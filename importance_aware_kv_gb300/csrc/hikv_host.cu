@@ -410,9 +410,13 @@ hikv_status hikv_decode_step(hikv_cache* c, int32_t layer0, int32_t nl, const vo
     if (q == out) return fail(HIKV_ERR_INVALID_ARG, "decode_step: out aliases q");
     const int u0 = layer0 * c->per_layer, nu = nl * c->per_layer;
     int maxn = 0;
+    bool uni_len = true, uni_b = true, uni_np = true;
     for (int u = u0; u < u0 + nu; ++u) {
         if (c->len[u] < 1) return fail(HIKV_ERR_STATE, "decode_step: unit %d is empty", u);
         maxn = std::max(maxn, c->len[u]);
+        uni_len &= c->len[u] == c->len[u0];
+        uni_b &= c->budget_unit[u] == c->budget_unit[u0];
+        uni_np &= c->next_pos[u] == c->next_pos[u0];
     }
     // CTAs per unit: enough clusters to fill the GPU ~3 deep, within 1..8
     int cs = 1;
@@ -441,6 +445,10 @@ hikv_status hikv_decode_step(hikv_cache* c, int32_t layer0, int32_t nl, const vo
     a.cand_slot = c->d_cand_slot;
     a.cs = cs;
     a.chunk_cap = smem_path ? chunk : 0;
+    a.uni_len = uni_len ? c->len[u0] : -1;
+    a.uni_budget = uni_b ? c->budget_unit[u0] : -1;
+    a.uni_next_pos = uni_np ? c->next_pos[u0] : -1;
+    a.identity_u0 = uni_b ? u0 : -1;   // equal budgets: launch order is the identity
     const size_t smem = decode_smem_bytes(c->dtype, c->d, c->G, smem_path, a.chunk_cap);
     cudaError_t e = launch_decode(a, c->tmap, c->dtype, c->d, c->G, smem_path, smem, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode_step: launch");

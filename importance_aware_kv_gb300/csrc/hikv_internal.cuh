@@ -133,6 +133,15 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     return false;
 }
 
+// Start pulling `bytes` at `src` from HBM into L2 (no destination, no wait).
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
 // 2-D tiled TMA load of box {x, y} of `tmap` into shared memory.
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tmap, int32_t x, int32_t y,
                                             uint64_t* bar) {
@@ -303,6 +312,11 @@ struct DecodeArgs {
     int32_t* cand_slot;     // [units][16]
     int32_t cs;             // CTAs per unit (cluster size)
     int32_t chunk_cap;      // max tokens per CTA handled by the smem path
+    // values the host mirror knows to be the same for every unit of the call
+    // (-1: read per unit from device memory); they spare the kernel a chain of
+    // dependent loads before its first copy can be issued
+    int32_t uni_len, uni_budget, uni_next_pos;
+    int32_t identity_u0;    // >= 0: unit of grid row y is identity_u0 + y (order unused)
 };
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmap, int dtype, int d, int group,
                           bool smem_path, size_t smem_bytes, cudaStream_t s);

@@ -139,14 +139,14 @@ __global__ void __launch_bounds__(kDecThreads, (G <= 4 ? 4 : 2))
 
     const int32_t c = (int32_t)cluster_ctarank();
     const int32_t CS = (int32_t)cluster_nctarank();
-    const int32_t u = a.order[blockIdx.y];
+    const int32_t u = a.identity_u0 >= 0 ? a.identity_u0 + (int32_t)blockIdx.y : a.order[blockIdx.y];
     const int32_t per_layer = v.batch * v.hkv;
     const int32_t li = u / per_layer - a.layer0;
     const int32_t b = (u / v.hkv) % v.batch;
     const int32_t g = u % v.hkv;
-    const int32_t n = v.len[u];
-    const int32_t Bu = v.budget[u];
-    const int32_t tnew = v.next_pos[u] - 1;
+    const int32_t n = a.uni_len >= 0 ? a.uni_len : v.len[u];
+    const int32_t Bu = a.uni_budget >= 0 ? a.uni_budget : v.budget[u];
+    const int32_t tnew = (a.uni_next_pos >= 0 ? a.uni_next_pos : v.next_pos[u]) - 1;
     const bool need_victim = n > Bu;
     const int32_t chunk = ceil_div(n, CS);
     const int32_t t0 = min(n, c * chunk);
@@ -179,8 +179,25 @@ __global__ void __launch_bounds__(kDecThreads, (G <= 4 ? 4 : 2))
 
     if (warp == kDecNCW) {
         // ---------------- producer ----------------
+        if (lane == 0) prefetch_tensormap(&tmap);
         const int32_t* ptab = v.page_table + (int64_t)u * v.max_pages;
-        for (int k = lane; k < min(npg, kDecMaxPg); k += 32) pg_s[k] = ptab[pg0 + k];
+        for (int k = lane; k < min(npg, kDecMaxPg); k += 32) {
+            const int32_t pg = ptab[pg0 + k];
+            pg_s[k] = pg;
+            // pull this page's part of the chunk (whole 16-slot tiles, K and V)
+            // into L2 right away, so HBM streams the CTA's entire chunk from
+            // the start while the shared-memory ring refills from L2
+            if (pg >= 0 && pg < v.pool_pages) {
+                const int32_t ps0 = (pg0 + k) << v.page_shift;
+                const int32_t a0 = max(ps0, first_blk * kDecTR);
+                const int32_t a1 = min(ps0 + v.page_tokens, (first_blk + nt) * kDecTR);
+                if (a1 > a0) {
+                    const uint8_t* kb = v.pool + (int64_t)pg * v.page_bytes + (int64_t)(a0 - ps0) * RB;
+                    prefetch_l2(kb, (uint32_t)(a1 - a0) * RB);
+                    prefetch_l2(kb + (int64_t)v.page_tokens * RB, (uint32_t)(a1 - a0) * RB);
+                }
+            }
+        }
         __syncwarp();
         if (lane == 0) {
             int it = 0;
