@@ -195,7 +195,8 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
     int optin = 0;
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device);
     c->smem_optin = (size_t)optin;
-    c->max_smem_chunk = decode_max_smem_chunk(c->dtype, c->d, c->G, std::min<size_t>(c->smem_optin, 160 * 1024));
+    // shared-memory logits path: chunks small enough for two CTAs per SM
+    c->max_smem_chunk = decode_max_smem_chunk(c->dtype, c->d, c->G, std::min<size_t>(c->smem_optin, 112 * 1024));
 
     View& v = c->v;
     const int row_bytes = c->d * c->esz;
@@ -418,14 +419,15 @@ hikv_status hikv_decode_step(hikv_cache* c, int32_t layer0, int32_t nl, const vo
         uni_b &= c->budget_unit[u] == c->budget_unit[u0];
         uni_np &= c->next_pos[u] == c->next_pos[u0];
     }
-    // CTAs per unit: enough clusters to fill the GPU ~3 deep, within 1..8
+    // CTAs per unit: as many as fit one wave at two CTAs per SM, then enough
+    // that a CTA's logits fit the shared memory of a two-per-SM CTA
     int cs = 1;
     if (c->cs_override > 0) {
         cs = std::min(c->cs_override, kMaxCS);
     } else {
-        const int target = 3 * c->sm_count;
-        while (cs < 8 && (int64_t)nu * cs < target) cs *= 2;
-        while (cs < kMaxCS && ceil_div(maxn, cs) > c->max_smem_chunk) cs *= 2;
+        const int slots = 2 * c->sm_count;
+        cs = std::max(1, std::min(8, slots / std::max(1, nu)));
+        while (cs < kMaxCS && ceil_div(maxn, cs) > c->max_smem_chunk) ++cs;
     }
     cs = std::min(cs, std::max(1, maxn));
     const int chunk = ceil_div(maxn, cs);

@@ -39,7 +39,8 @@ namespace hikv {
 constexpr int kDecNCW = 4;                       // consumer warps
 constexpr int kDecThreads = (kDecNCW + 1) * 32;  // + producer warp
 constexpr int kDecTR = 16;                       // slots per tile
-constexpr int kDecStages = 4;                    // ring depth (tiles)
+constexpr int kDecStages = 8;                    // ring depth (tiles): two per consumer warp
+constexpr int kDecPrefetch = 16;                 // tiles pulled into L2 ahead of the ring
 constexpr int kDecMaxPg = 256;                   // page ids cached in shared memory
 
 struct DecSmem {
@@ -181,23 +182,21 @@ __global__ void __launch_bounds__(kDecThreads, (G <= 4 ? 4 : 2))
         // ---------------- producer ----------------
         if (lane == 0) prefetch_tensormap(&tmap);
         const int32_t* ptab = v.page_table + (int64_t)u * v.max_pages;
-        for (int k = lane; k < min(npg, kDecMaxPg); k += 32) {
-            const int32_t pg = ptab[pg0 + k];
-            pg_s[k] = pg;
-            // pull this page's part of the chunk (whole 16-slot tiles, K and V)
-            // into L2 right away, so HBM streams the CTA's entire chunk from
-            // the start while the shared-memory ring refills from L2
-            if (pg >= 0 && pg < v.pool_pages) {
-                const int32_t ps0 = (pg0 + k) << v.page_shift;
-                const int32_t a0 = max(ps0, first_blk * kDecTR);
-                const int32_t a1 = min(ps0 + v.page_tokens, (first_blk + nt) * kDecTR);
-                if (a1 > a0) {
-                    const uint8_t* kb = v.pool + (int64_t)pg * v.page_bytes + (int64_t)(a0 - ps0) * RB;
-                    prefetch_l2(kb, (uint32_t)(a1 - a0) * RB);
-                    prefetch_l2(kb + (int64_t)v.page_tokens * RB, (uint32_t)(a1 - a0) * RB);
-                }
-            }
-        }
+        for (int k = lane; k < min(npg, kDecMaxPg); k += 32) pg_s[k] = ptab[pg0 + k];
+        __syncwarp();
+        // L2 prefetch of tile j (its K and V rows): HBM streams a window of
+        // kDecPrefetch tiles ahead of the shared-memory ring, which then
+        // refills from L2 instead of waiting a full HBM round trip per tile
+        auto prefetch_tile = [&](int j) {
+            const int32_t s0 = (first_blk + j) * kDecTR;
+            const int32_t pk = (s0 >> v.page_shift) - pg0;
+            const int32_t pg = pk < kDecMaxPg ? pg_s[pk] : ptab[pg0 + pk];
+            if (pg < 0 || pg >= v.pool_pages) return;
+            const uint8_t* kb = v.pool + (int64_t)pg * v.page_bytes + (int64_t)(s0 & (v.page_tokens - 1)) * RB;
+            prefetch_l2(kb, (uint32_t)TB);
+            prefetch_l2(kb + (int64_t)v.page_tokens * RB, (uint32_t)TB);
+        };
+        for (int j = lane; j < min(nt, kDecPrefetch); j += 32) prefetch_tile(j);
         __syncwarp();
         if (lane == 0) {
             int it = 0;
@@ -220,6 +219,7 @@ __global__ void __launch_bounds__(kDecThreads, (G <= 4 ? 4 : 2))
                 }
                 const int32_t yk = pg * 2 * v.page_tokens + (s0 & (v.page_tokens - 1));
                 uint8_t* dst = ring + st * 2 * TB;
+                if (it + kDecPrefetch < nt) prefetch_tile(it + kDecPrefetch);
                 mbar_arrive_expect_tx(&full[st], 2 * TB);
 #pragma unroll
                 for (int bx = 0; bx < NBOX; ++bx) {
@@ -350,12 +350,22 @@ __global__ void __launch_bounds__(kDecThreads, (G <= 4 ? 4 : 2))
             float x[EPL];
             Widen<T, EPL>::run(raw, x);
             const float2* pr = ps + r * G;
+            float2 pp[G];
+            if constexpr (G >= 2) {
+#pragma unroll
+                for (int h = 0; h < G; h += 2) {
+                    const float4 t4 = *reinterpret_cast<const float4*>(pr + h);
+                    pp[h] = make_float2(t4.x, t4.y);
+                    pp[h + 1] = make_float2(t4.z, t4.w);
+                }
+            } else {
+                pp[0] = pr[0];
+            }
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                const float2 pp = pr[h];
 #pragma unroll
                 for (int e = 0; e < EPL / 2; ++e)
-                    o2[h][e] = ffma2(make_float2(x[2 * e], x[2 * e + 1]), pp, o2[h][e]);
+                    o2[h][e] = ffma2(make_float2(x[2 * e], x[2 * e + 1]), pp[h], o2[h][e]);
             }
         }
         __syncwarp();
