@@ -451,6 +451,11 @@ hikv_status hikv_decode_step(hikv_cache* c, int32_t layer0, int32_t nl, const vo
     a.uni_budget = uni_b ? c->budget_unit[u0] : -1;
     a.uni_next_pos = uni_np ? c->next_pos[u0] : -1;
     a.identity_u0 = uni_b ? u0 : -1;   // equal budgets: launch order is the identity
+    // persistent clusters: at most one wave at two CTAs per SM
+    a.n_clusters = std::max(1, std::min(nu, (2 * c->sm_count) / cs));
+    // small calls fit in L2: prefetch each CTA's tiles there ahead of the ring
+    const int64_t call_bytes = (int64_t)nu * maxn * 2 * c->d * c->esz;
+    a.prefetch_tiles = call_bytes <= (48ll << 20) ? 16 : 0;
     const size_t smem = decode_smem_bytes(c->dtype, c->d, c->G, smem_path, a.chunk_cap);
     cudaError_t e = launch_decode(a, c->tmap, c->dtype, c->d, c->G, smem_path, smem, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode_step: launch");

@@ -123,6 +123,40 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parit
     return ok != 0;
 }
 
+// try_wait with cluster-scope acquire: completes the wait for data that CTAs
+// of the same cluster stored into this CTA's shared memory before arriving
+// (remotely) on the barrier with release semantics.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity, uint32_t* err) {
+    for (uint32_t i = 0; i < (1u << 21); ++i) {
+        if (mbar_try_wait_cluster(bar, parity, 1000u)) return true;
+    }
+    atomicOr(err, DEVERR_TIMEOUT);
+    return false;
+}
+
+// Arrive on the mbarrier at shared::cluster address `addr` (possibly in
+// another CTA of the cluster), releasing this thread's prior writes -- and
+// those ordered before them -- at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+
+__device__ __forceinline__ void prefetch_global_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // Bounded wait: gives up after 2^21 tries of at most ~1 us each (about two
 // seconds on a stalled barrier), records DEVERR_TIMEOUT and returns false.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t* err) {
@@ -316,7 +350,9 @@ struct DecodeArgs {
     // (-1: read per unit from device memory); they spare the kernel a chain of
     // dependent loads before its first copy can be issued
     int32_t uni_len, uni_budget, uni_next_pos;
-    int32_t identity_u0;    // >= 0: unit of grid row y is identity_u0 + y (order unused)
+    int32_t identity_u0;    // >= 0: unit of list index i is identity_u0 + i (order unused)
+    int32_t prefetch_tiles; // L2 prefetch distance in tiles (0: off)
+    int32_t n_clusters;     // persistent clusters launched; cluster y handles list indices y, y + n_clusters, ...
 };
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmap, int dtype, int d, int group,
                           bool smem_path, size_t smem_bytes, cudaStream_t s);

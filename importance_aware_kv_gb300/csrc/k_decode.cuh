@@ -9,27 +9,33 @@
 // role of the min-search that Kelle's systolic evictor runs alongside
 // attention (Kelle summary sec. 5.3) and of HiKV's min-heap (sec. III-B).
 //
-// One thread-block cluster per unit (layer, batch, KV head); its CS CTAs split
-// the unit's n live slots into equal chunks.  Per CTA:
-//   producer warp   loads the page ids of the chunk, then streams it in
-//                   16-slot tiles: the tile's K rows and V rows arrive with
-//                   2-D TMA tensor copies (128-byte swizzle) into an NSTAGE
-//                   ring (mbarrier full/empty pairs, bounded waits).
-//   consumer warps  tile i belongs to warp i % 4, which keeps a private
-//                   online softmax (running max m_w, sum l_w, unnormalised
-//                   O_w) over its tiles:
+// Persistent clusters: cluster y of CS CTAs processes the units of the launch
+// list at indices y, y + n_clusters, ...; for each unit, CTA c takes the c-th
+// of CS equal chunks of the unit's n live slots.  Per CTA:
+//   producer warp   for unit after unit: copies the unit's q (1-D TMA bulk
+//                   copy into a double buffer), loads the chunk's page ids,
+//                   and streams 16-slot tiles, K rows and V rows together,
+//                   with 2-D TMA tensor copies (128-byte swizzle) into an
+//                   NSTAGE ring (mbarrier full/empty pairs, bounded waits).  It
+//                   runs ahead into the next unit while the consumers finish
+//                   the current one.
+//   consumer warps  tile i of a unit belongs to warp i % 4, which keeps a
+//                   private online softmax (running max m_w, sum l_w,
+//                   unnormalised O_w):
 //     q.k   lane (row = lane % 16, half = lane / 16) owns half a K row: the
 //           swizzle makes those 16-byte reads conflict-free and lets q be a
 //           shared-memory broadcast; packed f32x2 FMAs, one shuffle joins the
 //           halves; logits (scaled by log2 e) are kept for the importance pass;
 //     p.v   lane owns d/32 output elements, packed f32x2 FMAs over the tile's
 //           V rows with p broadcast from shared memory.
-//   CTA merge of the warp states, then a cluster merge by remote stores into
-//   shared memory (DSMEM) before one cluster barrier:
+//   Per unit, the warp states merge per CTA, then each CTA stores its
+//   (m_c, l_c) into every partner's shared memory and its output slices into
+//   their owners' (DSMEM), and arrives remotely on their exchange mbarriers:
 //     m = max_c m_c, l = sum_c l_c 2^(m_c - m); out_h = sum_c O_c[h] 2^(m_c - m) / l;
 //     importance imp_j += sum_h 2^(s'_hj - m_h) / l_h (fp32 add, heads
-//     ascending); the eligible slot with the smallest (imp, -pos) is the
-//     step's victim, gathered in CTA 0 by a second remote store + barrier.
+//     ascending); each CTA's smallest eligible (imp, -pos) goes to CTA 0 the
+//     same way, which records the unit's victim.  Exchange buffers are double
+//     buffered by unit parity; no cluster barrier sits inside the unit loop.
 #pragma once
 
 #include "hikv_internal.cuh"
@@ -39,13 +45,13 @@ namespace hikv {
 constexpr int kDecNCW = 4;                       // consumer warps
 constexpr int kDecThreads = (kDecNCW + 1) * 32;  // + producer warp
 constexpr int kDecTR = 16;                       // slots per tile
-constexpr int kDecStages = 8;                    // ring depth (tiles): two per consumer warp
-constexpr int kDecPrefetch = 16;                 // tiles pulled into L2 ahead of the ring
+template <int G> struct DecStages { static constexpr int value = G >= 8 ? 6 : 8; };   // ring depth (tiles)
 constexpr int kDecMaxPg = 256;                   // page ids cached in shared memory
 
 struct DecSmem {
     // byte offsets into dynamic shared memory, from a 1024-aligned base
-    uint32_t ring, bars, q, ps, recv, small, pg, S, simp, spos, total;
+    uint32_t ring, bars, qraw, q, ps, red, xbuf, vbuf, small, pg, S, total;
+    uint32_t xbuf_bytes;
 };
 
 template <typename T, int D, int G>
@@ -53,31 +59,33 @@ __host__ __device__ inline DecSmem dec_layout(bool smem_s, int chunk_cap) {
     constexpr uint32_t RB = D * sizeof(T);
     DecSmem L{};
     uint32_t off = 0;
-    L.ring = off;                                 // K,V tiles; warp O partials after streaming
-    off += kDecStages * 2 * kDecTR * RB;
-    L.bars = off;
-    off += 2 * kDecStages * 8;
+    L.ring = off;                                 // K,V tiles
+    off += DecStages<G>::value * 2 * kDecTR * RB;
+    L.bars = off;                                 // full, empty [NST]; qfull, qempty, xbar, vbar [2]
+    off += (2 * DecStages<G>::value + 8) * 8;
+    off = (off + 127) & ~127u;
+    L.qraw = off;                                 // q of the unit as stored, [2][G][D]
+    off += 2 * G * D * sizeof(T);
+    off = (off + 15) & ~15u;
     L.q = off;                                    // q * scale * log2 e, fp32 [G][D]
     off += G * D * 4;
     L.ps = off;                                   // per-warp p of the tile, duplicated pairs [NCW][16][G][2]
     off += kDecNCW * kDecTR * G * 8;
-    L.recv = off;                                 // O slices from every CTA: G*D + kMaxCS floats
-    off += (G * D + kMaxCS) * 4;
+    L.red = off;                                  // warp O partials [NCW][G][D]
+    off += kDecNCW * G * D * 4;
+    // exchange buffer per unit parity: m [kMaxCS][G], l [kMaxCS][G], O slices [G*D + kMaxCS]
+    L.xbuf_bytes = (2 * kMaxCS * G + G * D + kMaxCS) * 4;
+    L.xbuf = off;
+    off += 2 * L.xbuf_bytes;
+    L.vbuf = off;                                 // [2] x (keys [kMaxCS] u64, slots [kMaxCS] i32)
+    off += 2 * kMaxCS * 12;
+    off = (off + 15) & ~15u;
     L.small = off;
-    off += 4096;
+    off += 2048;
     L.pg = off;                                   // page ids of the chunk
     off += kDecMaxPg * 4;
     L.S = off;
-    if (smem_s) {
-        off += (uint32_t)chunk_cap * G * 4;
-        off = (off + 15) & ~15u;
-        L.simp = off;
-        off += (uint32_t)chunk_cap * 4;
-        L.spos = off;
-        off += (uint32_t)chunk_cap * 4;
-    } else {
-        L.simp = L.spos = off;
-    }
+    if (smem_s) off += (uint32_t)chunk_cap * G * 4;
     L.total = ((off + 127) & ~127u) + 1024;       // + slack to align the base to 1024
     return L;
 }
@@ -88,8 +96,21 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
     return (uint32_t)((c >> 3) * (kDecTR * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
+struct DecUnit {
+    int32_t u, n, Bu, tnew;
+};
+
+__device__ __forceinline__ DecUnit dec_unit(const DecodeArgs& a, int32_t idx) {
+    DecUnit r;
+    r.u = a.identity_u0 >= 0 ? a.identity_u0 + idx : a.order[idx];
+    r.n = a.uni_len >= 0 ? a.uni_len : a.v.len[r.u];
+    r.Bu = a.uni_budget >= 0 ? a.uni_budget : a.v.budget[r.u];
+    r.tnew = (a.uni_next_pos >= 0 ? a.uni_next_pos : a.v.next_pos[r.u]) - 1;
+    return r;
+}
+
 template <typename T, int D, int G, bool SMEM_S>
-__global__ void __launch_bounds__(kDecThreads, (G <= 4 ? 4 : 2))
+__global__ void __launch_bounds__(kDecThreads, 2)
     k_decode(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap) {
     constexpr int ESZ = (int)sizeof(T);
     constexpr int RB = D * ESZ;              // row bytes: 128, 256 or 512
@@ -101,6 +122,8 @@ __global__ void __launch_bounds__(kDecThreads, (G <= 4 ? 4 : 2))
     constexpr int EPL = D / 32;              // p.v: elements per lane
     constexpr int LB = EPL * ESZ;            // p.v: bytes per lane
     constexpr int NCT = kDecNCW * 32;        // consumer threads
+    constexpr uint32_t QB = G * D * ESZ;     // bytes of one unit's q
+    constexpr int kDecStages = DecStages<G>::value;
     static_assert(EPL % 2 == 0 && EPC % 2 == 0, "pairs");
     using Raw = typename RawVec<LB>::type;
 
@@ -114,377 +137,420 @@ __global__ void __launch_bounds__(kDecThreads, (G <= 4 ? 4 : 2))
     uint8_t* ring = smem + L.ring;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
     uint64_t* empty = full + kDecStages;
+    uint64_t* qfull = empty + kDecStages;     // [2]
+    uint64_t* qempty = qfull + 2;             // [2]
+    uint64_t* xbar = qempty + 2;              // [2]
+    uint64_t* vbar = xbar + 2;                // [2]
     float* q_s = reinterpret_cast<float*>(smem + L.q);
     float2* ps_all = reinterpret_cast<float2*>(smem + L.ps);
-    float* orecv = reinterpret_cast<float*>(smem + L.recv);   // [CS][per]
+    float* red = reinterpret_cast<float*>(smem + L.red);
     float* sm = reinterpret_cast<float*>(smem + L.small);
-    float* m_recv = sm;                        // [kMaxCS][G]  (128)
-    float* l_recv = sm + 128;                  // [kMaxCS][G]  (128)
-    float* beta = sm + 256;                    // [kMaxCS][G]  (128)
-    float* mw_s = sm + 384;                    // [NCW][G]     (32)
-    float* lw_s = sm + 416;                    // [NCW][G]     (32)
-    float* wsc = sm + 448;                     // [NCW][G]     (32)
-    float* m_c = sm + 480;                     // [G]
-    float* l_c = sm + 488;                     // [G]
-    float* mfin = sm + 496;                    // [G]
-    float* linv = sm + 504;                    // [G]
-    unsigned long long* akey = reinterpret_cast<unsigned long long*>(sm + 512);  // [kMaxCS]
-    int32_t* aslot = reinterpret_cast<int32_t*>(akey + kMaxCS);                  // [kMaxCS]
-    unsigned long long* wkey = reinterpret_cast<unsigned long long*>(aslot + kMaxCS);  // [NCW]
-    int32_t* wslot = reinterpret_cast<int32_t*>(wkey + kDecNCW);                     // [NCW]
+    float* mw_s = sm;                          // [NCW][G]     (32)
+    float* lw_s = sm + 32;                     // [NCW][G]     (32)
+    float* wsc = sm + 64;                      // [NCW][G]     (32)
+    float* mfin = sm + 96;                     // [G]
+    float* linv = sm + 104;                    // [G]
+    float* m_c = sm + 112;                     // [G]
+    float* l_c = sm + 120;                     // [G]
+    float* beta = sm + 128;                    // [kMaxCS][G]  (128)
+    unsigned long long* wkey = reinterpret_cast<unsigned long long*>(sm + 256);  // [NCW]
+    int32_t* wslot = reinterpret_cast<int32_t*>(wkey + kDecNCW);                 // [NCW]
     volatile int32_t* abort_flag = wslot + kDecNCW;
     int32_t* pg_s = reinterpret_cast<int32_t*>(smem + L.pg);
     float* S_smem = reinterpret_cast<float*>(smem + L.S);
-    float* simp = reinterpret_cast<float*>(smem + L.simp);
-    int32_t* spos = reinterpret_cast<int32_t*>(smem + L.spos);
 
     const int32_t c = (int32_t)cluster_ctarank();
     const int32_t CS = (int32_t)cluster_nctarank();
-    const int32_t u = a.identity_u0 >= 0 ? a.identity_u0 + (int32_t)blockIdx.y : a.order[blockIdx.y];
-    const int32_t per_layer = v.batch * v.hkv;
-    const int32_t li = u / per_layer - a.layer0;
-    const int32_t b = (u / v.hkv) % v.batch;
-    const int32_t g = u % v.hkv;
-    const int32_t n = a.uni_len >= 0 ? a.uni_len : v.len[u];
-    const int32_t Bu = a.uni_budget >= 0 ? a.uni_budget : v.budget[u];
-    const int32_t tnew = (a.uni_next_pos >= 0 ? a.uni_next_pos : v.next_pos[u]) - 1;
-    const bool need_victim = n > Bu;
-    const int32_t chunk = ceil_div(n, CS);
-    const int32_t t0 = min(n, c * chunk);
-    int32_t t1 = min(n, t0 + chunk);
-    int32_t cnt = t1 - t0;
-    if (SMEM_S && cnt > a.chunk_cap) {   // host sizes chunk_cap; never taken
-        if (threadIdx.x == 0) atomicOr(v.err, DEVERR_STATE);
-        cnt = a.chunk_cap;
-        t1 = t0 + cnt;
-    }
-    const int32_t first_blk = t0 / kDecTR;
-    const int32_t nt = cnt > 0 ? (t1 - 1) / kDecTR - first_blk + 1 : 0;
-    const int32_t pg0 = t0 >> v.page_shift;                     // first page of the chunk
-    const int32_t npg = cnt > 0 ? ((t1 - 1) >> v.page_shift) - pg0 + 1 : 0;
-    const int64_t qbase = (((int64_t)li * v.batch + b) * v.hq + (int64_t)g * G) * D;
-    const int32_t per = ceil_div(G * D, CS);   // output elements finalised per CTA
-
-    float* Sb = SMEM_S ? S_smem : a.logits + ((int64_t)u * v.cap) * G;
-    const int32_t s_off = SMEM_S ? t0 : 0;   // S index of slot s = (s - s_off) * G
 
     if (tid == 0) {
         for (int s = 0; s < kDecStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&qfull[b], 1);
+            mbar_init(&qempty[b], 1);
+            mbar_init(&xbar[b], (uint32_t)CS);
+            mbar_init(&vbar[b], (uint32_t)CS);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
     __syncthreads();
+    // every CTA's barriers must be initialised before any partner arrives on them
+    cluster_sync_all();
 
     if (warp == kDecNCW) {
-        // ---------------- producer ----------------
+        // ======================= producer =======================
         if (lane == 0) prefetch_tensormap(&tmap);
-        const int32_t* ptab = v.page_table + (int64_t)u * v.max_pages;
-        for (int k = lane; k < min(npg, kDecMaxPg); k += 32) pg_s[k] = ptab[pg0 + k];
-        __syncwarp();
-        // L2 prefetch of tile j (its K and V rows): HBM streams a window of
-        // kDecPrefetch tiles ahead of the shared-memory ring, which then
-        // refills from L2 instead of waiting a full HBM round trip per tile
-        auto prefetch_tile = [&](int j) {
-            const int32_t s0 = (first_blk + j) * kDecTR;
-            const int32_t pk = (s0 >> v.page_shift) - pg0;
-            const int32_t pg = pk < kDecMaxPg ? pg_s[pk] : ptab[pg0 + pk];
-            if (pg < 0 || pg >= v.pool_pages) return;
-            const uint8_t* kb = v.pool + (int64_t)pg * v.page_bytes + (int64_t)(s0 & (v.page_tokens - 1)) * RB;
-            prefetch_l2(kb, (uint32_t)TB);
-            prefetch_l2(kb + (int64_t)v.page_tokens * RB, (uint32_t)TB);
-        };
-        for (int j = lane; j < min(nt, kDecPrefetch); j += 32) prefetch_tile(j);
-        __syncwarp();
-        if (lane == 0) {
-            int it = 0;
-            for (; it < nt; ++it) {
-                if (*abort_flag) break;
-                const int st = it % kDecStages;
-                const uint32_t round = (uint32_t)(it / kDecStages);
-                if (!mbar_wait_bounded(&empty[st], (round & 1u) ^ 1u, v.err)) {
+        int gi = 0;   // running tile counter of this CTA (lane 0's copy is authoritative)
+        for (int k = 0, idx = blockIdx.y; idx < a.n_units; ++k, idx += a.n_clusters) {
+            if (*abort_flag) break;
+            const DecUnit du = dec_unit(a, idx);
+            const int32_t per_layer = v.batch * v.hkv;
+            const int32_t li = du.u / per_layer - a.layer0;
+            const int32_t b = (du.u / v.hkv) % v.batch;
+            const int32_t g = du.u % v.hkv;
+            const int32_t chunk = ceil_div(du.n, CS);
+            const int32_t t0 = min(du.n, c * chunk);
+            const int32_t t1 = min(du.n, t0 + chunk);
+            const int32_t cnt = t1 - t0;
+            const int32_t first_blk = t0 / kDecTR;
+            const int32_t nt = cnt > 0 ? (t1 - 1) / kDecTR - first_blk + 1 : 0;
+            const int32_t pg0 = t0 >> v.page_shift;
+            const int32_t npg = cnt > 0 ? ((t1 - 1) >> v.page_shift) - pg0 + 1 : 0;
+            const int32_t* ptab = v.page_table + (int64_t)du.u * v.max_pages;
+            const int qb = k & 1;
+            if (lane == 0) {
+                // q of this unit into its half of the double buffer
+                if (!*abort_flag && mbar_wait_bounded(&qempty[qb], ((uint32_t)(k >> 1) & 1u) ^ 1u, v.err)) {
+                    const int64_t qbase = (((int64_t)li * v.batch + b) * v.hq + (int64_t)g * G) * D;
+                    mbar_arrive_expect_tx(&qfull[qb], QB);
+                    bulk_g2s(smem + L.qraw + qb * QB, a.q + qbase * ESZ, QB, &qfull[qb]);
+                } else {
                     *abort_flag = 1;
-                    break;
                 }
-                const int32_t s0 = (first_blk + it) * kDecTR;       // 16-aligned: never crosses a page
+            }
+            for (int j = lane; j < min(npg, kDecMaxPg); j += 32) pg_s[j] = ptab[pg0 + j];
+            __syncwarp();
+            auto page_of = [&](int32_t s0) -> int32_t {
                 const int32_t pk = (s0 >> v.page_shift) - pg0;
-                const int32_t pg = pk < kDecMaxPg ? pg_s[pk] : ptab[pg0 + pk];
-                if (pg < 0 || pg >= v.pool_pages) {
-                    atomicOr(v.err, DEVERR_PAGE);
-                    *abort_flag = 1;
-                    mbar_arrive(&full[st]);   // complete the stage without data
-                    break;
-                }
-                const int32_t yk = pg * 2 * v.page_tokens + (s0 & (v.page_tokens - 1));
-                uint8_t* dst = ring + st * 2 * TB;
-                if (it + kDecPrefetch < nt) prefetch_tile(it + kDecPrefetch);
-                mbar_arrive_expect_tx(&full[st], 2 * TB);
+                return pk < kDecMaxPg ? pg_s[pk] : ptab[pg0 + pk];
+            };
+            auto prefetch_tile = [&](int j) {
+                const int32_t s0 = (first_blk + j) * kDecTR;
+                const int32_t pg = page_of(s0);
+                if (pg < 0 || pg >= v.pool_pages) return;
+                const uint8_t* kb = v.pool + (int64_t)pg * v.page_bytes + (int64_t)(s0 & (v.page_tokens - 1)) * RB;
+                prefetch_l2(kb, (uint32_t)TB);
+                prefetch_l2(kb + (int64_t)v.page_tokens * RB, (uint32_t)TB);
+            };
+            const int pf = a.prefetch_tiles;
+            for (int j = lane; j < min(nt, pf); j += 32) prefetch_tile(j);
+            if (lane == 0) {
+                for (int i = 0; i < nt; ++i, ++gi) {
+                    if (*abort_flag) break;
+                    const int st = gi % kDecStages;
+                    if (!mbar_wait_bounded(&empty[st], ((uint32_t)(gi / kDecStages) & 1u) ^ 1u, v.err)) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    const int32_t s0 = (first_blk + i) * kDecTR;       // 16-aligned: never crosses a page
+                    const int32_t pg = page_of(s0);
+                    if (pg < 0 || pg >= v.pool_pages) {
+                        atomicOr(v.err, DEVERR_PAGE);
+                        *abort_flag = 1;
+                        mbar_arrive(&full[st]);   // complete the stage without data
+                        break;
+                    }
+                    if (pf > 0 && i + pf < nt) prefetch_tile(i + pf);
+                    const int32_t yk = pg * 2 * v.page_tokens + (s0 & (v.page_tokens - 1));
+                    uint8_t* dst = ring + st * 2 * TB;
+                    mbar_arrive_expect_tx(&full[st], 2 * TB);
 #pragma unroll
-                for (int bx = 0; bx < NBOX; ++bx) {
-                    tma_load_2d(dst + bx * (kDecTR * 128), &tmap, bx * (128 / ESZ), yk, &full[st]);
-                    tma_load_2d(dst + TB + bx * (kDecTR * 128), &tmap, bx * (128 / ESZ), yk + v.page_tokens,
-                                &full[st]);
+                    for (int bx = 0; bx < NBOX; ++bx) {
+                        tma_load_2d(dst + bx * (kDecTR * 128), &tmap, bx * (128 / ESZ), yk, &full[st]);
+                        tma_load_2d(dst + TB + bx * (kDecTR * 128), &tmap, bx * (128 / ESZ), yk + v.page_tokens,
+                                    &full[st]);
+                    }
                 }
             }
-            if (*abort_flag) {
-                // let copies already in flight land before the CTA can exit
-                for (int k = max(0, it - kDecStages); k < it; ++k)
-                    mbar_wait_bounded(&full[k % kDecStages], (uint32_t)(k / kDecStages) & 1u, v.err);
-            }
+            gi = __shfl_sync(0xffffffffu, gi, 0);
+            __syncwarp();
+        }
+        if (lane == 0 && *abort_flag) {
+            // let copies already in flight land before the CTA can exit
+            for (int j = max(0, gi - kDecStages); j < gi; ++j)
+                mbar_wait_bounded(&full[j % kDecStages], (uint32_t)(j / kDecStages) & 1u, v.err);
         }
         __syncwarp();
-        cluster_sync_all();
         cluster_sync_all();
         return;
     }
 
-    // ---------------- consumers ----------------
+    // ======================= consumers =======================
     const int ctid = tid;  // 0..127
-    for (int i = ctid; i < G * D; i += NCT)
-        q_s[i] = Elem<T>::to_f(reinterpret_cast<const T*>(a.q)[qbase + i]) * a.qscale;
-    if (SMEM_S) {
-        for (int j = ctid; j < cnt; j += NCT) {
-            simp[j] = v.imp[(int64_t)u * v.cap + t0 + j];
-            spos[j] = v.pos[(int64_t)u * v.cap + t0 + j];
-        }
-    }
-    named_bar_sync(1, NCT);
-
     float2* ps = ps_all + warp * (kDecTR * G);     // [16][G] duplicated p pairs
-    float m_w[G], l_w[G];
-    float2 o2[G][EPL / 2];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-        m_w[h] = -INFINITY;
-        l_w[h] = 0.f;
-#pragma unroll
-        for (int e = 0; e < EPL / 2; ++e) o2[h][e] = make_float2(0.f, 0.f);
-    }
     const int qr = lane & 15;           // q.k: tile row of this lane
     const int qh = lane >> 4;           // q.k: half of the row
     const int pv_chunk = (lane * LB) >> 4, pv_in = (lane * LB) & 15;
+    int gi_base = 0;
 
-    for (int i = warp; i < nt; i += kDecNCW) {
-        if (*abort_flag) break;
-        const int st = i % kDecStages;
-        if (!mbar_wait_bounded(&full[st], (uint32_t)(i / kDecStages) & 1u, v.err)) {
-            *abort_flag = 1;
-            break;
+    for (int k = 0, idx = blockIdx.y; idx < a.n_units; ++k, idx += a.n_clusters) {
+        const DecUnit du = dec_unit(a, idx);
+        const int32_t u = du.u;
+        const int32_t n = du.n;
+        const int32_t per_layer = v.batch * v.hkv;
+        const int32_t li = u / per_layer - a.layer0;
+        const int32_t b = (u / v.hkv) % v.batch;
+        const int32_t g = u % v.hkv;
+        const bool need_victim = n > du.Bu;
+        const int32_t chunk = ceil_div(n, CS);
+        const int32_t t0 = min(n, c * chunk);
+        int32_t t1 = min(n, t0 + chunk);
+        int32_t cnt = t1 - t0;
+        if (SMEM_S && cnt > a.chunk_cap) {   // host sizes chunk_cap; never taken
+            if (ctid == 0) atomicOr(v.err, DEVERR_STATE);
+            cnt = a.chunk_cap;
+            t1 = t0 + cnt;
         }
-        const int32_t s0 = (first_blk + i) * kDecTR;
-        const uint8_t* ktile = ring + st * 2 * TB;
-        const uint8_t* vtile = ktile + TB;
-        const int32_t lo_r = max(0, t0 - s0), hi_r = min(kDecTR, t1 - s0);   // valid rows [lo_r, hi_r)
+        const int32_t first_blk = t0 / kDecTR;
+        const int32_t nt = cnt > 0 ? (t1 - 1) / kDecTR - first_blk + 1 : 0;
+        const int64_t qbase = (((int64_t)li * v.batch + b) * v.hq + (int64_t)g * G) * D;
+        const int32_t per = ceil_div(G * D, CS);   // output elements finalised per CTA
+        const int xb = k & 1;
+        const uint32_t xpar = (uint32_t)(k >> 1) & 1u;
+        float* m_recv = reinterpret_cast<float*>(smem + L.xbuf + xb * L.xbuf_bytes);   // [kMaxCS][G]
+        float* l_recv = m_recv + kMaxCS * G;                                             // [kMaxCS][G]
+        float* orecv = l_recv + kMaxCS * G;                                              // [CS][per]
+        unsigned long long* akey = reinterpret_cast<unsigned long long*>(smem + L.vbuf + xb * kMaxCS * 12);
+        int32_t* aslot = reinterpret_cast<int32_t*>(akey + kMaxCS);
+        float* Sb = SMEM_S ? S_smem : a.logits + ((int64_t)u * v.cap) * G;
+        const int32_t s_off = SMEM_S ? t0 : 0;   // S index of slot s = (s - s_off) * G
+        const float* impg = v.imp + (int64_t)u * v.cap;
+        const int32_t* posg = v.pos + (int64_t)u * v.cap;
 
-        // ---- q.k: this lane's half row ----
-        float2 acc[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h) acc[h] = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int j = 0; j < CPL; ++j) {
-            const int cidx = qh * CPL + j;
-            const uint4 raw = *reinterpret_cast<const uint4*>(ktile + swz(qr, cidx));
-            float x[EPC];
-            Widen<T, EPC>::run(raw, x);
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float* qp = q_s + h * D + cidx * EPC;
-#pragma unroll
-                for (int e = 0; e < EPC; e += 4) {
-                    const float4 q4 = *reinterpret_cast<const float4*>(qp + e);
-                    acc[h] = ffma2(make_float2(x[e], x[e + 1]), make_float2(q4.x, q4.y), acc[h]);
-                    acc[h] = ffma2(make_float2(x[e + 2], x[e + 3]), make_float2(q4.z, q4.w), acc[h]);
-                }
-            }
+        // the importance pass reads these at the end of the unit: start them towards L2 now
+        for (int j = ctid * 32; j < cnt; j += NCT * 32) {
+            prefetch_global_l2(impg + t0 + j);
+            prefetch_global_l2(posg + t0 + j);
         }
-        const bool rv = qr >= lo_r && qr < hi_r;
-        float s[G];
+        // q of this unit
+        if (*abort_flag || !mbar_wait_bounded(&qfull[xb], xpar, v.err)) *abort_flag = 1;
+        {
+            const T* qraw = reinterpret_cast<const T*>(smem + L.qraw + xb * QB);
+            for (int i = ctid; i < G * D; i += NCT) q_s[i] = Elem<T>::to_f(qraw[i]) * a.qscale;
+        }
+        named_bar_sync(1, NCT);
+        if (ctid == 0) mbar_arrive(&qempty[xb]);
+
+        float m_w[G], l_w[G];
+        float2 o2[G][EPL / 2];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-            float t = acc[h].x + acc[h].y;
-            t += __shfl_xor_sync(0xffffffffu, t, 16);
-            s[h] = rv ? t : -INFINITY;
+            m_w[h] = -INFINITY;
+            l_w[h] = 0.f;
+#pragma unroll
+            for (int e = 0; e < EPL / 2; ++e) o2[h][e] = make_float2(0.f, 0.f);
         }
-        // ---- online softmax over this tile ----
-        float scl[G], p[G];
-        bool rescale = false;
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            float mt = s[h];
-#pragma unroll
-            for (int o = 8; o >= 1; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
-            const float mn = fmaxf(m_w[h], mt);
-            scl[h] = (mn == m_w[h]) ? 1.f : exp2f(m_w[h] - mn);
-            rescale |= (mn != m_w[h]);
-            m_w[h] = mn;
-            p[h] = rv ? exp2f(s[h] - mn) : 0.f;
-            float ls = p[h];
-#pragma unroll
-            for (int o = 8; o >= 1; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
-            l_w[h] = l_w[h] * scl[h] + ls;
-        }
-        if (qh == 0) {
-#pragma unroll
-            for (int h = 0; h < G; ++h) ps[qr * G + h] = make_float2(p[h], p[h]);
-            if (rv) {
-                float* srow = Sb + (int64_t)(s0 + qr - s_off) * G;
-#pragma unroll
-                for (int h = 0; h < G; ++h) srow[h] = s[h];
+
+        for (int i = warp; i < nt; i += kDecNCW) {
+            if (*abort_flag) break;
+            const int gi = gi_base + i;
+            const int st = gi % kDecStages;
+            if (!mbar_wait_bounded(&full[st], (uint32_t)(gi / kDecStages) & 1u, v.err)) {
+                *abort_flag = 1;
+                break;
             }
-        }
-        if (rescale) {
-#pragma unroll
-            for (int h = 0; h < G; ++h)
-#pragma unroll
-                for (int e = 0; e < EPL / 2; ++e) {
-                    o2[h][e].x *= scl[h];
-                    o2[h][e].y *= scl[h];
-                }
-        }
-        __syncwarp();
-        // ---- p.v over the tile's valid rows ----
-        for (int r = lo_r; r < hi_r; ++r) {
-            const Raw raw = *reinterpret_cast<const Raw*>(vtile + swz(r, pv_chunk) + pv_in);
-            float x[EPL];
-            Widen<T, EPL>::run(raw, x);
-            const float2* pr = ps + r * G;
-            float2 pp[G];
-            if constexpr (G >= 2) {
-#pragma unroll
-                for (int h = 0; h < G; h += 2) {
-                    const float4 t4 = *reinterpret_cast<const float4*>(pr + h);
-                    pp[h] = make_float2(t4.x, t4.y);
-                    pp[h + 1] = make_float2(t4.z, t4.w);
-                }
-            } else {
-                pp[0] = pr[0];
-            }
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-#pragma unroll
-                for (int e = 0; e < EPL / 2; ++e)
-                    o2[h][e] = ffma2(make_float2(x[2 * e], x[2 * e + 1]), pp[h], o2[h][e]);
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
-    }
+            const int32_t s0 = (first_blk + i) * kDecTR;
+            const uint8_t* ktile = ring + st * 2 * TB;
+            const uint8_t* vtile = ktile + TB;
+            const int32_t lo_r = max(0, t0 - s0), hi_r = min(kDecTR, t1 - s0);   // valid rows [lo_r, hi_r)
 
-    // ---- CTA merge of the warp states (ring reused for the O partials) ----
-    if (lane == 0) {
+            // ---- q.k: this lane's half row ----
+            float2 acc[G];
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-            mw_s[warp * G + h] = m_w[h];
-            lw_s[warp * G + h] = l_w[h];
-        }
-    }
-    named_bar_sync(1, NCT);   // every warp is done with the ring
-    float* red = reinterpret_cast<float*>(ring);   // [NCW][G][D]
+            for (int h = 0; h < G; ++h) acc[h] = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int h = 0; h < G; ++h)
+            for (int j = 0; j < CPL; ++j) {
+                const int cidx = qh * CPL + j;
+                const uint4 raw = *reinterpret_cast<const uint4*>(ktile + swz(qr, cidx));
+                float x[EPC];
+                Widen<T, EPC>::run(raw, x);
 #pragma unroll
-        for (int e = 0; e < EPL / 2; ++e)
-            *reinterpret_cast<float2*>(&red[(warp * G + h) * D + lane * EPL + 2 * e]) = o2[h][e];
-    if (ctid < G) {
-        float m = -INFINITY;
-        for (int w = 0; w < kDecNCW; ++w) m = fmaxf(m, mw_s[w * G + ctid]);
-        float l = 0.f;
-        for (int w = 0; w < kDecNCW; ++w) {
-            const float mw = mw_s[w * G + ctid];
-            const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - m);
-            wsc[w * G + ctid] = f;
-            l += lw_s[w * G + ctid] * f;
-        }
-        m_c[ctid] = m;
-        l_c[ctid] = l;
-    }
-    named_bar_sync(1, NCT);
-    // push (m_c, l_c) to every CTA of the cluster and O_c slices to their owners
-    if (ctid < CS * G) {
-        const int cc = ctid / G, h = ctid % G;
-        dsmem_st_f32(dsmem_addr(&m_recv[c * G + h], (uint32_t)cc), m_c[h]);
-        dsmem_st_f32(dsmem_addr(&l_recv[c * G + h], (uint32_t)cc), l_c[h]);
-    }
-    for (int idx = ctid; idx < G * D; idx += NCT) {
-        const int h = idx / D;
-        float sum = 0.f;
+                for (int h = 0; h < G; ++h) {
+                    const float* qp = q_s + h * D + cidx * EPC;
 #pragma unroll
-        for (int w = 0; w < kDecNCW; ++w) sum += red[w * G * D + idx] * wsc[w * G + h];
-        const int owner = idx / per, loc = idx - owner * per;
-        dsmem_st_f32(dsmem_addr(&orecv[c * per + loc], (uint32_t)owner), sum);
-    }
-
-    __syncwarp();
-    cluster_sync_all();  // #1: every CTA's (m_c, l_c) and O slices are in place
-
-    if (ctid < G) {
-        float m = -INFINITY;
-        for (int cc = 0; cc < CS; ++cc) m = fmaxf(m, m_recv[cc * G + ctid]);
-        float l = 0.f;
-        for (int cc = 0; cc < CS; ++cc)
-            if (l_recv[cc * G + ctid] > 0.f) l += l_recv[cc * G + ctid] * exp2f(m_recv[cc * G + ctid] - m);
-        mfin[ctid] = m;
-        linv[ctid] = 1.0f / l;
-    }
-    named_bar_sync(1, NCT);
-    if (ctid < CS * G) {
-        const int h = ctid % G;
-        beta[ctid] = (l_recv[ctid] > 0.f) ? exp2f(m_recv[ctid] - mfin[h]) * linv[h] : 0.f;
-    }
-    named_bar_sync(1, NCT);
-
-    // output slice owned by this CTA
-    {
-        T* outp = reinterpret_cast<T*>(a.out) + qbase;
-        for (int loc = ctid; loc < per; loc += NCT) {
-            const int idx = c * per + loc;
-            if (idx >= G * D) break;
-            const int h = idx / D;
-            float sum = 0.f;
-            for (int cc = 0; cc < CS; ++cc) sum += orecv[cc * per + loc] * beta[cc * G + h];
-            outp[idx] = Elem<T>::from_f(sum);
-        }
-    }
-    // importance update + local victim
-    {
-        float mf[G], li_[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            mf[h] = mfin[h];
-            li_[h] = linv[h];
-        }
-        unsigned long long kmin = ~0ull;
-        int32_t smin = -1;
-        const int32_t lo = v.sink, hi = tnew - v.window;
-        for (int j = ctid; j < cnt; j += NCT) {
-            const int32_t slot = t0 + j;
-            const float* srow = Sb + (int64_t)(slot - s_off) * G;
-            float inc = 0.f;
-#pragma unroll
-            for (int h = 0; h < G; ++h) inc += exp2f(srow[h] - mf[h]) * li_[h];
-            const int64_t mi = (int64_t)u * v.cap + slot;
-            const float old = SMEM_S ? simp[j] : v.imp[mi];
-            const float nw = old + inc;
-            v.imp[mi] = nw;
-            if (need_victim) {
-                const int32_t ps_ = SMEM_S ? spos[j] : v.pos[mi];
-                if (ps_ >= lo && ps_ <= hi) {
-                    const unsigned long long key =
-                        ((unsigned long long)__float_as_uint(nw) << 32) | (unsigned long long)(~(uint32_t)ps_);
-                    if (key < kmin) {
-                        kmin = key;
-                        smin = slot;
+                    for (int e = 0; e < EPC; e += 4) {
+                        const float4 q4 = *reinterpret_cast<const float4*>(qp + e);
+                        acc[h] = ffma2(make_float2(x[e], x[e + 1]), make_float2(q4.x, q4.y), acc[h]);
+                        acc[h] = ffma2(make_float2(x[e + 2], x[e + 3]), make_float2(q4.z, q4.w), acc[h]);
                     }
                 }
             }
-        }
-        if (need_victim) {
+            const bool rv = qr >= lo_r && qr < hi_r;
+            float s[G];
 #pragma unroll
-            for (int o2i = 16; o2i >= 1; o2i >>= 1) {
-                const unsigned long long ok = __shfl_xor_sync(0xffffffffu, kmin, o2i);
-                const int32_t os = __shfl_xor_sync(0xffffffffu, smin, o2i);
+            for (int h = 0; h < G; ++h) {
+                float t = acc[h].x + acc[h].y;
+                t += __shfl_xor_sync(0xffffffffu, t, 16);
+                s[h] = rv ? t : -INFINITY;
+            }
+            // ---- online softmax over this tile ----
+            float scl[G], p[G];
+            bool rescale = false;
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                float mt = s[h];
+#pragma unroll
+                for (int o = 8; o >= 1; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+                const float mn = fmaxf(m_w[h], mt);
+                scl[h] = (mn == m_w[h]) ? 1.f : exp2f(m_w[h] - mn);
+                rescale |= (mn != m_w[h]);
+                m_w[h] = mn;
+                p[h] = rv ? exp2f(s[h] - mn) : 0.f;
+                float ls = p[h];
+#pragma unroll
+                for (int o = 8; o >= 1; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+                l_w[h] = l_w[h] * scl[h] + ls;
+            }
+            if (qh == 0) {
+#pragma unroll
+                for (int h = 0; h < G; ++h) ps[qr * G + h] = make_float2(p[h], p[h]);
+                if (rv) {
+                    float* srow = Sb + (int64_t)(s0 + qr - s_off) * G;
+#pragma unroll
+                    for (int h = 0; h < G; ++h) srow[h] = s[h];
+                }
+            }
+            if (rescale) {
+#pragma unroll
+                for (int h = 0; h < G; ++h)
+#pragma unroll
+                    for (int e = 0; e < EPL / 2; ++e) {
+                        o2[h][e].x *= scl[h];
+                        o2[h][e].y *= scl[h];
+                    }
+            }
+            __syncwarp();
+            // ---- p.v over the tile's valid rows ----
+            for (int r = lo_r; r < hi_r; ++r) {
+                const Raw raw = *reinterpret_cast<const Raw*>(vtile + swz(r, pv_chunk) + pv_in);
+                float x[EPL];
+                Widen<T, EPL>::run(raw, x);
+                const float2* pr = ps + r * G;
+                float2 pp[G];
+                if constexpr (G >= 2) {
+#pragma unroll
+                    for (int h = 0; h < G; h += 2) {
+                        const float4 t4 = *reinterpret_cast<const float4*>(pr + h);
+                        pp[h] = make_float2(t4.x, t4.y);
+                        pp[h + 1] = make_float2(t4.z, t4.w);
+                    }
+                } else {
+                    pp[0] = pr[0];
+                }
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+#pragma unroll
+                    for (int e = 0; e < EPL / 2; ++e)
+                        o2[h][e] = ffma2(make_float2(x[2 * e], x[2 * e + 1]), pp[h], o2[h][e]);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
+        }
+        gi_base += nt;
+
+        // ---- CTA merge of the warp states ----
+        if (lane == 0) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                mw_s[warp * G + h] = m_w[h];
+                lw_s[warp * G + h] = l_w[h];
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int e = 0; e < EPL / 2; ++e)
+                *reinterpret_cast<float2*>(&red[(warp * G + h) * D + lane * EPL + 2 * e]) = o2[h][e];
+        named_bar_sync(1, NCT);
+        if (ctid < G) {
+            float m = -INFINITY;
+            for (int w = 0; w < kDecNCW; ++w) m = fmaxf(m, mw_s[w * G + ctid]);
+            float l = 0.f;
+            for (int w = 0; w < kDecNCW; ++w) {
+                const float mw = mw_s[w * G + ctid];
+                const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - m);
+                wsc[w * G + ctid] = f;
+                l += lw_s[w * G + ctid] * f;
+            }
+            m_c[ctid] = m;
+            l_c[ctid] = l;
+        }
+        named_bar_sync(1, NCT);
+        // store (m_c, l_c) into every CTA of the cluster, O_c slices into their owners
+        if (ctid < CS * G) {
+            const int cc = ctid / G, h = ctid % G;
+            dsmem_st_f32(dsmem_addr(&m_recv[c * G + h], (uint32_t)cc), m_c[h]);
+            dsmem_st_f32(dsmem_addr(&l_recv[c * G + h], (uint32_t)cc), l_c[h]);
+        }
+        for (int e = ctid; e < G * D; e += NCT) {
+            const int h = e / D;
+            float sum = 0.f;
+#pragma unroll
+            for (int w = 0; w < kDecNCW; ++w) sum += red[w * G * D + e] * wsc[w * G + h];
+            const int owner = e / per, loc = e - owner * per;
+            dsmem_st_f32(dsmem_addr(&orecv[c * per + loc], (uint32_t)owner), sum);
+        }
+        named_bar_sync(1, NCT);   // every remote store of this CTA is issued
+        if (ctid < CS) mbar_arrive_remote(dsmem_addr(&xbar[xb], (uint32_t)ctid));
+        if (*abort_flag || !mbar_wait_cluster_bounded(&xbar[xb], xpar, v.err)) *abort_flag = 1;
+
+        if (ctid < G) {
+            float m = -INFINITY;
+            for (int cc = 0; cc < CS; ++cc) m = fmaxf(m, m_recv[cc * G + ctid]);
+            float l = 0.f;
+            for (int cc = 0; cc < CS; ++cc)
+                if (l_recv[cc * G + ctid] > 0.f) l += l_recv[cc * G + ctid] * exp2f(m_recv[cc * G + ctid] - m);
+            mfin[ctid] = m;
+            linv[ctid] = 1.0f / l;
+        }
+        named_bar_sync(1, NCT);
+        if (ctid < CS * G) {
+            const int h = ctid % G;
+            beta[ctid] = (l_recv[ctid] > 0.f) ? exp2f(m_recv[ctid] - mfin[h]) * linv[h] : 0.f;
+        }
+        named_bar_sync(1, NCT);
+
+        // output slice owned by this CTA
+        {
+            T* outp = reinterpret_cast<T*>(a.out) + qbase;
+            for (int loc = ctid; loc < per; loc += NCT) {
+                const int e = c * per + loc;
+                if (e >= G * D) break;
+                const int h = e / D;
+                float sum = 0.f;
+                for (int cc = 0; cc < CS; ++cc) sum += orecv[cc * per + loc] * beta[cc * G + h];
+                outp[e] = Elem<T>::from_f(sum);
+            }
+        }
+        // importance update + local victim
+        unsigned long long kmin = ~0ull;
+        int32_t smin = -1;
+        {
+            float mf[G], li_[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                mf[h] = mfin[h];
+                li_[h] = linv[h];
+            }
+            const int32_t lo = v.sink, hi = du.tnew - v.window;
+            for (int j = ctid; j < cnt; j += NCT) {
+                const int32_t slot = t0 + j;
+                const float* srow = Sb + (int64_t)(slot - s_off) * G;
+                float inc = 0.f;
+#pragma unroll
+                for (int h = 0; h < G; ++h) inc += exp2f(srow[h] - mf[h]) * li_[h];
+                const float nw = impg[slot] + inc;
+                v.imp[(int64_t)u * v.cap + slot] = nw;
+                if (need_victim) {
+                    const int32_t pp = posg[slot];
+                    if (pp >= lo && pp <= hi) {
+                        const unsigned long long key =
+                            ((unsigned long long)__float_as_uint(nw) << 32) | (unsigned long long)(~(uint32_t)pp);
+                        if (key < kmin) {
+                            kmin = key;
+                            smin = slot;
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) {
+                const unsigned long long ok = __shfl_xor_sync(0xffffffffu, kmin, o);
+                const int32_t os = __shfl_xor_sync(0xffffffffu, smin, o);
                 if (ok < kmin) {
                     kmin = ok;
                     smin = os;
@@ -495,35 +561,37 @@ __global__ void __launch_bounds__(kDecThreads, (G <= 4 ? 4 : 2))
                 wslot[warp] = smin;
             }
         }
-    }
-    named_bar_sync(1, NCT);
-    if (ctid == 0 && need_victim) {
-        unsigned long long k = ~0ull;
-        int32_t sl = -1;
-        for (int w = 0; w < kDecNCW; ++w)
-            if (wkey[w] < k) {
-                k = wkey[w];
-                sl = wslot[w];
-            }
-        dsmem_st_u64(dsmem_addr(&akey[c], 0u), k);
-        dsmem_st_s32(dsmem_addr(&aslot[c], 0u), sl);
-    }
-
-    __syncwarp();
-    cluster_sync_all();  // #2: every CTA's local victim is in CTA 0
-
-    if (c == 0 && ctid == 0) {
-        int32_t vs = -1;
-        if (need_victim) {
-            unsigned long long k = ~0ull;
-            for (int cc = 0; cc < CS; ++cc)
-                if (akey[cc] < k) {
-                    k = akey[cc];
-                    vs = aslot[cc];
+        named_bar_sync(1, NCT);
+        if (ctid == 0) {
+            unsigned long long kk = ~0ull;
+            int32_t sl = -1;
+            for (int w = 0; w < kDecNCW; ++w)
+                if (wkey[w] < kk) {
+                    kk = wkey[w];
+                    sl = wslot[w];
                 }
+            dsmem_st_u64(dsmem_addr(&akey[c], 0u), kk);
+            dsmem_st_s32(dsmem_addr(&aslot[c], 0u), sl);
+            mbar_arrive_remote(dsmem_addr(&vbar[xb], 0u));
+            if (c == 0) {
+                int32_t vs = -1;
+                if (!*abort_flag && mbar_wait_cluster_bounded(&vbar[xb], xpar, v.err)) {
+                    unsigned long long best = ~0ull;
+                    for (int cc = 0; cc < CS; ++cc)
+                        if (akey[cc] < best) {
+                            best = akey[cc];
+                            vs = aslot[cc];
+                        }
+                } else {
+                    *abort_flag = 1;
+                }
+                v.victim[u] = need_victim ? vs : -1;
+            }
         }
-        v.victim[u] = vs;
+        named_bar_sync(1, NCT);   // shared buffers of this unit are free for the next
     }
+    __syncwarp();
+    cluster_sync_all();
 }
 
 template <typename T, int D, int G, bool SM>
@@ -538,7 +606,7 @@ cudaError_t decode_launch_one(const DecodeArgs& a, const CUtensorMap& tmap, size
         smem_set = smem;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)a.cs, (unsigned)a.n_units, 1);
+    cfg.gridDim = dim3((unsigned)a.cs, (unsigned)a.n_clusters, 1);
     cfg.blockDim = dim3(kDecThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
