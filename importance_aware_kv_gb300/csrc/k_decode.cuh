@@ -413,8 +413,11 @@ __global__ void __launch_bounds__(kDecThreads, 2)
                     }
             }
             __syncwarp();
-            // ---- p.v over the tile's valid rows ----
-            for (int r = lo_r; r < hi_r; ++r) {
+            // ---- p.v over the tile's valid rows (unrolled; invalid rows skipped, their
+            // stale V bytes may hold any bit pattern) ----
+#pragma unroll
+            for (int r = 0; r < kDecTR; ++r) {
+                if (r < lo_r || r >= hi_r) continue;
                 const Raw raw = *reinterpret_cast<const Raw*>(vtile + swz(r, pv_chunk) + pv_in);
                 float x[EPL];
                 Widen<T, EPL>::run(raw, x);
@@ -527,19 +530,31 @@ __global__ void __launch_bounds__(kDecThreads, 2)
                 li_[h] = linv[h];
             }
             const int32_t lo = v.sink, hi = du.tnew - v.window;
-            for (int j = ctid; j < cnt; j += NCT) {
-                const int32_t slot = t0 + j;
-                const float* srow = Sb + (int64_t)(slot - s_off) * G;
-                float inc = 0.f;
+            // the loads of this pass are issued together (one L2 round trip), then used
+            constexpr int kIP = 8;
+            for (int j0 = 0; j0 < cnt; j0 += kIP * NCT) {
+                float iv[kIP];
+                int32_t pv[kIP];
 #pragma unroll
-                for (int h = 0; h < G; ++h) inc += exp2f(srow[h] - mf[h]) * li_[h];
-                const float nw = impg[slot] + inc;
-                v.imp[(int64_t)u * v.cap + slot] = nw;
-                if (need_victim) {
-                    const int32_t pp = posg[slot];
-                    if (pp >= lo && pp <= hi) {
+                for (int q = 0; q < kIP; ++q) {
+                    const int j = j0 + q * NCT + ctid;
+                    iv[q] = j < cnt ? impg[t0 + j] : 0.f;
+                    pv[q] = (need_victim && j < cnt) ? posg[t0 + j] : 0;
+                }
+#pragma unroll
+                for (int q = 0; q < kIP; ++q) {
+                    const int j = j0 + q * NCT + ctid;
+                    if (j >= cnt) continue;
+                    const int32_t slot = t0 + j;
+                    const float* srow = Sb + (int64_t)(slot - s_off) * G;
+                    float inc = 0.f;
+#pragma unroll
+                    for (int h = 0; h < G; ++h) inc += exp2f(srow[h] - mf[h]) * li_[h];
+                    const float nw = iv[q] + inc;
+                    v.imp[(int64_t)u * v.cap + slot] = nw;
+                    if (need_victim && pv[q] >= lo && pv[q] <= hi) {
                         const unsigned long long key =
-                            ((unsigned long long)__float_as_uint(nw) << 32) | (unsigned long long)(~(uint32_t)pp);
+                            ((unsigned long long)__float_as_uint(nw) << 32) | (unsigned long long)(~(uint32_t)pv[q]);
                         if (key < kmin) {
                             kmin = key;
                             smin = slot;
