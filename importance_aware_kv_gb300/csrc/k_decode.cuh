@@ -632,7 +632,25 @@ cudaError_t decode_launch_one(const DecodeArgs& a, const CUtensorMap& tmap, size
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a, tmap);
+    // The clusters are persistent: launch no more than can be resident at
+    // once (clusters must fit in one GPC each), or the surplus would run as a
+    // second wave after the others had finished all their units.
+    static int cached_cs[kMaxCS + 1] = {};
+    static size_t cached_smem[kMaxCS + 1] = {};
+    static int cached_active[kMaxCS + 1] = {};
+    const int csi = a.cs <= kMaxCS ? a.cs : kMaxCS;
+    if (cached_cs[csi] != a.cs || cached_smem[csi] != smem) {
+        int active = 0;
+        cudaError_t e = cudaOccupancyMaxActiveClusters(&active, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        cached_cs[csi] = a.cs;
+        cached_smem[csi] = smem;
+        cached_active[csi] = active;
+    }
+    DecodeArgs b = a;
+    if (cached_active[csi] > 0 && b.n_clusters > cached_active[csi]) b.n_clusters = cached_active[csi];
+    cfg.gridDim = dim3((unsigned)b.cs, (unsigned)b.n_clusters, 1);
+    return cudaLaunchKernelEx(&cfg, kern, b, tmap);
 }
 
 template <typename T, int D, bool SM>
