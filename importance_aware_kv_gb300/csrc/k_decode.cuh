@@ -42,8 +42,11 @@
 
 namespace hikv {
 
-constexpr int kDecNCW = 4;                       // consumer warps
-constexpr int kDecThreads = (kDecNCW + 1) * 32;  // + producer warp
+// consumer warps per CTA (one more warp produces): 8 for G <= 4 so that two
+// CTAs give each SM scheduler four consumer warps to interleave; 4 for G = 8,
+// whose per-warp state is twice as large
+template <int G> struct DecWarps { static constexpr int value = G <= 4 ? 8 : 4; };
+template <int G> constexpr int dec_threads() { return (DecWarps<G>::value + 1) * 32; }
 constexpr int kDecTR = 16;                       // slots per tile
 template <int G> struct DecStages { static constexpr int value = G >= 8 ? 6 : 8; };   // ring depth (tiles)
 constexpr int kDecMaxPg = 256;                   // page ids cached in shared memory
@@ -57,6 +60,7 @@ struct DecSmem {
 template <typename T, int D, int G>
 __host__ __device__ inline DecSmem dec_layout(bool smem_s, int chunk_cap) {
     constexpr uint32_t RB = D * sizeof(T);
+    constexpr int kDecNCW = DecWarps<G>::value;
     DecSmem L{};
     uint32_t off = 0;
     L.ring = off;                                 // K,V tiles
@@ -110,8 +114,9 @@ __device__ __forceinline__ DecUnit dec_unit(const DecodeArgs& a, int32_t idx) {
 }
 
 template <typename T, int D, int G, bool SMEM_S>
-__global__ void __launch_bounds__(kDecThreads, 2)
+__global__ void __launch_bounds__(dec_threads<G>(), 2)
     k_decode(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap) {
+    constexpr int kDecNCW = DecWarps<G>::value;
     constexpr int ESZ = (int)sizeof(T);
     constexpr int RB = D * ESZ;              // row bytes: 128, 256 or 512
     constexpr int NBOX = RB / 128;           // 128-byte TMA boxes per row
@@ -145,6 +150,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     float2* ps_all = reinterpret_cast<float2*>(smem + L.ps);
     float* red = reinterpret_cast<float*>(smem + L.red);
     float* sm = reinterpret_cast<float*>(smem + L.small);
+    static_assert(kDecNCW * G <= 32, "warp state arrays");
     float* mw_s = sm;                          // [NCW][G]     (32)
     float* lw_s = sm + 32;                     // [NCW][G]     (32)
     float* wsc = sm + 64;                      // [NCW][G]     (32)
@@ -622,7 +628,7 @@ cudaError_t decode_launch_one(const DecodeArgs& a, const CUtensorMap& tmap, size
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)a.cs, (unsigned)a.n_clusters, 1);
-    cfg.blockDim = dim3(kDecThreads, 1, 1);
+    cfg.blockDim = dim3(dec_threads<G>(), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
