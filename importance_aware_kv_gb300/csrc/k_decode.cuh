@@ -42,10 +42,10 @@
 
 namespace hikv {
 
-// consumer warps per CTA (one more warp produces): 8 for G <= 4 so that two
-// CTAs give each SM scheduler four consumer warps to interleave; 4 for G = 8,
-// whose per-warp state is twice as large
-template <int G> struct DecWarps { static constexpr int value = G <= 4 ? 8 : 4; };
+// consumer warps per CTA (one more warp produces); with two ring stages per
+// warp each consumer's next tile lands while it computes the current one
+// (eight warps sharing the same ring, one stage each, measured slower)
+template <int G> struct DecWarps { static constexpr int value = 4; };
 template <int G> constexpr int dec_threads() { return (DecWarps<G>::value + 1) * 32; }
 constexpr int kDecTR = 16;                       // slots per tile
 template <int G> struct DecStages { static constexpr int value = G >= 8 ? 6 : 8; };   // ring depth (tiles)
