@@ -1,8 +1,11 @@
 """Benchmark of the budgeted, importance-aware KV-cache decode step on GB300.
 
-One step = the whole hot path for one decode token of every unit:
-hikv_append (new k, v) -> hikv_decode_step (fused attention + importance +
-victim argmin) -> hikv_evict (back to budget).  Workload: the Llama-3-8B-shaped
+One step = the whole hot path for one decode token of every unit: append the
+new k, v; attention with the importance update and victim argmin; evict back
+to the budget -- timed through hikv_decode_step_fused, which runs it as one
+kernel launch once every unit is at its budget (the three separate calls,
+hikv_append -> hikv_decode_step -> hikv_evict, are timed after it and reported
+as `three_call_path`).  Workload: the Llama-3-8B-shaped
 layer (batch 8, 32 query / 8 KV heads, d 128, bf16 K/V, 8192-token prompt,
 budget 1024, 4 sinks, 64-token window, eviction every step), seeded synthetic
 inputs resident in HBM before timing.  The decode stream continues past the
@@ -125,7 +128,7 @@ def gpu_id_for(dev_index: int) -> str:
 def step_bytes(w, n: int):
     """Algorithmic bytes of one decode step of one unit holding n tokens during
     attention: K/V rows, importance read+write, positions, q in, out, plus the
-    appended row; the decode kernel alone moves all but the append."""
+    appended row (read once from the caller's buffer, written into the pool)."""
     e = w.elem_bytes
     kv = 2 * n * w.d * e
     meta = 12 * n
@@ -199,7 +202,7 @@ def bench_gpu(args):
     w = W.WORKLOADS[WORKLOAD_INDEX]
     seed = w.index + 1000 * rank          # every rank decodes its own batch
     K, Wu, Ke = args.steps, args.warmup, args.e2e_steps
-    total_steps = Wu + K + Ke
+    total_steps = Wu + K + args.three_call_steps + Ke
     budgets = W.budgets(w, seed)
     cache = hk.Cache(hk.CacheConfig(w.layers, w.batch, w.hq, w.hkv, w.d, w.dtype, w.sink, w.window,
                                     budgets, w.prompt + total_steps + 1))
@@ -220,9 +223,7 @@ def bench_gpu(args):
     stream = torch.cuda.current_stream()
 
     def step(s):
-        cache.append(dks[s], dvs[s])
-        cache.decode_step(dqs[s], out)
-        cache.evict()
+        cache.step(dks[s], dvs[s], dqs[s], out, evict=True)
 
     for s in range(Wu):
         flush.fill_(float(s))
@@ -233,18 +234,41 @@ def bench_gpu(args):
     # shows up inside the timed events (the flush and the spin are outside).
     spin_cycles = int(args.spin_us * 2.0e3)
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(K)]
+    # ---- timed: the single-call step (append + decode + evict in one launch) ----
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     sampler = ClockSampler(gpu_id_for(local))
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    launches0 = cache.kernel_launches()
     for i in range(K):
         s = Wu + i
         flush.fill_(float(i))
         torch.cuda._sleep(spin_cycles)
-        e0, e1, e2, e3 = ev[i]
+        e0, e1 = ev[i]
+        e0.record(stream)
+        step(s)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    launches = cache.kernel_launches() - launches0
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    step_ms = [e0.elapsed_time(e1) for (e0, e1) in ev]
+    t_total = sum(step_ms) / 1e3
+    if world > 1:
+        t = torch.tensor([t_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_total = float(t.item())
+
+    # ---- the same steps as three calls (append, decode_step, evict), for context ----
+    K3 = args.three_call_steps
+    ev3 = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(K3)]
+    for i in range(K3):
+        s = Wu + K + i
+        flush.fill_(float(i))
+        torch.cuda._sleep(spin_cycles)
+        e0, e1, e2, e3 = ev3[i]
         e0.record(stream)
         cache.append(dks[s], dvs[s])
         e1.record(stream)
@@ -253,16 +277,12 @@ def bench_gpu(args):
         cache.evict()
         e3.record(stream)
     torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    clocks = sampler.stop()
-    step_ms = [e0.elapsed_time(e3) for (e0, e1, e2, e3) in ev]
-    dec_ms = [e1.elapsed_time(e2) for (e0, e1, e2, e3) in ev]
-    t_total = sum(step_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([t_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_total = float(t.item())
+    three = None
+    if K3 > 0:
+        ms3 = [e0.elapsed_time(e3) for (e0, e1, e2, e3) in ev3]
+        dec3 = [e1.elapsed_time(e2) for (e0, e1, e2, e3) in ev3]
+        three = {"steps": K3, "ms_per_step": sum(ms3) / K3, "steps_per_s": K3 / (sum(ms3) / 1e3),
+                 "decode_kernel_us": 1e3 * sum(dec3) / K3, "launches_per_step": 3}
 
     # ---- e2e through the C ABI with pinned host buffers ----
     hk_s = stream
@@ -278,16 +298,14 @@ def bench_gpu(args):
     e_end = torch.cuda.Event(enable_timing=True)
     e2e_ms = 0.0
     for i in range(Ke):
-        s = Wu + K + i
+        s = Wu + K + K3 + i
         flush.fill_(float(i))
         e_start.record(hk_s)
         k_dev.copy_(hk_k[s], non_blocking=True)
         v_dev.copy_(hk_v[s], non_blocking=True)
         q_dev.copy_(hk_q[s], non_blocking=True)
         kb, vb, qb = k_dev.view(torch.bfloat16), v_dev.view(torch.bfloat16), q_dev.view(torch.bfloat16)
-        cache.append(kb, vb)
-        cache.decode_step(qb, out)
-        cache.evict()
+        cache.step(kb, vb, qb, out, evict=True)
         out_host.copy_(out, non_blocking=True)
         e_end.record(hk_s)
         e_end.synchronize()
@@ -301,9 +319,10 @@ def bench_gpu(args):
     # ---- numbers ----
     kv, meta, qo, app = step_bytes(w, n_ret)
     units = w.units
-    dec_bytes = units * (kv + meta + qo)
-    step_bytes_all = units * (kv + meta + qo + app)
-    dec_avg_s = (sum(dec_ms) / len(dec_ms)) / 1e3
+    # the fused launch moves everything a step moves: it is the step's only kernel
+    dec_bytes = units * (kv + meta + qo + app)
+    step_bytes_all = dec_bytes
+    dec_avg_s = (sum(step_ms) / len(step_ms)) / 1e3
     peaks, src = measured_peaks()
     peak = float(peaks.get("hbm_gbs", 6800.0))
     achieved = dec_bytes / dec_avg_s / 1e9
@@ -328,13 +347,15 @@ def bench_gpu(args):
                    "parallelism": f"replicas x{world} (units sharded by rank, no collective)"},
         "hbm_gbs_step": step_bytes_all * world * K / t_total / 1e9,
         "retained_kv_gbs": units * kv * world * K / t_total / 1e9,
-        "roofline": {"kernel": "k_decode (fused attention + importance + argmin)", "bound": "hbm",
+        "roofline": {"kernel": "k_decode (append + attention + importance + victim + evict, one launch)",
+                     "bound": "hbm",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"{src} hbm_gbs", "traffic": traffic,
                      "bytes_per_launch": dec_bytes, "avg_launch_us": dec_avg_s * 1e6},
         "e2e": {"value": Ke / (e2e_ms / 1e3), "unit": "steps/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "steps": Ke},
-        "gpu_launches": 3 * K,
+        "gpu_launches": launches,
+        "three_call_path": three,
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -353,6 +374,7 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--three-call-steps", type=int, default=500)
     ap.add_argument("--spin-us", type=float, default=60.0)
     ap.add_argument("--impl", default="hikv", choices=["hikv", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -28,7 +28,8 @@ HIKV_F32, HIKV_BF16 = 0, 1
 # every entry point of include/hikv.h
 ABI_FUNCTIONS = ("hikv_create_cache", "hikv_destroy_cache", "hikv_append", "hikv_score_window",
                  "hikv_decode_step", "hikv_evict", "hikv_gather_retained", "hikv_get_lengths",
-                 "hikv_device_status", "hikv_last_error", "hikv_score_window_noalloc")
+                 "hikv_device_status", "hikv_last_error", "hikv_score_window_noalloc",
+                 "hikv_decode_step_fused", "hikv_kernel_launches")
 
 
 class HikvError(RuntimeError):
@@ -65,6 +66,8 @@ def _load():
         "hikv_device_status": ([P], S),
         "hikv_last_error": ([], ctypes.c_char_p),
         "hikv_score_window_noalloc": ([I32] * 8 + [ctypes.c_float, P, P, P, P], S),
+        "hikv_decode_step_fused": ([P, I32, I32, P, P, P, P, I32, P], S),
+        "hikv_kernel_launches": ([P], ctypes.c_int64),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -152,6 +155,12 @@ def hikv_decode_step(h, layer0: int, q, out, stream=None) -> None:
                                  _dev(out, "out", q.dtype, q.shape), _stream(stream)))
 
 
+def hikv_decode_step_fused(h, layer0: int, k, v, q, out, evict: bool = True, stream=None) -> None:
+    _check(_lib.hikv_decode_step_fused(h, layer0, q.shape[0], _dev(k, "k"), _dev(v, "v", k.dtype, k.shape),
+                                       _dev(q, "q", k.dtype), _dev(out, "out", q.dtype, q.shape),
+                                       1 if evict else 0, _stream(stream)))
+
+
 def hikv_evict(h, layer0: int, nlayers: int, stream=None) -> None:
     _check(_lib.hikv_evict(h, layer0, nlayers, _stream(stream)))
 
@@ -223,6 +232,14 @@ class Cache:
 
     def decode_step(self, q, out, layer0=0, stream=None):
         hikv_decode_step(self.h, layer0, q, out, stream)
+
+    def kernel_launches(self) -> int:
+        """Kernels this cache has launched so far (host counter)."""
+        return int(_lib.hikv_kernel_launches(self.h))
+
+    def step(self, k, v, q, out, evict=True, layer0=0, stream=None):
+        """append + decode_step (+ evict) as one call (one launch in steady state)."""
+        hikv_decode_step_fused(self.h, layer0, k, v, q, out, evict, stream)
 
     def evict(self, layer0=0, nlayers=None, stream=None):
         hikv_evict(self.h, layer0, self.cfg.num_layers if nlayers is None else nlayers, stream)

@@ -100,6 +100,7 @@ struct hikv_cache {
     std::vector<uint8_t> fresh;         // decode ran since the last state change
     int64_t pages_in_use = 0;
     int cs_override = 0;                // HIKV_DECODE_CS (tuning)
+    int64_t launches = 0;               // kernels launched through this cache
 };
 
 namespace {
@@ -358,6 +359,7 @@ hikv_status hikv_append(hikv_cache* c, int32_t layer0, int32_t nl, int32_t ntok,
     a.vv = (const uint8_t*)vv;
     a.base = c->d_append_base;
     cudaError_t e = launch_append(a, (cudaStream_t)stream);
+    c->launches += ntok <= 64 ? 1 : 2;
     if (e != cudaSuccess) return cuda_fail(e, "append: launch");
     for (int u = u0; u < u0 + nu; ++u) {
         c->len[u] += ntok;
@@ -398,23 +400,30 @@ hikv_status hikv_score_window(hikv_cache* c, int32_t layer0, int32_t nl, int32_t
     a.nchunks_grid = ceil_div(maxn, kWindowChunk);
     a.chunk = kWindowChunk;
     cudaError_t e = launch_window(a, c->dtype, c->d, c->G, (cudaStream_t)stream);
+    c->launches += 2;
     if (e != cudaSuccess) return cuda_fail(e, "score_window: launch");
     for (int u = u0; u < u0 + nu; ++u) c->fresh[u] = 0;
     return HIKV_OK;
 }
 
-hikv_status hikv_decode_step(hikv_cache* c, int32_t layer0, int32_t nl, const void* q, void* out,
-                             hikv_stream_t stream) {
-    g_err.clear();
-    if (!range_ok(c, layer0, nl)) return fail(HIKV_ERR_INVALID_ARG, "decode_step: bad cache or layer range");
-    if (!q || !out) return fail(HIKV_ERR_INVALID_ARG, "decode_step: null q or out");
-    if (q == out) return fail(HIKV_ERR_INVALID_ARG, "decode_step: out aliases q");
+}  // extern "C"
+
+namespace {
+
+// Launch the decode kernel over the units of [layer0, layer0 + nl).  With
+// fused = 1 the kernel first appends one token per unit (rows new_k/new_v)
+// and, with evict = 1, moves it into the victim's slot when the unit is over
+// budget; the host mirror then already holds the post-append lengths.
+hikv_status launch_decode_call(hikv_cache* c, int32_t layer0, int32_t nl, const void* q, void* out,
+                               int fused, int evict, const void* new_k, const void* new_v,
+                               hikv_stream_t stream, const char* who) {
     const int u0 = layer0 * c->per_layer, nu = nl * c->per_layer;
     int maxn = 0;
     bool uni_len = true, uni_b = true, uni_np = true;
     for (int u = u0; u < u0 + nu; ++u) {
-        if (c->len[u] < 1) return fail(HIKV_ERR_STATE, "decode_step: unit %d is empty", u);
-        maxn = std::max(maxn, c->len[u]);
+        const int n = c->len[u] + fused;
+        if (n < 1) return fail(HIKV_ERR_STATE, "%s: unit %d is empty", who, u);
+        maxn = std::max(maxn, n);
         uni_len &= c->len[u] == c->len[u0];
         uni_b &= c->budget_unit[u] == c->budget_unit[u0];
         uni_np &= c->next_pos[u] == c->next_pos[u0];
@@ -433,7 +442,7 @@ hikv_status hikv_decode_step(hikv_cache* c, int32_t layer0, int32_t nl, const vo
     const int chunk = ceil_div(maxn, cs);
     const bool smem_path = chunk <= c->max_smem_chunk;
     if (!smem_path && !c->d_logits)
-        return fail(HIKV_ERR_UNSUPPORTED, "decode_step: %d tokens per CTA exceed shared memory", chunk);
+        return fail(HIKV_ERR_UNSUPPORTED, "%s: %d tokens per CTA exceed shared memory", who, chunk);
     DecodeArgs a{};
     a.v = c->v;
     a.order = (nl == c->L) ? c->d_order_all : c->d_order_layer + u0;
@@ -447,19 +456,75 @@ hikv_status hikv_decode_step(hikv_cache* c, int32_t layer0, int32_t nl, const vo
     a.cand_slot = c->d_cand_slot;
     a.cs = cs;
     a.chunk_cap = smem_path ? chunk : 0;
-    a.uni_len = uni_len ? c->len[u0] : -1;
+    a.uni_len = uni_len ? c->len[u0] + fused : -1;
     a.uni_budget = uni_b ? c->budget_unit[u0] : -1;
-    a.uni_next_pos = uni_np ? c->next_pos[u0] : -1;
+    a.uni_next_pos = uni_np ? c->next_pos[u0] + fused : -1;
     a.identity_u0 = uni_b ? u0 : -1;   // equal budgets: launch order is the identity
     // persistent clusters: at most one wave at two CTAs per SM
     a.n_clusters = std::max(1, std::min(nu, (2 * c->sm_count) / cs));
     // small calls fit in L2: prefetch each CTA's tiles there ahead of the ring
     const int64_t call_bytes = (int64_t)nu * maxn * 2 * c->d * c->esz;
     a.prefetch_tiles = call_bytes <= (48ll << 20) ? 16 : 0;
+    a.fused = fused;
+    a.evict = evict;
+    a.new_k = (const uint8_t*)new_k;
+    a.new_v = (const uint8_t*)new_v;
     const size_t smem = decode_smem_bytes(c->dtype, c->d, c->G, smem_path, a.chunk_cap);
     cudaError_t e = launch_decode(a, c->tmap, c->dtype, c->d, c->G, smem_path, smem, (cudaStream_t)stream);
-    if (e != cudaSuccess) return cuda_fail(e, "decode_step: launch");
+    c->launches += 1;
+    if (e != cudaSuccess) return cuda_fail(e, who);
+    return HIKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+hikv_status hikv_decode_step(hikv_cache* c, int32_t layer0, int32_t nl, const void* q, void* out,
+                             hikv_stream_t stream) {
+    g_err.clear();
+    if (!range_ok(c, layer0, nl)) return fail(HIKV_ERR_INVALID_ARG, "decode_step: bad cache or layer range");
+    if (!q || !out) return fail(HIKV_ERR_INVALID_ARG, "decode_step: null q or out");
+    if (q == out) return fail(HIKV_ERR_INVALID_ARG, "decode_step: out aliases q");
+    hikv_status st = launch_decode_call(c, layer0, nl, q, out, 0, 0, nullptr, nullptr, stream, "decode_step");
+    if (st != HIKV_OK) return st;
+    const int u0 = layer0 * c->per_layer, nu = nl * c->per_layer;
     for (int u = u0; u < u0 + nu; ++u) c->fresh[u] = 1;
+    return HIKV_OK;
+}
+
+hikv_status hikv_decode_step_fused(hikv_cache* c, int32_t layer0, int32_t nl, const void* k, const void* v,
+                                   const void* q, void* out, int32_t evict, hikv_stream_t stream) {
+    g_err.clear();
+    if (!range_ok(c, layer0, nl)) return fail(HIKV_ERR_INVALID_ARG, "decode_step_fused: bad cache or layer range");
+    if (!k || !v || !q || !out) return fail(HIKV_ERR_INVALID_ARG, "decode_step_fused: null pointer");
+    if (q == out) return fail(HIKV_ERR_INVALID_ARG, "decode_step_fused: out aliases q");
+    if (((uintptr_t)k | (uintptr_t)v) & 15)
+        return fail(HIKV_ERR_INVALID_ARG, "decode_step_fused: k and v must be 16-byte aligned");
+    const int u0 = layer0 * c->per_layer, nu = nl * c->per_layer;
+    bool one_launch = true;
+    for (int u = u0; u < u0 + nu && one_launch; ++u) {
+        const int n = c->len[u] + 1;
+        if (n > c->cap) return fail(HIKV_ERR_CAPACITY, "decode_step_fused: unit %d would exceed max_tokens", u);
+        if ((int64_t)c->next_pos[u] + 1 > INT32_MAX) return fail(HIKV_ERR_CAPACITY, "decode_step_fused: positions overflow");
+        // the single launch needs the new slot's page mapped, and at most one eviction
+        if (ceil_div(n, c->P) > c->mapped[u]) one_launch = false;
+        if (evict && n - c->budget_unit[u] > 1) one_launch = false;
+    }
+    if (!one_launch) {
+        hikv_status st = hikv_append(c, layer0, nl, 1, k, v, stream);
+        if (st == HIKV_OK) st = hikv_decode_step(c, layer0, nl, q, out, stream);
+        if (st == HIKV_OK && evict) st = hikv_evict(c, layer0, nl, stream);
+        return st;
+    }
+    hikv_status st = launch_decode_call(c, layer0, nl, q, out, 1, evict ? 1 : 0, k, v, stream, "decode_step_fused");
+    if (st != HIKV_OK) return st;
+    for (int u = u0; u < u0 + nu; ++u) {
+        const bool cut = evict && c->len[u] + 1 > c->budget_unit[u];
+        c->len[u] = cut ? c->budget_unit[u] : c->len[u] + 1;
+        c->next_pos[u] += 1;
+        c->fresh[u] = cut ? 0 : 1;
+    }
     return HIKV_OK;
 }
 
@@ -482,6 +547,7 @@ hikv_status hikv_evict(hikv_cache* c, int32_t layer0, int32_t nl, hikv_stream_t 
     a.holes = c->d_holes;
     a.hole_off = c->d_hole_off;
     cudaError_t e = fast ? launch_evict_fast(a, (cudaStream_t)stream) : launch_evict_general(a, (cudaStream_t)stream);
+    c->launches += 1;
     if (e != cudaSuccess) return cuda_fail(e, "evict: launch");
     for (int u = u0; u < u0 + nu; ++u) {
         const int Bu = c->budget_unit[u];
@@ -518,6 +584,7 @@ hikv_status hikv_gather_retained(hikv_cache* c, int32_t layer0, int32_t nl, int3
     a.k_out = (uint8_t*)k_out;
     a.v_out = (uint8_t*)v_out;
     cudaError_t e = launch_gather(a, (cudaStream_t)stream);
+    c->launches += 1;
     if (e != cudaSuccess) return cuda_fail(e, "gather: launch");
     return HIKV_OK;
 }
@@ -528,6 +595,8 @@ hikv_status hikv_get_lengths(const hikv_cache* c, int32_t layer0, int32_t nl, in
     std::memcpy(lengths_host, c->len.data() + (size_t)layer0 * c->per_layer, sizeof(int32_t) * nl * c->per_layer);
     return HIKV_OK;
 }
+
+int64_t hikv_kernel_launches(const hikv_cache* c) { return c ? c->launches : -1; }
 
 hikv_status hikv_device_status(hikv_cache* c) {
     g_err.clear();

@@ -172,6 +172,12 @@ __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// order this thread's earlier generic-proxy global stores before its later
+// async-proxy (TMA) operations
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
@@ -353,6 +359,12 @@ struct DecodeArgs {
     int32_t identity_u0;    // >= 0: unit of list index i is identity_u0 + i (order unused)
     int32_t prefetch_tiles; // L2 prefetch distance in tiles (0: off)
     int32_t n_clusters;     // persistent clusters launched; cluster y handles list indices y, y + n_clusters, ...
+    // fused step (append + decode + one-token evict in one launch): fused = 1,
+    // new_k/new_v the appended rows [units of the call][d]; evict = 1 moves
+    // the new token into the victim's slot when the unit is over budget
+    int32_t fused, evict;
+    const uint8_t* new_k;
+    const uint8_t* new_v;
 };
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmap, int dtype, int d, int group,
                           bool smem_path, size_t smem_bytes, cudaStream_t s);

@@ -104,12 +104,16 @@ struct DecUnit {
     int32_t u, n, Bu, tnew;
 };
 
+// In a fused step the device length and position counters still describe the
+// cache before the append; the unit then holds one more token, the new one,
+// in slot n - 1 at position tnew.  (Uniform values from the host already
+// include the append.)
 __device__ __forceinline__ DecUnit dec_unit(const DecodeArgs& a, int32_t idx) {
     DecUnit r;
     r.u = a.identity_u0 >= 0 ? a.identity_u0 + idx : a.order[idx];
-    r.n = a.uni_len >= 0 ? a.uni_len : a.v.len[r.u];
+    r.n = a.uni_len >= 0 ? a.uni_len : a.v.len[r.u] + a.fused;
     r.Bu = a.uni_budget >= 0 ? a.uni_budget : a.v.budget[r.u];
-    r.tnew = (a.uni_next_pos >= 0 ? a.uni_next_pos : a.v.next_pos[r.u]) - 1;
+    r.tnew = (a.uni_next_pos >= 0 ? a.uni_next_pos : a.v.next_pos[r.u] + a.fused) - 1;
     return r;
 }
 
@@ -250,6 +254,21 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
                         break;
                     }
                     if (pf > 0 && i + pf < nt) prefetch_tile(i + pf);
+                    const int32_t sn = du.n - 1;   // fused step: the appended token's slot
+                    if (a.fused && sn >= s0 && sn < s0 + kDecTR) {
+                        const int64_t ui = (int64_t)du.u - (int64_t)a.layer0 * per_layer;
+                        const uint4* ks = reinterpret_cast<const uint4*>(a.new_k + ui * RB);
+                        const uint4* vs = reinterpret_cast<const uint4*>(a.new_v + ui * RB);
+                        uint8_t* kd = v.pool + (int64_t)pg * v.page_bytes + (int64_t)(sn & (v.page_tokens - 1)) * RB;
+                        uint4* kd4 = reinterpret_cast<uint4*>(kd);
+                        uint4* vd4 = reinterpret_cast<uint4*>(kd + (int64_t)v.page_tokens * RB);
+#pragma unroll 4
+                        for (int q = 0; q < RB / 16; ++q) {
+                            kd4[q] = ks[q];
+                            vd4[q] = vs[q];
+                        }
+                        fence_proxy_async_global();   // the TMA below must see these rows
+                    }
                     const int32_t yk = pg * 2 * v.page_tokens + (s0 & (v.page_tokens - 1));
                     uint8_t* dst = ring + st * 2 * TB;
                     mbar_arrive_expect_tx(&full[st], 2 * TB);
@@ -544,8 +563,9 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
 #pragma unroll
                 for (int q = 0; q < kIP; ++q) {
                     const int j = j0 + q * NCT + ctid;
-                    iv[q] = j < cnt ? impg[t0 + j] : 0.f;
-                    pv[q] = (need_victim && j < cnt) ? posg[t0 + j] : 0;
+                    const bool fresh_slot = a.fused && t0 + j == n - 1;
+                    iv[q] = (j < cnt && !fresh_slot) ? impg[t0 + j] : 0.f;
+                    pv[q] = fresh_slot ? du.tnew : ((need_victim && j < cnt) ? posg[t0 + j] : 0);
                 }
 #pragma unroll
                 for (int q = 0; q < kIP; ++q) {
@@ -558,6 +578,7 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
                     for (int h = 0; h < G; ++h) inc += exp2f(srow[h] - mf[h]) * li_[h];
                     const float nw = iv[q] + inc;
                     v.imp[(int64_t)u * v.cap + slot] = nw;
+                    if (a.fused && slot == n - 1) v.pos[(int64_t)u * v.cap + slot] = du.tnew;
                     if (need_victim && pv[q] >= lo && pv[q] <= hi) {
                         const unsigned long long key =
                             ((unsigned long long)__float_as_uint(nw) << 32) | (unsigned long long)(~(uint32_t)pv[q]);
@@ -606,7 +627,44 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
                 } else {
                     *abort_flag = 1;
                 }
-                v.victim[u] = need_victim ? vs : -1;
+                vs = need_victim ? vs : -1;
+                wslot[0] = vs;   // for the fused evict below
+                if (!a.fused) {
+                    v.victim[u] = vs;
+                } else {
+                    const bool cut = a.evict && vs >= 0;
+                    v.victim[u] = cut ? -1 : vs;
+                    v.len[u] = cut ? n - 1 : n;
+                    v.next_pos[u] = du.tnew + 1;
+                }
+            }
+        }
+        named_bar_sync(1, NCT);
+        // fused evict: the appended token (last slot) moves into the victim's
+        // slot.  Its rows come from the caller's k/v (what the slot holds);
+        // its final importance was written by the CTA owning the slot before
+        // that CTA's release-arrive on the exchange barrier CTA 0 acquired.
+        if (a.fused && a.evict && c == 0 && warp == 0) {
+            const int32_t vs = wslot[0];
+            const int32_t sn = n - 1;
+            if (vs >= 0 && vs != sn) {
+                const int32_t pd = v.page_table[(int64_t)u * v.max_pages + (vs >> v.page_shift)];
+                if (pd >= 0 && pd < v.pool_pages) {
+                    const int64_t ui = (int64_t)u - (int64_t)a.layer0 * per_layer;
+                    uint8_t* dst = v.pool + (int64_t)pd * v.page_bytes + (int64_t)(vs & (v.page_tokens - 1)) * RB;
+                    for (int q = lane; q < 2 * CPR; q += 32) {
+                        const bool isv = q >= CPR;
+                        const uint4* src = reinterpret_cast<const uint4*>((isv ? a.new_v : a.new_k) + ui * RB);
+                        uint4* d4 = reinterpret_cast<uint4*>(dst + (isv ? (int64_t)v.page_tokens * RB : 0));
+                        d4[q - (isv ? CPR : 0)] = src[q - (isv ? CPR : 0)];
+                    }
+                } else if (lane == 0) {
+                    atomicOr(v.err, DEVERR_PAGE);
+                }
+                if (lane == 0) {
+                    v.imp[(int64_t)u * v.cap + vs] = __ldcg(&v.imp[(int64_t)u * v.cap + sn]);
+                    v.pos[(int64_t)u * v.cap + vs] = du.tnew;
+                }
             }
         }
         named_bar_sync(1, NCT);   // shared buffers of this unit are free for the next

@@ -118,6 +118,19 @@ hikv_status hikv_score_window(hikv_cache* cache, int32_t layer0, int32_t nlayers
 hikv_status hikv_decode_step(hikv_cache* cache, int32_t layer0, int32_t nlayers,
                              const void* q, void* out, hikv_stream_t stream);
 
+/* One whole decode step in one call: exactly hikv_append (one token per unit,
+ * k, v: [nlayers][batch][Hkv][1][d]) + hikv_decode_step (q, out as there)
+ * and, with evict != 0, hikv_evict -- same results.  When every unit's new
+ * slot already has its page and no unit needs more than one eviction (the
+ * steady state once a unit reached its budget) it is a single kernel launch:
+ * the appended rows enter the cache inside the attention kernel and the
+ * evicted slot is refilled with the new token there.  Otherwise it runs the
+ * three calls.  k and v must be 16-byte aligned (HIKV_ERR_INVALID_ARG
+ * otherwise).  Errors: as the three calls. */
+hikv_status hikv_decode_step_fused(hikv_cache* cache, int32_t layer0, int32_t nlayers,
+                                   const void* k, const void* v, const void* q, void* out,
+                                   int32_t evict, hikv_stream_t stream);
+
 /* Cut every unit of the range holding n > B_u tokens to exactly B_u:
  * keep sinks, recent window and the B_u - S - W highest-importance others
  * (ties keep the lower position), compact the survivors into slots
@@ -141,6 +154,12 @@ hikv_status hikv_gather_retained(hikv_cache* cache, int32_t layer0, int32_t nlay
  * lengths_host: [nlayers * batch * Hkv].  Errors: INVALID_ARG. */
 hikv_status hikv_get_lengths(const hikv_cache* cache, int32_t layer0, int32_t nlayers,
                              int32_t* lengths_host);
+
+/* Number of kernels launched on the caller's streams through this cache
+ * since it was created (every entry point counts what it enqueued; a call
+ * that returned an error before launching counts nothing).  Host-only, no
+ * synchronisation.  Returns -1 for a null cache. */
+int64_t hikv_kernel_launches(const hikv_cache* cache);
 
 /* Synchronise the device and report device-side errors recorded by the
  * kernels (a bounded wait that gave up, a page id out of range); clears them.

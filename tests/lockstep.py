@@ -133,7 +133,9 @@ class Lockstep:
         qs = np.ascontiguousarray(np.moveaxis(q, 3, 0))
         return ks, vs, qs
 
-    def decode(self, steps=None, compare_every=1):
+    def decode(self, steps=None, compare_every=1, fused=False):
+        """Run the decode steps; fused=True drives each step through the
+        single append+decode+evict call instead of the three calls."""
         w = self.w
         steps = w.steps if steps is None else steps
         ks, vs, qs = self._decode_inputs()
@@ -142,10 +144,13 @@ class Lockstep:
         for s in range(steps):
             evict_now = (s + 1) % w.evict_every == 0
             for ls in self._all():
-                ls.cache.append(dks[s], dvs[s])
-                ls.cache.decode_step(dqs[s], out)
-                if evict_now:
-                    ls.cache.evict()
+                if fused:
+                    ls.cache.step(dks[s], dvs[s], dqs[s], out, evict=evict_now)
+                else:
+                    ls.cache.append(dks[s], dvs[s])
+                    ls.cache.decode_step(dqs[s], out)
+                    if evict_now:
+                        ls.cache.evict()
                 for si, l in enumerate(ls.sample):
                     ls.ora.append(si, W.to_f32(ks[s, l:l + 1]), W.to_f32(vs[s, l:l + 1]))
                 ora_out = [ls.ora.decode(si, W.to_f32(qs[s, l:l + 1])) for si, l in enumerate(ls.sample)]

@@ -2,7 +2,8 @@
 
 The GPU runs every layer of each workload with all-layer calls (the launch
 configuration of the benchmark); the CPU oracle checks sampled layers in
-lockstep: retained sets after every eviction (near-ties < 1e-6 relative
+lockstep (the 70B workload through the fused single-launch step, the ragged
+one through both paths): retained sets after every eviction (near-ties < 1e-6 relative
 allowed, then resynced), importance, and the outputs of every step.
 """
 import pytest
@@ -18,11 +19,11 @@ def built():
     build_native()
 
 
-def _run(w, **kw):
+def _run(w, fused=False, **kw):
     from tests.lockstep import Lockstep
     ls = Lockstep(w, **kw)
     ls.prefill()
-    rep = ls.decode()
+    rep = ls.decode(fused=fused)
     print(f"{w.name}: evictions {rep.evictions_checked}, near-ties {rep.near_tie_swaps}, "
           f"max out err {rep.max_out_err:.4g}, max imp rel err {rep.max_imp_err_rel:.3g}")
     if ls.twin is not None:
@@ -39,11 +40,13 @@ def test_32layer_ctx32k_evict_every_16():
     assert rep.evictions_checked == 2 * 32 * (1 + 128 // 16)
 
 
-def test_headkv_dirichlet_ragged_budgets():
-    rep = _run(W.WORKLOADS[3], sample_layers=[5])
+@pytest.mark.parametrize("fused", [False, True], ids=["3calls", "fused"])
+def test_headkv_dirichlet_ragged_budgets(fused):
+    rep = _run(W.WORKLOADS[3], fused=fused, sample_layers=[5])
     assert rep.evictions_checked == 128 * (1 + 128)
 
 
 def test_llama3_70b_ctx128k_with_full_cache_twin():
-    rep = _run(W.WORKLOADS[4], sample_layers=[0, 79], full_twin_layers=[40])
+    # every step is the single append+decode+evict launch
+    rep = _run(W.WORKLOADS[4], fused=True, sample_layers=[0, 79], full_twin_layers=[40])
     assert rep.evictions_checked == 2 * 8 * (1 + 64)

@@ -30,22 +30,28 @@ def _ls(w, **kw):
     return Lockstep(w, **kw)
 
 
-def _run(w, **kw):
+def _run(w, fused=False, **kw):
     ls = _ls(w, **kw)
     ls.prefill()
-    rep = ls.decode()
+    rep = ls.decode(fused=fused)
     ls.cache.close()
     return rep
 
 
-def test_tiny_fp32_workload_full_lockstep():
-    rep = _run(W.WORKLOADS[0])
+# fused: each decode step is the single append+decode+evict call
+FUSED = pytest.mark.parametrize("fused", [False, True], ids=["3calls", "fused"])
+
+
+@FUSED
+def test_tiny_fp32_workload_full_lockstep(fused):
+    rep = _run(W.WORKLOADS[0], fused=fused)
     assert rep.evictions_checked == 2 * (1 + 64)
     assert rep.max_out_err <= 1.0
 
 
-def test_llama3_8b_layer_full_lockstep():
-    rep = _run(W.WORKLOADS[1])
+@FUSED
+def test_llama3_8b_layer_full_lockstep(fused):
+    rep = _run(W.WORKLOADS[1], fused=fused)
     assert rep.evictions_checked == 64 * (1 + 256)
     print("near-tie swaps", rep.near_tie_swaps, "max bf16 err", rep.max_out_err,
           "max imp rel err", rep.max_imp_err_rel)
@@ -54,9 +60,10 @@ def test_llama3_8b_layer_full_lockstep():
 SMALL = W.Workload(100, "small", 2, 2, 8, 2, 128, "bf16", 300, 40, 96, 4, 16, 1, "bernoulli5x3")
 
 
+@FUSED
 @pytest.mark.parametrize("cs", [1, 2, 4, 8, 16])
-def test_cluster_split_sizes(cs):
-    _run(SMALL, cs=cs)
+def test_cluster_split_sizes(cs, fused):
+    _run(SMALL, cs=cs, fused=fused)
 
 
 @pytest.mark.parametrize("kw", [
@@ -66,8 +73,9 @@ def test_cluster_split_sizes(cs):
     dict(sink=4, window=16, budget=20),
     dict(sink=1, window=5, budget=77),           # ragged tile tails
 ])
-def test_degenerate_sink_window(kw):
-    _run(SMALL.with_(**kw))
+@FUSED
+def test_degenerate_sink_window(kw, fused):
+    _run(SMALL.with_(**kw), fused=fused)
 
 
 @pytest.mark.parametrize("shape", [
@@ -76,22 +84,30 @@ def test_degenerate_sink_window(kw):
     dict(hq=8, hkv=2, d=128, dtype="f32"),
     dict(hq=8, hkv=2, d=64, dtype="bf16"),
 ])
-def test_group_sizes_and_dtypes(shape):
-    _run(SMALL.with_(**shape))
+@FUSED
+def test_group_sizes_and_dtypes(shape, fused):
+    _run(SMALL.with_(**shape), fused=fused)
 
 
-def test_evict_every_16_batched_select():
-    _run(SMALL.with_(evict_every=16, steps=48, budget=120, window=20))
+@FUSED
+def test_evict_every_16_batched_select(fused):
+    # fused: 15 single-launch steps without eviction, then 16 over budget,
+    # which the fused call hands to the three separate calls
+    _run(SMALL.with_(evict_every=16, steps=48, budget=120, window=20), fused=fused)
 
 
-def test_ragged_budgets():
+@FUSED
+def test_ragged_budgets(fused):
     b = np.array([40, 96, 17 + 16, 200], dtype=np.int32)
-    _run(SMALL.with_(sink=1, window=16), budgets=b)
+    _run(SMALL.with_(sink=1, window=16), budgets=b, fused=fused)
 
 
-def test_page_size_variants():
-    _run(SMALL, page_tokens=16)
-    _run(SMALL, page_tokens=256)
+@FUSED
+def test_page_size_variants(fused):
+    # 16-token pages: the cache grows a page every 16 steps before the
+    # budget is reached, steps the fused call runs as three calls
+    _run(SMALL, page_tokens=16, fused=fused)
+    _run(SMALL, page_tokens=256, fused=fused)
 
 
 def test_long_chunk_global_logits_path():
@@ -99,9 +115,11 @@ def test_long_chunk_global_logits_path():
     # exceed shared memory, so the kernel keeps them in the global buffer
     w = W.Workload(101, "long", 1, 1, 8, 1, 128, "bf16", 50000, 6, 60000, 4, 64, 1, "zipf1.1")
     _run(w)
+    _run(w, fused=True)
 
 
-def test_zero_keys_tie_rule_exact():
+@FUSED
+def test_zero_keys_tie_rule_exact(fused):
     """All-zero keys: uniform softmax, whole classes of tokens tie exactly; the
     GPU must keep the lowest positions, with no near-tie allowance."""
     from tests.lockstep import Lockstep
@@ -115,7 +133,7 @@ def test_zero_keys_tie_rule_exact():
     W.gen_kv = zero_keys
     try:
         ls.prefill()
-        ls.decode()
+        ls.decode(fused=fused)
     finally:
         W.gen_kv = orig
     assert ls.rep.near_tie_swaps == 0
@@ -144,5 +162,13 @@ def test_host_errors_leave_cache_usable():
     c.decode_step(q, out)
     c.evict()
     assert list(c.lengths()) == [16, 16]
+    k1 = torch.randn(1, 1, 2, 1, 64, device=dev)
+    with pytest.raises(hk.HikvError) as ei:
+        c.step(k1, k1.clone(), q, q)                # out aliases q
+    assert ei.value.status == hk.HIKV_ERR_INVALID_ARG
+    c.step(k1, k1.clone(), q, out)                  # one launch: append, attend, evict
+    assert list(c.lengths()) == [16, 16]
+    c.step(k1, k1.clone(), q, out, evict=False)
+    assert list(c.lengths()) == [17, 17]
     c.device_status()
     c.close()
