@@ -174,9 +174,6 @@ __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
 
 // order this thread's earlier generic-proxy global stores before its later
 // async-proxy (TMA) operations
-__device__ __forceinline__ void fence_proxy_async_global() {
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-}
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");

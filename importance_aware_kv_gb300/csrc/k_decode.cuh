@@ -53,7 +53,7 @@ constexpr int kDecMaxPg = 256;                   // page ids cached in shared me
 
 struct DecSmem {
     // byte offsets into dynamic shared memory, from a 1024-aligned base
-    uint32_t ring, bars, qraw, q, ps, red, xbuf, vbuf, small, pg, S, total;
+    uint32_t ring, bars, qraw, nrow, q, ps, red, xbuf, vbuf, small, pg, S, total;
     uint32_t xbuf_bytes;
 };
 
@@ -70,6 +70,8 @@ __host__ __device__ inline DecSmem dec_layout(bool smem_s, int chunk_cap) {
     off = (off + 127) & ~127u;
     L.qraw = off;                                 // q of the unit as stored, [2][G][D]
     off += 2 * G * D * sizeof(T);
+    L.nrow = off;                                 // fused step: the new K and V rows, [2][2][D]
+    off += 2 * 2 * RB;
     off = (off + 15) & ~15u;
     L.q = off;                                    // q * scale * log2 e, fp32 [G][D]
     off += G * D * 4;
@@ -81,8 +83,8 @@ __host__ __device__ inline DecSmem dec_layout(bool smem_s, int chunk_cap) {
     L.xbuf_bytes = (2 * kMaxCS * G + G * D + kMaxCS) * 4;
     L.xbuf = off;
     off += 2 * L.xbuf_bytes;
-    L.vbuf = off;                                 // [2] x (keys [kMaxCS] u64, slots [kMaxCS] i32)
-    off += 2 * kMaxCS * 12;
+    L.vbuf = off;                                 // [2] x (keys [kMaxCS] u64, slots [kMaxCS] i32, new imp f32)
+    off += 2 * (kMaxCS * 12 + 16);
     off = (off + 15) & ~15u;
     L.small = off;
     off += 2048;
@@ -166,6 +168,7 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
     unsigned long long* wkey = reinterpret_cast<unsigned long long*>(sm + 256);  // [NCW]
     int32_t* wslot = reinterpret_cast<int32_t*>(wkey + kDecNCW);                 // [NCW]
     volatile int32_t* abort_flag = wslot + kDecNCW;
+    float* new_imp_s = sm + 280;               // fused: the new token's final importance
     int32_t* pg_s = reinterpret_cast<int32_t*>(smem + L.pg);
     float* S_smem = reinterpret_cast<float*>(smem + L.S);
 
@@ -215,8 +218,13 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
                 // q of this unit into its half of the double buffer
                 if (!*abort_flag && mbar_wait_bounded(&qempty[qb], ((uint32_t)(k >> 1) & 1u) ^ 1u, v.err)) {
                     const int64_t qbase = (((int64_t)li * v.batch + b) * v.hq + (int64_t)g * G) * D;
-                    mbar_arrive_expect_tx(&qfull[qb], QB);
+                    mbar_arrive_expect_tx(&qfull[qb], QB + (a.fused ? 2 * RB : 0));
                     bulk_g2s(smem + L.qraw + qb * QB, a.q + qbase * ESZ, QB, &qfull[qb]);
+                    if (a.fused) {   // the appended token's rows, for the tile patch and the evict move
+                        const int64_t ui = (int64_t)du.u - (int64_t)a.layer0 * per_layer;
+                        bulk_g2s(smem + L.nrow + qb * 2 * RB, a.new_k + ui * RB, RB, &qfull[qb]);
+                        bulk_g2s(smem + L.nrow + qb * 2 * RB + RB, a.new_v + ui * RB, RB, &qfull[qb]);
+                    }
                 } else {
                     *abort_flag = 1;
                 }
@@ -254,21 +262,6 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
                         break;
                     }
                     if (pf > 0 && i + pf < nt) prefetch_tile(i + pf);
-                    const int32_t sn = du.n - 1;   // fused step: the appended token's slot
-                    if (a.fused && sn >= s0 && sn < s0 + kDecTR) {
-                        const int64_t ui = (int64_t)du.u - (int64_t)a.layer0 * per_layer;
-                        const uint4* ks = reinterpret_cast<const uint4*>(a.new_k + ui * RB);
-                        const uint4* vs = reinterpret_cast<const uint4*>(a.new_v + ui * RB);
-                        uint8_t* kd = v.pool + (int64_t)pg * v.page_bytes + (int64_t)(sn & (v.page_tokens - 1)) * RB;
-                        uint4* kd4 = reinterpret_cast<uint4*>(kd);
-                        uint4* vd4 = reinterpret_cast<uint4*>(kd + (int64_t)v.page_tokens * RB);
-#pragma unroll 4
-                        for (int q = 0; q < RB / 16; ++q) {
-                            kd4[q] = ks[q];
-                            vd4[q] = vs[q];
-                        }
-                        fence_proxy_async_global();   // the TMA below must see these rows
-                    }
                     const int32_t yk = pg * 2 * v.page_tokens + (s0 & (v.page_tokens - 1));
                     uint8_t* dst = ring + st * 2 * TB;
                     mbar_arrive_expect_tx(&full[st], 2 * TB);
@@ -328,8 +321,12 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
         float* m_recv = reinterpret_cast<float*>(smem + L.xbuf + xb * L.xbuf_bytes);   // [kMaxCS][G]
         float* l_recv = m_recv + kMaxCS * G;                                             // [kMaxCS][G]
         float* orecv = l_recv + kMaxCS * G;                                              // [CS][per]
-        unsigned long long* akey = reinterpret_cast<unsigned long long*>(smem + L.vbuf + xb * kMaxCS * 12);
+        unsigned long long* akey = reinterpret_cast<unsigned long long*>(smem + L.vbuf + xb * (kMaxCS * 12 + 16));
         int32_t* aslot = reinterpret_cast<int32_t*>(akey + kMaxCS);
+        float* aimp = reinterpret_cast<float*>(aslot + kMaxCS);     // final importance of the new token
+        const uint8_t* nrow = smem + L.nrow + xb * 2 * RB;           // fused: new K row, new V row
+        const int32_t sn = n - 1;                                    // fused: the new token's slot
+        const bool owns_new = a.fused && cnt > 0 && sn >= t0 && sn < t1;
         float* Sb = SMEM_S ? S_smem : a.logits + ((int64_t)u * v.cap) * G;
         const int32_t s_off = SMEM_S ? t0 : 0;   // S index of slot s = (s - s_off) * G
         const float* impg = v.imp + (int64_t)u * v.cap;
@@ -347,7 +344,6 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
             for (int i = ctid; i < G * D; i += NCT) q_s[i] = Elem<T>::to_f(qraw[i]) * a.qscale;
         }
         named_bar_sync(1, NCT);
-        if (ctid == 0) mbar_arrive(&qempty[xb]);
 
         float m_w[G], l_w[G];
         float2 o2[G][EPL / 2];
@@ -368,9 +364,26 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
                 break;
             }
             const int32_t s0 = (first_blk + i) * kDecTR;
-            const uint8_t* ktile = ring + st * 2 * TB;
-            const uint8_t* vtile = ktile + TB;
+            uint8_t* ktile = ring + st * 2 * TB;
+            uint8_t* vtile = ktile + TB;
             const int32_t lo_r = max(0, t0 - s0), hi_r = min(kDecTR, t1 - s0);   // valid rows [lo_r, hi_r)
+            if (owns_new && sn >= s0 && sn < s0 + kDecTR) {
+                // the pool slot of the appended token was loaded stale: put the
+                // new rows into the landed tile, and into the pool for later steps
+                const int r = sn - s0;
+                const Raw nk = *reinterpret_cast<const Raw*>(nrow + lane * LB);
+                const Raw nv = *reinterpret_cast<const Raw*>(nrow + RB + lane * LB);
+                *reinterpret_cast<Raw*>(ktile + swz(r, pv_chunk) + pv_in) = nk;
+                *reinterpret_cast<Raw*>(vtile + swz(r, pv_chunk) + pv_in) = nv;
+                fence_proxy_async_smem();   // the stage is refilled by TMA later
+                const int32_t pg = v.page_table[(int64_t)u * v.max_pages + (sn >> v.page_shift)];
+                if (pg >= 0 && pg < v.pool_pages) {
+                    uint8_t* kd = v.pool + (int64_t)pg * v.page_bytes + (int64_t)(sn & (v.page_tokens - 1)) * RB;
+                    *reinterpret_cast<Raw*>(kd + lane * LB) = nk;
+                    *reinterpret_cast<Raw*>(kd + (int64_t)v.page_tokens * RB + lane * LB) = nv;
+                }
+                __syncwarp();
+            }
 
             // ---- q.k: this lane's half row ----
             float2 acc[G];
@@ -578,7 +591,10 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
                     for (int h = 0; h < G; ++h) inc += exp2f(srow[h] - mf[h]) * li_[h];
                     const float nw = iv[q] + inc;
                     v.imp[(int64_t)u * v.cap + slot] = nw;
-                    if (a.fused && slot == n - 1) v.pos[(int64_t)u * v.cap + slot] = du.tnew;
+                    if (a.fused && slot == sn) {
+                        v.pos[(int64_t)u * v.cap + slot] = du.tnew;
+                        *new_imp_s = nw;
+                    }
                     if (need_victim && pv[q] >= lo && pv[q] <= hi) {
                         const unsigned long long key =
                             ((unsigned long long)__float_as_uint(nw) << 32) | (unsigned long long)(~(uint32_t)pv[q]);
@@ -614,6 +630,7 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
                 }
             dsmem_st_u64(dsmem_addr(&akey[c], 0u), kk);
             dsmem_st_s32(dsmem_addr(&aslot[c], 0u), sl);
+            if (owns_new) dsmem_st_f32(dsmem_addr(aimp, 0u), *new_imp_s);
             mbar_arrive_remote(dsmem_addr(&vbar[xb], 0u));
             if (c == 0) {
                 int32_t vs = -1;
@@ -641,33 +658,27 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
         }
         named_bar_sync(1, NCT);
         // fused evict: the appended token (last slot) moves into the victim's
-        // slot.  Its rows come from the caller's k/v (what the slot holds);
-        // its final importance was written by the CTA owning the slot before
-        // that CTA's release-arrive on the exchange barrier CTA 0 acquired.
+        // slot: rows from the stash, final importance from the exchange
         if (a.fused && a.evict && c == 0 && warp == 0) {
             const int32_t vs = wslot[0];
-            const int32_t sn = n - 1;
             if (vs >= 0 && vs != sn) {
                 const int32_t pd = v.page_table[(int64_t)u * v.max_pages + (vs >> v.page_shift)];
                 if (pd >= 0 && pd < v.pool_pages) {
-                    const int64_t ui = (int64_t)u - (int64_t)a.layer0 * per_layer;
-                    uint8_t* dst = v.pool + (int64_t)pd * v.page_bytes + (int64_t)(vs & (v.page_tokens - 1)) * RB;
-                    for (int q = lane; q < 2 * CPR; q += 32) {
-                        const bool isv = q >= CPR;
-                        const uint4* src = reinterpret_cast<const uint4*>((isv ? a.new_v : a.new_k) + ui * RB);
-                        uint4* d4 = reinterpret_cast<uint4*>(dst + (isv ? (int64_t)v.page_tokens * RB : 0));
-                        d4[q - (isv ? CPR : 0)] = src[q - (isv ? CPR : 0)];
-                    }
+                    uint8_t* kd = v.pool + (int64_t)pd * v.page_bytes + (int64_t)(vs & (v.page_tokens - 1)) * RB;
+                    *reinterpret_cast<Raw*>(kd + lane * LB) = *reinterpret_cast<const Raw*>(nrow + lane * LB);
+                    *reinterpret_cast<Raw*>(kd + (int64_t)v.page_tokens * RB + lane * LB) =
+                        *reinterpret_cast<const Raw*>(nrow + RB + lane * LB);
                 } else if (lane == 0) {
                     atomicOr(v.err, DEVERR_PAGE);
                 }
                 if (lane == 0) {
-                    v.imp[(int64_t)u * v.cap + vs] = __ldcg(&v.imp[(int64_t)u * v.cap + sn]);
+                    v.imp[(int64_t)u * v.cap + vs] = *aimp;
                     v.pos[(int64_t)u * v.cap + vs] = du.tnew;
                 }
             }
         }
         named_bar_sync(1, NCT);   // shared buffers of this unit are free for the next
+        if (ctid == 0) mbar_arrive(&qempty[xb]);
     }
     __syncwarp();
     cluster_sync_all();
