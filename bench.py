@@ -352,8 +352,8 @@ def bench_gpu(args):
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"{src} hbm_gbs", "traffic": traffic,
                      "bytes_per_launch": dec_bytes, "avg_launch_us": dec_avg_s * 1e6},
-        "e2e": {"value": Ke / (e2e_ms / 1e3), "unit": "steps/s", "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h), "steps": Ke},
+        "e2e": ({"value": Ke / (e2e_ms / 1e3), "unit": "steps/s", "h2d_bytes_per_step": int(h2d),
+                 "d2h_bytes_per_step": int(d2h), "steps": Ke} if Ke > 0 else None),
         "gpu_launches": launches,
         "three_call_path": three,
         "clocks": clocks,

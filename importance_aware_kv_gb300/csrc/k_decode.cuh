@@ -20,8 +20,9 @@
 //                   runs ahead into the next unit while the consumers finish
 //                   the current one.
 //   consumer warps  tile i of a unit belongs to warp i % 4, which keeps a
-//                   private online softmax (running max m_w, sum l_w,
-//                   unnormalised O_w):
+//                   private online softmax (reference m_w, sum l_w,
+//                   unnormalised O_w; m_w follows the running max lazily,
+//                   moving only when a logit exceeds it by 2^8):
 //     q.k   lane (row = lane % 16, half = lane / 16) owns half a K row: the
 //           swizzle makes those 16-byte reads conflict-free and lets q be a
 //           shared-memory broadcast; packed f32x2 FMAs, one shuffle joins the
@@ -48,6 +49,7 @@ namespace hikv {
 template <int G> struct DecWarps { static constexpr int value = 4; };
 template <int G> constexpr int dec_threads() { return (DecWarps<G>::value + 1) * 32; }
 constexpr int kDecTR = 16;                       // slots per tile
+constexpr float kDecLazy = 8.f;                  // softmax reference slack (log2 units)
 template <int G> struct DecStages { static constexpr int value = G >= 8 ? 6 : 8; };   // ring depth (tiles)
 constexpr int kDecMaxPg = 256;                   // page ids cached in shared memory
 
@@ -414,23 +416,35 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
                 t += __shfl_xor_sync(0xffffffffu, t, 16);
                 s[h] = rv ? t : -INFINITY;
             }
-            // ---- online softmax over this tile ----
-            float scl[G], p[G];
-            bool rescale = false;
+            // ---- online softmax over this tile, lazily rescaled: the
+            // reference m_w moves (to the tile max) only when a logit exceeds
+            // it by more than kDecLazy, so p <= 2^kDecLazy; row sums stay
+            // per lane until the unit's merge ----
+            bool big = false;
+#pragma unroll
+            for (int h = 0; h < G; ++h) big |= s[h] > m_w[h] + kDecLazy;   // invalid rows: -inf
+            if (__any_sync(0xffffffffu, big)) {
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    float mt = s[h];
+#pragma unroll
+                    for (int o = 8; o >= 1; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+                    const float mn = fmaxf(m_w[h], mt);
+                    const float scl = exp2f(m_w[h] - mn);   // 1 when unchanged, 0 from -inf
+                    m_w[h] = mn;
+                    l_w[h] *= scl;
+#pragma unroll
+                    for (int e = 0; e < EPL / 2; ++e) {
+                        o2[h][e].x *= scl;
+                        o2[h][e].y *= scl;
+                    }
+                }
+            }
+            float p[G];
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                float mt = s[h];
-#pragma unroll
-                for (int o = 8; o >= 1; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
-                const float mn = fmaxf(m_w[h], mt);
-                scl[h] = (mn == m_w[h]) ? 1.f : exp2f(m_w[h] - mn);
-                rescale |= (mn != m_w[h]);
-                m_w[h] = mn;
-                p[h] = rv ? exp2f(s[h] - mn) : 0.f;
-                float ls = p[h];
-#pragma unroll
-                for (int o = 8; o >= 1; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
-                l_w[h] = l_w[h] * scl[h] + ls;
+                p[h] = rv ? exp2f(s[h] - m_w[h]) : 0.f;
+                l_w[h] += p[h];   // this lane's row; both halves of a row hold the same p
             }
             if (qh == 0) {
 #pragma unroll
@@ -440,15 +454,6 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
 #pragma unroll
                     for (int h = 0; h < G; ++h) srow[h] = s[h];
                 }
-            }
-            if (rescale) {
-#pragma unroll
-                for (int h = 0; h < G; ++h)
-#pragma unroll
-                    for (int e = 0; e < EPL / 2; ++e) {
-                        o2[h][e].x *= scl[h];
-                        o2[h][e].y *= scl[h];
-                    }
             }
             __syncwarp();
             // ---- p.v over the tile's valid rows (unrolled; invalid rows skipped, their
@@ -484,6 +489,10 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
         gi_base += nt;
 
         // ---- CTA merge of the warp states ----
+#pragma unroll
+        for (int h = 0; h < G; ++h)   // sum of the per-lane row sums over the 16 rows
+#pragma unroll
+            for (int o = 8; o >= 1; o >>= 1) l_w[h] += __shfl_xor_sync(0xffffffffu, l_w[h], o);
         if (lane == 0) {
 #pragma unroll
             for (int h = 0; h < G; ++h) {
