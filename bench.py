@@ -189,6 +189,9 @@ def bench_reference(args):
 
 # --------------------------------------------------------------------------
 def bench_gpu(args):
+    def stage(msg):
+        if args.verbose:
+            print(f"[bench] {msg}", file=sys.stderr, flush=True)
     import torch
     import torch.distributed as dist
     import importance_aware_kv_gb300 as hk
@@ -206,6 +209,7 @@ def bench_gpu(args):
     budgets = W.budgets(w, seed)
     cache = hk.Cache(hk.CacheConfig(w.layers, w.batch, w.hq, w.hkv, w.d, w.dtype, w.sink, w.window,
                                     budgets, w.prompt + total_steps + 1))
+    stage("cache created")
     # ---- setup (untimed): prompt, window scoring, cut to budget ----
     k, v = W.gen_kv(w, 0, w.layers, 0, w.prompt, seed)
     cache.append(W.to_torch(k).to(dev), W.to_torch(v).to(dev))
@@ -225,10 +229,12 @@ def bench_gpu(args):
     def step(s):
         cache.step(dks[s], dvs[s], dqs[s], out, evict=True)
 
+    stage("setup done")
     for s in range(Wu):
         flush.fill_(float(s))
         step(s)
     torch.cuda.synchronize()
+    stage("warm-up done")
     # A short spin kernel before each timed step lets the host enqueue the
     # whole step before the GPU reaches it, so host launch overhead never
     # shows up inside the timed events (the flush and the spin are outside).
@@ -261,6 +267,7 @@ def bench_gpu(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         t_total = float(t.item())
 
+    stage("timed fused steps done")
     # ---- the same steps as three calls (append, decode_step, evict), for context ----
     K3 = args.three_call_steps
     ev3 = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(K3)]
@@ -284,6 +291,7 @@ def bench_gpu(args):
         three = {"steps": K3, "ms_per_step": sum(ms3) / K3, "steps_per_s": K3 / (sum(ms3) / 1e3),
                  "decode_kernel_us": 1e3 * sum(dec3) / K3, "launches_per_step": 3}
 
+    stage("three-call steps done")
     # ---- e2e through the C ABI with pinned host buffers ----
     hk_s = stream
     hk_k = torch.from_numpy(ks.view(np.int16)).pin_memory()
@@ -310,6 +318,7 @@ def bench_gpu(args):
         e_end.record(hk_s)
         e_end.synchronize()
         e2e_ms += e_start.elapsed_time(e_end)
+    stage("e2e steps done")
     h2d = (ks[0].nbytes + vs[0].nbytes + qs[0].nbytes)
     d2h = out_host.numel() * 2
     cache.device_status()
@@ -378,6 +387,7 @@ def main():
     ap.add_argument("--spin-us", type=float, default=60.0)
     ap.add_argument("--impl", default="hikv", choices=["hikv", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--verbose", action="store_true", help="stage markers on stderr")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -82,6 +82,7 @@ struct hikv_cache {
     int device = 0, sm_count = 0;
     size_t smem_optin = 0;
     int max_smem_chunk = 0;             // decode smem path limit (tokens per CTA)
+    int dec_occ = 2;                    // decode CTAs per SM
     View v{};
     int32_t* d_append_base = nullptr;
     float* d_logits = nullptr;          // long-chunk decode logits (may be null)
@@ -93,6 +94,7 @@ struct hikv_cache {
     int wchunks = 0;
     int32_t* d_order_all = nullptr;
     int32_t* d_order_layer = nullptr;
+    std::vector<int32_t> order_all, order_layer;   // host copies: units by budget, descending
     CUtensorMap tmap;                   // the pool as rows of d elements, 16 x 128-byte swizzled boxes
     std::vector<void*> allocs;
     // host mirror
@@ -196,8 +198,12 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
     int optin = 0;
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device);
     c->smem_optin = (size_t)optin;
-    // shared-memory logits path: chunks small enough for two CTAs per SM
-    c->max_smem_chunk = decode_max_smem_chunk(c->dtype, c->d, c->G, std::min<size_t>(c->smem_optin, 112 * 1024));
+    // shared-memory logits path: chunks small enough for the decode occupancy
+    // decode CTAs per SM, and the dynamic shared memory each may take at that
+    // occupancy (228 KB per SM, 1 KB of it reserved per CTA)
+    c->dec_occ = dec_occupancy(c->d * c->esz, c->G);
+    c->max_smem_chunk = decode_max_smem_chunk(
+        c->dtype, c->d, c->G, std::min<size_t>(c->smem_optin, (228 * 1024) / c->dec_occ - 1024));
 
     View& v = c->v;
     const int row_bytes = c->d * c->esz;
@@ -237,7 +243,7 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
     ALLOC(v.budget, U);
     ALLOC(v.free_stack, (size_t)c->pool_pages);
     ALLOC(v.free_top, 1);
-    ALLOC(v.err, 1);
+    ALLOC(v.err, 8);   // [0] error bits, [1..5] where the first bounded wait gave up
     ALLOC(c->d_append_base, U);
     ALLOC(c->d_cand, U * kMaxCS);
     ALLOC(c->d_cand_slot, U * kMaxCS);
@@ -278,7 +284,10 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
     // initial device state
     std::vector<int32_t> stack((size_t)c->pool_pages);
     std::iota(stack.begin(), stack.end(), 0);
-    std::vector<int32_t> order_all(U), order_layer(U);
+    std::vector<int32_t>& order_all = c->order_all;
+    std::vector<int32_t>& order_layer = c->order_layer;
+    order_all.resize(U);
+    order_layer.resize(U);
     std::iota(order_all.begin(), order_all.end(), 0);
     std::stable_sort(order_all.begin(), order_all.end(),
                      [&](int a, int b) { return c->budget_unit[a] > c->budget_unit[b]; });
@@ -298,7 +307,7 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
               cudaMemset(v.next_pos, 0, U * 4) == cudaSuccess &&
               cudaMemset(v.mapped, 0, U * 4) == cudaSuccess &&
               cudaMemset(v.victim, 0xFF, U * 4) == cudaSuccess &&
-              cudaMemset(v.err, 0, 4) == cudaSuccess &&
+              cudaMemset(v.err, 0, 32) == cudaSuccess &&
               cudaMemcpy(v.budget, c->budget_unit.data(), U * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
               cudaMemcpy(v.free_stack, stack.data(), stack.size() * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
               cudaMemcpy(v.free_top, &top, 4, cudaMemcpyHostToDevice) == cudaSuccess &&
@@ -428,15 +437,40 @@ hikv_status launch_decode_call(hikv_cache* c, int32_t layer0, int32_t nl, const 
         uni_b &= c->budget_unit[u] == c->budget_unit[u0];
         uni_np &= c->next_pos[u] == c->next_pos[u0];
     }
-    // CTAs per unit: as many as fit one wave at two CTAs per SM, then enough
-    // that a CTA's logits fit the shared memory of a two-per-SM CTA
+    // CTAs per unit (cluster size cs): the persistent clusters take the units
+    // in launch order, cluster j the j-th, (j + n_clusters)-th, ... -- so the
+    // first cluster, which gets the largest unit of every round, bounds the
+    // step.  Its work is modelled in tokens per CTA plus a fixed per-unit cost
+    // (exchanges, importance pass, victim) worth kUnitCostTokens tokens, a fit
+    // to the measured decode times; cs minimises it.  The logits of a chunk too
+    // large for shared memory go to the global buffer, when there is one.
+    const int32_t* ord = (nl == c->L) ? c->order_all.data() : c->order_layer.data() + u0;
+    const bool identity = uni_b;   // equal budgets: launch order is the identity
     int cs = 1;
     if (c->cs_override > 0) {
         cs = std::min(c->cs_override, kMaxCS);
     } else {
-        const int slots = 2 * c->sm_count;
-        cs = std::max(1, std::min(8, slots / std::max(1, nu)));
-        while (cs < kMaxCS && ceil_div(maxn, cs) > c->max_smem_chunk) ++cs;
+        constexpr int64_t kUnitCostTokens = 190;
+        const int slots = c->dec_occ * c->sm_count;
+        int64_t best = INT64_MAX;
+        for (int k = 1; k <= std::min(kMaxCS, maxn); ++k) {
+            const int ck = ceil_div(maxn, k);
+            const bool sp = ck <= c->max_smem_chunk;
+            if (!sp && !c->d_logits) continue;
+            const size_t smem = decode_smem_bytes(c->dtype, c->d, c->G, sp, sp ? ck : 0);
+            int ncl = std::max(1, std::min(nu, slots / k));
+            const int active = decode_active_clusters(c->dtype, c->d, c->G, sp, k, smem);
+            if (active > 0) ncl = std::min(ncl, active);
+            int64_t cost = 0;
+            for (int i = 0; i < nu; i += ncl) {
+                const int u = identity ? u0 + i : ord[i];
+                cost += ceil_div(c->len[u] + fused, k) + kUnitCostTokens;
+            }
+            if (cost < best) {
+                best = cost;
+                cs = k;
+            }
+        }
     }
     cs = std::min(cs, std::max(1, maxn));
     const int chunk = ceil_div(maxn, cs);
@@ -460,8 +494,8 @@ hikv_status launch_decode_call(hikv_cache* c, int32_t layer0, int32_t nl, const 
     a.uni_budget = uni_b ? c->budget_unit[u0] : -1;
     a.uni_next_pos = uni_np ? c->next_pos[u0] + fused : -1;
     a.identity_u0 = uni_b ? u0 : -1;   // equal budgets: launch order is the identity
-    // persistent clusters: at most one wave at two CTAs per SM
-    a.n_clusters = std::max(1, std::min(nu, (2 * c->sm_count) / cs));
+    // persistent clusters: at most one wave at the decode occupancy
+    a.n_clusters = std::max(1, std::min(nu, (c->dec_occ * c->sm_count) / cs));
     // small calls fit in L2: prefetch each CTA's tiles there ahead of the ring
     const int64_t call_bytes = (int64_t)nu * maxn * 2 * c->d * c->esz;
     a.prefetch_tiles = call_bytes <= (48ll << 20) ? 16 : 0;
@@ -603,15 +637,21 @@ hikv_status hikv_device_status(hikv_cache* c) {
     if (!c) return fail(HIKV_ERR_INVALID_ARG, "device_status: null cache");
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "device_status: synchronize");
-    uint32_t w = 0;
-    e = cudaMemcpy(&w, c->v.err, 4, cudaMemcpyDeviceToHost);
+    uint32_t w[8] = {};
+    e = cudaMemcpy(w, c->v.err, sizeof(w), cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e, "device_status: read");
-    if (w) {
-        cudaMemset(c->v.err, 0, 4);
+    if (w[0] || w[1]) {
+        cudaMemset(c->v.err, 0, sizeof(w));
         cudaDeviceSynchronize();
     }
-    if (w & DEVERR_TIMEOUT) return fail(HIKV_ERR_TIMEOUT, "device: a bounded wait gave up (bits 0x%x)", w);
-    if (w) return fail(HIKV_ERR_STATE, "device: inconsistent state recorded (bits 0x%x)", w);
+    if (w[0] & DEVERR_TIMEOUT) {
+        static const char* const sites[] = {"?", "producer q-free", "producer stage-free", "producer drain",
+                                            "consumer q", "consumer tile", "cluster exchange", "victim exchange"};
+        return fail(HIKV_ERR_TIMEOUT,
+                    "device: a bounded wait gave up (bits 0x%x; first: %s wait, cluster %u, CTA %u, index 0x%x, "
+                    "after %u us)", w[0], sites[w[1] < 8 ? w[1] : 0], w[2], w[3], w[4], w[5]);
+    }
+    if (w[0]) return fail(HIKV_ERR_STATE, "device: inconsistent state recorded (bits 0x%x)", w[0]);
     return HIKV_OK;
 }
 

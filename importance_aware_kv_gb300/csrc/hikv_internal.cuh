@@ -53,6 +53,21 @@ struct View {
 
 constexpr int kMaxCS = 16;   // most CTAs (cluster size) per unit in the decode kernel
 
+// Shape of the decode kernel for a K/V row of `row_bytes` and group size
+// `group`: CTAs resident per SM (its register cap and the host's grid sizing
+// follow it), consumer warps per CTA, and ring stages (tiles of 16 K + 16 V
+// rows).  Two CTAs of four consumer warps (three CTAs of three warps measured
+// slower on every workload).  Two stages per consumer warp: the stage count
+// must be a multiple of the consumer warps, so that the same warp consumes
+// successive fills of a stage -- a consumer waits on a stage by phase parity,
+// which is only sound when it has itself seen the stage's previous phase
+// complete.
+__host__ __device__ constexpr int dec_occupancy(int /*row_bytes*/, int /*group*/) { return 2; }
+__host__ __device__ constexpr int dec_consumer_warps(int /*row_bytes*/, int /*group*/) { return 4; }
+__host__ __device__ constexpr int dec_stages(int row_bytes, int group) {
+    return 2 * dec_consumer_warps(row_bytes, group);
+}
+
 __host__ __device__ inline int32_t ceil_div(int32_t a, int32_t b) { return (a + b - 1) / b; }
 
 // Address of the K (or V) row of slot s of unit u; nullptr if the page is bad.
@@ -138,13 +153,6 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
     return ok != 0;
 }
 
-__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity, uint32_t* err) {
-    for (uint32_t i = 0; i < (1u << 21); ++i) {
-        if (mbar_try_wait_cluster(bar, parity, 1000u)) return true;
-    }
-    atomicOr(err, DEVERR_TIMEOUT);
-    return false;
-}
 
 // Arrive on the mbarrier at shared::cluster address `addr` (possibly in
 // another CTA of the cluster), releasing this thread's prior writes -- and
@@ -157,13 +165,54 @@ __device__ __forceinline__ void prefetch_global_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
-// Bounded wait: gives up after 2^21 tries of at most ~1 us each (about two
-// seconds on a stalled barrier), records DEVERR_TIMEOUT and returns false.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t* err) {
-    for (uint32_t i = 0; i < (1u << 21); ++i) {
-        if (mbar_try_wait_hint(bar, parity, 1000u)) return true;
-    }
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Where the first bounded wait of a launch sequence gave up: err[1] = site
+// (a kWait* code), err[2] = blockIdx.y, err[3] = blockIdx.x, err[4] = a
+// site-specific index, err[5] = microseconds waited.
+enum : uint32_t {
+    kWaitQEmpty = 1, kWaitEmpty = 2, kWaitDrain = 3, kWaitQFull = 4, kWaitFull = 5, kWaitXchg = 6,
+    kWaitVictim = 7
+};
+__device__ __forceinline__ void record_timeout(uint32_t* err, uint32_t site, uint32_t extra, uint64_t waited_ns) {
     atomicOr(err, DEVERR_TIMEOUT);
+    if (atomicCAS(err + 1, 0u, site) == 0u) {
+        err[2] = blockIdx.y;
+        err[3] = blockIdx.x;
+        err[4] = extra;
+        const uint64_t us = waited_ns / 1000u;
+        err[5] = us > 0xffffffffull ? 0xffffffffu : (uint32_t)us;
+    }
+}
+
+// Bounded waits: give up after about two seconds (global timer; at most 2^24
+// tries of a ~1 us suspend each, should the timer not advance), record where
+// and return false.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t site,
+                                                  uint32_t extra) {
+    if (mbar_try_wait_hint(bar, parity, 1000u)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 0; i < (1u << 24); ++i) {
+        if (mbar_try_wait_hint(bar, parity, 1000u)) return true;
+        if ((i & 63u) == 63u && global_ns() - t0 > kWaitLimitNs) break;
+    }
+    record_timeout(err, site, extra, global_ns() - t0);
+    return false;
+}
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity, uint32_t* err,
+                                                          uint32_t site, uint32_t extra) {
+    if (mbar_try_wait_cluster(bar, parity, 1000u)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 0; i < (1u << 24); ++i) {
+        if (mbar_try_wait_cluster(bar, parity, 1000u)) return true;
+        if ((i & 63u) == 63u && global_ns() - t0 > kWaitLimitNs) break;
+    }
+    record_timeout(err, site, extra, global_ns() - t0);
     return false;
 }
 
@@ -171,9 +220,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
-
-// order this thread's earlier generic-proxy global stores before its later
-// async-proxy (TMA) operations
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
@@ -225,6 +271,14 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// the two halves of cluster_sync_all, for work between them (whole warps)
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // shared::cluster address of `p` in CTA `rank` of this cluster
@@ -367,6 +421,8 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmap, int dtyp
                           bool smem_path, size_t smem_bytes, cudaStream_t s);
 size_t decode_smem_bytes(int dtype, int d, int group, bool smem_path, int chunk_cap);
 int decode_max_smem_chunk(int dtype, int d, int group, size_t smem_limit);
+// clusters of `cs` decode CTAs of `smem_bytes` each that fit on the GPU at once
+int decode_active_clusters(int dtype, int d, int group, bool smem_path, int cs, size_t smem_bytes);
 
 struct EvictArgs {
     View v;

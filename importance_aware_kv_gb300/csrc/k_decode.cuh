@@ -43,14 +43,11 @@
 
 namespace hikv {
 
-// consumer warps per CTA (one more warp produces); with two ring stages per
-// warp each consumer's next tile lands while it computes the current one
-// (eight warps sharing the same ring, one stage each, measured slower)
-template <int G> struct DecWarps { static constexpr int value = 4; };
-template <int G> constexpr int dec_threads() { return (DecWarps<G>::value + 1) * 32; }
+// threads of a decode CTA: the consumer warps and one producer warp
+template <typename T, int D, int G>
+constexpr int dec_threads() { return (dec_consumer_warps(D * (int)sizeof(T), G) + 1) * 32; }
 constexpr int kDecTR = 16;                       // slots per tile
 constexpr float kDecLazy = 8.f;                  // softmax reference slack (log2 units)
-template <int G> struct DecStages { static constexpr int value = G >= 8 ? 6 : 8; };   // ring depth (tiles)
 constexpr int kDecMaxPg = 256;                   // page ids cached in shared memory
 
 struct DecSmem {
@@ -62,13 +59,13 @@ struct DecSmem {
 template <typename T, int D, int G>
 __host__ __device__ inline DecSmem dec_layout(bool smem_s, int chunk_cap) {
     constexpr uint32_t RB = D * sizeof(T);
-    constexpr int kDecNCW = DecWarps<G>::value;
+    constexpr int kDecNCW = dec_consumer_warps(RB, G);
     DecSmem L{};
     uint32_t off = 0;
     L.ring = off;                                 // K,V tiles
-    off += DecStages<G>::value * 2 * kDecTR * RB;
+    off += dec_stages(RB, G) * 2 * kDecTR * RB;
     L.bars = off;                                 // full, empty [NST]; qfull, qempty, xbar, vbar [2]
-    off += (2 * DecStages<G>::value + 8) * 8;
+    off += (2 * dec_stages(RB, G) + 8) * 8;
     off = (off + 127) & ~127u;
     L.qraw = off;                                 // q of the unit as stored, [2][G][D]
     off += 2 * G * D * sizeof(T);
@@ -77,8 +74,8 @@ __host__ __device__ inline DecSmem dec_layout(bool smem_s, int chunk_cap) {
     off = (off + 15) & ~15u;
     L.q = off;                                    // q * scale * log2 e, fp32 [G][D]
     off += G * D * 4;
-    L.ps = off;                                   // per-warp p of the tile, duplicated pairs [NCW][16][G][2]
-    off += kDecNCW * kDecTR * G * 8;
+    L.ps = off;                                   // per-warp p of the tile [NCW][16][G]
+    off += kDecNCW * kDecTR * G * 4;
     L.red = off;                                  // warp O partials [NCW][G][D]
     off += kDecNCW * G * D * 4;
     // exchange buffer per unit parity: m [kMaxCS][G], l [kMaxCS][G], O slices [G*D + kMaxCS]
@@ -104,6 +101,21 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
     return (uint32_t)((c >> 3) * (kDecTR * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
+// G consecutive floats (a row of p or logits, 4G-byte aligned), vectorised
+template <int G>
+__device__ __forceinline__ void store_group(float* dst, const float (&x)[G]) {
+    if constexpr (G % 4 == 0) {
+#pragma unroll
+        for (int h = 0; h < G; h += 4)
+            *reinterpret_cast<float4*>(dst + h) = make_float4(x[h], x[h + 1], x[h + 2], x[h + 3]);
+    } else if constexpr (G == 2) {
+        *reinterpret_cast<float2*>(dst) = make_float2(x[0], x[1]);
+    } else {
+#pragma unroll
+        for (int h = 0; h < G; ++h) dst[h] = x[h];
+    }
+}
+
 struct DecUnit {
     int32_t u, n, Bu, tnew;
 };
@@ -122,10 +134,10 @@ __device__ __forceinline__ DecUnit dec_unit(const DecodeArgs& a, int32_t idx) {
 }
 
 template <typename T, int D, int G, bool SMEM_S>
-__global__ void __launch_bounds__(dec_threads<G>(), 2)
+__global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * sizeof(T), G))
     k_decode(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap) {
-    constexpr int kDecNCW = DecWarps<G>::value;
     constexpr int ESZ = (int)sizeof(T);
+    constexpr int kDecNCW = dec_consumer_warps(D * ESZ, G);
     constexpr int RB = D * ESZ;              // row bytes: 128, 256 or 512
     constexpr int NBOX = RB / 128;           // 128-byte TMA boxes per row
     constexpr int TB = kDecTR * RB;          // K (or V) tile bytes
@@ -136,7 +148,8 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
     constexpr int LB = EPL * ESZ;            // p.v: bytes per lane
     constexpr int NCT = kDecNCW * 32;        // consumer threads
     constexpr uint32_t QB = G * D * ESZ;     // bytes of one unit's q
-    constexpr int kDecStages = DecStages<G>::value;
+    constexpr int kDecStages = dec_stages(RB, G);
+    static_assert(kDecStages % kDecNCW == 0, "each stage must always be consumed by the same warp");
     static_assert(EPL % 2 == 0 && EPC % 2 == 0, "pairs");
     using Raw = typename RawVec<LB>::type;
 
@@ -155,10 +168,11 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
     uint64_t* xbar = qempty + 2;              // [2]
     uint64_t* vbar = xbar + 2;                // [2]
     float* q_s = reinterpret_cast<float*>(smem + L.q);
-    float2* ps_all = reinterpret_cast<float2*>(smem + L.ps);
+    float* ps_all = reinterpret_cast<float*>(smem + L.ps);
     float* red = reinterpret_cast<float*>(smem + L.red);
     float* sm = reinterpret_cast<float*>(smem + L.small);
     static_assert(kDecNCW * G <= 32, "warp state arrays");
+    static_assert(kMaxCS * G <= NCT, "one consumer thread per (CTA, head) of the exchange");
     float* mw_s = sm;                          // [NCW][G]     (32)
     float* lw_s = sm + 32;                     // [NCW][G]     (32)
     float* wsc = sm + 64;                      // [NCW][G]     (32)
@@ -177,6 +191,17 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
     const int32_t c = (int32_t)cluster_ctarank();
     const int32_t CS = (int32_t)cluster_nctarank();
 
+    // producer: the first unit's page ids, loaded while the barriers are set up
+    int32_t pre_pg = -1;
+    if (warp == kDecNCW && (int32_t)blockIdx.y < a.n_units) {
+        const DecUnit du = dec_unit(a, blockIdx.y);
+        const int32_t chunk = ceil_div(du.n, CS);
+        const int32_t t0 = min(du.n, c * chunk), t1 = min(du.n, t0 + chunk);
+        const int32_t pg0 = t0 >> v.page_shift;
+        const int32_t npg = t1 > t0 ? ((t1 - 1) >> v.page_shift) - pg0 + 1 : 0;
+        if (lane < npg) pre_pg = v.page_table[(int64_t)du.u * v.max_pages + pg0 + lane];
+    }
+
     if (tid == 0) {
         for (int s = 0; s < kDecStages; ++s) {
             mbar_init(&full[s], 1);
@@ -192,8 +217,11 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
         fence_mbar_init();
     }
     __syncthreads();
-    // every CTA's barriers must be initialised before any partner arrives on them
-    cluster_sync_all();
+    // every CTA's barriers must be initialised before any partner arrives on
+    // them: arrive here, wait before this CTA's first remote access (the
+    // CTA-local ring starts at once)
+    cluster_arrive();
+    bool cluster_ready = false;
 
     if (warp == kDecNCW) {
         // ======================= producer =======================
@@ -218,7 +246,7 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
             const int qb = k & 1;
             if (lane == 0) {
                 // q of this unit into its half of the double buffer
-                if (!*abort_flag && mbar_wait_bounded(&qempty[qb], ((uint32_t)(k >> 1) & 1u) ^ 1u, v.err)) {
+                if (!*abort_flag && mbar_wait_bounded(&qempty[qb], ((uint32_t)(k >> 1) & 1u) ^ 1u, v.err, kWaitQEmpty, (uint32_t)k)) {
                     const int64_t qbase = (((int64_t)li * v.batch + b) * v.hq + (int64_t)g * G) * D;
                     mbar_arrive_expect_tx(&qfull[qb], QB + (a.fused ? 2 * RB : 0));
                     bulk_g2s(smem + L.qraw + qb * QB, a.q + qbase * ESZ, QB, &qfull[qb]);
@@ -231,7 +259,7 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
                     *abort_flag = 1;
                 }
             }
-            for (int j = lane; j < min(npg, kDecMaxPg); j += 32) pg_s[j] = ptab[pg0 + j];
+            for (int j = lane; j < min(npg, kDecMaxPg); j += 32) pg_s[j] = (k == 0 && j < 32) ? pre_pg : ptab[pg0 + j];
             __syncwarp();
             auto page_of = [&](int32_t s0) -> int32_t {
                 const int32_t pk = (s0 >> v.page_shift) - pg0;
@@ -251,7 +279,8 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
                 for (int i = 0; i < nt; ++i, ++gi) {
                     if (*abort_flag) break;
                     const int st = gi % kDecStages;
-                    if (!mbar_wait_bounded(&empty[st], ((uint32_t)(gi / kDecStages) & 1u) ^ 1u, v.err)) {
+                    if (!mbar_wait_bounded(&empty[st], ((uint32_t)(gi / kDecStages) & 1u) ^ 1u, v.err, kWaitEmpty,
+                                           (uint32_t)gi)) {
                         *abort_flag = 1;
                         break;
                     }
@@ -281,16 +310,17 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
         if (lane == 0 && *abort_flag) {
             // let copies already in flight land before the CTA can exit
             for (int j = max(0, gi - kDecStages); j < gi; ++j)
-                mbar_wait_bounded(&full[j % kDecStages], (uint32_t)(j / kDecStages) & 1u, v.err);
+                mbar_wait_bounded(&full[j % kDecStages], (uint32_t)(j / kDecStages) & 1u, v.err, kWaitDrain, (uint32_t)j);
         }
         __syncwarp();
+        cluster_wait();
         cluster_sync_all();
         return;
     }
 
     // ======================= consumers =======================
-    const int ctid = tid;  // 0..127
-    float2* ps = ps_all + warp * (kDecTR * G);     // [16][G] duplicated p pairs
+    const int ctid = tid;  // consumer thread 0 .. NCT-1
+    float* ps = ps_all + warp * (kDecTR * G);      // [16][G] p of the tile
     const int qr = lane & 15;           // q.k: tile row of this lane
     const int qh = lane >> 4;           // q.k: half of the row
     const int pv_chunk = (lane * LB) >> 4, pv_in = (lane * LB) & 15;
@@ -340,7 +370,7 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
             prefetch_global_l2(posg + t0 + j);
         }
         // q of this unit
-        if (*abort_flag || !mbar_wait_bounded(&qfull[xb], xpar, v.err)) *abort_flag = 1;
+        if (*abort_flag || !mbar_wait_bounded(&qfull[xb], xpar, v.err, kWaitQFull, (uint32_t)k)) *abort_flag = 1;
         {
             const T* qraw = reinterpret_cast<const T*>(smem + L.qraw + xb * QB);
             for (int i = ctid; i < G * D; i += NCT) q_s[i] = Elem<T>::to_f(qraw[i]) * a.qscale;
@@ -361,7 +391,8 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
             if (*abort_flag) break;
             const int gi = gi_base + i;
             const int st = gi % kDecStages;
-            if (!mbar_wait_bounded(&full[st], (uint32_t)(gi / kDecStages) & 1u, v.err)) {
+            if (!mbar_wait_bounded(&full[st], (uint32_t)(gi / kDecStages) & 1u, v.err, kWaitFull,
+                                   (uint32_t)(gi | (warp << 24)))) {
                 *abort_flag = 1;
                 break;
             }
@@ -393,7 +424,7 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
             for (int h = 0; h < G; ++h) acc[h] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int j = 0; j < CPL; ++j) {
-                const int cidx = qh * CPL + j;
+                const int cidx = 2 * j + qh;   // halves interleave: their q reads fall in different banks
                 const uint4 raw = *reinterpret_cast<const uint4*>(ktile + swz(qr, cidx));
                 float x[EPC];
                 Widen<T, EPC>::run(raw, x);
@@ -447,13 +478,8 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
                 l_w[h] += p[h];   // this lane's row; both halves of a row hold the same p
             }
             if (qh == 0) {
-#pragma unroll
-                for (int h = 0; h < G; ++h) ps[qr * G + h] = make_float2(p[h], p[h]);
-                if (rv) {
-                    float* srow = Sb + (int64_t)(s0 + qr - s_off) * G;
-#pragma unroll
-                    for (int h = 0; h < G; ++h) srow[h] = s[h];
-                }
+                store_group<G>(ps + qr * G, p);
+                if (rv) store_group<G>(Sb + (int64_t)(s0 + qr - s_off) * G, s);
             }
             __syncwarp();
             // ---- p.v over the tile's valid rows (unrolled; invalid rows skipped, their
@@ -464,17 +490,24 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
                 const Raw raw = *reinterpret_cast<const Raw*>(vtile + swz(r, pv_chunk) + pv_in);
                 float x[EPL];
                 Widen<T, EPL>::run(raw, x);
-                const float2* pr = ps + r * G;
+                const float* pr = ps + r * G;
                 float2 pp[G];
-                if constexpr (G >= 2) {
+                if constexpr (G % 4 == 0) {
 #pragma unroll
-                    for (int h = 0; h < G; h += 2) {
+                    for (int h = 0; h < G; h += 4) {
                         const float4 t4 = *reinterpret_cast<const float4*>(pr + h);
-                        pp[h] = make_float2(t4.x, t4.y);
-                        pp[h + 1] = make_float2(t4.z, t4.w);
+                        pp[h] = make_float2(t4.x, t4.x);
+                        pp[h + 1] = make_float2(t4.y, t4.y);
+                        pp[h + 2] = make_float2(t4.z, t4.z);
+                        pp[h + 3] = make_float2(t4.w, t4.w);
                     }
+                } else if constexpr (G == 2) {
+                    const float2 t2 = *reinterpret_cast<const float2*>(pr);
+                    pp[0] = make_float2(t2.x, t2.x);
+                    pp[1] = make_float2(t2.y, t2.y);
                 } else {
-                    pp[0] = pr[0];
+#pragma unroll
+                    for (int h = 0; h < G; ++h) pp[h] = make_float2(pr[h], pr[h]);
                 }
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
@@ -520,6 +553,10 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
             l_c[ctid] = l;
         }
         named_bar_sync(1, NCT);
+        if (!cluster_ready) {   // partners' barriers are initialised from here on
+            cluster_wait();
+            cluster_ready = true;
+        }
         // store (m_c, l_c) into every CTA of the cluster, O_c slices into their owners
         if (ctid < CS * G) {
             const int cc = ctid / G, h = ctid % G;
@@ -536,7 +573,7 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
         }
         named_bar_sync(1, NCT);   // every remote store of this CTA is issued
         if (ctid < CS) mbar_arrive_remote(dsmem_addr(&xbar[xb], (uint32_t)ctid));
-        if (*abort_flag || !mbar_wait_cluster_bounded(&xbar[xb], xpar, v.err)) *abort_flag = 1;
+        if (*abort_flag || !mbar_wait_cluster_bounded(&xbar[xb], xpar, v.err, kWaitXchg, (uint32_t)k)) *abort_flag = 1;
 
         if (ctid < G) {
             float m = -INFINITY;
@@ -643,7 +680,7 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
             mbar_arrive_remote(dsmem_addr(&vbar[xb], 0u));
             if (c == 0) {
                 int32_t vs = -1;
-                if (!*abort_flag && mbar_wait_cluster_bounded(&vbar[xb], xpar, v.err)) {
+                if (!*abort_flag && mbar_wait_cluster_bounded(&vbar[xb], xpar, v.err, kWaitVictim, (uint32_t)k)) {
                     unsigned long long best = ~0ull;
                     for (int cc = 0; cc < CS; ++cc)
                         if (akey[cc] < best) {
@@ -690,11 +727,12 @@ __global__ void __launch_bounds__(dec_threads<G>(), 2)
         if (ctid == 0) mbar_arrive(&qempty[xb]);
     }
     __syncwarp();
+    if (!cluster_ready) cluster_wait();
     cluster_sync_all();
 }
 
 template <typename T, int D, int G, bool SM>
-cudaError_t decode_launch_one(const DecodeArgs& a, const CUtensorMap& tmap, size_t smem, cudaStream_t s) {
+cudaError_t decode_prepare(size_t smem) {
     auto kern = k_decode<T, D, G, SM>;
     static size_t smem_set = 0;  // largest dynamic smem opted into so far
     if (smem > smem_set) {
@@ -704,37 +742,59 @@ cudaError_t decode_launch_one(const DecodeArgs& a, const CUtensorMap& tmap, size
         if (e != cudaSuccess) return e;
         smem_set = smem;
     }
+    return cudaSuccess;
+}
+
+template <typename T, int D, int G>
+cudaLaunchConfig_t decode_config(int cs, int n_clusters, size_t smem, cudaStream_t s, cudaLaunchAttribute* attr) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)a.cs, (unsigned)a.n_clusters, 1);
-    cfg.blockDim = dim3(dec_threads<G>(), 1, 1);
+    cfg.gridDim = dim3((unsigned)cs, (unsigned)n_clusters, 1);
+    cfg.blockDim = dim3(dec_threads<T, D, G>(), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)a.cs;
+    attr[0].val.clusterDim.x = (unsigned)cs;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    // The clusters are persistent: launch no more than can be resident at
-    // once (clusters must fit in one GPC each), or the surplus would run as a
-    // second wave after the others had finished all their units.
+    return cfg;
+}
+
+// Clusters of `cs` CTAs with `smem` bytes each that can be resident at once
+// (clusters must fit in one GPC each); cached per (cs, smem).
+template <typename T, int D, int G, bool SM>
+int decode_active_clusters(int cs, size_t smem) {
     static int cached_cs[kMaxCS + 1] = {};
     static size_t cached_smem[kMaxCS + 1] = {};
     static int cached_active[kMaxCS + 1] = {};
-    const int csi = a.cs <= kMaxCS ? a.cs : kMaxCS;
-    if (cached_cs[csi] != a.cs || cached_smem[csi] != smem) {
+    const int csi = cs <= kMaxCS ? cs : kMaxCS;
+    if (cached_cs[csi] != cs || cached_smem[csi] != smem) {
+        if (decode_prepare<T, D, G, SM>(smem) != cudaSuccess) return 0;
+        cudaLaunchAttribute attr[1];
+        cudaLaunchConfig_t cfg = decode_config<T, D, G>(cs, 1, smem, nullptr, attr);
         int active = 0;
-        cudaError_t e = cudaOccupancyMaxActiveClusters(&active, kern, &cfg);
-        if (e != cudaSuccess) return e;
-        cached_cs[csi] = a.cs;
+        if (cudaOccupancyMaxActiveClusters(&active, k_decode<T, D, G, SM>, &cfg) != cudaSuccess) active = 0;
+        cached_cs[csi] = cs;
         cached_smem[csi] = smem;
         cached_active[csi] = active;
     }
+    return cached_active[csi];
+}
+
+template <typename T, int D, int G, bool SM>
+cudaError_t decode_launch_one(const DecodeArgs& a, const CUtensorMap& tmap, size_t smem, cudaStream_t s) {
+    cudaError_t e = decode_prepare<T, D, G, SM>(smem);
+    if (e != cudaSuccess) return e;
+    // The clusters are persistent: launch no more than can be resident at
+    // once, or the surplus would run as a second wave after the others had
+    // finished all their units.
     DecodeArgs b = a;
-    if (cached_active[csi] > 0 && b.n_clusters > cached_active[csi]) b.n_clusters = cached_active[csi];
-    cfg.gridDim = dim3((unsigned)b.cs, (unsigned)b.n_clusters, 1);
-    return cudaLaunchKernelEx(&cfg, kern, b, tmap);
+    const int active = decode_active_clusters<T, D, G, SM>(a.cs, smem);
+    if (active > 0 && b.n_clusters > active) b.n_clusters = active;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = decode_config<T, D, G>(b.cs, b.n_clusters, smem, s, attr);
+    return cudaLaunchKernelEx(&cfg, k_decode<T, D, G, SM>, b, tmap);
 }
 
 template <typename T, int D, bool SM>
@@ -746,6 +806,17 @@ cudaError_t decode_launch_g(const DecodeArgs& a, const CUtensorMap& tmap, int gr
         case 4: return decode_launch_one<T, D, 4, SM>(a, tmap, smem, s);
         case 8: return decode_launch_one<T, D, 8, SM>(a, tmap, smem, s);
         default: return cudaErrorInvalidValue;
+    }
+}
+
+template <typename T, int D, bool SM>
+int decode_active_g(int group, int cs, size_t smem) {
+    switch (group) {
+        case 1: return decode_active_clusters<T, D, 1, SM>(cs, smem);
+        case 2: return decode_active_clusters<T, D, 2, SM>(cs, smem);
+        case 4: return decode_active_clusters<T, D, 4, SM>(cs, smem);
+        case 8: return decode_active_clusters<T, D, 8, SM>(cs, smem);
+        default: return 0;
     }
 }
 
@@ -771,5 +842,9 @@ size_t decode_smem_t(int group, bool smem_path, int chunk_cap) {
     }                                                                                               \
     size_t decode_smem_##NAME(int group, bool smem_path, int chunk_cap) {                           \
         return decode_smem_t<T, D>(group, smem_path, chunk_cap);                                    \
+    }                                                                                               \
+    int decode_active_##NAME(int group, bool smem_path, int cs, size_t smem) {                      \
+        return smem_path ? decode_active_g<T, D, true>(group, cs, smem)                             \
+                         : decode_active_g<T, D, false>(group, cs, smem);                           \
     }                                                                                               \
     }

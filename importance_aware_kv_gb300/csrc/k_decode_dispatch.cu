@@ -5,7 +5,8 @@ namespace hikv {
 
 #define HIKV_DECL(NAME)                                                                            \
     cudaError_t decode_launch_##NAME(const DecodeArgs&, const CUtensorMap&, int, bool, size_t, cudaStream_t); \
-    size_t decode_smem_##NAME(int, bool, int);
+    size_t decode_smem_##NAME(int, bool, int);                                                     \
+    int decode_active_##NAME(int, bool, int, size_t);
 HIKV_DECL(f32_64)
 HIKV_DECL(f32_128)
 HIKV_DECL(bf16_64)
@@ -26,6 +27,14 @@ size_t decode_smem_bytes(int dtype, int d, int group, bool smem_path, int chunk_
     if (dtype == 0 && d == 128) return decode_smem_f32_128(group, smem_path, chunk_cap);
     if (dtype == 1 && d == 64) return decode_smem_bf16_64(group, smem_path, chunk_cap);
     if (dtype == 1 && d == 128) return decode_smem_bf16_128(group, smem_path, chunk_cap);
+    return 0;
+}
+
+int decode_active_clusters(int dtype, int d, int group, bool smem_path, int cs, size_t smem_bytes) {
+    if (dtype == 0 && d == 64) return decode_active_f32_64(group, smem_path, cs, smem_bytes);
+    if (dtype == 0 && d == 128) return decode_active_f32_128(group, smem_path, cs, smem_bytes);
+    if (dtype == 1 && d == 64) return decode_active_bf16_64(group, smem_path, cs, smem_bytes);
+    if (dtype == 1 && d == 128) return decode_active_bf16_128(group, smem_path, cs, smem_bytes);
     return 0;
 }
 
