@@ -521,6 +521,22 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
         }
         gi_base += nt;
 
+        // the importance pass's first loads, issued now so that they land
+        // during the merge and the cluster exchange
+        constexpr int kIP = 8;
+        float iv[kIP];
+        int32_t pv[kIP];
+        auto load_imp = [&](int j0) {
+#pragma unroll
+            for (int q = 0; q < kIP; ++q) {
+                const int j = j0 + q * NCT + ctid;
+                const bool fresh_slot = a.fused && t0 + j == sn;   // the new token: importance 0
+                iv[q] = (j < cnt && !fresh_slot) ? impg[t0 + j] : 0.f;
+                pv[q] = fresh_slot ? du.tnew : ((need_victim && j < cnt) ? posg[t0 + j] : 0);
+            }
+        };
+        load_imp(0);
+
         // ---- CTA merge of the warp states ----
 #pragma unroll
         for (int h = 0; h < G; ++h)   // sum of the per-lane row sums over the 16 rows
@@ -614,18 +630,10 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                 li_[h] = linv[h];
             }
             const int32_t lo = v.sink, hi = du.tnew - v.window;
-            // the loads of this pass are issued together (one L2 round trip), then used
-            constexpr int kIP = 8;
+            // the loads of each batch are issued together (one L2 round trip); the
+            // first batch's were issued before the exchanges
             for (int j0 = 0; j0 < cnt; j0 += kIP * NCT) {
-                float iv[kIP];
-                int32_t pv[kIP];
-#pragma unroll
-                for (int q = 0; q < kIP; ++q) {
-                    const int j = j0 + q * NCT + ctid;
-                    const bool fresh_slot = a.fused && t0 + j == n - 1;
-                    iv[q] = (j < cnt && !fresh_slot) ? impg[t0 + j] : 0.f;
-                    pv[q] = fresh_slot ? du.tnew : ((need_victim && j < cnt) ? posg[t0 + j] : 0);
-                }
+                if (j0 > 0) load_imp(j0);
 #pragma unroll
                 for (int q = 0; q < kIP; ++q) {
                     const int j = j0 + q * NCT + ctid;
