@@ -61,6 +61,27 @@ def dist_env():
     return rank, world, local
 
 
+def rank_seed(w, rank: int) -> int:
+    """Seed of a rank's inputs: every rank decodes its own batch of units."""
+    return w.index + 1000 * rank
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of the ranks' values (the job ends with its slowest rank)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, steps: int, t_max: float) -> float:
+    """Steps/s of the whole job: every rank ran `steps` steps of its own units."""
+    return world * steps / t_max
+
+
 class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -125,46 +146,70 @@ def gpu_id_for(dev_index: int) -> str:
 
 
 # --------------------------------------------------------------------------
-def step_bytes(w, n: int):
-    """Algorithmic bytes of one decode step of one unit holding n tokens during
-    attention: K/V rows, importance read+write, positions, q in, out, plus the
-    appended row (read once from the caller's buffer, written into the pool)."""
+def step_bytes(w, n):
+    """Algorithmic bytes of one decode step of units holding n tokens (array or
+    scalar) during attention: K/V rows, importance read+write, positions, q in,
+    out, plus the appended row (read once from the caller's buffer, written
+    into the pool).  Returns the total over the units given."""
+    n = np.asarray(n, dtype=np.int64)
     e = w.elem_bytes
-    kv = 2 * n * w.d * e
-    meta = 12 * n
-    qo = 2 * w.group * w.d * e
-    app = 2 * w.d * e
-    return kv, meta, qo, app
+    per_unit = 2 * n * w.d * e + 12 * n + 2 * w.group * w.d * e + 2 * w.d * e
+    return int(per_unit.sum())
 
 
-def run_cpu_oracle(w, seed, steps, warmup, budget_s=20.0):
-    """Time the oracle's decode loop (append -> decode -> evict, every unit)."""
+def layer_chunk(w, max_bytes=2e9):
+    """Layers per prefill chunk: at most ~2 GB of prompt K/V at a time."""
+    import workloads as W
+    per_layer = W.kv_bytes(w.batch, w.prompt, 1, w.hkv, w.d, w.elem_bytes)
+    return max(1, min(w.layers, int(max_bytes // max(1, per_layer))))
+
+
+def run_cpu_oracle(w, seed, steps, warmup, budget_s=20.0, layers=None):
+    """Time the oracle's decode loop (append -> decode -> evict when due) on the
+    given layers (default all) and scale to whole-workload steps/s: a step of
+    the workload needs every layer, so sampled rate x (sampled / all layers).
+    Returns (steps/s of the whole workload, threads, steps timed, sample text)."""
     import oracle
     import workloads as W
     threads = os.cpu_count() or 1
-    O = oracle.Oracle(w.layers, w.batch, w.hq, w.hkv, w.d, w.sink, w.window, W.budgets(w, seed),
+    layers = list(range(w.layers)) if layers is None else list(layers)
+    b_all = W.budgets(w, seed)
+    bs = np.concatenate([b_all[l * w.hkv:(l + 1) * w.hkv] for l in layers])
+    O = oracle.Oracle(len(layers), w.batch, w.hq, w.hkv, w.d, w.sink, w.window, bs,
                       out_bf16=(w.dtype == "bf16"), threads=threads)
-    k, v = W.gen_kv(w, 0, w.layers, 0, w.prompt, seed)
-    O.append(0, W.to_f32(k), W.to_f32(v))
-    del k, v
-    O.score_window(0, W.to_f32(W.gen_q(w, 0, w.layers, w.prompt - w.nq, w.nq, seed)))
-    O.evict(0, w.layers)
+    for si, l in enumerate(layers):
+        k, v = W.gen_kv(w, l, 1, 0, w.prompt, seed)
+        O.append(si, W.to_f32(k), W.to_f32(v))
+        del k, v
+        O.score_window(si, W.to_f32(W.gen_q(w, l, 1, w.prompt - w.nq, w.nq, seed)))
+    O.evict(0, len(layers))
     total = warmup + steps
-    ks, vs = W.gen_kv(w, 0, w.layers, w.prompt, total, seed)
-    qs = W.gen_q(w, 0, w.layers, w.prompt, total, seed)
+    ks = [W.gen_kv(w, l, 1, w.prompt, total, seed) for l in layers]
+    qs = [W.gen_q(w, l, 1, w.prompt, total, seed) for l in layers]
     done, t_used = 0, 0.0
     for s in range(total):
         t0 = time.perf_counter()
-        O.append(0, W.to_f32(ks[:, :, :, s:s + 1]), W.to_f32(vs[:, :, :, s:s + 1]))
-        O.decode(0, W.to_f32(qs[:, :, :, s]))
-        O.evict(0, w.layers)
+        for si in range(len(layers)):
+            O.append(si, W.to_f32(ks[si][0][:, :, :, s:s + 1]), W.to_f32(ks[si][1][:, :, :, s:s + 1]))
+            O.decode(si, W.to_f32(qs[si][:, :, :, s]))
+        if (s + 1) % w.evict_every == 0:
+            O.evict(0, len(layers))
         dt = time.perf_counter() - t0
         if s >= warmup:
             t_used += dt
             done += 1
             if t_used > budget_s:
                 break
-    return done / t_used, threads, done
+    frac = len(layers) / w.layers
+    sample = (f"{done} decode steps of all {w.units} units" if frac == 1 else
+              f"{done} decode steps of layer(s) {layers} ({len(layers) * w.batch * w.hkv} of {w.units} "
+              f"units), rate scaled by {len(layers)}/{w.layers} layers")
+    return frac * done / t_used, threads, done, sample
+
+
+def oracle_sample_layers(w):
+    """Layers the CPU oracle times: all of a one-layer workload, else one."""
+    return None if w.layers == 1 else [0]
 
 
 def bench_reference(args):
@@ -172,16 +217,16 @@ def bench_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    w = W.WORKLOADS[WORKLOAD_INDEX]
-    val, cores, done = run_cpu_oracle(w, w.index, args.steps, args.warmup, budget_s=120.0)
+    w = W.WORKLOADS[args.workload]
+    val, cores, done, sample = run_cpu_oracle(w, w.index, args.steps, args.warmup, budget_s=120.0,
+                                              layers=oracle_sample_layers(w))
     line = {
         "impl": "reference", "metric": METRIC, "value": val, "unit": "steps/s", "n_gpus": 0,
         "steps": done, "warmup": args.warmup, "ms_per_step": 1e3 / val, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
         "config": {"workload": w.name, "units": w.units, "budget": w.budget, "sink": w.sink,
                    "window": w.window, "evict_every": w.evict_every},
-        "cpu_baseline": {"value": val, "unit": "steps/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{done} decode steps of the full workload after prefill"},
+        "cpu_baseline": {"value": val, "unit": "steps/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": val, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -202,22 +247,31 @@ def bench_gpu(args):
         dist.init_process_group("nccl", init_method="env://")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = W.WORKLOADS[WORKLOAD_INDEX]
-    seed = w.index + 1000 * rank          # every rank decodes its own batch
-    K, Wu, Ke = args.steps, args.warmup, args.e2e_steps
-    total_steps = Wu + K + args.three_call_steps + Ke
+    w = W.WORKLOADS[args.workload]
+    seed = rank_seed(w, rank)
+    K, Wu, Ke, K3 = args.steps, args.warmup, args.e2e_steps, args.three_call_steps
+    L = w.layers
+    KL = args.per_layer_steps if args.per_layer_steps >= 0 else (0 if L == 1 else 100)
+    total_steps = Wu + K + K3 + KL + Ke
     budgets = W.budgets(w, seed)
     cache = hk.Cache(hk.CacheConfig(w.layers, w.batch, w.hq, w.hkv, w.d, w.dtype, w.sink, w.window,
                                     budgets, w.prompt + total_steps + 1))
     stage("cache created")
-    # ---- setup (untimed): prompt, window scoring, cut to budget ----
-    k, v = W.gen_kv(w, 0, w.layers, 0, w.prompt, seed)
-    cache.append(W.to_torch(k).to(dev), W.to_torch(v).to(dev))
-    del k, v
-    cache.score_window(W.to_torch(W.gen_q(w, 0, w.layers, w.prompt - w.nq, w.nq, seed)).to(dev))
+    # ---- setup (untimed): prompt in layer chunks, window scoring, cut to budget ----
+    lc = layer_chunk(w)
+    for l0 in range(0, L, lc):
+        nl = min(lc, L - l0)
+        k, v = W.gen_kv(w, l0, nl, 0, w.prompt, seed)
+        cache.append(W.to_torch(k).to(dev), W.to_torch(v).to(dev), layer0=l0)
+        del k, v
+    cache.score_window(W.to_torch(W.gen_q(w, 0, L, w.prompt - w.nq, w.nq, seed)).to(dev))
     cache.evict()
-    ks, vs = W.gen_kv(w, 0, w.layers, w.prompt, total_steps, seed)
-    qs = W.gen_q(w, 0, w.layers, w.prompt, total_steps, seed)
+    # decode inputs for R distinct steps, cycled when all steps' inputs would
+    # exceed ~1 GB (the appended rows still take fresh positions every step)
+    per_step_in = L * w.batch * (2 * w.hkv + w.hq) * w.d * w.elem_bytes
+    R = int(min(total_steps, max(64, 1e9 // per_step_in)))
+    ks, vs = W.gen_kv(w, 0, L, w.prompt, R, seed)
+    qs = W.gen_q(w, 0, L, w.prompt, R, seed)
     ks = np.ascontiguousarray(np.moveaxis(ks, 3, 0)[:, :, :, :, None, :])
     vs = np.ascontiguousarray(np.moveaxis(vs, 3, 0)[:, :, :, :, None, :])
     qs = np.ascontiguousarray(np.moveaxis(qs, 3, 0))
@@ -225,19 +279,30 @@ def bench_gpu(args):
     out = torch.empty_like(dqs[0])
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
+    E = w.evict_every
+    counter = {"s": 0}                    # decode steps taken so far (eviction cadence)
 
-    def step(s):
-        cache.step(dks[s], dvs[s], dqs[s], out, evict=True)
+    def next_step():
+        s = counter["s"]
+        counter["s"] += 1
+        return s % R, (s + 1) % E == 0
+
+    def bytes_now():
+        return step_bytes(w, cache.lengths().astype(np.int64) + 1)
+
+    def step_fused():
+        r, ev_ = next_step()
+        cache.step(dks[r], dvs[r], dqs[r], out, evict=ev_)
 
     stage("setup done")
-    for s in range(Wu):
-        flush.fill_(float(s))
-        step(s)
+    for _ in range(Wu):
+        flush.fill_(1.0)
+        step_fused()
     torch.cuda.synchronize()
     stage("warm-up done")
-    # A short spin kernel before each timed step lets the host enqueue the
-    # whole step before the GPU reaches it, so host launch overhead never
-    # shows up inside the timed events (the flush and the spin are outside).
+    # A spin kernel before each timed step lets the host enqueue the whole
+    # step before the GPU reaches it, so host launch overhead never shows up
+    # inside the timed events (the flush and the spin are outside them).
     spin_cycles = int(args.spin_us * 2.0e3)
 
     # ---- timed: the single-call step (append + decode + evict in one launch) ----
@@ -247,13 +312,14 @@ def bench_gpu(args):
         dist.barrier()
     torch.cuda.synchronize()
     launches0 = cache.kernel_launches()
+    alg_bytes = 0
     for i in range(K):
-        s = Wu + i
+        alg_bytes += bytes_now()
         flush.fill_(float(i))
         torch.cuda._sleep(spin_cycles)
         e0, e1 = ev[i]
         e0.record(stream)
-        step(s)
+        step_fused()
         e1.record(stream)
     torch.cuda.synchronize()
     launches = cache.kernel_launches() - launches0
@@ -261,27 +327,23 @@ def bench_gpu(args):
         dist.barrier()
     clocks = sampler.stop()
     step_ms = [e0.elapsed_time(e1) for (e0, e1) in ev]
-    t_total = sum(step_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([t_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_total = float(t.item())
-
+    t_total = max_over_ranks(sum(step_ms) / 1e3, world, dev)
     stage("timed fused steps done")
-    # ---- the same steps as three calls (append, decode_step, evict), for context ----
-    K3 = args.three_call_steps
+
+    # ---- the same steps as three calls (append, decode_step, evict when due) ----
     ev3 = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(K3)]
     for i in range(K3):
-        s = Wu + K + i
+        r, ev_ = next_step()
         flush.fill_(float(i))
         torch.cuda._sleep(spin_cycles)
         e0, e1, e2, e3 = ev3[i]
         e0.record(stream)
-        cache.append(dks[s], dvs[s])
+        cache.append(dks[r], dvs[r])
         e1.record(stream)
-        cache.decode_step(dqs[s], out)
+        cache.decode_step(dqs[r], out)
         e2.record(stream)
-        cache.evict()
+        if ev_:
+            cache.evict()
         e3.record(stream)
     torch.cuda.synchronize()
     three = None
@@ -289,88 +351,106 @@ def bench_gpu(args):
         ms3 = [e0.elapsed_time(e3) for (e0, e1, e2, e3) in ev3]
         dec3 = [e1.elapsed_time(e2) for (e0, e1, e2, e3) in ev3]
         three = {"steps": K3, "ms_per_step": sum(ms3) / K3, "steps_per_s": K3 / (sum(ms3) / 1e3),
-                 "decode_kernel_us": 1e3 * sum(dec3) / K3, "launches_per_step": 3}
-
+                 "decode_kernel_us": 1e3 * sum(dec3) / K3}
     stage("three-call steps done")
+
+    # ---- per-layer launches: one fused call per layer and step, as a model
+    # whose layers run in turn would issue them ----
+    per_layer = None
+    if KL > 0:
+        evl = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(KL)]
+        pl_launch0 = cache.kernel_launches()
+        for i in range(KL):
+            r, ev_ = next_step()
+            flush.fill_(float(i))
+            torch.cuda._sleep(spin_cycles + L * 40000)   # room to enqueue L calls
+            e0, e1 = evl[i]
+            e0.record(stream)
+            for l in range(L):
+                cache.step(dks[r][l:l + 1], dvs[r][l:l + 1], dqs[r][l:l + 1], out[l:l + 1], evict=ev_,
+                           layer0=l)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        msl = [e0.elapsed_time(e1) for (e0, e1) in evl]
+        per_layer = {"steps": KL, "launches_per_step": (cache.kernel_launches() - pl_launch0) / KL,
+                     "ms_per_step": sum(msl) / KL, "steps_per_s": KL / (sum(msl) / 1e3)}
+        stage("per-layer steps done")
+
     # ---- e2e through the C ABI with pinned host buffers ----
-    hk_s = stream
-    hk_k = torch.from_numpy(ks.view(np.int16)).pin_memory()
-    hk_v = torch.from_numpy(vs.view(np.int16)).pin_memory()
-    hk_q = torch.from_numpy(qs.view(np.int16)).pin_memory()
-    k_dev = torch.empty(ks.shape[1:], dtype=torch.int16, device=dev)
+    hk_k = torch.from_numpy(ks.view(np.int16) if ks.dtype == np.uint16 else ks).pin_memory()
+    hk_v = torch.from_numpy(vs.view(np.int16) if vs.dtype == np.uint16 else vs).pin_memory()
+    hk_q = torch.from_numpy(qs.view(np.int16) if qs.dtype == np.uint16 else qs).pin_memory()
+    k_dev = torch.empty(tuple(hk_k.shape[1:]), dtype=hk_k.dtype, device=dev)
     v_dev = torch.empty_like(k_dev)
-    q_dev = torch.empty(qs.shape[1:], dtype=torch.int16, device=dev)
-    out_host = torch.empty(tuple(out.shape), dtype=torch.bfloat16).pin_memory()
+    q_dev = torch.empty(tuple(hk_q.shape[1:]), dtype=hk_q.dtype, device=dev)
+    out_host = torch.empty(tuple(out.shape), dtype=out.dtype).pin_memory()
+    as_wdt = (lambda t: t.view(torch.bfloat16)) if w.dtype == "bf16" else (lambda t: t)
     torch.cuda.synchronize()
     e_start = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
     e2e_ms = 0.0
     for i in range(Ke):
-        s = Wu + K + K3 + i
+        r, ev_ = next_step()
         flush.fill_(float(i))
-        e_start.record(hk_s)
-        k_dev.copy_(hk_k[s], non_blocking=True)
-        v_dev.copy_(hk_v[s], non_blocking=True)
-        q_dev.copy_(hk_q[s], non_blocking=True)
-        kb, vb, qb = k_dev.view(torch.bfloat16), v_dev.view(torch.bfloat16), q_dev.view(torch.bfloat16)
-        cache.step(kb, vb, qb, out, evict=True)
+        e_start.record(stream)
+        k_dev.copy_(hk_k[r], non_blocking=True)
+        v_dev.copy_(hk_v[r], non_blocking=True)
+        q_dev.copy_(hk_q[r], non_blocking=True)
+        cache.step(as_wdt(k_dev), as_wdt(v_dev), as_wdt(q_dev), out, evict=ev_)
         out_host.copy_(out, non_blocking=True)
-        e_end.record(hk_s)
+        e_end.record(stream)
         e_end.synchronize()
         e2e_ms += e_start.elapsed_time(e_end)
     stage("e2e steps done")
-    h2d = (ks[0].nbytes + vs[0].nbytes + qs[0].nbytes)
-    d2h = out_host.numel() * 2
+    h2d = hk_k[0].nbytes + hk_v[0].nbytes + hk_q[0].nbytes
+    d2h = out_host.nbytes
     cache.device_status()
-    n_ret = int(cache.lengths().max()) + 1      # tokens attended per unit per step
+    lens = cache.lengths()
     cache.close()
 
     # ---- numbers ----
-    kv, meta, qo, app = step_bytes(w, n_ret)
-    units = w.units
-    # the fused launch moves everything a step moves: it is the step's only kernel
-    dec_bytes = units * (kv + meta + qo + app)
-    step_bytes_all = dec_bytes
-    dec_avg_s = (sum(step_ms) / len(step_ms)) / 1e3
+    avg_s = t_total / K
     peaks, src = measured_peaks()
     peak = float(peaks.get("hbm_gbs", 6800.0))
-    achieved = dec_bytes / dec_avg_s / 1e9
+    achieved = alg_bytes / K / avg_s / 1e9
     traffic = None
     try:
         with open(TRAFFIC_FILE) as f:
             tr = json.load(f)
-        if tr.get("kernel_sha") == kernel_sha():
+        if tr.get("kernel_sha") == kernel_sha() and tr.get("workload") == w.name:
             traffic = tr.get("dram_bytes_per_launch")
     except (OSError, ValueError):
         pass
-    value = world * K / t_total
+    value = whole_job_rate(world, K, t_total)
     line = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": K,
         "warmup": Wu, "ms_per_step": t_total * 1e3 / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded)",
-        "config": {"workload": w.name, "layers": w.layers, "batch": w.batch, "q_heads": w.hq,
+        "config": {"workload": w.name, "layers": L, "batch": w.batch, "q_heads": w.hq,
                    "kv_heads": w.hkv, "head_dim": w.d, "kv_dtype": w.dtype, "prompt": w.prompt,
                    "budget": w.budget, "sink": w.sink, "window": w.window,
-                   "evict_every": w.evict_every, "tokens_attended_per_unit": n_ret,
+                   "evict_every": E, "tokens_attended_per_unit_max": int(lens.max()) + 1,
+                   "decode_inputs": (f"{R} distinct steps" + (", cycled" if R < total_steps else "")),
                    "l2": "flushed between timed steps (256 MB write, outside the timed events)",
                    "parallelism": f"replicas x{world} (units sharded by rank, no collective)"},
-        "hbm_gbs_step": step_bytes_all * world * K / t_total / 1e9,
-        "retained_kv_gbs": units * kv * world * K / t_total / 1e9,
+        "hbm_gbs_step": alg_bytes * world / t_total / 1e9,
         "roofline": {"kernel": "k_decode (append + attention + importance + victim + evict, one launch)",
-                     "bound": "hbm",
-                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_source": f"{src} hbm_gbs", "traffic": traffic,
-                     "bytes_per_launch": dec_bytes, "avg_launch_us": dec_avg_s * 1e6},
+                     "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": f"{src} hbm_gbs", "traffic": traffic,
+                     "bytes_per_launch": alg_bytes // K, "avg_launch_us": avg_s * 1e6,
+                     "launches_per_step": launches / K},
         "e2e": ({"value": Ke / (e2e_ms / 1e3), "unit": "steps/s", "h2d_bytes_per_step": int(h2d),
                  "d2h_bytes_per_step": int(d2h), "steps": Ke} if Ke > 0 else None),
         "gpu_launches": launches,
         "three_call_path": three,
+        "per_layer_launches": per_layer,
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        val, cores, done = run_cpu_oracle(w, seed, min(64, w.steps), 2, budget_s=20.0)
+        val, cores, done, sample = run_cpu_oracle(w, seed, min(64, w.steps), 2, budget_s=20.0,
+                                                  layers=oracle_sample_layers(w))
         line["cpu_baseline"] = {"value": val, "unit": "steps/s", "cores": cores, "kind": "oracle",
-                                "sample": f"{done} decode steps (all {units} units) after prefill"}
+                                "sample": sample}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -384,6 +464,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--three-call-steps", type=int, default=500)
+    ap.add_argument("--per-layer-steps", type=int, default=-1,
+                    help="steps timed as one launch per layer (default 100 for multi-layer workloads)")
+    ap.add_argument("--workload", type=int, default=WORKLOAD_INDEX,
+                    help="workload index (default: the Llama-3-8B layer the metric is quoted on)")
     ap.add_argument("--spin-us", type=float, default=60.0)
     ap.add_argument("--impl", default="hikv", choices=["hikv", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")

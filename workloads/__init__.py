@@ -151,8 +151,10 @@ def budgets(w: Workload, seed: Optional[int] = None) -> np.ndarray:
     return np.full(n, int(w.budget), dtype=np.int32)
 
 
-def heavy_scale(w: Workload, seed: int, layer: int, batch: int) -> Optional[np.ndarray]:
-    """Key scale per position [total_positions] for one (layer, batch) sequence.
+def heavy_scale(w: Workload, seed: int, layer: int, batch: int, upto: int = 0) -> Optional[np.ndarray]:
+    """Key scale per position [T] for one (layer, batch) sequence, where
+    T = max(total_positions, upto): a run generating positions past the
+    workload's own steps passes `upto` so every generated position has one.
 
     Applies to the keys of every KV head at that position.
       fixed8x4     : exactly 8 distinct prompt positions, x4
@@ -161,7 +163,7 @@ def heavy_scale(w: Workload, seed: int, layer: int, batch: int) -> Optional[np.n
     """
     if w.heavy is None:
         return None
-    T = w.total_positions
+    T = max(w.total_positions, int(upto))
     lib = _load()
     u = np.empty(T, dtype=np.float64)
     lib.synth_uniform(seed, T_HEAVY, layer, batch, 0, 0, T, u.ctypes.data)
@@ -219,8 +221,9 @@ def gen_kv(w: Workload, layer0: int, nlayers: int, pos0: int, npos: int,
     for li in range(nlayers):
         layer = layer0 + li
         for b in range(w.batch):
-            hs = heavy_scale(w, seed, layer, b)
+            hs = heavy_scale(w, seed, layer, b, upto=pos0 + npos)
             sc = None if hs is None else np.ascontiguousarray(hs[pos0: pos0 + npos])
+            assert sc is None or sc.size == npos
             for g in range(w.hkv):
                 jobs.append((seed, T_KEY, layer, b, g, pos0, npos, sc, k[li, b, g]))
                 jobs.append((seed, T_VALUE, layer, b, g, pos0, npos, None, v[li, b, g]))
@@ -236,8 +239,9 @@ def gen_kv_unit(w: Workload, layer: int, batch: int, g: int, pos0: int, npos: in
     dt = np.uint16 if bf else np.float32
     k = np.empty((npos, w.d), dtype=dt)
     v = np.empty_like(k)
-    hs = heavy_scale(w, seed, layer, batch)
+    hs = heavy_scale(w, seed, layer, batch, upto=pos0 + npos)
     sc = None if hs is None else np.ascontiguousarray(hs[pos0: pos0 + npos])
+    assert sc is None or sc.size == npos
     _fill_streams([(seed, T_KEY, layer, batch, g, pos0, npos, sc, k),
                    (seed, T_VALUE, layer, batch, g, pos0, npos, None, v)], w.d, bf)
     return k, v
