@@ -258,14 +258,27 @@ def bench_gpu(args):
                                     budgets, w.prompt + total_steps + 1))
     stage("cache created")
     # ---- setup (untimed): prompt in layer chunks, window scoring, cut to budget ----
+    stream = torch.cuda.current_stream()
     lc = layer_chunk(w)
     for l0 in range(0, L, lc):
         nl = min(lc, L - l0)
         k, v = W.gen_kv(w, l0, nl, 0, w.prompt, seed)
         cache.append(W.to_torch(k).to(dev), W.to_torch(v).to(dev), layer0=l0)
         del k, v
-    cache.score_window(W.to_torch(W.gen_q(w, 0, L, w.prompt - w.nq, w.nq, seed)).to(dev))
-    cache.evict()
+    dq_win = W.to_torch(W.gen_q(w, 0, L, w.prompt - w.nq, w.nq, seed)).to(dev)
+    se = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    torch.cuda.synchronize()
+    se[0].record(stream)
+    cache.score_window(dq_win)           # a0: prompt importance from the observation window
+    se[1].record(stream)
+    cache.evict()                        # a0: the cut to the budget
+    se[2].record(stream)
+    torch.cuda.synchronize()
+    setup = {"prompt_tokens_per_unit": w.prompt, "window_queries": w.nq,
+             "window_scoring_ms": se[0].elapsed_time(se[1]), "prefill_cut_ms": se[1].elapsed_time(se[2]),
+             "window_scoring_k_gbs": W.kv_bytes(w.batch, w.prompt, L, w.hkv, w.d, w.elem_bytes) / 2 /
+             (se[0].elapsed_time(se[1]) / 1e3) / 1e9}
+    del dq_win
     # decode inputs for R distinct steps, cycled when all steps' inputs would
     # exceed ~1 GB (the appended rows still take fresh positions every step)
     per_step_in = L * w.batch * (2 * w.hkv + w.hq) * w.d * w.elem_bytes
@@ -278,7 +291,6 @@ def bench_gpu(args):
     dks, dvs, dqs = (W.to_torch(x).to(dev) for x in (ks, vs, qs))
     out = torch.empty_like(dqs[0])
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream()
     E = w.evict_every
     counter = {"s": 0}                    # decode steps taken so far (eviction cadence)
 
@@ -444,6 +456,7 @@ def bench_gpu(args):
         "gpu_launches": launches,
         "three_call_path": three,
         "per_layer_launches": per_layer,
+        "setup": setup,
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:

@@ -408,7 +408,10 @@ hikv_status hikv_score_window(hikv_cache* c, int32_t layer0, int32_t nl, int32_t
     a.nchunks_max = c->wchunks;
     a.nchunks_grid = ceil_div(maxn, kWindowChunk);
     a.chunk = kWindowChunk;
-    cudaError_t e = launch_window(a, c->dtype, c->d, c->G, (cudaStream_t)stream);
+    const int nqv = nq * c->G;
+    cudaError_t e = window_tc_supported(c->dtype, c->d, nqv)
+                        ? launch_window_tc(a, c->tmap, c->d, nqv, (cudaStream_t)stream)
+                        : launch_window(a, c->dtype, c->d, c->G, (cudaStream_t)stream);
     c->launches += 2;
     if (e != cudaSuccess) return cuda_fail(e, "score_window: launch");
     for (int u = u0; u < u0 + nu; ++u) c->fresh[u] = 0;
