@@ -52,6 +52,7 @@ def _load():
                 "ora_num_threads": ([_P, _I], _I),
                 "ora_append": ([_P, _I, _I, _I, _P, _P], _I),
                 "ora_score_window": ([_P, _I, _I, _I, _P], _I),
+                "ora_pool_importance": ([_P, _I, _I, _I], _I),
                 "ora_decode": ([_P, _I, _I, _P, _P], _I),
                 "ora_evict": ([_P, _I, _I], _I),
                 "ora_len": ([_P, _I], _I),
@@ -123,6 +124,10 @@ class Oracle:
         q = _f32(q)
         nl, nq = q.shape[0], q.shape[3]
         assert self.lib.ora_score_window(self.h, layer0, nl, nq, _ptr(q)) == 0
+
+    def pool_importance(self, layer0, nl, kpool):
+        """SnapKV: each score becomes the max over the next kpool positions."""
+        assert self.lib.ora_pool_importance(self.h, layer0, nl, int(kpool)) == 0
 
     def decode(self, layer0, q):
         q = _f32(q)

@@ -26,6 +26,11 @@
 //                   prompt queries, causally masked, summed (HiKV sec. III-D;
 //                   SnapKV observation window, blog sec. 3).  Queries are
 //                   applied in position order.
+//  * pooled score   SnapKV variant of the prefill score: each token's score
+//                   becomes the largest window score of the k_pool positions
+//                   starting at its own, S_pooled[i] = max_{0<=m<k} A_obs[i+m]
+//                   (blog sec. 3 "SnapKV"), positions with no retained token
+//                   (past the end) contributing nothing.
 //  * eviction       when n > B: sinks (pos < S) and the recent window
 //                   (pos > t - W) are always kept; of the rest keep the
 //                   B - S - W with the largest importance, ties by lowest
@@ -205,6 +210,28 @@ int ora_score_window(void* h, int layer0, int nl, int nq, const float* q) {
                 float inc = (float)colsum[j];
                 U.e[j].imp = U.e[j].imp + inc;
             }
+        }
+    });
+    return 0;
+}
+
+// SnapKV pooling of the current scores: imp[pos p] <- max of the scores of the
+// retained positions in [p, p + kpool).  kpool <= 1 leaves them unchanged.
+int ora_pool_importance(void* h, int layer0, int nl, int kpool) {
+    Oracle* O = (Oracle*)h;
+    if (!range_ok(O, layer0, nl) || kpool < 0) return 1;
+    if (kpool <= 1) return 0;
+    int per_layer = O->B * O->Hkv;
+    parallel_units(O->nthreads, nl * per_layer, [&](int i) {
+        Unit& U = O->units[layer0 * per_layer + i];
+        std::vector<float> raw(U.e.size());
+        for (size_t j = 0; j < U.e.size(); ++j) raw[j] = U.e[j].imp;
+        for (size_t j = 0; j < U.e.size(); ++j) {
+            float best = raw[j];
+            // entries are in ascending position: scan forward while in range
+            for (size_t m = j + 1; m < U.e.size() && U.e[m].pos < U.e[j].pos + kpool; ++m)
+                best = std::max(best, raw[m]);
+            U.e[j].imp = best;
         }
     });
     return 0;

@@ -312,3 +312,86 @@ def test_kv_size_worked_example():
     m = W.kv_bytes(int(vals["batch"]), int(vals["length"]), int(vals["layers"]),
                    int(vals["kv_heads"]), int(vals["head_dim"]), int(vals["elem_bytes"]))
     assert round(m / 1e9, 1) == vals["gigabytes"]
+
+
+# --------------------------------------------------------------------------
+# SnapKV pooling (blog sec. 3 "SnapKV"): S_pooled[i] = max_{0<=m<k} A_obs[i+m]
+# --------------------------------------------------------------------------
+def _window_scores_ref(K, Qw, G, prompt, nq, d):
+    """Observation-window scores by brute force: each of the last nq prompt
+    queries, causally masked, softmax in float64, summed over the group."""
+    L, B, Hkv = K.shape[:3]
+    out = np.zeros((B, Hkv, prompt))
+    for b in range(B):
+        for g in range(Hkv):
+            for i in range(nq):
+                qpos = prompt - nq + i
+                for hh in range(G):
+                    s = Qw[0, b, g * G + hh, i].astype(np.float64) @ K[0, b, g, :qpos + 1].T.astype(np.float64)
+                    out[b, g, :qpos + 1] += torch.softmax(torch.from_numpy(s / np.sqrt(d)), 0).numpy()
+    return out
+
+
+def _forward_maxpool(pos, score, k):
+    """max over the retained positions in [p, p + k), by explicit search."""
+    out = np.empty_like(score)
+    for j, p in enumerate(pos):
+        out[j] = max(score[m] for m in range(len(pos)) if p <= pos[m] < p + k)
+    return out
+
+
+@pytest.mark.parametrize("kpool", [1, 3, 5, 7])
+def test_pooled_window_score_equals_brute_force(kpool):
+    rng = np.random.default_rng(11 + kpool)
+    L, B, Hq, Hkv, d = 1, 2, 4, 2, 8
+    G = Hq // Hkv
+    prompt, nq = 20, 4
+    O = oracle.Oracle(L, B, Hq, Hkv, d, 1, 2, np.full(Hkv, 1000))
+    K = _rand(rng, L, B, Hkv, prompt, d) * 2
+    Qw = _rand(rng, L, B, Hq, nq, d) * 2
+    O.append(0, K, _rand(rng, L, B, Hkv, prompt, d))
+    O.score_window(0, Qw)
+    O.pool_importance(0, L, kpool)
+    raw = _window_scores_ref(K, Qw, G, prompt, nq, d)
+    for b in range(B):
+        for g in range(Hkv):
+            pos, imp = O.state(O.unit(0, b, g))
+            want = _forward_maxpool(np.arange(prompt), raw[b, g], kpool)
+            np.testing.assert_allclose(imp, want, rtol=2e-6, atol=1e-7)
+            assert np.all(imp >= raw[b, g].astype(np.float32) - 1e-6)   # pooling never lowers a score
+
+
+def test_pooled_spike_spreads_to_the_k_positions_before_it():
+    # one key aligned with every window query takes almost all the mass: after
+    # pooling with k, exactly positions p-k+1 .. p carry the spike
+    L, B, Hq, Hkv, d = 1, 1, 2, 1, 4
+    prompt, nq, k, p = 24, 2, 5, 10
+    O = oracle.Oracle(L, B, Hq, Hkv, d, 0, 0, np.full(Hkv, 1000))
+    K = np.zeros((L, B, Hkv, prompt, d), np.float32)
+    K[0, 0, 0, p] = [40, 0, 0, 0]
+    Qw = np.zeros((L, B, Hq, nq, d), np.float32)
+    Qw[..., 0] = 40
+    O.append(0, K, np.zeros_like(K))
+    O.score_window(0, Qw)
+    _, raw = O.state(0)
+    assert raw[p] > 0.999 * Hq * nq and raw.sum() - raw[p] < 1e-3
+    O.pool_importance(0, L, k)
+    _, imp = O.state(0)
+    spiked = np.nonzero(imp > 0.5 * Hq * nq)[0]
+    np.testing.assert_array_equal(spiked, np.arange(p - k + 1, p + 1))
+
+
+def test_pooling_after_an_eviction_uses_positions():
+    # with gaps in the retained positions the window [p, p + k) is by position
+    rng = np.random.default_rng(3)
+    L, B, Hq, Hkv, d = 1, 1, 2, 1, 8
+    prompt, nq, k = 40, 4, 4
+    O = oracle.Oracle(L, B, Hq, Hkv, d, 2, 4, np.full(Hkv, 20))
+    O.append(0, _rand(rng, L, B, Hkv, prompt, d) * 2, _rand(rng, L, B, Hkv, prompt, d))
+    O.score_window(0, _rand(rng, L, B, Hq, nq, d) * 2)
+    O.evict(0, L)
+    pos, before = O.state(0)
+    assert len(pos) == 20 and np.any(np.diff(pos) > 1)
+    O.pool_importance(0, L, k)
+    _, after = O.state(0)
+    np.testing.assert_array_equal(after, _forward_maxpool(pos, before, k))
