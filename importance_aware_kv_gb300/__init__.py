@@ -45,7 +45,8 @@ class hikv_config(ctypes.Structure):
                 ("num_sink", ctypes.c_int32), ("recent_window", ctypes.c_int32),
                 ("budgets", ctypes.POINTER(ctypes.c_int32)), ("max_tokens", ctypes.c_int32),
                 ("page_tokens", ctypes.c_int32), ("pool_pages", ctypes.c_int64),
-                ("max_window_queries", ctypes.c_int32), ("scale", ctypes.c_float)]
+                ("max_window_queries", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("pool_kernel", ctypes.c_int32)]
 
 
 def _load():
@@ -122,6 +123,7 @@ class CacheConfig:
     pool_pages: int = 0
     max_window_queries: int = 0
     scale: float = 0.0
+    pool_kernel: int = 0           # SnapKV max-pool of the prompt scores (0/1: off)
 
 
 def hikv_create_cache(cfg: CacheConfig) -> ctypes.c_void_p:
@@ -130,7 +132,7 @@ def hikv_create_cache(cfg: CacheConfig) -> ctypes.c_void_p:
                     HIKV_BF16 if cfg.dtype == "bf16" else HIKV_F32, cfg.num_sink,
                     cfg.recent_window, b.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
                     cfg.max_tokens, cfg.page_tokens, cfg.pool_pages, cfg.max_window_queries,
-                    cfg.scale)
+                    cfg.scale, cfg.pool_kernel)
     h = ctypes.c_void_p()
     _check(_lib.hikv_create_cache(ctypes.byref(c), ctypes.byref(h)))
     return h

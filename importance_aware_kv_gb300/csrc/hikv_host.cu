@@ -103,6 +103,7 @@ struct hikv_cache {
     int64_t pages_in_use = 0;
     int cs_override = 0;                // HIKV_DECODE_CS (tuning)
     int64_t launches = 0;               // kernels launched through this cache
+    int pool_k = 0;                     // SnapKV pooling of the prompt scores (> 1: on)
 };
 
 namespace {
@@ -163,6 +164,8 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
     if (f.pool_pages < 0) return fail(HIKV_ERR_INVALID_ARG, "create: negative pool_pages");
     if (f.max_window_queries < 0) return fail(HIKV_ERR_INVALID_ARG, "create: negative max_window_queries");
     if (!(f.scale >= 0.f) || !std::isfinite(f.scale)) return fail(HIKV_ERR_INVALID_ARG, "create: bad scale");
+    if (f.pool_kernel < 0 || f.pool_kernel > kMaxPoolKernel)
+        return fail(HIKV_ERR_INVALID_ARG, "create: pool_kernel %d not in [0, %d]", f.pool_kernel, kMaxPoolKernel);
     const int64_t units64 = (int64_t)f.num_layers * f.batch * f.num_kv_heads;
     if (units64 > 65535) return fail(HIKV_ERR_UNSUPPORTED, "create: %lld units > 65535", (long long)units64);
     for (int i = 0; i < f.num_layers * f.num_kv_heads; ++i) {
@@ -187,6 +190,7 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
         return fail(HIKV_ERR_UNSUPPORTED, "create: pool of %lld pages too large", (long long)f.pool_pages);
     }
     c->scale = f.scale > 0.f ? f.scale : 1.0f / std::sqrt((float)c->d);
+    c->pool_k = f.pool_kernel;
     c->budget_unit.resize(c->units);
     for (int u = 0; u < c->units; ++u)
         c->budget_unit[u] = f.budgets[(u / c->per_layer) * c->Hkv + u % c->Hkv];
@@ -394,6 +398,8 @@ hikv_status hikv_score_window(hikv_cache* c, int32_t layer0, int32_t nl, int32_t
     for (int u = u0; u < u0 + nu; ++u) {
         if (c->next_pos[u] < nq || c->len[u] < 1)
             return fail(HIKV_ERR_STATE, "score_window: unit %d has fewer than nq=%d positions", u, nq);
+        if (c->pool_k > 1 && c->len[u] != c->next_pos[u])
+            return fail(HIKV_ERR_STATE, "score_window: pooling needs unit %d's prompt uncut", u);
         maxn = std::max(maxn, c->len[u]);
     }
     WindowArgs a{};
@@ -413,6 +419,10 @@ hikv_status hikv_score_window(hikv_cache* c, int32_t layer0, int32_t nl, int32_t
                         ? launch_window_tc(a, c->tmap, c->d, nqv, (cudaStream_t)stream)
                         : launch_window(a, c->dtype, c->d, c->G, (cudaStream_t)stream);
     c->launches += 2;
+    if (e == cudaSuccess && c->pool_k > 1) {
+        e = launch_pool_importance(c->v, u0, nu, c->pool_k, (cudaStream_t)stream);
+        c->launches += 1;
+    }
     if (e != cudaSuccess) return cuda_fail(e, "score_window: launch");
     for (int u = u0; u < u0 + nu; ++u) c->fresh[u] = 0;
     return HIKV_OK;

@@ -444,6 +444,10 @@ struct WindowArgs {
     int32_t chunk;      // tokens per CTA
 };
 cudaError_t launch_window(const WindowArgs& a, int dtype, int d, int group, cudaStream_t s);
+// SnapKV pooling of the prompt scores of units [u0, u0 + nu) (slots must be
+// in position order: nothing removed yet)
+constexpr int kMaxPoolKernel = 64;
+cudaError_t launch_pool_importance(const View& v, int32_t u0, int32_t nu, int k, cudaStream_t s);
 // the tensor-core variant (bf16 K/V, at most 128 query vectors G*nq)
 bool window_tc_supported(int dtype, int d, int nqv);
 cudaError_t launch_window_tc(const WindowArgs& a, const CUtensorMap& tmap, int d, int nqv, cudaStream_t s);

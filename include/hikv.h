@@ -77,6 +77,13 @@ typedef struct {
                                max_tokens at once) */
     int32_t max_window_queries; /* largest nq for hikv_score_window (0 => 32) */
     float scale;            /* logit scale; 0 => 1/sqrt(head_dim) */
+    int32_t pool_kernel;    /* SnapKV prefill selection (KV cache compression blog,
+                               sec. 3 "SnapKV"): with k = pool_kernel > 1,
+                               hikv_score_window replaces each prompt token's score
+                               by the largest window score of positions [p, p + k)
+                               (positions past the prompt contribute nothing), and
+                               the cut then keeps the top pooled scores.  0 or 1 =>
+                               plain window scores.  At most 64. */
 } hikv_config;
 
 /* Create a cache: allocates the page pool, page tables, per-slot importance

@@ -50,7 +50,7 @@ def _out_np(t: torch.Tensor) -> np.ndarray:
 class Lockstep:
     def __init__(self, w: W.Workload, seed=None, sample_layers=None, cs=None, budgets=None,
                  device="cuda", layer_chunk=None, full_cache=False, page_tokens=64,
-                 check_kv=True, full_twin_layers=None):
+                 check_kv=True, full_twin_layers=None, pool_kernel=0):
         import importance_aware_kv_gb300 as hk
         self.hk = hk
         self.w = w
@@ -63,13 +63,14 @@ class Lockstep:
         self.layer_chunk = layer_chunk or max(1, min(w.layers, int(2e9 // max(1, W.kv_bytes(
             w.batch, w.prompt, 1, w.hkv, w.d, w.elem_bytes)))))
         self.check_kv = check_kv
+        self.pool = pool_kernel
         if cs is not None:
             os.environ["HIKV_DECODE_CS"] = str(cs)
         try:
             self.cache = hk.Cache(hk.CacheConfig(
                 w.layers, w.batch, w.hq, w.hkv, w.d, w.dtype, w.sink, w.window,
                 self.budgets, w.total_positions, page_tokens=page_tokens,
-                max_window_queries=max(32, w.nq)))
+                max_window_queries=max(32, w.nq), pool_kernel=pool_kernel))
         finally:
             if cs is not None:
                 os.environ.pop("HIKV_DECODE_CS", None)
@@ -86,10 +87,12 @@ class Lockstep:
             self.twin.__dict__.update(dict(hk=hk, w=w, seed=self.seed, dev=self.dev,
                                            budgets=np.full_like(self.budgets, w.total_positions),
                                            sample=list(full_twin_layers), layer_chunk=self.layer_chunk,
-                                           check_kv=False, rep=Report(), upl=self.upl, twin=None))
+                                           check_kv=False, rep=Report(), upl=self.upl, twin=None,
+                                           pool=pool_kernel))
             self.twin.cache = hk.Cache(hk.CacheConfig(
                 w.layers, w.batch, w.hq, w.hkv, w.d, w.dtype, w.sink, w.window, self.twin.budgets,
-                w.total_positions, page_tokens=page_tokens, max_window_queries=max(32, w.nq)))
+                w.total_positions, page_tokens=page_tokens, max_window_queries=max(32, w.nq),
+                pool_kernel=pool_kernel))
             self.twin.ora = oracle.Oracle(len(self.twin.sample), w.batch, w.hq, w.hkv, w.d, w.sink,
                                           w.window, np.full(len(self.twin.sample) * w.hkv, w.total_positions),
                                           out_bf16=(w.dtype == "bf16"), threads=os.cpu_count() or 1)
@@ -114,6 +117,7 @@ class Lockstep:
             ls.cache.score_window(dq)
             for si, l in enumerate(ls.sample):
                 ls.ora.score_window(si, W.to_f32(q[l:l + 1]))
+                ls.ora.pool_importance(si, 1, getattr(ls, "pool", 0))
             ls.compare_state(after_evict=False)
             ls.cache.evict()
             for si in range(len(ls.sample)):

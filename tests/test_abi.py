@@ -48,6 +48,8 @@ def _cfg(hk, **kw):
     (dict(page_tokens=48), 1),
     (dict(max_tokens=0), 1),
     (dict(num_sink=-1), 1),
+    (dict(pool_kernel=-1), 1),
+    (dict(pool_kernel=65), 1),                                    # SnapKV kernel above 64
 ])
 def test_create_rejects_bad_config_on_host(hk, kw, status):
     with pytest.raises(hk.HikvError) as ei:

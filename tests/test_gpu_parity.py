@@ -118,6 +118,36 @@ def test_long_chunk_global_logits_path():
     _run(w, fused=True)
 
 
+@pytest.mark.parametrize("kpool", [3, 7, 64])
+def test_snapkv_pooled_prefill_selection(kpool):
+    # SnapKV: the prompt scores are max-pooled over the next k positions
+    # before the cut; f32 (CUDA-core scoring) and bf16 (tensor-core scoring)
+    _run(SMALL.with_(sink=1, window=16), pool_kernel=kpool)
+    _run(SMALL.with_(sink=1, window=16, dtype="f32", d=64), pool_kernel=kpool, fused=True)
+
+
+def test_snapkv_llama3_8b_layer():
+    rep = _run(W.WORKLOADS[1], pool_kernel=7, fused=True)
+    assert rep.evictions_checked == 64 * (1 + 256)
+
+
+def test_snapkv_needs_the_uncut_prompt():
+    import importance_aware_kv_gb300 as hk
+    cfg = hk.CacheConfig(1, 1, 4, 2, 64, "bf16", 1, 4, [16, 16], 64, page_tokens=16, pool_kernel=5)
+    c = hk.Cache(cfg)
+    dev = torch.device("cuda")
+    k = torch.randn(1, 1, 2, 40, 64, device=dev).to(torch.bfloat16)
+    c.append(k, k.clone())
+    q = torch.randn(1, 1, 4, 8, 64, device=dev).to(torch.bfloat16)
+    c.score_window(q)
+    c.evict()
+    with pytest.raises(hk.HikvError) as ei:
+        c.score_window(q)                           # slots no longer in position order
+    assert ei.value.status == hk.HIKV_ERR_STATE
+    c.device_status()
+    c.close()
+
+
 @FUSED
 def test_zero_keys_tie_rule_exact(fused):
     """All-zero keys: uniform softmax, whole classes of tokens tie exactly; the
