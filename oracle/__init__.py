@@ -53,6 +53,7 @@ def _load():
                 "ora_append": ([_P, _I, _I, _I, _P, _P], _I),
                 "ora_score_window": ([_P, _I, _I, _I, _P], _I),
                 "ora_pool_importance": ([_P, _I, _I, _I], _I),
+                "ora_set_recent_only": ([_P, _I], _I),
                 "ora_decode": ([_P, _I, _I, _P, _P], _I),
                 "ora_evict": ([_P, _I, _I], _I),
                 "ora_len": ([_P, _I], _I),
@@ -124,6 +125,10 @@ class Oracle:
         q = _f32(q)
         nl, nq = q.shape[0], q.shape[3]
         assert self.lib.ora_score_window(self.h, layer0, nl, nq, _ptr(q)) == 0
+
+    def set_recent_only(self, on=True):
+        """HiKV Stage I: decode steps add mass only to the recent bank."""
+        assert self.lib.ora_set_recent_only(self.h, 1 if on else 0) == 0
 
     def pool_importance(self, layer0, nl, kpool):
         """SnapKV: each score becomes the max over the next kpool positions."""

@@ -26,6 +26,15 @@
 //                   prompt queries, causally masked, summed (HiKV sec. III-D;
 //                   SnapKV observation window, blog sec. 3).  Queries are
 //                   applied in position order.
+//  * recent bank    HiKV Stage I variant of the importance (HiKV sec. III-B,
+//                   Algorithm 1 "IS[l] += P_t[l] for l in R"): a decode step
+//                   adds attention mass only to tokens of the recent bank --
+//                   the W newest positions and the one leaving it this step,
+//                   pos >= t - W -- so a token's score is frozen once it is
+//                   older.  Eviction is unchanged: of the tokens outside the
+//                   window the lowest score goes, ties taking the newest,
+//                   which is HiKV's "promote the ejected token only if its
+//                   score exceeds the minimum of the important bank".
 //  * pooled score   SnapKV variant of the prefill score: each token's score
 //                   becomes the largest window score of the k_pool positions
 //                   starting at its own, S_pooled[i] = max_{0<=m<k} A_obs[i+m]
@@ -66,6 +75,7 @@ struct Oracle {
     double scale;
     int out_bf16;
     int nthreads;
+    int recent_only = 0;             // HiKV Stage I: accumulate in the recent bank only
     std::vector<int32_t> budget;     // [L * Hkv]
     std::vector<Unit> units;         // [L][B][Hkv]
     int unit_index(int l, int b, int g) const { return (l * B + b) * Hkv + g; }
@@ -259,11 +269,21 @@ int ora_decode(void* h, int layer0, int nl, const float* q, float* out) {
             for (int c = 0; c < O->d; ++c)
                 out[row + c] = O->out_bf16 ? round_bf16(o[c]) : (float)o[c];
         }
+        const int32_t t = U.next_pos - 1;   // this step's token
         for (size_t j = 0; j < U.e.size(); ++j) {
+            if (O->recent_only && U.e[j].pos < t - O->W) continue;   // frozen (important bank)
             float inc = (float)colsum[j];
             U.e[j].imp = U.e[j].imp + inc;
         }
     });
+    return 0;
+}
+
+// Importance rule of decode steps: 0 = H2O cumulative (every retained token),
+// 1 = HiKV recent bank only.
+int ora_set_recent_only(void* h, int on) {
+    Oracle* O = (Oracle*)h;
+    O->recent_only = on ? 1 : 0;
     return 0;
 }
 

@@ -395,3 +395,111 @@ def test_pooling_after_an_eviction_uses_positions():
     O.pool_importance(0, L, k)
     _, after = O.state(0)
     np.testing.assert_array_equal(after, _forward_maxpool(pos, before, k))
+
+
+# --------------------------------------------------------------------------
+# HiKV Stage I (HiKV sec. III-B, Algorithm 1): scores accumulate only in the
+# recent bank; the token leaving it is promoted only if its score exceeds the
+# important bank's minimum.
+# --------------------------------------------------------------------------
+def _softmax_row(q, keys, d):
+    s = keys.astype(np.float64) @ q.astype(np.float64) / np.sqrt(d)
+    return torch.softmax(torch.from_numpy(s), 0).numpy()
+
+
+def test_recent_bank_accumulation_equals_brute_force():
+    rng = np.random.default_rng(21)
+    L, B, Hq, Hkv, d = 1, 1, 4, 2, 8
+    G = Hq // Hkv
+    prompt, nq, steps, W = 10, 3, 8, 4
+    O = oracle.Oracle(L, B, Hq, Hkv, d, 0, W, np.full(Hkv, 1000))   # no eviction
+    O.set_recent_only(True)
+    K = _rand(rng, L, B, Hkv, prompt + steps, d) * 2
+    V = _rand(rng, L, B, Hkv, prompt + steps, d)
+    Qw = _rand(rng, L, B, Hq, nq, d) * 2
+    O.append(0, K[:, :, :, :prompt], V[:, :, :, :prompt])
+    O.score_window(0, Qw)
+    expect = np.zeros((Hkv, prompt + steps))
+    expect[:, :prompt] = _window_scores_ref(K, Qw, G, prompt, nq, d)[0]
+    for s_ in range(steps):
+        t = prompt + s_
+        O.append(0, K[:, :, :, t:t + 1], V[:, :, :, t:t + 1])
+        q = _rand(rng, L, B, Hq, d)
+        before = [O.state(O.unit(0, 0, g))[1].copy() for g in range(Hkv)]
+        O.decode(0, q)
+        for g in range(Hkv):
+            inc = sum(_softmax_row(q[0, 0, g * G + hh], K[0, 0, g, :t + 1], d) for hh in range(G))
+            recent = np.arange(t + 1) >= t - W
+            expect[g, :t + 1] += np.where(recent, inc, 0.0)
+            _, now = O.state(O.unit(0, 0, g))
+            old = np.arange(t) < t - W                       # frozen: bit-identical
+            np.testing.assert_array_equal(now[:t][old], before[g][:t][old])
+    for g in range(Hkv):
+        _, imp = O.state(O.unit(0, 0, g))
+        np.testing.assert_allclose(imp, expect[g], rtol=2e-6, atol=1e-7)
+
+
+def test_recent_bank_with_a_window_covering_everything_is_h2o():
+    rng = np.random.default_rng(22)
+    L, B, Hq, Hkv, d = 1, 2, 2, 1, 8
+    prompt, steps = 6, 5
+    outs = []
+    for recent in (False, True):
+        r = np.random.default_rng(22)
+        O = oracle.Oracle(L, B, Hq, Hkv, d, 0, 1000, np.full(Hkv, 2000))
+        O.set_recent_only(recent)
+        O.append(0, _rand(r, L, B, Hkv, prompt, d), _rand(r, L, B, Hkv, prompt, d))
+        O.score_window(0, _rand(r, L, B, Hq, 2, d))
+        for _ in range(steps):
+            O.append(0, _rand(r, L, B, Hkv, 1, d), _rand(r, L, B, Hkv, 1, d))
+            O.decode(0, _rand(r, L, B, Hq, d))
+        outs.append([O.state(u)[1] for u in range(O.units)])
+    for a, b in zip(*outs):
+        np.testing.assert_array_equal(a, b)
+
+
+def test_dual_bank_eviction_matches_hikv_fifo_and_min_heap():
+    """Restate HiKV Stage I directly -- a FIFO recent bank of W tokens, an
+    important bank of B - W tokens with frozen scores, the ejected token
+    promoted only if its score exceeds the bank's minimum -- and compare the
+    retained tokens and scores with the oracle's argmin formulation."""
+    rng = np.random.default_rng(23)
+    L, B_, Hq, Hkv, d = 1, 1, 2, 1, 8
+    G = Hq // Hkv
+    prompt, nq, steps, W, Bud = 24, 4, 30, 6, 12
+    O = oracle.Oracle(L, B_, Hq, Hkv, d, 0, W, np.full(Hkv, Bud))
+    O.set_recent_only(True)
+    K = _rand(rng, L, B_, Hkv, prompt + steps, d) * 2
+    V = _rand(rng, L, B_, Hkv, prompt + steps, d)
+    Qw = _rand(rng, L, B_, Hq, nq, d) * 2
+    O.append(0, K[:, :, :, :prompt], V[:, :, :, :prompt])
+    O.score_window(0, Qw)
+    O.evict(0, L)
+    # the dual bank, initialised as HiKV sec. III-D describes: the last W
+    # prompt tokens form the recent bank, the top B - W of the rest the
+    # important bank
+    score = dict(enumerate(_window_scores_ref(K, Qw, G, prompt, nq, d)[0, 0]))
+    recent = list(range(prompt - W, prompt))
+    rest = sorted(range(prompt - W), key=lambda p: (-score[p], p))
+    important = set(rest[:Bud - W])
+    for s_ in range(steps):
+        t = prompt + s_
+        O.append(0, K[:, :, :, t:t + 1], V[:, :, :, t:t + 1])
+        q = _rand(rng, L, B_, Hq, d)
+        O.decode(0, q)
+        O.evict(0, L)
+        recent.append(t)
+        score[t] = 0.0
+        kept = sorted(important) + recent
+        inc = sum(_softmax_row(q[0, 0, hh], K[0, 0, 0, kept], d) for hh in range(G))
+        for p, x in zip(kept, inc):
+            if p in recent:
+                score[p] += x
+        evi = recent.pop(0)
+        low = min(important, key=lambda p: (score[p], -p))
+        if score[evi] > score[low]:
+            important.remove(low)
+            important.add(evi)
+        pos, imp = O.state(0)
+        assert sorted(important) + recent == list(pos), s_
+        np.testing.assert_allclose(imp, [score[p] for p in pos], rtol=2e-6, atol=1e-7)
