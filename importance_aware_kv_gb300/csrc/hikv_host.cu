@@ -164,6 +164,8 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
     if (f.pool_pages < 0) return fail(HIKV_ERR_INVALID_ARG, "create: negative pool_pages");
     if (f.max_window_queries < 0) return fail(HIKV_ERR_INVALID_ARG, "create: negative max_window_queries");
     if (!(f.scale >= 0.f) || !std::isfinite(f.scale)) return fail(HIKV_ERR_INVALID_ARG, "create: bad scale");
+    if (f.importance_mode != 0 && f.importance_mode != 1)
+        return fail(HIKV_ERR_INVALID_ARG, "create: importance_mode %d not in {0, 1}", f.importance_mode);
     if (f.pool_kernel < 0 || f.pool_kernel > kMaxPoolKernel)
         return fail(HIKV_ERR_INVALID_ARG, "create: pool_kernel %d not in [0, %d]", f.pool_kernel, kMaxPoolKernel);
     const int64_t units64 = (int64_t)f.num_layers * f.batch * f.num_kv_heads;
@@ -217,6 +219,7 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
     v.pool_pages = (int32_t)c->pool_pages; v.units = c->units;
     v.batch = c->B; v.hq = c->Hq; v.hkv = c->Hkv; v.group = G; v.d = c->d;
     v.sink = c->S; v.window = c->W;
+    v.recent_only = f.importance_mode == 1;
 
     const size_t U = (size_t)c->units;
     // hole lists: a unit cut from n <= cap to B leaves at most min(B, cap - B) holes

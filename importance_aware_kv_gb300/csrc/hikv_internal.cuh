@@ -49,6 +49,7 @@ struct View {
     int32_t units;
     int32_t batch, hq, hkv, group, d;
     int32_t sink, window;
+    int32_t recent_only;  // HiKV Stage I: decode steps add mass only to pos >= t - window
 };
 
 constexpr int kMaxCS = 16;   // most CTAs (cluster size) per unit in the decode kernel

@@ -532,7 +532,7 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                 const int j = j0 + q * NCT + ctid;
                 const bool fresh_slot = a.fused && t0 + j == sn;   // the new token: importance 0
                 iv[q] = (j < cnt && !fresh_slot) ? impg[t0 + j] : 0.f;
-                pv[q] = fresh_slot ? du.tnew : ((need_victim && j < cnt) ? posg[t0 + j] : 0);
+                pv[q] = fresh_slot ? du.tnew : (((need_victim || v.recent_only) && j < cnt) ? posg[t0 + j] : 0);
             }
         };
         load_imp(0);
@@ -643,7 +643,10 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                     float inc = 0.f;
 #pragma unroll
                     for (int h = 0; h < G; ++h) inc += exp2f(srow[h] - mf[h]) * li_[h];
-                    const float nw = iv[q] + inc;
+                    // HiKV Stage I: only the recent bank (and the token leaving it)
+                    // accumulates; older scores stay frozen
+                    const bool grows = !v.recent_only || pv[q] >= du.tnew - v.window;
+                    const float nw = grows ? iv[q] + inc : iv[q];
                     v.imp[(int64_t)u * v.cap + slot] = nw;
                     if (a.fused && slot == sn) {
                         v.pos[(int64_t)u * v.cap + slot] = du.tnew;

@@ -84,6 +84,17 @@ typedef struct {
                                (positions past the prompt contribute nothing), and
                                the cut then keeps the top pooled scores.  0 or 1 =>
                                plain window scores.  At most 64. */
+    int32_t importance_mode; /* 0: H2O -- every decode step adds each retained token's
+                               attention mass, summed over the group, to its score
+                               (blog sec. 3 "H2O").  1: HiKV Stage I -- only tokens
+                               of the recent bank (the recent_window newest
+                               positions and the one leaving it this step,
+                               pos >= t - W) accumulate; older scores are frozen
+                               (HiKV sec. III-B, Algorithm 1).  With budget 2W and
+                               no sinks this is HiKV's dual bank: the eviction of
+                               the lowest score outside the window is its "promote
+                               the ejected token only if it beats the important
+                               bank's minimum". */
 } hikv_config;
 
 /* Create a cache: allocates the page pool, page tables, per-slot importance

@@ -50,7 +50,7 @@ def _out_np(t: torch.Tensor) -> np.ndarray:
 class Lockstep:
     def __init__(self, w: W.Workload, seed=None, sample_layers=None, cs=None, budgets=None,
                  device="cuda", layer_chunk=None, full_cache=False, page_tokens=64,
-                 check_kv=True, full_twin_layers=None, pool_kernel=0):
+                 check_kv=True, full_twin_layers=None, pool_kernel=0, importance_mode=0):
         import importance_aware_kv_gb300 as hk
         self.hk = hk
         self.w = w
@@ -70,13 +70,15 @@ class Lockstep:
             self.cache = hk.Cache(hk.CacheConfig(
                 w.layers, w.batch, w.hq, w.hkv, w.d, w.dtype, w.sink, w.window,
                 self.budgets, w.total_positions, page_tokens=page_tokens,
-                max_window_queries=max(32, w.nq), pool_kernel=pool_kernel))
+                max_window_queries=max(32, w.nq), pool_kernel=pool_kernel,
+                importance_mode=importance_mode))
         finally:
             if cs is not None:
                 os.environ.pop("HIKV_DECODE_CS", None)
         bs = np.concatenate([self.budgets[l * w.hkv:(l + 1) * w.hkv] for l in self.sample])
         self.ora = oracle.Oracle(len(self.sample), w.batch, w.hq, w.hkv, w.d, w.sink, w.window, bs,
                                  out_bf16=(w.dtype == "bf16"), threads=os.cpu_count() or 1)
+        self.ora.set_recent_only(importance_mode == 1)
         self.rep = Report()
         self.upl = w.batch * w.hkv
         # optional twin: a no-eviction cache fed the same inputs, checked on

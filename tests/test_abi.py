@@ -50,6 +50,7 @@ def _cfg(hk, **kw):
     (dict(num_sink=-1), 1),
     (dict(pool_kernel=-1), 1),
     (dict(pool_kernel=65), 1),                                    # SnapKV kernel above 64
+    (dict(importance_mode=2), 1),
 ])
 def test_create_rejects_bad_config_on_host(hk, kw, status):
     with pytest.raises(hk.HikvError) as ei:

@@ -131,6 +131,23 @@ def test_snapkv_llama3_8b_layer():
     assert rep.evictions_checked == 64 * (1 + 256)
 
 
+@FUSED
+@pytest.mark.parametrize("kw", [
+    dict(sink=0, window=48, budget=96),                     # HiKV's equal split, no sinks
+    dict(sink=4, window=16, budget=96),
+    dict(sink=0, window=48, budget=96, dtype="f32", d=64, hq=4, hkv=2),
+])
+def test_hikv_recent_bank_importance(kw, fused):
+    _run(SMALL.with_(**kw), importance_mode=1, fused=fused)
+
+
+def test_hikv_dual_bank_llama3_8b_layer():
+    # budget 1024 split into a 512-token recent bank and a 512-token important bank
+    w = W.WORKLOADS[1].with_(sink=0, window=512)
+    rep = _run(w, importance_mode=1, fused=True)
+    assert rep.evictions_checked == 64 * (1 + 256)
+
+
 def test_snapkv_needs_the_uncut_prompt():
     import importance_aware_kv_gb300 as hk
     cfg = hk.CacheConfig(1, 1, 4, 2, 64, "bf16", 1, 4, [16, 16], 64, page_tokens=16, pool_kernel=5)
