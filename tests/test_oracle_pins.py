@@ -503,3 +503,31 @@ def test_dual_bank_eviction_matches_hikv_fifo_and_min_heap():
         pos, imp = O.state(0)
         assert sorted(important) + recent == list(pos), s_
         np.testing.assert_allclose(imp, [score[p] for p in pos], rtol=2e-6, atol=1e-7)
+
+
+# --------------------------------------------------------------------------
+# budget schedules (blog sec. 3 "PyramidKV", "DuoAttention")
+# --------------------------------------------------------------------------
+def test_pyramid_budgets_closed_forms():
+    from oracle import budgets
+    b = budgets.pyramid(5, 2, 100, 20, 1).reshape(5, 2)
+    assert np.all(b[:, 0] == b[:, 1])                  # one budget per layer
+    np.testing.assert_array_equal(b[:, 0], [180, 140, 100, 60, 20])   # C_max = 180 .. C_min, step 40
+    assert b[:, 0].mean() == 100                       # mean = C_avg
+    b = budgets.pyramid(4, 1, 10, 3, 1)                # 17, 12.33, 7.67, 3 -> nearest
+    np.testing.assert_array_equal(b, [17, 12, 8, 3])
+    b = budgets.pyramid(5, 1, 10, 9, 1)                # 11, 10.5, 10, 9.5, 9 -> halves go up
+    np.testing.assert_array_equal(b, [11, 11, 10, 10, 9])
+    assert np.all(np.diff(budgets.pyramid(32, 1, 2048, 256, 1)) <= 0)   # decaying
+    np.testing.assert_array_equal(budgets.pyramid(1, 3, 77, 10, 1), [77, 77, 77])
+    np.testing.assert_array_equal(budgets.pyramid(3, 1, 50, 10, 40), [90, 50, 40])   # raised to the floor
+    b = budgets.pyramid(3, 1, 11, 10, 1)               # 12, 11, 10
+    np.testing.assert_array_equal(b, [12, 11, 10])
+    b = budgets.pyramid(4, 1, 11, 10, 1)               # 12, 11.33, 10.67, 10 -> 12, 11, 11, 10
+    np.testing.assert_array_equal(b, [12, 11, 11, 10])
+
+
+def test_duo_budgets():
+    from oracle import budgets
+    mask = np.array([[1, 0, 0], [0, 1, 0]], dtype=np.uint8)
+    np.testing.assert_array_equal(budgets.duo(mask, 4096, 4, 256), [4096, 260, 260, 260, 4096, 260])
