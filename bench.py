@@ -164,7 +164,25 @@ def layer_chunk(w, max_bytes=2e9):
     return max(1, min(w.layers, int(max_bytes // max(1, per_layer))))
 
 
-def run_cpu_oracle(w, seed, steps, warmup, budget_s=20.0, layers=None):
+def schedule_budgets(w, seed, schedule):
+    """Budget table of a run: the workload's own, or a schedule computed by
+    the library -- "pyramid:AVG:MIN" (PyramidKV) or "duo:FRAC" (DuoAttention,
+    a seeded FRAC of the heads retrieval heads with the full cache)."""
+    import workloads as W
+    if schedule in (None, "", "workload"):
+        return W.budgets(w, seed)
+    import importance_aware_kv_gb300 as hk
+    kind, *args = schedule.split(":")
+    if kind == "pyramid":
+        avg, mn = int(args[0]), int(args[1])
+        return hk.budgets_pyramid(w.layers, w.hkv, avg, mn, max(1, w.sink + w.window))
+    if kind == "duo":
+        mask = W.retrieval_mask(w, float(args[0]), seed)
+        return hk.budgets_duo(mask, w.total_positions, w.sink, w.window)
+    raise ValueError(f"unknown schedule {schedule!r}")
+
+
+def run_cpu_oracle(w, seed, steps, warmup, budget_s=20.0, layers=None, budgets=None):
     """Time the oracle's decode loop (append -> decode -> evict when due) on the
     given layers (default all) and scale to whole-workload steps/s: a step of
     the workload needs every layer, so sampled rate x (sampled / all layers).
@@ -173,7 +191,7 @@ def run_cpu_oracle(w, seed, steps, warmup, budget_s=20.0, layers=None):
     import workloads as W
     threads = os.cpu_count() or 1
     layers = list(range(w.layers)) if layers is None else list(layers)
-    b_all = W.budgets(w, seed)
+    b_all = W.budgets(w, seed) if budgets is None else np.asarray(budgets, np.int32)
     bs = np.concatenate([b_all[l * w.hkv:(l + 1) * w.hkv] for l in layers])
     O = oracle.Oracle(len(layers), w.batch, w.hq, w.hkv, w.d, w.sink, w.window, bs,
                       out_bf16=(w.dtype == "bf16"), threads=threads)
@@ -253,7 +271,7 @@ def bench_gpu(args):
     L = w.layers
     KL = args.per_layer_steps if args.per_layer_steps >= 0 else (0 if L == 1 else 100)
     total_steps = Wu + K + K3 + KL + Ke
-    budgets = W.budgets(w, seed)
+    budgets = schedule_budgets(w, seed, args.schedule)
     cache = hk.Cache(hk.CacheConfig(w.layers, w.batch, w.hq, w.hkv, w.d, w.dtype, w.sink, w.window,
                                     budgets, w.prompt + total_steps + 1))
     stage("cache created")
@@ -442,6 +460,8 @@ def bench_gpu(args):
                    "kv_heads": w.hkv, "head_dim": w.d, "kv_dtype": w.dtype, "prompt": w.prompt,
                    "budget": w.budget, "sink": w.sink, "window": w.window,
                    "evict_every": E, "tokens_attended_per_unit_max": int(lens.max()) + 1,
+                   "budget_schedule": args.schedule or "workload",
+                   "tokens_attended_per_unit_mean": float(lens.mean()) + 1,
                    "decode_inputs": (f"{R} distinct steps" + (", cycled" if R < total_steps else "")),
                    "l2": "flushed between timed steps (256 MB write, outside the timed events)",
                    "parallelism": f"replicas x{world} (units sharded by rank, no collective)"},
@@ -461,7 +481,7 @@ def bench_gpu(args):
     }
     if rank == 0 and not args.no_cpu_baseline:
         val, cores, done, sample = run_cpu_oracle(w, seed, min(64, w.steps), 2, budget_s=20.0,
-                                                  layers=oracle_sample_layers(w))
+                                                  layers=oracle_sample_layers(w), budgets=budgets)
         line["cpu_baseline"] = {"value": val, "unit": "steps/s", "cores": cores, "kind": "oracle",
                                 "sample": sample}
     if rank == 0:
@@ -479,6 +499,8 @@ def main():
     ap.add_argument("--three-call-steps", type=int, default=500)
     ap.add_argument("--per-layer-steps", type=int, default=-1,
                     help="steps timed as one launch per layer (default 100 for multi-layer workloads)")
+    ap.add_argument("--schedule", default="workload",
+                    help='budgets: "workload", "pyramid:AVG:MIN" or "duo:FRAC"')
     ap.add_argument("--workload", type=int, default=WORKLOAD_INDEX,
                     help="workload index (default: the Llama-3-8B layer the metric is quoted on)")
     ap.add_argument("--spin-us", type=float, default=60.0)

@@ -29,7 +29,8 @@ HIKV_F32, HIKV_BF16 = 0, 1
 ABI_FUNCTIONS = ("hikv_create_cache", "hikv_destroy_cache", "hikv_append", "hikv_score_window",
                  "hikv_decode_step", "hikv_evict", "hikv_gather_retained", "hikv_get_lengths",
                  "hikv_device_status", "hikv_last_error", "hikv_score_window_noalloc",
-                 "hikv_decode_step_fused", "hikv_kernel_launches")
+                 "hikv_decode_step_fused", "hikv_kernel_launches", "hikv_budgets_pyramid",
+                 "hikv_budgets_duo")
 
 
 class HikvError(RuntimeError):
@@ -69,6 +70,8 @@ def _load():
         "hikv_score_window_noalloc": ([I32] * 8 + [ctypes.c_float, P, P, P, P], S),
         "hikv_decode_step_fused": ([P, I32, I32, P, P, P, P, I32, P], S),
         "hikv_kernel_launches": ([P], ctypes.c_int64),
+        "hikv_budgets_pyramid": ([I32, I32, I32, I32, I32, P], S),
+        "hikv_budgets_duo": ([I32, I32, P, I32, I32, I32, P], S),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -162,6 +165,25 @@ def hikv_decode_step_fused(h, layer0: int, k, v, q, out, evict: bool = True, str
     _check(_lib.hikv_decode_step_fused(h, layer0, q.shape[0], _dev(k, "k"), _dev(v, "v", k.dtype, k.shape),
                                        _dev(q, "q", k.dtype), _dev(out, "out", q.dtype, q.shape),
                                        1 if evict else 0, _stream(stream)))
+
+
+def budgets_pyramid(num_layers: int, num_kv_heads: int, avg: int, min_budget: int,
+                    floor_budget: int = 1) -> np.ndarray:
+    """PyramidKV per-layer budgets, [num_layers * num_kv_heads] int32 (C ABI)."""
+    out = np.empty(num_layers * num_kv_heads, dtype=np.int32)
+    _check(_lib.hikv_budgets_pyramid(num_layers, num_kv_heads, avg, min_budget, floor_budget, out.ctypes.data))
+    return out
+
+
+def budgets_duo(retrieval, full_budget: int, num_sink: int, recent_window: int) -> np.ndarray:
+    """DuoAttention budgets from a [num_layers][num_kv_heads] retrieval-head mask (C ABI)."""
+    m = np.ascontiguousarray(np.asarray(retrieval, dtype=bool), dtype=np.uint8)
+    if m.ndim != 2:
+        raise ValueError("retrieval must be [num_layers][num_kv_heads]")
+    out = np.empty(m.size, dtype=np.int32)
+    _check(_lib.hikv_budgets_duo(m.shape[0], m.shape[1], m.ctypes.data, full_budget, num_sink, recent_window,
+                                 out.ctypes.data))
+    return out
 
 
 def hikv_evict(h, layer0: int, nlayers: int, stream=None) -> None:

@@ -603,7 +603,7 @@ hikv_status hikv_evict(hikv_cache* c, int32_t layer0, int32_t nl, hikv_stream_t 
         const int Bu = c->budget_unit[u];
         if (c->len[u] > Bu) {
             c->len[u] = Bu;
-            const int keep = std::min(ceil_div(Bu + 1, c->P), c->max_pages);
+            const int keep = pages_kept(Bu, c->P, c->max_pages);
             if (c->mapped[u] > keep) {
                 c->pages_in_use -= c->mapped[u] - keep;
                 c->mapped[u] = keep;
@@ -647,6 +647,37 @@ hikv_status hikv_get_lengths(const hikv_cache* c, int32_t layer0, int32_t nl, in
 }
 
 int64_t hikv_kernel_launches(const hikv_cache* c) { return c ? c->launches : -1; }
+
+hikv_status hikv_budgets_pyramid(int32_t num_layers, int32_t num_kv_heads, int32_t avg, int32_t min_budget,
+                                 int32_t floor_budget, int32_t* out) {
+    g_err.clear();
+    if (num_layers < 1 || num_kv_heads < 1 || !out || min_budget < 0 || min_budget > avg || avg < 1 ||
+        floor_budget < 0 || avg > (1 << 29))
+        return fail(HIKV_ERR_INVALID_ARG, "budgets_pyramid: bad arguments");
+    const int64_t cmax = 2 * (int64_t)avg - min_budget, cmin = min_budget, den = num_layers - 1;
+    for (int32_t l = 0; l < num_layers; ++l) {
+        int64_t c = avg;
+        if (den > 0) {
+            // round_half_up(cmax - l (cmax - cmin) / den) = floor((2 (cmax den - l (cmax - cmin)) + den) / (2 den))
+            const int64_t num = 2 * (cmax * den - (int64_t)l * (cmax - cmin)) + den;
+            c = num >= 0 ? num / (2 * den) : -((-num + 2 * den - 1) / (2 * den));
+        }
+        c = std::max<int64_t>(c, floor_budget);
+        for (int32_t h = 0; h < num_kv_heads; ++h) out[(int64_t)l * num_kv_heads + h] = (int32_t)c;
+    }
+    return HIKV_OK;
+}
+
+hikv_status hikv_budgets_duo(int32_t num_layers, int32_t num_kv_heads, const uint8_t* retrieval,
+                             int32_t full_budget, int32_t num_sink, int32_t recent_window, int32_t* out) {
+    g_err.clear();
+    if (num_layers < 1 || num_kv_heads < 1 || !retrieval || !out || num_sink < 0 || recent_window < 0 ||
+        full_budget < num_sink + recent_window)
+        return fail(HIKV_ERR_INVALID_ARG, "budgets_duo: bad arguments");
+    for (int64_t i = 0; i < (int64_t)num_layers * num_kv_heads; ++i)
+        out[i] = retrieval[i] ? full_budget : num_sink + recent_window;
+    return HIKV_OK;
+}
 
 hikv_status hikv_device_status(hikv_cache* c) {
     g_err.clear();

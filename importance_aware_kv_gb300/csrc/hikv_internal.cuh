@@ -54,6 +54,15 @@ struct View {
 
 constexpr int kMaxCS = 16;   // most CTAs (cluster size) per unit in the decode kernel
 
+// Pages a unit keeps after being cut to its budget B: room for B + kKeepSlack
+// tokens, so the appends of up to kKeepSlack steps before the next eviction
+// (a batched eviction interval) never need a page.
+constexpr int kKeepSlack = 16;
+__host__ __device__ inline int32_t pages_kept(int32_t B, int32_t page_tokens, int32_t max_pages) {
+    const int32_t k = (B + kKeepSlack + page_tokens - 1) / page_tokens;
+    return k < max_pages ? k : max_pages;
+}
+
 // Shape of the decode kernel for a K/V row of `row_bytes` and group size
 // `group`: CTAs resident per SM (its register cap and the host's grid sizing
 // follow it), consumer warps per CTA, and ring stages (tiles of 16 K + 16 V

@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kEvThreads) k_evict_general(EvictArgs a) {
         v.len[u] = B;
         v.victim[u] = -1;
         // return whole pages past slot B (one spare slot kept for the next append)
-        const int32_t keep = min(ceil_div(B + 1, v.page_tokens), v.max_pages);
+        const int32_t keep = pages_kept(B, v.page_tokens, v.max_pages);
         const int32_t m = v.mapped[u];
         if (m > keep) {
             const int32_t cnt = m - keep;

@@ -152,7 +152,8 @@ hikv_status hikv_decode_step_fused(hikv_cache* cache, int32_t layer0, int32_t nl
 /* Cut every unit of the range holding n > B_u tokens to exactly B_u:
  * keep sinks, recent window and the B_u - S - W highest-importance others
  * (ties keep the lower position), compact the survivors into slots
- * [0, B_u) and return whole pages beyond the unit's need to the pool.
+ * [0, B_u) and return to the pool the whole pages beyond room for B_u + 16
+ * tokens (so up to 16 more steps append without allocating).
  * Survivors keep their importance.  No-op for units with n <= B_u.  The
  * caller picks the interval: after every step, every E steps, or once after
  * prefill.  Errors: INVALID_ARG. */
@@ -172,6 +173,28 @@ hikv_status hikv_gather_retained(hikv_cache* cache, int32_t layer0, int32_t nlay
  * lengths_host: [nlayers * batch * Hkv].  Errors: INVALID_ARG. */
 hikv_status hikv_get_lengths(const hikv_cache* cache, int32_t layer0, int32_t nlayers,
                              int32_t* lengths_host);
+
+/* Budget schedules: host-only helpers that fill a budgets table for
+ * hikv_config (no device, no cache).  out_host: [num_layers * num_kv_heads].
+ *
+ * PyramidKV (KV cache compression blog, sec. 3 "PyramidKV"): layer l =
+ * 1..num_layers gets C_l = C_max - (l - 1)(C_max - C_min)/(num_layers - 1)
+ * with C_min = min_budget and C_max = 2 * avg - min_budget, so that the
+ * mean is avg; each C_l is rounded half up and raised to at least
+ * floor_budget (pass max(1, S + W)); one layer gets avg.  Every KV head of
+ * a layer shares the layer's budget.  HIKV_ERR_INVALID_ARG unless
+ * num_layers, num_kv_heads >= 1, 0 <= min_budget <= avg, floor_budget >= 0
+ * and out_host is non-null. */
+hikv_status hikv_budgets_pyramid(int32_t num_layers, int32_t num_kv_heads, int32_t avg, int32_t min_budget,
+                                 int32_t floor_budget, int32_t* out_host);
+
+/* DuoAttention (blog sec. 3 "DuoAttention"): heads flagged in retrieval_host
+ * ([num_layers * num_kv_heads], nonzero = retrieval head) keep the full
+ * cache (full_budget, e.g. max_tokens); the others, streaming heads, keep
+ * num_sink + recent_window tokens.  HIKV_ERR_INVALID_ARG on null pointers,
+ * sizes < 1 or full_budget < num_sink + recent_window. */
+hikv_status hikv_budgets_duo(int32_t num_layers, int32_t num_kv_heads, const uint8_t* retrieval_host,
+                             int32_t full_budget, int32_t num_sink, int32_t recent_window, int32_t* out_host);
 
 /* Number of kernels launched on the caller's streams through this cache
  * since it was created (every entry point counts what it enqueued; a call

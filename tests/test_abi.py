@@ -74,3 +74,24 @@ def test_create_without_device_reports_cuda(hk):
     with pytest.raises(hk.HikvError) as ei:
         hk.hikv_create_cache(_cfg(hk))
     assert ei.value.status == hk.HIKV_ERR_CUDA
+
+
+def test_budget_schedules_match_the_oracle(hk):
+    from oracle import budgets
+    rng = np.random.default_rng(7)
+    for L in (1, 2, 3, 5, 32, 80):
+        for hkv in (1, 8):
+            for avg, mn, fl in ((1024, 128, 68), (100, 20, 1), (10, 9, 1), (2048, 0, 260), (7, 7, 1)):
+                np.testing.assert_array_equal(hk.budgets_pyramid(L, hkv, avg, mn, fl),
+                                              budgets.pyramid(L, hkv, avg, mn, fl))
+        mask = rng.random((L, 8)) < 0.3
+        np.testing.assert_array_equal(hk.budgets_duo(mask, 4096, 4, 256), budgets.duo(mask, 4096, 4, 256))
+
+
+def test_budget_schedules_reject_bad_arguments(hk):
+    for args in ((0, 1, 10, 5, 1), (2, 1, 10, 11, 1), (2, 1, 0, 0, 1), (2, 1, 10, -1, 1), (2, 1, 10, 5, -1)):
+        with pytest.raises(hk.HikvError) as ei:
+            hk.budgets_pyramid(*args)
+        assert ei.value.status == hk.HIKV_ERR_INVALID_ARG
+    with pytest.raises(hk.HikvError):
+        hk.budgets_duo(np.ones((2, 2), bool), 100, 64, 64)   # full budget below S + W

@@ -148,6 +148,26 @@ def test_hikv_dual_bank_llama3_8b_layer():
     assert rep.evictions_checked == 64 * (1 + 256)
 
 
+@FUSED
+def test_pyramidkv_layer_budgets(fused):
+    import importance_aware_kv_gb300 as hk
+    w = SMALL.with_(layers=4, sink=2, window=16)
+    b = hk.budgets_pyramid(w.layers, w.hkv, 96, 40, w.sink + w.window)
+    assert len(set(b.tolist())) == 4                 # a different budget per layer
+    _run(w, budgets=b, fused=fused)
+
+
+@FUSED
+def test_duoattention_retrieval_and_streaming_heads(fused):
+    import importance_aware_kv_gb300 as hk
+    w = SMALL.with_(layers=4, sink=4, window=16)
+    mask = W.retrieval_mask(w, 0.3, seed=5)
+    b = hk.budgets_duo(mask, w.total_positions, w.sink, w.window)
+    assert 0 < mask.sum() < mask.size
+    rep = _run(w, budgets=b, fused=fused)
+    assert rep.evictions_checked > 0
+
+
 def test_snapkv_needs_the_uncut_prompt():
     import importance_aware_kv_gb300 as hk
     cfg = hk.CacheConfig(1, 1, 4, 2, 64, "bf16", 1, 4, [16, 16], 64, page_tokens=16, pool_kernel=5)

@@ -151,6 +151,18 @@ def budgets(w: Workload, seed: Optional[int] = None) -> np.ndarray:
     return np.full(n, int(w.budget), dtype=np.int32)
 
 
+def retrieval_mask(w: Workload, frac: float, seed: Optional[int] = None) -> np.ndarray:
+    """A seeded choice of DuoAttention retrieval heads: round(frac * heads) of
+    the layers * hkv (layer, KV head) pairs, [layers][hkv] bool.  (The pages
+    identify them by a trained gate; synthetic runs draw them.)"""
+    seed = w.index if seed is None else seed
+    n = w.layers * w.hkv
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 0xD0A7])))
+    m = np.zeros(n, dtype=bool)
+    m[rng.permutation(n)[: int(round(frac * n))]] = True
+    return m.reshape(w.layers, w.hkv)
+
+
 def heavy_scale(w: Workload, seed: int, layer: int, batch: int, upto: int = 0) -> Optional[np.ndarray]:
     """Key scale per position [T] for one (layer, batch) sequence, where
     T = max(total_positions, upto): a run generating positions past the
