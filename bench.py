@@ -406,15 +406,18 @@ def bench_gpu(args):
                      "ms_per_step": sum(msl) / KL, "steps_per_s": KL / (sum(msl) / 1e3)}
         stage("per-layer steps done")
 
-    # ---- e2e through the C ABI with pinned host buffers ----
-    hk_k = torch.from_numpy(ks.view(np.int16) if ks.dtype == np.uint16 else ks).pin_memory()
-    hk_v = torch.from_numpy(vs.view(np.int16) if vs.dtype == np.uint16 else vs).pin_memory()
-    hk_q = torch.from_numpy(qs.view(np.int16) if qs.dtype == np.uint16 else qs).pin_memory()
-    k_dev = torch.empty(tuple(hk_k.shape[1:]), dtype=hk_k.dtype, device=dev)
-    v_dev = torch.empty_like(k_dev)
-    q_dev = torch.empty(tuple(hk_q.shape[1:]), dtype=hk_q.dtype, device=dev)
-    out_host = torch.empty(tuple(out.shape), dtype=out.dtype).pin_memory()
+    # ---- e2e through the C ABI with pinned host buffers: every step copies
+    # its k, v and q in (one packed copy) and the output back ----
+    def flat(a):
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).reshape(a.shape[0], -1)
+    packed = torch.cat([flat(ks), flat(vs), flat(qs)], dim=1).pin_memory()   # [R][k | v | q]
+    nk, nq_ = flat(ks).shape[1], flat(qs).shape[1]
+    in_dev = torch.empty(packed.shape[1], dtype=packed.dtype, device=dev)
     as_wdt = (lambda t: t.view(torch.bfloat16)) if w.dtype == "bf16" else (lambda t: t)
+    k_dev = as_wdt(in_dev[:nk]).view(ks.shape[1:])
+    v_dev = as_wdt(in_dev[nk:2 * nk]).view(vs.shape[1:])
+    q_dev = as_wdt(in_dev[2 * nk:2 * nk + nq_]).view(qs.shape[1:])
+    out_host = torch.empty(tuple(out.shape), dtype=out.dtype).pin_memory()
     torch.cuda.synchronize()
     e_start = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
@@ -423,16 +426,14 @@ def bench_gpu(args):
         r, ev_ = next_step()
         flush.fill_(float(i))
         e_start.record(stream)
-        k_dev.copy_(hk_k[r], non_blocking=True)
-        v_dev.copy_(hk_v[r], non_blocking=True)
-        q_dev.copy_(hk_q[r], non_blocking=True)
-        cache.step(as_wdt(k_dev), as_wdt(v_dev), as_wdt(q_dev), out, evict=ev_)
+        in_dev.copy_(packed[r], non_blocking=True)
+        cache.step(k_dev, v_dev, q_dev, out, evict=ev_)
         out_host.copy_(out, non_blocking=True)
         e_end.record(stream)
         e_end.synchronize()
         e2e_ms += e_start.elapsed_time(e_end)
     stage("e2e steps done")
-    h2d = hk_k[0].nbytes + hk_v[0].nbytes + hk_q[0].nbytes
+    h2d = packed[0].nbytes
     d2h = out_host.nbytes
     cache.device_status()
     lens = cache.lengths()

@@ -104,12 +104,14 @@ __global__ void __launch_bounds__(kEvThreads) k_evict_general(EvictArgs a) {
     const float* imp = v.imp + (int64_t)u * v.cap;
     const int32_t* pos = v.pos + (int64_t)u * v.cap;
 
-    __shared__ uint32_t hist[256];
+    __shared__ uint32_t hist[kEvWarps][256];   // per-warp histograms
     __shared__ unsigned long long s_prefix, s_mask;
     __shared__ int32_t s_rem;
     __shared__ int32_t wsum[kEvWarps];
+    __shared__ int32_t mv_src[kEvThreads], mv_dst[kEvThreads];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
-    // --- radix select of the kmid-th largest candidate key ---
+    // --- radix select of the kmid-th largest candidate key, 8 bits a pass ---
     if (threadIdx.x == 0) {
         s_prefix = 0ull;
         s_mask = 0ull;
@@ -119,30 +121,59 @@ __global__ void __launch_bounds__(kEvThreads) k_evict_general(EvictArgs a) {
     if (kmid > 0) {
         for (int pass = 0; pass < 8; ++pass) {
             const int shift = 56 - 8 * pass;
-            for (int i = threadIdx.x; i < 256; i += kEvThreads) hist[i] = 0;
+            for (int i = threadIdx.x; i < kEvWarps * 256; i += kEvThreads) (&hist[0][0])[i] = 0;
             __syncthreads();
             const unsigned long long prefix = s_prefix, mask = s_mask;
-            for (int32_t s = threadIdx.x; s < n; s += kEvThreads) {
-                const int32_t p = pos[s];
-                if (p < lo || p > hi) continue;
-                const unsigned long long key = mk_key(imp[s], p);
-                if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+            // keys of a candidate set share their high bits, so most fall in
+            // a few bins: lanes with the same bin add once per warp
+            for (int32_t s0 = 0; s0 < n; s0 += kEvThreads) {
+                const int32_t s = s0 + threadIdx.x;
+                uint32_t bin = 256u;   // no bin
+                if (s < n) {
+                    const int32_t p = pos[s];
+                    if (p >= lo && p <= hi) {
+                        const unsigned long long key = mk_key(imp[s], p);
+                        if ((key & mask) == prefix) bin = (uint32_t)(key >> shift) & 255u;
+                    }
+                }
+                const unsigned peers = __match_any_sync(0xffffffffu, bin);
+                if (bin < 256u && lane == __ffs(peers) - 1) atomicAdd(&hist[warp][bin], (uint32_t)__popc(peers));
             }
             __syncthreads();
-            if (threadIdx.x == 0) {
-                int32_t rem = s_rem, cum = 0, sel = 0;
-                for (int bin = 255; bin >= 0; --bin) {
-                    const int32_t h = (int32_t)hist[bin];
-                    if (cum + h >= rem) {
-                        sel = bin;
-                        rem -= cum;
-                        break;
-                    }
-                    cum += h;
+            if (warp == 0) {
+                // lane l owns bins 8l .. 8l+7; find, from the top bin down, the
+                // bin where the running count reaches rem
+                uint32_t c[8];
+                int32_t tot = 0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    uint32_t x = 0;
+                    for (int w = 0; w < kEvWarps; ++w) x += hist[w][8 * lane + j];
+                    c[j] = x;
+                    tot += (int32_t)x;
                 }
-                s_rem = rem;
-                s_prefix = prefix | ((unsigned long long)sel << shift);
-                s_mask = mask | (255ull << shift);
+                int32_t incl = tot;   // bins of lanes >= this one
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int32_t y = __shfl_down_sync(0xffffffffu, incl, o);
+                    if (lane + o < 32) incl += y;
+                }
+                const int32_t above = incl - tot;   // bins of lanes > this one
+                const int32_t rem = s_rem;
+                if (above < rem && rem <= incl) {
+                    int32_t cum = above, sel = 8 * lane, r = rem;
+                    for (int j = 7; j >= 0; --j) {
+                        if (cum + (int32_t)c[j] >= rem) {
+                            sel = 8 * lane + j;
+                            r = rem - cum;
+                            break;
+                        }
+                        cum += (int32_t)c[j];
+                    }
+                    s_rem = r;
+                    s_prefix = prefix | ((unsigned long long)sel << shift);
+                    s_mask = mask | (255ull << shift);
+                }
             }
             __syncthreads();
         }
@@ -172,7 +203,9 @@ __global__ void __launch_bounds__(kEvThreads) k_evict_general(EvictArgs a) {
     __syncthreads();
     const int32_t nholes = min(base, hole_cap);
 
-    // --- movers: survivors in [B, n), ascending; k-th mover -> k-th hole ---
+    // --- movers: survivors in [B, n), ascending; k-th mover -> k-th hole.
+    // Each batch of 256 slots lists its movers, then the warps copy them,
+    // one 2-row move per warp (a lane per 16-byte chunk) ---
     base = 0;
     for (int32_t s0 = B; s0 < n; s0 += kEvThreads) {
         const int32_t s = s0 + threadIdx.x;
@@ -180,10 +213,18 @@ __global__ void __launch_bounds__(kEvThreads) k_evict_general(EvictArgs a) {
         int32_t tot;
         const int32_t r = block_rank(f, wsum, &tot);
         if (f) {
-            if (base + r < nholes) move_slot(v, u, s, holes[base + r], 0, 1);
-            else atomicOr(v.err, DEVERR_STATE);
+            if (base + r < nholes) {
+                mv_src[r] = s;
+                mv_dst[r] = holes[base + r];
+            } else {
+                atomicOr(v.err, DEVERR_STATE);
+            }
         }
+        __syncthreads();
+        const int32_t cnt = min(tot, max(0, nholes - base));
+        for (int32_t m = warp; m < cnt; m += kEvWarps) move_slot(v, u, mv_src[m], mv_dst[m], lane, 32);
         base += tot;
+        __syncthreads();   // the mover list is rewritten by the next batch
     }
     __syncthreads();
     if (threadIdx.x == 0) {
