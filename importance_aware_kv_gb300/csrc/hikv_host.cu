@@ -12,6 +12,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <numeric>
+#include <queue>
 #include <string>
 #include <vector>
 
@@ -95,6 +96,20 @@ struct hikv_cache {
     int32_t* d_order_all = nullptr;
     int32_t* d_order_layer = nullptr;
     std::vector<int32_t> order_all, order_layer;   // host copies: units by budget, descending
+    // balanced unit-to-cluster assignment of ragged decode calls (device copy
+    // [units] list + [clusters + 1] offsets), recomputed when its inputs change
+    // Device layout: [units] lists (a call over units [u0, u0 + nu) keeps its
+    // list at [u0, ...)) + per first layer of a call an offsets region, so the
+    // per-layer calls of a step each keep theirs and re-upload nothing while
+    // their lengths repeat.
+    int32_t* d_assign = nullptr;        // clusters: [units] + [L][max clusters + 1]
+    std::vector<int32_t> asg;
+    std::vector<uint64_t> asg_key;      // [L]
+    // the same for the warp-per-unit kernel's per-warp unit lists
+    int32_t* d_sassign = nullptr;       // [units] + [L][4 * max CTAs + 1]
+    std::vector<int32_t> sasg;
+    std::vector<uint64_t> sasg_key;     // [L]
+    int small_mode = 1;                 // HIKV_DECODE_SMALL (tuning): 0 never, 1 auto, 2 always when eligible
     CUtensorMap tmap;                   // the pool as rows of d elements, 16 x 128-byte swizzled boxes
     std::vector<void*> allocs;
     // host mirror
@@ -197,6 +212,7 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
     for (int u = 0; u < c->units; ++u)
         c->budget_unit[u] = f.budgets[(u / c->per_layer) * c->Hkv + u % c->Hkv];
     if (const char* e = std::getenv("HIKV_DECODE_CS")) c->cs_override = std::atoi(e);
+    if (const char* e = std::getenv("HIKV_DECODE_SMALL")) c->small_mode = std::atoi(e);
 
     cudaError_t e = cudaGetDevice(&c->device);
     if (e != cudaSuccess) { delete c; return cuda_fail(e, "create: cudaGetDevice"); }
@@ -259,6 +275,10 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
     ALLOC(c->d_wpart, U * c->wchunks * (size_t)c->max_wq * G * 2);
     ALLOC(c->d_order_all, U);
     ALLOC(c->d_order_layer, U);
+    ALLOC(c->d_assign, U + (size_t)c->L * (c->dec_occ * c->sm_count + 1));
+    ALLOC(c->d_sassign, U + (size_t)c->L * (kSmallWarps * c->dec_occ * c->sm_count + 1));
+    c->asg_key.assign(c->L, 0);
+    c->sasg_key.assign(c->L, 0);
     if (need_logits) ALLOC(c->d_logits, U * (size_t)c->cap * G);
 #undef ALLOC
 
@@ -439,34 +459,61 @@ namespace {
 // fused = 1 the kernel first appends one token per unit (rows new_k/new_v)
 // and, with evict = 1, moves it into the victim's slot when the unit is over
 // budget; the host mirror then already holds the post-append lengths.
-hikv_status launch_decode_call(hikv_cache* c, int32_t layer0, int32_t nl, const void* q, void* out,
-                               int fused, int evict, const void* new_k, const void* new_v,
-                               hikv_stream_t stream, const char* who) {
-    const int u0 = layer0 * c->per_layer, nu = nl * c->per_layer;
-    int maxn = 0;
-    bool uni_len = true, uni_b = true, uni_np = true;
-    for (int u = u0; u < u0 + nu; ++u) {
-        const int n = c->len[u] + fused;
-        if (n < 1) return fail(HIKV_ERR_STATE, "%s: unit %d is empty", who, u);
-        maxn = std::max(maxn, n);
-        uni_len &= c->len[u] == c->len[u0];
-        uni_b &= c->budget_unit[u] == c->budget_unit[u0];
-        uni_np &= c->next_pos[u] == c->next_pos[u0];
+// Deal `units` (sorted by size, largest first) to `bins` bins, each to the
+// least-loaded bin (LPT); writes the bin-major list and bin offsets into
+// out [units.size() + bins + 1].
+void lpt_assign(const std::vector<int32_t>& units, const std::vector<int64_t>& load, int bins,
+                std::vector<int32_t>& out) {
+    const int n = (int)units.size();
+    std::vector<int32_t> owner(n), count(bins, 0);
+    std::priority_queue<std::pair<int64_t, int32_t>, std::vector<std::pair<int64_t, int32_t>>,
+                        std::greater<std::pair<int64_t, int32_t>>> heap;
+    for (int j = 0; j < bins; ++j) heap.push({0, j});
+    for (int i = 0; i < n; ++i) {
+        auto [l, j] = heap.top();
+        heap.pop();
+        owner[i] = j;
+        ++count[j];
+        heap.push({l + load[i], j});
     }
-    // CTAs per unit (cluster size cs): the persistent clusters take the units
-    // in launch order, cluster j the j-th, (j + n_clusters)-th, ... -- so the
-    // first cluster, which gets the largest unit of every round, bounds the
-    // step.  Its work is modelled in tokens per CTA plus a fixed per-unit cost
-    // (exchanges, importance pass, victim) worth kUnitCostTokens tokens, a fit
-    // to the measured decode times; cs minimises it.  The logits of a chunk too
-    // large for shared memory go to the global buffer, when there is one.
-    const int32_t* ord = (nl == c->L) ? c->order_all.data() : c->order_layer.data() + u0;
-    const bool identity = uni_b;   // equal budgets: launch order is the identity
+    out.assign((size_t)n + bins + 1, 0);
+    int32_t* off = out.data() + n;
+    for (int j = 0; j < bins; ++j) off[j + 1] = off[j] + count[j];
+    std::vector<int32_t> fill(off, off + bins);
+    for (int i = 0; i < n; ++i) out[fill[owner[i]]++] = units[i];   // largest first within a bin
+}
+
+uint64_t fnv_mix(uint64_t h, uint64_t x) { return (h ^ x) * 1099511628211ull; }
+
+// The cluster kernel over all units of the range (equal budgets: identity
+// order) or over `subset` (ragged: largest first, dealt by LPT).
+hikv_status launch_clusters(hikv_cache* c, int32_t layer0, int32_t nl, const std::vector<int32_t>* subset,
+                            bool uni_len, bool uni_b, bool uni_np, const void* q, void* out, int fused,
+                            int evict, const void* new_k, const void* new_v, hikv_stream_t stream,
+                            const char* who) {
+    const int u0 = layer0 * c->per_layer;
+    const int nu = subset ? (int)subset->size() : nl * c->per_layer;
+    auto unit_at = [&](int i) { return subset ? (*subset)[i] : u0 + i; };
+    int maxn = 0;
+    int64_t total = 0;
+    for (int i = 0; i < nu; ++i) {
+        const int n = c->len[unit_at(i)] + fused;
+        maxn = std::max(maxn, n);
+        total += n;
+    }
+    // CTAs per unit (cluster size cs) by a cost model of the busiest cluster:
+    // tokens per CTA plus a fixed per-unit cost (exchanges, importance pass,
+    // victim) worth kUnitCostTokens tokens, a fit to the measured decode
+    // times.  Equal units go round-robin, so the busiest cluster gets
+    // ceil(units / clusters) of them; ragged ones are dealt by LPT, whose
+    // busiest cluster is about max(average load, largest unit).  The logits
+    // of a chunk too large for shared memory go to the global buffer, when
+    // there is one.
+    constexpr int64_t kUnitCostTokens = 190;
     int cs = 1;
     if (c->cs_override > 0) {
         cs = std::min(c->cs_override, kMaxCS);
     } else {
-        constexpr int64_t kUnitCostTokens = 190;
         const int slots = c->dec_occ * c->sm_count;
         int64_t best = INT64_MAX;
         for (int k = 1; k <= std::min(kMaxCS, maxn); ++k) {
@@ -477,10 +524,12 @@ hikv_status launch_decode_call(hikv_cache* c, int32_t layer0, int32_t nl, const 
             int ncl = std::max(1, std::min(nu, slots / k));
             const int active = decode_active_clusters(c->dtype, c->d, c->G, sp, k, smem);
             if (active > 0) ncl = std::min(ncl, active);
-            int64_t cost = 0;
-            for (int i = 0; i < nu; i += ncl) {
-                const int u = identity ? u0 + i : ord[i];
-                cost += ceil_div(c->len[u] + fused, k) + kUnitCostTokens;
+            int64_t cost;
+            if (!subset) {
+                cost = (int64_t)ceil_div(nu, ncl) * (ceil_div(maxn, k) + kUnitCostTokens);
+            } else {
+                const int64_t sum = (total + (int64_t)nu * (k - 1)) / k + (int64_t)nu * kUnitCostTokens;
+                cost = std::max<int64_t>((sum + ncl - 1) / ncl, ceil_div(maxn, k) + kUnitCostTokens);
             }
             if (cost < best) {
                 best = cost;
@@ -493,6 +542,40 @@ hikv_status launch_decode_call(hikv_cache* c, int32_t layer0, int32_t nl, const 
     const bool smem_path = chunk <= c->max_smem_chunk;
     if (!smem_path && !c->d_logits)
         return fail(HIKV_ERR_UNSUPPORTED, "%s: %d tokens per CTA exceed shared memory", who, chunk);
+    const size_t smem = decode_smem_bytes(c->dtype, c->d, c->G, smem_path, smem_path ? chunk : 0);
+    // persistent clusters: at most one wave (the clusters that fit at once)
+    int ncl = std::max(1, std::min(nu, (c->dec_occ * c->sm_count) / cs));
+    {
+        const int active = decode_active_clusters(c->dtype, c->d, c->G, smem_path, cs, smem);
+        if (active > 0) ncl = std::min(ncl, active);
+    }
+    const int32_t* d_assign = nullptr;
+    const int32_t* d_assign_off = nullptr;
+    if (subset) {
+        uint64_t key = 1469598103934665603ull;
+        key = fnv_mix(key, (uint64_t)cs);
+        key = fnv_mix(key, (uint64_t)ncl);
+        key = fnv_mix(key, (uint64_t)fused);
+        for (int i = 0; i < nu; ++i) {
+            key = fnv_mix(key, (uint64_t)(uint32_t)(*subset)[i]);
+            key = fnv_mix(key, (uint64_t)(uint32_t)c->len[(*subset)[i]]);
+        }
+        d_assign = c->d_assign + u0;
+        d_assign_off = c->d_assign + c->units + (size_t)layer0 * (c->dec_occ * c->sm_count + 1);
+        if (key != c->asg_key[layer0]) {
+            std::vector<int64_t> load(nu);
+            for (int i = 0; i < nu; ++i) load[i] = ceil_div(c->len[(*subset)[i]] + fused, cs) + kUnitCostTokens;
+            lpt_assign(*subset, load, ncl, c->asg);
+            // pageable sources: the copies are staged before the calls return
+            cudaError_t e = cudaMemcpyAsync(const_cast<int32_t*>(d_assign), c->asg.data(), nu * sizeof(int32_t),
+                                            cudaMemcpyHostToDevice, (cudaStream_t)stream);
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync(const_cast<int32_t*>(d_assign_off), c->asg.data() + nu,
+                                    (ncl + 1) * sizeof(int32_t), cudaMemcpyHostToDevice, (cudaStream_t)stream);
+            if (e != cudaSuccess) return cuda_fail(e, who);
+            c->asg_key[layer0] = key;
+        }
+    }
     DecodeArgs a{};
     a.v = c->v;
     a.order = (nl == c->L) ? c->d_order_all : c->d_order_layer + u0;
@@ -506,24 +589,117 @@ hikv_status launch_decode_call(hikv_cache* c, int32_t layer0, int32_t nl, const 
     a.cand_slot = c->d_cand_slot;
     a.cs = cs;
     a.chunk_cap = smem_path ? chunk : 0;
-    a.uni_len = uni_len ? c->len[u0] + fused : -1;
-    a.uni_budget = uni_b ? c->budget_unit[u0] : -1;
-    a.uni_next_pos = uni_np ? c->next_pos[u0] + fused : -1;
-    a.identity_u0 = uni_b ? u0 : -1;   // equal budgets: launch order is the identity
-    // persistent clusters: at most one wave at the decode occupancy
-    a.n_clusters = std::max(1, std::min(nu, (c->dec_occ * c->sm_count) / cs));
+    a.uni_len = (!subset && uni_len) ? c->len[u0] + fused : -1;
+    a.uni_budget = (!subset && uni_b) ? c->budget_unit[u0] : -1;
+    a.uni_next_pos = (!subset && uni_np) ? c->next_pos[u0] + fused : -1;
+    a.identity_u0 = subset ? -1 : u0;
+    a.n_clusters = ncl;
+    a.assign = d_assign;
+    a.assign_off = d_assign_off;
     // small calls fit in L2: prefetch each CTA's tiles there ahead of the ring
-    const int64_t call_bytes = (int64_t)nu * maxn * 2 * c->d * c->esz;
+    const int64_t call_bytes = total * 2 * c->d * c->esz;
     a.prefetch_tiles = call_bytes <= (48ll << 20) ? 16 : 0;
     a.fused = fused;
     a.evict = evict;
     a.new_k = (const uint8_t*)new_k;
     a.new_v = (const uint8_t*)new_v;
-    const size_t smem = decode_smem_bytes(c->dtype, c->d, c->G, smem_path, a.chunk_cap);
     cudaError_t e = launch_decode(a, c->tmap, c->dtype, c->d, c->G, smem_path, smem, (cudaStream_t)stream);
     c->launches += 1;
     if (e != cudaSuccess) return cuda_fail(e, who);
     return HIKV_OK;
+}
+
+// The warp-per-unit kernel over `units` (largest first), dealt by LPT to
+// four warps per CTA.
+hikv_status launch_small(hikv_cache* c, int32_t layer0, const std::vector<int32_t>& units, const void* q,
+                         void* out, int fused, int evict, const void* new_k, const void* new_v,
+                         hikv_stream_t stream, const char* who) {
+    constexpr int64_t kWarpUnitCostTokens = 48;   // per-unit cost of a warp (its epilogue), in tokens
+    const int nu = (int)units.size();
+    const int n_ctas = std::max(1, std::min(c->dec_occ * c->sm_count, ceil_div(nu, kSmallWarps)));
+    const int warps = n_ctas * kSmallWarps;
+    uint64_t key = 7809847782465536322ull;
+    key = fnv_mix(key, (uint64_t)warps);
+    key = fnv_mix(key, (uint64_t)fused);
+    for (int i = 0; i < nu; ++i) {
+        key = fnv_mix(key, (uint64_t)(uint32_t)units[i]);
+        key = fnv_mix(key, (uint64_t)(uint32_t)c->len[units[i]]);
+    }
+    const int32_t u0 = layer0 * c->per_layer;
+    int32_t* d_list = c->d_sassign + u0;
+    int32_t* d_off = c->d_sassign + c->units + (size_t)layer0 * (kSmallWarps * c->dec_occ * c->sm_count + 1);
+    if (key != c->sasg_key[layer0]) {
+        std::vector<int64_t> load(nu);
+        for (int i = 0; i < nu; ++i) load[i] = c->len[units[i]] + fused + kWarpUnitCostTokens;
+        lpt_assign(units, load, warps, c->sasg);
+        cudaError_t e = cudaMemcpyAsync(d_list, c->sasg.data(), nu * sizeof(int32_t), cudaMemcpyHostToDevice,
+                                        (cudaStream_t)stream);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(d_off, c->sasg.data() + nu, (warps + 1) * sizeof(int32_t), cudaMemcpyHostToDevice,
+                                (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_fail(e, who);
+        c->sasg_key[layer0] = key;
+    }
+    SmallArgs a{};
+    a.v = c->v;
+    a.list = d_list;
+    a.warp_off = d_off;
+    a.layer0 = layer0;
+    a.q = (const uint8_t*)q;
+    a.out = (uint8_t*)out;
+    a.qscale = c->scale * 1.4426950408889634f;
+    a.fused = fused;
+    a.evict = evict;
+    a.new_k = (const uint8_t*)new_k;
+    a.new_v = (const uint8_t*)new_v;
+    cudaError_t e = launch_decode_small(a, c->tmap, c->dtype, c->d, c->G, n_ctas, (cudaStream_t)stream);
+    c->launches += 1;
+    if (e != cudaSuccess) return cuda_fail(e, who);
+    return HIKV_OK;
+}
+
+// Launch the decode kernels over the units of [layer0, layer0 + nl).  With
+// fused = 1 they first append one token per unit (rows new_k/new_v) and,
+// with evict = 1, move it into the victim's slot when the unit is over
+// budget; the host mirror then already holds the post-append lengths.
+// Equal budgets: one cluster-kernel launch.  Ragged budgets (group <= 4):
+// units of at most small_unit_cap(G) tokens go to the warp-per-unit kernel,
+// the others to the cluster kernel.
+hikv_status launch_decode_call(hikv_cache* c, int32_t layer0, int32_t nl, const void* q, void* out,
+                               int fused, int evict, const void* new_k, const void* new_v,
+                               hikv_stream_t stream, const char* who) {
+    const int u0 = layer0 * c->per_layer, nu = nl * c->per_layer;
+    bool uni_len = true, uni_b = true, uni_np = true;
+    for (int u = u0; u < u0 + nu; ++u) {
+        const int n = c->len[u] + fused;
+        if (n < 1) return fail(HIKV_ERR_STATE, "%s: unit %d is empty", who, u);
+        uni_len &= c->len[u] == c->len[u0];
+        uni_b &= c->budget_unit[u] == c->budget_unit[u0];
+        uni_np &= c->next_pos[u] == c->next_pos[u0];
+    }
+    if (uni_b)
+        return launch_clusters(c, layer0, nl, nullptr, uni_len, uni_b, uni_np, q, out, fused, evict, new_k, new_v,
+                               stream, who);
+    std::vector<int32_t> units(nu);
+    std::iota(units.begin(), units.end(), u0);
+    std::stable_sort(units.begin(), units.end(), [&](int x, int y) { return c->len[x] > c->len[y]; });
+    // split only when the small units are enough to occupy the GPU by
+    // themselves: each launch has a fixed latency of its own, and a call of
+    // few units (one layer of a model) is better served by one launch
+    std::vector<int32_t> big, small;
+    bool split = c->G <= kSmallWarps && c->small_mode != 0 && c->cs_override <= 0;
+    if (split && c->small_mode == 1) {
+        int nsmall = 0;
+        for (int32_t u : units) nsmall += c->len[u] + fused <= small_unit_cap(c->G);
+        split = nsmall >= 2 * c->sm_count;
+    }
+    for (int32_t u : units) (split && c->len[u] + fused <= small_unit_cap(c->G) ? small : big).push_back(u);
+    hikv_status st = HIKV_OK;
+    if (!big.empty())
+        st = launch_clusters(c, layer0, nl, &big, false, false, false, q, out, fused, evict, new_k, new_v, stream, who);
+    if (st == HIKV_OK && !small.empty())
+        st = launch_small(c, layer0, small, q, out, fused, evict, new_k, new_v, stream, who);
+    return st;
 }
 
 }  // namespace

@@ -418,6 +418,10 @@ struct DecodeArgs {
     // dependent loads before its first copy can be issued
     int32_t uni_len, uni_budget, uni_next_pos;
     int32_t identity_u0;    // >= 0: unit of list index i is identity_u0 + i (order unused)
+    // when set, cluster j takes the units assign[assign_off[j] .. assign_off[j+1])
+    // (a balanced assignment) instead of every n_clusters-th of the launch order
+    const int32_t* assign;
+    const int32_t* assign_off;
     int32_t prefetch_tiles; // L2 prefetch distance in tiles (0: off)
     int32_t n_clusters;     // persistent clusters launched; cluster y handles list indices y, y + n_clusters, ...
     // fused step (append + decode + one-token evict in one launch): fused = 1,
@@ -433,6 +437,26 @@ size_t decode_smem_bytes(int dtype, int d, int group, bool smem_path, int chunk_
 int decode_max_smem_chunk(int dtype, int d, int group, size_t smem_limit);
 // clusters of `cs` decode CTAs of `smem_bytes` each that fit on the GPU at once
 int decode_active_clusters(int dtype, int d, int group, bool smem_path, int cs, size_t smem_bytes);
+
+// Small-unit decode: one consumer warp per unit (units of at most
+// small_unit_cap(G) tokens; group sizes up to 4), same arithmetic as k_decode.
+constexpr int kSmallWarps = 4;              // consumer warps per CTA (one unit each)
+constexpr int kSmallLogitFloats = 1536;     // logits kept per warp: tokens x G
+__host__ __device__ constexpr int small_unit_cap(int G) { return kSmallLogitFloats / G; }
+struct SmallArgs {
+    View v;
+    const int32_t* list;      // unit ids, warp-major
+    const int32_t* warp_off;  // [n_warps + 1]: warp i takes list[warp_off[i] .. warp_off[i+1])
+    int32_t layer0;
+    const uint8_t* q;
+    uint8_t* out;
+    float qscale;             // scale * log2(e)
+    int32_t fused, evict;     // as in DecodeArgs
+    const uint8_t* new_k;
+    const uint8_t* new_v;
+};
+cudaError_t launch_decode_small(const SmallArgs& a, const CUtensorMap& tmap, int dtype, int d, int group,
+                                int n_ctas, cudaStream_t s);
 
 struct EvictArgs {
     View v;

@@ -126,7 +126,7 @@ struct DecUnit {
 // include the append.)
 __device__ __forceinline__ DecUnit dec_unit(const DecodeArgs& a, int32_t idx) {
     DecUnit r;
-    r.u = a.identity_u0 >= 0 ? a.identity_u0 + idx : a.order[idx];
+    r.u = a.assign ? a.assign[idx] : (a.identity_u0 >= 0 ? a.identity_u0 + idx : a.order[idx]);
     r.n = a.uni_len >= 0 ? a.uni_len : a.v.len[r.u] + a.fused;
     r.Bu = a.uni_budget >= 0 ? a.uni_budget : a.v.budget[r.u];
     r.tnew = (a.uni_next_pos >= 0 ? a.uni_next_pos : a.v.next_pos[r.u] + a.fused) - 1;
@@ -191,10 +191,15 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
     const int32_t c = (int32_t)cluster_ctarank();
     const int32_t CS = (int32_t)cluster_nctarank();
 
+    // this cluster's units: list indices it0, it0 + istep, ... < it1
+    const int32_t it0 = a.assign_off ? a.assign_off[blockIdx.y] : (int32_t)blockIdx.y;
+    const int32_t it1 = a.assign_off ? a.assign_off[blockIdx.y + 1] : a.n_units;
+    const int32_t istep = a.assign_off ? 1 : a.n_clusters;
+
     // producer: the first unit's page ids, loaded while the barriers are set up
     int32_t pre_pg = -1;
-    if (warp == kDecNCW && (int32_t)blockIdx.y < a.n_units) {
-        const DecUnit du = dec_unit(a, blockIdx.y);
+    if (warp == kDecNCW && it0 < it1) {
+        const DecUnit du = dec_unit(a, it0);
         const int32_t chunk = ceil_div(du.n, CS);
         const int32_t t0 = min(du.n, c * chunk), t1 = min(du.n, t0 + chunk);
         const int32_t pg0 = t0 >> v.page_shift;
@@ -227,7 +232,7 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
         // ======================= producer =======================
         if (lane == 0) prefetch_tensormap(&tmap);
         int gi = 0;   // running tile counter of this CTA (lane 0's copy is authoritative)
-        for (int k = 0, idx = blockIdx.y; idx < a.n_units; ++k, idx += a.n_clusters) {
+        for (int k = 0, idx = it0; idx < it1; ++k, idx += istep) {
             if (*abort_flag) break;
             const DecUnit du = dec_unit(a, idx);
             const int32_t per_layer = v.batch * v.hkv;
@@ -326,7 +331,7 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
     const int pv_chunk = (lane * LB) >> 4, pv_in = (lane * LB) & 15;
     int gi_base = 0;
 
-    for (int k = 0, idx = blockIdx.y; idx < a.n_units; ++k, idx += a.n_clusters) {
+    for (int k = 0, idx = it0; idx < it1; ++k, idx += istep) {
         const DecUnit du = dec_unit(a, idx);
         const int32_t u = du.u;
         const int32_t n = du.n;
@@ -567,8 +572,24 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
             }
             m_c[ctid] = m;
             l_c[ctid] = l;
+            if (CS == 1) {   // a one-CTA unit's state is final
+                mfin[ctid] = m;
+                linv[ctid] = 1.0f / l;
+            }
         }
         named_bar_sync(1, NCT);
+        if (CS == 1) {
+            // no partners: the output straight from the merged warp partials
+            // (the general path's values: its weights are exactly 1 here)
+            T* outp = reinterpret_cast<T*>(a.out) + qbase;
+            for (int e = ctid; e < G * D; e += NCT) {
+                const int h = e / D;
+                float sum = 0.f;
+#pragma unroll
+                for (int w = 0; w < kDecNCW; ++w) sum += red[w * G * D + e] * wsc[w * G + h];
+                outp[e] = Elem<T>::from_f(sum * linv[h]);
+            }
+        } else {
         if (!cluster_ready) {   // partners' barriers are initialised from here on
             cluster_wait();
             cluster_ready = true;
@@ -619,6 +640,7 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                 outp[e] = Elem<T>::from_f(sum);
             }
         }
+        }   // CS > 1
         // importance update + local victim
         unsigned long long kmin = ~0ull;
         int32_t smin = -1;
@@ -685,13 +707,20 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                     kk = wkey[w];
                     sl = wslot[w];
                 }
-            dsmem_st_u64(dsmem_addr(&akey[c], 0u), kk);
-            dsmem_st_s32(dsmem_addr(&aslot[c], 0u), sl);
-            if (owns_new) dsmem_st_f32(dsmem_addr(aimp, 0u), *new_imp_s);
-            mbar_arrive_remote(dsmem_addr(&vbar[xb], 0u));
+            if (CS > 1) {
+                dsmem_st_u64(dsmem_addr(&akey[c], 0u), kk);
+                dsmem_st_s32(dsmem_addr(&aslot[c], 0u), sl);
+                if (owns_new) dsmem_st_f32(dsmem_addr(aimp, 0u), *new_imp_s);
+                mbar_arrive_remote(dsmem_addr(&vbar[xb], 0u));
+            } else if (owns_new) {
+                *aimp = *new_imp_s;
+            }
             if (c == 0) {
                 int32_t vs = -1;
-                if (!*abort_flag && mbar_wait_cluster_bounded(&vbar[xb], xpar, v.err, kWaitVictim, (uint32_t)k)) {
+                if (CS == 1) {
+                    vs = sl;
+                } else if (!*abort_flag &&
+                           mbar_wait_cluster_bounded(&vbar[xb], xpar, v.err, kWaitVictim, (uint32_t)k)) {
                     unsigned long long best = ~0ull;
                     for (int cc = 0; cc < CS; ++cc)
                         if (akey[cc] < best) {
@@ -857,5 +886,9 @@ size_t decode_smem_t(int group, bool smem_path, int chunk_cap) {
     int decode_active_##NAME(int group, bool smem_path, int cs, size_t smem) {                      \
         return smem_path ? decode_active_g<T, D, true>(group, cs, smem)                             \
                          : decode_active_g<T, D, false>(group, cs, smem);                           \
+    }                                                                                               \
+    cudaError_t decode_small_launch_##NAME(const SmallArgs& a, const CUtensorMap& tmap, int group,  \
+                                           int n_ctas, cudaStream_t s) {                            \
+        return decode_small_launch_g<T, D>(a, tmap, group, n_ctas, s);                              \
     }                                                                                               \
     }

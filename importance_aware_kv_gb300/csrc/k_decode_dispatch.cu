@@ -6,7 +6,8 @@ namespace hikv {
 #define HIKV_DECL(NAME)                                                                            \
     cudaError_t decode_launch_##NAME(const DecodeArgs&, const CUtensorMap&, int, bool, size_t, cudaStream_t); \
     size_t decode_smem_##NAME(int, bool, int);                                                     \
-    int decode_active_##NAME(int, bool, int, size_t);
+    int decode_active_##NAME(int, bool, int, size_t);                                               \
+    cudaError_t decode_small_launch_##NAME(const SmallArgs&, const CUtensorMap&, int, int, cudaStream_t);
 HIKV_DECL(f32_64)
 HIKV_DECL(f32_128)
 HIKV_DECL(bf16_64)
@@ -36,6 +37,15 @@ int decode_active_clusters(int dtype, int d, int group, bool smem_path, int cs, 
     if (dtype == 1 && d == 64) return decode_active_bf16_64(group, smem_path, cs, smem_bytes);
     if (dtype == 1 && d == 128) return decode_active_bf16_128(group, smem_path, cs, smem_bytes);
     return 0;
+}
+
+cudaError_t launch_decode_small(const SmallArgs& a, const CUtensorMap& tmap, int dtype, int d, int group,
+                                int n_ctas, cudaStream_t s) {
+    if (dtype == 0 && d == 64) return decode_small_launch_f32_64(a, tmap, group, n_ctas, s);
+    if (dtype == 0 && d == 128) return decode_small_launch_f32_128(a, tmap, group, n_ctas, s);
+    if (dtype == 1 && d == 64) return decode_small_launch_bf16_64(a, tmap, group, n_ctas, s);
+    if (dtype == 1 && d == 128) return decode_small_launch_bf16_128(a, tmap, group, n_ctas, s);
+    return cudaErrorInvalidValue;
 }
 
 // Largest chunk (tokens per CTA) whose logits fit the shared-memory path.

@@ -50,7 +50,7 @@ def _out_np(t: torch.Tensor) -> np.ndarray:
 class Lockstep:
     def __init__(self, w: W.Workload, seed=None, sample_layers=None, cs=None, budgets=None,
                  device="cuda", layer_chunk=None, full_cache=False, page_tokens=64,
-                 check_kv=True, full_twin_layers=None, pool_kernel=0, importance_mode=0):
+                 check_kv=True, full_twin_layers=None, pool_kernel=0, importance_mode=0, small_mode=None):
         import importance_aware_kv_gb300 as hk
         self.hk = hk
         self.w = w
@@ -66,6 +66,8 @@ class Lockstep:
         self.pool = pool_kernel
         if cs is not None:
             os.environ["HIKV_DECODE_CS"] = str(cs)
+        if small_mode is not None:
+            os.environ["HIKV_DECODE_SMALL"] = str(small_mode)
         try:
             self.cache = hk.Cache(hk.CacheConfig(
                 w.layers, w.batch, w.hq, w.hkv, w.d, w.dtype, w.sink, w.window,
@@ -75,6 +77,7 @@ class Lockstep:
         finally:
             if cs is not None:
                 os.environ.pop("HIKV_DECODE_CS", None)
+            os.environ.pop("HIKV_DECODE_SMALL", None)
         bs = np.concatenate([self.budgets[l * w.hkv:(l + 1) * w.hkv] for l in self.sample])
         self.ora = oracle.Oracle(len(self.sample), w.batch, w.hq, w.hkv, w.d, w.sink, w.window, bs,
                                  out_bf16=(w.dtype == "bf16"), threads=os.cpu_count() or 1)

@@ -97,9 +97,32 @@ def test_evict_every_16_batched_select(fused):
 
 
 @FUSED
-def test_ragged_budgets(fused):
+@pytest.mark.parametrize("small_mode", [2, 0, 1], ids=["warp_per_unit", "clusters_only", "auto"])
+def test_ragged_budgets(fused, small_mode):
+    # ragged budgets may route units of at most 384 tokens (G = 4) to the
+    # warp-per-unit kernel (2: always; 1: when they are many; 0: never)
     b = np.array([40, 96, 17 + 16, 200], dtype=np.int32)
-    _run(SMALL.with_(sink=1, window=16), budgets=b, fused=fused)
+    _run(SMALL.with_(sink=1, window=16), budgets=b, fused=fused, small_mode=small_mode)
+
+
+@FUSED
+def test_ragged_mix_of_small_and_large_units(fused):
+    # budgets on both sides of the small-unit cap: both kernels in one call
+    w = SMALL.with_(layers=4, prompt=1200, steps=24, sink=2, window=32)
+    b = np.array([40, 1000, 380, 385, 64, 700, 120, 383], dtype=np.int32)
+    _run(w, budgets=b, fused=fused, small_mode=2)
+
+
+@pytest.mark.parametrize("shape", [
+    dict(hq=2, hkv=2, d=64, dtype="f32"),        # G = 1
+    dict(hq=4, hkv=2, d=128, dtype="bf16"),      # G = 2
+    dict(hq=8, hkv=2, d=64, dtype="bf16"),
+    dict(hq=8, hkv=2, d=128, dtype="f32"),
+])
+def test_warp_per_unit_group_sizes_and_dtypes(shape):
+    b = np.array([40, 96, 33, 200], dtype=np.int32)
+    _run(SMALL.with_(sink=1, window=16, **shape), budgets=b, fused=True, small_mode=2)
+    _run(SMALL.with_(sink=1, window=16, **shape), budgets=b, importance_mode=1, small_mode=2)
 
 
 @FUSED
