@@ -110,6 +110,7 @@ struct hikv_cache {
     std::vector<int32_t> sasg;
     std::vector<uint64_t> sasg_key;     // [L]
     int small_mode = 1;                 // HIKV_DECODE_SMALL (tuning): 0 never, 1 auto, 2 always when eligible
+    int first_burst = 4;                // one tile per consumer warp first (HIKV_DECODE_BURST: tuning)
     CUtensorMap tmap;                   // the pool as rows of d elements, 16 x 128-byte swizzled boxes
     std::vector<void*> allocs;
     // host mirror
@@ -213,6 +214,7 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
         c->budget_unit[u] = f.budgets[(u / c->per_layer) * c->Hkv + u % c->Hkv];
     if (const char* e = std::getenv("HIKV_DECODE_CS")) c->cs_override = std::atoi(e);
     if (const char* e = std::getenv("HIKV_DECODE_SMALL")) c->small_mode = std::atoi(e);
+    if (const char* e = std::getenv("HIKV_DECODE_BURST")) c->first_burst = std::atoi(e);
 
     cudaError_t e = cudaGetDevice(&c->device);
     if (e != cudaSuccess) { delete c; return cuda_fail(e, "create: cudaGetDevice"); }
@@ -599,6 +601,7 @@ hikv_status launch_clusters(hikv_cache* c, int32_t layer0, int32_t nl, const std
     // small calls fit in L2: prefetch each CTA's tiles there ahead of the ring
     const int64_t call_bytes = total * 2 * c->d * c->esz;
     a.prefetch_tiles = call_bytes <= (48ll << 20) ? 16 : 0;
+    a.first_burst = c->first_burst;
     a.fused = fused;
     a.evict = evict;
     a.new_k = (const uint8_t*)new_k;

@@ -423,6 +423,9 @@ struct DecodeArgs {
     const int32_t* assign;
     const int32_t* assign_off;
     int32_t prefetch_tiles; // L2 prefetch distance in tiles (0: off)
+    int32_t first_burst;    // tiles queued before waiting for the first to land (0: no wait); with
+                            // every CTA queueing its whole ring at once, a CTA's first tile
+                            // waits behind the others' (measured: 4 saves ~0.6 us of 25)
     int32_t n_clusters;     // persistent clusters launched; cluster y handles list indices y, y + n_clusters, ...
     // fused step (append + decode + one-token evict in one launch): fused = 1,
     // new_k/new_v the appended rows [units of the call][d]; evict = 1 moves

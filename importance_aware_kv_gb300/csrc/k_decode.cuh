@@ -283,6 +283,13 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
             if (lane == 0) {
                 for (int i = 0; i < nt; ++i, ++gi) {
                     if (*abort_flag) break;
+                    // the CTA's first tiles jump the DRAM queue: past the first
+                    // burst, wait until tile 0 has landed before queueing more
+                    if (gi == a.first_burst && a.first_burst > 0 &&
+                        !mbar_wait_bounded(&full[0], 0u, v.err, kWaitFull, 0u)) {
+                        *abort_flag = 1;
+                        break;
+                    }
                     const int st = gi % kDecStages;
                     if (!mbar_wait_bounded(&empty[st], ((uint32_t)(gi / kDecStages) & 1u) ^ 1u, v.err, kWaitEmpty,
                                            (uint32_t)gi)) {
