@@ -248,7 +248,7 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
         holes_total += std::max(0, std::min(c->budget_unit[u], c->cap - c->budget_unit[u]));
     }
     c->wchunks = ceil_div(c->cap, kWindowChunk);
-    const bool need_logits = ceil_div(c->cap, kMaxCS) > c->max_smem_chunk;
+    const bool need_logits = dec_chunk_max(c->cap, kMaxCS) > c->max_smem_chunk;
 
 #define ALLOC(ptr, n)                                                       \
     if ((e = dalloc(c, &(ptr), (n))) != cudaSuccess) {                      \
@@ -519,7 +519,7 @@ hikv_status launch_clusters(hikv_cache* c, int32_t layer0, int32_t nl, const std
         const int slots = c->dec_occ * c->sm_count;
         int64_t best = INT64_MAX;
         for (int k = 1; k <= std::min(kMaxCS, maxn); ++k) {
-            const int ck = ceil_div(maxn, k);
+            const int ck = dec_chunk_max(maxn, k);
             const bool sp = ck <= c->max_smem_chunk;
             if (!sp && !c->d_logits) continue;
             const size_t smem = decode_smem_bytes(c->dtype, c->d, c->G, sp, sp ? ck : 0);
@@ -540,7 +540,7 @@ hikv_status launch_clusters(hikv_cache* c, int32_t layer0, int32_t nl, const std
         }
     }
     cs = std::min(cs, std::max(1, maxn));
-    const int chunk = ceil_div(maxn, cs);
+    const int chunk = dec_chunk_max(maxn, cs);   // most slots a CTA holds
     const bool smem_path = chunk <= c->max_smem_chunk;
     if (!smem_path && !c->d_logits)
         return fail(HIKV_ERR_UNSUPPORTED, "%s: %d tokens per CTA exceed shared memory", who, chunk);

@@ -54,6 +54,26 @@ struct View {
 
 constexpr int kMaxCS = 16;   // most CTAs (cluster size) per unit in the decode kernel
 
+// Slots [t0, t1) of CTA c of a cs-CTA cluster for a unit of n tokens:
+// chunks of ceil((n - 1) / cs) rounded up to whole 16-slot tiles, the last
+// CTA taking the rest.  With n = 16k + 1 (a budget of whole tiles plus the
+// new token) every CTA holds whole tiles and the last one a single extra
+// row, so no tile is loaded by two CTAs and the tile counts balance.
+__host__ __device__ inline int32_t dec_chunk(int32_t n, int32_t cs) {
+    const int32_t m = n > 1 ? n - 1 : 1;
+    return ((m + cs - 1) / cs + 15) / 16 * 16;
+}
+__host__ __device__ inline void dec_range(int32_t n, int32_t cs, int32_t c, int32_t& t0, int32_t& t1) {
+    const int32_t ch = dec_chunk(n, cs);
+    t0 = c * ch < n ? c * ch : n;
+    t1 = c == cs - 1 ? n : (t0 + ch < n ? t0 + ch : n);
+}
+// most slots a CTA holds (the last CTA's chunk plus one)
+__host__ __device__ inline int32_t dec_chunk_max(int32_t n, int32_t cs) {
+    const int32_t ch = dec_chunk(n, cs);
+    return ch + 1 < n ? ch + 1 : n;
+}
+
 // Pages a unit keeps after being cut to its budget B: room for B + kKeepSlack
 // tokens, so the appends of up to kKeepSlack steps before the next eviction
 // (a batched eviction interval) never need a page.

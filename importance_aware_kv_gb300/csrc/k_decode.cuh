@@ -200,8 +200,8 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
     int32_t pre_pg = -1;
     if (warp == kDecNCW && it0 < it1) {
         const DecUnit du = dec_unit(a, it0);
-        const int32_t chunk = ceil_div(du.n, CS);
-        const int32_t t0 = min(du.n, c * chunk), t1 = min(du.n, t0 + chunk);
+        int32_t t0, t1;
+        dec_range(du.n, CS, c, t0, t1);
         const int32_t pg0 = t0 >> v.page_shift;
         const int32_t npg = t1 > t0 ? ((t1 - 1) >> v.page_shift) - pg0 + 1 : 0;
         if (lane < npg) pre_pg = v.page_table[(int64_t)du.u * v.max_pages + pg0 + lane];
@@ -239,12 +239,14 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
             const int32_t li = du.u / per_layer - a.layer0;
             const int32_t b = (du.u / v.hkv) % v.batch;
             const int32_t g = du.u % v.hkv;
-            const int32_t chunk = ceil_div(du.n, CS);
-            const int32_t t0 = min(du.n, c * chunk);
-            const int32_t t1 = min(du.n, t0 + chunk);
+            int32_t t0, t1;
+            dec_range(du.n, CS, c, t0, t1);
             const int32_t cnt = t1 - t0;
             const int32_t first_blk = t0 / kDecTR;
-            const int32_t nt = cnt > 0 ? (t1 - 1) / kDecTR - first_blk + 1 : 0;
+            // a single row alone in the last tile is not loaded: a consumer
+            // warp folds it in as one row (see the consumers)
+            const bool tail = cnt > 1 && (cnt - 1) % kDecTR == 0;
+            const int32_t nt = tail ? (cnt - 1) / kDecTR : (cnt > 0 ? (t1 - 1) / kDecTR - first_blk + 1 : 0);
             const int32_t pg0 = t0 >> v.page_shift;
             const int32_t npg = cnt > 0 ? ((t1 - 1) >> v.page_shift) - pg0 + 1 : 0;
             const int32_t* ptab = v.page_table + (int64_t)du.u * v.max_pages;
@@ -347,17 +349,19 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
         const int32_t b = (u / v.hkv) % v.batch;
         const int32_t g = u % v.hkv;
         const bool need_victim = n > du.Bu;
-        const int32_t chunk = ceil_div(n, CS);
-        const int32_t t0 = min(n, c * chunk);
-        int32_t t1 = min(n, t0 + chunk);
-        int32_t cnt = t1 - t0;
-        if (SMEM_S && cnt > a.chunk_cap) {   // host sizes chunk_cap; never taken
-            if (ctid == 0) atomicOr(v.err, DEVERR_STATE);
-            cnt = a.chunk_cap;
-            t1 = t0 + cnt;
-        }
+        int32_t t0, t1;
+        dec_range(n, CS, c, t0, t1);
+        const int32_t cnt = t1 - t0;
+        if (SMEM_S && cnt > a.chunk_cap && ctid == 0) atomicOr(v.err, DEVERR_STATE);   // the host sizes chunk_cap
         const int32_t first_blk = t0 / kDecTR;
-        const int32_t nt = cnt > 0 ? (t1 - 1) / kDecTR - first_blk + 1 : 0;
+        // a single row alone in the CTA's last tile (t0 is tile-aligned) is
+        // folded in by the warp next in the tile rotation instead of being
+        // loaded as a tile: with a budget of whole tiles this is the new
+        // token, and the warps' tile counts stay equal
+        const bool tail = cnt > 1 && (cnt - 1) % kDecTR == 0;
+        const int32_t ts = t1 - 1;   // the tail slot
+        const int32_t nt = tail ? (cnt - 1) / kDecTR : (cnt > 0 ? (t1 - 1) / kDecTR - first_blk + 1 : 0);
+        const int tail_warp = nt % kDecNCW;
         const int64_t qbase = (((int64_t)li * v.batch + b) * v.hq + (int64_t)g * G) * D;
         const int32_t per = ceil_div(G * D, CS);   // output elements finalised per CTA
         const int xb = k & 1;
@@ -376,6 +380,21 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
         const float* impg = v.imp + (int64_t)u * v.cap;
         const int32_t* posg = v.pos + (int64_t)u * v.cap;
 
+        // the tail row's K and V: the staged rows when it is the new token,
+        // else this lane's share read from the pool now (used after the tiles)
+        const bool tail_here = tail && warp == tail_warp;
+        const bool tail_staged = a.fused && ts == sn;
+        Raw tail_k{}, tail_v{};
+        if (tail_here && !tail_staged) {
+            const int32_t pg = v.page_table[(int64_t)u * v.max_pages + (ts >> v.page_shift)];
+            if (pg >= 0 && pg < v.pool_pages) {
+                const uint8_t* kr = v.pool + (int64_t)pg * v.page_bytes + (int64_t)(ts & (v.page_tokens - 1)) * RB;
+                tail_k = *reinterpret_cast<const Raw*>(kr + lane * LB);
+                tail_v = *reinterpret_cast<const Raw*>(kr + (int64_t)v.page_tokens * RB + lane * LB);
+            } else if (lane == 0) {
+                atomicOr(v.err, DEVERR_PAGE);
+            }
+        }
         // the importance pass reads these at the end of the unit: start them towards L2 now
         for (int j = ctid * 32; j < cnt; j += NCT * 32) {
             prefetch_global_l2(impg + t0 + j);
@@ -491,7 +510,7 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
             }
             if (qh == 0) {
                 store_group<G>(ps + qr * G, p);
-                if (rv) store_group<G>(Sb + (int64_t)(s0 + qr - s_off) * G, s);
+                if (rv && (!SMEM_S || s0 + qr - s_off < a.chunk_cap)) store_group<G>(Sb + (int64_t)(s0 + qr - s_off) * G, s);
             }
             __syncwarp();
             // ---- p.v over the tile's valid rows (unrolled; invalid rows skipped, their
@@ -532,6 +551,60 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
             if (lane == 0) mbar_arrive(&empty[st]);
         }
         gi_base += nt;
+        if (tail_here && !*abort_flag) {
+            // the tail row as a rank-1 update of this warp's state; a lane owns
+            // d/32 of its dimensions, so q.k is a warp sum
+            if (tail_staged) {
+                tail_k = *reinterpret_cast<const Raw*>(nrow + lane * LB);
+                tail_v = *reinterpret_cast<const Raw*>(nrow + RB + lane * LB);
+            }
+            float xk[EPL], xv[EPL];
+            Widen<T, EPL>::run(tail_k, xk);
+            Widen<T, EPL>::run(tail_v, xv);
+            float s[G];
+            bool big = false;
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                float t = 0.f;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) t = fmaf(q_s[h * D + lane * EPL + e], xk[e], t);
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+                s[h] = t;
+                big |= t > m_w[h] + kDecLazy;
+            }
+            if (big) {   // warp-uniform: s is
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    const float mn = fmaxf(m_w[h], s[h]);
+                    const float scl = exp2f(m_w[h] - mn);
+                    m_w[h] = mn;
+                    l_w[h] *= scl;
+#pragma unroll
+                    for (int e = 0; e < EPL / 2; ++e) {
+                        o2[h][e].x *= scl;
+                        o2[h][e].y *= scl;
+                    }
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float p = exp2f(s[h] - m_w[h]);
+                if ((lane & 15) == 0) l_w[h] += p;   // once in each half's row sum
+#pragma unroll
+                for (int e = 0; e < EPL / 2; ++e)
+                    o2[h][e] = ffma2(make_float2(xv[2 * e], xv[2 * e + 1]), make_float2(p, p), o2[h][e]);
+            }
+            if (lane == 0 && (!SMEM_S || ts - s_off < a.chunk_cap)) store_group<G>(Sb + (int64_t)(ts - s_off) * G, s);
+            if (tail_staged) {   // the new token's rows into the pool for later steps
+                const int32_t pg = v.page_table[(int64_t)u * v.max_pages + (sn >> v.page_shift)];
+                if (pg >= 0 && pg < v.pool_pages) {
+                    uint8_t* kd = v.pool + (int64_t)pg * v.page_bytes + (int64_t)(sn & (v.page_tokens - 1)) * RB;
+                    *reinterpret_cast<Raw*>(kd + lane * LB) = tail_k;
+                    *reinterpret_cast<Raw*>(kd + (int64_t)v.page_tokens * RB + lane * LB) = tail_v;
+                }
+            }
+        }
 
         // the importance pass's first loads, issued now so that they land
         // during the merge and the cluster exchange
