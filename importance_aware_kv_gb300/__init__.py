@@ -30,7 +30,7 @@ ABI_FUNCTIONS = ("hikv_create_cache", "hikv_destroy_cache", "hikv_append", "hikv
                  "hikv_decode_step", "hikv_evict", "hikv_gather_retained", "hikv_get_lengths",
                  "hikv_device_status", "hikv_last_error", "hikv_score_window_noalloc",
                  "hikv_decode_step_fused", "hikv_kernel_launches", "hikv_budgets_pyramid",
-                 "hikv_budgets_duo")
+                 "hikv_budgets_duo", "hikv_selftest_timeout")
 
 
 class HikvError(RuntimeError):
@@ -72,6 +72,7 @@ def _load():
         "hikv_kernel_launches": ([P], ctypes.c_int64),
         "hikv_budgets_pyramid": ([I32, I32, I32, I32, I32, P], S),
         "hikv_budgets_duo": ([I32, I32, P, I32, I32, I32, P], S),
+        "hikv_selftest_timeout": ([P, I32, P], S),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -249,14 +250,49 @@ class Cache:
         except Exception:
             pass
 
+    # The C ABI takes raw pointers and cannot see buffer sizes: the binding
+    # checks every tensor against the configuration before passing it on.
+    def _dtype(self):
+        import torch
+        return torch.bfloat16 if self.cfg.dtype == "bf16" else torch.float32
+
+    def _check_tensor(self, t, name, shape):
+        if t.dtype != self._dtype():
+            raise TypeError(f"{name} has dtype {t.dtype}, the cache holds {self._dtype()}")
+        if tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+    def _layers(self, t, layer0):
+        nl = t.shape[0] if t.dim() else 0
+        if not (0 <= layer0 and nl >= 1 and layer0 + nl <= self.cfg.num_layers):
+            raise ValueError(f"layers [{layer0}, {layer0 + nl}) outside [0, {self.cfg.num_layers})")
+        return nl
+
     def append(self, k, v, layer0=0, stream=None):
+        c = self.cfg
+        nl = self._layers(k, layer0)
+        ntok = k.shape[3] if k.dim() == 5 else -1
+        self._check_tensor(k, "k", (nl, c.batch, c.num_kv_heads, ntok, c.head_dim))
+        self._check_tensor(v, "v", tuple(k.shape))
         hikv_append(self.h, layer0, k, v, stream)
 
     def score_window(self, q, layer0=0, stream=None):
+        c = self.cfg
+        nl = self._layers(q, layer0)
+        nq = q.shape[3] if q.dim() == 5 else -1
+        self._check_tensor(q, "q", (nl, c.batch, c.num_q_heads, nq, c.head_dim))
         hikv_score_window(self.h, layer0, q, stream)
 
     def decode_step(self, q, out, layer0=0, stream=None):
+        c = self.cfg
+        nl = self._layers(q, layer0)
+        self._check_tensor(q, "q", (nl, c.batch, c.num_q_heads, c.head_dim))
+        self._check_tensor(out, "out", tuple(q.shape))
         hikv_decode_step(self.h, layer0, q, out, stream)
+
+    def selftest_timeout(self, limit_us: int = 20000, stream=None):
+        """Enqueue a kernel whose bounded wait runs out (see hikv.h)."""
+        _check(_lib.hikv_selftest_timeout(self.h, limit_us, _stream(stream)))
 
     def kernel_launches(self) -> int:
         """Kernels this cache has launched so far (host counter)."""
@@ -264,6 +300,12 @@ class Cache:
 
     def step(self, k, v, q, out, evict=True, layer0=0, stream=None):
         """append + decode_step (+ evict) as one call (one launch in steady state)."""
+        c = self.cfg
+        nl = self._layers(q, layer0)
+        self._check_tensor(k, "k", (nl, c.batch, c.num_kv_heads, 1, c.head_dim))
+        self._check_tensor(v, "v", tuple(k.shape))
+        self._check_tensor(q, "q", (nl, c.batch, c.num_q_heads, c.head_dim))
+        self._check_tensor(out, "out", tuple(q.shape))
         hikv_decode_step_fused(self.h, layer0, k, v, q, out, evict, stream)
 
     def evict(self, layer0=0, nlayers=None, stream=None):

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <cmath>
@@ -24,6 +25,17 @@ size_t window_smem_bytes(int d, int nqv);
 }
 
 using namespace hikv;
+
+namespace {
+
+// NVTX range around an entry point (seen by nsys / ncu timelines; a no-op
+// when no tool is attached)
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+};
+
+}  // namespace
 
 namespace {
 
@@ -124,10 +136,18 @@ struct hikv_cache {
 
 namespace {
 
+// HIKV_FAULT_ALLOC_AT=n makes the n-th device allocation of a create (from
+// 1) fail, to test the cleanup path without exhausting the device
+int fault_alloc_at() {
+    const char* e = std::getenv("HIKV_FAULT_ALLOC_AT");
+    return e ? std::atoi(e) : 0;
+}
+
 template <class T>
 cudaError_t dalloc(hikv_cache* c, T** p, size_t count) {
     *p = nullptr;
     if (count == 0) count = 1;
+    if (fault_alloc_at() > 0 && (int)c->allocs.size() + 1 == fault_alloc_at()) return cudaErrorMemoryAllocation;
     cudaError_t e = cudaMalloc((void**)p, count * sizeof(T));
     if (e == cudaSuccess) c->allocs.push_back(*p);
     return e;
@@ -371,6 +391,7 @@ hikv_status hikv_destroy_cache(hikv_cache* c) {
 hikv_status hikv_append(hikv_cache* c, int32_t layer0, int32_t nl, int32_t ntok, const void* k,
                         const void* vv, hikv_stream_t stream) {
     g_err.clear();
+    NvtxRange nvtx("hikv_append");
     if (!range_ok(c, layer0, nl)) return fail(HIKV_ERR_INVALID_ARG, "append: bad cache or layer range");
     if (ntok < 0) return fail(HIKV_ERR_INVALID_ARG, "append: ntok < 0");
     if (ntok == 0) return HIKV_OK;
@@ -412,6 +433,7 @@ hikv_status hikv_append(hikv_cache* c, int32_t layer0, int32_t nl, int32_t ntok,
 hikv_status hikv_score_window(hikv_cache* c, int32_t layer0, int32_t nl, int32_t nq, const void* q,
                               hikv_stream_t stream) {
     g_err.clear();
+    NvtxRange nvtx("hikv_score_window");
     if (!range_ok(c, layer0, nl)) return fail(HIKV_ERR_INVALID_ARG, "score_window: bad cache or layer range");
     if (nq < 1 || nq > c->max_wq)
         return fail(HIKV_ERR_INVALID_ARG, "score_window: nq=%d not in [1, %d]", nq, c->max_wq);
@@ -712,6 +734,7 @@ extern "C" {
 hikv_status hikv_decode_step(hikv_cache* c, int32_t layer0, int32_t nl, const void* q, void* out,
                              hikv_stream_t stream) {
     g_err.clear();
+    NvtxRange nvtx("hikv_decode_step");
     if (!range_ok(c, layer0, nl)) return fail(HIKV_ERR_INVALID_ARG, "decode_step: bad cache or layer range");
     if (!q || !out) return fail(HIKV_ERR_INVALID_ARG, "decode_step: null q or out");
     if (q == out) return fail(HIKV_ERR_INVALID_ARG, "decode_step: out aliases q");
@@ -725,6 +748,7 @@ hikv_status hikv_decode_step(hikv_cache* c, int32_t layer0, int32_t nl, const vo
 hikv_status hikv_decode_step_fused(hikv_cache* c, int32_t layer0, int32_t nl, const void* k, const void* v,
                                    const void* q, void* out, int32_t evict, hikv_stream_t stream) {
     g_err.clear();
+    NvtxRange nvtx("hikv_decode_step_fused");
     if (!range_ok(c, layer0, nl)) return fail(HIKV_ERR_INVALID_ARG, "decode_step_fused: bad cache or layer range");
     if (!k || !v || !q || !out) return fail(HIKV_ERR_INVALID_ARG, "decode_step_fused: null pointer");
     if (q == out) return fail(HIKV_ERR_INVALID_ARG, "decode_step_fused: out aliases q");
@@ -759,6 +783,7 @@ hikv_status hikv_decode_step_fused(hikv_cache* c, int32_t layer0, int32_t nl, co
 
 hikv_status hikv_evict(hikv_cache* c, int32_t layer0, int32_t nl, hikv_stream_t stream) {
     g_err.clear();
+    NvtxRange nvtx("hikv_evict");
     if (!range_ok(c, layer0, nl)) return fail(HIKV_ERR_INVALID_ARG, "evict: bad cache or layer range");
     const int u0 = layer0 * c->per_layer, nu = nl * c->per_layer;
     bool any = false, fast = true;
@@ -797,6 +822,7 @@ hikv_status hikv_gather_retained(hikv_cache* c, int32_t layer0, int32_t nl, int3
                                  int32_t* positions, float* importance, void* k_out, void* v_out,
                                  hikv_stream_t stream) {
     g_err.clear();
+    NvtxRange nvtx("hikv_gather_retained");
     if (!range_ok(c, layer0, nl)) return fail(HIKV_ERR_INVALID_ARG, "gather: bad cache or layer range");
     if (!lengths || !positions || !importance) return fail(HIKV_ERR_INVALID_ARG, "gather: null output");
     const int u0 = layer0 * c->per_layer, nu = nl * c->per_layer;
@@ -826,6 +852,16 @@ hikv_status hikv_get_lengths(const hikv_cache* c, int32_t layer0, int32_t nl, in
 }
 
 int64_t hikv_kernel_launches(const hikv_cache* c) { return c ? c->launches : -1; }
+
+hikv_status hikv_selftest_timeout(hikv_cache* c, int32_t limit_us, hikv_stream_t stream) {
+    g_err.clear();
+    if (!c || limit_us < 1 || limit_us > 2000000)
+        return fail(HIKV_ERR_INVALID_ARG, "selftest_timeout: bad cache or limit");
+    cudaError_t e = launch_selftest_timeout(c->v, (uint64_t)limit_us * 1000u, (cudaStream_t)stream);
+    c->launches += 1;
+    if (e != cudaSuccess) return cuda_fail(e, "selftest_timeout: launch");
+    return HIKV_OK;
+}
 
 hikv_status hikv_budgets_pyramid(int32_t num_layers, int32_t num_kv_heads, int32_t avg, int32_t min_budget,
                                  int32_t floor_budget, int32_t* out) {
@@ -872,10 +908,11 @@ hikv_status hikv_device_status(hikv_cache* c) {
     }
     if (w[0] & DEVERR_TIMEOUT) {
         static const char* const sites[] = {"?", "producer q-free", "producer stage-free", "producer drain",
-                                            "consumer q", "consumer tile", "cluster exchange", "victim exchange"};
+                                            "consumer q", "consumer tile", "cluster exchange", "victim exchange",
+                                            "self-test"};
         return fail(HIKV_ERR_TIMEOUT,
                     "device: a bounded wait gave up (bits 0x%x; first: %s wait, cluster %u, CTA %u, index 0x%x, "
-                    "after %u us)", w[0], sites[w[1] < 8 ? w[1] : 0], w[2], w[3], w[4], w[5]);
+                    "after %u us)", w[0], sites[w[1] < 9 ? w[1] : 0], w[2], w[3], w[4], w[5]);
     }
     if (w[0]) return fail(HIKV_ERR_STATE, "device: inconsistent state recorded (bits 0x%x)", w[0]);
     return HIKV_OK;

@@ -206,7 +206,7 @@ __device__ __forceinline__ uint64_t global_ns() {
 // site-specific index, err[5] = microseconds waited.
 enum : uint32_t {
     kWaitQEmpty = 1, kWaitEmpty = 2, kWaitDrain = 3, kWaitQFull = 4, kWaitFull = 5, kWaitXchg = 6,
-    kWaitVictim = 7
+    kWaitVictim = 7, kWaitSelftest = 8
 };
 __device__ __forceinline__ void record_timeout(uint32_t* err, uint32_t site, uint32_t extra, uint64_t waited_ns) {
     atomicOr(err, DEVERR_TIMEOUT);
@@ -224,12 +224,12 @@ __device__ __forceinline__ void record_timeout(uint32_t* err, uint32_t site, uin
 // and return false.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t site,
-                                                  uint32_t extra) {
+                                                  uint32_t extra, uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait_hint(bar, parity, 1000u)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t i = 0; i < (1u << 24); ++i) {
         if (mbar_try_wait_hint(bar, parity, 1000u)) return true;
-        if ((i & 63u) == 63u && global_ns() - t0 > kWaitLimitNs) break;
+        if ((i & 63u) == 63u && global_ns() - t0 > limit_ns) break;
     }
     record_timeout(err, site, extra, global_ns() - t0);
     return false;
@@ -519,5 +519,6 @@ struct GatherArgs {
     uint8_t* v_out;
 };
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s);
+cudaError_t launch_selftest_timeout(const View& v, uint64_t limit_ns, cudaStream_t s);
 
 }  // namespace hikv

@@ -102,4 +102,22 @@ cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// Failure-detection self-test: one CTA waits, bounded by limit_ns, on an
+// mbarrier that nothing arrives on; the wait gives up, records the timeout
+// (site kWaitSelftest) in the device error word and the kernel returns, so
+// the context stays usable.  No trap, no unbounded spin.
+__global__ void k_selftest_timeout(View v, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        mbar_wait_bounded(&bar, 0u, v.err, kWaitSelftest, 0u, limit_ns);   // phase 0 never completes
+    }
+}
+
+cudaError_t launch_selftest_timeout(const View& v, uint64_t limit_ns, cudaStream_t s) {
+    k_selftest_timeout<<<1, 32, 0, s>>>(v, limit_ns);
+    return cudaGetLastError();
+}
+
 }  // namespace hikv

@@ -196,6 +196,15 @@ hikv_status hikv_budgets_pyramid(int32_t num_layers, int32_t num_kv_heads, int32
 hikv_status hikv_budgets_duo(int32_t num_layers, int32_t num_kv_heads, const uint8_t* retrieval_host,
                              int32_t full_budget, int32_t num_sink, int32_t recent_window, int32_t* out_host);
 
+/* Failure-detection self-test: enqueues one kernel whose bounded device wait
+ * (on a barrier nothing arrives on) gives up after limit_us microseconds
+ * (1 .. 2e6) and records the timeout in the cache's device error word, as a
+ * real stalled wait would; the kernel then returns and the context stays
+ * usable.  The next hikv_device_status reports HIKV_ERR_TIMEOUT (site
+ * "self-test") and clears it.  HIKV_ERR_INVALID_ARG on a null cache or a
+ * limit out of range. */
+hikv_status hikv_selftest_timeout(hikv_cache* cache, int32_t limit_us, hikv_stream_t stream);
+
 /* Number of kernels launched on the caller's streams through this cache
  * since it was created (every entry point counts what it enqueued; a call
  * that returned an error before launching counts nothing).  Host-only, no
