@@ -266,12 +266,15 @@ def bench_gpu(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = W.WORKLOADS[args.workload]
-    seed = rank_seed(w, rank)
+    seed = rank_seed(w, rank) if args.seed is None else args.seed + 1000 * rank
     K, Wu, Ke, K3 = args.steps, args.warmup, args.e2e_steps, args.three_call_steps
     L = w.layers
     KL = args.per_layer_steps if args.per_layer_steps >= 0 else (0 if L == 1 else 100)
     total_steps = Wu + K + K3 + KL + Ke
     budgets = schedule_budgets(w, seed, args.schedule)
+    if args.full_cache:   # no eviction: every unit keeps its whole context
+        budgets = np.full_like(budgets, w.prompt + Wu + K + args.three_call_steps + max(args.per_layer_steps, 100)
+                               + Ke + 1)
     cache = hk.Cache(hk.CacheConfig(w.layers, w.batch, w.hq, w.hkv, w.d, w.dtype, w.sink, w.window,
                                     budgets, w.prompt + total_steps + 1))
     stage("cache created")
@@ -343,8 +346,10 @@ def bench_gpu(args):
     torch.cuda.synchronize()
     launches0 = cache.kernel_launches()
     alg_bytes = 0
+    kv_bytes = 0
     for i in range(K):
         alg_bytes += bytes_now()
+        kv_bytes += int((2 * (cache.lengths().astype(np.int64) + 1) * w.d * w.elem_bytes).sum())
         flush.fill_(float(i))
         torch.cuda._sleep(spin_cycles)
         e0, e1 = ev[i]
@@ -467,6 +472,8 @@ def bench_gpu(args):
                    "l2": "flushed between timed steps (256 MB write, outside the timed events)",
                    "parallelism": f"replicas x{world} (units sharded by rank, no collective)"},
         "hbm_gbs_step": alg_bytes * world / t_total / 1e9,
+        "retained_kv_gbs": kv_bytes * world / t_total / 1e9,
+        "hbm_fraction_nominal": achieved / 8000.0,
         "roofline": {"kernel": "k_decode (append + attention + importance + victim + evict, one launch)",
                      "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{src} hbm_gbs", "traffic": traffic,
@@ -500,6 +507,8 @@ def main():
     ap.add_argument("--three-call-steps", type=int, default=500)
     ap.add_argument("--per-layer-steps", type=int, default=-1,
                     help="steps timed as one launch per layer (default 100 for multi-layer workloads)")
+    ap.add_argument("--seed", type=int, default=None, help="input seed (default: the workload index)")
+    ap.add_argument("--full-cache", action="store_true", help="budgets above the context: no eviction")
     ap.add_argument("--schedule", default="workload",
                     help='budgets: "workload", "pyramid:AVG:MIN" or "duo:FRAC"')
     ap.add_argument("--workload", type=int, default=WORKLOAD_INDEX,
