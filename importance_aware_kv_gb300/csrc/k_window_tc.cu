@@ -21,7 +21,10 @@
 // 128-byte swizzle), double-buffered on two mbarriers.  Warp w computes rows
 // [16 (w mod RB), +16) of the query block against a 64/NCS-token slice of
 // the tile (RB = NQV/16 row blocks, NCS = 8/RB column slices); its A
-// fragments (the queries) stay in registers for the whole chunk.
+// fragments (the queries) stay in registers for the whole chunk.  Rows are
+// query-major (row = query * G + head), so the G heads of a query sit in
+// lanes that differ only in lane bits 2.. and pass 2 sums them with G - 1
+// shuffles before staging one increment per (query, token).
 #include "hikv_internal.cuh"
 
 namespace hikv {
@@ -54,7 +57,7 @@ struct WinTc {
     static constexpr int OFF_BAR = 2 * TILE;                   // 2 mbarriers, then a status word
     static constexpr int OFF_POS = OFF_BAR + 64;               // [kTcTok] int32
     static constexpr int OFF_ML = OFF_POS + kTcTok * 4;        // [NCS][NQV][2] (pass 1) / MF,LI [NQV][2]
-    static constexpr int OFF_P = OFF_ML + NCS * NQV * 2 * 4;   // [NQV][kTcTok + 4] fp32 (pass 2)
+    static constexpr int OFF_P = OFF_ML + NCS * NQV * 2 * 4;   // [NQV][kTcTok + 4] fp32 increments (pass 2)
     static constexpr int BYTES = OFF_P + NQV * (kTcTok + 4) * 4 + 1024;
 };
 
@@ -145,22 +148,24 @@ __global__ void __launch_bounds__(kTcThreads) k_window_tc(const WindowArgs a, co
     const int li = u / per_layer - a.layer0, b = (u / v.hkv) % v.batch, gh = u % v.hkv;
     const uint16_t* qb = reinterpret_cast<const uint16_t*>(a.q) +
                          (((int64_t)li * v.batch + b) * v.hq + (int64_t)gh * v.group) * nq * D;
-    const int row0 = rb * 16 + g, row1 = row0 + 8;
+    const int G = v.group;
+    const int row0 = rb * 16 + g, row1 = row0 + 8;   // row = query * G + head
+    auto qrow = [&](int row) { return (int64_t)((row % G) * nq + row / G) * D; };   // q is [G][nq][d]
     uint32_t af[C::KS][4];
 #pragma unroll
     for (int ks = 0; ks < C::KS; ++ks) {
         const int k0 = ks * 16 + 2 * t;
         auto ld = [&](int row, int k) -> uint32_t {
-            return row < nqv ? *reinterpret_cast<const uint32_t*>(qb + (int64_t)row * D + k) : 0u;
+            return row < nqv ? *reinterpret_cast<const uint32_t*>(qb + qrow(row) + k) : 0u;
         };
         af[ks][0] = ld(row0, k0);
         af[ks][1] = ld(row1, k0);
         af[ks][2] = ld(row0, k0 + 8);
         af[ks][3] = ld(row1, k0 + 8);
     }
-    // causal limit of each of this lane's two rows (query vector hh*nq + i sits at tnew - nq + 1 + i)
-    const int32_t qpos0 = row0 < nqv ? tnew - nq + 1 + row0 % nq : INT32_MIN;
-    const int32_t qpos1 = row1 < nqv ? tnew - nq + 1 + row1 % nq : INT32_MIN;
+    // causal limit of each of this lane's two rows (query i sits at tnew - nq + 1 + i)
+    const int32_t qpos0 = row0 < nqv ? tnew - nq + 1 + row0 / G : INT32_MIN;
+    const int32_t qpos1 = row1 < nqv ? tnew - nq + 1 + row1 / G : INT32_MIN;
 
     float mr[2] = {-INFINITY, -INFINITY}, lr[2] = {0.f, 0.f};   // pass 1: this warp's slice
     float mf[2] = {0.f, 0.f}, lif[2] = {0.f, 0.f};              // pass 2: final per row
@@ -258,31 +263,34 @@ __global__ void __launch_bounds__(kTcThreads) k_window_tc(const WindowArgs a, co
                 }
             }
         } else {
-            // probabilities of this tile into Pt [query vector][token]
+            // probabilities summed over the G heads of each query: the heads of
+            // a query are rows q*G .. q*G+G-1, held by lanes that differ in
+            // lane bits 2 .. 2+log2(G)-1 (row = rb*16 + lane/4)
 #pragma unroll
             for (int nb = 0; nb < C::NB; ++nb) {
+                float pr[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float m = j < 2 ? mf[0] : mf[1], li_ = j < 2 ? lif[0] : lif[1];
+                    pr[j] = vis[nb][j] ? exp2f(s[nb][j] - m) * li_ : 0.f;
+                }
+                for (int o = 4; o < 4 * G; o <<= 1)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) pr[j] += __shfl_xor_sync(0xffffffffu, pr[j], o);
                 const int col = cslice * C::COLS + nb * 8 + 2 * t;
-                if (row0 < nqv)
-                    *reinterpret_cast<float2*>(&Pt[row0 * PT + col]) =
-                        make_float2(vis[nb][0] ? exp2f(s[nb][0] - mf[0]) * lif[0] : 0.f,
-                                    vis[nb][1] ? exp2f(s[nb][1] - mf[0]) * lif[0] : 0.f);
-                if (row1 < nqv)
-                    *reinterpret_cast<float2*>(&Pt[row1 * PT + col]) =
-                        make_float2(vis[nb][2] ? exp2f(s[nb][2] - mf[1]) * lif[1] : 0.f,
-                                    vis[nb][3] ? exp2f(s[nb][3] - mf[1]) * lif[1] : 0.f);
+                if (g % G == 0) {   // the head-0 lane of each query writes its increments
+                    if (row0 < nqv) *reinterpret_cast<float2*>(&Pt[(row0 / G) * PT + col]) = make_float2(pr[0], pr[1]);
+                    if (row1 < nqv) *reinterpret_cast<float2*>(&Pt[(row1 / G) * PT + col]) = make_float2(pr[2], pr[3]);
+                }
             }
             __syncthreads();
-            // per token: queries in position order, heads ascending within a query
+            // per token: queries in position order
             for (int r = tid; r < kTcTok; r += kTcThreads) {
                 const int32_t sidx = s0 + r;
                 if (sidx >= c1) continue;
                 const int64_t mi = (int64_t)u * v.cap + sidx;
                 float imp = v.imp[mi];
-                for (int qi = 0; qi < nq; ++qi) {
-                    float inc = 0.f;
-                    for (int hh = 0; hh < v.group; ++hh) inc += Pt[(hh * nq + qi) * PT + r];
-                    imp = imp + inc;
-                }
+                for (int qi = 0; qi < nq; ++qi) imp = imp + Pt[qi * PT + r];
                 v.imp[mi] = imp;
             }
         }
