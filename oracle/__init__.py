@@ -54,6 +54,8 @@ def _load():
                 "ora_score_window": ([_P, _I, _I, _I, _P], _I),
                 "ora_pool_importance": ([_P, _I, _I, _I], _I),
                 "ora_set_recent_only": ([_P, _I], _I),
+                "ora_set_element_budget": ([_P, _I], _I),
+                "ora_stage2_near_ties": ([_P, _I, _I, _P], _I),
                 "ora_decode": ([_P, _I, _I, _P, _P], _I),
                 "ora_evict": ([_P, _I, _I], _I),
                 "ora_len": ([_P, _I], _I),
@@ -129,6 +131,19 @@ class Oracle:
     def set_recent_only(self, on=True):
         """HiKV Stage I: decode steps add mass only to the recent bank."""
         assert self.lib.ora_set_recent_only(self.h, 1 if on else 0) == 0
+
+    def set_element_budget(self, b2):
+        """HiKV Stage II: 0 < b2 < d dimensions of q and b2 entries of every
+        d-entry chunk of P take part (0 or d: exact attention)."""
+        if self.lib.ora_set_element_budget(self.h, int(b2)) != 0:
+            raise ValueError(f"oracle: element budget {b2} outside [0, {self.d}]")
+
+    def stage2_near_ties(self, layer0, nl):
+        """[nl][B][Hq] bool: heads whose latest Stage II chunk selection was
+        decided by less than 1e-4 (relative) in p."""
+        f = np.zeros((nl, self.B, self.Hq), np.uint8)
+        assert self.lib.ora_stage2_near_ties(self.h, layer0, nl, _ptr(f)) == 0
+        return f.astype(bool)
 
     def pool_importance(self, layer0, nl, kpool):
         """SnapKV: each score becomes the max over the next kpool positions."""

@@ -40,6 +40,16 @@
 //                   starting at its own, S_pooled[i] = max_{0<=m<k} A_obs[i+m]
 //                   (blog sec. 3 "SnapKV"), positions with no retained token
 //                   (past the end) contributing nothing.
+//  * element level  HiKV Stage II (sec. III-C, Algorithm 1), an approximation
+//                   switched on by an element budget 0 < B2 < d.  Per query
+//                   head, only the B2 dimensions of q with the largest
+//                   magnitude (ties: the lower index) enter the logits; the
+//                   softmax P of those logits over every retained token feeds
+//                   the importance unchanged; for the output, P is cut into
+//                   chunks of d consecutive entries in position order, each
+//                   chunk keeps its B2 largest entries (ties: the lower
+//                   position) and the output is the sum of those p_j v_j, not
+//                   renormalised.  A chunk of at most B2 entries keeps all.
 //  * eviction       when n > B: sinks (pos < S) and the recent window
 //                   (pos > t - W) are always kept; of the rest keep the
 //                   B - S - W with the largest importance, ties by lowest
@@ -76,6 +86,8 @@ struct Oracle {
     int out_bf16;
     int nthreads;
     int recent_only = 0;             // HiKV Stage I: accumulate in the recent bank only
+    int elem = 0;                    // HiKV Stage II element budget B2 (0: off)
+    std::vector<uint8_t> near_tie;   // [L*B*Hq]: Stage II chunk selection decided by < 1e-4
     std::vector<int32_t> budget;     // [L * Hkv]
     std::vector<Unit> units;         // [L][B][Hkv]
     int unit_index(int l, int b, int g) const { return (l * B + b) * Hkv + g; }
@@ -140,6 +152,56 @@ void attend(const Oracle& O, const std::vector<Entry>& e, const float* q,
     }
 }
 
+// HiKV Stage II attention of one query head over every entry of `e` (which is
+// in position order).  Writes the whole softmax P into p and the output of
+// the chunk-selected entries into o; sets *near_tie when the B2-th and the
+// (B2+1)-th largest p of some chunk differ by less than 1e-4 of the former
+// (a selection that the rounding of the logits could flip).
+void attend_stage2(const Oracle& O, const std::vector<Entry>& e, const float* q,
+                   std::vector<double>& p, double* o, bool* near_tie) {
+    const int d = O.d, B2 = O.elem;
+    const size_t n = e.size();
+    // K side: the B2 dimensions of largest |q|, the lower index first on ties
+    std::vector<int> dims(d);
+    for (int c = 0; c < d; ++c) dims[c] = c;
+    std::stable_sort(dims.begin(), dims.end(),
+                     [&](int a, int b) { return std::fabs(q[a]) > std::fabs(q[b]); });
+    dims.resize(B2);
+    std::sort(dims.begin(), dims.end());
+    std::vector<double> s(n);
+    double m = -INFINITY;
+    for (size_t j = 0; j < n; ++j) {
+        double acc = 0.0;
+        for (int c : dims) acc += (double)q[c] * (double)e[j].k[c];
+        s[j] = O.scale * acc;
+        m = std::max(m, s[j]);
+    }
+    double l = 0.0;
+    for (size_t j = 0; j < n; ++j) l += std::exp(s[j] - m);
+    p.assign(n, 0.0);
+    for (size_t j = 0; j < n; ++j) p[j] = std::exp(s[j] - m) / l;
+    // V side: chunks of d entries, the B2 largest p of each
+    std::vector<uint8_t> keep(n, 0);
+    for (size_t c0 = 0; c0 < n; c0 += d) {
+        const size_t c1 = std::min(n, c0 + (size_t)d);
+        if (c1 - c0 <= (size_t)B2) {
+            for (size_t j = c0; j < c1; ++j) keep[j] = 1;
+            continue;
+        }
+        std::vector<size_t> idx;
+        for (size_t j = c0; j < c1; ++j) idx.push_back(j);
+        std::stable_sort(idx.begin(), idx.end(), [&](size_t a, size_t b) { return p[a] > p[b]; });
+        for (int r = 0; r < B2; ++r) keep[idx[r]] = 1;
+        const double last = p[idx[B2 - 1]], next = p[idx[B2]];
+        if (last - next < 1e-4 * last) *near_tie = true;
+    }
+    for (int c = 0; c < d; ++c) o[c] = 0.0;
+    for (size_t j = 0; j < n; ++j) {
+        if (!keep[j]) continue;
+        for (int c = 0; c < d; ++c) o[c] += p[j] * (double)e[j].v[c];
+    }
+}
+
 bool range_ok(const Oracle* O, int layer0, int nl) {
     return O && layer0 >= 0 && nl >= 0 && layer0 + nl <= O->L;
 }
@@ -159,6 +221,7 @@ void* ora_create(int L, int B, int Hq, int Hkv, int d, int S, int W,
     O->nthreads = nthreads > 0 ? nthreads : 1;
     O->budget.assign(budgets, budgets + L * Hkv);
     O->units.resize((size_t)L * B * Hkv);
+    O->near_tie.assign((size_t)L * B * Hq, 0);
     return O;
 }
 
@@ -264,7 +327,13 @@ int ora_decode(void* h, int layer0, int nl, const float* q, float* out) {
         for (int hh = 0; hh < O->G; ++hh) {
             int head = g * O->G + hh;
             size_t row = (((size_t)li * O->B + b) * O->Hq + head) * O->d;
-            attend(*O, U.e, q + row, INT32_MAX, p, o.data());
+            if (O->elem > 0 && O->elem < O->d) {
+                bool tie = false;
+                attend_stage2(*O, U.e, q + row, p, o.data(), &tie);
+                O->near_tie[(size_t)u / O->Hkv * O->Hq + head] = tie ? 1 : 0;
+            } else {
+                attend(*O, U.e, q + row, INT32_MAX, p, o.data());
+            }
             for (size_t j = 0; j < U.e.size(); ++j) colsum[j] += p[j];
             for (int c = 0; c < O->d; ++c)
                 out[row + c] = O->out_bf16 ? round_bf16(o[c]) : (float)o[c];
@@ -284,6 +353,26 @@ int ora_decode(void* h, int layer0, int nl, const float* q, float* out) {
 int ora_set_recent_only(void* h, int on) {
     Oracle* O = (Oracle*)h;
     O->recent_only = on ? 1 : 0;
+    return 0;
+}
+
+// HiKV Stage II element budget of decode steps: 0 (or d) = exact attention,
+// 0 < b2 < d = the element-level approximation.
+int ora_set_element_budget(void* h, int b2) {
+    Oracle* O = (Oracle*)h;
+    if (!O || b2 < 0 || b2 > O->d) return 1;
+    O->elem = b2;
+    return 0;
+}
+
+// Per query head of layers [layer0, layer0 + nl): 1 where the latest Stage II
+// decode step took a chunk selection that was decided by less than 1e-4
+// (relative) between the last kept and the first dropped p.  [nl][B][Hq].
+int ora_stage2_near_ties(void* h, int layer0, int nl, uint8_t* flags) {
+    Oracle* O = (Oracle*)h;
+    if (!range_ok(O, layer0, nl)) return 1;
+    const size_t per = (size_t)O->B * O->Hq;
+    std::memcpy(flags, O->near_tie.data() + (size_t)layer0 * per, (size_t)nl * per);
     return 0;
 }
 

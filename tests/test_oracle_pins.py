@@ -531,3 +531,113 @@ def test_duo_budgets():
     from oracle import budgets
     mask = np.array([[1, 0, 0], [0, 1, 0]], dtype=np.uint8)
     np.testing.assert_array_equal(budgets.duo(mask, 4096, 4, 256), [4096, 260, 260, 260, 4096, 260])
+
+
+# --------------------------------------------------------------------------
+# HiKV Stage II (sec. III-C, Algorithm 1): element-level selection.  Pinned
+# by brute force over subsets (a top-k set is the k-subset with the largest
+# sum), by the special case that reduces to exact attention, and by a
+# construction whose selected entries are known in advance.
+# --------------------------------------------------------------------------
+def _best_subset(values, k):
+    """Indices of the k-subset with the largest sum (values distinct)."""
+    from itertools import combinations
+    best, arg = -np.inf, None
+    for c in combinations(range(len(values)), k):
+        s = float(np.sum(np.asarray(values, np.float64)[list(c)]))
+        if s > best:
+            best, arg = s, c
+    return list(arg)
+
+
+def test_stage2_equals_brute_force_subsets():
+    rng = np.random.default_rng(21)
+    d, B2, G, n = 8, 3, 2, 21           # P chunks of 8, 8 and 5 entries
+    O = oracle.Oracle(1, 1, G, 1, d, 0, 0, [1000])
+    O.set_element_budget(B2)
+    K, V = _rand(rng, 1, 1, 1, n, d), _rand(rng, 1, 1, 1, n, d)
+    O.append(0, K, V)
+    q = _rand(rng, 1, 1, G, d)
+    out = O.decode(0, q)
+    _, imp = O.state(0)
+    scale = 1.0 / np.sqrt(d)
+    colsum = np.zeros(n)
+    for h in range(G):
+        qh = q[0, 0, h].astype(np.float64)
+        dims = _best_subset(np.abs(qh), B2)
+        s = scale * (K[0, 0, 0][:, dims].astype(np.float64) @ qh[dims])
+        p = np.exp(s - s.max())
+        p /= p.sum()
+        colsum += p
+        keep = []
+        for c0 in range(0, n, d):
+            idx = list(range(c0, min(n, c0 + d)))
+            keep += idx if len(idx) <= B2 else [idx[i] for i in _best_subset(p[idx], B2)]
+        ref = p[keep] @ V[0, 0, 0][keep].astype(np.float64)
+        np.testing.assert_allclose(out[0, 0, h], ref, rtol=0, atol=1e-12 * np.abs(ref).max() + 1e-7 * np.abs(ref).max())
+        # a plain global top-3 of P would pick another set here
+        assert sorted(keep) != sorted(np.argsort(-p)[:len(keep)].tolist())
+    # the importance takes the whole P: its head-summed columns, and mass G
+    np.testing.assert_allclose(imp, colsum.astype(np.float32), rtol=1e-7, atol=0)
+    assert abs(float(np.sum(imp, dtype=np.float64)) - G) < 1e-5
+    assert not O.stage2_near_ties(0, 1).any()
+
+
+def test_stage2_with_sparse_query_and_short_context_is_exact_attention():
+    # q has exactly B2 non-zero dimensions, some negative: the magnitude rule
+    # keeps all of them, so the logits are the exact ones; n <= B2 leaves a
+    # single chunk that keeps every entry.  Output = library SDPA.
+    rng = np.random.default_rng(5)
+    d, B2, G, n = 32, 16, 4, 16
+    O = oracle.Oracle(1, 2, G, 1, d, 0, 0, [1000])
+    O.set_element_budget(B2)
+    K, V = _rand(rng, 1, 2, 1, n, d), _rand(rng, 1, 2, 1, n, d)
+    O.append(0, K, V)
+    q = np.zeros((1, 2, G, d), np.float32)
+    for b in range(2):
+        for h in range(G):
+            dims = rng.choice(d, B2, replace=False)
+            q[0, b, h, dims] = rng.uniform(0.2, 2.0, B2) * rng.choice([-1.0, 1.0], B2)
+    out = O.decode(0, q)
+    for b in range(2):
+        ref = _sdpa_ref(q[0, b][:, None, :], K[0, b], V[0, b], G)[:, 0]
+        np.testing.assert_allclose(out[0, b], ref, rtol=0, atol=1e-6 * np.abs(ref).max())
+
+
+def test_stage2_chunks_are_retained_entries_in_position_order():
+    # S = 2 sinks and a W = 10 window with budget S + W keep positions
+    # {0, 1, 14..23} of a 24-token prompt; after position 24 is appended the
+    # 13 entries form the chunks [0, 1, 14..19] and [20..24] (by rank, not by
+    # position value).  Keys are a_p * ones, so the logits follow a_p and the
+    # B2 = 3 entries kept in each chunk are known in advance.
+    d, B2, S, Wn = 8, 3, 2, 10
+    O = oracle.Oracle(1, 1, 1, 1, d, S, Wn, [S + Wn])
+    O.set_element_budget(B2)
+    a = np.zeros(25)
+    a[[0, 1, 14, 15, 16, 17, 18, 19]] = [0.1, 0.9, 0.2, 0.8, 0.3, 0.7, 0.4, 0.6]
+    a[[20, 21, 22, 23, 24]] = [0.5, 0.05, 0.95, 0.15, 0.85]
+    a[2:14] = np.linspace(1.0, 2.0, 12)          # evicted before the decode step
+    K = np.repeat(a[:, None], d, axis=1).astype(np.float32)[None, None, None]
+    V = np.zeros((1, 1, 1, 25, d), np.float32)
+    V[..., 0] = 1.0
+    V[..., 1] = np.arange(25, dtype=np.float32)
+    O.append(0, K[:, :, :, :24], V[:, :, :, :24])
+    O.evict(0, 1)
+    pos, _ = O.state(0)
+    assert pos.tolist() == [0, 1] + list(range(14, 24))
+    O.append(0, K[:, :, :, 24:], V[:, :, :, 24:])
+    q = np.zeros((1, 1, 1, d), np.float32)
+    q[0, 0, 0, [1, 4, 6]] = [3.0, 2.0, 1.0]       # the three largest |q|
+    out = O.decode(0, q)[0, 0, 0]
+    kept_pos = [0, 1] + list(range(14, 25))
+    s = (1.0 / np.sqrt(d)) * 6.0 * a[kept_pos]    # <q, a_p * ones> = 6 a_p
+    p = np.exp(s - s.max())
+    p /= p.sum()
+    chosen = {1, 15, 17, 20, 22, 24}              # top 3 of a in each chunk
+    sel = np.array([x in chosen for x in kept_pos])
+    assert abs(out[0] - p[sel].sum()) < 1e-6
+    assert abs(out[1] - (p[sel] * np.array(kept_pos)[sel]).sum()) < 1e-5
+    # the two plausible misreadings keep other sets: chunks by position value
+    # (0-7, 8-15, 16-23, 24) and one global top 6
+    for wrong in ({0, 1, 14, 15, 17, 19, 22, 24}, {1, 15, 17, 19, 22, 24}):
+        assert abs(out[0] - p[np.array([x in wrong for x in kept_pos])].sum()) > 1e-3
