@@ -47,7 +47,8 @@ class hikv_config(ctypes.Structure):
                 ("budgets", ctypes.POINTER(ctypes.c_int32)), ("max_tokens", ctypes.c_int32),
                 ("page_tokens", ctypes.c_int32), ("pool_pages", ctypes.c_int64),
                 ("max_window_queries", ctypes.c_int32), ("scale", ctypes.c_float),
-                ("pool_kernel", ctypes.c_int32), ("importance_mode", ctypes.c_int32)]
+                ("pool_kernel", ctypes.c_int32), ("importance_mode", ctypes.c_int32),
+                ("element_budget", ctypes.c_int32)]
 
 
 def _load():
@@ -129,6 +130,7 @@ class CacheConfig:
     scale: float = 0.0
     pool_kernel: int = 0           # SnapKV max-pool of the prompt scores (0/1: off)
     importance_mode: int = 0       # 0: H2O cumulative, 1: HiKV recent bank only
+    element_budget: int = 0        # HiKV Stage II B2 (0 or head_dim: exact attention)
 
 
 def hikv_create_cache(cfg: CacheConfig) -> ctypes.c_void_p:
@@ -137,7 +139,7 @@ def hikv_create_cache(cfg: CacheConfig) -> ctypes.c_void_p:
                     HIKV_BF16 if cfg.dtype == "bf16" else HIKV_F32, cfg.num_sink,
                     cfg.recent_window, b.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
                     cfg.max_tokens, cfg.page_tokens, cfg.pool_pages, cfg.max_window_queries,
-                    cfg.scale, cfg.pool_kernel, cfg.importance_mode)
+                    cfg.scale, cfg.pool_kernel, cfg.importance_mode, cfg.element_budget)
     h = ctypes.c_void_p()
     _check(_lib.hikv_create_cache(ctypes.byref(c), ctypes.byref(h)))
     return h

@@ -132,6 +132,12 @@ struct hikv_cache {
     int cs_override = 0;                // HIKV_DECODE_CS (tuning)
     int64_t launches = 0;               // kernels launched through this cache
     int pool_k = 0;                     // SnapKV pooling of the prompt scores (> 1: on)
+    // HiKV Stage II element-level decode (elem > 0: on)
+    int elem = 0;
+    int elem_stride = 0;                // row stride of its order / logit buffers
+    int32_t* d_eorder = nullptr;        // [units][elem_stride]
+    float* d_elg = nullptr;             // [units][G][elem_stride]
+    float* d_epart = nullptr;           // [units][max spans][G][d + 2]
 };
 
 namespace {
@@ -202,6 +208,9 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
     if (!(f.scale >= 0.f) || !std::isfinite(f.scale)) return fail(HIKV_ERR_INVALID_ARG, "create: bad scale");
     if (f.importance_mode != 0 && f.importance_mode != 1)
         return fail(HIKV_ERR_INVALID_ARG, "create: importance_mode %d not in {0, 1}", f.importance_mode);
+    if (f.element_budget < 0 || f.element_budget > f.head_dim)
+        return fail(HIKV_ERR_INVALID_ARG, "create: element_budget %d not in [0, head_dim=%d]", f.element_budget,
+                    f.head_dim);
     if (f.pool_kernel < 0 || f.pool_kernel > kMaxPoolKernel)
         return fail(HIKV_ERR_INVALID_ARG, "create: pool_kernel %d not in [0, %d]", f.pool_kernel, kMaxPoolKernel);
     const int64_t units64 = (int64_t)f.num_layers * f.batch * f.num_kv_heads;
@@ -229,6 +238,7 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
     }
     c->scale = f.scale > 0.f ? f.scale : 1.0f / std::sqrt((float)c->d);
     c->pool_k = f.pool_kernel;
+    c->elem = f.element_budget < f.head_dim ? f.element_budget : 0;
     c->budget_unit.resize(c->units);
     for (int u = 0; u < c->units; ++u)
         c->budget_unit[u] = f.budgets[(u / c->per_layer) * c->Hkv + u % c->Hkv];
@@ -302,6 +312,13 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
     c->asg_key.assign(c->L, 0);
     c->sasg_key.assign(c->L, 0);
     if (need_logits) ALLOC(c->d_logits, U * (size_t)c->cap * G);
+    if (c->elem) {
+        c->elem_stride = std::min(c->cap, elem_max_tokens());
+        const int spans = ceil_div(c->elem_stride, elem_span_ranks());
+        ALLOC(c->d_eorder, U * (size_t)c->elem_stride);
+        ALLOC(c->d_elg, U * (size_t)G * c->elem_stride);
+        ALLOC(c->d_epart, U * (size_t)spans * G * (c->d + 2));
+    }
 #undef ALLOC
 
     // TMA descriptor of the pool: [pool_pages * 2P rows][d elements], boxes of
@@ -731,6 +748,38 @@ hikv_status launch_decode_call(hikv_cache* c, int32_t layer0, int32_t nl, const 
 
 extern "C" {
 
+// HiKV Stage II decode of the layer range: sort, span and merge kernels.
+static hikv_status launch_elem_call(hikv_cache* c, int32_t layer0, int32_t nl, const void* q, void* out,
+                                    hikv_stream_t stream) {
+    const int u0 = layer0 * c->per_layer, nu = nl * c->per_layer;
+    int max_n = 0;
+    for (int u = u0; u < u0 + nu; ++u) {
+        if (c->len[u] <= 0) return fail(HIKV_ERR_STATE, "decode_step: unit %d is empty", u);
+        if (c->len[u] > c->elem_stride)
+            return fail(HIKV_ERR_CAPACITY, "decode_step: unit %d holds %d tokens, more than the %d of an element-level step",
+                        u, c->len[u], c->elem_stride);
+        max_n = std::max(max_n, c->len[u]);
+    }
+    ElemArgs a{};
+    a.v = c->v;
+    a.q = q;
+    a.out = out;
+    a.u0 = u0;
+    a.nunits = nu;
+    a.layer0 = layer0;
+    a.b2 = c->elem;
+    a.ostride = c->elem_stride;
+    a.nsp = ceil_div(max_n, elem_span_ranks());
+    a.qscale = c->scale * 1.4426950408889634f;
+    a.order = c->d_eorder;
+    a.lg = c->d_elg;
+    a.part = c->d_epart;
+    cudaError_t e = launch_elem_decode(a, c->dtype, c->d, max_n, (cudaStream_t)stream);
+    c->launches += 3;
+    if (e != cudaSuccess) return cuda_fail(e, "decode_step: element-level launch");
+    return HIKV_OK;
+}
+
 hikv_status hikv_decode_step(hikv_cache* c, int32_t layer0, int32_t nl, const void* q, void* out,
                              hikv_stream_t stream) {
     g_err.clear();
@@ -738,7 +787,8 @@ hikv_status hikv_decode_step(hikv_cache* c, int32_t layer0, int32_t nl, const vo
     if (!range_ok(c, layer0, nl)) return fail(HIKV_ERR_INVALID_ARG, "decode_step: bad cache or layer range");
     if (!q || !out) return fail(HIKV_ERR_INVALID_ARG, "decode_step: null q or out");
     if (q == out) return fail(HIKV_ERR_INVALID_ARG, "decode_step: out aliases q");
-    hikv_status st = launch_decode_call(c, layer0, nl, q, out, 0, 0, nullptr, nullptr, stream, "decode_step");
+    hikv_status st = c->elem ? launch_elem_call(c, layer0, nl, q, out, stream)
+                             : launch_decode_call(c, layer0, nl, q, out, 0, 0, nullptr, nullptr, stream, "decode_step");
     if (st != HIKV_OK) return st;
     const int u0 = layer0 * c->per_layer, nu = nl * c->per_layer;
     for (int u = u0; u < u0 + nu; ++u) c->fresh[u] = 1;
@@ -755,7 +805,7 @@ hikv_status hikv_decode_step_fused(hikv_cache* c, int32_t layer0, int32_t nl, co
     if (((uintptr_t)k | (uintptr_t)v) & 15)
         return fail(HIKV_ERR_INVALID_ARG, "decode_step_fused: k and v must be 16-byte aligned");
     const int u0 = layer0 * c->per_layer, nu = nl * c->per_layer;
-    bool one_launch = true;
+    bool one_launch = c->elem == 0;   // the element-level step has kernels of its own
     for (int u = u0; u < u0 + nu && one_launch; ++u) {
         const int n = c->len[u] + 1;
         if (n > c->cap) return fail(HIKV_ERR_CAPACITY, "decode_step_fused: unit %d would exceed max_tokens", u);

@@ -521,4 +521,22 @@ struct GatherArgs {
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s);
 cudaError_t launch_selftest_timeout(const View& v, uint64_t limit_ns, cudaStream_t s);
 
+// HiKV Stage II element-level decode (k_elem.cu): sort, span and merge kernels.
+struct ElemArgs {
+    View v;
+    const void* q;         // [nl][B][Hq][d]
+    void* out;             // [nl][B][Hq][d]
+    int32_t u0, nunits, layer0;
+    int32_t b2;            // element budget, 0 < b2 < d
+    int32_t ostride;       // row stride of order / lg (>= every unit's length)
+    int32_t nsp;           // span CTAs per unit in the grid
+    float qscale;          // scale * log2(e)
+    int32_t* order;        // [nunits][ostride] slots in position order
+    float* lg;             // [nunits][G][ostride] logits by slot (log2 domain)
+    float* part;           // [nunits][nsp][G][d + 2] span (m, l, o)
+};
+int elem_span_ranks();
+int elem_max_tokens();
+cudaError_t launch_elem_decode(const ElemArgs& a, int dtype, int d, int max_n, cudaStream_t s);
+
 }  // namespace hikv

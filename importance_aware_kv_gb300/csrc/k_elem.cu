@@ -1,0 +1,525 @@
+// HiKV Stage II: element-level decode attention (HiKV sec. III-C, Algorithm 1).
+//
+// An approximation of the decode step, switched on by an element budget
+// 0 < B2 < d.  Per query head h of a unit:
+//   * K side: only the B2 dimensions of q_h with the largest |q| (ties: the
+//     lower index) enter the logits, s_j = scale * sum_{c in E_Q} q_h[c] k_j[c];
+//   * the softmax P of those logits over every retained token feeds the
+//     importance update unchanged (Algorithm 1 adds P_t to the scores);
+//   * V side: P is cut into chunks of d entries in position order (rank by
+//     position among the retained tokens); each chunk keeps its B2 largest
+//     entries (ties: the lower position) and the output is the sum of those
+//     p_j v_j, not renormalised.  A chunk of at most B2 entries keeps all.
+// Selecting the largest p of a chunk is selecting its largest logits (exp is
+// increasing and every entry of a head shares m and l), so the kernels select
+// on the logits.
+//
+// Three kernels per call:
+//   k_elem_order  one CTA per unit: bitonic sort of (position, slot) keys in
+//                 shared memory -> the unit's slots in position order;
+//   k_elem_span   one CTA per (unit, span of kElemSpan ranks): masked-q
+//                 logits of the span's rows (8 lanes per row), per-span
+//                 softmax statistics, the top-B2 selection of each d-rank
+//                 chunk and head (a radix select on the logit bits in one
+//                 warp), then p.v over the rows that at least one head of
+//                 the group selected -- V rows no head selected are not read;
+//   k_elem_merge  one CTA per unit: merges the spans' (m, l, o), writes the
+//                 output, adds sum_h 2^(s - m_h) / l_h to every retained
+//                 token's importance (HiKV Stage I mode: the recent bank
+//                 only) and records the eviction victim, as the exact decode
+//                 kernel does.
+//
+// The K side reads whole rows: the pool stores token-major rows, so B2 of the
+// d dimensions of a row lie in nearly every 32-byte sector (DRAM's unit), and
+// under GQA the union of the group's dimension sets covers most of d anyway.
+#include "hikv_internal.cuh"
+
+namespace hikv {
+namespace {
+
+constexpr int kElemThreads = 256;
+constexpr int kElemWarps = kElemThreads / 32;
+constexpr int kElemSpan = 512;       // ranks per span CTA (a multiple of d)
+constexpr int kElemMaxG = 8;
+constexpr int kOrderThreads = 1024;
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// N consecutive elements of type T at p (16-byte aligned when N*sizeof(T) >= 16,
+// else N*sizeof(T)-aligned), widened to float.
+template <typename T, int N>
+__device__ __forceinline__ void load_vec(const uint8_t* p, float (&x)[N]) {
+    constexpr int BYTES = N * (int)sizeof(T);
+    if constexpr (BYTES >= 16) {
+        static_assert(BYTES % 16 == 0, "vector width");
+#pragma unroll
+        for (int i = 0; i < BYTES / 16; ++i) {
+            const uint4 w = __ldg(reinterpret_cast<const uint4*>(p) + i);
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                if constexpr (sizeof(T) == 2) {
+                    x[i * 8 + 2 * k] = __uint_as_float(ws[k] << 16);
+                    x[i * 8 + 2 * k + 1] = __uint_as_float(ws[k] & 0xFFFF0000u);
+                } else {
+                    x[i * 4 + k] = __uint_as_float(ws[k]);
+                }
+            }
+        }
+    } else if constexpr (BYTES == 8) {
+        const uint2 w = __ldg(reinterpret_cast<const uint2*>(p));
+        if constexpr (sizeof(T) == 2) {
+            x[0] = __uint_as_float(w.x << 16);
+            x[1] = __uint_as_float(w.x & 0xFFFF0000u);
+            x[2] = __uint_as_float(w.y << 16);
+            x[3] = __uint_as_float(w.y & 0xFFFF0000u);
+        } else {
+            x[0] = __uint_as_float(w.x);
+            x[1] = __uint_as_float(w.y);
+        }
+    } else {
+        static_assert(BYTES == 4 && sizeof(T) == 2, "vector width");
+        const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(p));
+        x[0] = __uint_as_float(w << 16);
+        x[1] = __uint_as_float(w & 0xFFFF0000u);
+    }
+}
+
+__device__ __forceinline__ void store_out(float* p, float x) { *p = x; }
+__device__ __forceinline__ void store_out(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+
+// order-preserving map of a float's bits to an unsigned key
+__device__ __forceinline__ uint32_t ord_key(float x) {
+    const uint32_t b = __float_as_uint(x);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// ---------------------------------------------------------------------------
+// k_elem_order: slots of each unit in position order (positions are unique)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kOrderThreads) k_elem_order(const ElemArgs a, int npow2) {
+    extern __shared__ unsigned long long okeys[];
+    const View& v = a.v;
+    const int32_t uu = blockIdx.x, u = a.u0 + uu;
+    const int32_t n = v.len[u];
+    const int tid = threadIdx.x;
+    for (int i = tid; i < npow2; i += kOrderThreads)
+        okeys[i] = i < n ? ((unsigned long long)(uint32_t)v.pos[(int64_t)u * v.cap + i] << 32) | (uint32_t)i
+                         : ~0ull;
+    __syncthreads();
+    for (int k = 2; k <= npow2; k <<= 1)
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = tid; i < npow2; i += kOrderThreads) {
+                const int ij = i ^ j;
+                if (ij > i) {
+                    const unsigned long long x = okeys[i], y = okeys[ij];
+                    const bool up = (i & k) == 0;
+                    if ((x > y) == up) {
+                        okeys[i] = y;
+                        okeys[ij] = x;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    int32_t* ord = a.order + (int64_t)uu * a.ostride;
+    for (int i = tid; i < n; i += kOrderThreads) ord[i] = (int32_t)(uint32_t)okeys[i];
+}
+
+// ---------------------------------------------------------------------------
+// k_elem_span
+// ---------------------------------------------------------------------------
+template <int D>
+struct SpanLayout {
+    size_t sl, qr, qm, S, sel, ul, ml, op, cnt, total;
+    __host__ __device__ SpanLayout(int G) {
+        size_t o = 0;
+        auto take = [&](size_t bytes) { size_t r = o; o += (bytes + 15) / 16 * 16; return r; };
+        sl = take(kElemSpan * 4);                        // slot of each rank
+        qr = take((size_t)G * D * 4);                    // q as float
+        qm = take((size_t)G * D * 4);                    // q with the dropped dimensions zeroed
+        S = take((size_t)G * kElemSpan * 4);             // logits, then p of the kept entries
+        sel = take((size_t)G * kElemSpan);               // kept by head h
+        ul = take(kElemSpan * 4);                        // ranks some head kept
+        ml = take((size_t)2 * kElemMaxG * 4);            // span (m, l) per head
+        op = take((size_t)kElemWarps * G * D * 4);       // per-warp output sums
+        cnt = take(kElemWarps * 4 + 16);
+        total = o;
+    }
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kElemThreads) k_elem_span(const ElemArgs a) {
+    constexpr int DK = D / 8;    // dimensions per lane in the q.k pass (8 lanes per row)
+    constexpr int DV = D / 32;   // dimensions per lane in the p.v pass (a warp per row)
+    extern __shared__ __align__(16) uint8_t esm[];
+    const View& v = a.v;
+    const int G = v.group;
+    const SpanLayout<D> L(G);
+    int32_t* sl = reinterpret_cast<int32_t*>(esm + L.sl);
+    float* qr = reinterpret_cast<float*>(esm + L.qr);
+    float* qm = reinterpret_cast<float*>(esm + L.qm);
+    float* S = reinterpret_cast<float*>(esm + L.S);
+    uint8_t* sel = esm + L.sel;
+    int32_t* ul = reinterpret_cast<int32_t*>(esm + L.ul);
+    float* ml = reinterpret_cast<float*>(esm + L.ml);
+    float* op = reinterpret_cast<float*>(esm + L.op);
+    int32_t* wcnt = reinterpret_cast<int32_t*>(esm + L.cnt);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int32_t uu = blockIdx.y, u = a.u0 + uu, sp = blockIdx.x;
+    const int32_t n = v.len[u];
+    const int32_t r0 = sp * kElemSpan;
+    if (r0 >= n) return;
+    const int32_t cnt = min(n - r0, kElemSpan);
+    const int per_layer = v.batch * v.hkv;
+    const int li = u / per_layer - a.layer0, b = (u / v.hkv) % v.batch, gh = u % v.hkv;
+    const int64_t qoff = (((int64_t)li * v.batch + b) * v.hq + (int64_t)gh * G) * D;
+
+    const int32_t* ord = a.order + (int64_t)uu * a.ostride;
+    for (int i = tid; i < cnt; i += kElemThreads) sl[i] = ord[r0 + i];
+    const T* qg = reinterpret_cast<const T*>(a.q) + qoff;
+    for (int e = tid; e < G * D; e += kElemThreads) qr[e] = to_f(qg[e]);
+    __syncthreads();
+    // K side: keep dimension c of head h iff fewer than B2 dimensions beat it
+    // (larger |q|, or equal |q| at a lower index)
+    for (int e = tid; e < G * D; e += kElemThreads) {
+        const int h = e / D, c = e - h * D;
+        const float x = fabsf(qr[e]);
+        const float* row = qr + h * D;
+        int beat = 0;
+        for (int c2 = 0; c2 < D; ++c2) {
+            const float y = fabsf(row[c2]);
+            beat += (y > x) || (y == x && c2 < c);
+        }
+        qm[e] = beat < a.b2 ? qr[e] : 0.f;
+    }
+    __syncthreads();
+
+    // logits of the span's rows: 8 lanes per row, DK dimensions each
+    {
+        const int grp = lane >> 3, sub = lane & 7;
+        float* lgu = a.lg + (int64_t)uu * G * a.ostride;
+        for (int i0 = warp * 4; i0 < cnt; i0 += kElemWarps * 4 * 2) {
+            float kx[2][DK];
+            bool ok[2];
+            int32_t slot[2];
+#pragma unroll
+            for (int w = 0; w < 2; ++w) {
+                const int i = i0 + w * kElemWarps * 4 + grp;
+                ok[w] = i < cnt;
+                slot[w] = ok[w] ? sl[i] : 0;
+                const uint8_t* rp = ok[w] ? row_ptr(v, u, slot[w], false) : nullptr;
+                ok[w] = ok[w] && rp;
+                if (ok[w]) load_vec<T, DK>(rp + sub * DK * (int)sizeof(T), kx[w]);
+            }
+#pragma unroll
+            for (int w = 0; w < 2; ++w) {
+                const int i = i0 + w * kElemWarps * 4 + grp;
+                for (int h = 0; h < G; ++h) {
+                    const float4* qv = reinterpret_cast<const float4*>(qm + h * D + sub * DK);
+                    float acc = 0.f;
+#pragma unroll
+                    for (int c4 = 0; c4 < DK / 4; ++c4) {
+                        const float4 qq = qv[c4];
+                        if (ok[w]) {
+                            acc = fmaf(qq.x, kx[w][4 * c4], acc);
+                            acc = fmaf(qq.y, kx[w][4 * c4 + 1], acc);
+                            acc = fmaf(qq.z, kx[w][4 * c4 + 2], acc);
+                            acc = fmaf(qq.w, kx[w][4 * c4 + 3], acc);
+                        }
+                    }
+                    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+                    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+                    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+                    if (sub == 0 && i < cnt) {
+                        const float s = ok[w] ? acc * a.qscale : -INFINITY;
+                        S[h * kElemSpan + i] = s;
+                        lgu[(int64_t)h * a.ostride + slot[w]] = s;
+                    }
+                }
+            }
+        }
+    }
+    __syncthreads();
+
+    // per-head span statistics (warp h), then the chunk selections
+    for (int h = warp; h < G; h += kElemWarps) {
+        float m = -INFINITY;
+        for (int i = lane; i < cnt; i += 32) m = fmaxf(m, S[h * kElemSpan + i]);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float l = 0.f;
+        if (m > -INFINITY)
+            for (int i = lane; i < cnt; i += 32) l += exp2f(S[h * kElemSpan + i] - m);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+        if (lane == 0) {
+            ml[2 * h] = m;
+            ml[2 * h + 1] = l;
+        }
+    }
+    {
+        constexpr int PER = D / 32;   // ranks of a chunk per lane: k * 32 + lane
+        const int nch = (cnt + D - 1) / D;
+        for (int task = warp; task < nch * G; task += kElemWarps) {
+            const int ch = task / G, h = task - ch * G;
+            const int base = ch * D;
+            const int m_c = min(D, cnt - base);
+            const float* Sh = S + h * kElemSpan + base;
+            uint8_t* selh = sel + h * kElemSpan + base;
+            if (m_c <= a.b2) {
+                for (int k = lane; k < m_c; k += 32) selh[k] = 1;
+                continue;
+            }
+            uint32_t key[PER];
+            bool val[PER];
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                const int r = k * 32 + lane;
+                val[k] = r < m_c;
+                key[k] = val[k] ? ord_key(Sh[r]) : 0u;
+            }
+            // the B2-th largest key: set bits from the top while >= B2 keys reach
+            uint32_t thr = 0u;
+            for (int bit = 31; bit >= 0; --bit) {
+                const uint32_t cand = thr | (1u << bit);
+                int c = 0;
+#pragma unroll
+                for (int k = 0; k < PER; ++k) c += __popc(__ballot_sync(0xffffffffu, val[k] && key[k] >= cand));
+                if (c >= a.b2) thr = cand;
+            }
+            int above = 0;
+#pragma unroll
+            for (int k = 0; k < PER; ++k) above += __popc(__ballot_sync(0xffffffffu, val[k] && key[k] > thr));
+            // equal keys fill the rest, lower rank (position) first
+            int need = a.b2 - above, before = 0;
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                const unsigned eq = __ballot_sync(0xffffffffu, val[k] && key[k] == thr);
+                const int mine = before + __popc(eq & ((1u << lane) - 1u));
+                const bool take = val[k] && (key[k] > thr || (key[k] == thr && mine < need));
+                if (val[k]) selh[k * 32 + lane] = take ? 1 : 0;
+                before += __popc(eq);
+            }
+        }
+    }
+    __syncthreads();
+
+    // p of the kept entries (span-local reference), and the union of the heads' rows
+    int keep_n = 0;
+    {
+        const int i = tid;   // kElemThreads >= kElemSpan / 2: two ranks per thread
+        int mine[2] = {0, 0};
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+            const int r = i + w * kElemThreads;
+            if (r >= cnt) continue;
+            int any = 0;
+            for (int h = 0; h < G; ++h) {
+                const bool k = sel[h * kElemSpan + r] != 0;
+                const float p = k ? exp2f(S[h * kElemSpan + r] - ml[2 * h]) : 0.f;
+                S[h * kElemSpan + r] = p;
+                any |= k;
+            }
+            mine[w] = any;
+        }
+        // ordered compaction of the kept ranks (rank order; deterministic sums)
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+            const unsigned m = __ballot_sync(0xffffffffu, mine[w]);
+            if (lane == 0) wcnt[warp] = __popc(m);
+            __syncthreads();
+            int off = keep_n;
+            for (int x = 0; x < warp; ++x) off += wcnt[x];
+            for (int x = 0; x < kElemWarps; ++x) keep_n += wcnt[x];
+            if (mine[w]) ul[off + __popc(m & ((1u << lane) - 1u))] = tid + w * kElemThreads;
+            __syncthreads();
+        }
+    }
+
+    // p.v over the kept rows: a warp per row, DV dimensions per lane
+    float acc[kElemMaxG][DV];
+#pragma unroll
+    for (int h = 0; h < kElemMaxG; ++h)
+#pragma unroll
+        for (int c = 0; c < DV; ++c) acc[h][c] = 0.f;
+    constexpr int UNR = 4;
+    for (int j0 = warp; j0 < keep_n; j0 += kElemWarps * UNR) {
+        float vx[UNR][DV];
+        int rr[UNR];
+        bool ok[UNR];
+#pragma unroll
+        for (int w = 0; w < UNR; ++w) {
+            const int j = j0 + w * kElemWarps;
+            ok[w] = j < keep_n;
+            rr[w] = ok[w] ? ul[j] : 0;
+            const uint8_t* rp = ok[w] ? row_ptr(v, u, sl[rr[w]], true) : nullptr;
+            ok[w] = ok[w] && rp;
+            if (ok[w]) load_vec<T, DV>(rp + lane * DV * (int)sizeof(T), vx[w]);
+        }
+#pragma unroll
+        for (int w = 0; w < UNR; ++w) {
+            if (!ok[w]) continue;
+#pragma unroll
+            for (int h = 0; h < kElemMaxG; ++h) {
+                if (h >= G) break;
+                const float p = S[h * kElemSpan + rr[w]];
+#pragma unroll
+                for (int c = 0; c < DV; ++c) acc[h][c] = fmaf(p, vx[w][c], acc[h][c]);
+            }
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < kElemMaxG; ++h) {
+        if (h >= G) break;
+#pragma unroll
+        for (int c = 0; c < DV; ++c) op[((size_t)warp * G + h) * D + lane * DV + c] = acc[h][c];
+    }
+    __syncthreads();
+    float* part = a.part + ((int64_t)uu * a.nsp + sp) * G * (D + 2);
+    for (int e = tid; e < G * D; e += kElemThreads) {
+        float s = 0.f;
+        for (int w = 0; w < kElemWarps; ++w) s += op[(size_t)w * G * D + e];
+        const int h = e / D, c = e - h * D;
+        part[h * (D + 2) + 2 + c] = s;
+    }
+    if (tid < G) {
+        part[tid * (D + 2)] = ml[2 * tid];
+        part[tid * (D + 2) + 1] = ml[2 * tid + 1];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// k_elem_merge
+// ---------------------------------------------------------------------------
+template <typename T, int D>
+__global__ void __launch_bounds__(kElemThreads) k_elem_merge(const ElemArgs a) {
+    __shared__ float mfin[kElemMaxG], linv[kElemMaxG];
+    __shared__ float wsp[kElemMaxG * 64];   // per (head, span) merge weight
+    __shared__ unsigned long long wkey[kElemWarps];
+    __shared__ int32_t wslot[kElemWarps];
+    const View& v = a.v;
+    const int G = v.group;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int32_t uu = blockIdx.x, u = a.u0 + uu;
+    const int32_t n = v.len[u];
+    const int nsp = (n + kElemSpan - 1) / kElemSpan;
+    const float* part = a.part + (int64_t)uu * a.nsp * G * (D + 2);
+    if (tid < G) {
+        const int h = tid;
+        float m = -INFINITY;
+        for (int s = 0; s < nsp; ++s) m = fmaxf(m, part[((int64_t)s * G + h) * (D + 2)]);
+        float l = 0.f;
+        for (int s = 0; s < nsp; ++s) {
+            const float ls = part[((int64_t)s * G + h) * (D + 2) + 1];
+            const float w = ls > 0.f ? exp2f(part[((int64_t)s * G + h) * (D + 2)] - m) : 0.f;
+            wsp[h * 64 + s] = w;
+            l += ls * w;
+        }
+        mfin[h] = m;
+        linv[h] = 1.0f / l;
+    }
+    __syncthreads();
+    const int per_layer = v.batch * v.hkv;
+    const int li = u / per_layer - a.layer0, b = (u / v.hkv) % v.batch, gh = u % v.hkv;
+    T* outg = reinterpret_cast<T*>(a.out) + (((int64_t)li * v.batch + b) * v.hq + (int64_t)gh * G) * D;
+    for (int e = tid; e < G * D; e += kElemThreads) {
+        const int h = e / D, c = e - h * D;
+        float o = 0.f;
+        for (int s = 0; s < nsp; ++s) o = fmaf(part[((int64_t)s * G + h) * (D + 2) + 2 + c], wsp[h * 64 + s], o);
+        store_out(outg + e, o * linv[h]);
+    }
+    // importance from the whole P, and the victim (smallest (imp, -pos) outside sinks and window)
+    const int32_t tnew = v.next_pos[u] - 1;
+    const bool need_victim = n > v.budget[u];
+    const int32_t lo = v.sink, hi = tnew - v.window;
+    const float* lgu = a.lg + (int64_t)uu * G * a.ostride;
+    unsigned long long kmin = ~0ull;
+    int32_t smin = -1;
+    for (int j = tid; j < n; j += kElemThreads) {
+        float inc = 0.f;
+        for (int h = 0; h < G; ++h) inc += exp2f(lgu[(int64_t)h * a.ostride + j] - mfin[h]) * linv[h];
+        const int64_t mi = (int64_t)u * v.cap + j;
+        const int32_t p = v.pos[mi];
+        const bool grows = !v.recent_only || p >= tnew - v.window;
+        const float nw = grows ? v.imp[mi] + inc : v.imp[mi];
+        v.imp[mi] = nw;
+        if (need_victim && p >= lo && p <= hi) {
+            const unsigned long long key =
+                ((unsigned long long)__float_as_uint(nw) << 32) | (unsigned long long)(~(uint32_t)p);
+            if (key < kmin) {
+                kmin = key;
+                smin = j;
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const unsigned long long ok = __shfl_xor_sync(0xffffffffu, kmin, o);
+        const int32_t os = __shfl_xor_sync(0xffffffffu, smin, o);
+        if (ok < kmin) {
+            kmin = ok;
+            smin = os;
+        }
+    }
+    if (lane == 0) {
+        wkey[warp] = kmin;
+        wslot[warp] = smin;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        unsigned long long kk = ~0ull;
+        int32_t s = -1;
+        for (int w = 0; w < kElemWarps; ++w)
+            if (wkey[w] < kk) {
+                kk = wkey[w];
+                s = wslot[w];
+            }
+        v.victim[u] = need_victim ? s : -1;
+    }
+}
+
+template <typename T, int D>
+cudaError_t launch_elem_t(const ElemArgs& a, int max_n, cudaStream_t s) {
+    int npow2 = 32;
+    while (npow2 < max_n) npow2 <<= 1;
+    const size_t osmem = (size_t)npow2 * 8;
+    const size_t ssmem = SpanLayout<D>(a.v.group).total;
+    static size_t o_set = 0, s_set = 0;
+    if (osmem > 48 * 1024 && osmem > o_set) {
+        cudaError_t e = cudaFuncSetAttribute(k_elem_order, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)osmem);
+        if (e != cudaSuccess) return e;
+        o_set = osmem;
+    }
+    if (ssmem > 48 * 1024 && ssmem > s_set) {
+        cudaError_t e = cudaFuncSetAttribute(k_elem_span<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssmem);
+        if (e != cudaSuccess) return e;
+        s_set = ssmem;
+    }
+    k_elem_order<<<a.nunits, kOrderThreads, osmem, s>>>(a, npow2);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    k_elem_span<T, D><<<dim3(a.nsp, a.nunits), kElemThreads, ssmem, s>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    k_elem_merge<T, D><<<a.nunits, kElemThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int elem_span_ranks() { return kElemSpan; }
+int elem_max_tokens() { return 16384; }
+
+cudaError_t launch_elem_decode(const ElemArgs& a, int dtype, int d, int max_n, cudaStream_t s) {
+    if (a.v.group > kElemMaxG || a.nsp > 64) return cudaErrorInvalidValue;
+    if (dtype == 0 && d == 64) return launch_elem_t<float, 64>(a, max_n, s);
+    if (dtype == 0 && d == 128) return launch_elem_t<float, 128>(a, max_n, s);
+    if (dtype == 1 && d == 64) return launch_elem_t<__nv_bfloat16, 64>(a, max_n, s);
+    if (dtype == 1 && d == 128) return launch_elem_t<__nv_bfloat16, 128>(a, max_n, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace hikv

@@ -95,6 +95,19 @@ typedef struct {
                                the lowest score outside the window is its "promote
                                the ejected token only if it beats the important
                                bank's minimum". */
+    int32_t element_budget; /* HiKV Stage II (HiKV sec. III-C, Algorithm 1): with
+                               0 < B2 = element_budget < head_dim, decode steps
+                               approximate attention at element level -- per query
+                               head only the B2 dimensions of q with the largest
+                               magnitude enter the logits; the softmax P of those
+                               logits over every retained token updates the
+                               importance; P is cut into chunks of head_dim
+                               entries in position order and only each chunk's B2
+                               largest entries (ties: the lower position)
+                               contribute p_j v_j to the output, which is not
+                               renormalised.  Units must then hold at most 16384
+                               tokens when a decode step runs.  0 or head_dim =>
+                               exact attention. */
 } hikv_config;
 
 /* Create a cache: allocates the page pool, page tables, per-slot importance
@@ -132,7 +145,10 @@ hikv_status hikv_score_window(hikv_cache* cache, int32_t layer0, int32_t nlayers
  * [nlayers][batch][Hq][d] in the cache dtype; out may not alias q.
  * Also records, for each unit holding more than its budget, its single
  * least-important evictable token, which a following hikv_evict uses when it
- * needs to drop exactly one token.  Errors: INVALID_ARG, STATE (an empty unit). */
+ * needs to drop exactly one token.  With an element_budget set the step is
+ * HiKV Stage II's element-level approximation (see hikv_config).
+ * Errors: INVALID_ARG, STATE (an empty unit), CAPACITY (Stage II and a unit
+ * holding more than 16384 tokens). */
 hikv_status hikv_decode_step(hikv_cache* cache, int32_t layer0, int32_t nlayers,
                              const void* q, void* out, hikv_stream_t stream);
 

@@ -26,6 +26,7 @@ import workloads as W
 TIE_REL = 1e-6
 IMP_REL, IMP_ABS_FRAC = 1e-4, 1e-6
 OUT_F32_REL, OUT_BF16_ABS = 1e-5, 2e-2
+STAGE2_SWAP_ABS = 2e-2
 
 
 @dataclass
@@ -36,6 +37,7 @@ class Report:
     importance_checked: int = 0
     max_out_err: float = 0.0
     max_imp_err_rel: float = 0.0
+    stage2_near_tie_rows: int = 0   # HiKV Stage II rows compared at the loose bound (selection decided by < 1e-4)
     notes: list = field(default_factory=list)
 
 
@@ -50,7 +52,8 @@ def _out_np(t: torch.Tensor) -> np.ndarray:
 class Lockstep:
     def __init__(self, w: W.Workload, seed=None, sample_layers=None, cs=None, budgets=None,
                  device="cuda", layer_chunk=None, full_cache=False, page_tokens=64,
-                 check_kv=True, full_twin_layers=None, pool_kernel=0, importance_mode=0, small_mode=None):
+                 check_kv=True, full_twin_layers=None, pool_kernel=0, importance_mode=0, small_mode=None,
+                 element_budget=0):
         import importance_aware_kv_gb300 as hk
         self.hk = hk
         self.w = w
@@ -73,7 +76,7 @@ class Lockstep:
                 w.layers, w.batch, w.hq, w.hkv, w.d, w.dtype, w.sink, w.window,
                 self.budgets, w.total_positions, page_tokens=page_tokens,
                 max_window_queries=max(32, w.nq), pool_kernel=pool_kernel,
-                importance_mode=importance_mode))
+                importance_mode=importance_mode, element_budget=element_budget))
         finally:
             if cs is not None:
                 os.environ.pop("HIKV_DECODE_CS", None)
@@ -82,6 +85,8 @@ class Lockstep:
         self.ora = oracle.Oracle(len(self.sample), w.batch, w.hq, w.hkv, w.d, w.sink, w.window, bs,
                                  out_bf16=(w.dtype == "bf16"), threads=os.cpu_count() or 1)
         self.ora.set_recent_only(importance_mode == 1)
+        self.ora.set_element_budget(element_budget)
+        self.elem = 0 < element_budget < w.d
         self.rep = Report()
         self.upl = w.batch * w.hkv
         # optional twin: a no-eviction cache fed the same inputs, checked on
@@ -93,7 +98,7 @@ class Lockstep:
                                            budgets=np.full_like(self.budgets, w.total_positions),
                                            sample=list(full_twin_layers), layer_chunk=self.layer_chunk,
                                            check_kv=False, rep=Report(), upl=self.upl, twin=None,
-                                           pool=pool_kernel))
+                                           pool=pool_kernel, elem=False))
             self.twin.cache = hk.Cache(hk.CacheConfig(
                 w.layers, w.batch, w.hq, w.hkv, w.d, w.dtype, w.sink, w.window, self.twin.budgets,
                 w.total_positions, page_tokens=page_tokens, max_window_queries=max(32, w.nq),
@@ -163,13 +168,14 @@ class Lockstep:
                 for si, l in enumerate(ls.sample):
                     ls.ora.append(si, W.to_f32(ks[s, l:l + 1]), W.to_f32(vs[s, l:l + 1]))
                 ora_out = [ls.ora.decode(si, W.to_f32(qs[s, l:l + 1])) for si, l in enumerate(ls.sample)]
+                ties = [ls.ora.stage2_near_ties(si, 1)[0] if ls.elem else None for si in range(len(ls.sample))]
                 if evict_now:
                     for si in range(len(ls.sample)):
                         ls.ora.evict(si, 1)
                 if (s % compare_every == 0) or s == steps - 1:
                     got = _out_np(out)
                     for si, l in enumerate(ls.sample):
-                        ls.compare_out(got[l], ora_out[si][0], s)
+                        ls.compare_out(got[l], ora_out[si][0], s, skip=ties[si])
                 if evict_now:
                     ls.compare_state(after_evict=True)
         for ls in self._all():
@@ -178,8 +184,21 @@ class Lockstep:
         return self.rep
 
     # ------------------------------------------------------------------
-    def compare_out(self, got, want, step):
+    def compare_out(self, got, want, step, skip=None):
+        """skip: [B][Hq] HiKV Stage II rows whose chunk selection the oracle
+        decided by less than 1e-4 in p, which rounding may flip: an entry of
+        p ~ 1/n swapped for its neighbour moves the row by far less than
+        STAGE2_SWAP_ABS, so those rows are held to that bound instead."""
         w = self.w
+        if skip is not None and skip.any():
+            loose = skip.reshape(-1)
+            self.rep.stage2_near_tie_rows += int(loose.sum())
+            g2, w2 = got.reshape(-1, w.d)[loose], want.reshape(-1, w.d)[loose]
+            m = float(np.abs(g2 - w2).max())
+            if m > STAGE2_SWAP_ABS:
+                raise AssertionError(f"step {step}: near-tie Stage II row err {m:.3e} > {STAGE2_SWAP_ABS}")
+            got = got.reshape(-1, w.d)[~loose]
+            want = want.reshape(-1, w.d)[~loose]
         if w.dtype == "f32":
             rows_got = got.reshape(-1, w.d)
             rows_want = want.reshape(-1, w.d)

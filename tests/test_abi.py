@@ -51,6 +51,8 @@ def _cfg(hk, **kw):
     (dict(pool_kernel=-1), 1),
     (dict(pool_kernel=65), 1),                                    # SnapKV kernel above 64
     (dict(importance_mode=2), 1),
+    (dict(element_budget=-1), 1),
+    (dict(element_budget=129), 1),                                # HiKV Stage II B2 above head_dim
 ])
 def test_create_rejects_bad_config_on_host(hk, kw, status):
     with pytest.raises(hk.HikvError) as ei:

@@ -171,6 +171,57 @@ def test_hikv_dual_bank_llama3_8b_layer():
     assert rep.evictions_checked == 64 * (1 + 256)
 
 
+# HiKV Stage II: element-level attention against the oracle's statement of it.
+# Output rows whose chunk selection the oracle decided by less than 1e-4 in p
+# are left out of the output comparison (counted in the report); importance,
+# which takes the whole P, and the retained sets are compared everywhere.
+@FUSED
+@pytest.mark.parametrize("kw,b2", [
+    (dict(), 64),                                                   # one chunk of 97 entries
+    (dict(prompt=1200, budget=700), 32),                            # two spans, six chunks, ragged tail
+    (dict(prompt=1200, budget=700), 1),                             # extreme budgets
+    (dict(prompt=1200, budget=700), 127),
+    (dict(dtype="f32", d=64, hq=4, hkv=2, budget=300), 16),         # G = 2, d = 64, fp32
+    (dict(hq=16, hkv=2, budget=600, prompt=900), 64),               # G = 8
+    (dict(hq=2, hkv=2, budget=200), 48),                            # G = 1
+    (dict(dtype="f32", d=128, hq=8, hkv=1, budget=1100, prompt=1500), 96),
+], ids=["b64_1chunk", "b32_2spans", "b1", "b127", "f32_d64_g2", "g8", "g1", "f32_g8_3spans"])
+def test_hikv_stage2_element_level(kw, b2, fused):
+    rep = _run(SMALL.with_(**kw), element_budget=b2, fused=fused)
+    assert rep.evictions_checked > 0
+    print("stage2 rows skipped as near-ties:", rep.stage2_near_tie_rows, "of", rep.outputs_checked)
+
+
+def test_hikv_stage2_with_recent_bank():
+    rep = _run(SMALL.with_(sink=0, window=48, budget=96), element_budget=48, importance_mode=1, fused=True)
+    assert rep.evictions_checked > 0
+
+
+def test_hikv_stage2_llama3_8b_layer():
+    # r_II = 2 on the Llama-3-8B layer: 1025 tokens = 9 chunks of 128 per head
+    ls = _ls(W.WORKLOADS[1], element_budget=64)
+    ls.prefill()
+    rep = ls.decode(steps=24, fused=True)
+    ls.cache.close()
+    assert rep.evictions_checked == 64 * (1 + 24)
+    print("stage2 8B layer: rows skipped", rep.stage2_near_tie_rows, "max bf16 err", rep.max_out_err)
+
+
+def test_hikv_stage2_rejects_units_above_its_limit():
+    import importance_aware_kv_gb300 as hk
+    w = SMALL.with_(layers=1, batch=1, hkv=1, hq=4, prompt=16500, budget=17000, steps=1)
+    cache = hk.Cache(hk.CacheConfig(w.layers, w.batch, w.hq, w.hkv, w.d, w.dtype, w.sink, w.window,
+                                    [w.budget], w.total_positions, element_budget=64))
+    k, v = W.gen_kv(w, 0, 1, 0, w.prompt, 1)
+    cache.append(W.to_torch(k).cuda(), W.to_torch(v).cuda())
+    q = torch.zeros((1, 1, w.hq, w.d), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(q)
+    with pytest.raises(hk.HikvError) as ei:
+        cache.decode_step(q, out)
+    assert ei.value.status == hk.HIKV_ERR_CAPACITY
+    cache.close()
+
+
 @FUSED
 def test_pyramidkv_layer_budgets(fused):
     import importance_aware_kv_gb300 as hk
