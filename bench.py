@@ -182,7 +182,7 @@ def schedule_budgets(w, seed, schedule):
     raise ValueError(f"unknown schedule {schedule!r}")
 
 
-def run_cpu_oracle(w, seed, steps, warmup, budget_s=20.0, layers=None, budgets=None):
+def run_cpu_oracle(w, seed, steps, warmup, budget_s=20.0, layers=None, budgets=None, element_budget=0):
     """Time the oracle's decode loop (append -> decode -> evict when due) on the
     given layers (default all) and scale to whole-workload steps/s: a step of
     the workload needs every layer, so sampled rate x (sampled / all layers).
@@ -195,6 +195,7 @@ def run_cpu_oracle(w, seed, steps, warmup, budget_s=20.0, layers=None, budgets=N
     bs = np.concatenate([b_all[l * w.hkv:(l + 1) * w.hkv] for l in layers])
     O = oracle.Oracle(len(layers), w.batch, w.hq, w.hkv, w.d, w.sink, w.window, bs,
                       out_bf16=(w.dtype == "bf16"), threads=threads)
+    O.set_element_budget(element_budget)
     for si, l in enumerate(layers):
         k, v = W.gen_kv(w, l, 1, 0, w.prompt, seed)
         O.append(si, W.to_f32(k), W.to_f32(v))
@@ -275,8 +276,9 @@ def bench_gpu(args):
     if args.full_cache:   # no eviction: every unit keeps its whole context
         budgets = np.full_like(budgets, w.prompt + Wu + K + args.three_call_steps + max(args.per_layer_steps, 100)
                                + Ke + 1)
+    elem = args.element_budget if 0 < args.element_budget < w.d else 0
     cache = hk.Cache(hk.CacheConfig(w.layers, w.batch, w.hq, w.hkv, w.d, w.dtype, w.sink, w.window,
-                                    budgets, w.prompt + total_steps + 1))
+                                    budgets, w.prompt + total_steps + 1, element_budget=elem))
     stage("cache created")
     # ---- setup (untimed): prompt in layer chunks, window scoring, cut to budget ----
     stream = torch.cuda.current_stream()
@@ -345,6 +347,7 @@ def bench_gpu(args):
         dist.barrier()
     torch.cuda.synchronize()
     launches0 = cache.kernel_launches()
+    vrows0 = cache.element_rows() if elem else 0
     alg_bytes = 0
     kv_bytes = 0
     for i in range(K):
@@ -358,6 +361,11 @@ def bench_gpu(args):
         e1.record(stream)
     torch.cuda.synchronize()
     launches = cache.kernel_launches() - launches0
+    vrows = cache.element_rows() - vrows0 if elem else 0
+    if elem:
+        # HiKV Stage II reads whole K rows but only the V rows some head kept
+        v_all = kv_bytes // 2
+        alg_bytes = alg_bytes - v_all + vrows * w.d * w.elem_bytes
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
@@ -453,7 +461,7 @@ def bench_gpu(args):
     try:
         with open(TRAFFIC_FILE) as f:
             tr = json.load(f)
-        if tr.get("kernel_sha") == kernel_sha() and tr.get("workload") == w.name:
+        if tr.get("kernel_sha") == kernel_sha() and tr.get("workload") == w.name and not elem:
             traffic = tr.get("dram_bytes_per_launch")
     except (OSError, ValueError):
         pass
@@ -467,6 +475,7 @@ def bench_gpu(args):
                    "budget": w.budget, "sink": w.sink, "window": w.window,
                    "evict_every": E, "tokens_attended_per_unit_max": int(lens.max()) + 1,
                    "budget_schedule": args.schedule or "workload",
+                   "element_budget": elem,
                    "tokens_attended_per_unit_mean": float(lens.mean()) + 1,
                    "decode_inputs": (f"{R} distinct steps" + (", cycled" if R < total_steps else "")),
                    "l2": "flushed between timed steps (256 MB write, outside the timed events)",
@@ -474,7 +483,8 @@ def bench_gpu(args):
         "hbm_gbs_step": alg_bytes * world / t_total / 1e9,
         "retained_kv_gbs": kv_bytes * world / t_total / 1e9,
         "hbm_fraction_nominal": achieved / 8000.0,
-        "roofline": {"kernel": "k_decode (append + attention + importance + victim + evict, one launch)",
+        "roofline": {"kernel": ("k_decode (append + attention + importance + victim + evict, one launch)" if not elem
+                                else "HiKV Stage II step (append, k_elem_order, k_elem_span with the merge in its last CTA per unit, evict)"),
                      "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{src} hbm_gbs", "traffic": traffic,
                      "bytes_per_launch": alg_bytes // K, "avg_launch_us": avg_s * 1e6,
@@ -483,13 +493,15 @@ def bench_gpu(args):
                  "d2h_bytes_per_step": int(d2h), "steps": Ke} if Ke > 0 else None),
         "gpu_launches": launches,
         "three_call_path": three,
+        "stage2_v_rows_read_fraction": (vrows / max(1, kv_bytes // (2 * w.d * w.elem_bytes))) if elem else None,
         "per_layer_launches": per_layer,
         "setup": setup,
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
         val, cores, done, sample = run_cpu_oracle(w, seed, min(64, w.steps), 2, budget_s=20.0,
-                                                  layers=oracle_sample_layers(w), budgets=budgets)
+                                                  layers=oracle_sample_layers(w), budgets=budgets,
+                                                  element_budget=elem)
         line["cpu_baseline"] = {"value": val, "unit": "steps/s", "cores": cores, "kind": "oracle",
                                 "sample": sample}
     if rank == 0:
@@ -516,6 +528,8 @@ def main():
     ap.add_argument("--spin-us", type=float, default=60.0)
     ap.add_argument("--impl", default="hikv", choices=["hikv", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--element-budget", type=int, default=0,
+                    help="HiKV Stage II element budget B2 (0: exact attention)")
     ap.add_argument("--verbose", action="store_true", help="stage markers on stderr")
     args = ap.parse_args()
     if args.warmup < 3:

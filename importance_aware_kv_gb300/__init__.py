@@ -30,7 +30,7 @@ ABI_FUNCTIONS = ("hikv_create_cache", "hikv_destroy_cache", "hikv_append", "hikv
                  "hikv_decode_step", "hikv_evict", "hikv_gather_retained", "hikv_get_lengths",
                  "hikv_device_status", "hikv_last_error", "hikv_score_window_noalloc",
                  "hikv_decode_step_fused", "hikv_kernel_launches", "hikv_budgets_pyramid",
-                 "hikv_budgets_duo", "hikv_selftest_timeout")
+                 "hikv_budgets_duo", "hikv_selftest_timeout", "hikv_element_rows")
 
 
 class HikvError(RuntimeError):
@@ -71,6 +71,7 @@ def _load():
         "hikv_score_window_noalloc": ([I32] * 8 + [ctypes.c_float, P, P, P, P], S),
         "hikv_decode_step_fused": ([P, I32, I32, P, P, P, P, I32, P], S),
         "hikv_kernel_launches": ([P], ctypes.c_int64),
+        "hikv_element_rows": ([P, ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
         "hikv_budgets_pyramid": ([I32, I32, I32, I32, I32, P], S),
         "hikv_budgets_duo": ([I32, I32, P, I32, I32, I32, P], S),
         "hikv_selftest_timeout": ([P, I32, P], S),
@@ -299,6 +300,12 @@ class Cache:
     def kernel_launches(self) -> int:
         """Kernels this cache has launched so far (host counter)."""
         return int(_lib.hikv_kernel_launches(self.h))
+
+    def element_rows(self) -> int:
+        """V rows the HiKV Stage II decode steps have read so far (synchronous)."""
+        r = ctypes.c_int64()
+        _check(_lib.hikv_element_rows(self.h, ctypes.byref(r)))
+        return int(r.value)
 
     def step(self, k, v, q, out, evict=True, layer0=0, stream=None):
         """append + decode_step (+ evict) as one call (one launch in steady state)."""

@@ -138,6 +138,9 @@ struct hikv_cache {
     int32_t* d_eorder = nullptr;        // [units][elem_stride]
     float* d_elg = nullptr;             // [units][G][elem_stride]
     float* d_epart = nullptr;           // [units][max spans][G][d + 2]
+    unsigned long long* d_erows = nullptr;   // V rows the element-level steps read
+    float* d_eqmask = nullptr;          // [units][G][d]
+    int32_t* d_edone = nullptr;         // [units]
 };
 
 namespace {
@@ -318,6 +321,9 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
         ALLOC(c->d_eorder, U * (size_t)c->elem_stride);
         ALLOC(c->d_elg, U * (size_t)G * c->elem_stride);
         ALLOC(c->d_epart, U * (size_t)spans * G * (c->d + 2));
+        ALLOC(c->d_erows, 1);
+        ALLOC(c->d_eqmask, U * (size_t)G * c->d);
+        ALLOC(c->d_edone, U);
     }
 #undef ALLOC
 
@@ -374,6 +380,8 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
               cudaMemset(v.mapped, 0, U * 4) == cudaSuccess &&
               cudaMemset(v.victim, 0xFF, U * 4) == cudaSuccess &&
               cudaMemset(v.err, 0, 32) == cudaSuccess &&
+              (!c->d_erows || cudaMemset(c->d_erows, 0, 8) == cudaSuccess) &&
+              (!c->d_edone || cudaMemset(c->d_edone, 0, U * 4) == cudaSuccess) &&
               cudaMemcpy(v.budget, c->budget_unit.data(), U * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
               cudaMemcpy(v.free_stack, stack.data(), stack.size() * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
               cudaMemcpy(v.free_top, &top, 4, cudaMemcpyHostToDevice) == cudaSuccess &&
@@ -774,8 +782,11 @@ static hikv_status launch_elem_call(hikv_cache* c, int32_t layer0, int32_t nl, c
     a.order = c->d_eorder;
     a.lg = c->d_elg;
     a.part = c->d_epart;
+    a.rows_loaded = c->d_erows;
+    a.qmask = c->d_eqmask;
+    a.done = c->d_edone;
     cudaError_t e = launch_elem_decode(a, c->dtype, c->d, max_n, (cudaStream_t)stream);
-    c->launches += 3;
+    c->launches += 2;
     if (e != cudaSuccess) return cuda_fail(e, "decode_step: element-level launch");
     return HIKV_OK;
 }
@@ -891,6 +902,18 @@ hikv_status hikv_gather_retained(hikv_cache* c, int32_t layer0, int32_t nl, int3
     cudaError_t e = launch_gather(a, (cudaStream_t)stream);
     c->launches += 1;
     if (e != cudaSuccess) return cuda_fail(e, "gather: launch");
+    return HIKV_OK;
+}
+
+hikv_status hikv_element_rows(const hikv_cache* c, int64_t* rows_host) {
+    g_err.clear();
+    if (!c || !rows_host) return fail(HIKV_ERR_INVALID_ARG, "element_rows: null cache or output");
+    *rows_host = 0;
+    if (!c->d_erows) return HIKV_OK;
+    unsigned long long r = 0;
+    cudaError_t e = cudaMemcpy(&r, c->d_erows, 8, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "element_rows: read");
+    *rows_host = (int64_t)r;
     return HIKV_OK;
 }
 

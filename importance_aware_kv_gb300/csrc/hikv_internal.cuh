@@ -534,6 +534,9 @@ struct ElemArgs {
     int32_t* order;        // [nunits][ostride] slots in position order
     float* lg;             // [nunits][G][ostride] logits by slot (log2 domain)
     float* part;           // [nunits][nsp][G][d + 2] span (m, l, o)
+    float* qmask;          // [nunits][G][d] q with the dropped dimensions zeroed
+    int32_t* done;         // [nunits] span CTAs finished (0 between calls)
+    unsigned long long* rows_loaded;   // += V rows read (may be null)
 };
 int elem_span_ranks();
 int elem_max_tokens();

@@ -14,20 +14,22 @@
 // increasing and every entry of a head shares m and l), so the kernels select
 // on the logits.
 //
-// Three kernels per call:
-//   k_elem_order  one CTA per unit: bitonic sort of (position, slot) keys in
-//                 shared memory -> the unit's slots in position order;
+// Two kernels per call:
+//   k_elem_order  one CTA per unit: the unit's slots in position order (a
+//                 bucket count of the positions, then ranks within buckets),
+//                 and each query head's q with all but its B2 largest-|q|
+//                 dimensions zeroed (a radix select on the |q| bits);
 //   k_elem_span   one CTA per (unit, span of kElemSpan ranks): masked-q
 //                 logits of the span's rows (8 lanes per row), per-span
 //                 softmax statistics, the top-B2 selection of each d-rank
 //                 chunk and head (a radix select on the logit bits in one
 //                 warp), then p.v over the rows that at least one head of
-//                 the group selected -- V rows no head selected are not read;
-//   k_elem_merge  one CTA per unit: merges the spans' (m, l, o), writes the
-//                 output, adds sum_h 2^(s - m_h) / l_h to every retained
-//                 token's importance (HiKV Stage I mode: the recent bank
-//                 only) and records the eviction victim, as the exact decode
-//                 kernel does.
+//                 the group selected -- V rows no head selected are not read.
+//                 The unit's last span CTA to finish then merges the spans'
+//                 (m, l, o), writes the output, adds sum_h 2^(s - m_h) / l_h to
+//                 every retained token's importance (HiKV Stage I mode: the
+//                 recent bank only) and records the eviction victim, as the
+//                 exact decode kernel does.
 //
 // The K side reads whole rows: the pool stores token-major rows, so B2 of the
 // d dimensions of a row lie in nearly every 32-byte sector (DRAM's unit), and
@@ -39,8 +41,9 @@ namespace {
 
 constexpr int kElemThreads = 256;
 constexpr int kElemWarps = kElemThreads / 32;
-constexpr int kElemSpan = 512;       // ranks per span CTA (a multiple of d)
+constexpr int kElemSpan = 128;       // ranks per span CTA (a multiple of d)
 constexpr int kElemMaxG = 8;
+constexpr int kElemMaxSpans = 16384 / kElemSpan;
 constexpr int kOrderThreads = 1024;
 
 __device__ __forceinline__ float to_f(float x) { return x; }
@@ -86,6 +89,32 @@ __device__ __forceinline__ void load_vec(const uint8_t* p, float (&x)[N]) {
     }
 }
 
+// raw 16-byte words of N elements of T (N * sizeof(T) a multiple of 16), and their widening
+template <typename T, int N>
+struct RawVec {
+    static constexpr int W = N * (int)sizeof(T) / 16;
+    uint4 w[W];
+    __device__ __forceinline__ void load(const uint8_t* p) {
+#pragma unroll
+        for (int i = 0; i < W; ++i) w[i] = __ldg(reinterpret_cast<const uint4*>(p) + i);
+    }
+    __device__ __forceinline__ void widen(float (&x)[N]) const {
+#pragma unroll
+        for (int i = 0; i < W; ++i) {
+            const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                if constexpr (sizeof(T) == 2) {
+                    x[i * 8 + 2 * k] = __uint_as_float(ws[k] << 16);
+                    x[i * 8 + 2 * k + 1] = __uint_as_float(ws[k] & 0xFFFF0000u);
+                } else {
+                    x[i * 4 + k] = __uint_as_float(ws[k]);
+                }
+            }
+        }
+    }
+};
+
 __device__ __forceinline__ void store_out(float* p, float x) { *p = x; }
 __device__ __forceinline__ void store_out(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
 
@@ -96,35 +125,219 @@ __device__ __forceinline__ uint32_t ord_key(float x) {
 }
 
 // ---------------------------------------------------------------------------
-// k_elem_order: slots of each unit in position order (positions are unique)
+// k_elem_order: slots of each unit in position order (positions are unique).
+// Positions are binned into kOrderBuckets buckets of 2^shift consecutive
+// positions; a slot's rank is the count of earlier buckets plus the members of
+// its own bucket at a lower position (a bucket holds at most 2^shift tokens).
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kOrderThreads) k_elem_order(const ElemArgs a, int npow2) {
-    extern __shared__ unsigned long long okeys[];
+constexpr int kOrderBuckets = 4096;
+
+__host__ __device__ inline size_t order_smem(int max_n) { return (size_t)(2 * kOrderBuckets + 2 * max_n + 32) * 4; }
+
+__global__ void __launch_bounds__(kOrderThreads) k_elem_order(const ElemArgs a) {
+    extern __shared__ int32_t osm[];
+    int32_t* cur = osm;                        // [kOrderBuckets] counts, then cursors
+    int32_t* start = cur + kOrderBuckets;      // [kOrderBuckets] exclusive prefix
+    int32_t* wsum = start + kOrderBuckets;     // [32]
+    int32_t* ps = wsum + 32;                   // [n] positions
+    int32_t* mem = ps + a.ostride;             // [n] slots grouped by bucket
     const View& v = a.v;
     const int32_t uu = blockIdx.x, u = a.u0 + uu;
     const int32_t n = v.len[u];
-    const int tid = threadIdx.x;
-    for (int i = tid; i < npow2; i += kOrderThreads)
-        okeys[i] = i < n ? ((unsigned long long)(uint32_t)v.pos[(int64_t)u * v.cap + i] << 32) | (uint32_t)i
-                         : ~0ull;
+    const int32_t t = v.next_pos[u] - 1;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int shift = 0;
+    while ((((int64_t)t + 1 + (1ll << shift) - 1) >> shift) > kOrderBuckets) ++shift;
+    for (int b = tid; b < kOrderBuckets; b += kOrderThreads) cur[b] = 0;
     __syncthreads();
-    for (int k = 2; k <= npow2; k <<= 1)
-        for (int j = k >> 1; j > 0; j >>= 1) {
-            for (int i = tid; i < npow2; i += kOrderThreads) {
-                const int ij = i ^ j;
-                if (ij > i) {
-                    const unsigned long long x = okeys[i], y = okeys[ij];
-                    const bool up = (i & k) == 0;
-                    if ((x > y) == up) {
-                        okeys[i] = y;
-                        okeys[ij] = x;
-                    }
+    for (int j = tid; j < n; j += kOrderThreads) {
+        int32_t p = v.pos[(int64_t)u * v.cap + j];
+        if (p < 0 || p > t) {
+            atomicOr(v.err, DEVERR_STATE);
+            p = p < 0 ? 0 : t;
+        }
+        ps[j] = p;
+        atomicAdd(&cur[p >> shift], 1);
+    }
+    __syncthreads();
+    // exclusive scan of the counts: 4 consecutive buckets per thread
+    constexpr int PER = kOrderBuckets / kOrderThreads;
+    int32_t c[PER], run = 0;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        c[k] = cur[tid * PER + k];
+        run += c[k];
+    }
+    int32_t incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int32_t base = incl - run;
+    for (int w = 0; w < warp; ++w) base += wsum[w];
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        start[tid * PER + k] = base;
+        cur[tid * PER + k] = base;
+        base += c[k];
+    }
+    __syncthreads();
+    for (int j = tid; j < n; j += kOrderThreads) mem[atomicAdd(&cur[ps[j] >> shift], 1)] = j;
+    __syncthreads();
+    int32_t* ord = a.order + (int64_t)uu * a.ostride;
+    for (int j = tid; j < n; j += kOrderThreads) {
+        const int32_t p = ps[j], b = p >> shift;
+        const int32_t e = b + 1 < kOrderBuckets ? start[b + 1] : n;
+        int32_t r = start[b];
+        for (int k = start[b]; k < e; ++k) r += ps[mem[k]] < p;
+        ord[r] = j;
+    }
+    // K side of the unit's query heads: warp h keeps the b2 dimensions of q_h
+    // with the largest |q| (ties: the lower index) and zeroes the rest
+    if (warp < v.group) {
+        const int h = warp, D = v.d, PERL = D / 32;   // PERL <= 4
+        const int per_layer = v.batch * v.hkv;
+        const int li = u / per_layer - a.layer0, b = (u / v.hkv) % v.batch, gh = u % v.hkv;
+        const int64_t qoff = (((int64_t)li * v.batch + b) * v.hq + (int64_t)gh * v.group + h) * D;
+        float x[4];
+        uint32_t key[4];
+        for (int k = 0; k < 4; ++k) {
+            const int c = k * 32 + lane;
+            x[k] = 0.f;
+            if (k < PERL)
+                x[k] = v.row_bytes == D * 2 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.q)[qoff + c])
+                                            : reinterpret_cast<const float*>(a.q)[qoff + c];
+            key[k] = __float_as_uint(fabsf(x[k]));   // |q| >= 0: its bits order like its value
+        }
+        uint32_t thr = 0u;
+        for (int bit = 31; bit >= 0; --bit) {
+            const uint32_t cand = thr | (1u << bit);
+            int cntb = 0;
+            for (int k = 0; k < PERL; ++k) cntb += __popc(__ballot_sync(0xffffffffu, key[k] >= cand));
+            if (cntb >= a.b2) thr = cand;
+        }
+        int above = 0;
+        for (int k = 0; k < PERL; ++k) above += __popc(__ballot_sync(0xffffffffu, key[k] > thr));
+        const int need = a.b2 - above;
+        int before = 0;
+        float* qm = a.qmask + ((int64_t)uu * v.group + h) * D;
+        for (int k = 0; k < PERL; ++k) {
+            const unsigned eq = __ballot_sync(0xffffffffu, key[k] == thr);
+            const int mine = before + __popc(eq & ((1u << lane) - 1u));
+            const bool keep = key[k] > thr || (key[k] == thr && mine < need);
+            qm[k * 32 + lane] = keep ? x[k] : 0.f;
+            before += __popc(eq);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// merge of a unit's spans (run by its last span CTA): output, importance from
+// the whole P, and the victim -- the smallest (imp, -pos) outside sinks and window
+// ---------------------------------------------------------------------------
+template <typename T, int D, int G>
+__device__ void merge_unit(const ElemArgs& a, int32_t uu, int32_t u, int32_t n, float* scratch,
+                           unsigned long long* wkey, int32_t* wslot) {
+    const View& v = a.v;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nsp = (n + kElemSpan - 1) / kElemSpan;
+    float* mfin = scratch;                 // [G]
+    float* linv = scratch + kElemMaxG;     // [G]
+    float* wsp = scratch + 2 * kElemMaxG;  // [G][nsp]
+    const float* part = a.part + (int64_t)uu * a.nsp * G * (D + 2);
+    if (tid < G) {
+        const int h = tid;
+        float m = -INFINITY;
+        for (int s = 0; s < nsp; ++s) m = fmaxf(m, __ldcg(part + ((int64_t)s * G + h) * (D + 2)));
+        float l = 0.f;
+        for (int s = 0; s < nsp; ++s) {
+            const float ls = __ldcg(part + ((int64_t)s * G + h) * (D + 2) + 1);
+            const float w = ls > 0.f ? exp2f(__ldcg(part + ((int64_t)s * G + h) * (D + 2)) - m) : 0.f;
+            wsp[h * nsp + s] = w;
+            l += ls * w;
+        }
+        mfin[h] = m;
+        linv[h] = 1.0f / l;
+    }
+    __syncthreads();
+    const int per_layer = v.batch * v.hkv;
+    const int li = u / per_layer - a.layer0, b = (u / v.hkv) % v.batch, gh = u % v.hkv;
+    T* outg = reinterpret_cast<T*>(a.out) + (((int64_t)li * v.batch + b) * v.hq + (int64_t)gh * G) * D;
+    for (int e = tid; e < G * D; e += kElemThreads) {
+        const int h = e / D, c = e - h * D;
+        float o = 0.f;
+        for (int s = 0; s < nsp; ++s) o = fmaf(__ldcg(part + ((int64_t)s * G + h) * (D + 2) + 2 + c), wsp[h * nsp + s], o);
+        store_out(outg + e, o * linv[h]);
+    }
+    const int32_t tnew = v.next_pos[u] - 1;
+    const bool need_victim = n > v.budget[u];
+    const int32_t lo = v.sink, hi = tnew - v.window;
+    const float* lgu = a.lg + (int64_t)uu * G * a.ostride;
+    unsigned long long kmin = ~0ull;
+    int32_t smin = -1;
+    constexpr int MB = G >= 8 ? 1 : 8 / G;   // slots per thread whose loads are issued together
+    for (int j0 = tid; j0 < n; j0 += kElemThreads * MB) {
+        float lgv[MB][G], iv[MB];
+        int32_t pv[MB];
+#pragma unroll
+        for (int q = 0; q < MB; ++q) {
+            const int j = j0 + q * kElemThreads;
+            if (j >= n) continue;
+            const int64_t mi = (int64_t)u * v.cap + j;
+#pragma unroll
+            for (int h = 0; h < G; ++h) lgv[q][h] = __ldcg(lgu + (int64_t)h * a.ostride + j);
+            iv[q] = v.imp[mi];
+            pv[q] = v.pos[mi];
+        }
+#pragma unroll
+        for (int q = 0; q < MB; ++q) {
+            const int j = j0 + q * kElemThreads;
+            if (j >= n) continue;
+            float inc = 0.f;
+#pragma unroll
+            for (int h = 0; h < G; ++h) inc += exp2f(lgv[q][h] - mfin[h]) * linv[h];
+            const int32_t p = pv[q];
+            const bool grows = !v.recent_only || p >= tnew - v.window;
+            const float nw = grows ? iv[q] + inc : iv[q];
+            v.imp[(int64_t)u * v.cap + j] = nw;
+            if (need_victim && p >= lo && p <= hi) {
+                const unsigned long long key =
+                    ((unsigned long long)__float_as_uint(nw) << 32) | (unsigned long long)(~(uint32_t)p);
+                if (key < kmin) {
+                    kmin = key;
+                    smin = j;
                 }
             }
-            __syncthreads();
         }
-    int32_t* ord = a.order + (int64_t)uu * a.ostride;
-    for (int i = tid; i < n; i += kOrderThreads) ord[i] = (int32_t)(uint32_t)okeys[i];
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const unsigned long long ok = __shfl_xor_sync(0xffffffffu, kmin, o);
+        const int32_t os = __shfl_xor_sync(0xffffffffu, smin, o);
+        if (ok < kmin) {
+            kmin = ok;
+            smin = os;
+        }
+    }
+    __syncthreads();   // the warp counts sharing this scratch are no longer read
+    if (lane == 0) {
+        wkey[warp] = kmin;
+        wslot[warp] = smin;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        unsigned long long kk = ~0ull;
+        int32_t sl = -1;
+        for (int w = 0; w < kElemWarps; ++w)
+            if (wkey[w] < kk) {
+                kk = wkey[w];
+                sl = wslot[w];
+            }
+        v.victim[u] = need_victim ? sl : -1;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -132,33 +345,30 @@ __global__ void __launch_bounds__(kOrderThreads) k_elem_order(const ElemArgs a, 
 // ---------------------------------------------------------------------------
 template <int D>
 struct SpanLayout {
-    size_t sl, qr, qm, S, sel, ul, ml, op, cnt, total;
+    size_t sl, qm, S, sel, ul, ml, op, cnt, total;
     __host__ __device__ SpanLayout(int G) {
         size_t o = 0;
         auto take = [&](size_t bytes) { size_t r = o; o += (bytes + 15) / 16 * 16; return r; };
         sl = take(kElemSpan * 4);                        // slot of each rank
-        qr = take((size_t)G * D * 4);                    // q as float
         qm = take((size_t)G * D * 4);                    // q with the dropped dimensions zeroed
         S = take((size_t)G * kElemSpan * 4);             // logits, then p of the kept entries
         sel = take((size_t)G * kElemSpan);               // kept by head h
         ul = take(kElemSpan * 4);                        // ranks some head kept
         ml = take((size_t)2 * kElemMaxG * 4);            // span (m, l) per head
-        op = take((size_t)kElemWarps * G * D * 4);       // per-warp output sums
-        cnt = take(kElemWarps * 4 + 16);
+        op = take((size_t)kElemWarps * G * D * 4);       // per-warp output sums; merge weights
+        cnt = take(kElemWarps * 16 + 16);                // warp counts / victim keys, last-CTA flag
         total = o;
     }
 };
 
-template <typename T, int D>
-__global__ void __launch_bounds__(kElemThreads) k_elem_span(const ElemArgs a) {
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(kElemThreads, (G >= 8 || sizeof(T) == 4) ? 3 : 4) k_elem_span(const ElemArgs a) {
     constexpr int DK = D / 8;    // dimensions per lane in the q.k pass (8 lanes per row)
     constexpr int DV = D / 32;   // dimensions per lane in the p.v pass (a warp per row)
     extern __shared__ __align__(16) uint8_t esm[];
     const View& v = a.v;
-    const int G = v.group;
     const SpanLayout<D> L(G);
     int32_t* sl = reinterpret_cast<int32_t*>(esm + L.sl);
-    float* qr = reinterpret_cast<float*>(esm + L.qr);
     float* qm = reinterpret_cast<float*>(esm + L.qm);
     float* S = reinterpret_cast<float*>(esm + L.S);
     uint8_t* sel = esm + L.sel;
@@ -173,27 +383,16 @@ __global__ void __launch_bounds__(kElemThreads) k_elem_span(const ElemArgs a) {
     const int32_t r0 = sp * kElemSpan;
     if (r0 >= n) return;
     const int32_t cnt = min(n - r0, kElemSpan);
-    const int per_layer = v.batch * v.hkv;
-    const int li = u / per_layer - a.layer0, b = (u / v.hkv) % v.batch, gh = u % v.hkv;
-    const int64_t qoff = (((int64_t)li * v.batch + b) * v.hq + (int64_t)gh * G) * D;
 
     const int32_t* ord = a.order + (int64_t)uu * a.ostride;
     for (int i = tid; i < cnt; i += kElemThreads) sl[i] = ord[r0 + i];
-    const T* qg = reinterpret_cast<const T*>(a.q) + qoff;
-    for (int e = tid; e < G * D; e += kElemThreads) qr[e] = to_f(qg[e]);
-    __syncthreads();
-    // K side: keep dimension c of head h iff fewer than B2 dimensions beat it
-    // (larger |q|, or equal |q| at a lower index)
+    // q staged interleaved by lane: the 4-float piece c4 of lane sub's DK
+    // dimensions (sub * DK + 4 c4 ...) sits at (c4 * 8 + sub) * 4, so the 8
+    // lanes of a row read 8 consecutive float4 (no bank conflicts)
+    const float* qmg = a.qmask + (int64_t)uu * G * D;
     for (int e = tid; e < G * D; e += kElemThreads) {
-        const int h = e / D, c = e - h * D;
-        const float x = fabsf(qr[e]);
-        const float* row = qr + h * D;
-        int beat = 0;
-        for (int c2 = 0; c2 < D; ++c2) {
-            const float y = fabsf(row[c2]);
-            beat += (y > x) || (y == x && c2 < c);
-        }
-        qm[e] = beat < a.b2 ? qr[e] : 0.f;
+        const int h = e / D, c = e - h * D, sub = c / DK, rem = c - sub * DK;
+        qm[h * D + ((rem >> 2) * 8 + sub) * 4 + (rem & 3)] = qmg[e];
     }
     __syncthreads();
 
@@ -201,33 +400,38 @@ __global__ void __launch_bounds__(kElemThreads) k_elem_span(const ElemArgs a) {
     {
         const int grp = lane >> 3, sub = lane & 7;
         float* lgu = a.lg + (int64_t)uu * G * a.ostride;
-        for (int i0 = warp * 4; i0 < cnt; i0 += kElemWarps * 4 * 2) {
-            float kx[2][DK];
-            bool ok[2];
-            int32_t slot[2];
+        // rows in flight per 8-lane group: about 32 registers of raw K words
+        constexpr int RAW = DK * (int)sizeof(T) / 4;
+        constexpr int UK = RAW <= 8 ? 4 : 2;
+        for (int i0 = warp * 4; i0 < cnt; i0 += kElemWarps * 4 * UK) {
+            RawVec<T, DK> kr[UK];
+            bool ok[UK];
+            int32_t slot[UK];
 #pragma unroll
-            for (int w = 0; w < 2; ++w) {
+            for (int w = 0; w < UK; ++w) {
                 const int i = i0 + w * kElemWarps * 4 + grp;
                 ok[w] = i < cnt;
                 slot[w] = ok[w] ? sl[i] : 0;
                 const uint8_t* rp = ok[w] ? row_ptr(v, u, slot[w], false) : nullptr;
                 ok[w] = ok[w] && rp;
-                if (ok[w]) load_vec<T, DK>(rp + sub * DK * (int)sizeof(T), kx[w]);
+                if (ok[w]) kr[w].load(rp + sub * DK * (int)sizeof(T));
             }
 #pragma unroll
-            for (int w = 0; w < 2; ++w) {
+            for (int w = 0; w < UK; ++w) {
                 const int i = i0 + w * kElemWarps * 4 + grp;
+                float kx[1][DK];
+                kr[w].widen(kx[0]);
                 for (int h = 0; h < G; ++h) {
-                    const float4* qv = reinterpret_cast<const float4*>(qm + h * D + sub * DK);
+                    const float4* qv = reinterpret_cast<const float4*>(qm + h * D) + sub;
                     float acc = 0.f;
 #pragma unroll
                     for (int c4 = 0; c4 < DK / 4; ++c4) {
-                        const float4 qq = qv[c4];
+                        const float4 qq = qv[c4 * 8];
                         if (ok[w]) {
-                            acc = fmaf(qq.x, kx[w][4 * c4], acc);
-                            acc = fmaf(qq.y, kx[w][4 * c4 + 1], acc);
-                            acc = fmaf(qq.z, kx[w][4 * c4 + 2], acc);
-                            acc = fmaf(qq.w, kx[w][4 * c4 + 3], acc);
+                            acc = fmaf(qq.x, kx[0][4 * c4], acc);
+                            acc = fmaf(qq.y, kx[0][4 * c4 + 1], acc);
+                            acc = fmaf(qq.z, kx[0][4 * c4 + 2], acc);
+                            acc = fmaf(qq.w, kx[0][4 * c4 + 3], acc);
                         }
                     }
                     acc += __shfl_xor_sync(0xffffffffu, acc, 1);
@@ -310,11 +514,12 @@ __global__ void __launch_bounds__(kElemThreads) k_elem_span(const ElemArgs a) {
     // p of the kept entries (span-local reference), and the union of the heads' rows
     int keep_n = 0;
     {
-        const int i = tid;   // kElemThreads >= kElemSpan / 2: two ranks per thread
-        int mine[2] = {0, 0};
+        constexpr int RPT = (kElemSpan + kElemThreads - 1) / kElemThreads;   // ranks per thread
+        int mine[RPT];
 #pragma unroll
-        for (int w = 0; w < 2; ++w) {
-            const int r = i + w * kElemThreads;
+        for (int w = 0; w < RPT; ++w) {
+            mine[w] = 0;
+            const int r = tid + w * kElemThreads;
             if (r >= cnt) continue;
             int any = 0;
             for (int h = 0; h < G; ++h) {
@@ -327,7 +532,7 @@ __global__ void __launch_bounds__(kElemThreads) k_elem_span(const ElemArgs a) {
         }
         // ordered compaction of the kept ranks (rank order; deterministic sums)
 #pragma unroll
-        for (int w = 0; w < 2; ++w) {
+        for (int w = 0; w < RPT; ++w) {
             const unsigned m = __ballot_sync(0xffffffffu, mine[w]);
             if (lane == 0) wcnt[warp] = __popc(m);
             __syncthreads();
@@ -339,13 +544,15 @@ __global__ void __launch_bounds__(kElemThreads) k_elem_span(const ElemArgs a) {
         }
     }
 
+    if (tid == 0 && a.rows_loaded) atomicAdd(a.rows_loaded, (unsigned long long)keep_n);
+
     // p.v over the kept rows: a warp per row, DV dimensions per lane
-    float acc[kElemMaxG][DV];
+    float acc[G][DV];
 #pragma unroll
-    for (int h = 0; h < kElemMaxG; ++h)
+    for (int h = 0; h < G; ++h)
 #pragma unroll
         for (int c = 0; c < DV; ++c) acc[h][c] = 0.f;
-    constexpr int UNR = 4;
+    constexpr int UNR = G >= 4 ? 4 : 8;   // rows in flight per warp
     for (int j0 = warp; j0 < keep_n; j0 += kElemWarps * UNR) {
         float vx[UNR][DV];
         int rr[UNR];
@@ -363,8 +570,7 @@ __global__ void __launch_bounds__(kElemThreads) k_elem_span(const ElemArgs a) {
         for (int w = 0; w < UNR; ++w) {
             if (!ok[w]) continue;
 #pragma unroll
-            for (int h = 0; h < kElemMaxG; ++h) {
-                if (h >= G) break;
+            for (int h = 0; h < G; ++h) {
                 const float p = S[h * kElemSpan + rr[w]];
 #pragma unroll
                 for (int c = 0; c < DV; ++c) acc[h][c] = fmaf(p, vx[w][c], acc[h][c]);
@@ -372,8 +578,7 @@ __global__ void __launch_bounds__(kElemThreads) k_elem_span(const ElemArgs a) {
         }
     }
 #pragma unroll
-    for (int h = 0; h < kElemMaxG; ++h) {
-        if (h >= G) break;
+    for (int h = 0; h < G; ++h) {
 #pragma unroll
         for (int c = 0; c < DV; ++c) op[((size_t)warp * G + h) * D + lane * DV + c] = acc[h][c];
     }
@@ -389,104 +594,26 @@ __global__ void __launch_bounds__(kElemThreads) k_elem_span(const ElemArgs a) {
         part[tid * (D + 2)] = ml[2 * tid];
         part[tid * (D + 2) + 1] = ml[2 * tid + 1];
     }
-}
-
-// ---------------------------------------------------------------------------
-// k_elem_merge
-// ---------------------------------------------------------------------------
-template <typename T, int D>
-__global__ void __launch_bounds__(kElemThreads) k_elem_merge(const ElemArgs a) {
-    __shared__ float mfin[kElemMaxG], linv[kElemMaxG];
-    __shared__ float wsp[kElemMaxG * 64];   // per (head, span) merge weight
-    __shared__ unsigned long long wkey[kElemWarps];
-    __shared__ int32_t wslot[kElemWarps];
-    const View& v = a.v;
-    const int G = v.group;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int32_t uu = blockIdx.x, u = a.u0 + uu;
-    const int32_t n = v.len[u];
-    const int nsp = (n + kElemSpan - 1) / kElemSpan;
-    const float* part = a.part + (int64_t)uu * a.nsp * G * (D + 2);
-    if (tid < G) {
-        const int h = tid;
-        float m = -INFINITY;
-        for (int s = 0; s < nsp; ++s) m = fmaxf(m, part[((int64_t)s * G + h) * (D + 2)]);
-        float l = 0.f;
-        for (int s = 0; s < nsp; ++s) {
-            const float ls = part[((int64_t)s * G + h) * (D + 2) + 1];
-            const float w = ls > 0.f ? exp2f(part[((int64_t)s * G + h) * (D + 2)] - m) : 0.f;
-            wsp[h * 64 + s] = w;
-            l += ls * w;
-        }
-        mfin[h] = m;
-        linv[h] = 1.0f / l;
-    }
-    __syncthreads();
-    const int per_layer = v.batch * v.hkv;
-    const int li = u / per_layer - a.layer0, b = (u / v.hkv) % v.batch, gh = u % v.hkv;
-    T* outg = reinterpret_cast<T*>(a.out) + (((int64_t)li * v.batch + b) * v.hq + (int64_t)gh * G) * D;
-    for (int e = tid; e < G * D; e += kElemThreads) {
-        const int h = e / D, c = e - h * D;
-        float o = 0.f;
-        for (int s = 0; s < nsp; ++s) o = fmaf(part[((int64_t)s * G + h) * (D + 2) + 2 + c], wsp[h * 64 + s], o);
-        store_out(outg + e, o * linv[h]);
-    }
-    // importance from the whole P, and the victim (smallest (imp, -pos) outside sinks and window)
-    const int32_t tnew = v.next_pos[u] - 1;
-    const bool need_victim = n > v.budget[u];
-    const int32_t lo = v.sink, hi = tnew - v.window;
-    const float* lgu = a.lg + (int64_t)uu * G * a.ostride;
-    unsigned long long kmin = ~0ull;
-    int32_t smin = -1;
-    for (int j = tid; j < n; j += kElemThreads) {
-        float inc = 0.f;
-        for (int h = 0; h < G; ++h) inc += exp2f(lgu[(int64_t)h * a.ostride + j] - mfin[h]) * linv[h];
-        const int64_t mi = (int64_t)u * v.cap + j;
-        const int32_t p = v.pos[mi];
-        const bool grows = !v.recent_only || p >= tnew - v.window;
-        const float nw = grows ? v.imp[mi] + inc : v.imp[mi];
-        v.imp[mi] = nw;
-        if (need_victim && p >= lo && p <= hi) {
-            const unsigned long long key =
-                ((unsigned long long)__float_as_uint(nw) << 32) | (unsigned long long)(~(uint32_t)p);
-            if (key < kmin) {
-                kmin = key;
-                smin = j;
-            }
-        }
-    }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-        const unsigned long long ok = __shfl_xor_sync(0xffffffffu, kmin, o);
-        const int32_t os = __shfl_xor_sync(0xffffffffu, smin, o);
-        if (ok < kmin) {
-            kmin = ok;
-            smin = os;
-        }
-    }
-    if (lane == 0) {
-        wkey[warp] = kmin;
-        wslot[warp] = smin;
-    }
+    // the unit's last span CTA to finish merges them (no waiting: the others
+    // have published their partials before counting themselves in)
+    int32_t* last = wcnt + kElemWarps * 4;
+    __threadfence();   // every thread's partial and logit stores, before the count
     __syncthreads();
     if (tid == 0) {
-        unsigned long long kk = ~0ull;
-        int32_t s = -1;
-        for (int w = 0; w < kElemWarps; ++w)
-            if (wkey[w] < kk) {
-                kk = wkey[w];
-                s = wslot[w];
-            }
-        v.victim[u] = need_victim ? s : -1;
+        const int32_t nsp_u = (n + kElemSpan - 1) / kElemSpan;
+        *last = atomicAdd(&a.done[uu], 1) == nsp_u - 1;
     }
+    __syncthreads();
+    if (!*last) return;
+    __threadfence();
+    if (tid == 0) a.done[uu] = 0;   // ready for the next call
+    merge_unit<T, D, G>(a, uu, u, n, op, reinterpret_cast<unsigned long long*>(wcnt), wcnt + kElemWarps * 2);
 }
 
-template <typename T, int D>
+template <typename T, int D, int G>
 cudaError_t launch_elem_t(const ElemArgs& a, int max_n, cudaStream_t s) {
-    int npow2 = 32;
-    while (npow2 < max_n) npow2 <<= 1;
-    const size_t osmem = (size_t)npow2 * 8;
-    const size_t ssmem = SpanLayout<D>(a.v.group).total;
+    const size_t osmem = order_smem(a.ostride);
+    const size_t ssmem = SpanLayout<D>(G).total;
     static size_t o_set = 0, s_set = 0;
     if (osmem > 48 * 1024 && osmem > o_set) {
         cudaError_t e = cudaFuncSetAttribute(k_elem_order, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)osmem);
@@ -494,18 +621,26 @@ cudaError_t launch_elem_t(const ElemArgs& a, int max_n, cudaStream_t s) {
         o_set = osmem;
     }
     if (ssmem > 48 * 1024 && ssmem > s_set) {
-        cudaError_t e = cudaFuncSetAttribute(k_elem_span<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssmem);
+        cudaError_t e = cudaFuncSetAttribute(k_elem_span<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssmem);
         if (e != cudaSuccess) return e;
         s_set = ssmem;
     }
-    k_elem_order<<<a.nunits, kOrderThreads, osmem, s>>>(a, npow2);
+    k_elem_order<<<a.nunits, kOrderThreads, osmem, s>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    k_elem_span<T, D><<<dim3(a.nsp, a.nunits), kElemThreads, ssmem, s>>>(a);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    k_elem_merge<T, D><<<a.nunits, kElemThreads, 0, s>>>(a);
+    k_elem_span<T, D, G><<<dim3(a.nsp, a.nunits), kElemThreads, ssmem, s>>>(a);
     return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t launch_elem_g(const ElemArgs& a, int max_n, cudaStream_t s) {
+    switch (a.v.group) {
+        case 1: return launch_elem_t<T, D, 1>(a, max_n, s);
+        case 2: return launch_elem_t<T, D, 2>(a, max_n, s);
+        case 4: return launch_elem_t<T, D, 4>(a, max_n, s);
+        case 8: return launch_elem_t<T, D, 8>(a, max_n, s);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace
@@ -514,11 +649,11 @@ int elem_span_ranks() { return kElemSpan; }
 int elem_max_tokens() { return 16384; }
 
 cudaError_t launch_elem_decode(const ElemArgs& a, int dtype, int d, int max_n, cudaStream_t s) {
-    if (a.v.group > kElemMaxG || a.nsp > 64) return cudaErrorInvalidValue;
-    if (dtype == 0 && d == 64) return launch_elem_t<float, 64>(a, max_n, s);
-    if (dtype == 0 && d == 128) return launch_elem_t<float, 128>(a, max_n, s);
-    if (dtype == 1 && d == 64) return launch_elem_t<__nv_bfloat16, 64>(a, max_n, s);
-    if (dtype == 1 && d == 128) return launch_elem_t<__nv_bfloat16, 128>(a, max_n, s);
+    if (a.v.group > kElemMaxG || a.nsp > kElemMaxSpans || a.ostride > elem_max_tokens()) return cudaErrorInvalidValue;
+    if (dtype == 0 && d == 64) return launch_elem_g<float, 64>(a, max_n, s);
+    if (dtype == 0 && d == 128) return launch_elem_g<float, 128>(a, max_n, s);
+    if (dtype == 1 && d == 64) return launch_elem_g<__nv_bfloat16, 64>(a, max_n, s);
+    if (dtype == 1 && d == 128) return launch_elem_g<__nv_bfloat16, 128>(a, max_n, s);
     return cudaErrorInvalidValue;
 }
 

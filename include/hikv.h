@@ -185,6 +185,14 @@ hikv_status hikv_gather_retained(hikv_cache* cache, int32_t layer0, int32_t nlay
                                  int32_t* lengths, int32_t* positions, float* importance,
                                  void* k_out, void* v_out, hikv_stream_t stream);
 
+/* Diagnostic: the number of V rows the element-level (HiKV Stage II) decode
+ * steps of this cache have read since it was created -- rows that at least
+ * one query head of the unit's group kept (HiKV sec. III-C: V is loaded only
+ * at the selected entries of P).  0 when element_budget is off.  Synchronous
+ * (a device-to-host copy after the work queued before it on the legacy
+ * stream).  Errors: INVALID_ARG, CUDA. */
+hikv_status hikv_element_rows(const hikv_cache* cache, int64_t* rows_host);
+
 /* HOST copy of the host mirror of each unit's length (no device access):
  * lengths_host: [nlayers * batch * Hkv].  Errors: INVALID_ARG. */
 hikv_status hikv_get_lengths(const hikv_cache* cache, int32_t layer0, int32_t nlayers,

@@ -202,8 +202,12 @@ def test_hikv_stage2_llama3_8b_layer():
     ls = _ls(W.WORKLOADS[1], element_budget=64)
     ls.prefill()
     rep = ls.decode(steps=24, fused=True)
+    rows = ls.cache.element_rows()
     ls.cache.close()
     assert rep.evictions_checked == 64 * (1 + 24)
+    # V rows read: at most every attended row (64 units x 1025 x 24 steps), and
+    # at least the B2 of each full chunk that one head keeps (8 x 64 + 1 per unit)
+    assert 64 * 24 * (8 * 64 + 1) <= rows <= 64 * 24 * 1025
     print("stage2 8B layer: rows skipped", rep.stage2_near_tie_rows, "max bf16 err", rep.max_out_err)
 
 
