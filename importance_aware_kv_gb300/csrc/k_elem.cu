@@ -46,9 +46,6 @@ constexpr int kElemMaxG = 8;
 constexpr int kElemMaxSpans = 16384 / kElemSpan;
 constexpr int kOrderThreads = 1024;
 
-__device__ __forceinline__ float to_f(float x) { return x; }
-__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
-
 // N consecutive elements of type T at p (16-byte aligned when N*sizeof(T) >= 16,
 // else N*sizeof(T)-aligned), widened to float.
 template <typename T, int N>
@@ -146,6 +143,19 @@ __global__ void __launch_bounds__(kOrderThreads) k_elem_order(const ElemArgs a) 
     const int32_t n = v.len[u];
     const int32_t t = v.next_pos[u] - 1;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // q of this warp's head (warps < G), loaded first so its latency overlaps the ranking
+    const int D = v.d, PERL = D / 32;   // PERL <= 4
+    float x[4] = {0.f, 0.f, 0.f, 0.f};
+    if (warp < v.group) {
+        const int per_layer = v.batch * v.hkv;
+        const int li = u / per_layer - a.layer0, b = (u / v.hkv) % v.batch, gh = u % v.hkv;
+        const int64_t qoff = (((int64_t)li * v.batch + b) * v.hq + (int64_t)gh * v.group + warp) * D;
+        for (int k = 0; k < PERL; ++k) {
+            const int c = k * 32 + lane;
+            x[k] = v.row_bytes == D * 2 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.q)[qoff + c])
+                                        : reinterpret_cast<const float*>(a.q)[qoff + c];
+        }
+    }
     int shift = 0;
     while ((((int64_t)t + 1 + (1ll << shift) - 1) >> shift) > kOrderBuckets) ++shift;
     for (int b = tid; b < kOrderBuckets; b += kOrderThreads) cur[b] = 0;
@@ -198,20 +208,10 @@ __global__ void __launch_bounds__(kOrderThreads) k_elem_order(const ElemArgs a) 
     // K side of the unit's query heads: warp h keeps the b2 dimensions of q_h
     // with the largest |q| (ties: the lower index) and zeroes the rest
     if (warp < v.group) {
-        const int h = warp, D = v.d, PERL = D / 32;   // PERL <= 4
-        const int per_layer = v.batch * v.hkv;
-        const int li = u / per_layer - a.layer0, b = (u / v.hkv) % v.batch, gh = u % v.hkv;
-        const int64_t qoff = (((int64_t)li * v.batch + b) * v.hq + (int64_t)gh * v.group + h) * D;
-        float x[4];
+        const int h = warp;
         uint32_t key[4];
-        for (int k = 0; k < 4; ++k) {
-            const int c = k * 32 + lane;
-            x[k] = 0.f;
-            if (k < PERL)
-                x[k] = v.row_bytes == D * 2 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.q)[qoff + c])
-                                            : reinterpret_cast<const float*>(a.q)[qoff + c];
-            key[k] = __float_as_uint(fabsf(x[k]));   // |q| >= 0: its bits order like its value
-        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) key[k] = __float_as_uint(fabsf(x[k]));   // |q| >= 0: bits order like values
         uint32_t thr = 0u;
         for (int bit = 31; bit >= 0; --bit) {
             const uint32_t cand = thr | (1u << bit);
@@ -246,16 +246,23 @@ __device__ void merge_unit(const ElemArgs& a, int32_t uu, int32_t u, int32_t n, 
     const int nsp = (n + kElemSpan - 1) / kElemSpan;
     float* mfin = scratch;                 // [G]
     float* linv = scratch + kElemMaxG;     // [G]
-    float* wsp = scratch + 2 * kElemMaxG;  // [G][nsp]
+    float* wsp = scratch + 2 * kElemMaxG;  // [G][nsp]: span m, then merge weight
+    float* lsp = wsp + G * nsp;            // [G][nsp]: span l
     const float* part = a.part + (int64_t)uu * a.nsp * G * (D + 2);
+    for (int e = tid; e < G * nsp; e += kElemThreads) {   // all spans' (m, l) in one round trip
+        const int s = e / G, h = e - s * G;
+        wsp[h * nsp + s] = __ldcg(part + (int64_t)e * (D + 2));
+        lsp[h * nsp + s] = __ldcg(part + (int64_t)e * (D + 2) + 1);
+    }
+    __syncthreads();
     if (tid < G) {
         const int h = tid;
         float m = -INFINITY;
-        for (int s = 0; s < nsp; ++s) m = fmaxf(m, __ldcg(part + ((int64_t)s * G + h) * (D + 2)));
+        for (int s = 0; s < nsp; ++s) m = fmaxf(m, wsp[h * nsp + s]);
         float l = 0.f;
         for (int s = 0; s < nsp; ++s) {
-            const float ls = __ldcg(part + ((int64_t)s * G + h) * (D + 2) + 1);
-            const float w = ls > 0.f ? exp2f(__ldcg(part + ((int64_t)s * G + h) * (D + 2)) - m) : 0.f;
+            const float ls = lsp[h * nsp + s];
+            const float w = ls > 0.f ? exp2f(wsp[h * nsp + s] - m) : 0.f;
             wsp[h * nsp + s] = w;
             l += ls * w;
         }
@@ -269,6 +276,7 @@ __device__ void merge_unit(const ElemArgs& a, int32_t uu, int32_t u, int32_t n, 
     for (int e = tid; e < G * D; e += kElemThreads) {
         const int h = e / D, c = e - h * D;
         float o = 0.f;
+#pragma unroll 8
         for (int s = 0; s < nsp; ++s) o = fmaf(__ldcg(part + ((int64_t)s * G + h) * (D + 2) + 2 + c), wsp[h * nsp + s], o);
         store_out(outg + e, o * linv[h]);
     }
