@@ -44,6 +44,7 @@ constexpr int kElemWarps = kElemThreads / 32;
 constexpr int kElemSpan = 128;       // ranks per span CTA (a multiple of d)
 constexpr int kElemMaxG = 8;
 constexpr int kElemMaxSpans = 16384 / kElemSpan;
+constexpr int kElemMaxPages = 16384 / 16;   // pages of a unit at the smallest page size
 constexpr int kOrderThreads = 1024;
 
 // N consecutive elements of type T at p (16-byte aligned when N*sizeof(T) >= 16,
@@ -249,6 +250,24 @@ __device__ void merge_unit(const ElemArgs& a, int32_t uu, int32_t u, int32_t n, 
     float* wsp = scratch + 2 * kElemMaxG;  // [G][nsp]: span m, then merge weight
     float* lsp = wsp + G * nsp;            // [G][nsp]: span l
     const float* part = a.part + (int64_t)uu * a.nsp * G * (D + 2);
+    // the importance pass's first loads go out first: they do not depend on the merge
+    const float* lgu = a.lg + (int64_t)uu * G * a.ostride;
+    constexpr int MB = G >= 8 ? 1 : 8 / G;   // slots per thread whose loads are issued together
+    float lgv[MB][G], iv[MB];
+    int32_t pv[MB];
+    auto load_batch = [&](int j0) {
+#pragma unroll
+        for (int q = 0; q < MB; ++q) {
+            const int j = j0 + q * kElemThreads;
+            if (j >= n) continue;
+            const int64_t mi = (int64_t)u * v.cap + j;
+#pragma unroll
+            for (int h = 0; h < G; ++h) lgv[q][h] = __ldcg(lgu + (int64_t)h * a.ostride + j);
+            iv[q] = v.imp[mi];
+            pv[q] = v.pos[mi];
+        }
+    };
+    load_batch(tid);
     for (int e = tid; e < G * nsp; e += kElemThreads) {   // all spans' (m, l) in one round trip
         const int s = e / G, h = e - s * G;
         wsp[h * nsp + s] = __ldcg(part + (int64_t)e * (D + 2));
@@ -283,23 +302,10 @@ __device__ void merge_unit(const ElemArgs& a, int32_t uu, int32_t u, int32_t n, 
     const int32_t tnew = v.next_pos[u] - 1;
     const bool need_victim = n > v.budget[u];
     const int32_t lo = v.sink, hi = tnew - v.window;
-    const float* lgu = a.lg + (int64_t)uu * G * a.ostride;
     unsigned long long kmin = ~0ull;
     int32_t smin = -1;
-    constexpr int MB = G >= 8 ? 1 : 8 / G;   // slots per thread whose loads are issued together
     for (int j0 = tid; j0 < n; j0 += kElemThreads * MB) {
-        float lgv[MB][G], iv[MB];
-        int32_t pv[MB];
-#pragma unroll
-        for (int q = 0; q < MB; ++q) {
-            const int j = j0 + q * kElemThreads;
-            if (j >= n) continue;
-            const int64_t mi = (int64_t)u * v.cap + j;
-#pragma unroll
-            for (int h = 0; h < G; ++h) lgv[q][h] = __ldcg(lgu + (int64_t)h * a.ostride + j);
-            iv[q] = v.imp[mi];
-            pv[q] = v.pos[mi];
-        }
+        if (j0 != tid) load_batch(j0);
 #pragma unroll
         for (int q = 0; q < MB; ++q) {
             const int j = j0 + q * kElemThreads;
@@ -353,11 +359,12 @@ __device__ void merge_unit(const ElemArgs& a, int32_t uu, int32_t u, int32_t n, 
 // ---------------------------------------------------------------------------
 template <int D>
 struct SpanLayout {
-    size_t sl, qm, S, sel, ul, ml, op, cnt, total;
+    size_t sl, pt, qm, S, sel, ul, ml, op, cnt, total;
     __host__ __device__ SpanLayout(int G) {
         size_t o = 0;
         auto take = [&](size_t bytes) { size_t r = o; o += (bytes + 15) / 16 * 16; return r; };
         sl = take(kElemSpan * 4);                        // slot of each rank
+        pt = take(kElemMaxPages * 4);                    // the unit's page table
         qm = take((size_t)G * D * 4);                    // q with the dropped dimensions zeroed
         S = take((size_t)G * kElemSpan * 4);             // logits, then p of the kept entries
         sel = take((size_t)G * kElemSpan);               // kept by head h
@@ -377,6 +384,7 @@ __global__ void __launch_bounds__(kElemThreads, (G >= 8 || sizeof(T) == 4) ? 3 :
     const View& v = a.v;
     const SpanLayout<D> L(G);
     int32_t* sl = reinterpret_cast<int32_t*>(esm + L.sl);
+    int32_t* pt = reinterpret_cast<int32_t*>(esm + L.pt);
     float* qm = reinterpret_cast<float*>(esm + L.qm);
     float* S = reinterpret_cast<float*>(esm + L.S);
     uint8_t* sel = esm + L.sel;
@@ -387,22 +395,56 @@ __global__ void __launch_bounds__(kElemThreads, (G >= 8 || sizeof(T) == 4) ? 3 :
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t uu = blockIdx.y, u = a.u0 + uu, sp = blockIdx.x;
-    const int32_t n = v.len[u];
+    // the length, this span's slots, the unit's page table and the masked q
+    // are independent loads: all are issued before the length is used
     const int32_t r0 = sp * kElemSpan;
+    const int32_t n = v.len[u];
+    static_assert(kElemSpan <= kElemThreads, "one rank per thread");
+    const int32_t* ord = a.order + (int64_t)uu * a.ostride;
+    const int32_t my_slot = (tid < kElemSpan && r0 + tid < a.ostride) ? ord[r0 + tid] : 0;
+    constexpr int PPT = kElemMaxPages / kElemThreads;
+    const int npg = min(v.max_pages, (a.ostride + v.page_tokens - 1) >> v.page_shift);
+    int32_t my_pg[PPT];
+#pragma unroll
+    for (int k = 0; k < PPT; ++k) {
+        const int i = tid + k * kElemThreads;
+        my_pg[k] = i < npg ? v.page_table[(int64_t)u * v.max_pages + i] : -1;
+    }
+    constexpr int QPT = (G * D + kElemThreads - 1) / kElemThreads;
+    const float* qmg = a.qmask + (int64_t)uu * G * D;
+    float my_q[QPT];
+#pragma unroll
+    for (int k = 0; k < QPT; ++k) {
+        const int e = tid + k * kElemThreads;
+        my_q[k] = e < G * D ? qmg[e] : 0.f;
+    }
     if (r0 >= n) return;
     const int32_t cnt = min(n - r0, kElemSpan);
-
-    const int32_t* ord = a.order + (int64_t)uu * a.ostride;
-    for (int i = tid; i < cnt; i += kElemThreads) sl[i] = ord[r0 + i];
+    if (tid < cnt) sl[tid] = my_slot;
+#pragma unroll
+    for (int k = 0; k < PPT; ++k)
+        if (tid + k * kElemThreads < npg) pt[tid + k * kElemThreads] = my_pg[k];
     // q staged interleaved by lane: the 4-float piece c4 of lane sub's DK
     // dimensions (sub * DK + 4 c4 ...) sits at (c4 * 8 + sub) * 4, so the 8
     // lanes of a row read 8 consecutive float4 (no bank conflicts)
-    const float* qmg = a.qmask + (int64_t)uu * G * D;
-    for (int e = tid; e < G * D; e += kElemThreads) {
+#pragma unroll
+    for (int k = 0; k < QPT; ++k) {
+        const int e = tid + k * kElemThreads;
+        if (e >= G * D) break;
         const int h = e / D, c = e - h * D, sub = c / DK, rem = c - sub * DK;
-        qm[h * D + ((rem >> 2) * 8 + sub) * 4 + (rem & 3)] = qmg[e];
+        qm[h * D + ((rem >> 2) * 8 + sub) * 4 + (rem & 3)] = my_q[k];
     }
     __syncthreads();
+    // row of a slot from the staged page table (slot < n <= ostride, so its page index is < npg)
+    auto rowp = [&](int32_t slot, bool is_v) -> const uint8_t* {
+        const int32_t pg = pt[slot >> v.page_shift];
+        if (pg < 0 || pg >= v.pool_pages) {
+            atomicOr(v.err, DEVERR_PAGE);
+            return nullptr;
+        }
+        return v.pool + (int64_t)pg * v.page_bytes +
+               ((is_v ? (int64_t)v.page_tokens : 0) + (slot & (v.page_tokens - 1))) * v.row_bytes;
+    };
 
     // logits of the span's rows: 8 lanes per row, DK dimensions each
     {
@@ -420,7 +462,7 @@ __global__ void __launch_bounds__(kElemThreads, (G >= 8 || sizeof(T) == 4) ? 3 :
                 const int i = i0 + w * kElemWarps * 4 + grp;
                 ok[w] = i < cnt;
                 slot[w] = ok[w] ? sl[i] : 0;
-                const uint8_t* rp = ok[w] ? row_ptr(v, u, slot[w], false) : nullptr;
+                const uint8_t* rp = ok[w] ? rowp(slot[w], false) : nullptr;
                 ok[w] = ok[w] && rp;
                 if (ok[w]) kr[w].load(rp + sub * DK * (int)sizeof(T));
             }
@@ -570,7 +612,7 @@ __global__ void __launch_bounds__(kElemThreads, (G >= 8 || sizeof(T) == 4) ? 3 :
             const int j = j0 + w * kElemWarps;
             ok[w] = j < keep_n;
             rr[w] = ok[w] ? ul[j] : 0;
-            const uint8_t* rp = ok[w] ? row_ptr(v, u, sl[rr[w]], true) : nullptr;
+            const uint8_t* rp = ok[w] ? rowp(sl[rr[w]], true) : nullptr;
             ok[w] = ok[w] && rp;
             if (ok[w]) load_vec<T, DV>(rp + lane * DV * (int)sizeof(T), vx[w]);
         }
