@@ -484,7 +484,7 @@ def bench_gpu(args):
         "retained_kv_gbs": kv_bytes * world / t_total / 1e9,
         "hbm_fraction_nominal": achieved / 8000.0,
         "roofline": {"kernel": ("k_decode (append + attention + importance + victim + evict, one launch)" if not elem
-                                else "HiKV Stage II step (append, k_elem_order, k_elem_span with the merge in its last CTA per unit, evict)"),
+                                else "HiKV Stage II step (k_elem_order with the append, k_elem_span with the merge and the eviction in its last CTA per unit)"),
                      "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{src} hbm_gbs", "traffic": traffic,
                      "bytes_per_launch": alg_bytes // K, "avg_launch_us": avg_s * 1e6,

@@ -757,16 +757,21 @@ hikv_status launch_decode_call(hikv_cache* c, int32_t layer0, int32_t nl, const 
 extern "C" {
 
 // HiKV Stage II decode of the layer range: sort, span and merge kernels.
+// fused = 1: the order kernel appends new_k / new_v first and, with evict, the
+// merge drops the victim (the host checked that the new slots' pages are
+// mapped and that no unit needs more than one eviction).
 static hikv_status launch_elem_call(hikv_cache* c, int32_t layer0, int32_t nl, const void* q, void* out,
-                                    hikv_stream_t stream) {
+                                    hikv_stream_t stream, int fused = 0, int evict = 0,
+                                    const void* new_k = nullptr, const void* new_v = nullptr) {
     const int u0 = layer0 * c->per_layer, nu = nl * c->per_layer;
     int max_n = 0;
     for (int u = u0; u < u0 + nu; ++u) {
-        if (c->len[u] <= 0) return fail(HIKV_ERR_STATE, "decode_step: unit %d is empty", u);
-        if (c->len[u] > c->elem_stride)
+        const int n = c->len[u] + (fused ? 1 : 0);
+        if (n <= 0) return fail(HIKV_ERR_STATE, "decode_step: unit %d is empty", u);
+        if (n > c->elem_stride)
             return fail(HIKV_ERR_CAPACITY, "decode_step: unit %d holds %d tokens, more than the %d of an element-level step",
-                        u, c->len[u], c->elem_stride);
-        max_n = std::max(max_n, c->len[u]);
+                        u, n, c->elem_stride);
+        max_n = std::max(max_n, n);
     }
     ElemArgs a{};
     a.v = c->v;
@@ -785,6 +790,10 @@ static hikv_status launch_elem_call(hikv_cache* c, int32_t layer0, int32_t nl, c
     a.rows_loaded = c->d_erows;
     a.qmask = c->d_eqmask;
     a.done = c->d_edone;
+    a.fused = fused;
+    a.evict = evict;
+    a.new_k = new_k;
+    a.new_v = new_v;
     cudaError_t e = launch_elem_decode(a, c->dtype, c->d, max_n, (cudaStream_t)stream);
     c->launches += 2;
     if (e != cudaSuccess) return cuda_fail(e, "decode_step: element-level launch");
@@ -816,7 +825,7 @@ hikv_status hikv_decode_step_fused(hikv_cache* c, int32_t layer0, int32_t nl, co
     if (((uintptr_t)k | (uintptr_t)v) & 15)
         return fail(HIKV_ERR_INVALID_ARG, "decode_step_fused: k and v must be 16-byte aligned");
     const int u0 = layer0 * c->per_layer, nu = nl * c->per_layer;
-    bool one_launch = c->elem == 0;   // the element-level step has kernels of its own
+    bool one_launch = true;
     for (int u = u0; u < u0 + nu && one_launch; ++u) {
         const int n = c->len[u] + 1;
         if (n > c->cap) return fail(HIKV_ERR_CAPACITY, "decode_step_fused: unit %d would exceed max_tokens", u);
@@ -831,7 +840,8 @@ hikv_status hikv_decode_step_fused(hikv_cache* c, int32_t layer0, int32_t nl, co
         if (st == HIKV_OK && evict) st = hikv_evict(c, layer0, nl, stream);
         return st;
     }
-    hikv_status st = launch_decode_call(c, layer0, nl, q, out, 1, evict ? 1 : 0, k, v, stream, "decode_step_fused");
+    hikv_status st = c->elem ? launch_elem_call(c, layer0, nl, q, out, stream, 1, evict ? 1 : 0, k, v)
+                             : launch_decode_call(c, layer0, nl, q, out, 1, evict ? 1 : 0, k, v, stream, "decode_step_fused");
     if (st != HIKV_OK) return st;
     for (int u = u0; u < u0 + nu; ++u) {
         const bool cut = evict && c->len[u] + 1 > c->budget_unit[u];

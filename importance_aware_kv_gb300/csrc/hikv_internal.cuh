@@ -536,6 +536,9 @@ struct ElemArgs {
     float* part;           // [nunits][nsp][G][d + 2] span (m, l, o)
     float* qmask;          // [nunits][G][d] q with the dropped dimensions zeroed
     int32_t* done;         // [nunits] span CTAs finished (0 between calls)
+    int32_t fused, evict;  // fused step: append new_k / new_v first; with evict, drop the victim at the end
+    const void* new_k;     // [nunits][d] (fused)
+    const void* new_v;
     unsigned long long* rows_loaded;   // += V rows read (may be null)
 };
 int elem_span_ranks();

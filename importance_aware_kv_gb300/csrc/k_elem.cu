@@ -122,6 +122,17 @@ __device__ __forceinline__ uint32_t ord_key(float x) {
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
+// address of slot s's K (or V) row in unit u, null (and the error bit) for an unmapped page
+__device__ __forceinline__ uint8_t* elem_row(const View& v, int32_t u, int32_t s, bool is_v) {
+    const int32_t pg = v.page_table[(int64_t)u * v.max_pages + (s >> v.page_shift)];
+    if (pg < 0 || pg >= v.pool_pages) {
+        atomicOr(v.err, DEVERR_PAGE);
+        return nullptr;
+    }
+    return v.pool + (int64_t)pg * v.page_bytes +
+           ((is_v ? (int64_t)v.page_tokens : 0) + (s & (v.page_tokens - 1))) * v.row_bytes;
+}
+
 // ---------------------------------------------------------------------------
 // k_elem_order: slots of each unit in position order (positions are unique).
 // Positions are binned into kOrderBuckets buckets of 2^shift consecutive
@@ -141,9 +152,29 @@ __global__ void __launch_bounds__(kOrderThreads) k_elem_order(const ElemArgs a) 
     int32_t* mem = ps + a.ostride;             // [n] slots grouped by bucket
     const View& v = a.v;
     const int32_t uu = blockIdx.x, u = a.u0 + uu;
-    const int32_t n = v.len[u];
-    const int32_t t = v.next_pos[u] - 1;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int32_t n0 = v.len[u], p0 = v.next_pos[u];
+    // fused step: the new token enters slot n0 first (its page is mapped: the host checked)
+    const int32_t n = a.fused ? n0 + 1 : n0;
+    const int32_t t = a.fused ? p0 : p0 - 1;
+    if (a.fused) {
+        __syncthreads();   // every thread has read the old length and position
+        const int vec = v.row_bytes / 16;
+        if (tid < 2 * vec) {
+            const bool isv = tid >= vec;
+            const int c = isv ? tid - vec : tid;
+            const uint8_t* src = reinterpret_cast<const uint8_t*>(isv ? a.new_v : a.new_k) + (int64_t)uu * v.row_bytes;
+            uint8_t* dst = elem_row(v, u, n0, isv);
+            if (dst) reinterpret_cast<uint4*>(dst)[c] = reinterpret_cast<const uint4*>(src)[c];
+        }
+        if (tid == 0) {
+            v.pos[(int64_t)u * v.cap + n0] = p0;
+            v.imp[(int64_t)u * v.cap + n0] = 0.f;
+            v.len[u] = n;
+            v.next_pos[u] = p0 + 1;
+        }
+        __syncthreads();   // the new slot's position is visible to the block
+    }
     // q of this warp's head (warps < G), loaded first so its latency overlaps the ranking
     const int D = v.d, PERL = D / 32;   // PERL <= 4
     float x[4] = {0.f, 0.f, 0.f, 0.f};
@@ -350,7 +381,33 @@ __device__ void merge_unit(const ElemArgs& a, int32_t uu, int32_t u, int32_t n, 
                 kk = wkey[w];
                 sl = wslot[w];
             }
-        v.victim[u] = need_victim ? sl : -1;
+        wslot[kElemWarps] = need_victim ? sl : -1;
+    }
+    __syncthreads();   // the victim, and every slot's new importance, are visible to the block
+    const int32_t vs = wslot[kElemWarps];
+    if (!a.fused) {
+        if (tid == 0) v.victim[u] = vs;
+        return;
+    }
+    // fused step: with evict, the appended token (last slot) moves into the victim's slot
+    const bool cut = a.evict && vs >= 0;
+    if (cut && vs != n - 1) {
+        const int vec = v.row_bytes / 16;
+        if (tid < 2 * vec) {
+            const bool isv = tid >= vec;
+            const int c = isv ? tid - vec : tid;
+            const uint8_t* src = elem_row(v, u, n - 1, isv);
+            uint8_t* dst = elem_row(v, u, vs, isv);
+            if (src && dst) reinterpret_cast<uint4*>(dst)[c] = reinterpret_cast<const uint4*>(src)[c];
+        }
+        if (tid == 0) {
+            v.imp[(int64_t)u * v.cap + vs] = v.imp[(int64_t)u * v.cap + n - 1];
+            v.pos[(int64_t)u * v.cap + vs] = v.pos[(int64_t)u * v.cap + n - 1];
+        }
+    }
+    if (tid == 0) {
+        v.victim[u] = cut ? -1 : vs;
+        v.len[u] = cut ? n - 1 : n;
     }
 }
 
