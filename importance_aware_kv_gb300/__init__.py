@@ -98,6 +98,40 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
+def _raw_stream_fn():
+    import torch
+    return getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+_RAW_STREAM = None
+
+
+def _stream_of(t, stream):
+    """The stream handle for a call: the given one, else the current stream of
+    t's device (read without building a Stream object when torch allows)."""
+    global _RAW_STREAM
+    if stream is not None:
+        return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    if _RAW_STREAM is None:
+        _RAW_STREAM = _raw_stream_fn() or False
+    if _RAW_STREAM:
+        return _RAW_STREAM(t.device.index)
+    return _stream(None).value
+
+
+def _ptr_checked(t, name, dtype, shape):
+    """One pass of the checks _dev makes, returning the device pointer as an int."""
+    if not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if t.shape != shape:
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
 def _dev(t, name, dtype=None, shape=None):
     import torch
     if t is None:
@@ -238,6 +272,7 @@ class Cache:
 
     def __init__(self, cfg: CacheConfig):
         self.cfg = cfg
+        self._step_shapes = {}
         self.units_per_layer = cfg.batch * cfg.num_kv_heads
         self.units = cfg.num_layers * self.units_per_layer
         self.h = hikv_create_cache(cfg)
@@ -308,14 +343,23 @@ class Cache:
         return int(r.value)
 
     def step(self, k, v, q, out, evict=True, layer0=0, stream=None):
-        """append + decode_step (+ evict) as one call (one launch in steady state)."""
-        c = self.cfg
+        """append + decode_step (+ evict) as one call (one launch in steady state).
+        The per-step call of a decode loop: each tensor is checked once."""
+        import torch
         nl = self._layers(q, layer0)
-        self._check_tensor(k, "k", (nl, c.batch, c.num_kv_heads, 1, c.head_dim))
-        self._check_tensor(v, "v", tuple(k.shape))
-        self._check_tensor(q, "q", (nl, c.batch, c.num_q_heads, c.head_dim))
-        self._check_tensor(out, "out", tuple(q.shape))
-        hikv_decode_step_fused(self.h, layer0, k, v, q, out, evict, stream)
+        shapes = self._step_shapes.get(nl)
+        if shapes is None:
+            c = self.cfg
+            shapes = (torch.Size((nl, c.batch, c.num_kv_heads, 1, c.head_dim)),
+                      torch.Size((nl, c.batch, c.num_q_heads, c.head_dim)))
+            self._step_shapes[nl] = shapes
+        dt = self._dtype()
+        kp = _ptr_checked(k, "k", dt, shapes[0])
+        vp = _ptr_checked(v, "v", dt, shapes[0])
+        qp = _ptr_checked(q, "q", dt, shapes[1])
+        op = _ptr_checked(out, "out", dt, shapes[1])
+        _check(_lib.hikv_decode_step_fused(self.h, layer0, nl, kp, vp, qp, op, 1 if evict else 0,
+                                           _stream_of(q, stream)))
 
     def evict(self, layer0=0, nlayers=None, stream=None):
         hikv_evict(self.h, layer0, self.cfg.num_layers if nlayers is None else nlayers, stream)

@@ -87,6 +87,17 @@ def test_binding_rejects_misuse_before_any_launch(hk):
     with pytest.raises(ValueError):
         q = torch.zeros(2, 2, 4, 64, device=dev, dtype=torch.bfloat16)       # 2 layers, cache has 1
         c.decode_step(q, q.clone())
+    # the per-step call checks each tensor once, as thoroughly
+    k1 = torch.zeros(1, 2, 2, 1, 64, device=dev, dtype=torch.bfloat16)
+    q1 = torch.zeros(1, 2, 4, 64, device=dev, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        c.step(k1, k1.clone(), q1.float(), q1.clone())                          # fp32 q
+    with pytest.raises(ValueError):
+        c.step(k1[:, :, :1], k1.clone(), q1, q1.clone())                        # k has 1 KV head
+    with pytest.raises(ValueError):
+        c.step(k1, k1.clone(), q1, torch.zeros(1, 2, 64, 4, device=dev, dtype=torch.bfloat16).transpose(2, 3))
+    with pytest.raises(TypeError):
+        c.step(k1.cpu(), k1.clone(), q1, q1.clone())                            # host tensor
     assert c.kernel_launches() == n0
     c.close()
     with pytest.raises(hk.HikvError) as ei:                  # use after close
