@@ -545,4 +545,9 @@ int elem_span_ranks();
 int elem_max_tokens();
 cudaError_t launch_elem_decode(const ElemArgs& a, int dtype, int d, int max_n, cudaStream_t s);
 
+// Per-(kernel, device) attribute settings and occupancy queries, thread-safe (func_attr.cu).
+cudaError_t func_smem_optin(const void* func, size_t bytes);
+cudaError_t func_allow_nonportable_clusters(const void* func);
+int func_active_clusters(const void* func, int cs, const cudaLaunchConfig_t& cfg);
+
 }  // namespace hikv

@@ -853,16 +853,10 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
 
 template <typename T, int D, int G, bool SM>
 cudaError_t decode_prepare(size_t smem) {
-    auto kern = k_decode<T, D, G, SM>;
-    static size_t smem_set = 0;  // largest dynamic smem opted into so far
-    if (smem > smem_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-        smem_set = smem;
-    }
-    return cudaSuccess;
+    const void* kern = reinterpret_cast<const void*>(k_decode<T, D, G, SM>);
+    cudaError_t e = func_smem_optin(kern, smem);
+    if (e != cudaSuccess) return e;
+    return func_allow_nonportable_clusters(kern);
 }
 
 template <typename T, int D, int G>
@@ -882,24 +876,13 @@ cudaLaunchConfig_t decode_config(int cs, int n_clusters, size_t smem, cudaStream
 }
 
 // Clusters of `cs` CTAs with `smem` bytes each that can be resident at once
-// (clusters must fit in one GPC each); cached per (cs, smem).
+// (clusters must fit in one GPC each); cached per (kernel, device, cs, smem).
 template <typename T, int D, int G, bool SM>
 int decode_active_clusters(int cs, size_t smem) {
-    static int cached_cs[kMaxCS + 1] = {};
-    static size_t cached_smem[kMaxCS + 1] = {};
-    static int cached_active[kMaxCS + 1] = {};
-    const int csi = cs <= kMaxCS ? cs : kMaxCS;
-    if (cached_cs[csi] != cs || cached_smem[csi] != smem) {
-        if (decode_prepare<T, D, G, SM>(smem) != cudaSuccess) return 0;
-        cudaLaunchAttribute attr[1];
-        cudaLaunchConfig_t cfg = decode_config<T, D, G>(cs, 1, smem, nullptr, attr);
-        int active = 0;
-        if (cudaOccupancyMaxActiveClusters(&active, k_decode<T, D, G, SM>, &cfg) != cudaSuccess) active = 0;
-        cached_cs[csi] = cs;
-        cached_smem[csi] = smem;
-        cached_active[csi] = active;
-    }
-    return cached_active[csi];
+    if (decode_prepare<T, D, G, SM>(smem) != cudaSuccess) return 0;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = decode_config<T, D, G>(cs, 1, smem, nullptr, attr);
+    return func_active_clusters(reinterpret_cast<const void*>(k_decode<T, D, G, SM>), cs, cfg);
 }
 
 template <typename T, int D, int G, bool SM>

@@ -407,12 +407,8 @@ __global__ void __launch_bounds__(kSmallThreads, 2)
 template <typename T, int D, int G>
 cudaError_t decode_small_launch_one(const SmallArgs& a, const CUtensorMap& tmap, int n_ctas, cudaStream_t s) {
     constexpr int smem = SmallLayout<T, D, G>::TOTAL;
-    static bool set = false;
-    if (!set) {
-        cudaError_t e = cudaFuncSetAttribute(k_decode_small<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        set = true;
-    }
+    const cudaError_t e = func_smem_optin(reinterpret_cast<const void*>(k_decode_small<T, D, G>), smem);
+    if (e != cudaSuccess) return e;
     k_decode_small<T, D, G><<<n_ctas, kSmallThreads, smem, s>>>(a, tmap);
     return cudaGetLastError();
 }

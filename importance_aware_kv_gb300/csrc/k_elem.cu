@@ -721,17 +721,9 @@ template <typename T, int D, int G>
 cudaError_t launch_elem_t(const ElemArgs& a, int max_n, cudaStream_t s) {
     const size_t osmem = order_smem(a.ostride);
     const size_t ssmem = SpanLayout<D>(G).total;
-    static size_t o_set = 0, s_set = 0;
-    if (osmem > 48 * 1024 && osmem > o_set) {
-        cudaError_t e = cudaFuncSetAttribute(k_elem_order, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)osmem);
-        if (e != cudaSuccess) return e;
-        o_set = osmem;
-    }
-    if (ssmem > 48 * 1024 && ssmem > s_set) {
-        cudaError_t e = cudaFuncSetAttribute(k_elem_span<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssmem);
-        if (e != cudaSuccess) return e;
-        s_set = ssmem;
-    }
+    cudaError_t e0 = func_smem_optin(reinterpret_cast<const void*>(k_elem_order), osmem);
+    if (e0 == cudaSuccess) e0 = func_smem_optin(reinterpret_cast<const void*>(k_elem_span<T, D, G>), ssmem);
+    if (e0 != cudaSuccess) return e0;
     k_elem_order<<<a.nunits, kOrderThreads, osmem, s>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;

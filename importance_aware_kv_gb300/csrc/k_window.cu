@@ -227,18 +227,15 @@ cudaError_t launch_window(const WindowArgs& a, int dtype, int d, int group, cuda
     dim3 grid(a.nchunks_grid, a.nunits);
     cudaError_t e;
     if (dtype == 0) {
-        e = cudaFuncSetAttribute(k_window_p1<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(k_window_p2<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        e = func_smem_optin(reinterpret_cast<const void*>(k_window_p1<float>), smem);
+        if (e == cudaSuccess) e = func_smem_optin(reinterpret_cast<const void*>(k_window_p2<float>), smem);
         if (e != cudaSuccess) return e;
         k_window_p1<float><<<grid, kWinThreads, smem, s>>>(a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         k_window_p2<float><<<grid, kWinThreads, smem, s>>>(a);
     } else {
-        e = cudaFuncSetAttribute(k_window_p1<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(k_window_p2<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)smem);
+        e = func_smem_optin(reinterpret_cast<const void*>(k_window_p1<__nv_bfloat16>), smem);
+        if (e == cudaSuccess) e = func_smem_optin(reinterpret_cast<const void*>(k_window_p2<__nv_bfloat16>), smem);
         if (e != cudaSuccess) return e;
         k_window_p1<__nv_bfloat16><<<grid, kWinThreads, smem, s>>>(a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -286,14 +286,14 @@ extern "C" hikv_status hikv_score_window_noalloc(int32_t nlayers, int32_t batch,
     dim3 grid(nch, (unsigned)units);
     cudaStream_t s = (cudaStream_t)stream;
     if (dtype == HIKV_F32) {
-        if ((e = cudaFuncSetAttribute(k_na_p1<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) ||
-            (e = cudaFuncSetAttribute(k_na_p2<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
+        if ((e = func_smem_optin(reinterpret_cast<const void*>(k_na_p1<float>), smem)) ||
+            (e = func_smem_optin(reinterpret_cast<const void*>(k_na_p2<float>), smem)))
             return na_fail(HIKV_ERR_CUDA, "score_window_noalloc: cudaFuncSetAttribute failed");
         k_na_p1<float><<<grid, kNaThreads, smem, s>>>(a);
         k_na_p2<float><<<grid, kNaThreads, smem, s>>>(a);
     } else {
-        if ((e = cudaFuncSetAttribute(k_na_p1<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) ||
-            (e = cudaFuncSetAttribute(k_na_p2<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
+        if ((e = func_smem_optin(reinterpret_cast<const void*>(k_na_p1<__nv_bfloat16>), smem)) ||
+            (e = func_smem_optin(reinterpret_cast<const void*>(k_na_p2<__nv_bfloat16>), smem)))
             return na_fail(HIKV_ERR_CUDA, "score_window_noalloc: cudaFuncSetAttribute failed");
         k_na_p1<__nv_bfloat16><<<grid, kNaThreads, smem, s>>>(a);
         k_na_p2<__nv_bfloat16><<<grid, kNaThreads, smem, s>>>(a);

@@ -327,14 +327,9 @@ __global__ void __launch_bounds__(kTcThreads) k_window_tc(const WindowArgs a, co
 template <int D, int NQV>
 cudaError_t launch_tc(const WindowArgs& a, const CUtensorMap& tmap, cudaStream_t s) {
     constexpr int smem = WinTc<D, NQV>::BYTES;
-    static bool set = false;
-    if (!set) {
-        cudaError_t e = cudaFuncSetAttribute(k_window_tc<D, NQV, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(k_window_tc<D, NQV, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        set = true;
-    }
+    cudaError_t e0 = func_smem_optin(reinterpret_cast<const void*>(k_window_tc<D, NQV, false>), smem);
+    if (e0 == cudaSuccess) e0 = func_smem_optin(reinterpret_cast<const void*>(k_window_tc<D, NQV, true>), smem);
+    if (e0 != cudaSuccess) return e0;
     dim3 grid(a.nchunks_grid, a.nunits);
     k_window_tc<D, NQV, false><<<grid, kTcThreads, smem, s>>>(a, tmap);
     cudaError_t e = cudaGetLastError();
