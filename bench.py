@@ -267,6 +267,8 @@ def bench_gpu(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = W.WORKLOADS[args.workload]
+    if args.layers:   # the workload cut to its first L layers (small cases for profiling)
+        w = w.with_(layers=min(args.layers, w.layers), name=f"{w.name}-first{min(args.layers, w.layers)}layers")
     seed = rank_seed(w, rank) if args.seed is None else args.seed + 1000 * rank
     K, Wu, Ke, K3 = args.steps, args.warmup, args.e2e_steps, args.three_call_steps
     L = w.layers
@@ -525,6 +527,8 @@ def main():
                     help='budgets: "workload", "pyramid:AVG:MIN" or "duo:FRAC"')
     ap.add_argument("--workload", type=int, default=WORKLOAD_INDEX,
                     help="workload index (default: the Llama-3-8B layer the metric is quoted on)")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="cut the workload to its first L layers (profiling a smaller case; 0: all)")
     ap.add_argument("--spin-us", type=float, default=60.0)
     ap.add_argument("--impl", default="hikv", choices=["hikv", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -32,6 +32,8 @@ namespace {
 
 constexpr int kTcThreads = 256;
 constexpr int kTcTok = 64;                 // tokens per tile
+constexpr int kMaxTcChunk = 1024;          // tokens per CTA at most
+constexpr int kMaxChunkPages = kMaxTcChunk / 16 + 1;   // pages such a chunk can touch (pages hold >= 16 tokens)
 constexpr int kTcGroups = kTcTok / 16;     // 16-row TMA row groups per tile
 
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -40,6 +42,16 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a
         "{%0, %1, %2, %3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Four 8x8 b16 matrices from shared memory: lane l gives the address of row
+// (l mod 8) of matrix l / 8 (16 contiguous bytes); register i receives matrix
+// i, each lane holding row lane / 4, columns 2 (lane mod 4) and + 1 -- for a
+// token-major K tile that is the B fragment of mma m16n8k16 (col-major B).
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t saddr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(saddr));
 }
 
 template <int D, int NQV>
@@ -52,13 +64,17 @@ struct WinTc {
     static constexpr int NBOX = D * 2 / 128;       // 128-byte boxes per row
     static constexpr int TILE = kTcGroups * NBOX * 2048;   // bytes of one K tile
     static_assert(RB * NCS == 8 && NB >= 1, "warp tiling");
+    static_assert(KS % 2 == 0, "ldmatrix.x4 covers two k16 steps");
+    // TMA ring depth: three CTAs per SM with 3 stages up to 64 query rows, two with 4 above
+    static constexpr int STAGES = NQV <= 64 ? 3 : 4;
     // shared memory (from a 1024-aligned base)
-    static constexpr int OFF_TILE = 0;                         // [2][TILE]
-    static constexpr int OFF_BAR = 2 * TILE;                   // 2 mbarriers, then a status word
-    static constexpr int OFF_POS = OFF_BAR + 64;               // [kTcTok] int32
-    static constexpr int OFF_ML = OFF_POS + kTcTok * 4;        // [NCS][NQV][2] (pass 1) / MF,LI [NQV][2]
+    static constexpr int OFF_TILE = 0;                         // [STAGES][TILE]
+    static constexpr int OFF_BAR = STAGES * TILE;           // STAGES mbarriers, then a status word
+    static constexpr int OFF_POS = OFF_BAR + 8 * STAGES + 16;   // [2][kTcTok] int32
+    static constexpr int OFF_ML = OFF_POS + 2 * kTcTok * 4;    // [NCS][NQV][2] (pass 1) / MF,LI [NQV][2]
     static constexpr int OFF_P = OFF_ML + NCS * NQV * 2 * 4;   // [NQV][kTcTok + 4] fp32 increments (pass 2)
-    static constexpr int BYTES = OFF_P + NQV * (kTcTok + 4) * 4 + 1024;
+    static constexpr int OFF_PG = OFF_P + NQV * (kTcTok + 4) * 4;   // [kMaxChunkPages] page ids of the chunk
+    static constexpr int BYTES = OFF_PG + kMaxChunkPages * 4 + 1024;
 };
 
 // byte offset of element e of tile row r in a tile loaded as row groups of
@@ -71,10 +87,10 @@ __device__ __forceinline__ uint32_t tile_off(int r, int e) {
 
 // Queue the TMA loads of tile [s0, s0 + 64) of unit u into `dst`; returns the
 // bytes that will arrive on `bar` (row groups wholly past the chunk end are
-// not loaded).
+// not loaded).  pgs: the page ids of the chunk starting at c0.
 template <int NBOX>
-__device__ uint32_t issue_tile(const View& v, const CUtensorMap* tmap, int32_t u, int32_t s0, int32_t c1,
-                               uint8_t* dst, uint64_t* bar) {
+__device__ uint32_t issue_tile(const View& v, const CUtensorMap* tmap, const int32_t* pgs, int32_t c0, int32_t s0,
+                               int32_t c1, uint8_t* dst, uint64_t* bar) {
     uint32_t bytes = 0;
     int32_t ys[kTcGroups];
 #pragma unroll
@@ -82,7 +98,7 @@ __device__ uint32_t issue_tile(const View& v, const CUtensorMap* tmap, int32_t u
         ys[j] = -1;
         const int32_t s = s0 + 16 * j;
         if (s >= c1) continue;
-        const int32_t pg = v.page_table[(int64_t)u * v.max_pages + (s >> v.page_shift)];
+        const int32_t pg = pgs[(s >> v.page_shift) - (c0 >> v.page_shift)];   // the chunk's page ids, staged
         if (pg < 0 || pg >= v.pool_pages) {
             atomicOr(v.err, DEVERR_PAGE);
             continue;
@@ -102,7 +118,7 @@ __device__ uint32_t issue_tile(const View& v, const CUtensorMap* tmap, int32_t u
 }
 
 template <int D, int NQV, bool PASS2>
-__global__ void __launch_bounds__(kTcThreads) k_window_tc(const WindowArgs a, const __grid_constant__ CUtensorMap tmap) {
+__global__ void __launch_bounds__(kTcThreads, NQV <= 64 ? 3 : 2) k_window_tc(const WindowArgs a, const __grid_constant__ CUtensorMap tmap) {
     using C = WinTc<D, NQV>;
     extern __shared__ __align__(128) uint8_t wsm_raw[];
     uint8_t* smem = wsm_raw + ((1024u - (smem_u32(wsm_raw) & 1023u)) & 1023u);
@@ -127,21 +143,34 @@ __global__ void __launch_bounds__(kTcThreads) k_window_tc(const WindowArgs a, co
     const int32_t tnew = v.next_pos[u] - 1;
     uint8_t* tiles = smem + C::OFF_TILE;
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-    volatile int32_t* landed = reinterpret_cast<volatile int32_t*>(smem + C::OFF_BAR + 16);
+    volatile int32_t* landed = reinterpret_cast<volatile int32_t*>(smem + C::OFF_BAR + 8 * C::STAGES);
     int32_t* Ps = reinterpret_cast<int32_t*>(smem + C::OFF_POS);
     float* ML = reinterpret_cast<float*>(smem + C::OFF_ML);
     float* Pt = reinterpret_cast<float*>(smem + C::OFF_P);
+    int32_t* pgs = reinterpret_cast<int32_t*>(smem + C::OFF_PG);
     constexpr int PT = kTcTok + 4;   // row stride of Pt
 
     if (tid == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
+#pragma unroll
+        for (int st = 0; st < C::STAGES; ++st) mbar_init(&bar[st], 1);
         fence_mbar_init();
         prefetch_tensormap(&tmap);
     }
+    {   // the chunk's page ids, once (the refills then need no global round trip)
+        const int p0 = c0 >> v.page_shift, np = ((c1 - 1) >> v.page_shift) - p0 + 1;
+        for (int i = tid; i < np; i += kTcThreads) pgs[i] = v.page_table[(int64_t)u * v.max_pages + p0 + i];
+    }
     __syncthreads();
     const int ntiles = ceil_div(c1 - c0, kTcTok);
-    if (tid == 0) issue_tile<C::NBOX>(v, &tmap, u, c0, c1, tiles, &bar[0]);
+    // the first C::STAGES - 1 tiles go out at once; each iteration then queues
+    // the tile C::STAGES - 1 ahead into the stage the previous tile released
+    if (tid == 0)
+        for (int j = 0; j < C::STAGES - 1 && j < ntiles; ++j)
+            issue_tile<C::NBOX>(v, &tmap, pgs, c0, c0 + j * kTcTok, c1, tiles + j * C::TILE, &bar[j]);
+    // positions of tile 0, then one tile ahead in a register (threads < kTcTok)
+    int32_t pnext = (tid < kTcTok && c0 + tid < c1) ? v.pos[(int64_t)u * v.cap + c0 + tid] : INT32_MAX;
+    // pass 2: the importance of this thread's token of the next tile, likewise
+    float inext = (PASS2 && tid < kTcTok && c0 + tid < c1) ? v.imp[(int64_t)u * v.cap + c0 + tid] : 0.f;
 
     // A fragments: query rows rb*16 + g and + 8 (rows past nqv are zero), raw bf16
     const int per_layer = v.batch * v.hkv;
@@ -191,35 +220,56 @@ __global__ void __launch_bounds__(kTcThreads) k_window_tc(const WindowArgs a, co
 
     for (int i = 0; i < ntiles; ++i) {
         const int32_t s0 = c0 + i * kTcTok;
-        for (int r = tid; r < kTcTok; r += kTcThreads)
-            Ps[r] = (s0 + r < c1) ? v.pos[(int64_t)u * v.cap + s0 + r] : INT32_MAX;
-        if (tid == 0 && i + 1 < ntiles)   // the other buffer was released at the end of tile i - 1
-            issue_tile<C::NBOX>(v, &tmap, u, s0 + kTcTok, c1, tiles + ((i + 1) & 1) * C::TILE, &bar[(i + 1) & 1]);
+        const int st = i % C::STAGES;
+        int32_t* Pi = Ps + (i & 1) * kTcTok;   // read by tile i - 2 last: released two barriers ago
+        float icur = 0.f;
+        if (tid < kTcTok) {
+            Pi[tid] = pnext;
+            icur = inext;
+            const int32_t sn = s0 + kTcTok + tid;
+            pnext = sn < c1 ? v.pos[(int64_t)u * v.cap + sn] : INT32_MAX;   // lands during tile i
+            if (PASS2) inext = sn < c1 ? v.imp[(int64_t)u * v.cap + sn] : 0.f;
+        }
+        if (tid == 0 && i + C::STAGES - 1 < ntiles) {   // its stage held tile i - 1, released at its end
+            const int j = i + C::STAGES - 1;
+            issue_tile<C::NBOX>(v, &tmap, pgs, c0, c0 + j * kTcTok, c1, tiles + (j % C::STAGES) * C::TILE,
+                                &bar[j % C::STAGES]);
+        }
         // one thread waits for the tile (bounded); the CTA barrier then orders
         // every thread's reads after the copy, and all take the same branch
-        if (tid == 0) *landed = mbar_wait_bounded(&bar[i & 1], (uint32_t)(i >> 1) & 1u, v.err, kWaitFull, (uint32_t)i);
+        if (tid == 0) *landed = mbar_wait_bounded(&bar[st], (uint32_t)(i / C::STAGES) & 1u, v.err, kWaitFull, (uint32_t)i);
         __syncthreads();
         if (!*landed) {
-            // give up; let the copy already queued for the next tile land first
-            if (tid == 0 && i + 1 < ntiles)
-                mbar_wait_bounded(&bar[(i + 1) & 1], (uint32_t)((i + 1) >> 1) & 1u, v.err, kWaitDrain, (uint32_t)i);
+            // give up; let the copies already queued for the following tiles land first
+            if (tid == 0)
+                for (int j = i + 1; j < ntiles && j < i + C::STAGES; ++j)
+                    mbar_wait_bounded(&bar[j % C::STAGES], (uint32_t)(j / C::STAGES) & 1u, v.err, kWaitDrain, (uint32_t)i);
             __syncthreads();
             break;
         }
-        const uint8_t* tile = tiles + (i & 1) * C::TILE;
+        const uint8_t* tile = tiles + st * C::TILE;
 
         // S = Q K^T for rows [rb*16, +16) x tokens [cslice*COLS, +COLS) of the tile
         float acc[C::NB][4];
 #pragma unroll
         for (int nb = 0; nb < C::NB; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.f;
+        // B fragments by ldmatrix.x4: matrices (k16 step ks, low 8 dims), (ks,
+        // high 8), (ks + 1, low), (ks + 1, high) of token block nb; this lane
+        // addresses row (lane mod 8) of matrix lane / 8
+        {
+            const uint32_t tbase = smem_u32(tile);
+            const int mi = lane >> 3, rrow = lane & 7;
 #pragma unroll
-        for (int ks = 0; ks < C::KS; ++ks) {
+            for (int ks = 0; ks < C::KS; ks += 2) {
 #pragma unroll
-            for (int nb = 0; nb < C::NB; ++nb) {
-                const int col = cslice * C::COLS + nb * 8 + g;   // token row of the B fragment
-                const uint32_t b0 = *reinterpret_cast<const uint32_t*>(tile + tile_off<C::NBOX>(col, ks * 16 + 2 * t));
-                const uint32_t b1 = *reinterpret_cast<const uint32_t*>(tile + tile_off<C::NBOX>(col, ks * 16 + 8 + 2 * t));
-                mma_bf16_16816(acc[nb], af[ks], b0, b1);
+                for (int nb = 0; nb < C::NB; ++nb) {
+                    const int row = cslice * C::COLS + nb * 8 + rrow;
+                    const int k0 = (ks + (mi >> 1)) * 16 + (mi & 1) * 8;
+                    uint32_t b[4];
+                    ldmatrix_x4(b, tbase + tile_off<C::NBOX>(row, k0));
+                    mma_bf16_16816(acc[nb], af[ks], b[0], b[1]);
+                    mma_bf16_16816(acc[nb], af[ks + 1], b[2], b[3]);
+                }
             }
         }
         // logits (log2 domain) and causal visibility: value j of block nb is
@@ -231,7 +281,7 @@ __global__ void __launch_bounds__(kTcThreads) k_window_tc(const WindowArgs a, co
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int col = cslice * C::COLS + nb * 8 + 2 * t + (j & 1);
-                const int32_t p = Ps[col];
+                const int32_t p = Pi[col];
                 vis[nb][j] = p <= (j < 2 ? qpos0 : qpos1);
                 s[nb][j] = acc[nb][j] * qscale;
             }
@@ -284,14 +334,13 @@ __global__ void __launch_bounds__(kTcThreads) k_window_tc(const WindowArgs a, co
                 }
             }
             __syncthreads();
-            // per token: queries in position order
-            for (int r = tid; r < kTcTok; r += kTcThreads) {
-                const int32_t sidx = s0 + r;
-                if (sidx >= c1) continue;
-                const int64_t mi = (int64_t)u * v.cap + sidx;
-                float imp = v.imp[mi];
-                for (int qi = 0; qi < nq; ++qi) imp = imp + Pt[qi * PT + r];
-                v.imp[mi] = imp;
+            // per token (thread r < kTcTok): queries in position order, onto
+            // the importance loaded one tile ahead (no other CTA touches it)
+            static_assert(kTcTok <= kTcThreads, "one token per thread");
+            if (tid < kTcTok && s0 + tid < c1) {
+                float imp = icur;
+                for (int qi = 0; qi < nq; ++qi) imp = imp + Pt[qi * PT + tid];
+                v.imp[(int64_t)u * v.cap + s0 + tid] = imp;
             }
         }
         __syncthreads();   // the tile buffer, Ps and Pt are free again
@@ -351,6 +400,7 @@ cudaError_t launch_tc_d(const WindowArgs& a, const CUtensorMap& tmap, int nqv, c
 bool window_tc_supported(int dtype, int d, int nqv) { return dtype == 1 && (d == 64 || d == 128) && nqv <= 128; }
 
 cudaError_t launch_window_tc(const WindowArgs& a, const CUtensorMap& tmap, int d, int nqv, cudaStream_t s) {
+    if (a.chunk > kMaxTcChunk || a.chunk % kTcTok) return cudaErrorInvalidValue;
     return d == 64 ? launch_tc_d<64>(a, tmap, nqv, s) : launch_tc_d<128>(a, tmap, nqv, s);
 }
 
