@@ -185,7 +185,8 @@ def test_hikv_dual_bank_llama3_8b_layer():
     (dict(hq=16, hkv=2, budget=600, prompt=900), 64),               # G = 8
     (dict(hq=2, hkv=2, budget=200), 48),                            # G = 1
     (dict(dtype="f32", d=128, hq=8, hkv=1, budget=1100, prompt=1500), 96),
-], ids=["b64_1chunk", "b32_2spans", "b1", "b127", "f32_d64_g2", "g8", "g1", "f32_g8_3spans"])
+    (dict(prompt=900, budget=300, evict_every=4), 64),              # fused steps without eviction, batched cuts
+], ids=["b64_1chunk", "b32_2spans", "b1", "b127", "f32_d64_g2", "g8", "g1", "f32_g8_3spans", "evict_every4"])
 def test_hikv_stage2_element_level(kw, b2, fused):
     rep = _run(SMALL.with_(**kw), element_budget=b2, fused=fused)
     assert rep.evictions_checked > 0
