@@ -193,6 +193,15 @@ def test_hikv_stage2_element_level(kw, b2, fused):
     print("stage2 rows skipped as near-ties:", rep.stage2_near_tie_rows, "of", rep.outputs_checked)
 
 
+def test_hikv_stage2_positions_spread_over_70k():
+    # a 70,000-token prompt cut to 300: the retained positions span 0..70,011,
+    # so the order kernel bins them 32 positions to a bucket and ranks inside
+    # buckets; 16-token pages put a page boundary every 16 slots
+    w = SMALL.with_(layers=1, batch=1, hq=8, hkv=2, prompt=70000, budget=300, steps=12)
+    rep = _run(w, element_budget=64, fused=True, page_tokens=16)
+    assert rep.evictions_checked == 2 * (1 + 12)
+
+
 def test_hikv_stage2_with_recent_bank():
     rep = _run(SMALL.with_(sink=0, window=48, budget=96), element_budget=48, importance_mode=1, fused=True)
     assert rep.evictions_checked > 0
