@@ -173,8 +173,9 @@ def test_hikv_dual_bank_llama3_8b_layer():
 
 # HiKV Stage II: element-level attention against the oracle's statement of it.
 # Output rows whose chunk selection the oracle decided by less than 1e-4 in p
-# are left out of the output comparison (counted in the report); importance,
-# which takes the whole P, and the retained sets are compared everywhere.
+# are held to |d| <= 2e-2 instead of the dtype's bound (counted in the
+# report); importance, which takes the whole P, and the retained sets are
+# compared at the usual tolerances everywhere.
 @FUSED
 @pytest.mark.parametrize("kw,b2", [
     (dict(), 64),                                                   # one chunk of 97 entries
@@ -190,7 +191,7 @@ def test_hikv_dual_bank_llama3_8b_layer():
 def test_hikv_stage2_element_level(kw, b2, fused):
     rep = _run(SMALL.with_(**kw), element_budget=b2, fused=fused)
     assert rep.evictions_checked > 0
-    print("stage2 rows skipped as near-ties:", rep.stage2_near_tie_rows, "of", rep.outputs_checked)
+    print("stage2 near-tie rows (loose bound):", rep.stage2_near_tie_rows, "elements checked:", rep.outputs_checked)
 
 
 def test_hikv_stage2_positions_spread_over_70k():
@@ -218,7 +219,7 @@ def test_hikv_stage2_llama3_8b_layer():
     # V rows read: at most every attended row (64 units x 1025 x 24 steps), and
     # at least the B2 of each full chunk that one head keeps (8 x 64 + 1 per unit)
     assert 64 * 24 * (8 * 64 + 1) <= rows <= 64 * 24 * 1025
-    print("stage2 8B layer: rows skipped", rep.stage2_near_tie_rows, "max bf16 err", rep.max_out_err)
+    print("stage2 8B layer: near-tie rows (loose bound)", rep.stage2_near_tie_rows, "max bf16 err", rep.max_out_err)
 
 
 def test_hikv_stage2_rejects_units_above_its_limit():
