@@ -454,6 +454,33 @@ def bench_gpu(args):
     lens = cache.lengths()
     cache.close()
 
+    # ---- size floor (context for the roofline fraction): how long the
+    # plainest kernels take to read, and to copy, one step's bytes from a
+    # flushed L2, timed the same way as the steps ----
+    def size_floor(nbytes, reps=20):
+        buf = torch.empty(max(1, nbytes // 2), dtype=torch.bfloat16, device=dev).normal_()
+        dst = torch.empty_like(buf)
+        acc = torch.empty((), dtype=torch.float32, device=dev)
+        out = {}
+        for name, fn in (("read_us", lambda: torch.sum(buf, 0, dtype=torch.float32, out=acc)),
+                         ("copy_us", lambda: dst.copy_(buf))):
+            fn()
+            ts = []
+            for i in range(reps):
+                flush.fill_(float(i))
+                torch.cuda._sleep(spin_cycles)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                b.synchronize()
+                ts.append(a.elapsed_time(b) * 1e3)
+            out[name] = float(np.median(ts))
+        del buf, dst
+        return out
+    floor = size_floor(int(alg_bytes // K)) if K > 0 else None
+    stage("size floor done")
+
     # ---- numbers ----
     avg_s = t_total / K
     peaks, src = measured_peaks()
@@ -499,6 +526,9 @@ def bench_gpu(args):
         "per_layer_launches": per_layer,
         "setup": setup,
         "clocks": clocks,
+        "size_floor": ({"bytes": int(alg_bytes // K), "kernels": "torch sum (read) and copy of a buffer of one "
+                        "step's algorithmic bytes, L2 flushed before each, median of 20",
+                        **floor, "step_us": avg_s * 1e6} if floor else None),
     }
     if rank == 0 and not args.no_cpu_baseline:
         val, cores, done, sample = run_cpu_oracle(w, seed, min(64, w.steps), 2, budget_s=20.0,
