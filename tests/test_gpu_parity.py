@@ -187,7 +187,10 @@ def test_hikv_dual_bank_llama3_8b_layer():
     (dict(hq=2, hkv=2, budget=200), 48),                            # G = 1
     (dict(dtype="f32", d=128, hq=8, hkv=1, budget=1100, prompt=1500), 96),
     (dict(prompt=900, budget=300, evict_every=4), 64),              # fused steps without eviction, batched cuts
-], ids=["b64_1chunk", "b32_2spans", "b1", "b127", "f32_d64_g2", "g8", "g1", "f32_g8_3spans", "evict_every4"])
+    (dict(budget=127), 64),                                         # n = 128: one full span, no tail
+    (dict(budget=128), 64),                                         # n = 129: a second span of one rank
+], ids=["b64_1chunk", "b32_2spans", "b1", "b127", "f32_d64_g2", "g8", "g1", "f32_g8_3spans", "evict_every4",
+        "n128", "n129"])
 def test_hikv_stage2_element_level(kw, b2, fused):
     rep = _run(SMALL.with_(**kw), element_budget=b2, fused=fused)
     assert rep.evictions_checked > 0
