@@ -182,11 +182,15 @@ def schedule_budgets(w, seed, schedule):
     raise ValueError(f"unknown schedule {schedule!r}")
 
 
-def run_cpu_oracle(w, seed, steps, warmup, budget_s=20.0, layers=None, budgets=None, element_budget=0):
+def run_cpu_oracle(w, seed, steps, warmup, budget_s=20.0, layers=None, budgets=None, element_budget=0,
+                   steps_1thread=0, budget_1thread_s=10.0):
     """Time the oracle's decode loop (append -> decode -> evict when due) on the
     given layers (default all) and scale to whole-workload steps/s: a step of
     the workload needs every layer, so sampled rate x (sampled / all layers).
-    Returns (steps/s of the whole workload, threads, steps timed, sample text)."""
+    With steps_1thread > 0 the loop then continues for up to that many steps
+    (or budget_1thread_s seconds) on one thread.
+    Returns (steps/s of the whole workload, threads, steps timed, sample text,
+    (steps/s on one thread, steps timed on one thread) or None)."""
     import oracle
     import workloads as W
     threads = os.cpu_count() or 1
@@ -202,28 +206,43 @@ def run_cpu_oracle(w, seed, steps, warmup, budget_s=20.0, layers=None, budgets=N
         del k, v
         O.score_window(si, W.to_f32(W.gen_q(w, l, 1, w.prompt - w.nq, w.nq, seed)))
     O.evict(0, len(layers))
-    total = warmup + steps
+    total = warmup + steps + steps_1thread
     ks = [W.gen_kv(w, l, 1, w.prompt, total, seed) for l in layers]
     qs = [W.gen_q(w, l, 1, w.prompt, total, seed) for l in layers]
-    done, t_used = 0, 0.0
-    for s in range(total):
+    def one_step(s):
         t0 = time.perf_counter()
         for si in range(len(layers)):
             O.append(si, W.to_f32(ks[si][0][:, :, :, s:s + 1]), W.to_f32(ks[si][1][:, :, :, s:s + 1]))
             O.decode(si, W.to_f32(qs[si][:, :, :, s]))
         if (s + 1) % w.evict_every == 0:
             O.evict(0, len(layers))
-        dt = time.perf_counter() - t0
-        if s >= warmup:
+        return time.perf_counter() - t0
+
+    done, t_used, s = 0, 0.0, 0
+    while s < warmup + steps:
+        dt = one_step(s)
+        s += 1
+        if s > warmup:
             t_used += dt
             done += 1
             if t_used > budget_s:
                 break
     frac = len(layers) / w.layers
+    single = None
+    if steps_1thread > 0:
+        O.threads(1)
+        done1, t1 = 0, 0.0
+        for _ in range(steps_1thread):
+            t1 += one_step(s)
+            s += 1
+            done1 += 1
+            if t1 > budget_1thread_s:
+                break
+        single = (frac * done1 / t1, done1)
     sample = (f"{done} decode steps of all {w.units} units" if frac == 1 else
               f"{done} decode steps of layer(s) {layers} ({len(layers) * w.batch * w.hkv} of {w.units} "
               f"units), rate scaled by {len(layers)}/{w.layers} layers")
-    return frac * done / t_used, threads, done, sample
+    return frac * done / t_used, threads, done, sample, single
 
 
 def oracle_sample_layers(w):
@@ -237,7 +256,7 @@ def bench_reference(args):
     if rank != 0:
         return
     w = W.WORKLOADS[args.workload]
-    val, cores, done, sample = run_cpu_oracle(w, w.index, args.steps, args.warmup, budget_s=120.0,
+    val, cores, done, sample, _ = run_cpu_oracle(w, w.index, args.steps, args.warmup, budget_s=120.0,
                                               layers=oracle_sample_layers(w))
     line = {
         "impl": "reference", "metric": METRIC, "value": val, "unit": "steps/s", "n_gpus": 0,
@@ -531,11 +550,14 @@ def bench_gpu(args):
                         **floor, "step_us": avg_s * 1e6} if floor else None),
     }
     if rank == 0 and not args.no_cpu_baseline:
-        val, cores, done, sample = run_cpu_oracle(w, seed, min(64, w.steps), 2, budget_s=20.0,
+        val, cores, done, sample, single = run_cpu_oracle(w, seed, min(64, w.steps), 2, budget_s=20.0,
                                                   layers=oracle_sample_layers(w), budgets=budgets,
-                                                  element_budget=elem)
+                                                  element_budget=elem, steps_1thread=16)
         line["cpu_baseline"] = {"value": val, "unit": "steps/s", "cores": cores, "kind": "oracle",
                                 "sample": sample}
+        if single:
+            line["cpu_baseline"]["value_1thread"] = single[0]
+            line["cpu_baseline"]["sample_1thread"] = f"{single[1]} further steps of the same sample on one thread"
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
