@@ -94,6 +94,11 @@ __host__ __device__ inline int32_t pages_kept(int32_t B, int32_t page_tokens, in
 // complete.
 __host__ __device__ constexpr int dec_occupancy(int /*row_bytes*/, int /*group*/) { return 2; }
 __host__ __device__ constexpr int dec_consumer_warps(int /*row_bytes*/, int /*group*/) { return 4; }
+// Head groups of a decode CTA: with G = 8 each tile is consumed by two warps,
+// one per half of the group's query heads (two sets of dec_consumer_warps
+// warps rotating over the same tiles), so a warp carries the state of four
+// heads and twice the warps hide the tile loop's latency.
+__host__ __device__ constexpr int dec_head_groups(int group) { return group == 8 ? 2 : 1; }
 __host__ __device__ constexpr int dec_stages(int row_bytes, int group) {
     return 2 * dec_consumer_warps(row_bytes, group);
 }

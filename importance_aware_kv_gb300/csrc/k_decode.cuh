@@ -45,7 +45,7 @@ namespace hikv {
 
 // threads of a decode CTA: the consumer warps and one producer warp
 template <typename T, int D, int G>
-constexpr int dec_threads() { return (dec_consumer_warps(D * (int)sizeof(T), G) + 1) * 32; }
+constexpr int dec_threads() { return (dec_consumer_warps(D * (int)sizeof(T), G) * dec_head_groups(G) + 1) * 32; }
 constexpr int kDecTR = 16;                       // slots per tile
 constexpr float kDecLazy = 8.f;                  // softmax reference slack (log2 units)
 constexpr int kDecMaxPg = 256;                   // page ids cached in shared memory
@@ -59,7 +59,7 @@ struct DecSmem {
 template <typename T, int D, int G>
 __host__ __device__ inline DecSmem dec_layout(bool smem_s, int chunk_cap) {
     constexpr uint32_t RB = D * sizeof(T);
-    constexpr int kDecNCW = dec_consumer_warps(RB, G);
+    constexpr int kDecNGW = dec_consumer_warps(RB, G);   // warps per head group
     DecSmem L{};
     uint32_t off = 0;
     L.ring = off;                                 // K,V tiles
@@ -74,10 +74,10 @@ __host__ __device__ inline DecSmem dec_layout(bool smem_s, int chunk_cap) {
     off = (off + 15) & ~15u;
     L.q = off;                                    // q * scale * log2 e, fp32 [G][D]
     off += G * D * 4;
-    L.ps = off;                                   // per-warp p of the tile [NCW][16][G]
-    off += kDecNCW * kDecTR * G * 4;
-    L.red = off;                                  // warp O partials [NCW][G][D]
-    off += kDecNCW * G * D * 4;
+    L.ps = off;                                   // per-warp p of the tile [NCW * HG][16][G / HG]
+    off += kDecNGW * kDecTR * G * 4;              // (= NCW * HG * 16 * G / HG)
+    L.red = off;                                  // warp O partials [NGW][G][D]
+    off += kDecNGW * G * D * 4;
     // exchange buffer per unit parity: m [kMaxCS][G], l [kMaxCS][G], O slices [G*D + kMaxCS]
     L.xbuf_bytes = (2 * kMaxCS * G + G * D + kMaxCS) * 4;
     L.xbuf = off;
@@ -137,7 +137,10 @@ template <typename T, int D, int G, bool SMEM_S>
 __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * sizeof(T), G))
     k_decode(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap) {
     constexpr int ESZ = (int)sizeof(T);
-    constexpr int kDecNCW = dec_consumer_warps(D * ESZ, G);
+    constexpr int kDecNGW = dec_consumer_warps(D * ESZ, G);   // warps of a head group (the tile rotation)
+    constexpr int kHG = dec_head_groups(G);                   // head groups
+    constexpr int kDecNCW = kDecNGW * kHG;                    // consumer warps
+    constexpr int GW = G / kHG;                               // query heads of a warp
     constexpr int RB = D * ESZ;              // row bytes: 128, 256 or 512
     constexpr int NBOX = RB / 128;           // 128-byte TMA boxes per row
     constexpr int TB = kDecTR * RB;          // K (or V) tile bytes
@@ -149,7 +152,7 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
     constexpr int NCT = kDecNCW * 32;        // consumer threads
     constexpr uint32_t QB = G * D * ESZ;     // bytes of one unit's q
     constexpr int kDecStages = dec_stages(RB, G);
-    static_assert(kDecStages % kDecNCW == 0, "each stage must always be consumed by the same warp");
+    static_assert(kDecStages % kDecNGW == 0, "each stage must always be consumed by the same warp of each group");
     static_assert(EPL % 2 == 0 && EPC % 2 == 0, "pairs");
     using Raw = typename RawVec<LB>::type;
 
@@ -171,11 +174,11 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
     float* ps_all = reinterpret_cast<float*>(smem + L.ps);
     float* red = reinterpret_cast<float*>(smem + L.red);
     float* sm = reinterpret_cast<float*>(smem + L.small);
-    static_assert(kDecNCW * G <= 32, "warp state arrays");
+    static_assert(kDecNGW * G <= 32, "warp state arrays");
     static_assert(kMaxCS * G <= NCT, "one consumer thread per (CTA, head) of the exchange");
-    float* mw_s = sm;                          // [NCW][G]     (32)
-    float* lw_s = sm + 32;                     // [NCW][G]     (32)
-    float* wsc = sm + 64;                      // [NCW][G]     (32)
+    float* mw_s = sm;                          // [NGW][G]     (32)
+    float* lw_s = sm + 32;                     // [NGW][G]     (32)
+    float* wsc = sm + 64;                      // [NGW][G]     (32)
     float* mfin = sm + 96;                     // [G]
     float* linv = sm + 104;                    // [G]
     float* m_c = sm + 112;                     // [G]
@@ -184,7 +187,8 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
     unsigned long long* wkey = reinterpret_cast<unsigned long long*>(sm + 256);  // [NCW]
     int32_t* wslot = reinterpret_cast<int32_t*>(wkey + kDecNCW);                 // [NCW]
     volatile int32_t* abort_flag = wslot + kDecNCW;
-    float* new_imp_s = sm + 280;               // fused: the new token's final importance
+    float* new_imp_s = sm + 288;               // fused: the new token's final importance
+    static_assert(256 + 3 * kDecNCW + 1 <= 288, "victim slots overlap");
     int32_t* pg_s = reinterpret_cast<int32_t*>(smem + L.pg);
     float* S_smem = reinterpret_cast<float*>(smem + L.S);
 
@@ -210,7 +214,7 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
     if (tid == 0) {
         for (int s = 0; s < kDecStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], (uint32_t)kHG);   // one warp of each head group releases the stage
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&qfull[b], 1);
@@ -334,7 +338,9 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
 
     // ======================= consumers =======================
     const int ctid = tid;  // consumer thread 0 .. NCT-1
-    float* ps = ps_all + warp * (kDecTR * G);      // [16][G] p of the tile
+    const int wg = warp / kDecNGW, wi = warp % kDecNGW;   // head group, place in the tile rotation
+    const int h0 = wg * GW;                               // this warp's heads: h0 .. h0 + GW - 1
+    float* ps = ps_all + warp * (kDecTR * GW);     // [16][GW] p of the tile
     const int qr = lane & 15;           // q.k: tile row of this lane
     const int qh = lane >> 4;           // q.k: half of the row
     const int pv_chunk = (lane * LB) >> 4, pv_in = (lane * LB) & 15;
@@ -361,7 +367,7 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
         const bool tail = cnt > 1 && (cnt - 1) % kDecTR == 0;
         const int32_t ts = t1 - 1;   // the tail slot
         const int32_t nt = tail ? (cnt - 1) / kDecTR : (cnt > 0 ? (t1 - 1) / kDecTR - first_blk + 1 : 0);
-        const int tail_warp = nt % kDecNCW;
+        const int tail_warp = nt % kDecNGW;
         const int64_t qbase = (((int64_t)li * v.batch + b) * v.hq + (int64_t)g * G) * D;
         const int32_t per = ceil_div(G * D, CS);   // output elements finalised per CTA
         const int xb = k & 1;
@@ -382,7 +388,7 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
 
         // the tail row's K and V: the staged rows when it is the new token,
         // else this lane's share read from the pool now (used after the tiles)
-        const bool tail_here = tail && warp == tail_warp;
+        const bool tail_here = tail && wi == tail_warp;   // one warp of each head group
         const bool tail_staged = a.fused && ts == sn;
         Raw tail_k{}, tail_v{};
         if (tail_here && !tail_staged) {
@@ -408,17 +414,17 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
         }
         named_bar_sync(1, NCT);
 
-        float m_w[G], l_w[G];
-        float2 o2[G][EPL / 2];
+        float m_w[GW], l_w[GW];
+        float2 o2[GW][EPL / 2];
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
+        for (int h = 0; h < GW; ++h) {
             m_w[h] = -INFINITY;
             l_w[h] = 0.f;
 #pragma unroll
             for (int e = 0; e < EPL / 2; ++e) o2[h][e] = make_float2(0.f, 0.f);
         }
 
-        for (int i = warp; i < nt; i += kDecNCW) {
+        for (int i = wi; i < nt; i += kDecNGW) {
             if (*abort_flag) break;
             const int gi = gi_base + i;
             const int st = gi % kDecStages;
@@ -440,7 +446,9 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                 *reinterpret_cast<Raw*>(ktile + swz(r, pv_chunk) + pv_in) = nk;
                 *reinterpret_cast<Raw*>(vtile + swz(r, pv_chunk) + pv_in) = nv;
                 fence_proxy_async_smem();   // the stage is refilled by TMA later
-                const int32_t pg = v.page_table[(int64_t)u * v.max_pages + (sn >> v.page_shift)];
+                // (both head groups' warps patch the landed tile with the same
+                // bytes before reading it; one of them writes the pool)
+                const int32_t pg = wg == 0 ? v.page_table[(int64_t)u * v.max_pages + (sn >> v.page_shift)] : -1;
                 if (pg >= 0 && pg < v.pool_pages) {
                     uint8_t* kd = v.pool + (int64_t)pg * v.page_bytes + (int64_t)(sn & (v.page_tokens - 1)) * RB;
                     *reinterpret_cast<Raw*>(kd + lane * LB) = nk;
@@ -450,9 +458,9 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
             }
 
             // ---- q.k: this lane's half row ----
-            float2 acc[G];
+            float2 acc[GW];
 #pragma unroll
-            for (int h = 0; h < G; ++h) acc[h] = make_float2(0.f, 0.f);
+            for (int h = 0; h < GW; ++h) acc[h] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int j = 0; j < CPL; ++j) {
                 const int cidx = 2 * j + qh;   // halves interleave: their q reads fall in different banks
@@ -460,8 +468,8 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                 float x[EPC];
                 Widen<T, EPC>::run(raw, x);
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    const float* qp = q_s + h * D + cidx * EPC;
+                for (int h = 0; h < GW; ++h) {
+                    const float* qp = q_s + (h0 + h) * D + cidx * EPC;
 #pragma unroll
                     for (int e = 0; e < EPC; e += 4) {
                         const float4 q4 = *reinterpret_cast<const float4*>(qp + e);
@@ -471,9 +479,9 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                 }
             }
             const bool rv = qr >= lo_r && qr < hi_r;
-            float s[G];
+            float s[GW];
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
+            for (int h = 0; h < GW; ++h) {
                 float t = acc[h].x + acc[h].y;
                 t += __shfl_xor_sync(0xffffffffu, t, 16);
                 s[h] = rv ? t : -INFINITY;
@@ -484,10 +492,10 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
             // per lane until the unit's merge ----
             bool big = false;
 #pragma unroll
-            for (int h = 0; h < G; ++h) big |= s[h] > m_w[h] + kDecLazy;   // invalid rows: -inf
+            for (int h = 0; h < GW; ++h) big |= s[h] > m_w[h] + kDecLazy;   // invalid rows: -inf
             if (__any_sync(0xffffffffu, big)) {
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
+                for (int h = 0; h < GW; ++h) {
                     float mt = s[h];
 #pragma unroll
                     for (int o = 8; o >= 1; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
@@ -502,15 +510,16 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                     }
                 }
             }
-            float p[G];
+            float p[GW];
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
+            for (int h = 0; h < GW; ++h) {
                 p[h] = rv ? exp2f(s[h] - m_w[h]) : 0.f;
                 l_w[h] += p[h];   // this lane's row; both halves of a row hold the same p
             }
             if (qh == 0) {
-                store_group<G>(ps + qr * G, p);
-                if (rv && (!SMEM_S || s0 + qr - s_off < a.chunk_cap)) store_group<G>(Sb + (int64_t)(s0 + qr - s_off) * G, s);
+                store_group<GW>(ps + qr * GW, p);
+                if (rv && (!SMEM_S || s0 + qr - s_off < a.chunk_cap))
+                    store_group<GW>(Sb + (int64_t)(s0 + qr - s_off) * G + h0, s);   // this group's heads of the row
             }
             __syncwarp();
             // ---- p.v over the tile's valid rows (unrolled; invalid rows skipped, their
@@ -521,27 +530,27 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                 const Raw raw = *reinterpret_cast<const Raw*>(vtile + swz(r, pv_chunk) + pv_in);
                 float x[EPL];
                 Widen<T, EPL>::run(raw, x);
-                const float* pr = ps + r * G;
-                float2 pp[G];
-                if constexpr (G % 4 == 0) {
+                const float* pr = ps + r * GW;
+                float2 pp[GW];
+                if constexpr (GW % 4 == 0) {
 #pragma unroll
-                    for (int h = 0; h < G; h += 4) {
+                    for (int h = 0; h < GW; h += 4) {
                         const float4 t4 = *reinterpret_cast<const float4*>(pr + h);
                         pp[h] = make_float2(t4.x, t4.x);
                         pp[h + 1] = make_float2(t4.y, t4.y);
                         pp[h + 2] = make_float2(t4.z, t4.z);
                         pp[h + 3] = make_float2(t4.w, t4.w);
                     }
-                } else if constexpr (G == 2) {
+                } else if constexpr (GW == 2) {
                     const float2 t2 = *reinterpret_cast<const float2*>(pr);
                     pp[0] = make_float2(t2.x, t2.x);
                     pp[1] = make_float2(t2.y, t2.y);
                 } else {
 #pragma unroll
-                    for (int h = 0; h < G; ++h) pp[h] = make_float2(pr[h], pr[h]);
+                    for (int h = 0; h < GW; ++h) pp[h] = make_float2(pr[h], pr[h]);
                 }
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
+                for (int h = 0; h < GW; ++h) {
 #pragma unroll
                     for (int e = 0; e < EPL / 2; ++e)
                         o2[h][e] = ffma2(make_float2(x[2 * e], x[2 * e + 1]), pp[h], o2[h][e]);
@@ -561,13 +570,13 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
             float xk[EPL], xv[EPL];
             Widen<T, EPL>::run(tail_k, xk);
             Widen<T, EPL>::run(tail_v, xv);
-            float s[G];
+            float s[GW];
             bool big = false;
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
+            for (int h = 0; h < GW; ++h) {
                 float t = 0.f;
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) t = fmaf(q_s[h * D + lane * EPL + e], xk[e], t);
+                for (int e = 0; e < EPL; ++e) t = fmaf(q_s[(h0 + h) * D + lane * EPL + e], xk[e], t);
 #pragma unroll
                 for (int o = 16; o >= 1; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
                 s[h] = t;
@@ -575,7 +584,7 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
             }
             if (big) {   // warp-uniform: s is
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
+                for (int h = 0; h < GW; ++h) {
                     const float mn = fmaxf(m_w[h], s[h]);
                     const float scl = exp2f(m_w[h] - mn);
                     m_w[h] = mn;
@@ -588,15 +597,15 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                 }
             }
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
+            for (int h = 0; h < GW; ++h) {
                 const float p = exp2f(s[h] - m_w[h]);
                 if ((lane & 15) == 0) l_w[h] += p;   // once in each half's row sum
 #pragma unroll
                 for (int e = 0; e < EPL / 2; ++e)
                     o2[h][e] = ffma2(make_float2(xv[2 * e], xv[2 * e + 1]), make_float2(p, p), o2[h][e]);
             }
-            if (lane == 0 && (!SMEM_S || ts - s_off < a.chunk_cap)) store_group<G>(Sb + (int64_t)(ts - s_off) * G, s);
-            if (tail_staged) {   // the new token's rows into the pool for later steps
+            if (lane == 0 && (!SMEM_S || ts - s_off < a.chunk_cap)) store_group<GW>(Sb + (int64_t)(ts - s_off) * G + h0, s);
+            if (tail_staged && wg == 0) {   // the new token's rows into the pool for later steps
                 const int32_t pg = v.page_table[(int64_t)u * v.max_pages + (sn >> v.page_shift)];
                 if (pg >= 0 && pg < v.pool_pages) {
                     uint8_t* kd = v.pool + (int64_t)pg * v.page_bytes + (int64_t)(sn & (v.page_tokens - 1)) * RB;
@@ -623,28 +632,30 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
         load_imp(0);
 
         // ---- CTA merge of the warp states ----
+        // (state of head h0 + h of rotation place wi at [wi][h0 + h]: a head's
+        // partials come from the kDecNGW warps of its head group)
 #pragma unroll
-        for (int h = 0; h < G; ++h)   // sum of the per-lane row sums over the 16 rows
+        for (int h = 0; h < GW; ++h)   // sum of the per-lane row sums over the 16 rows
 #pragma unroll
             for (int o = 8; o >= 1; o >>= 1) l_w[h] += __shfl_xor_sync(0xffffffffu, l_w[h], o);
         if (lane == 0) {
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                mw_s[warp * G + h] = m_w[h];
-                lw_s[warp * G + h] = l_w[h];
+            for (int h = 0; h < GW; ++h) {
+                mw_s[wi * G + h0 + h] = m_w[h];
+                lw_s[wi * G + h0 + h] = l_w[h];
             }
         }
 #pragma unroll
-        for (int h = 0; h < G; ++h)
+        for (int h = 0; h < GW; ++h)
 #pragma unroll
             for (int e = 0; e < EPL / 2; ++e)
-                *reinterpret_cast<float2*>(&red[(warp * G + h) * D + lane * EPL + 2 * e]) = o2[h][e];
+                *reinterpret_cast<float2*>(&red[(wi * G + h0 + h) * D + lane * EPL + 2 * e]) = o2[h][e];
         named_bar_sync(1, NCT);
         if (ctid < G) {
             float m = -INFINITY;
-            for (int w = 0; w < kDecNCW; ++w) m = fmaxf(m, mw_s[w * G + ctid]);
+            for (int w = 0; w < kDecNGW; ++w) m = fmaxf(m, mw_s[w * G + ctid]);
             float l = 0.f;
-            for (int w = 0; w < kDecNCW; ++w) {
+            for (int w = 0; w < kDecNGW; ++w) {
                 const float mw = mw_s[w * G + ctid];
                 const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - m);
                 wsc[w * G + ctid] = f;
@@ -666,7 +677,7 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                 const int h = e / D;
                 float sum = 0.f;
 #pragma unroll
-                for (int w = 0; w < kDecNCW; ++w) sum += red[w * G * D + e] * wsc[w * G + h];
+                for (int w = 0; w < kDecNGW; ++w) sum += red[w * G * D + e] * wsc[w * G + h];
                 outp[e] = Elem<T>::from_f(sum * linv[h]);
             }
         } else {
@@ -684,7 +695,7 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
             const int h = e / D;
             float sum = 0.f;
 #pragma unroll
-            for (int w = 0; w < kDecNCW; ++w) sum += red[w * G * D + e] * wsc[w * G + h];
+            for (int w = 0; w < kDecNGW; ++w) sum += red[w * G * D + e] * wsc[w * G + h];
             const int owner = e / per, loc = e - owner * per;
             dsmem_st_f32(dsmem_addr(&orecv[c * per + loc], (uint32_t)owner), sum);
         }
