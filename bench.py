@@ -382,6 +382,7 @@ def bench_gpu(args):
         e1.record(stream)
     torch.cuda.synchronize()
     launches = cache.kernel_launches() - launches0
+    dec_cfg = cache.last_decode_config()
     vrows = cache.element_rows() - vrows0 if elem else 0
     if elem:
         # HiKV Stage II reads whole K rows but only the V rows some head kept
@@ -540,6 +541,7 @@ def bench_gpu(args):
         "e2e": ({"value": Ke / (e2e_ms / 1e3), "unit": "steps/s", "h2d_bytes_per_step": int(h2d),
                  "d2h_bytes_per_step": int(d2h), "steps": Ke} if Ke > 0 else None),
         "gpu_launches": launches,
+        "decode_launch": dec_cfg,
         "three_call_path": three,
         "stage2_v_rows_read_fraction": (vrows / max(1, kv_bytes // (2 * w.d * w.elem_bytes))) if elem else None,
         "per_layer_launches": per_layer,

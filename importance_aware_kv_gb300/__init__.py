@@ -30,7 +30,8 @@ ABI_FUNCTIONS = ("hikv_create_cache", "hikv_destroy_cache", "hikv_append", "hikv
                  "hikv_decode_step", "hikv_evict", "hikv_gather_retained", "hikv_get_lengths",
                  "hikv_device_status", "hikv_last_error", "hikv_score_window_noalloc",
                  "hikv_decode_step_fused", "hikv_kernel_launches", "hikv_budgets_pyramid",
-                 "hikv_budgets_duo", "hikv_selftest_timeout", "hikv_element_rows")
+                 "hikv_budgets_duo", "hikv_selftest_timeout", "hikv_element_rows",
+                 "hikv_last_decode_config")
 
 
 class HikvError(RuntimeError):
@@ -72,6 +73,7 @@ def _load():
         "hikv_decode_step_fused": ([P, I32, I32, P, P, P, P, I32, P], S),
         "hikv_kernel_launches": ([P], ctypes.c_int64),
         "hikv_element_rows": ([P, ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
+        "hikv_last_decode_config": ([P, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
         "hikv_budgets_pyramid": ([I32, I32, I32, I32, I32, P], S),
         "hikv_budgets_duo": ([I32, I32, P, I32, I32, I32, P], S),
         "hikv_selftest_timeout": ([P, I32, P], S),
@@ -335,6 +337,12 @@ class Cache:
     def kernel_launches(self) -> int:
         """Kernels this cache has launched so far (host counter)."""
         return int(_lib.hikv_kernel_launches(self.h))
+
+    def last_decode_config(self) -> dict:
+        """Cluster size, clusters and logits placement of the latest decode launch."""
+        out = (ctypes.c_int32 * 3)()
+        _check(_lib.hikv_last_decode_config(self.h, out))
+        return {"cluster_size": out[0], "clusters": out[1], "smem_logits": bool(out[2])}
 
     def element_rows(self) -> int:
         """V rows the HiKV Stage II decode steps have read so far (synchronous)."""

@@ -131,6 +131,7 @@ struct hikv_cache {
     int64_t pages_in_use = 0;
     int cs_override = 0;                // HIKV_DECODE_CS (tuning)
     int64_t launches = 0;               // kernels launched through this cache
+    int32_t last_cs = 0, last_clusters = 0, last_smem_logits = 0;   // the latest cluster launch
     int pool_k = 0;                     // SnapKV pooling of the prompt scores (> 1: on)
     // HiKV Stage II element-level decode (elem > 0: on)
     int elem = 0;
@@ -557,8 +558,11 @@ hikv_status launch_clusters(hikv_cache* c, int32_t layer0, int32_t nl, const std
     // ceil(units / clusters) of them; ragged ones are dealt by LPT, whose
     // busiest cluster is about max(average load, largest unit).  The logits
     // of a chunk too large for shared memory go to the global buffer, when
-    // there is one.
-    constexpr int64_t kUnitCostTokens = 190;
+    // there is one.  With G = 8 the kernel's two head groups stream a CTA's
+    // tokens faster, so the same per-unit work weighs more tokens (refit on
+    // the 70B workload, 640 units of 4097 tokens: cluster size 2 took 466 us,
+    // 3 496 us, 4 487 us, 8 552 us).
+    const int64_t kUnitCostTokens = c->G == 8 ? 400 : 190;
     int cs = 1;
     if (c->cs_override > 0) {
         cs = std::min(c->cs_override, kMaxCS);
@@ -655,6 +659,9 @@ hikv_status launch_clusters(hikv_cache* c, int32_t layer0, int32_t nl, const std
     a.new_v = (const uint8_t*)new_v;
     cudaError_t e = launch_decode(a, c->tmap, c->dtype, c->d, c->G, smem_path, smem, (cudaStream_t)stream);
     c->launches += 1;
+    c->last_cs = cs;
+    c->last_clusters = ncl;
+    c->last_smem_logits = smem_path ? 1 : 0;
     if (e != cudaSuccess) return cuda_fail(e, who);
     return HIKV_OK;
 }
@@ -912,6 +919,15 @@ hikv_status hikv_gather_retained(hikv_cache* c, int32_t layer0, int32_t nl, int3
     cudaError_t e = launch_gather(a, (cudaStream_t)stream);
     c->launches += 1;
     if (e != cudaSuccess) return cuda_fail(e, "gather: launch");
+    return HIKV_OK;
+}
+
+hikv_status hikv_last_decode_config(const hikv_cache* c, int32_t* out_host) {
+    g_err.clear();
+    if (!c || !out_host) return fail(HIKV_ERR_INVALID_ARG, "last_decode_config: null cache or output");
+    out_host[0] = c->last_cs;
+    out_host[1] = c->last_clusters;
+    out_host[2] = c->last_smem_logits;
     return HIKV_OK;
 }
 

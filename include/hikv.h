@@ -185,6 +185,13 @@ hikv_status hikv_gather_retained(hikv_cache* cache, int32_t layer0, int32_t nlay
                                  int32_t* lengths, int32_t* positions, float* importance,
                                  void* k_out, void* v_out, hikv_stream_t stream);
 
+/* Diagnostic: the configuration of the latest cluster-kernel decode launch
+ * of this cache, chosen by the host's cost model.  out_host[3]: cluster size
+ * (CTAs per unit), clusters launched, 1 if the logits stayed in shared
+ * memory (0: the global buffer).  Zeros before the first launch.  Host only.
+ * Errors: INVALID_ARG. */
+hikv_status hikv_last_decode_config(const hikv_cache* cache, int32_t* out_host);
+
 /* Diagnostic: the number of V rows the element-level (HiKV Stage II) decode
  * steps of this cache have read since it was created -- rows that at least
  * one query head of the unit's group kept (HiKV sec. III-C: V is loaded only
