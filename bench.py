@@ -39,10 +39,16 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "k_decode_llama3_8b_traffic.json")
 
 
 def kernel_sha() -> str:
+    """Hash of the decode kernel's code (comments and whitespace removed, so
+    an edited comment keeps the traffic measured on the same code valid)."""
+    import re
     h = hashlib.sha256()
     for p in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, p), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, p), encoding="utf-8") as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -22,7 +22,10 @@
 //   consumer warps  tile i of a unit belongs to warp i % 4, which keeps a
 //                   private online softmax (reference m_w, sum l_w,
 //                   unnormalised O_w; m_w follows the running max lazily,
-//                   moving only when a logit exceeds it by 2^8):
+//                   moving only when a logit exceeds it by 2^8).  With G = 8
+//                   there are two such groups of four warps: both take tile
+//                   i, one for heads 0-3 and one for heads 4-7, and a stage
+//                   is released once each group's warp has arrived:
 //     q.k   lane (row = lane % 16, half = lane / 16) owns half a K row: the
 //           swizzle makes those 16-byte reads conflict-free and lets q be a
 //           shared-memory broadcast; packed f32x2 FMAs, one shuffle joins the
