@@ -535,22 +535,12 @@ void lpt_assign(const std::vector<int32_t>& units, const std::vector<int64_t>& l
 
 uint64_t fnv_mix(uint64_t h, uint64_t x) { return (h ^ x) * 1099511628211ull; }
 
-// The cluster kernel over all units of the range (equal budgets: identity
-// order) or over `subset` (ragged: largest first, dealt by LPT).
-hikv_status launch_clusters(hikv_cache* c, int32_t layer0, int32_t nl, const std::vector<int32_t>* subset,
-                            bool uni_len, bool uni_b, bool uni_np, const void* q, void* out, int fused,
-                            int evict, const void* new_k, const void* new_v, hikv_stream_t stream,
-                            const char* who) {
-    const int u0 = layer0 * c->per_layer;
-    const int nu = subset ? (int)subset->size() : nl * c->per_layer;
-    auto unit_at = [&](int i) { return subset ? (*subset)[i] : u0 + i; };
-    int maxn = 0;
-    int64_t total = 0;
-    for (int i = 0; i < nu; ++i) {
-        const int n = c->len[unit_at(i)] + fused;
-        maxn = std::max(maxn, n);
-        total += n;
-    }
+// The fixed per-unit work of the decode kernel, in tokens of streaming.
+int64_t unit_cost_tokens(const hikv_cache* c) { return c->G == 8 ? 400 : 190; }
+
+// CTAs per unit for a launch of nu units, the longest maxn tokens, total
+// tokens in all (ragged: dealt by LPT).
+int choose_cluster_size(const hikv_cache* c, int nu, int maxn, int64_t total, bool ragged) {
     // CTAs per unit (cluster size cs) by a cost model of the busiest cluster:
     // tokens per CTA plus a fixed per-unit cost (exchanges, importance pass,
     // victim) worth kUnitCostTokens tokens, a fit to the measured decode
@@ -562,7 +552,7 @@ hikv_status launch_clusters(hikv_cache* c, int32_t layer0, int32_t nl, const std
     // tokens faster, so the same per-unit work weighs more tokens (refit on
     // the 70B workload, 640 units of 4097 tokens: cluster size 2 took 466 us,
     // 3 496 us, 4 487 us, 8 552 us).
-    const int64_t kUnitCostTokens = c->G == 8 ? 400 : 190;
+    const int64_t kUnitCostTokens = unit_cost_tokens(c);
     int cs = 1;
     if (c->cs_override > 0) {
         cs = std::min(c->cs_override, kMaxCS);
@@ -578,7 +568,7 @@ hikv_status launch_clusters(hikv_cache* c, int32_t layer0, int32_t nl, const std
             const int active = decode_active_clusters(c->dtype, c->d, c->G, sp, k, smem);
             if (active > 0) ncl = std::min(ncl, active);
             int64_t cost;
-            if (!subset) {
+            if (!ragged) {
                 cost = (int64_t)ceil_div(nu, ncl) * (ceil_div(maxn, k) + kUnitCostTokens);
             } else {
                 const int64_t sum = (total + (int64_t)nu * (k - 1)) / k + (int64_t)nu * kUnitCostTokens;
@@ -590,6 +580,38 @@ hikv_status launch_clusters(hikv_cache* c, int32_t layer0, int32_t nl, const std
             }
         }
     }
+    return cs;
+}
+
+// Clusters resident at once for cluster size cs (the persistent grid).
+int resident_clusters(const hikv_cache* c, int nu, int maxn, int cs) {
+    const int chunk = dec_chunk_max(maxn, cs);
+    const bool sp = chunk <= c->max_smem_chunk;
+    const size_t smem = decode_smem_bytes(c->dtype, c->d, c->G, sp, sp ? chunk : 0);
+    int ncl = std::max(1, std::min(nu, (c->dec_occ * c->sm_count) / cs));
+    const int active = decode_active_clusters(c->dtype, c->d, c->G, sp, cs, smem);
+    if (active > 0) ncl = std::min(ncl, active);
+    return ncl;
+}
+
+// The cluster kernel over all units of the range (equal budgets: identity
+// order; range_count >= 0 limits it to units [range_first, + range_count) of
+// the range) or over `subset` (ragged: largest first, dealt by LPT).
+hikv_status launch_clusters(hikv_cache* c, int32_t layer0, int32_t nl, const std::vector<int32_t>* subset,
+                            bool uni_len, bool uni_b, bool uni_np, const void* q, void* out, int fused,
+                            int evict, const void* new_k, const void* new_v, hikv_stream_t stream,
+                            const char* who, int range_first = 0, int range_count = -1, int force_cs = 0) {
+    const int u0 = layer0 * c->per_layer + (subset ? 0 : range_first);
+    const int nu = subset ? (int)subset->size() : (range_count >= 0 ? range_count : nl * c->per_layer);
+    auto unit_at = [&](int i) { return subset ? (*subset)[i] : u0 + i; };
+    int maxn = 0;
+    int64_t total = 0;
+    for (int i = 0; i < nu; ++i) {
+        const int n = c->len[unit_at(i)] + fused;
+        maxn = std::max(maxn, n);
+        total += n;
+    }
+    int cs = force_cs > 0 ? force_cs : choose_cluster_size(c, nu, maxn, total, subset != nullptr);
     cs = std::min(cs, std::max(1, maxn));
     const int chunk = dec_chunk_max(maxn, cs);   // most slots a CTA holds
     const bool smem_path = chunk <= c->max_smem_chunk;
@@ -617,7 +639,7 @@ hikv_status launch_clusters(hikv_cache* c, int32_t layer0, int32_t nl, const std
         d_assign_off = c->d_assign + c->units + (size_t)layer0 * (c->dec_occ * c->sm_count + 1);
         if (key != c->asg_key[layer0]) {
             std::vector<int64_t> load(nu);
-            for (int i = 0; i < nu; ++i) load[i] = ceil_div(c->len[(*subset)[i]] + fused, cs) + kUnitCostTokens;
+            for (int i = 0; i < nu; ++i) load[i] = ceil_div(c->len[(*subset)[i]] + fused, cs) + unit_cost_tokens(c);
             lpt_assign(*subset, load, ncl, c->asg);
             // pageable sources: the copies are staged before the calls return
             cudaError_t e = cudaMemcpyAsync(const_cast<int32_t*>(d_assign), c->asg.data(), nu * sizeof(int32_t),
@@ -734,9 +756,31 @@ hikv_status launch_decode_call(hikv_cache* c, int32_t layer0, int32_t nl, const 
         uni_b &= c->budget_unit[u] == c->budget_unit[u0];
         uni_np &= c->next_pos[u] == c->next_pos[u0];
     }
-    if (uni_b)
+    if (uni_b) {
+        // Equal units go round-robin over the resident clusters.  When the
+        // last round would keep at most half of them busy, the full rounds go
+        // in one launch and the rest in a second one, each with the cluster
+        // size the cost model picks for it, so the rest spreads over the
+        // whole GPU instead of a few clusters (70B workload, 640 units: 467 ->
+        // 434 us as 608 units at cluster size 1 plus 32 at size 8; forcing
+        // size 2 on the 608, the size the split was counted with, took 451).
+        if (uni_len && c->cs_override <= 0) {
+            const int n = c->len[u0] + fused;
+            const int cs = choose_cluster_size(c, nu, n, (int64_t)n * nu, false);
+            const int ncl = resident_clusters(c, nu, n, cs);
+            const int rem = nu % ncl;
+            if (nu > ncl && rem > 0 && 2 * rem <= ncl) {
+                const int full = nu - rem;
+                hikv_status st = launch_clusters(c, layer0, nl, nullptr, uni_len, uni_b, uni_np, q, out, fused, evict,
+                                                 new_k, new_v, stream, who, 0, full);
+                if (st != HIKV_OK) return st;
+                return launch_clusters(c, layer0, nl, nullptr, uni_len, uni_b, uni_np, q, out, fused, evict, new_k,
+                                       new_v, stream, who, full, rem);
+            }
+        }
         return launch_clusters(c, layer0, nl, nullptr, uni_len, uni_b, uni_np, q, out, fused, evict, new_k, new_v,
                                stream, who);
+    }
     std::vector<int32_t> units(nu);
     std::iota(units.begin(), units.end(), u0);
     std::stable_sort(units.begin(), units.end(), [&](int x, int y) { return c->len[x] > c->len[y]; });

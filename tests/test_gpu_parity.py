@@ -126,6 +126,13 @@ def test_warp_per_unit_group_sizes_and_dtypes(shape):
 
 
 @FUSED
+def test_more_units_than_resident_clusters(fused):
+    # 404 equal units: more than one round of clusters, so the host may launch
+    # the full rounds and the remaining units separately
+    _run(SMALL.with_(layers=1, batch=101, hq=8, hkv=4, steps=6), fused=fused)
+
+
+@FUSED
 def test_page_size_variants(fused):
     # 16-token pages: the cache grows a page every 16 steps before the
     # budget is reached, steps the fused call runs as three calls
