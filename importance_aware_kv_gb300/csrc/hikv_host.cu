@@ -600,7 +600,7 @@ int resident_clusters(const hikv_cache* c, int nu, int maxn, int cs) {
 hikv_status launch_clusters(hikv_cache* c, int32_t layer0, int32_t nl, const std::vector<int32_t>* subset,
                             bool uni_len, bool uni_b, bool uni_np, const void* q, void* out, int fused,
                             int evict, const void* new_k, const void* new_v, hikv_stream_t stream,
-                            const char* who, int range_first = 0, int range_count = -1, int force_cs = 0) {
+                            const char* who, int range_first = 0, int range_count = -1) {
     const int u0 = layer0 * c->per_layer + (subset ? 0 : range_first);
     const int nu = subset ? (int)subset->size() : (range_count >= 0 ? range_count : nl * c->per_layer);
     auto unit_at = [&](int i) { return subset ? (*subset)[i] : u0 + i; };
@@ -611,7 +611,7 @@ hikv_status launch_clusters(hikv_cache* c, int32_t layer0, int32_t nl, const std
         maxn = std::max(maxn, n);
         total += n;
     }
-    int cs = force_cs > 0 ? force_cs : choose_cluster_size(c, nu, maxn, total, subset != nullptr);
+    int cs = choose_cluster_size(c, nu, maxn, total, subset != nullptr);
     cs = std::min(cs, std::max(1, maxn));
     const int chunk = dec_chunk_max(maxn, cs);   // most slots a CTA holds
     const bool smem_path = chunk <= c->max_smem_chunk;
