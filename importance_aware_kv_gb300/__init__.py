@@ -338,11 +338,13 @@ class Cache:
         """Kernels this cache has launched so far (host counter)."""
         return int(_lib.hikv_kernel_launches(self.h))
 
-    def last_decode_config(self) -> dict:
-        """Cluster size, clusters and logits placement of the latest decode launch."""
-        out = (ctypes.c_int32 * 3)()
+    def last_decode_config(self) -> list:
+        """The cluster-kernel launches of the latest decode call: units,
+        cluster size, clusters and logits placement of each."""
+        out = (ctypes.c_int32 * 8)()
         _check(_lib.hikv_last_decode_config(self.h, out))
-        return {"cluster_size": out[0], "clusters": out[1], "smem_logits": bool(out[2])}
+        return [{"units": out[4 * i], "cluster_size": out[4 * i + 1], "clusters": out[4 * i + 2],
+                 "smem_logits": bool(out[4 * i + 3])} for i in range(2) if out[4 * i + 1] > 0]
 
     def element_rows(self) -> int:
         """V rows the HiKV Stage II decode steps have read so far (synchronous)."""

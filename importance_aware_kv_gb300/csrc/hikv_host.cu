@@ -131,7 +131,10 @@ struct hikv_cache {
     int64_t pages_in_use = 0;
     int cs_override = 0;                // HIKV_DECODE_CS (tuning)
     int64_t launches = 0;               // kernels launched through this cache
-    int32_t last_cs = 0, last_clusters = 0, last_smem_logits = 0;   // the latest cluster launch
+    // the cluster launches of the latest decode call (at most two): units,
+    // cluster size, clusters, logits in shared memory
+    int32_t last_cfg[2][4] = {};
+    int last_ncfg = 0;
     int pool_k = 0;                     // SnapKV pooling of the prompt scores (> 1: on)
     // HiKV Stage II element-level decode (elem > 0: on)
     int elem = 0;
@@ -681,9 +684,13 @@ hikv_status launch_clusters(hikv_cache* c, int32_t layer0, int32_t nl, const std
     a.new_v = (const uint8_t*)new_v;
     cudaError_t e = launch_decode(a, c->tmap, c->dtype, c->d, c->G, smem_path, smem, (cudaStream_t)stream);
     c->launches += 1;
-    c->last_cs = cs;
-    c->last_clusters = ncl;
-    c->last_smem_logits = smem_path ? 1 : 0;
+    if (c->last_ncfg < 2) {
+        int32_t* r = c->last_cfg[c->last_ncfg++];
+        r[0] = nu;
+        r[1] = cs;
+        r[2] = ncl;
+        r[3] = smem_path ? 1 : 0;
+    }
     if (e != cudaSuccess) return cuda_fail(e, who);
     return HIKV_OK;
 }
@@ -748,6 +755,7 @@ hikv_status launch_decode_call(hikv_cache* c, int32_t layer0, int32_t nl, const 
                                int fused, int evict, const void* new_k, const void* new_v,
                                hikv_stream_t stream, const char* who) {
     const int u0 = layer0 * c->per_layer, nu = nl * c->per_layer;
+    c->last_ncfg = 0;
     bool uni_len = true, uni_b = true, uni_np = true;
     for (int u = u0; u < u0 + nu; ++u) {
         const int n = c->len[u] + fused;
@@ -969,9 +977,8 @@ hikv_status hikv_gather_retained(hikv_cache* c, int32_t layer0, int32_t nl, int3
 hikv_status hikv_last_decode_config(const hikv_cache* c, int32_t* out_host) {
     g_err.clear();
     if (!c || !out_host) return fail(HIKV_ERR_INVALID_ARG, "last_decode_config: null cache or output");
-    out_host[0] = c->last_cs;
-    out_host[1] = c->last_clusters;
-    out_host[2] = c->last_smem_logits;
+    for (int i = 0; i < 2; ++i)
+        for (int j = 0; j < 4; ++j) out_host[i * 4 + j] = i < c->last_ncfg ? c->last_cfg[i][j] : 0;
     return HIKV_OK;
 }
 

@@ -185,11 +185,12 @@ hikv_status hikv_gather_retained(hikv_cache* cache, int32_t layer0, int32_t nlay
                                  int32_t* lengths, int32_t* positions, float* importance,
                                  void* k_out, void* v_out, hikv_stream_t stream);
 
-/* Diagnostic: the configuration of the latest cluster-kernel decode launch
- * of this cache, chosen by the host's cost model.  out_host[3]: cluster size
- * (CTAs per unit), clusters launched, 1 if the logits stayed in shared
- * memory (0: the global buffer).  Zeros before the first launch.  Host only.
- * Errors: INVALID_ARG. */
+/* Diagnostic: the cluster-kernel launches of the latest decode call of this
+ * cache, as the host's cost model configured them (a call of equal units
+ * whose last round of clusters would be at most half busy runs as two
+ * launches).  out_host[8]: per launch (up to two, zeros past the last)
+ * units, cluster size (CTAs per unit), clusters, and 1 if the logits stayed
+ * in shared memory (0: the global buffer).  Host only.  Errors: INVALID_ARG. */
 hikv_status hikv_last_decode_config(const hikv_cache* cache, int32_t* out_host);
 
 /* Diagnostic: the number of V rows the element-level (HiKV Stage II) decode
