@@ -353,7 +353,8 @@ class Cache:
         return int(r.value)
 
     def step(self, k, v, q, out, evict=True, layer0=0, stream=None):
-        """append + decode_step (+ evict) as one call (one launch in steady state).
+        """append + decode_step (+ evict) as one call (fused into the attention
+        kernel in the steady state).
         The per-step call of a decode loop: each tensor is checked once."""
         import torch
         nl = self._layers(q, layer0)

@@ -156,10 +156,13 @@ hikv_status hikv_decode_step(hikv_cache* cache, int32_t layer0, int32_t nlayers,
  * k, v: [nlayers][batch][Hkv][1][d]) + hikv_decode_step (q, out as there)
  * and, with evict != 0, hikv_evict -- same results.  When every unit's new
  * slot already has its page and no unit needs more than one eviction (the
- * steady state once a unit reached its budget) it is a single kernel launch:
- * the appended rows enter the cache inside the attention kernel and the
- * evicted slot is refilled with the new token there.  Otherwise it runs the
- * three calls.  k and v must be 16-byte aligned (HIKV_ERR_INVALID_ARG
+ * steady state once a unit reached its budget) the appended rows enter the
+ * cache inside the attention kernel and the evicted slot is refilled with
+ * the new token there: one kernel launch (two when the call's equal units
+ * need more rounds of clusters than one and the last round would be at most
+ * half busy, or when ragged units split between the cluster and the
+ * warp-per-unit kernels; with an element_budget, the element-level
+ * kernels).  Otherwise it runs the three calls.  k and v must be 16-byte aligned (HIKV_ERR_INVALID_ARG
  * otherwise).  Errors: as the three calls. */
 hikv_status hikv_decode_step_fused(hikv_cache* cache, int32_t layer0, int32_t nlayers,
                                    const void* k, const void* v, const void* q, void* out,
