@@ -30,6 +30,9 @@
 //                 every retained token's importance (HiKV Stage I mode: the
 //                 recent bank only) and records the eviction victim, as the
 //                 exact decode kernel does.
+// In a fused step (append + decode + evict in one call) k_elem_order first
+// writes the new token into its slot, and the merging CTA moves it into the
+// victim's slot when the unit is cut, so the step is these two launches.
 //
 // The K side reads whole rows: the pool stores token-major rows, so B2 of the
 // d dimensions of a row lie in nearly every 32-byte sector (DRAM's unit), and
