@@ -52,6 +52,8 @@ def _load():
                 "ora_num_threads": ([_P, _I], _I),
                 "ora_append": ([_P, _I, _I, _I, _P, _P], _I),
                 "ora_score_window": ([_P, _I, _I, _I, _P], _I),
+                "ora_score_band": ([_P, _I, _I, _I, _P], _I),
+                "ora_stage2_alternatives": ([_P, _I, _I, _I, _P, _I], _I),
                 "ora_pool_importance": ([_P, _I, _I, _I], _I),
                 "ora_set_recent_only": ([_P, _I], _I),
                 "ora_set_element_budget": ([_P, _I], _I),
@@ -128,6 +130,16 @@ class Oracle:
         nl, nq = q.shape[0], q.shape[3]
         assert self.lib.ora_score_window(self.h, layer0, nl, nq, _ptr(q)) == 0
 
+    def score_band(self, layer0, q, band):
+        """HiKV prefill initialisation: q [nl][B][Hq][n][d] holds the queries
+        of every held position 0..n-1; each token's score grows by its causal
+        attention column summed over the band of queries from its position."""
+        q = _f32(q)
+        nl = q.shape[0]
+        rc = self.lib.ora_score_band(self.h, layer0, nl, int(band), _ptr(q))
+        if rc:
+            raise ValueError(f"oracle: score_band failed ({rc})")
+
     def set_recent_only(self, on=True):
         """HiKV Stage I: decode steps add mass only to the recent bank."""
         assert self.lib.ora_set_recent_only(self.h, 1 if on else 0) == 0
@@ -139,11 +151,21 @@ class Oracle:
             raise ValueError(f"oracle: element budget {b2} outside [0, {self.d}]")
 
     def stage2_near_ties(self, layer0, nl):
-        """[nl][B][Hq] bool: heads whose latest Stage II chunk selection was
-        decided by less than 1e-4 (relative) in p."""
+        """[nl][B][Hq] uint8 for the latest Stage II step: 0 where every chunk
+        selection is certain under float32 rounding of the logits, 1 where
+        some is not (see stage2_alternatives), 2 where too many selections
+        were admissible to list."""
         f = np.zeros((nl, self.B, self.Hq), np.uint8)
         assert self.lib.ora_stage2_near_ties(self.h, layer0, nl, _ptr(f)) == 0
-        return f.astype(bool)
+        return f
+
+    def stage2_alternatives(self, layer, b, head, max_alts=4096):
+        """[count][d] float32: every output of query head `head` that a
+        selection admissible under float32 rounding gives (the exact one
+        included); None when there were too many."""
+        out = np.empty((max_alts, self.d), np.float32)
+        n = self.lib.ora_stage2_alternatives(self.h, layer, b, head, _ptr(out), max_alts)
+        return None if n < 0 else out[:n].copy()
 
     def pool_importance(self, layer0, nl, kpool):
         """SnapKV: each score becomes the max over the next kpool positions."""

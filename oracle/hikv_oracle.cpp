@@ -35,6 +35,12 @@
 //                   window the lowest score goes, ties taking the newest,
 //                   which is HiKV's "promote the ejected token only if its
 //                   score exceeds the minimum of the important bank".
+//  * band score     HiKV's own prefill initialisation (HiKV sec. III-D): each
+//                   prompt token's score is its causal attention column
+//                   summed over the band of queries from its own position
+//                   onward, IS(l) = sum_{k < band} P_{l+k}[l] (the IS
+//                   definition of sec. III-B, with band = B_I / 2), queries
+//                   past the prompt contributing nothing.
 //  * pooled score   SnapKV variant of the prefill score: each token's score
 //                   becomes the largest window score of the k_pool positions
 //                   starting at its own, S_pooled[i] = max_{0<=m<k} A_obs[i+m]
@@ -87,7 +93,11 @@ struct Oracle {
     int nthreads;
     int recent_only = 0;             // HiKV Stage I: accumulate in the recent bank only
     int elem = 0;                    // HiKV Stage II element budget B2 (0: off)
-    std::vector<uint8_t> near_tie;   // [L*B*Hq]: Stage II chunk selection decided by < 1e-4
+    // [L*B*Hq], latest Stage II decode step: 0 = the chunk selections are
+    // certain, 1 = near ties (alts holds every admissible output), 2 = near
+    // ties with too many admissible outputs to list
+    std::vector<uint8_t> near_tie;
+    std::vector<std::vector<float>> alts;   // [L*B*Hq][count * d]
     std::vector<int32_t> budget;     // [L * Hkv]
     std::vector<Unit> units;         // [L][B][Hkv]
     int unit_index(int l, int b, int g) const { return (l * B + b) * Hkv + g; }
@@ -152,13 +162,29 @@ void attend(const Oracle& O, const std::vector<Entry>& e, const float* q,
     }
 }
 
+// One chunk of P whose selection a float32 evaluation of the logits could
+// decide differently: `sure` entries are kept under every such evaluation,
+// `unsure` entries may or may not be, and exactly `pick` of them are.
+struct UnsureChunk {
+    std::vector<size_t> unsure;
+    int pick = 0;
+};
+
 // HiKV Stage II attention of one query head over every entry of `e` (which is
 // in position order).  Writes the whole softmax P into p and the output of
-// the chunk-selected entries into o; sets *near_tie when the B2-th and the
-// (B2+1)-th largest p of some chunk differ by less than 1e-4 of the former
-// (a selection that the rounding of the logits could flip).
+// the chunk-selected entries into o.
+//
+// Near ties.  A kernel selects a chunk's largest p by comparing its float32
+// logits.  The rounding error of a float32 dot product of the B2 selected
+// terms is at most (B2 + 2) * 2^-24 * scale * sum_c |q_c k_jc| (B2 - 1
+// additions, the scaling of q, one more for the conversion), doubled here
+// for margin.  Where an entry kept by the exact (double) order and one
+// dropped by it are closer than their two bounds, either could win in
+// float32; every chunk with such pairs is reported in `unsure` (the entries
+// in doubt and how many of them are kept), so that a caller can enumerate
+// every selection a correct float32 kernel may make.
 void attend_stage2(const Oracle& O, const std::vector<Entry>& e, const float* q,
-                   std::vector<double>& p, double* o, bool* near_tie) {
+                   std::vector<double>& p, double* o, std::vector<UnsureChunk>* unsure) {
     const int d = O.d, B2 = O.elem;
     const size_t n = e.size();
     // K side: the B2 dimensions of largest |q|, the lower index first on ties
@@ -168,12 +194,17 @@ void attend_stage2(const Oracle& O, const std::vector<Entry>& e, const float* q,
                      [&](int a, int b) { return std::fabs(q[a]) > std::fabs(q[b]); });
     dims.resize(B2);
     std::sort(dims.begin(), dims.end());
-    std::vector<double> s(n);
+    std::vector<double> s(n), err(n);
     double m = -INFINITY;
+    const double ulp = std::ldexp(1.0, -24);
     for (size_t j = 0; j < n; ++j) {
-        double acc = 0.0;
-        for (int c : dims) acc += (double)q[c] * (double)e[j].k[c];
+        double acc = 0.0, mag = 0.0;
+        for (int c : dims) {
+            acc += (double)q[c] * (double)e[j].k[c];
+            mag += std::fabs((double)q[c] * (double)e[j].k[c]);
+        }
         s[j] = O.scale * acc;
+        err[j] = 2.0 * (B2 + 2) * ulp * O.scale * mag;
         m = std::max(m, s[j]);
     }
     double l = 0.0;
@@ -192,14 +223,84 @@ void attend_stage2(const Oracle& O, const std::vector<Entry>& e, const float* q,
         for (size_t j = c0; j < c1; ++j) idx.push_back(j);
         std::stable_sort(idx.begin(), idx.end(), [&](size_t a, size_t b) { return p[a] > p[b]; });
         for (int r = 0; r < B2; ++r) keep[idx[r]] = 1;
-        const double last = p[idx[B2 - 1]], next = p[idx[B2]];
-        if (last - next < 1e-4 * last) *near_tie = true;
+        if (unsure) {
+            // lowest a kept entry could read, highest a dropped one could read
+            double kept_lo = INFINITY, drop_hi = -INFINITY;
+            for (int r = 0; r < B2; ++r) kept_lo = std::min(kept_lo, s[idx[r]] - err[idx[r]]);
+            for (size_t r = B2; r < idx.size(); ++r) drop_hi = std::max(drop_hi, s[idx[r]] + err[idx[r]]);
+            UnsureChunk uc;
+            for (size_t r = 0; r < idx.size(); ++r) {
+                const size_t j = idx[r];
+                const bool kept = (int)r < B2;
+                if (kept ? (s[j] - err[j] <= drop_hi) : (s[j] + err[j] >= kept_lo)) {
+                    uc.unsure.push_back(j);
+                    if (kept) ++uc.pick;
+                }
+            }
+            if (uc.pick > 0 && uc.unsure.size() > (size_t)uc.pick) unsure->push_back(std::move(uc));
+        }
     }
     for (int c = 0; c < d; ++c) o[c] = 0.0;
     for (size_t j = 0; j < n; ++j) {
         if (!keep[j]) continue;
         for (int c = 0; c < d; ++c) o[c] += p[j] * (double)e[j].v[c];
     }
+}
+
+// Every output the selections allowed by `chunks` give: the exact output o
+// with, in each unsure chunk, its `pick` kept entries replaced by any `pick`
+// of its unsure entries.  Each alternative is rounded to the output type and
+// appended to alts ([count][d]).  Returns false when there would be more
+// than max_alts alternatives.
+bool stage2_alternatives(const Oracle& O, const std::vector<Entry>& e, const std::vector<double>& p,
+                         const double* o, const std::vector<UnsureChunk>& chunks, size_t max_alts,
+                         std::vector<float>& alts) {
+    const int d = O.d;
+    // the exact selection's output minus every unsure kept entry
+    std::vector<double> base(o, o + d);
+    // per chunk: the index sets to try (combinations of `pick` of `unsure`)
+    std::vector<std::vector<std::vector<size_t>>> choices;
+    size_t total = 1;
+    for (const auto& uc : chunks) {
+        const std::vector<size_t>& un = uc.unsure;
+        // the exact selection keeps the `pick` unsure entries of largest p
+        std::vector<size_t> by_p(un);
+        std::stable_sort(by_p.begin(), by_p.end(), [&](size_t a, size_t b) { return p[a] > p[b]; });
+        for (int r = 0; r < uc.pick; ++r)
+            for (int c = 0; c < d; ++c) base[c] -= p[by_p[r]] * (double)e[by_p[r]].v[c];
+        std::vector<std::vector<size_t>> combos;
+        std::vector<int> sel(uc.pick);
+        for (int r = 0; r < uc.pick; ++r) sel[r] = r;
+        const int m = (int)un.size();
+        while (true) {
+            std::vector<size_t> cset;
+            for (int r : sel) cset.push_back(un[r]);
+            combos.push_back(std::move(cset));
+            if (combos.size() > max_alts) return false;
+            int r = uc.pick - 1;
+            while (r >= 0 && sel[r] == m - uc.pick + r) --r;
+            if (r < 0) break;
+            ++sel[r];
+            for (int t = r + 1; t < uc.pick; ++t) sel[t] = sel[t - 1] + 1;
+        }
+        total *= combos.size();
+        if (total > max_alts) return false;
+        choices.push_back(std::move(combos));
+    }
+    std::vector<size_t> ix(choices.size(), 0);
+    std::vector<double> acc(d);
+    for (size_t a = 0; a < total; ++a) {
+        acc = base;
+        for (size_t k = 0; k < choices.size(); ++k)
+            for (size_t j : choices[k][ix[k]])
+                for (int c = 0; c < d; ++c) acc[c] += p[j] * (double)e[j].v[c];
+        for (int c = 0; c < d; ++c) alts.push_back(O.out_bf16 ? round_bf16(acc[c]) : (float)acc[c]);
+        for (size_t k = 0; k < choices.size(); ++k) {   // next index of the mixed-radix counter
+            if (++ix[k] < choices[k].size()) break;
+            ix[k] = 0;
+        }
+    }
+    return true;
 }
 
 bool range_ok(const Oracle* O, int layer0, int nl) {
@@ -222,6 +323,7 @@ void* ora_create(int L, int B, int Hq, int Hkv, int d, int S, int W,
     O->budget.assign(budgets, budgets + L * Hkv);
     O->units.resize((size_t)L * B * Hkv);
     O->near_tie.assign((size_t)L * B * Hq, 0);
+    O->alts.assign((size_t)L * B * Hq, {});
     return O;
 }
 
@@ -288,6 +390,47 @@ int ora_score_window(void* h, int layer0, int nl, int nq, const float* q) {
     return 0;
 }
 
+// HiKV prefill initialisation (HiKV sec. III-D, with the IS definition of
+// sec. III-B): every prompt token l gets IS(l) = sum over the band of queries
+// i = l .. l + band - 1 (those that exist, i < n) of P_i[l], P_i being query
+// i's causal softmax over the tokens at positions <= i, summed over the G
+// query heads of the group.  q [nl][B][Hq][n][d] holds the queries of every
+// held position 0..n-1; the unit must hold exactly those positions (a prompt
+// not yet cut).  The band sum is formed in double and rounded once; the
+// running score is a float32 add.
+int ora_score_band(void* h, int layer0, int nl, int band, const float* q) {
+    Oracle* O = (Oracle*)h;
+    if (!range_ok(O, layer0, nl) || band < 1) return 1;
+    int per_layer = O->B * O->Hkv;
+    const int n = (int)O->units[layer0 * per_layer].e.size();
+    for (int i = 0; i < nl * per_layer; ++i) {
+        const Unit& U = O->units[layer0 * per_layer + i];
+        if ((int)U.e.size() != n || U.next_pos != n) return 2;
+        for (int j = 0; j < n; ++j)
+            if (U.e[j].pos != j) return 2;
+    }
+    parallel_units(O->nthreads, nl * per_layer, [&](int i) {
+        int u = layer0 * per_layer + i;
+        Unit& U = O->units[u];
+        int li = i / per_layer, b = (i / O->Hkv) % O->B, g = i % O->Hkv;
+        std::vector<double> p, is(n, 0.0);
+        for (int qi = 0; qi < n; ++qi) {          // query at position qi
+            for (int hh = 0; hh < O->G; ++hh) {
+                int head = g * O->G + hh;
+                const float* qv = q + ((((size_t)li * O->B + b) * O->Hq + head) * n + qi) * O->d;
+                attend(*O, U.e, qv, qi, p, nullptr);
+                // tokens l whose band l .. l + band - 1 contains qi
+                for (int l = std::max(0, qi - band + 1); l <= qi; ++l) is[l] += p[l];
+            }
+        }
+        for (int l = 0; l < n; ++l) {
+            float inc = (float)is[l];
+            U.e[l].imp = U.e[l].imp + inc;
+        }
+    });
+    return 0;
+}
+
 // SnapKV pooling of the current scores: imp[pos p] <- max of the scores of the
 // retained positions in [p, p + kpool).  kpool <= 1 leaves them unchanged.
 int ora_pool_importance(void* h, int layer0, int nl, int kpool) {
@@ -328,9 +471,13 @@ int ora_decode(void* h, int layer0, int nl, const float* q, float* out) {
             int head = g * O->G + hh;
             size_t row = (((size_t)li * O->B + b) * O->Hq + head) * O->d;
             if (O->elem > 0 && O->elem < O->d) {
-                bool tie = false;
-                attend_stage2(*O, U.e, q + row, p, o.data(), &tie);
-                O->near_tie[(size_t)u / O->Hkv * O->Hq + head] = tie ? 1 : 0;
+                std::vector<UnsureChunk> unsure;
+                attend_stage2(*O, U.e, q + row, p, o.data(), &unsure);
+                const size_t hr = (size_t)u / O->Hkv * O->Hq + head;
+                O->alts[hr].clear();
+                O->near_tie[hr] = 0;
+                if (!unsure.empty())
+                    O->near_tie[hr] = stage2_alternatives(*O, U.e, p, o.data(), unsure, 4096, O->alts[hr]) ? 1 : 2;
             } else {
                 attend(*O, U.e, q + row, INT32_MAX, p, o.data());
             }
@@ -365,15 +512,31 @@ int ora_set_element_budget(void* h, int b2) {
     return 0;
 }
 
-// Per query head of layers [layer0, layer0 + nl): 1 where the latest Stage II
-// decode step took a chunk selection that was decided by less than 1e-4
-// (relative) between the last kept and the first dropped p.  [nl][B][Hq].
+// Per query head of layers [layer0, layer0 + nl), for the latest Stage II
+// decode step: 0 where every chunk selection is certain under float32
+// rounding of the logits, 1 where some is not (ora_stage2_alternatives lists
+// the admissible outputs), 2 where there were too many to list.  [nl][B][Hq].
 int ora_stage2_near_ties(void* h, int layer0, int nl, uint8_t* flags) {
     Oracle* O = (Oracle*)h;
     if (!range_ok(O, layer0, nl)) return 1;
     const size_t per = (size_t)O->B * O->Hq;
     std::memcpy(flags, O->near_tie.data() + (size_t)layer0 * per, (size_t)nl * per);
     return 0;
+}
+
+// The admissible outputs of query head `head` of (layer, batch) at the latest
+// Stage II decode step, each rounded to the output type: [count][d] into out
+// (room for max rows).  Returns count (0 when the selection was certain), or
+// -1 when they do not fit or were too many to list.
+int ora_stage2_alternatives(void* h, int layer, int b, int head, float* out, int max) {
+    Oracle* O = (Oracle*)h;
+    if (!range_ok(O, layer, 1) || b < 0 || b >= O->B || head < 0 || head >= O->Hq) return -1;
+    const size_t hr = ((size_t)layer * O->B + b) * O->Hq + head;
+    if (O->near_tie[hr] == 2) return -1;
+    const int count = (int)(O->alts[hr].size() / O->d);
+    if (count > max) return -1;
+    std::memcpy(out, O->alts[hr].data(), O->alts[hr].size() * sizeof(float));
+    return count;
 }
 
 // Cut every unit of the range with n > B to exactly B entries.

@@ -641,3 +641,194 @@ def test_stage2_chunks_are_retained_entries_in_position_order():
     # (0-7, 8-15, 16-23, 24) and one global top 6
     for wrong in ({0, 1, 14, 15, 17, 19, 22, 24}, {1, 15, 17, 19, 22, 24}):
         assert abs(out[0] - p[np.array([x in wrong for x in kept_pos])].sum()) > 1e-3
+
+
+# --------------------------------------------------------------------------
+# HiKV prefill initialisation (HiKV sec. III-D with the IS definition of
+# sec. III-B): IS(l) = sum over the band of queries l .. l + band - 1 of
+# P_i[l], causal, summed over the group's heads.  Pinned by the full causal
+# P matrix built with library softmax, a zero-key closed form in exact
+# rationals, and the band's two extremes.
+# --------------------------------------------------------------------------
+def _causal_p(q, keys, d):
+    """[n][n] causal softmax matrix of one head (row i = query at position i),
+    library softmax in float64 with masked entries at -inf."""
+    s = q.astype(np.float64) @ keys.astype(np.float64).T / np.sqrt(d)
+    n = s.shape[0]
+    s[np.triu_indices(n, 1)] = -np.inf
+    return torch.softmax(torch.from_numpy(s), 1).numpy()
+
+
+def _band_ref(Q, K, G, band, d):
+    """IS per (b, g, token) from the full P matrices."""
+    L, B, Hkv, n = K.shape[:4]
+    out = np.zeros((B, Hkv, n))
+    for b in range(B):
+        for g in range(Hkv):
+            for hh in range(G):
+                P = _causal_p(Q[0, b, g * G + hh], K[0, b, g], d)
+                for l in range(n):
+                    out[b, g, l] += P[l:min(n, l + band), l].sum()
+    return out
+
+
+@pytest.mark.parametrize("band", [1, 3, 7, 20, 40])
+def test_band_score_equals_full_attention_columns(band):
+    rng = np.random.default_rng(31 + band)
+    L, B, Hq, Hkv, d, n = 1, 2, 4, 2, 8, 20
+    G = Hq // Hkv
+    O = oracle.Oracle(L, B, Hq, Hkv, d, 0, 4, np.full(Hkv, 1000))
+    K = _rand(rng, L, B, Hkv, n, d) * 2
+    Q = _rand(rng, L, B, Hq, n, d) * 2
+    O.append(0, K, _rand(rng, L, B, Hkv, n, d))
+    O.score_band(0, Q, band)
+    ref = _band_ref(Q, K, G, band, d)
+    for b in range(B):
+        for g in range(Hkv):
+            pos, imp = O.state(O.unit(0, b, g))
+            np.testing.assert_array_equal(pos, np.arange(n))
+            np.testing.assert_allclose(imp, ref[b, g], rtol=2e-7, atol=1e-9)
+    # the observation window of the last `band` queries is another score
+    # unless the band covers the whole prompt, where the two coincide
+    Ow = oracle.Oracle(L, B, Hq, Hkv, d, 0, 4, np.full(Hkv, 1000))
+    Ow.append(0, K, np.zeros_like(K))
+    Ow.score_window(0, Q[:, :, :, n - min(band, n):])
+    same = np.allclose(Ow.state(0)[1], O.state(0)[1], rtol=1e-6, atol=1e-7)
+    assert same == (band >= n)
+
+
+def test_band_score_zero_keys_closed_form():
+    # all-zero keys: query i spreads 1/(i+1) over tokens 0..i, so
+    # IS(l) = G * sum_{i=l}^{min(l+band, n)-1} 1/(i+1), in exact rationals
+    L, B, Hq, Hkv, d, n, band = 1, 1, 8, 1, 16, 37, 9
+    G = Hq // Hkv
+    rng = np.random.default_rng(4)
+    O = oracle.Oracle(L, B, Hq, Hkv, d, 0, 0, [1000])
+    O.append(0, np.zeros((L, B, Hkv, n, d), np.float32), _rand(rng, L, B, Hkv, n, d))
+    O.score_band(0, _rand(rng, L, B, Hq, n, d), band)
+    _, imp = O.state(0)
+    for l in range(n):
+        want = G * sum(Fraction(1, i + 1) for i in range(l, min(n, l + band)))
+        assert abs(float(imp[l]) - float(want)) <= 2 ** -22 * float(want), l
+
+
+def test_band_one_is_the_diagonal_and_a_full_band_holds_all_mass():
+    rng = np.random.default_rng(5)
+    L, B, Hq, Hkv, d, n = 1, 1, 2, 1, 8, 15
+    G = Hq // Hkv
+    K = _rand(rng, L, B, Hkv, n, d) * 2
+    Q = _rand(rng, L, B, Hq, n, d) * 2
+    O1 = oracle.Oracle(L, B, Hq, Hkv, d, 0, 0, [1000])
+    O1.append(0, K, K)
+    O1.score_band(0, Q, 1)
+    _, imp = O1.state(0)
+    diag = sum(np.diag(_causal_p(Q[0, 0, h], K[0, 0, 0], d)) for h in range(G))
+    np.testing.assert_allclose(imp, diag, rtol=2e-7)
+    assert imp[0] == G                             # query 0 sees only token 0
+    On = oracle.Oracle(L, B, Hq, Hkv, d, 0, 0, [1000])
+    On.append(0, K, K)
+    On.score_band(0, Q, n)                         # every query's whole row
+    assert abs(float(np.sum(On.state(0)[1], dtype=np.float64)) - G * n) < 1e-5
+
+
+def test_band_score_needs_the_uncut_prompt():
+    rng = np.random.default_rng(6)
+    O = oracle.Oracle(1, 1, 2, 1, 8, 0, 2, [8])
+    O.append(0, _rand(rng, 1, 1, 1, 12, 8), _rand(rng, 1, 1, 1, 12, 8))
+    O.evict(0, 1)
+    with pytest.raises(ValueError):
+        O.score_band(0, _rand(rng, 1, 1, 2, 8, 8), 4)
+
+
+def test_hikv_band_init_then_dual_bank_matches_fifo_and_min_heap():
+    """HiKV from prefill to decode, restated directly: every prompt token's
+    IS is its attention column over its own band of W = B_I/2 queries; the
+    last W prompt tokens fill the recent bank and the top W of the rest the
+    important bank (sec. III-D); decoding then runs the FIFO + frozen-score
+    min-heap rule of sec. III-B.  The oracle (band scores, the cut, recent-
+    bank accumulation, argmin eviction) must keep the same tokens with the
+    same scores at every step."""
+    rng = np.random.default_rng(41)
+    L, B_, Hq, Hkv, d = 1, 1, 2, 1, 8
+    G = Hq // Hkv
+    prompt, steps, W = 30, 25, 5
+    Bud = 2 * W
+    O = oracle.Oracle(L, B_, Hq, Hkv, d, 0, W, np.full(Hkv, Bud))
+    O.set_recent_only(True)
+    K = _rand(rng, L, B_, Hkv, prompt + steps, d) * 2
+    V = _rand(rng, L, B_, Hkv, prompt + steps, d)
+    Q = _rand(rng, L, B_, Hq, prompt, d) * 2
+    O.append(0, K[:, :, :, :prompt], V[:, :, :, :prompt])
+    O.score_band(0, Q, W)
+    O.evict(0, L)
+    P = [_causal_p(Q[0, 0, h], K[0, 0, 0, :prompt], d) for h in range(G)]
+    score = {l: sum(P[h][l:min(prompt, l + W), l].sum() for h in range(G)) for l in range(prompt)}
+    recent = list(range(prompt - W, prompt))
+    rest = sorted(range(prompt - W), key=lambda p: (-score[p], p))
+    important = set(rest[:Bud - W])
+    pos, imp = O.state(0)
+    assert sorted(important) + recent == list(pos)
+    np.testing.assert_allclose(imp, [score[p] for p in pos], rtol=2e-6, atol=1e-7)
+    for s_ in range(steps):
+        t = prompt + s_
+        O.append(0, K[:, :, :, t:t + 1], V[:, :, :, t:t + 1])
+        q = _rand(rng, L, B_, Hq, d)
+        O.decode(0, q)
+        O.evict(0, L)
+        recent.append(t)
+        score[t] = 0.0
+        kept = sorted(important) + recent
+        inc = sum(_softmax_row(q[0, 0, hh], K[0, 0, 0, kept], d) for hh in range(G))
+        for p, x in zip(kept, inc):
+            if p in recent:
+                score[p] += x
+        evi = recent.pop(0)
+        low = min(important, key=lambda p: (score[p], -p))
+        if score[evi] > score[low]:
+            important.remove(low)
+            important.add(evi)
+        pos, imp = O.state(0)
+        assert sorted(important) + recent == list(pos), s_
+        np.testing.assert_allclose(imp, [score[p] for p in pos], rtol=2e-6, atol=1e-7)
+
+
+# --------------------------------------------------------------------------
+# HiKV Stage II near ties: when float32 rounding of the logits could change
+# a chunk's selection, the oracle lists every admissible output.
+# --------------------------------------------------------------------------
+def test_stage2_exact_tie_lists_both_selections():
+    # chunk of d = 8 entries, B2 = 3; entries 2 and 5 have identical keys, so
+    # identical logits, and they are the 3rd and 4th largest: either may be
+    # kept.  Their values differ, so the two admissible outputs differ.
+    d, B2 = 8, 3
+    O = oracle.Oracle(1, 1, 1, 1, d, 0, 0, [1000])
+    O.set_element_budget(B2)
+    a = np.array([0.9, 0.8, 0.5, 0.1, 0.2, 0.5, 0.0, 0.3])
+    K = np.repeat(a[:, None], d, axis=1).astype(np.float32)[None, None, None]
+    V = np.zeros((1, 1, 1, d, d), np.float32)
+    V[0, 0, 0, np.arange(d), np.arange(d)] = 1.0          # one-hot values: out[j] = p_j if kept
+    O.append(0, K, V)
+    q = np.zeros((1, 1, 1, d), np.float32)
+    q[0, 0, 0, :3] = [2.0, 1.5, 1.0]
+    out = O.decode(0, q)[0, 0, 0]
+    assert O.stage2_near_ties(0, 1)[0, 0, 0] == 1
+    alts = O.stage2_alternatives(0, 0, 0)
+    assert alts.shape == (2, d)
+    kept_sets = sorted(tuple(np.nonzero(x)[0].tolist()) for x in alts)
+    assert kept_sets == [(0, 1, 2), (0, 1, 5)]
+    # the exact output keeps the lower position of the tie and is listed
+    assert tuple(np.nonzero(out)[0].tolist()) == (0, 1, 2)
+    assert any(np.array_equal(out, x) for x in alts)
+
+
+def test_stage2_separated_logits_have_no_alternatives():
+    d, B2 = 8, 3
+    O = oracle.Oracle(1, 1, 1, 1, d, 0, 0, [1000])
+    O.set_element_budget(B2)
+    a = np.linspace(0.0, 1.0, d)
+    K = np.repeat(a[:, None], d, axis=1).astype(np.float32)[None, None, None]
+    O.append(0, K, K)
+    q = np.ones((1, 1, 1, d), np.float32)
+    O.decode(0, q)
+    assert O.stage2_near_ties(0, 1)[0, 0, 0] == 0
+    assert O.stage2_alternatives(0, 0, 0).shape == (0, d)
