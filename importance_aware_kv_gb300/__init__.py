@@ -31,7 +31,7 @@ ABI_FUNCTIONS = ("hikv_create_cache", "hikv_destroy_cache", "hikv_append", "hikv
                  "hikv_device_status", "hikv_last_error", "hikv_score_window_noalloc",
                  "hikv_decode_step_fused", "hikv_kernel_launches", "hikv_budgets_pyramid",
                  "hikv_budgets_duo", "hikv_selftest_timeout", "hikv_element_rows",
-                 "hikv_last_decode_config")
+                 "hikv_last_decode_config", "hikv_score_band", "hikv_read_floor")
 
 
 class HikvError(RuntimeError):
@@ -49,7 +49,7 @@ class hikv_config(ctypes.Structure):
                 ("page_tokens", ctypes.c_int32), ("pool_pages", ctypes.c_int64),
                 ("max_window_queries", ctypes.c_int32), ("scale", ctypes.c_float),
                 ("pool_kernel", ctypes.c_int32), ("importance_mode", ctypes.c_int32),
-                ("element_budget", ctypes.c_int32)]
+                ("element_budget", ctypes.c_int32), ("band_scoring", ctypes.c_int32)]
 
 
 def _load():
@@ -63,6 +63,7 @@ def _load():
         "hikv_destroy_cache": ([P], S),
         "hikv_append": ([P, I32, I32, I32, P, P, P], S),
         "hikv_score_window": ([P, I32, I32, I32, P, P], S),
+        "hikv_score_band": ([P, I32, I32, I32, P, P], S),
         "hikv_decode_step": ([P, I32, I32, P, P, P], S),
         "hikv_evict": ([P, I32, I32, P], S),
         "hikv_gather_retained": ([P, I32, I32, I32, P, P, P, P, P, P], S),
@@ -77,6 +78,7 @@ def _load():
         "hikv_budgets_pyramid": ([I32, I32, I32, I32, I32, P], S),
         "hikv_budgets_duo": ([I32, I32, P, I32, I32, I32, P], S),
         "hikv_selftest_timeout": ([P, I32, P], S),
+        "hikv_read_floor": ([P, I64, I32, P, P], S),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -168,6 +170,7 @@ class CacheConfig:
     pool_kernel: int = 0           # SnapKV max-pool of the prompt scores (0/1: off)
     importance_mode: int = 0       # 0: H2O cumulative, 1: HiKV recent bank only
     element_budget: int = 0        # HiKV Stage II B2 (0 or head_dim: exact attention)
+    band_scoring: int = 0          # 1: allow score_band (HiKV banded prefill scores)
 
 
 def hikv_create_cache(cfg: CacheConfig) -> ctypes.c_void_p:
@@ -176,7 +179,8 @@ def hikv_create_cache(cfg: CacheConfig) -> ctypes.c_void_p:
                     HIKV_BF16 if cfg.dtype == "bf16" else HIKV_F32, cfg.num_sink,
                     cfg.recent_window, b.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
                     cfg.max_tokens, cfg.page_tokens, cfg.pool_pages, cfg.max_window_queries,
-                    cfg.scale, cfg.pool_kernel, cfg.importance_mode, cfg.element_budget)
+                    cfg.scale, cfg.pool_kernel, cfg.importance_mode, cfg.element_budget,
+                    cfg.band_scoring)
     h = ctypes.c_void_p()
     _check(_lib.hikv_create_cache(ctypes.byref(c), ctypes.byref(h)))
     return h
@@ -265,6 +269,16 @@ def hikv_score_window_noalloc(k, q, importance, num_q_heads: int, scale: float =
         _dev(importance, "importance", torch.float32, (nl, b, hkv, ntok)), _stream(stream)))
 
 
+def read_floor(buf, ctas_per_sm: int = 2, sink=None, stream=None) -> None:
+    """Measurement aid: one plain streaming read of a CUDA tensor's bytes
+    (hikv_read_floor); `sink` a 4-byte CUDA tensor (allocated if None)."""
+    import torch
+    if sink is None:
+        sink = torch.zeros(1, dtype=torch.int32, device=buf.device)
+    _check(_lib.hikv_read_floor(_dev(buf, "buf"), buf.numel() * buf.element_size(), ctas_per_sm,
+                                _dev(sink, "sink"), _stream(stream)))
+
+
 def hikv_last_error() -> str:
     return _lib.hikv_last_error().decode()
 
@@ -322,6 +336,19 @@ class Cache:
         nq = q.shape[3] if q.dim() == 5 else -1
         self._check_tensor(q, "q", (nl, c.batch, c.num_q_heads, nq, c.head_dim))
         hikv_score_window(self.h, layer0, q, stream)
+
+    def score_band(self, q, band, layer0=0, stream=None):
+        """HiKV prefill initialisation: q [nl][B][Hq][n][d] holds the queries
+        of every held position; each token's score grows by its attention
+        column over the band of queries from its own position."""
+        c = self.cfg
+        nl = self._layers(q, layer0)
+        n = q.shape[3] if q.dim() == 5 else -1
+        self._check_tensor(q, "q", (nl, c.batch, c.num_q_heads, n, c.head_dim))
+        lens = self.lengths(layer0, nl)
+        if lens.size and int(lens[0]) != n:
+            raise ValueError(f"q holds {n} positions, the units hold {int(lens[0])} tokens")
+        _check(_lib.hikv_score_band(self.h, layer0, nl, int(band), _dev(q, "q"), _stream(stream)))
 
     def decode_step(self, q, out, layer0=0, stream=None):
         c = self.cfg

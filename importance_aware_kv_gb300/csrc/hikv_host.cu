@@ -145,6 +145,8 @@ struct hikv_cache {
     unsigned long long* d_erows = nullptr;   // V rows the element-level steps read
     float* d_eqmask = nullptr;          // [units][G][d]
     int32_t* d_edone = nullptr;         // [units]
+    // HiKV banded prefill scores (band_scoring): one layer's per-query softmax statistics
+    float2* d_band = nullptr;           // [per_layer][G][cap]
 };
 
 namespace {
@@ -218,6 +220,8 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
     if (f.element_budget < 0 || f.element_budget > f.head_dim)
         return fail(HIKV_ERR_INVALID_ARG, "create: element_budget %d not in [0, head_dim=%d]", f.element_budget,
                     f.head_dim);
+    if (f.band_scoring != 0 && f.band_scoring != 1)
+        return fail(HIKV_ERR_INVALID_ARG, "create: band_scoring %d not in {0, 1}", f.band_scoring);
     if (f.pool_kernel < 0 || f.pool_kernel > kMaxPoolKernel)
         return fail(HIKV_ERR_INVALID_ARG, "create: pool_kernel %d not in [0, %d]", f.pool_kernel, kMaxPoolKernel);
     const int64_t units64 = (int64_t)f.num_layers * f.batch * f.num_kv_heads;
@@ -329,6 +333,7 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
         ALLOC(c->d_eqmask, U * (size_t)G * c->d);
         ALLOC(c->d_edone, U);
     }
+    if (f.band_scoring) ALLOC(c->d_band, (size_t)c->per_layer * G * c->cap);
 #undef ALLOC
 
     // TMA descriptor of the pool: [pool_pages * 2P rows][d elements], boxes of
@@ -500,6 +505,34 @@ hikv_status hikv_score_window(hikv_cache* c, int32_t layer0, int32_t nl, int32_t
         c->launches += 1;
     }
     if (e != cudaSuccess) return cuda_fail(e, "score_window: launch");
+    for (int u = u0; u < u0 + nu; ++u) c->fresh[u] = 0;
+    return HIKV_OK;
+}
+
+hikv_status hikv_score_band(hikv_cache* c, int32_t layer0, int32_t nl, int32_t band, const void* q,
+                            hikv_stream_t stream) {
+    g_err.clear();
+    NvtxRange nvtx("hikv_score_band");
+    if (!range_ok(c, layer0, nl)) return fail(HIKV_ERR_INVALID_ARG, "score_band: bad cache or layer range");
+    if (band < 1) return fail(HIKV_ERR_INVALID_ARG, "score_band: band=%d < 1", band);
+    if (!q) return fail(HIKV_ERR_INVALID_ARG, "score_band: null q");
+    if (!c->d_band) return fail(HIKV_ERR_STATE, "score_band: the cache was created without band_scoring");
+    const int u0 = layer0 * c->per_layer, nu = nl * c->per_layer;
+    const int n = c->len[u0];
+    for (int u = u0; u < u0 + nu; ++u) {
+        if (c->len[u] != n)
+            return fail(HIKV_ERR_STATE, "score_band: unit %d holds %d tokens, unit %d holds %d", u, c->len[u], u0, n);
+        if (c->len[u] != c->next_pos[u])
+            return fail(HIKV_ERR_STATE, "score_band: unit %d has been cut (needs the whole prompt)", u);
+    }
+    if (n < 1) return fail(HIKV_ERR_STATE, "score_band: empty units");
+    cudaError_t e = cudaSuccess;
+    for (int li = 0; li < nl && e == cudaSuccess; ++li) {
+        e = launch_band(c->v, (layer0 + li) * c->per_layer, c->per_layer, li, (const uint8_t*)q, n, band,
+                        c->scale * 1.4426950408889634f, c->d_band, c->dtype, (cudaStream_t)stream);
+        c->launches += 2;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "score_band: launch");
     for (int u = u0; u < u0 + nu; ++u) c->fresh[u] = 0;
     return HIKV_OK;
 }

@@ -514,6 +514,12 @@ cudaError_t launch_pool_importance(const View& v, int32_t u0, int32_t nu, int k,
 bool window_tc_supported(int dtype, int d, int nqv);
 cudaError_t launch_window_tc(const WindowArgs& a, const CUtensorMap& tmap, int d, int nqv, cudaStream_t s);
 
+// HiKV banded prefill scores of the units [u0, u0 + units) of one layer
+// (k_band.cu): q is the call's [nl][B][Hq][n][d] with this layer at index
+// li; stats the [units][G][n] (m, 1/l) work buffer.
+cudaError_t launch_band(const View& v, int32_t u0, int32_t units, int32_t li, const uint8_t* q, int32_t n,
+                        int32_t band, float qscale, float2* stats, int dtype, cudaStream_t s);
+
 struct GatherArgs {
     View v;
     int32_t u0, nunits, cap;

@@ -108,6 +108,10 @@ typedef struct {
                                renormalised.  Units must then hold at most 16384
                                tokens when a decode step runs.  0 or head_dim =>
                                exact attention. */
+    int32_t band_scoring;   /* 1: allow hikv_score_band (HiKV's banded prefill
+                               scores); create then also allocates its per-query
+                               softmax statistics, batch * Hkv * G * max_tokens *
+                               8 bytes.  0: off. */
 } hikv_config;
 
 /* Create a cache: allocates the page pool, page tables, per-slot importance
@@ -139,6 +143,26 @@ hikv_status hikv_append(hikv_cache* cache, int32_t layer0, int32_t nlayers, int3
  * nq positions). */
 hikv_status hikv_score_window(hikv_cache* cache, int32_t layer0, int32_t nlayers, int32_t nq,
                               const void* q, hikv_stream_t stream);
+
+/* HiKV prefill initialisation (HiKV sec. III-D, with the importance score
+ * IS of sec. III-B): every prompt token l of a unit gets
+ *     imp_l += sum_{h in group} sum_{i = l}^{min(l + band, n) - 1} P_hi[l],
+ * P_hi being query head h's softmax at position i over the tokens at
+ * positions <= i (causal) -- the attention column the token receives from
+ * the band of queries starting at its own position.  With band = B_I / 2 =
+ * the recent window, importance_mode = 1, no sinks and a budget of 2W, the
+ * following hikv_evict fills HiKV's two banks as the paper describes (the
+ * last W prompt tokens, then the W best-scored of the rest), and decoding
+ * continues its Stage I rule.
+ * q: [nlayers][batch][Hq][n][d] in the cache dtype, the queries of every
+ * held position 0..n-1.  Every unit of the range must hold exactly n tokens,
+ * appended and never cut (so slot = position).  No pooling is applied.
+ * The cache must have been created with band_scoring = 1.  Cost: O(n^2 d G)
+ * per unit (it forms every prompt query's softmax statistics).
+ * Errors: INVALID_ARG (band < 1, null q), STATE (band_scoring off, units of
+ * unequal length, a cut or empty unit). */
+hikv_status hikv_score_band(hikv_cache* cache, int32_t layer0, int32_t nlayers, int32_t band,
+                            const void* q, hikv_stream_t stream);
 
 /* One decode step of attention over every retained token (including any
  * appended since the last step), plus the importance update.  q and out:
@@ -273,7 +297,10 @@ hikv_status hikv_device_status(hikv_cache* cache);
  * process exits; calls needing more -- nlayers*batch*Hkv * ceil(ntok/1024) *
  * G*nq * 2 floats -- are rejected with HIKV_ERR_INVALID_ARG and a message.
  * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * (cudaGetSymbolAddress) and keeps it for the life of the process; make that
+ * first call before any stream capture.  A cudaDeviceReset unloads the
+ * module and may move the array, so a process that resets a device must not
+ * call this entry point on that device afterwards.
  * Every call shares the one array: calls that overlap on the GPU (other
  * streams, other threads) race and must be serialised by the caller.
  * Errors: INVALID_ARG, UNSUPPORTED (head_dim, dtype or too many query
@@ -282,6 +309,17 @@ hikv_status hikv_score_window_noalloc(int32_t nlayers, int32_t batch, int32_t nu
                                       int32_t num_kv_heads, int32_t head_dim, int32_t dtype,
                                       int32_t ntok, int32_t nq, float scale, const void* k,
                                       const void* q, float* importance, hikv_stream_t stream);
+
+/* Measurement aid, no part of the method: the plainest streaming read of
+ * `bytes` bytes at `buf` (DEVICE, 16-byte aligned, bytes a positive multiple
+ * of 16) -- eight independent 16-byte loads per thread and round over a
+ * grid of ctas_per_sm (1..4) CTAs of 512 threads per SM, nothing stored
+ * except, almost never, one word to `sink` (DEVICE, 4 bytes) to keep the
+ * loads alive.  Timed around a cold buffer, it is the floor for any kernel
+ * that reads that many bytes once in one launch.
+ * Errors: INVALID_ARG, CUDA (launch). */
+hikv_status hikv_read_floor(const void* buf, int64_t bytes, int32_t ctas_per_sm, uint32_t* sink,
+                            hikv_stream_t stream);
 
 /* Message for the last failing call on this thread ("" if none). */
 const char* hikv_last_error(void);
