@@ -5,13 +5,23 @@ new k, v; attention with the importance update and victim argmin; evict back
 to the budget -- timed through hikv_decode_step_fused, which runs it as one
 kernel launch once every unit is at its budget (the three separate calls,
 hikv_append -> hikv_decode_step -> hikv_evict, are timed after it and reported
-as `three_call_path`).  Workload: the Llama-3-8B-shaped
-layer (batch 8, 32 query / 8 KV heads, d 128, bf16 K/V, 8192-token prompt,
-budget 1024, 4 sinks, 64-token window, eviction every step), seeded synthetic
-inputs resident in HBM before timing.  The decode stream continues past the
-workload's 256 steps when more are timed; per-step work is fixed by the
-budget.  The retained set (34 MB) fits in L2, so L2 is flushed (256 MB write)
-between timed steps, outside the timed events.
+as `three_call_path`).  Headline workload: the Llama-3-8B-shaped layer (batch
+8, 32 query / 8 KV heads, d 128, bf16 K/V, 8192-token prompt, budget 1024, 4
+sinks, 64-token window, eviction every step), seeded synthetic inputs resident
+in HBM before timing.  The decode stream continues past the workload's 256
+steps when more are timed; per-step work is fixed by the budget.  The
+retained set (34 MB) fits in L2, so L2 is flushed (256 MB write) between
+timed steps, outside the timed events.
+
+The same run then measures the other workloads (`other_workloads`): the
+32-layer 32K-context stack evicting every 16 steps, the HeadKV Dirichlet
+budgets, the Llama-3-70B 128K context, and the same 70B context with the
+full cache (no eviction) as the uncompressed reference point -- each with its
+step rate, HBM fraction, read floor, end-to-end rate and the CPU oracle's
+rate.  Their prompt K/V are drawn on the device (torch's seeded generator,
+N(0,1) with the workload's heavy-hitter key factors) so that 17-43 GB of
+prompt need not be generated on the host; decode-step inputs come from the
+workload generator as for the headline.
 
 Prints one JSON line.  `--impl reference` times the CPU oracle instead.
 """
@@ -33,6 +43,7 @@ import numpy as np  # noqa: E402
 
 METRIC = "decode steps/s and achieved HBM GB/s (fraction of ~8 TB/s) at 1 GB300"
 WORKLOAD_INDEX = 1
+OTHER_WORKLOADS = (2, 3, 4, "4-full")
 KERNEL_SOURCES = ["importance_aware_kv_gb300/csrc/k_decode.cuh",
                   "importance_aware_kv_gb300/csrc/hikv_internal.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "k_decode_llama3_8b_traffic.json")
@@ -67,11 +78,6 @@ def dist_env():
     return rank, world, local
 
 
-def rank_seed(w, rank: int) -> int:
-    """Seed of a rank's inputs: every rank decodes its own batch of units."""
-    return w.index + 1000 * rank
-
-
 def max_over_ranks(x: float, world: int, device) -> float:
     """The largest of the ranks' values (the job ends with its slowest rank)."""
     if world <= 1:
@@ -83,13 +89,68 @@ def max_over_ranks(x: float, world: int, device) -> float:
     return float(t.item())
 
 
-def whole_job_rate(world: int, steps: int, t_max: float) -> float:
-    """Steps/s of the whole job: every rank ran `steps` steps of its own units."""
-    return world * steps / t_max
+def whole_job_rate(world: int, steps: int, t_max: float, scaling: str = "weak") -> float:
+    """Workload steps/s of the whole job, ended by its slowest rank.  A step
+    decodes one token of every unit of the job's workload; under weak
+    scaling that workload is `world` times the configured one, so a job
+    step counts `world` configured-workload steps."""
+    return (world if scaling == "weak" else 1) * steps / t_max
+
+
+# --------------------------------------------------------------------------
+# multi-GPU: the units of one workload shared out across ranks (no collective)
+# --------------------------------------------------------------------------
+def split_contiguous(loads, parts: int):
+    """Contiguous, non-empty ranges [bounds[r], bounds[r + 1]) of `loads`:
+    a sweep that closes range r once it holds its share of the load not yet
+    assigned (an item joins while less than half of it overshoots that
+    share), so no range exceeds its share by more than one item."""
+    loads = [int(x) for x in loads]
+    n = len(loads)
+    if not 1 <= parts <= n:
+        raise ValueError(f"cannot split {n} items into {parts} non-empty ranges")
+    bounds = [0]
+    for r in range(parts - 1):
+        i0 = bounds[-1]
+        share = sum(loads[i0:]) / (parts - r)
+        last = n - (parts - r - 1)          # leave one item for each range still to come
+        acc, i = 0, i0
+        while i < last and (i == i0 or acc + loads[i] / 2 <= share):
+            acc += loads[i]
+            i += 1
+        bounds.append(i)
+    bounds.append(n)
+    return bounds
+
+
+def rank_shard(w, world: int, rank: int, budgets):
+    """(l0, l1, b0, b1): the units of w that rank `rank` of `world` decodes.
+    Batch rows when they divide evenly (every row has the same budgets, so
+    the shares are equal); otherwise contiguous layer ranges balanced by the
+    sum of their units' budgets B_u (a unit's decode work is proportional to
+    its budget; per-head budgets make layers unequal).  The library's calls
+    take whole layers, so a layer is the finest split."""
+    if world == 1:
+        return 0, w.layers, 0, w.batch
+    if w.batch % world == 0:
+        per = w.batch // world
+        return 0, w.layers, rank * per, (rank + 1) * per
+    loads = np.asarray(budgets, np.int64).reshape(w.layers, w.hkv).sum(axis=1) * w.batch
+    bounds = split_contiguous(loads, world)
+    return bounds[rank], bounds[rank + 1], 0, w.batch
+
+
+def global_workload(w, world: int, scaling: str):
+    """The workload all ranks decode together: `weak` scales the batch with
+    the ranks (each rank then holds as many units as one GPU alone), `strong`
+    shares out w itself."""
+    return w.with_(batch=w.batch * world, name=f"{w.name}-x{world}batch") if scaling == "weak" and world > 1 else w
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks / throttle reasons sampled every 20 ms, from before
+    the first timed step (the sampler's first sample is awaited) to after
+    the last one."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -106,9 +167,23 @@ class ClockSampler:
         except (OSError, FileNotFoundError):
             self.proc = None
 
-    def stop(self):
+    def wait_first(self, timeout_s: float = 3.0):
+        """Block until the sampler has written a sample (or timeout)."""
+        if self.proc is None:
+            return
+        t0 = time.time()
+        while time.time() - t0 < timeout_s:
+            try:
+                if os.path.getsize(self.out) > 0:
+                    return
+            except OSError:
+                pass
+            time.sleep(0.01)
+
+    def stop(self, linger_s: float = 0.05):
         if self.proc is None:
             return None
+        time.sleep(linger_s)   # one more sample after the timed region
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -134,7 +209,7 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "window": "20 ms samples from before the first timed step to after the last"}
 
 
 def gpu_id_for(dev_index: int) -> str:
@@ -188,6 +263,20 @@ def schedule_budgets(w, seed, schedule):
     raise ValueError(f"unknown schedule {schedule!r}")
 
 
+def workload_config(w, schedule="workload", element_budget=0, full_cache=False, world=1, scaling="weak"):
+    """The `config` of a bench line: the workload and the run's options only
+    (no measured values), the same for the GPU arm and the reference arm."""
+    return {"workload": w.name + ("-full-cache" if full_cache else ""), "layers": w.layers, "batch": w.batch,
+            "q_heads": w.hq, "kv_heads": w.hkv, "head_dim": w.d, "kv_dtype": w.dtype, "prompt": w.prompt,
+            "budget": "full cache" if full_cache else w.budget, "sink": w.sink, "window": w.window,
+            "evict_every": w.evict_every, "budget_schedule": schedule or "workload",
+            "element_budget": element_budget,
+            "l2": "flushed between timed steps (256 MB write, outside the timed events)",
+            "parallelism": (f"units of one workload ({'the configured one' if scaling == 'strong' else f'batch x{world}'})"
+                            f" shared out across {world} ranks: batch rows, else layers balanced by Sum B_u;"
+                            " no collective" if world > 1 else "one GPU")}
+
+
 def run_cpu_oracle(w, seed, steps, warmup, budget_s=20.0, layers=None, budgets=None, element_budget=0,
                    steps_1thread=0, budget_1thread_s=10.0):
     """Time the oracle's decode loop (append -> decode -> evict when due) on the
@@ -215,6 +304,7 @@ def run_cpu_oracle(w, seed, steps, warmup, budget_s=20.0, layers=None, budgets=N
     total = warmup + steps + steps_1thread
     ks = [W.gen_kv(w, l, 1, w.prompt, total, seed) for l in layers]
     qs = [W.gen_q(w, l, 1, w.prompt, total, seed) for l in layers]
+
     def one_step(s):
         t0 = time.perf_counter()
         for si in range(len(layers)):
@@ -263,13 +353,12 @@ def bench_reference(args):
         return
     w = W.WORKLOADS[args.workload]
     val, cores, done, sample, _ = run_cpu_oracle(w, w.index, args.steps, args.warmup, budget_s=120.0,
-                                              layers=oracle_sample_layers(w))
+                                                 layers=oracle_sample_layers(w))
     line = {
         "impl": "reference", "metric": METRIC, "value": val, "unit": "steps/s", "n_gpus": 0,
         "steps": done, "warmup": args.warmup, "ms_per_step": 1e3 / val, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-        "config": {"workload": w.name, "units": w.units, "budget": w.budget, "sink": w.sink,
-                   "window": w.window, "evict_every": w.evict_every},
+        "config": workload_config(w, args.schedule, 0, False, world, args.scaling),
         "cpu_baseline": {"value": val, "unit": "steps/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": val, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -277,44 +366,58 @@ def bench_reference(args):
 
 
 # --------------------------------------------------------------------------
-def bench_gpu(args):
-    def stage(msg):
-        if args.verbose:
-            print(f"[bench] {msg}", file=sys.stderr, flush=True)
+def device_prompt(w, l0, nl, seed, dev):
+    """Prompt K, V of layers [l0, l0 + nl) drawn on the device: N(0,1) from
+    torch's generator seeded by (seed, l0), keys times the workload's
+    heavy-hitter factors of each (layer, batch) sequence."""
     import torch
-    import torch.distributed as dist
+    import workloads as W
+    g = torch.Generator(device=dev)
+    g.manual_seed(1_000_003 * (seed + 1) + l0)
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    shape = (nl, w.batch, w.hkv, w.prompt, w.d)
+    k = torch.randn(shape, generator=g, device=dev, dtype=torch.float32)
+    if w.heavy is not None:
+        f = np.stack([np.stack([W.heavy_scale(w, seed, w.layer0 + l0 + li, w.batch0 + b)[: w.prompt]
+                                for b in range(w.batch)]) for li in range(nl)])
+        k *= torch.from_numpy(f).to(dev)[:, :, None, :, None]
+    k = k.to(dt)
+    v = torch.randn(shape, generator=g, device=dev, dtype=torch.float32).to(dt)
+    return k, v
+
+
+def measure(w, seed, dev, opts, stage=lambda m: None):
+    """Run one workload on the GPU: setup (untimed), then the timed fused
+    steps, the three-call steps, per-layer launches, end-to-end steps and the
+    read floor.  Returns the results as a dict."""
+    import torch
     import importance_aware_kv_gb300 as hk
     import workloads as W
 
-    rank, world, local = dist_env()
-    if world > 1:
-        dist.init_process_group("nccl", init_method="env://")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    w = W.WORKLOADS[args.workload]
-    if args.layers:   # the workload cut to its first L layers (small cases for profiling)
-        w = w.with_(layers=min(args.layers, w.layers), name=f"{w.name}-first{min(args.layers, w.layers)}layers")
-    seed = rank_seed(w, rank) if args.seed is None else args.seed + 1000 * rank
-    K, Wu, Ke, K3 = args.steps, args.warmup, args.e2e_steps, args.three_call_steps
+    K, Wu, K3, KL, Ke = opts["steps"], opts["warmup"], opts["three_call_steps"], opts["per_layer_steps"], \
+        opts["e2e_steps"]
     L = w.layers
-    KL = args.per_layer_steps if args.per_layer_steps >= 0 else (0 if L == 1 else 100)
     total_steps = Wu + K + K3 + KL + Ke
-    budgets = schedule_budgets(w, seed, args.schedule)
-    if args.full_cache:   # no eviction: every unit keeps its whole context
-        budgets = np.full_like(budgets, w.prompt + Wu + K + args.three_call_steps + max(args.per_layer_steps, 100)
-                               + Ke + 1)
-    elem = args.element_budget if 0 < args.element_budget < w.d else 0
+    budgets = opts["budgets"]
+    if opts["full_cache"]:   # no eviction: every unit keeps its whole context
+        budgets = np.full_like(budgets, w.prompt + total_steps + 1)
+    elem = opts["element_budget"] if 0 < opts["element_budget"] < w.d else 0
     cache = hk.Cache(hk.CacheConfig(w.layers, w.batch, w.hq, w.hkv, w.d, w.dtype, w.sink, w.window,
                                     budgets, w.prompt + total_steps + 1, element_budget=elem))
-    stage("cache created")
+    stage(f"{w.name}: cache created")
     # ---- setup (untimed): prompt in layer chunks, window scoring, cut to budget ----
     stream = torch.cuda.current_stream()
     lc = layer_chunk(w)
     for l0 in range(0, L, lc):
         nl = min(lc, L - l0)
-        k, v = W.gen_kv(w, l0, nl, 0, w.prompt, seed)
-        cache.append(W.to_torch(k).to(dev), W.to_torch(v).to(dev), layer0=l0)
-        del k, v
+        if opts["prompt_source"] == "device":
+            dk, dv = device_prompt(w, l0, nl, seed, dev)
+        else:
+            k, v = W.gen_kv(w, l0, nl, 0, w.prompt, seed)
+            dk, dv = W.to_torch(k).to(dev), W.to_torch(v).to(dev)
+            del k, v
+        cache.append(dk, dv, layer0=l0)
+        del dk, dv
     dq_win = W.to_torch(W.gen_q(w, 0, L, w.prompt - w.nq, w.nq, seed)).to(dev)
     se = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
     torch.cuda.synchronize()
@@ -325,6 +428,8 @@ def bench_gpu(args):
     se[2].record(stream)
     torch.cuda.synchronize()
     setup = {"prompt_tokens_per_unit": w.prompt, "window_queries": w.nq,
+             "prompt_source": ("device (torch seeded N(0,1) x heavy-hitter factors)"
+                               if opts["prompt_source"] == "device" else "workload generator (host)"),
              "window_scoring_ms": se[0].elapsed_time(se[1]), "prefill_cut_ms": se[1].elapsed_time(se[2]),
              "window_scoring_k_gbs": W.kv_bytes(w.batch, w.prompt, L, w.hkv, w.d, w.elem_bytes) / 2 /
              (se[0].elapsed_time(se[1]) / 1e3) / 1e9}
@@ -341,7 +446,7 @@ def bench_gpu(args):
     dks, dvs, dqs = (W.to_torch(x).to(dev) for x in (ks, vs, qs))
     out = torch.empty_like(dqs[0])
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    E = w.evict_every
+    E = w.evict_every if not opts["full_cache"] else 1
     counter = {"s": 0}                    # decode steps taken so far (eviction cadence)
 
     def next_step():
@@ -356,21 +461,23 @@ def bench_gpu(args):
         r, ev_ = next_step()
         cache.step(dks[r], dvs[r], dqs[r], out, evict=ev_)
 
-    stage("setup done")
+    stage(f"{w.name}: setup done")
     for _ in range(Wu):
         flush.fill_(1.0)
         step_fused()
     torch.cuda.synchronize()
-    stage("warm-up done")
     # A spin kernel before each timed step lets the host enqueue the whole
     # step before the GPU reaches it, so host launch overhead never shows up
     # inside the timed events (the flush and the spin are outside them).
-    spin_cycles = int(args.spin_us * 2.0e3)
+    spin_cycles = int(opts["spin_us"] * 2.0e3)
 
     # ---- timed: the single-call step (append + decode + evict in one launch) ----
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    sampler = ClockSampler(gpu_id_for(local))
-    if world > 1:
+    sampler = opts.get("sampler")
+    if sampler is not None:
+        sampler.wait_first()
+    if opts["world"] > 1:
+        import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
     launches0 = cache.kernel_launches()
@@ -394,12 +501,12 @@ def bench_gpu(args):
         # HiKV Stage II reads whole K rows but only the V rows some head kept
         v_all = kv_bytes // 2
         alg_bytes = alg_bytes - v_all + vrows * w.d * w.elem_bytes
-    if world > 1:
+    if opts["world"] > 1:
         dist.barrier()
-    clocks = sampler.stop()
+    clocks = sampler.stop() if sampler is not None else None
     step_ms = [e0.elapsed_time(e1) for (e0, e1) in ev]
-    t_total = max_over_ranks(sum(step_ms) / 1e3, world, dev)
-    stage("timed fused steps done")
+    t_total = max_over_ranks(sum(step_ms) / 1e3, opts["world"], dev)
+    stage(f"{w.name}: timed fused steps done")
 
     # ---- the same steps as three calls (append, decode_step, evict when due) ----
     ev3 = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(K3)]
@@ -423,12 +530,11 @@ def bench_gpu(args):
         dec3 = [e1.elapsed_time(e2) for (e0, e1, e2, e3) in ev3]
         three = {"steps": K3, "ms_per_step": sum(ms3) / K3, "steps_per_s": K3 / (sum(ms3) / 1e3),
                  "decode_kernel_us": 1e3 * sum(dec3) / K3}
-    stage("three-call steps done")
 
     # ---- per-layer launches: one fused call per layer and step, as a model
     # whose layers run in turn would issue them ----
     per_layer = None
-    if KL > 0:
+    if KL > 0 and L > 1:
         evl = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(KL)]
         pl_launch0 = cache.kernel_launches()
         for i in range(KL):
@@ -445,7 +551,6 @@ def bench_gpu(args):
         msl = [e0.elapsed_time(e1) for (e0, e1) in evl]
         per_layer = {"steps": KL, "launches_per_step": (cache.kernel_launches() - pl_launch0) / KL,
                      "ms_per_step": sum(msl) / KL, "steps_per_s": KL / (sum(msl) / 1e3)}
-        stage("per-layer steps done")
 
     # ---- e2e through the C ABI with pinned host buffers: every step copies
     # its k, v and q in (one packed copy) and the output back ----
@@ -473,23 +578,26 @@ def bench_gpu(args):
         e_end.record(stream)
         e_end.synchronize()
         e2e_ms += e_start.elapsed_time(e_end)
-    stage("e2e steps done")
     h2d = packed[0].nbytes
     d2h = out_host.nbytes
     cache.device_status()
     lens = cache.lengths()
     cache.close()
+    del dks, dvs, dqs, packed, in_dev
+    stage(f"{w.name}: e2e steps done")
 
-    # ---- size floor (context for the roofline fraction): how long the
-    # plainest kernels take to read, and to copy, one step's bytes from a
-    # flushed L2, timed the same way as the steps ----
+    # ---- read floor (context for the roofline fraction): a plain streaming
+    # read, and a torch copy, of one step's algorithmic bytes from a flushed
+    # L2, timed the same way as the steps ----
     def size_floor(nbytes, reps=20):
-        buf = torch.empty(max(1, nbytes // 2), dtype=torch.bfloat16, device=dev).normal_()
+        nb = max(16, nbytes // 16 * 16)
+        buf = torch.empty(nb // 2, dtype=torch.bfloat16, device=dev).normal_()
         dst = torch.empty_like(buf)
-        acc = torch.empty((), dtype=torch.float32, device=dev)
-        out = {}
-        for name, fn in (("read_us", lambda: torch.sum(buf, 0, dtype=torch.float32, out=acc)),
-                         ("copy_us", lambda: dst.copy_(buf))):
+        sink = torch.zeros(1, dtype=torch.int32, device=dev)
+        res = {}
+        kernels = [(f"read_us_{c}cta", (lambda c=c: hk.read_floor(buf, c, sink))) for c in (1, 2, 4)]
+        kernels.append(("copy_us", lambda: dst.copy_(buf)))
+        for name, fn in kernels:
             fn()
             ts = []
             for i in range(reps):
@@ -501,17 +609,102 @@ def bench_gpu(args):
                 b.record(stream)
                 b.synchronize()
                 ts.append(a.elapsed_time(b) * 1e3)
-            out[name] = float(np.median(ts))
+            res[name] = float(np.median(ts))
+        res["read_us"] = min(v for k_, v in res.items() if k_.startswith("read_us_"))
+        res["read_gbs"] = nb / res["read_us"] / 1e3
         del buf, dst
-        return out
+        return res
     floor = size_floor(int(alg_bytes // K)) if K > 0 else None
-    stage("size floor done")
+    del flush
+    torch.cuda.empty_cache()
 
-    # ---- numbers ----
     avg_s = t_total / K
+    r = {"K": K, "Wu": Wu, "t_total": t_total, "avg_s": avg_s, "alg_bytes": alg_bytes, "kv_bytes": kv_bytes,
+         "launches": launches, "dec_cfg": dec_cfg, "three": three, "per_layer": per_layer, "setup": setup,
+         "clocks": clocks, "floor": floor, "lens": lens, "elem": elem, "vrows": vrows,
+         "decode_inputs": f"{R} distinct steps" + (", cycled" if R < total_steps else ""),
+         "e2e": ({"value": Ke / (e2e_ms / 1e3), "unit": "steps/s", "h2d_bytes_per_step": int(h2d),
+                  "d2h_bytes_per_step": int(d2h), "steps": Ke} if Ke > 0 else None)}
+    stage(f"{w.name}: read floor done")
+    return r
+
+
+def other_workloads(args, dev, peak, stage):
+    """The other workloads and the 70B full-cache reference point, measured
+    briefly in the same run."""
+    import workloads as W
+    out = []
+    for key in OTHER_WORKLOADS:
+        full = isinstance(key, str) and key.endswith("-full")
+        w = W.WORKLOADS[int(str(key).split("-")[0])]
+        seed = w.index
+        K = 5 if full else args.other_steps
+        opts = {"steps": K, "warmup": 3, "three_call_steps": 0, "per_layer_steps": 0 if full else 10,
+                "e2e_steps": 3 if full else 10, "budgets": W.budgets(w, seed), "full_cache": full,
+                "element_budget": 0, "prompt_source": "device", "spin_us": args.spin_us, "world": 1}
+        t0 = time.time()
+        r = measure(w, seed, dev, opts, stage)
+        gpu_s = time.time() - t0
+        achieved = r["alg_bytes"] / r["K"] / r["avg_s"] / 1e9
+        e = {"config": workload_config(w, "workload", 0, full), "steps": r["K"],
+             "steps_per_s": r["K"] / r["t_total"], "ms_per_step": r["avg_s"] * 1e3,
+             "hbm_gbs": achieved, "frac": achieved / peak, "frac_nominal": achieved / 8000.0,
+             "bytes_per_step": r["alg_bytes"] // r["K"],
+             "retained_kv_gbs": r["kv_bytes"] / r["t_total"] / 1e9,
+             "tokens_attended_per_unit_mean": float(r["lens"].mean()) + 1,
+             "launches_per_step": r["launches"] / r["K"], "decode_launch": r["dec_cfg"],
+             "read_floor": r["floor"], "step_over_read_floor": (r["avg_s"] * 1e6 / r["floor"]["read_us"])
+             if r["floor"] else None,
+             "per_layer_launches": r["per_layer"], "e2e": r["e2e"], "setup": r["setup"],
+             "gpu_wall_s": gpu_s}
+        if not args.no_cpu_baseline:
+            t0 = time.time()
+            val, cores, done, sample, _ = run_cpu_oracle(
+                w, seed, 8, 1, budget_s=args.other_cpu_s, layers=[0],
+                budgets=(np.full(w.layers * w.hkv, w.total_positions + 64, np.int32) if full else None))
+            e["cpu_baseline"] = {"value": val, "unit": "steps/s", "cores": cores, "kind": "oracle", "sample": sample,
+                                 "wall_s": time.time() - t0}
+        out.append(e)
+        stage(f"other workload {e['config']['workload']} done")
+    return out
+
+
+def bench_gpu(args):
+    def stage(msg):
+        if args.verbose:
+            print(f"[bench {time.strftime('%H:%M:%S')}] {msg}", file=sys.stderr, flush=True)
+    import torch
+    import torch.distributed as dist
+    import workloads as W
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = W.WORKLOADS[args.workload]
+    if args.layers:   # the workload cut to its first L layers (small cases for profiling)
+        w = w.with_(layers=min(args.layers, w.layers), name=f"{w.name}-first{min(args.layers, w.layers)}layers")
+    seed = w.index if args.seed is None else args.seed
+    cfg_w = w
+    gw = global_workload(w, world, args.scaling)
+    g_budgets = schedule_budgets(gw, seed, args.schedule)
+    l0, l1, b0, b1 = rank_shard(gw, world, rank, g_budgets)
+    w = W.shard(gw, l0, l1, b0, b1) if world > 1 else gw
+    budgets = g_budgets[l0 * gw.hkv:l1 * gw.hkv]
+    L = w.layers
+    opts = {"steps": args.steps, "warmup": args.warmup, "three_call_steps": args.three_call_steps,
+            "per_layer_steps": args.per_layer_steps if args.per_layer_steps >= 0 else (0 if L == 1 else 100),
+            "e2e_steps": args.e2e_steps, "budgets": budgets, "full_cache": args.full_cache,
+            "element_budget": args.element_budget, "prompt_source": "host", "spin_us": args.spin_us,
+            "world": world, "sampler": ClockSampler(gpu_id_for(local))}
+    r = measure(w, seed, dev, opts, stage)
+    K = r["K"]
     peaks, src = measured_peaks()
     peak = float(peaks.get("hbm_gbs", 6800.0))
-    achieved = alg_bytes / K / avg_s / 1e9
+    avg_s = r["avg_s"]
+    achieved = r["alg_bytes"] / K / avg_s / 1e9
+    elem = r["elem"]
     traffic = None
     try:
         with open(TRAFFIC_FILE) as f:
@@ -520,52 +713,57 @@ def bench_gpu(args):
             traffic = tr.get("dram_bytes_per_launch")
     except (OSError, ValueError):
         pass
-    value = whole_job_rate(world, K, t_total)
+    value = whole_job_rate(world, K, r["t_total"], args.scaling)
+    lens = r["lens"]
     line = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": K,
-        "warmup": Wu, "ms_per_step": t_total * 1e3 / K, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded)",
-        "config": {"workload": w.name, "layers": L, "batch": w.batch, "q_heads": w.hq,
-                   "kv_heads": w.hkv, "head_dim": w.d, "kv_dtype": w.dtype, "prompt": w.prompt,
-                   "budget": w.budget, "sink": w.sink, "window": w.window,
-                   "evict_every": E, "tokens_attended_per_unit_max": int(lens.max()) + 1,
-                   "budget_schedule": args.schedule or "workload",
-                   "element_budget": elem,
-                   "tokens_attended_per_unit_mean": float(lens.mean()) + 1,
-                   "decode_inputs": (f"{R} distinct steps" + (", cycled" if R < total_steps else "")),
-                   "l2": "flushed between timed steps (256 MB write, outside the timed events)",
-                   "parallelism": f"replicas x{world} (units sharded by rank, no collective)"},
-        "hbm_gbs_step": alg_bytes * world / t_total / 1e9,
-        "retained_kv_gbs": kv_bytes * world / t_total / 1e9,
+        "warmup": r["Wu"], "ms_per_step": r["t_total"] * 1e3 / K, "higher_is_better": True,
+        "scaling": args.scaling, "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded)",
+        "config": workload_config(cfg_w, args.schedule, elem if elem else 0, args.full_cache, world,
+                                  args.scaling),
+        "workload_observed": {"tokens_attended_per_unit_max": int(lens.max()) + 1,
+                              "tokens_attended_per_unit_mean": float(lens.mean()) + 1,
+                              "decode_inputs": r["decode_inputs"], "units_rank0": int(lens.size),
+                              "shard_rank0": {"layers": [l0, l1], "batch_rows": [b0, b1]}},
+        "hbm_gbs_step": r["alg_bytes"] * world / r["t_total"] / 1e9,
+        "retained_kv_gbs": r["kv_bytes"] * world / r["t_total"] / 1e9,
         "hbm_fraction_nominal": achieved / 8000.0,
         "roofline": {"kernel": ("k_decode (append + attention + importance + victim + evict, one launch)" if not elem
                                 else "HiKV Stage II step (k_elem_order with the append, k_elem_span with the merge and the eviction in its last CTA per unit)"),
                      "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{src} hbm_gbs", "traffic": traffic,
-                     "bytes_per_launch": alg_bytes // K, "avg_launch_us": avg_s * 1e6,
-                     "launches_per_step": launches / K},
-        "e2e": ({"value": Ke / (e2e_ms / 1e3), "unit": "steps/s", "h2d_bytes_per_step": int(h2d),
-                 "d2h_bytes_per_step": int(d2h), "steps": Ke} if Ke > 0 else None),
-        "gpu_launches": launches,
-        "decode_launch": dec_cfg,
-        "three_call_path": three,
-        "stage2_v_rows_read_fraction": (vrows / max(1, kv_bytes // (2 * w.d * w.elem_bytes))) if elem else None,
-        "per_layer_launches": per_layer,
-        "setup": setup,
-        "clocks": clocks,
-        "size_floor": ({"bytes": int(alg_bytes // K), "kernels": "torch sum (read) and copy of a buffer of one "
-                        "step's algorithmic bytes, L2 flushed before each, median of 20",
-                        **floor, "step_us": avg_s * 1e6} if floor else None),
+                     "bytes_per_launch": r["alg_bytes"] // K, "avg_launch_us": avg_s * 1e6,
+                     "launches_per_step": r["launches"] / K,
+                     "frac_of_read_floor": (r["floor"]["read_us"] / (avg_s * 1e6)) if r["floor"] else None},
+        "e2e": r["e2e"],
+        "gpu_launches": r["launches"],
+        "decode_launch": r["dec_cfg"],
+        "three_call_path": r["three"],
+        "stage2_v_rows_read_fraction": (r["vrows"] / max(1, r["kv_bytes"] // (2 * w.d * w.elem_bytes))) if elem
+        else None,
+        "per_layer_launches": r["per_layer"],
+        "setup": r["setup"],
+        "clocks": r["clocks"],
+        "size_floor": ({"bytes": int(r["alg_bytes"] // K),
+                        "kernels": "hikv_read_floor (plain 16-byte streaming loads, best of 1/2/4 CTAs per SM) "
+                                   "and a torch copy of a buffer of one step's algorithmic bytes, L2 flushed "
+                                   "before each, median of 20",
+                        **r["floor"], "step_us": avg_s * 1e6} if r["floor"] else None),
     }
     if rank == 0 and not args.no_cpu_baseline:
         val, cores, done, sample, single = run_cpu_oracle(w, seed, min(64, w.steps), 2, budget_s=20.0,
-                                                  layers=oracle_sample_layers(w), budgets=budgets,
-                                                  element_budget=elem, steps_1thread=16)
+                                                          layers=oracle_sample_layers(w), budgets=budgets,
+                                                          element_budget=elem, steps_1thread=16)
         line["cpu_baseline"] = {"value": val, "unit": "steps/s", "cores": cores, "kind": "oracle",
                                 "sample": sample}
         if single:
             line["cpu_baseline"]["value_1thread"] = single[0]
             line["cpu_baseline"]["sample_1thread"] = f"{single[1]} further steps of the same sample on one thread"
+        stage("cpu baseline done")
+    if rank == 0 and world == 1 and not args.no_other_workloads and args.workload == WORKLOAD_INDEX \
+            and not args.layers and not args.full_cache and not elem and args.schedule in (None, "", "workload"):
+        line["other_workloads"] = other_workloads(args, dev, peak, stage)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -575,6 +773,9 @@ def bench_gpu(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--scaling", default="weak", choices=["weak", "strong"],
+                    help="N > 1: weak = the batch grows with the ranks (each rank as many units as one GPU "
+                         "alone); strong = the configured workload's units shared out")
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--e2e-steps", type=int, default=200)
@@ -592,6 +793,10 @@ def main():
     ap.add_argument("--spin-us", type=float, default=60.0)
     ap.add_argument("--impl", default="hikv", choices=["hikv", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="measure only the headline workload")
+    ap.add_argument("--other-steps", type=int, default=20, help="timed steps of each other workload")
+    ap.add_argument("--other-cpu-s", type=float, default=5.0, help="CPU-oracle seconds per other workload")
     ap.add_argument("--element-budget", type=int, default=0,
                     help="HiKV Stage II element budget B2 (0: exact attention)")
     ap.add_argument("--verbose", action="store_true", help="stage markers on stderr")

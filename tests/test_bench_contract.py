@@ -37,6 +37,10 @@ def test_reference_arm_prints_one_contract_line():
     assert d["value"] > 0 and d["unit"] == "steps/s" and d["higher_is_better"] is True
     assert d["warmup"] == 3 and d["vs_baseline"] is None
     assert d["config"]["workload"] == "llama3-8b-layer-b8-ctx8k"
+    # the GPU arm's config comes from the same function: the two lines agree
+    import bench
+    import workloads as W
+    assert d["config"] == json.loads(json.dumps(bench.workload_config(W.WORKLOADS[1])))
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     e2e = d["e2e"]

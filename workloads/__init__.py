@@ -91,6 +91,12 @@ class Workload:
     evict_every: int      # E: evict after every E decode steps
     heavy: Optional[str]  # heavy-hitter recipe
     nq: int = 16          # prefill observation window (queries scored)
+    # a shard of a larger workload (see shard()): its first layer and batch
+    # row there, and that workload's layer count (0: this one's).  Inputs
+    # and budgets are those of the larger workload's units.
+    layer0: int = 0
+    batch0: int = 0
+    layers_total: int = 0
 
     @property
     def group(self) -> int:
@@ -110,6 +116,14 @@ class Workload:
 
     def with_(self, **kw) -> "Workload":
         return replace(self, **kw)
+
+
+def shard(w: Workload, l0: int, l1: int, b0: int, b1: int) -> Workload:
+    """Layers [l0, l1) x batch rows [b0, b1) of w (every KV head) as a
+    workload of its own, whose inputs and budgets are w's for those units."""
+    assert 0 <= l0 < l1 <= w.layers and 0 <= b0 < b1 <= w.batch
+    return w.with_(name=f"{w.name}[l{l0}:{l1},b{b0}:{b1}]", layers=l1 - l0, batch=b1 - b0,
+                   layer0=w.layer0 + l0, batch0=w.batch0 + b0, layers_total=w.layers_total or w.layers)
 
 
 WORKLOADS = [
@@ -140,15 +154,16 @@ def budgets(w: Workload, seed: Optional[int] = None) -> np.ndarray:
     [64, 2048] with no renormalisation after the clamp.
     """
     seed = w.index if seed is None else seed
-    n = w.layers * w.hkv
+    n = (w.layers_total or w.layers) * w.hkv
+    rows = slice(w.layer0 * w.hkv, (w.layer0 + w.layers) * w.hkv)   # a shard's layers
     if w.budget == "dirichlet":
         rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 0xB0D6E7])))
         frac = rng.dirichlet(np.full(n, 0.5))
         raw = frac * (256.0 * n)
         b = np.floor(raw + 0.5).astype(np.int64)
         b = np.clip(b, 64, 2048)
-        return b.astype(np.int32)
-    return np.full(n, int(w.budget), dtype=np.int32)
+        return b.astype(np.int32)[rows].copy()
+    return np.full(n, int(w.budget), dtype=np.int32)[rows].copy()
 
 
 def retrieval_mask(w: Workload, frac: float, seed: Optional[int] = None) -> np.ndarray:
@@ -231,14 +246,15 @@ def gen_kv(w: Workload, layer0: int, nlayers: int, pos0: int, npos: int,
     v = np.empty_like(k)
     jobs = []
     for li in range(nlayers):
-        layer = layer0 + li
+        layer = w.layer0 + layer0 + li
         for b in range(w.batch):
-            hs = heavy_scale(w, seed, layer, b, upto=pos0 + npos)
+            bg = w.batch0 + b
+            hs = heavy_scale(w, seed, layer, bg, upto=pos0 + npos)
             sc = None if hs is None else np.ascontiguousarray(hs[pos0: pos0 + npos])
             assert sc is None or sc.size == npos
             for g in range(w.hkv):
-                jobs.append((seed, T_KEY, layer, b, g, pos0, npos, sc, k[li, b, g]))
-                jobs.append((seed, T_VALUE, layer, b, g, pos0, npos, None, v[li, b, g]))
+                jobs.append((seed, T_KEY, layer, bg, g, pos0, npos, sc, k[li, b, g]))
+                jobs.append((seed, T_VALUE, layer, bg, g, pos0, npos, None, v[li, b, g]))
     _fill_streams(jobs, w.d, bf)
     return k, v
 
@@ -251,6 +267,7 @@ def gen_kv_unit(w: Workload, layer: int, batch: int, g: int, pos0: int, npos: in
     dt = np.uint16 if bf else np.float32
     k = np.empty((npos, w.d), dtype=dt)
     v = np.empty_like(k)
+    layer, batch = w.layer0 + layer, w.batch0 + batch
     hs = heavy_scale(w, seed, layer, batch, upto=pos0 + npos)
     sc = None if hs is None else np.ascontiguousarray(hs[pos0: pos0 + npos])
     assert sc is None or sc.size == npos
@@ -270,7 +287,8 @@ def gen_q(w: Workload, layer0: int, nlayers: int, pos0: int, npos: int,
     for li in range(nlayers):
         for b in range(w.batch):
             for h in range(w.hq):
-                jobs.append((seed, T_QUERY, layer0 + li, b, h, pos0, npos, None, q[li, b, h]))
+                jobs.append((seed, T_QUERY, w.layer0 + layer0 + li, w.batch0 + b, h, pos0, npos, None,
+                             q[li, b, h]))
     _fill_streams(jobs, w.d, bf)
     return q
 
