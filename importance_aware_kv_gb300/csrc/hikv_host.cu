@@ -279,6 +279,11 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
     v.batch = c->B; v.hq = c->Hq; v.hkv = c->Hkv; v.group = G; v.d = c->d;
     v.sink = c->S; v.window = c->W;
     v.recent_only = f.importance_mode == 1;
+    // Home pages: a pool that holds every unit's max_tokens at once (the
+    // default) gives unit u the pages u * max_pages .. for good, so kernels
+    // compute a slot's page instead of loading it, and appends and evictions
+    // move no pages.  A smaller pool shares its pages through the free stack.
+    v.home_pages = c->pool_pages >= (int64_t)c->units * c->max_pages ? 1 : 0;
 
     const size_t U = (size_t)c->units;
     // hole lists: a unit cut from n <= cap to B leaves at most min(B, cap - B) holes
@@ -365,6 +370,12 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
     // initial device state
     std::vector<int32_t> stack((size_t)c->pool_pages);
     std::iota(stack.begin(), stack.end(), 0);
+    std::vector<int32_t> home_table, home_mapped;
+    if (v.home_pages) {
+        home_table.resize(U * (size_t)c->max_pages);
+        std::iota(home_table.begin(), home_table.end(), 0);
+        home_mapped.assign(U, c->max_pages);
+    }
     std::vector<int32_t>& order_all = c->order_all;
     std::vector<int32_t>& order_layer = c->order_layer;
     order_all.resize(U);
@@ -378,7 +389,7 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
         std::stable_sort(first, first + c->per_layer,
                          [&](int a, int b) { return c->budget_unit[a] > c->budget_unit[b]; });
     }
-    const int32_t top = (int32_t)c->pool_pages;
+    const int32_t top = v.home_pages ? 0 : (int32_t)c->pool_pages;   // home pages: the stack stays empty
     const int32_t minus1 = -1;
     (void)minus1;
     bool ok = cudaMemset(v.page_table, 0xFF, U * c->max_pages * 4) == cudaSuccess &&
@@ -397,6 +408,10 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
               cudaMemcpy(c->d_hole_off, hole_off.data(), U * 8, cudaMemcpyHostToDevice) == cudaSuccess &&
               cudaMemcpy(c->d_order_all, order_all.data(), U * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
               cudaMemcpy(c->d_order_layer, order_layer.data(), U * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
+              (!v.home_pages ||
+               (cudaMemcpy(v.page_table, home_table.data(), home_table.size() * 4, cudaMemcpyHostToDevice) ==
+                    cudaSuccess &&
+                cudaMemcpy(v.mapped, home_mapped.data(), U * 4, cudaMemcpyHostToDevice) == cudaSuccess)) &&
               cudaDeviceSynchronize() == cudaSuccess;
     if (!ok) {
         e = cudaGetLastError();
@@ -406,7 +421,8 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
     }
     c->len.assign(U, 0);
     c->next_pos.assign(U, 0);
-    c->mapped.assign(U, 0);
+    c->mapped.assign(U, v.home_pages ? c->max_pages : 0);
+    if (v.home_pages) c->pages_in_use = (int64_t)U * c->max_pages;
     c->fresh.assign(U, 0);
     *out = c;
     return HIKV_OK;
@@ -972,7 +988,7 @@ hikv_status hikv_evict(hikv_cache* c, int32_t layer0, int32_t nl, hikv_stream_t 
         if (c->len[u] > Bu) {
             c->len[u] = Bu;
             const int keep = pages_kept(Bu, c->P, c->max_pages);
-            if (c->mapped[u] > keep) {
+            if (!c->v.home_pages && c->mapped[u] > keep) {
                 c->pages_in_use -= c->mapped[u] - keep;
                 c->mapped[u] = keep;
             }

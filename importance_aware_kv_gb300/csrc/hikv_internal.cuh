@@ -50,8 +50,13 @@ struct View {
     int32_t batch, hq, hkv, group, d;
     int32_t sink, window;
     int32_t recent_only;  // HiKV Stage I: decode steps add mass only to pos >= t - window
+    int32_t home_pages;   // 1: page k of unit u is u * max_pages + k, mapped at create for good
+                          // (the pool holds every unit's max_tokens); 0: pages from the free stack
 };
 
+#ifndef HIKV_G8_GROUPS
+#define HIKV_G8_GROUPS 1
+#endif
 constexpr int kMaxCS = 16;   // most CTAs (cluster size) per unit in the decode kernel
 
 // Slots [t0, t1) of CTA c of a cs-CTA cluster for a unit of n tokens:
@@ -98,12 +103,19 @@ __host__ __device__ constexpr int dec_consumer_warps(int /*row_bytes*/, int /*gr
 // one per half of the group's query heads (two sets of dec_consumer_warps
 // warps rotating over the same tiles), so a warp carries the state of four
 // heads and twice the warps hide the tile loop's latency.
-__host__ __device__ constexpr int dec_head_groups(int group) { return group == 8 ? 2 : 1; }
+__host__ __device__ constexpr int dec_head_groups(int group) { return group == 8 ? HIKV_G8_GROUPS : 1; }
 __host__ __device__ constexpr int dec_stages(int row_bytes, int group) {
     return 2 * dec_consumer_warps(row_bytes, group);
 }
 
 __host__ __device__ inline int32_t ceil_div(int32_t a, int32_t b) { return (a + b - 1) / b; }
+
+// Page id of slot s of unit u: computed for home pages (no memory access),
+// else read from the page table.
+__device__ __forceinline__ int32_t unit_page(const View& v, int32_t u, int32_t s) {
+    return v.home_pages ? u * v.max_pages + (s >> v.page_shift)
+                        : v.page_table[(int64_t)u * v.max_pages + (s >> v.page_shift)];
+}
 
 // Address of the K (or V) row of slot s of unit u; nullptr if the page is bad.
 __device__ __forceinline__ uint8_t* row_ptr(const View& v, int32_t u, int32_t s, bool is_v) {

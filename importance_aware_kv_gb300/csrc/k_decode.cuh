@@ -104,6 +104,42 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
     return (uint32_t)((c >> 3) * (kDecTR * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
+// byte offset of 16-byte chunk c of row r in a tile of the cluster kernel:
+// rows of RBYTES bytes in order, as one 1-D bulk copy of a page's
+// consecutive rows lays them down (a warp reading whole rows, chunk by lane,
+// reads contiguous bytes: no bank conflicts without a swizzle)
+template <int RBYTES>
+__device__ __forceinline__ uint32_t lin(int r, int c) {
+    return (uint32_t)(r * RBYTES + (c << 4));
+}
+
+// Reduce-scatter of v[0, N) over the lanes that differ in the bits of M,
+// M / 2, ..., 1: at each level a lane keeps the half of its values that its
+// bit selects (upper half when set) and adds the partner's copy of that
+// half.  Afterwards v[0] holds, complete, the value whose index the lane's
+// bits spell out (most significant level first); once one value is left,
+// the remaining levels only sum it, so lanes differing in those bits hold
+// the same total.  Values of different indices are never added together.
+template <int M, int N>
+__device__ __forceinline__ void qk_reduce(float* v, int lane) {
+    if constexpr (M >= 1) {
+        if constexpr (N > 1) {
+            constexpr int H = N / 2;
+            const bool up = (lane & M) != 0;
+#pragma unroll
+            for (int j = 0; j < H; ++j) {
+                const float send = up ? v[j] : v[j + H];
+                const float keep = up ? v[j + H] : v[j];
+                v[j] = keep + __shfl_xor_sync(0xffffffffu, send, M);
+            }
+            qk_reduce<M / 2, H>(v, lane);
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], M);
+            qk_reduce<M / 2, 1>(v, lane);
+        }
+    }
+}
+
 // G consecutive floats (a row of p or logits, 4G-byte aligned), vectorised
 template <int G>
 __device__ __forceinline__ void store_group(float* dst, const float (&x)[G]) {
@@ -148,7 +184,6 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
     constexpr int NBOX = RB / 128;           // 128-byte TMA boxes per row
     constexpr int TB = kDecTR * RB;          // K (or V) tile bytes
     constexpr int CPR = RB / 16;             // 16-byte chunks per row
-    constexpr int CPL = CPR / 2;             // q.k: chunks per lane (half a row)
     constexpr int EPC = 16 / ESZ;            // elements per chunk
     constexpr int EPL = D / 32;              // p.v: elements per lane
     constexpr int LB = EPL * ESZ;            // p.v: bytes per lane
@@ -156,6 +191,24 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
     constexpr uint32_t QB = G * D * ESZ;     // bytes of one unit's q
     constexpr int kDecStages = dec_stages(RB, G);
     static_assert(kDecStages % kDecNGW == 0, "each stage must always be consumed by the same warp of each group");
+    // q.k mapping: QK_LPR lanes share a K row, each taking one 16-byte chunk
+    // of it against the same dimensions of q, which the lane keeps in
+    // registers; a warp step covers QK_RPW rows.  A tile's QK_STEPS steps
+    // run in QK_NSUB sub-blocks of QK_SUB steps, whose QK_NV = QK_SUB * GW
+    // (row, head) partial sums are reduce-scattered over the row's lanes:
+    // every lane ends each sub-block holding one finished logit, of one
+    // fixed head (QK_DUP lanes hold the same one when QK_NV < QK_LPR).  The
+    // per-tile shared-memory reads are then the K tile itself, not q again
+    // for every row.
+    constexpr int QK_LPR = RB / 16;
+    constexpr int QK_RPW = 32 / QK_LPR;
+    constexpr int QK_STEPS = kDecTR / QK_RPW;
+    constexpr int QK_EPL = 16 / ESZ;
+    constexpr int QK_SUB = (QK_LPR / GW) > QK_STEPS ? QK_STEPS : (QK_LPR / GW);
+    constexpr int QK_NSUB = QK_STEPS / QK_SUB;
+    constexpr int QK_NV = QK_SUB * GW;
+    constexpr int QK_DUP = QK_LPR / QK_NV;
+    static_assert(QK_SUB >= 1 && QK_STEPS % QK_SUB == 0 && QK_LPR % QK_NV == 0, "one logit per lane and sub-block");
     static_assert(EPL % 2 == 0 && EPC % 2 == 0, "pairs");
     using Raw = typename RawVec<LB>::type;
 
@@ -211,7 +264,7 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
         dec_range(du.n, CS, c, t0, t1);
         const int32_t pg0 = t0 >> v.page_shift;
         const int32_t npg = t1 > t0 ? ((t1 - 1) >> v.page_shift) - pg0 + 1 : 0;
-        if (lane < npg) pre_pg = v.page_table[(int64_t)du.u * v.max_pages + pg0 + lane];
+        if (lane < npg && !v.home_pages) pre_pg = v.page_table[(int64_t)du.u * v.max_pages + pg0 + lane];
     }
 
     if (tid == 0) {
@@ -273,9 +326,11 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                     *abort_flag = 1;
                 }
             }
-            for (int j = lane; j < min(npg, kDecMaxPg); j += 32) pg_s[j] = (k == 0 && j < 32) ? pre_pg : ptab[pg0 + j];
+            if (!v.home_pages)
+                for (int j = lane; j < min(npg, kDecMaxPg); j += 32) pg_s[j] = (k == 0 && j < 32) ? pre_pg : ptab[pg0 + j];
             __syncwarp();
             auto page_of = [&](int32_t s0) -> int32_t {
+                if (v.home_pages) return du.u * v.max_pages + (s0 >> v.page_shift);
                 const int32_t pk = (s0 >> v.page_shift) - pg0;
                 return pk < kDecMaxPg ? pg_s[pk] : ptab[pg0 + pk];
             };
@@ -314,15 +369,13 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                         break;
                     }
                     if (pf > 0 && i + pf < nt) prefetch_tile(i + pf);
-                    const int32_t yk = pg * 2 * v.page_tokens + (s0 & (v.page_tokens - 1));
+                    // the tile's 16 K rows and 16 V rows are contiguous in the page:
+                    // one 1-D bulk copy each
+                    const uint8_t* kb = v.pool + (int64_t)pg * v.page_bytes + (int64_t)(s0 & (v.page_tokens - 1)) * RB;
                     uint8_t* dst = ring + st * 2 * TB;
                     mbar_arrive_expect_tx(&full[st], 2 * TB);
-#pragma unroll
-                    for (int bx = 0; bx < NBOX; ++bx) {
-                        tma_load_2d(dst + bx * (kDecTR * 128), &tmap, bx * (128 / ESZ), yk, &full[st]);
-                        tma_load_2d(dst + TB + bx * (kDecTR * 128), &tmap, bx * (128 / ESZ), yk + v.page_tokens,
-                                    &full[st]);
-                    }
+                    bulk_g2s(dst, kb, (uint32_t)TB, &full[st]);
+                    bulk_g2s(dst + TB, kb + (int64_t)v.page_tokens * RB, (uint32_t)TB, &full[st]);
                 }
             }
             gi = __shfl_sync(0xffffffffu, gi, 0);
@@ -344,8 +397,12 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
     const int wg = warp / kDecNGW, wi = warp % kDecNGW;   // head group, place in the tile rotation
     const int h0 = wg * GW;                               // this warp's heads: h0 .. h0 + GW - 1
     float* ps = ps_all + warp * (kDecTR * GW);     // [16][GW] p of the tile
-    const int qr = lane & 15;           // q.k: tile row of this lane
-    const int qh = lane >> 4;           // q.k: half of the row
+    const int qk_c = lane % QK_LPR;                 // q.k: chunk of the row this lane reads
+    const int qk_rg = lane / QK_LPR;                // q.k: row of the warp step
+    const int qk_k = qk_c / QK_DUP;                 // q.k: index of the logit this lane ends with
+    const int qk_step = qk_k / GW;                  //      its step within the sub-block
+    const int hk = qk_k % GW;                       //      its head (of this warp's GW)
+    const bool qk_own = (qk_c % QK_DUP) == 0;       //      the lane that records it
     const int pv_chunk = (lane * LB) >> 4, pv_in = (lane * LB) & 15;
     int gi_base = 0;
 
@@ -395,7 +452,7 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
         const bool tail_staged = a.fused && ts == sn;
         Raw tail_k{}, tail_v{};
         if (tail_here && !tail_staged) {
-            const int32_t pg = v.page_table[(int64_t)u * v.max_pages + (ts >> v.page_shift)];
+            const int32_t pg = unit_page(v, u, ts);
             if (pg >= 0 && pg < v.pool_pages) {
                 const uint8_t* kr = v.pool + (int64_t)pg * v.page_bytes + (int64_t)(ts & (v.page_tokens - 1)) * RB;
                 tail_k = *reinterpret_cast<const Raw*>(kr + lane * LB);
@@ -417,12 +474,23 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
         }
         named_bar_sync(1, NCT);
 
-        float m_w[GW], l_w[GW];
+        // q of this warp's heads at this lane's chunk, in registers
+        float2 qreg[GW][QK_EPL / 2];
+#pragma unroll
+        for (int h = 0; h < GW; ++h)
+#pragma unroll
+            for (int e = 0; e < QK_EPL / 2; ++e)
+                qreg[h][e] = *reinterpret_cast<const float2*>(q_s + (h0 + h) * D + qk_c * QK_EPL + 2 * e);
+        // softmax state: the reference m_w of every head (the same in all
+        // lanes), this lane's share of its head's row sum, and the tail row's
+        // share of each head's (lane 0)
+        float m_w[GW], l_tail[GW];
+        float m_own = -INFINITY, l_own = 0.f;
         float2 o2[GW][EPL / 2];
 #pragma unroll
         for (int h = 0; h < GW; ++h) {
             m_w[h] = -INFINITY;
-            l_w[h] = 0.f;
+            l_tail[h] = 0.f;
 #pragma unroll
             for (int e = 0; e < EPL / 2; ++e) o2[h][e] = make_float2(0.f, 0.f);
         }
@@ -446,12 +514,12 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                 const int r = sn - s0;
                 const Raw nk = *reinterpret_cast<const Raw*>(nrow + lane * LB);
                 const Raw nv = *reinterpret_cast<const Raw*>(nrow + RB + lane * LB);
-                *reinterpret_cast<Raw*>(ktile + swz(r, pv_chunk) + pv_in) = nk;
-                *reinterpret_cast<Raw*>(vtile + swz(r, pv_chunk) + pv_in) = nv;
+                *reinterpret_cast<Raw*>(ktile + lin<RB>(r, pv_chunk) + pv_in) = nk;
+                *reinterpret_cast<Raw*>(vtile + lin<RB>(r, pv_chunk) + pv_in) = nv;
                 fence_proxy_async_smem();   // the stage is refilled by TMA later
                 // (both head groups' warps patch the landed tile with the same
                 // bytes before reading it; one of them writes the pool)
-                const int32_t pg = wg == 0 ? v.page_table[(int64_t)u * v.max_pages + (sn >> v.page_shift)] : -1;
+                const int32_t pg = wg == 0 ? unit_page(v, u, sn) : -1;
                 if (pg >= 0 && pg < v.pool_pages) {
                     uint8_t* kd = v.pool + (int64_t)pg * v.page_bytes + (int64_t)(sn & (v.page_tokens - 1)) * RB;
                     *reinterpret_cast<Raw*>(kd + lane * LB) = nk;
@@ -460,34 +528,30 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                 __syncwarp();
             }
 
-            // ---- q.k: this lane's half row ----
-            float2 acc[GW];
+            // ---- q.k: per sub-block, each lane's chunk of QK_SUB rows against
+            // q in registers, then the partial sums reduce-scattered ----
+            float sv[QK_NSUB];
 #pragma unroll
-            for (int h = 0; h < GW; ++h) acc[h] = make_float2(0.f, 0.f);
+            for (int sb = 0; sb < QK_NSUB; ++sb) {
+                float part[QK_NV];
 #pragma unroll
-            for (int j = 0; j < CPL; ++j) {
-                const int cidx = 2 * j + qh;   // halves interleave: their q reads fall in different banks
-                const uint4 raw = *reinterpret_cast<const uint4*>(ktile + swz(qr, cidx));
-                float x[EPC];
-                Widen<T, EPC>::run(raw, x);
+                for (int j = 0; j < QK_SUB; ++j) {
+                    const int r = (sb * QK_SUB + j) * QK_RPW + qk_rg;
+                    const uint4 raw = *reinterpret_cast<const uint4*>(ktile + lin<RB>(r, qk_c));
+                    float x[QK_EPL];
+                    Widen<T, QK_EPL>::run(raw, x);
 #pragma unroll
-                for (int h = 0; h < GW; ++h) {
-                    const float* qp = q_s + (h0 + h) * D + cidx * EPC;
+                    for (int h = 0; h < GW; ++h) {
+                        float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int e = 0; e < EPC; e += 4) {
-                        const float4 q4 = *reinterpret_cast<const float4*>(qp + e);
-                        acc[h] = ffma2(make_float2(x[e], x[e + 1]), make_float2(q4.x, q4.y), acc[h]);
-                        acc[h] = ffma2(make_float2(x[e + 2], x[e + 3]), make_float2(q4.z, q4.w), acc[h]);
+                        for (int e = 0; e < QK_EPL / 2; ++e)
+                            acc = ffma2(make_float2(x[2 * e], x[2 * e + 1]), qreg[h][e], acc);
+                        part[j * GW + h] = acc.x + acc.y;
                     }
                 }
-            }
-            const bool rv = qr >= lo_r && qr < hi_r;
-            float s[GW];
-#pragma unroll
-            for (int h = 0; h < GW; ++h) {
-                float t = acc[h].x + acc[h].y;
-                t += __shfl_xor_sync(0xffffffffu, t, 16);
-                s[h] = rv ? t : -INFINITY;
+                qk_reduce<QK_LPR / 2, QK_NV>(part, lane);
+                const int r = (sb * QK_SUB + qk_step) * QK_RPW + qk_rg;
+                sv[sb] = (r >= lo_r && r < hi_r) ? part[0] : -INFINITY;   // invalid rows: -inf
             }
             // ---- online softmax over this tile, lazily rescaled: the
             // reference m_w moves (to the tile max) only when a logit exceeds
@@ -495,17 +559,24 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
             // per lane until the unit's merge ----
             bool big = false;
 #pragma unroll
-            for (int h = 0; h < GW; ++h) big |= s[h] > m_w[h] + kDecLazy;   // invalid rows: -inf
+            for (int sb = 0; sb < QK_NSUB; ++sb) big |= sv[sb] > m_own + kDecLazy;
             if (__any_sync(0xffffffffu, big)) {
+                float tmax = sv[0];
+#pragma unroll
+                for (int sb = 1; sb < QK_NSUB; ++sb) tmax = fmaxf(tmax, sv[sb]);
 #pragma unroll
                 for (int h = 0; h < GW; ++h) {
-                    float mt = s[h];
+                    float mt = hk == h ? tmax : -INFINITY;
 #pragma unroll
-                    for (int o = 8; o >= 1; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+                    for (int o = 16; o >= 1; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
                     const float mn = fmaxf(m_w[h], mt);
                     const float scl = exp2f(m_w[h] - mn);   // 1 when unchanged, 0 from -inf
                     m_w[h] = mn;
-                    l_w[h] *= scl;
+                    l_tail[h] *= scl;
+                    if (hk == h) {
+                        l_own *= scl;
+                        m_own = mn;
+                    }
 #pragma unroll
                     for (int e = 0; e < EPL / 2; ++e) {
                         o2[h][e].x *= scl;
@@ -513,16 +584,17 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                     }
                 }
             }
-            float p[GW];
 #pragma unroll
-            for (int h = 0; h < GW; ++h) {
-                p[h] = rv ? exp2f(s[h] - m_w[h]) : 0.f;
-                l_w[h] += p[h];   // this lane's row; both halves of a row hold the same p
-            }
-            if (qh == 0) {
-                store_group<GW>(ps + qr * GW, p);
-                if (rv && (!SMEM_S || s0 + qr - s_off < a.chunk_cap))
-                    store_group<GW>(Sb + (int64_t)(s0 + qr - s_off) * G + h0, s);   // this group's heads of the row
+            for (int sb = 0; sb < QK_NSUB; ++sb) {
+                const int r = (sb * QK_SUB + qk_step) * QK_RPW + qk_rg;
+                const bool rv = sv[sb] > -INFINITY;
+                const float p = rv ? exp2f(sv[sb] - m_own) : 0.f;
+                if (qk_own) {
+                    l_own += p;
+                    ps[r * GW + hk] = p;
+                    if (rv && (!SMEM_S || s0 + r - s_off < a.chunk_cap))
+                        Sb[(int64_t)(s0 + r - s_off) * G + h0 + hk] = sv[sb];   // for the importance pass
+                }
             }
             __syncwarp();
             // ---- p.v over the tile's valid rows (unrolled; invalid rows skipped, their
@@ -530,7 +602,7 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
 #pragma unroll
             for (int r = 0; r < kDecTR; ++r) {
                 if (r < lo_r || r >= hi_r) continue;
-                const Raw raw = *reinterpret_cast<const Raw*>(vtile + swz(r, pv_chunk) + pv_in);
+                const Raw raw = *reinterpret_cast<const Raw*>(vtile + lin<RB>(r, pv_chunk) + pv_in);
                 float x[EPL];
                 Widen<T, EPL>::run(raw, x);
                 const float* pr = ps + r * GW;
@@ -591,7 +663,11 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                     const float mn = fmaxf(m_w[h], s[h]);
                     const float scl = exp2f(m_w[h] - mn);
                     m_w[h] = mn;
-                    l_w[h] *= scl;
+                    l_tail[h] *= scl;
+                    if (hk == h) {
+                        l_own *= scl;
+                        m_own = mn;
+                    }
 #pragma unroll
                     for (int e = 0; e < EPL / 2; ++e) {
                         o2[h][e].x *= scl;
@@ -602,14 +678,14 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
 #pragma unroll
             for (int h = 0; h < GW; ++h) {
                 const float p = exp2f(s[h] - m_w[h]);
-                if ((lane & 15) == 0) l_w[h] += p;   // once in each half's row sum
+                if (lane == 0) l_tail[h] += p;
 #pragma unroll
                 for (int e = 0; e < EPL / 2; ++e)
                     o2[h][e] = ffma2(make_float2(xv[2 * e], xv[2 * e + 1]), make_float2(p, p), o2[h][e]);
             }
             if (lane == 0 && (!SMEM_S || ts - s_off < a.chunk_cap)) store_group<GW>(Sb + (int64_t)(ts - s_off) * G + h0, s);
             if (tail_staged && wg == 0) {   // the new token's rows into the pool for later steps
-                const int32_t pg = v.page_table[(int64_t)u * v.max_pages + (sn >> v.page_shift)];
+                const int32_t pg = unit_page(v, u, sn);
                 if (pg >= 0 && pg < v.pool_pages) {
                     uint8_t* kd = v.pool + (int64_t)pg * v.page_bytes + (int64_t)(sn & (v.page_tokens - 1)) * RB;
                     *reinterpret_cast<Raw*>(kd + lane * LB) = tail_k;
@@ -637,10 +713,15 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
         // ---- CTA merge of the warp states ----
         // (state of head h0 + h of rotation place wi at [wi][h0 + h]: a head's
         // partials come from the kDecNGW warps of its head group)
+        float l_w[GW];   // each head's row sum over this warp's rows
 #pragma unroll
-        for (int h = 0; h < GW; ++h)   // sum of the per-lane row sums over the 16 rows
+        for (int h = 0; h < GW; ++h) {
+            float t = (qk_own && hk == h) ? l_own : 0.f;
+            if (lane == 0) t += l_tail[h];
 #pragma unroll
-            for (int o = 8; o >= 1; o >>= 1) l_w[h] += __shfl_xor_sync(0xffffffffu, l_w[h], o);
+            for (int o = 16; o >= 1; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+            l_w[h] = t;
+        }
         if (lane == 0) {
 #pragma unroll
             for (int h = 0; h < GW; ++h) {
@@ -842,7 +923,7 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
         if (a.fused && a.evict && c == 0 && warp == 0) {
             const int32_t vs = wslot[0];
             if (vs >= 0 && vs != sn) {
-                const int32_t pd = v.page_table[(int64_t)u * v.max_pages + (vs >> v.page_shift)];
+                const int32_t pd = unit_page(v, u, vs);
                 if (pd >= 0 && pd < v.pool_pages) {
                     uint8_t* kd = v.pool + (int64_t)pd * v.page_bytes + (int64_t)(vs & (v.page_tokens - 1)) * RB;
                     *reinterpret_cast<Raw*>(kd + lane * LB) = *reinterpret_cast<const Raw*>(nrow + lane * LB);

@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(kEvThreads) k_evict_general(EvictArgs a) {
         // return whole pages past slot B (one spare slot kept for the next append)
         const int32_t keep = pages_kept(B, v.page_tokens, v.max_pages);
         const int32_t m = v.mapped[u];
-        if (m > keep) {
+        if (!v.home_pages && m > keep) {
             const int32_t cnt = m - keep;
             const int32_t old = atomicAdd(v.free_top, cnt);
             if (old + cnt > v.pool_pages) atomicOr(v.err, DEVERR_POOL);

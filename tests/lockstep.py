@@ -72,7 +72,7 @@ class Lockstep:
     def __init__(self, w: W.Workload, seed=None, sample_layers=None, cs=None, budgets=None,
                  device="cuda", layer_chunk=None, full_cache=False, page_tokens=64,
                  check_kv=True, full_twin_layers=None, pool_kernel=0, importance_mode=0, small_mode=None,
-                 element_budget=0, prefill_band=0):
+                 element_budget=0, prefill_band=0, pool_pages=0):
         import importance_aware_kv_gb300 as hk
         self.hk = hk
         self.w = w
@@ -97,7 +97,7 @@ class Lockstep:
                 self.budgets, w.total_positions, page_tokens=page_tokens,
                 max_window_queries=max(32, w.nq), pool_kernel=pool_kernel,
                 importance_mode=importance_mode, element_budget=element_budget,
-                band_scoring=1 if prefill_band > 0 else 0))
+                band_scoring=1 if prefill_band > 0 else 0, pool_pages=pool_pages))
         finally:
             if cs is not None:
                 os.environ.pop("HIKV_DECODE_CS", None)

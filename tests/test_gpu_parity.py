@@ -141,6 +141,15 @@ def test_page_size_variants(fused):
     _run(SMALL, page_tokens=256, fused=fused)
 
 
+@FUSED
+def test_shared_page_pool(fused):
+    # a pool smaller than every unit's max_tokens (8 units x 5 pages of 64,
+    # against 8 x 6 for home pages): pages come from the shared free stack,
+    # the decode kernel reads page ids from the table, the cut returns pages
+    w = SMALL
+    _run(w, pool_pages=w.units * 5, fused=fused)
+
+
 def test_long_chunk_global_logits_path():
     # 50k tokens in one unit at G = 8: even 16 CTAs leave chunks whose logits
     # exceed shared memory, so the kernel keeps them in the global buffer
