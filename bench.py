@@ -9,9 +9,13 @@ as `three_call_path`).  Headline workload: the Llama-3-8B-shaped layer (batch
 8, 32 query / 8 KV heads, d 128, bf16 K/V, 8192-token prompt, budget 1024, 4
 sinks, 64-token window, eviction every step), seeded synthetic inputs resident
 in HBM before timing.  The decode stream continues past the workload's 256
-steps when more are timed; per-step work is fixed by the budget.  The
-retained set (34 MB) fits in L2, so L2 is flushed (256 MB write) between
-timed steps, outside the timed events.
+steps when more are timed; per-step work is fixed by the budget.  One step
+reads 34.5 MB, which would fit in L2: the timed steps run in turn on copies
+of the layer's cache holding together more than twice the L2, so each
+step's K/V comes cold from HBM while code and small inputs stay warm, as in
+a model's decode loop (the same steps after a 256 MB L2 flush are timed
+too, `flushed_l2_steps`).  Larger workloads read more than twice the L2 per
+step and need neither.
 
 The same run then measures the other workloads (`other_workloads`): the
 32-layer 32K-context stack evicting every 16 steps, the HeadKV Dirichlet
@@ -263,7 +267,36 @@ def schedule_budgets(w, seed, schedule):
     raise ValueError(f"unknown schedule {schedule!r}")
 
 
-def workload_config(w, schedule="workload", element_budget=0, full_cache=False, world=1, scaling="weak"):
+L2_ASSUMED = 160_000_000   # bytes; above a GB300's 129 MB L2, so NC copies are surely colder than L2
+
+
+def cold_copies(w, budgets=None, full_cache=False):
+    """(NC, bytes of one step): how many copies of the cache the timed steps
+    rotate through so that each step's K/V is cold -- 1 when a step reads at
+    least twice the L2 itself."""
+    import workloads as W
+    b = W.budgets(w) if budgets is None else np.asarray(budgets)
+    n_est = np.minimum(np.repeat(b.astype(np.int64).reshape(w.layers, w.hkv), w.batch, axis=0).reshape(-1),
+                       w.prompt) + 1
+    if full_cache:
+        n_est = np.full(w.units, w.prompt + 1, np.int64)
+    est = step_bytes(w, n_est)
+    nc = 1 if est >= 2 * L2_ASSUMED else int(-(-2 * L2_ASSUMED // max(1, est)))
+    return (nc if nc <= 16 else 1), est   # more than 16 copies: flush L2 instead
+
+
+def l2_policy(w, full_cache=False):
+    nc, est = cold_copies(w, None, full_cache)
+    if nc == 1 and est < 2 * L2_ASSUMED:
+        return "flushed between timed steps (256 MB write, outside the timed events)"
+    if nc == 1:
+        return f"inputs larger than L2: one step reads {est / 1e6:.0f} MB, no flush"
+    return (f"inputs larger than L2: {nc} copies of the cache ({nc * est / 1e6:.0f} MB of K/V) decoded in turn, "
+            f"no flush")
+
+
+def workload_config(w, schedule="workload", element_budget=0, full_cache=False, world=1, scaling="weak",
+                    l2_mode="auto"):
     """The `config` of a bench line: the workload and the run's options only
     (no measured values), the same for the GPU arm and the reference arm."""
     return {"workload": w.name + ("-full-cache" if full_cache else ""), "layers": w.layers, "batch": w.batch,
@@ -271,7 +304,8 @@ def workload_config(w, schedule="workload", element_budget=0, full_cache=False, 
             "budget": "full cache" if full_cache else w.budget, "sink": w.sink, "window": w.window,
             "evict_every": w.evict_every, "budget_schedule": schedule or "workload",
             "element_budget": element_budget,
-            "l2": "flushed between timed steps (256 MB write, outside the timed events)",
+            "l2": (l2_policy(w, full_cache) if l2_mode != "flush"
+                   else "flushed between timed steps (256 MB write, outside the timed events)"),
             "parallelism": (f"units of one workload ({'the configured one' if scaling == 'strong' else f'batch x{world}'})"
                             f" shared out across {world} ranks: batch rows, else layers balanced by Sum B_u;"
                             " no collective" if world > 1 else "one GPU")}
@@ -402,9 +436,21 @@ def measure(w, seed, dev, opts, stage=lambda m: None):
     if opts["full_cache"]:   # no eviction: every unit keeps its whole context
         budgets = np.full_like(budgets, w.prompt + total_steps + 1)
     elem = opts["element_budget"] if 0 < opts["element_budget"] < w.d else 0
-    cache = hk.Cache(hk.CacheConfig(w.layers, w.batch, w.hq, w.hkv, w.d, w.dtype, w.sink, w.window,
-                                    budgets, w.prompt + total_steps + 1, element_budget=elem))
-    stage(f"{w.name}: cache created")
+    # Cold data between timed steps.  A step whose bytes are at least twice
+    # the L2 evicts its own data; a smaller one (one layer) runs on NC copies
+    # of the cache in turn, NC x its bytes >= twice the L2, so each step's
+    # K/V is cold while code and the next inputs stay warm as in a model's
+    # decode loop; the same steps after an L2 flush (256 MB write) are timed
+    # too and reported beside them.
+    NC, est = cold_copies(w, budgets, opts["full_cache"])
+    l2 = L2_ASSUMED
+    if opts.get("l2_mode") == "flush":   # the earlier method: one cache, a 256 MB write before every step
+        NC, l2 = 1, float("inf")
+    cfg = hk.CacheConfig(w.layers, w.batch, w.hq, w.hkv, w.d, w.dtype, w.sink, w.window,
+                         budgets, w.prompt + total_steps * NC + 1, element_budget=elem)
+    caches = [hk.Cache(cfg) for _ in range(NC)]
+    cache = caches[0]
+    stage(f"{w.name}: {NC} cache(s) created")
     # ---- setup (untimed): prompt in layer chunks, window scoring, cut to budget ----
     stream = torch.cuda.current_stream()
     lc = layer_chunk(w)
@@ -416,7 +462,8 @@ def measure(w, seed, dev, opts, stage=lambda m: None):
             k, v = W.gen_kv(w, l0, nl, 0, w.prompt, seed)
             dk, dv = W.to_torch(k).to(dev), W.to_torch(v).to(dev)
             del k, v
-        cache.append(dk, dv, layer0=l0)
+        for c_ in caches:
+            c_.append(dk, dv, layer0=l0)
         del dk, dv
     dq_win = W.to_torch(W.gen_q(w, 0, L, w.prompt - w.nq, w.nq, seed)).to(dev)
     se = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
@@ -426,6 +473,9 @@ def measure(w, seed, dev, opts, stage=lambda m: None):
     se[1].record(stream)
     cache.evict()                        # a0: the cut to the budget
     se[2].record(stream)
+    for c_ in caches[1:]:
+        c_.score_window(dq_win)
+        c_.evict()
     torch.cuda.synchronize()
     setup = {"prompt_tokens_per_unit": w.prompt, "window_queries": w.nq,
              "prompt_source": ("device (torch seeded N(0,1) x heavy-hitter factors)"
@@ -447,28 +497,31 @@ def measure(w, seed, dev, opts, stage=lambda m: None):
     out = torch.empty_like(dqs[0])
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     E = w.evict_every if not opts["full_cache"] else 1
-    counter = {"s": 0}                    # decode steps taken so far (eviction cadence)
+    taken = [0] * NC                      # decode steps each cache has taken (its eviction cadence)
+    turn = {"i": 0}
 
     def next_step():
-        s = counter["s"]
-        counter["s"] += 1
-        return s % R, (s + 1) % E == 0
+        """The next cache in turn, its input index and whether it evicts."""
+        ci = turn["i"] % NC
+        turn["i"] += 1
+        s = taken[ci]
+        taken[ci] += 1
+        return caches[ci], s % R, (s + 1) % E == 0
 
-    def bytes_now():
-        return step_bytes(w, cache.lengths().astype(np.int64) + 1)
+    def peek():
+        return caches[turn["i"] % NC]
 
     def step_fused():
-        r, ev_ = next_step()
-        cache.step(dks[r], dvs[r], dqs[r], out, evict=ev_)
+        c_, r, ev_ = next_step()
+        c_.step(dks[r], dvs[r], dqs[r], out, evict=ev_)
 
     stage(f"{w.name}: setup done")
-    for _ in range(Wu):
-        flush.fill_(1.0)
+    for _ in range(max(Wu, NC)):
         step_fused()
     torch.cuda.synchronize()
     # A spin kernel before each timed step lets the host enqueue the whole
     # step before the GPU reaches it, so host launch overhead never shows up
-    # inside the timed events (the flush and the spin are outside them).
+    # inside the timed events (the spin is outside them).
     spin_cycles = int(opts["spin_us"] * 2.0e3)
 
     # ---- timed: the single-call step (append + decode + evict in one launch) ----
@@ -480,23 +533,25 @@ def measure(w, seed, dev, opts, stage=lambda m: None):
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
-    launches0 = cache.kernel_launches()
-    vrows0 = cache.element_rows() if elem else 0
+    launches0 = sum(c_.kernel_launches() for c_ in caches)
+    vrows0 = sum(c_.element_rows() for c_ in caches) if elem else 0
     alg_bytes = 0
     kv_bytes = 0
     for i in range(K):
-        alg_bytes += bytes_now()
-        kv_bytes += int((2 * (cache.lengths().astype(np.int64) + 1) * w.d * w.elem_bytes).sum())
-        flush.fill_(float(i))
+        n_now = peek().lengths().astype(np.int64) + 1
+        alg_bytes += step_bytes(w, n_now)
+        kv_bytes += int((2 * n_now * w.d * w.elem_bytes).sum())
+        if NC == 1 and est < 2 * l2:
+            flush.fill_(float(i))
         torch.cuda._sleep(spin_cycles)
         e0, e1 = ev[i]
         e0.record(stream)
         step_fused()
         e1.record(stream)
     torch.cuda.synchronize()
-    launches = cache.kernel_launches() - launches0
+    launches = sum(c_.kernel_launches() for c_ in caches) - launches0
     dec_cfg = cache.last_decode_config()
-    vrows = cache.element_rows() - vrows0 if elem else 0
+    vrows = sum(c_.element_rows() for c_ in caches) - vrows0 if elem else 0
     if elem:
         # HiKV Stage II reads whole K rows but only the V rows some head kept
         v_all = kv_bytes // 2
@@ -508,20 +563,38 @@ def measure(w, seed, dev, opts, stage=lambda m: None):
     t_total = max_over_ranks(sum(step_ms) / 1e3, opts["world"], dev)
     stage(f"{w.name}: timed fused steps done")
 
+    # ---- the same single-call steps, each after an L2 flush (cold code and
+    # metadata as well as data) ----
+    flushed = None
+    if NC > 1 and opts.get("flushed_steps", 0) > 0:
+        KF = opts["flushed_steps"]
+        evf = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(KF)]
+        for i in range(KF):
+            flush.fill_(float(i))
+            torch.cuda._sleep(spin_cycles)
+            evf[i][0].record(stream)
+            step_fused()
+            evf[i][1].record(stream)
+        torch.cuda.synchronize()
+        msf = [a.elapsed_time(b) for a, b in evf]
+        flushed = {"steps": KF, "ms_per_step": sum(msf) / KF, "steps_per_s": KF / (sum(msf) / 1e3),
+                   "l2": "256 MB write before each step"}
+
     # ---- the same steps as three calls (append, decode_step, evict when due) ----
     ev3 = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(K3)]
     for i in range(K3):
-        r, ev_ = next_step()
-        flush.fill_(float(i))
+        c_, r, ev_ = next_step()
+        if NC == 1 and est < 2 * l2:
+            flush.fill_(float(i))
         torch.cuda._sleep(spin_cycles)
         e0, e1, e2, e3 = ev3[i]
         e0.record(stream)
-        cache.append(dks[r], dvs[r])
+        c_.append(dks[r], dvs[r])
         e1.record(stream)
-        cache.decode_step(dqs[r], out)
+        c_.decode_step(dqs[r], out)
         e2.record(stream)
         if ev_:
-            cache.evict()
+            c_.evict()
         e3.record(stream)
     torch.cuda.synchronize()
     three = None
@@ -536,20 +609,18 @@ def measure(w, seed, dev, opts, stage=lambda m: None):
     per_layer = None
     if KL > 0 and L > 1:
         evl = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(KL)]
-        pl_launch0 = cache.kernel_launches()
+        pl_launch0 = sum(c_.kernel_launches() for c_ in caches)
         for i in range(KL):
-            r, ev_ = next_step()
-            flush.fill_(float(i))
+            c_, r, ev_ = next_step()
             torch.cuda._sleep(spin_cycles + L * 40000)   # room to enqueue L calls
             e0, e1 = evl[i]
             e0.record(stream)
             for l in range(L):
-                cache.step(dks[r][l:l + 1], dvs[r][l:l + 1], dqs[r][l:l + 1], out[l:l + 1], evict=ev_,
-                           layer0=l)
+                c_.step(dks[r][l:l + 1], dvs[r][l:l + 1], dqs[r][l:l + 1], out[l:l + 1], evict=ev_, layer0=l)
             e1.record(stream)
         torch.cuda.synchronize()
         msl = [e0.elapsed_time(e1) for (e0, e1) in evl]
-        per_layer = {"steps": KL, "launches_per_step": (cache.kernel_launches() - pl_launch0) / KL,
+        per_layer = {"steps": KL, "launches_per_step": (sum(c_.kernel_launches() for c_ in caches) - pl_launch0) / KL,
                      "ms_per_step": sum(msl) / KL, "steps_per_s": KL / (sum(msl) / 1e3)}
 
     # ---- e2e through the C ABI with pinned host buffers: every step copies
@@ -569,50 +640,57 @@ def measure(w, seed, dev, opts, stage=lambda m: None):
     e_end = torch.cuda.Event(enable_timing=True)
     e2e_ms = 0.0
     for i in range(Ke):
-        r, ev_ = next_step()
-        flush.fill_(float(i))
+        c_, r, ev_ = next_step()
+        if NC == 1 and est < 2 * l2:
+            flush.fill_(float(i))
         e_start.record(stream)
         in_dev.copy_(packed[r], non_blocking=True)
-        cache.step(k_dev, v_dev, q_dev, out, evict=ev_)
+        c_.step(k_dev, v_dev, q_dev, out, evict=ev_)
         out_host.copy_(out, non_blocking=True)
         e_end.record(stream)
         e_end.synchronize()
         e2e_ms += e_start.elapsed_time(e_end)
     h2d = packed[0].nbytes
     d2h = out_host.nbytes
-    cache.device_status()
+    for c_ in caches:
+        c_.device_status()
     lens = cache.lengths()
-    cache.close()
-    del dks, dvs, dqs, packed, in_dev
+    for c_ in caches:
+        c_.close()
+    del dks, dvs, dqs, packed, in_dev, caches, cache
     stage(f"{w.name}: e2e steps done")
 
     # ---- read floor (context for the roofline fraction): a plain streaming
     # read, and a torch copy, of one step's algorithmic bytes from a flushed
     # L2, timed the same way as the steps ----
     def size_floor(nbytes, reps=20):
+        """Plain reads (and a copy) of nbytes of cold data, cold the same way
+        as the steps: NC buffers in turn, or one flushed buffer."""
         nb = max(16, nbytes // 16 * 16)
-        buf = torch.empty(nb // 2, dtype=torch.bfloat16, device=dev).normal_()
-        dst = torch.empty_like(buf)
+        bufs = [torch.empty(nb // 2, dtype=torch.bfloat16, device=dev).normal_() for _ in range(NC)]
+        dst = torch.empty_like(bufs[0])
         sink = torch.zeros(1, dtype=torch.int32, device=dev)
         res = {}
-        kernels = [(f"read_us_{c}cta", (lambda c=c: hk.read_floor(buf, c, sink))) for c in (1, 2, 4)]
-        kernels.append(("copy_us", lambda: dst.copy_(buf)))
+        kernels = [(f"read_us_{c}cta", (lambda b, c=c: hk.read_floor(b, c, sink))) for c in (1, 2, 4)]
+        kernels.append(("copy_us", lambda b: dst.copy_(b)))
         for name, fn in kernels:
-            fn()
+            for b in bufs:
+                fn(b)
             ts = []
             for i in range(reps):
-                flush.fill_(float(i))
+                if NC == 1:
+                    flush.fill_(float(i))
                 torch.cuda._sleep(spin_cycles)
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
-                fn()
+                fn(bufs[i % NC])
                 b.record(stream)
                 b.synchronize()
                 ts.append(a.elapsed_time(b) * 1e3)
             res[name] = float(np.median(ts))
         res["read_us"] = min(v for k_, v in res.items() if k_.startswith("read_us_"))
         res["read_gbs"] = nb / res["read_us"] / 1e3
-        del buf, dst
+        del bufs, dst
         return res
     floor = size_floor(int(alg_bytes // K)) if K > 0 else None
     del flush
@@ -620,6 +698,7 @@ def measure(w, seed, dev, opts, stage=lambda m: None):
 
     avg_s = t_total / K
     r = {"K": K, "Wu": Wu, "t_total": t_total, "avg_s": avg_s, "alg_bytes": alg_bytes, "kv_bytes": kv_bytes,
+         "NC": NC, "flushed": flushed,
          "launches": launches, "dec_cfg": dec_cfg, "three": three, "per_layer": per_layer, "setup": setup,
          "clocks": clocks, "floor": floor, "lens": lens, "elem": elem, "vrows": vrows,
          "decode_inputs": f"{R} distinct steps" + (", cycled" if R < total_steps else ""),
@@ -697,7 +776,8 @@ def bench_gpu(args):
             "per_layer_steps": args.per_layer_steps if args.per_layer_steps >= 0 else (0 if L == 1 else 100),
             "e2e_steps": args.e2e_steps, "budgets": budgets, "full_cache": args.full_cache,
             "element_budget": args.element_budget, "prompt_source": "host", "spin_us": args.spin_us,
-            "world": world, "sampler": ClockSampler(gpu_id_for(local))}
+            "world": world, "sampler": ClockSampler(gpu_id_for(local)), "flushed_steps": min(args.steps, 200),
+            "l2_mode": args.l2}
     r = measure(w, seed, dev, opts, stage)
     K = r["K"]
     peaks, src = measured_peaks()
@@ -721,7 +801,7 @@ def bench_gpu(args):
         "scaling": args.scaling, "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded)",
         "config": workload_config(cfg_w, args.schedule, elem if elem else 0, args.full_cache, world,
-                                  args.scaling),
+                                  args.scaling, args.l2),
         "workload_observed": {"tokens_attended_per_unit_max": int(lens.max()) + 1,
                               "tokens_attended_per_unit_mean": float(lens.mean()) + 1,
                               "decode_inputs": r["decode_inputs"], "units_rank0": int(lens.size),
@@ -740,6 +820,7 @@ def bench_gpu(args):
         "gpu_launches": r["launches"],
         "decode_launch": r["dec_cfg"],
         "three_call_path": r["three"],
+        "flushed_l2_steps": r["flushed"],
         "stage2_v_rows_read_fraction": (r["vrows"] / max(1, r["kv_bytes"] // (2 * w.d * w.elem_bytes))) if elem
         else None,
         "per_layer_launches": r["per_layer"],
@@ -747,8 +828,8 @@ def bench_gpu(args):
         "clocks": r["clocks"],
         "size_floor": ({"bytes": int(r["alg_bytes"] // K),
                         "kernels": "hikv_read_floor (plain 16-byte streaming loads, best of 1/2/4 CTAs per SM) "
-                                   "and a torch copy of a buffer of one step's algorithmic bytes, L2 flushed "
-                                   "before each, median of 20",
+                                   "and a torch copy of a buffer of one step's algorithmic bytes, cold the same "
+                                   "way as the steps (as many buffers in turn as cache copies), median of 20",
                         **r["floor"], "step_us": avg_s * 1e6} if r["floor"] else None),
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -799,6 +880,9 @@ def main():
     ap.add_argument("--other-cpu-s", type=float, default=5.0, help="CPU-oracle seconds per other workload")
     ap.add_argument("--element-budget", type=int, default=0,
                     help="HiKV Stage II element budget B2 (0: exact attention)")
+    ap.add_argument("--l2", default="auto", choices=["auto", "flush"],
+                    help="cold data between timed steps: auto = inputs larger than L2 (cache copies in turn for "
+                         "small steps), flush = a 256 MB write before every step")
     ap.add_argument("--verbose", action="store_true", help="stage markers on stderr")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -55,7 +55,7 @@ struct View {
 };
 
 #ifndef HIKV_G8_GROUPS
-#define HIKV_G8_GROUPS 1
+#define HIKV_G8_GROUPS 2
 #endif
 constexpr int kMaxCS = 16;   // most CTAs (cluster size) per unit in the decode kernel
 
@@ -98,15 +98,14 @@ __host__ __device__ inline int32_t pages_kept(int32_t B, int32_t page_tokens, in
 // which is only sound when it has itself seen the stage's previous phase
 // complete.
 __host__ __device__ constexpr int dec_occupancy(int /*row_bytes*/, int /*group*/) { return 2; }
+// consumer warps of one head group
 __host__ __device__ constexpr int dec_consumer_warps(int /*row_bytes*/, int /*group*/) { return 4; }
 // Head groups of a decode CTA: with G = 8 each tile is consumed by two warps,
 // one per half of the group's query heads (two sets of dec_consumer_warps
 // warps rotating over the same tiles), so a warp carries the state of four
 // heads and twice the warps hide the tile loop's latency.
 __host__ __device__ constexpr int dec_head_groups(int group) { return group == 8 ? HIKV_G8_GROUPS : 1; }
-__host__ __device__ constexpr int dec_stages(int row_bytes, int group) {
-    return 2 * dec_consumer_warps(row_bytes, group);
-}
+__host__ __device__ constexpr int dec_stages(int /*row_bytes*/, int /*group*/) { return 8; }
 
 __host__ __device__ inline int32_t ceil_div(int32_t a, int32_t b) { return (a + b - 1) / b; }
 
@@ -323,6 +322,12 @@ __device__ __forceinline__ void cluster_sync_all() {
 // the two halves of cluster_sync_all, for work between them (whole warps)
 __device__ __forceinline__ void cluster_arrive() {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+// arrive without release semantics: for signalling that this CTA's mbarriers
+// are initialised, whose fence.mbarrier_init already released them at
+// cluster scope (a release here would also wait for this thread's copies)
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");

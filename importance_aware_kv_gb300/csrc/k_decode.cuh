@@ -113,6 +113,28 @@ __device__ __forceinline__ uint32_t lin(int r, int c) {
     return (uint32_t)(r * RBYTES + (c << 4));
 }
 
+// Queue the copies of one tile -- 16 K rows and the 16 V rows P slots after
+// them, starting at slot s0 of page pg -- into a ring stage (K at dst, V at
+// dst + TB), completing on `bar`: two 1-D bulk copies of the contiguous rows
+// (row-split path), or 2-D TMA boxes of 16 rows x 128 bytes that lay the
+// rows down 128-byte swizzled (half-row path).
+template <bool RS, int NBOX, int ESZ, int RB, int TB>
+__device__ __forceinline__ void dec_load_tile(uint8_t* dst, const View& v, int32_t pg, int32_t s0,
+                                              const CUtensorMap* tmap, uint64_t* bar) {
+    if constexpr (RS) {
+        const uint8_t* kb = v.pool + (int64_t)pg * v.page_bytes + (int64_t)(s0 & (v.page_tokens - 1)) * RB;
+        bulk_g2s(dst, kb, (uint32_t)TB, bar);
+        bulk_g2s(dst + TB, kb + (int64_t)v.page_tokens * RB, (uint32_t)TB, bar);
+    } else {
+        const int32_t yk = pg * 2 * v.page_tokens + (s0 & (v.page_tokens - 1));
+#pragma unroll
+        for (int bx = 0; bx < NBOX; ++bx) {
+            tma_load_2d(dst + bx * (16 * 128), tmap, bx * (128 / ESZ), yk, bar);
+            tma_load_2d(dst + TB + bx * (16 * 128), tmap, bx * (128 / ESZ), yk + v.page_tokens, bar);
+        }
+    }
+}
+
 // Reduce-scatter of v[0, N) over the lanes that differ in the bits of M,
 // M / 2, ..., 1: at each level a lane keeps the half of its values that its
 // bit selects (upper half when set) and adds the partner's copy of that
@@ -200,6 +222,12 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
     // fixed head (QK_DUP lanes hold the same one when QK_NV < QK_LPR).  The
     // per-tile shared-memory reads are then the K tile itself, not q again
     // for every row.
+    // G = 8 runs two head groups of four warps at 96 registers, where the
+    // q registers above do not fit: its warps keep the half-row mapping
+    // (lane = tile row and half of it, q read from shared memory) over
+    // 128-byte-swizzled tiles that 2-D TMA boxes lay down
+    constexpr bool kRS = kHG == 1;
+    constexpr int CPL = CPR / 2;             // half-row q.k: chunks per lane
     constexpr int QK_LPR = RB / 16;
     constexpr int QK_RPW = 32 / QK_LPR;
     constexpr int QK_STEPS = kDecTR / QK_RPW;
@@ -267,7 +295,13 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
         if (lane < npg && !v.home_pages) pre_pg = v.page_table[(int64_t)du.u * v.max_pages + pg0 + lane];
     }
 
-    if (tid == 0) {
+    // The producer's lane 0 sets up the barriers and then queues the first
+    // unit's q (and new rows) and, with home pages (tile addresses need no
+    // lookup), its first tiles before the CTA-wide sync: those copies are the
+    // launch's critical path.
+    int32_t pre_issued = 0;
+    bool pre_q = false;
+    if (warp == kDecNCW && lane == 0) {
         for (int s = 0; s < kDecStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], (uint32_t)kHG);   // one warp of each head group releases the stage
@@ -280,18 +314,57 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
         }
         *abort_flag = 0;
         fence_mbar_init();
+        if (it0 < it1) {
+            const DecUnit du = dec_unit(a, it0);
+            const int32_t per_layer = v.batch * v.hkv;
+            const int32_t li = du.u / per_layer - a.layer0;
+            const int64_t qbase = (((int64_t)li * v.batch + (du.u / v.hkv) % v.batch) * v.hq +
+                                   (int64_t)(du.u % v.hkv) * G) * D;
+            mbar_arrive_expect_tx(&qfull[0], QB + (a.fused ? 2 * RB : 0));
+            bulk_g2s(smem + L.qraw, a.q + qbase * ESZ, QB, &qfull[0]);
+            if (a.fused) {
+                const int64_t ui = (int64_t)du.u - (int64_t)a.layer0 * per_layer;
+                bulk_g2s(smem + L.nrow, a.new_k + ui * RB, RB, &qfull[0]);
+                bulk_g2s(smem + L.nrow + RB, a.new_v + ui * RB, RB, &qfull[0]);
+            }
+            pre_q = true;
+        }
+        if (v.home_pages && it0 < it1) {
+            const DecUnit du = dec_unit(a, it0);
+            int32_t t0, t1;
+            dec_range(du.n, CS, c, t0, t1);
+            const int32_t cnt = t1 - t0;
+            const int32_t first_blk = t0 / kDecTR;
+            const bool tail = cnt > 1 && (cnt - 1) % kDecTR == 0;
+            const int32_t nt = tail ? (cnt - 1) / kDecTR : (cnt > 0 ? (t1 - 1) / kDecTR - first_blk + 1 : 0);
+            const int32_t burst = min(nt, a.first_burst > 0 ? min(a.first_burst, kDecStages) : kDecStages);
+            for (int i = 0; i < burst; ++i) {
+                const int32_t s0 = (first_blk + i) * kDecTR;
+                const int32_t pg = du.u * v.max_pages + (s0 >> v.page_shift);
+                if (pg < 0 || pg >= v.pool_pages) {
+                    atomicOr(v.err, DEVERR_PAGE);
+                    *abort_flag = 1;
+                    mbar_arrive(&full[i]);   // complete the stage without data
+                    break;
+                }
+                uint8_t* dst = ring + i * 2 * TB;
+                mbar_arrive_expect_tx(&full[i], 2 * TB);
+                dec_load_tile<kRS, NBOX, ESZ, RB, TB>(dst, v, pg, s0, &tmap, &full[i]);
+                pre_issued = i + 1;
+            }
+        }
     }
     __syncthreads();
     // every CTA's barriers must be initialised before any partner arrives on
     // them: arrive here, wait before this CTA's first remote access (the
     // CTA-local ring starts at once)
-    cluster_arrive();
+    cluster_arrive_relaxed();
     bool cluster_ready = false;
 
     if (warp == kDecNCW) {
         // ======================= producer =======================
-        if (lane == 0) prefetch_tensormap(&tmap);
-        int gi = 0;   // running tile counter of this CTA (lane 0's copy is authoritative)
+        if (!kRS && lane == 0) prefetch_tensormap(&tmap);
+        int gi = pre_issued;   // running tile counter of this CTA (lane 0's copy is authoritative)
         for (int k = 0, idx = it0; idx < it1; ++k, idx += istep) {
             if (*abort_flag) break;
             const DecUnit du = dec_unit(a, idx);
@@ -311,7 +384,7 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
             const int32_t npg = cnt > 0 ? ((t1 - 1) >> v.page_shift) - pg0 + 1 : 0;
             const int32_t* ptab = v.page_table + (int64_t)du.u * v.max_pages;
             const int qb = k & 1;
-            if (lane == 0) {
+            if (lane == 0 && !(k == 0 && pre_q)) {
                 // q of this unit into its half of the double buffer
                 if (!*abort_flag && mbar_wait_bounded(&qempty[qb], ((uint32_t)(k >> 1) & 1u) ^ 1u, v.err, kWaitQEmpty, (uint32_t)k)) {
                     const int64_t qbase = (((int64_t)li * v.batch + b) * v.hq + (int64_t)g * G) * D;
@@ -345,7 +418,7 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
             const int pf = a.prefetch_tiles;
             for (int j = lane; j < min(nt, pf); j += 32) prefetch_tile(j);
             if (lane == 0) {
-                for (int i = 0; i < nt; ++i, ++gi) {
+                for (int i = k == 0 ? pre_issued : 0; i < nt; ++i, ++gi) {
                     if (*abort_flag) break;
                     // the CTA's first tiles jump the DRAM queue: past the first
                     // burst, wait until tile 0 has landed before queueing more
@@ -369,13 +442,9 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                         break;
                     }
                     if (pf > 0 && i + pf < nt) prefetch_tile(i + pf);
-                    // the tile's 16 K rows and 16 V rows are contiguous in the page:
-                    // one 1-D bulk copy each
-                    const uint8_t* kb = v.pool + (int64_t)pg * v.page_bytes + (int64_t)(s0 & (v.page_tokens - 1)) * RB;
                     uint8_t* dst = ring + st * 2 * TB;
                     mbar_arrive_expect_tx(&full[st], 2 * TB);
-                    bulk_g2s(dst, kb, (uint32_t)TB, &full[st]);
-                    bulk_g2s(dst + TB, kb + (int64_t)v.page_tokens * RB, (uint32_t)TB, &full[st]);
+                    dec_load_tile<kRS, NBOX, ESZ, RB, TB>(dst, v, pg, s0, &tmap, &full[st]);
                 }
             }
             gi = __shfl_sync(0xffffffffu, gi, 0);
@@ -397,6 +466,8 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
     const int wg = warp / kDecNGW, wi = warp % kDecNGW;   // head group, place in the tile rotation
     const int h0 = wg * GW;                               // this warp's heads: h0 .. h0 + GW - 1
     float* ps = ps_all + warp * (kDecTR * GW);     // [16][GW] p of the tile
+    const int qr = lane & 15;                       // half-row q.k: tile row of this lane
+    const int qh = lane >> 4;                       //               half of the row
     const int qk_c = lane % QK_LPR;                 // q.k: chunk of the row this lane reads
     const int qk_rg = lane / QK_LPR;                // q.k: row of the warp step
     const int qk_k = qk_c / QK_DUP;                 // q.k: index of the logit this lane ends with
@@ -404,6 +475,11 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
     const int hk = qk_k % GW;                       //      its head (of this warp's GW)
     const bool qk_own = (qk_c % QK_DUP) == 0;       //      the lane that records it
     const int pv_chunk = (lane * LB) >> 4, pv_in = (lane * LB) & 15;
+    // byte offset of 16-byte chunk c of tile row r in a ring stage
+    auto toff = [](int r, int c) -> uint32_t {
+        if constexpr (kRS) return lin<RB>(r, c);
+        else return swz(r, c);
+    };
     int gi_base = 0;
 
     for (int k = 0, idx = it0; idx < it1; ++k, idx += istep) {
@@ -475,22 +551,26 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
         named_bar_sync(1, NCT);
 
         // q of this warp's heads at this lane's chunk, in registers
-        float2 qreg[GW][QK_EPL / 2];
+        float2 qreg[kRS ? GW : 1][QK_EPL / 2];
+        if constexpr (kRS) {
 #pragma unroll
-        for (int h = 0; h < GW; ++h)
+            for (int h = 0; h < GW; ++h)
 #pragma unroll
-            for (int e = 0; e < QK_EPL / 2; ++e)
-                qreg[h][e] = *reinterpret_cast<const float2*>(q_s + (h0 + h) * D + qk_c * QK_EPL + 2 * e);
+                for (int e = 0; e < QK_EPL / 2; ++e)
+                    qreg[h][e] = *reinterpret_cast<const float2*>(q_s + (h0 + h) * D + qk_c * QK_EPL + 2 * e);
+        }
         // softmax state: the reference m_w of every head (the same in all
         // lanes), this lane's share of its head's row sum, and the tail row's
         // share of each head's (lane 0)
         float m_w[GW], l_tail[GW];
+        float l_row[GW];   // half-row path: this lane's row sums of every head
         float m_own = -INFINITY, l_own = 0.f;
         float2 o2[GW][EPL / 2];
 #pragma unroll
         for (int h = 0; h < GW; ++h) {
             m_w[h] = -INFINITY;
             l_tail[h] = 0.f;
+            l_row[h] = 0.f;
 #pragma unroll
             for (int e = 0; e < EPL / 2; ++e) o2[h][e] = make_float2(0.f, 0.f);
         }
@@ -514,8 +594,8 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                 const int r = sn - s0;
                 const Raw nk = *reinterpret_cast<const Raw*>(nrow + lane * LB);
                 const Raw nv = *reinterpret_cast<const Raw*>(nrow + RB + lane * LB);
-                *reinterpret_cast<Raw*>(ktile + lin<RB>(r, pv_chunk) + pv_in) = nk;
-                *reinterpret_cast<Raw*>(vtile + lin<RB>(r, pv_chunk) + pv_in) = nv;
+                *reinterpret_cast<Raw*>(ktile + toff(r, pv_chunk) + pv_in) = nk;
+                *reinterpret_cast<Raw*>(vtile + toff(r, pv_chunk) + pv_in) = nv;
                 fence_proxy_async_smem();   // the stage is refilled by TMA later
                 // (both head groups' warps patch the landed tile with the same
                 // bytes before reading it; one of them writes the pool)
@@ -528,6 +608,7 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                 __syncwarp();
             }
 
+            if constexpr (kRS) {
             // ---- q.k: per sub-block, each lane's chunk of QK_SUB rows against
             // q in registers, then the partial sums reduce-scattered ----
             float sv[QK_NSUB];
@@ -537,7 +618,7 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
 #pragma unroll
                 for (int j = 0; j < QK_SUB; ++j) {
                     const int r = (sb * QK_SUB + j) * QK_RPW + qk_rg;
-                    const uint4 raw = *reinterpret_cast<const uint4*>(ktile + lin<RB>(r, qk_c));
+                    const uint4 raw = *reinterpret_cast<const uint4*>(ktile + toff(r, qk_c));
                     float x[QK_EPL];
                     Widen<T, QK_EPL>::run(raw, x);
 #pragma unroll
@@ -596,13 +677,76 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                         Sb[(int64_t)(s0 + r - s_off) * G + h0 + hk] = sv[sb];   // for the importance pass
                 }
             }
+            } else {
+            // ---- q.k: this lane's half row (q from shared memory) ----
+            float2 acc[GW];
+#pragma unroll
+            for (int h = 0; h < GW; ++h) acc[h] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) {
+                const int cidx = 2 * j + qh;   // halves interleave: their q reads fall in different banks
+                const uint4 raw = *reinterpret_cast<const uint4*>(ktile + swz(qr, cidx));
+                float x[EPC];
+                Widen<T, EPC>::run(raw, x);
+#pragma unroll
+                for (int h = 0; h < GW; ++h) {
+                    const float* qp = q_s + (h0 + h) * D + cidx * EPC;
+#pragma unroll
+                    for (int e = 0; e < EPC; e += 4) {
+                        const float4 q4 = *reinterpret_cast<const float4*>(qp + e);
+                        acc[h] = ffma2(make_float2(x[e], x[e + 1]), make_float2(q4.x, q4.y), acc[h]);
+                        acc[h] = ffma2(make_float2(x[e + 2], x[e + 3]), make_float2(q4.z, q4.w), acc[h]);
+                    }
+                }
+            }
+            const bool rv = qr >= lo_r && qr < hi_r;
+            float sh[GW];
+#pragma unroll
+            for (int h = 0; h < GW; ++h) {
+                float t = acc[h].x + acc[h].y;
+                t += __shfl_xor_sync(0xffffffffu, t, 16);
+                sh[h] = rv ? t : -INFINITY;
+            }
+            // ---- online softmax, lazily rescaled (as above, per head) ----
+            bool big = false;
+#pragma unroll
+            for (int h = 0; h < GW; ++h) big |= sh[h] > m_w[h] + kDecLazy;   // invalid rows: -inf
+            if (__any_sync(0xffffffffu, big)) {
+#pragma unroll
+                for (int h = 0; h < GW; ++h) {
+                    float mt = sh[h];
+#pragma unroll
+                    for (int o = 8; o >= 1; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+                    const float mn = fmaxf(m_w[h], mt);
+                    const float scl = exp2f(m_w[h] - mn);   // 1 when unchanged, 0 from -inf
+                    m_w[h] = mn;
+                    l_row[h] *= scl;
+#pragma unroll
+                    for (int e = 0; e < EPL / 2; ++e) {
+                        o2[h][e].x *= scl;
+                        o2[h][e].y *= scl;
+                    }
+                }
+            }
+            float p[GW];
+#pragma unroll
+            for (int h = 0; h < GW; ++h) {
+                p[h] = rv ? exp2f(sh[h] - m_w[h]) : 0.f;
+                l_row[h] += p[h];   // this lane's row; both halves of a row hold the same p
+            }
+            if (qh == 0) {
+                store_group<GW>(ps + qr * GW, p);
+                if (rv && (!SMEM_S || s0 + qr - s_off < a.chunk_cap))
+                    store_group<GW>(Sb + (int64_t)(s0 + qr - s_off) * G + h0, sh);   // this group's heads of the row
+            }
+            }   // half-row path
             __syncwarp();
             // ---- p.v over the tile's valid rows (unrolled; invalid rows skipped, their
             // stale V bytes may hold any bit pattern) ----
 #pragma unroll
             for (int r = 0; r < kDecTR; ++r) {
                 if (r < lo_r || r >= hi_r) continue;
-                const Raw raw = *reinterpret_cast<const Raw*>(vtile + lin<RB>(r, pv_chunk) + pv_in);
+                const Raw raw = *reinterpret_cast<const Raw*>(vtile + toff(r, pv_chunk) + pv_in);
                 float x[EPL];
                 Widen<T, EPL>::run(raw, x);
                 const float* pr = ps + r * GW;
@@ -663,10 +807,14 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                     const float mn = fmaxf(m_w[h], s[h]);
                     const float scl = exp2f(m_w[h] - mn);
                     m_w[h] = mn;
-                    l_tail[h] *= scl;
-                    if (hk == h) {
-                        l_own *= scl;
-                        m_own = mn;
+                    if constexpr (kRS) {
+                        l_tail[h] *= scl;
+                        if (hk == h) {
+                            l_own *= scl;
+                            m_own = mn;
+                        }
+                    } else {
+                        l_row[h] *= scl;
                     }
 #pragma unroll
                     for (int e = 0; e < EPL / 2; ++e) {
@@ -678,7 +826,10 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
 #pragma unroll
             for (int h = 0; h < GW; ++h) {
                 const float p = exp2f(s[h] - m_w[h]);
-                if (lane == 0) l_tail[h] += p;
+                if (lane == 0) {   // the tail row, once in the warp's row sums
+                    if constexpr (kRS) l_tail[h] += p;
+                    else l_row[h] += p;
+                }
 #pragma unroll
                 for (int e = 0; e < EPL / 2; ++e)
                     o2[h][e] = ffma2(make_float2(xv[2 * e], xv[2 * e + 1]), make_float2(p, p), o2[h][e]);
@@ -716,8 +867,9 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
         float l_w[GW];   // each head's row sum over this warp's rows
 #pragma unroll
         for (int h = 0; h < GW; ++h) {
-            float t = (qk_own && hk == h) ? l_own : 0.f;
-            if (lane == 0) t += l_tail[h];
+            float t;
+            if constexpr (kRS) t = ((qk_own && hk == h) ? l_own : 0.f) + (lane == 0 ? l_tail[h] : 0.f);
+            else t = lane < 16 ? l_row[h] : 0.f;   // lanes 16-31 hold the same rows
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
             l_w[h] = t;
