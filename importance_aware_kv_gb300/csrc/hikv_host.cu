@@ -147,6 +147,14 @@ struct hikv_cache {
     int32_t* d_edone = nullptr;         // [units]
     // HiKV banded prefill scores (band_scoring): one layer's per-query softmax statistics
     float2* d_band = nullptr;           // [per_layer][G][cap]
+    // Programmatic dependent launch: the units [pdl_lo, pdl_hi) the latest
+    // kernel this cache launched may write, and its stream (pdl_valid: that
+    // latest launch is known); a decode launch on disjoint units of the same
+    // stream may load its pages before waiting for it
+    bool pdl_on = true;                 // HIKV_PDL=0 (tuning) turns it off
+    bool pdl_valid = false;
+    int pdl_lo = 0, pdl_hi = 0;
+    hikv_stream_t pdl_stream = nullptr;
 };
 
 namespace {
@@ -171,6 +179,20 @@ cudaError_t dalloc(hikv_cache* c, T** p, size_t count) {
 void free_all(hikv_cache* c) {
     for (void* p : c->allocs) cudaFree(p);
     c->allocs.clear();
+}
+
+// Programmatic dependent launch bookkeeping (see hikv_cache::pdl_*): a launch
+// of units [lo, hi) on `stream`; pdl_forget() when an entry point launches
+// kernels that do not record their units.
+void pdl_record(hikv_cache* c, int lo, int hi, hikv_stream_t stream) {
+    c->pdl_valid = true;
+    c->pdl_lo = lo;
+    c->pdl_hi = hi;
+    c->pdl_stream = stream;
+}
+void pdl_forget(hikv_cache* c) { if (c) c->pdl_valid = false; }
+bool pdl_disjoint(const hikv_cache* c, int lo, int hi, hikv_stream_t stream) {
+    return c->pdl_on && c->pdl_valid && c->pdl_stream == stream && (hi <= c->pdl_lo || lo >= c->pdl_hi);
 }
 
 bool range_ok(const hikv_cache* c, int32_t layer0, int32_t nl) {
@@ -256,6 +278,7 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
     if (const char* e = std::getenv("HIKV_DECODE_CS")) c->cs_override = std::atoi(e);
     if (const char* e = std::getenv("HIKV_DECODE_SMALL")) c->small_mode = std::atoi(e);
     if (const char* e = std::getenv("HIKV_DECODE_BURST")) c->first_burst = std::atoi(e);
+    if (const char* e = std::getenv("HIKV_PDL")) c->pdl_on = std::atoi(e) != 0;
 
     cudaError_t e = cudaGetDevice(&c->device);
     if (e != cudaSuccess) { delete c; return cuda_fail(e, "create: cudaGetDevice"); }
@@ -441,6 +464,7 @@ hikv_status hikv_destroy_cache(hikv_cache* c) {
 hikv_status hikv_append(hikv_cache* c, int32_t layer0, int32_t nl, int32_t ntok, const void* k,
                         const void* vv, hikv_stream_t stream) {
     g_err.clear();
+    pdl_forget(c);
     NvtxRange nvtx("hikv_append");
     if (!range_ok(c, layer0, nl)) return fail(HIKV_ERR_INVALID_ARG, "append: bad cache or layer range");
     if (ntok < 0) return fail(HIKV_ERR_INVALID_ARG, "append: ntok < 0");
@@ -483,6 +507,7 @@ hikv_status hikv_append(hikv_cache* c, int32_t layer0, int32_t nl, int32_t ntok,
 hikv_status hikv_score_window(hikv_cache* c, int32_t layer0, int32_t nl, int32_t nq, const void* q,
                               hikv_stream_t stream) {
     g_err.clear();
+    pdl_forget(c);
     NvtxRange nvtx("hikv_score_window");
     if (!range_ok(c, layer0, nl)) return fail(HIKV_ERR_INVALID_ARG, "score_window: bad cache or layer range");
     if (nq < 1 || nq > c->max_wq)
@@ -528,6 +553,7 @@ hikv_status hikv_score_window(hikv_cache* c, int32_t layer0, int32_t nl, int32_t
 hikv_status hikv_score_band(hikv_cache* c, int32_t layer0, int32_t nl, int32_t band, const void* q,
                             hikv_stream_t stream) {
     g_err.clear();
+    pdl_forget(c);
     NvtxRange nvtx("hikv_score_band");
     if (!range_ok(c, layer0, nl)) return fail(HIKV_ERR_INVALID_ARG, "score_band: bad cache or layer range");
     if (band < 1) return fail(HIKV_ERR_INVALID_ARG, "score_band: band=%d < 1", band);
@@ -731,8 +757,15 @@ hikv_status launch_clusters(hikv_cache* c, int32_t layer0, int32_t nl, const std
     a.evict = evict;
     a.new_k = (const uint8_t*)new_k;
     a.new_v = (const uint8_t*)new_v;
+    int ulo = u0, uhi = u0 + nu;   // the units this launch writes
+    if (subset) {
+        ulo = *std::min_element(subset->begin(), subset->end());
+        uhi = *std::max_element(subset->begin(), subset->end()) + 1;
+    }
+    a.pdl_early = pdl_disjoint(c, ulo, uhi, stream) ? 1 : 0;
     cudaError_t e = launch_decode(a, c->tmap, c->dtype, c->d, c->G, smem_path, smem, (cudaStream_t)stream);
     c->launches += 1;
+    pdl_record(c, ulo, uhi, stream);
     if (c->last_ncfg < 2) {
         int32_t* r = c->last_cfg[c->last_ncfg++];
         r[0] = nu;
@@ -789,6 +822,10 @@ hikv_status launch_small(hikv_cache* c, int32_t layer0, const std::vector<int32_
     a.new_v = (const uint8_t*)new_v;
     cudaError_t e = launch_decode_small(a, c->tmap, c->dtype, c->d, c->G, n_ctas, (cudaStream_t)stream);
     c->launches += 1;
+    // (launched without programmatic serialisation: it starts after the
+    // previous grid completes; a following decode launch may overlap it)
+    pdl_record(c, *std::min_element(units.begin(), units.end()), *std::max_element(units.begin(), units.end()) + 1,
+               stream);
     if (e != cudaSuccess) return cuda_fail(e, who);
     return HIKV_OK;
 }
@@ -872,6 +909,7 @@ extern "C" {
 static hikv_status launch_elem_call(hikv_cache* c, int32_t layer0, int32_t nl, const void* q, void* out,
                                     hikv_stream_t stream, int fused = 0, int evict = 0,
                                     const void* new_k = nullptr, const void* new_v = nullptr) {
+    pdl_forget(c);
     const int u0 = layer0 * c->per_layer, nu = nl * c->per_layer;
     int max_n = 0;
     for (int u = u0; u < u0 + nu; ++u) {
@@ -963,6 +1001,7 @@ hikv_status hikv_decode_step_fused(hikv_cache* c, int32_t layer0, int32_t nl, co
 
 hikv_status hikv_evict(hikv_cache* c, int32_t layer0, int32_t nl, hikv_stream_t stream) {
     g_err.clear();
+    pdl_forget(c);
     NvtxRange nvtx("hikv_evict");
     if (!range_ok(c, layer0, nl)) return fail(HIKV_ERR_INVALID_ARG, "evict: bad cache or layer range");
     const int u0 = layer0 * c->per_layer, nu = nl * c->per_layer;
@@ -1002,6 +1041,7 @@ hikv_status hikv_gather_retained(hikv_cache* c, int32_t layer0, int32_t nl, int3
                                  int32_t* positions, float* importance, void* k_out, void* v_out,
                                  hikv_stream_t stream) {
     g_err.clear();
+    pdl_forget(c);
     NvtxRange nvtx("hikv_gather_retained");
     if (!range_ok(c, layer0, nl)) return fail(HIKV_ERR_INVALID_ARG, "gather: bad cache or layer range");
     if (!lengths || !positions || !importance) return fail(HIKV_ERR_INVALID_ARG, "gather: null output");
@@ -1055,6 +1095,7 @@ int64_t hikv_kernel_launches(const hikv_cache* c) { return c ? c->launches : -1;
 
 hikv_status hikv_selftest_timeout(hikv_cache* c, int32_t limit_us, hikv_stream_t stream) {
     g_err.clear();
+    pdl_forget(c);
     if (!c || limit_us < 1 || limit_us > 2000000)
         return fail(HIKV_ERR_INVALID_ARG, "selftest_timeout: bad cache or limit");
     cudaError_t e = launch_selftest_timeout(c->v, (uint64_t)limit_us * 1000u, (cudaStream_t)stream);

@@ -333,6 +333,15 @@ __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Programmatic dependent launch: wait until the grid this one depends on
+// (the previous kernel in the stream, when launched with programmatic stream
+// serialisation) has completed and its memory is visible -- a no-op
+// otherwise; and let the next grid in the stream be scheduled early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // shared::cluster address of `p` in CTA `rank` of this cluster
 __device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
     uint32_t r;
@@ -475,6 +484,10 @@ struct DecodeArgs {
     int32_t fused, evict;
     const uint8_t* new_k;
     const uint8_t* new_v;
+    // programmatic dependent launch: 1 when the grid this launch may overlap
+    // (the previous one in the stream) writes none of this launch's units, so
+    // the kernel may load their pages before waiting for it; 0: wait first
+    int32_t pdl_early;
 };
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmap, int dtype, int d, int group,
                           bool smem_path, size_t smem_bytes, cudaStream_t s);

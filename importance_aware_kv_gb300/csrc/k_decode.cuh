@@ -284,6 +284,13 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
     const int32_t it1 = a.assign_off ? a.assign_off[blockIdx.y + 1] : a.n_units;
     const int32_t istep = a.assign_off ? 1 : a.n_clusters;
 
+    // Programmatic dependent launch: this grid may start while the previous
+    // one in the stream runs.  Unless the host found that one to write none
+    // of this launch's units, wait for it before touching anything; else the
+    // first tiles (this launch's own units) are queued before the wait, and
+    // the caller's inputs (q, new rows) are read and `out` written after it.
+    if (!a.pdl_early) griddep_wait();
+
     // producer: the first unit's page ids, loaded while the barriers are set up
     int32_t pre_pg = -1;
     if (warp == kDecNCW && it0 < it1) {
@@ -314,21 +321,6 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
         }
         *abort_flag = 0;
         fence_mbar_init();
-        if (it0 < it1) {
-            const DecUnit du = dec_unit(a, it0);
-            const int32_t per_layer = v.batch * v.hkv;
-            const int32_t li = du.u / per_layer - a.layer0;
-            const int64_t qbase = (((int64_t)li * v.batch + (du.u / v.hkv) % v.batch) * v.hq +
-                                   (int64_t)(du.u % v.hkv) * G) * D;
-            mbar_arrive_expect_tx(&qfull[0], QB + (a.fused ? 2 * RB : 0));
-            bulk_g2s(smem + L.qraw, a.q + qbase * ESZ, QB, &qfull[0]);
-            if (a.fused) {
-                const int64_t ui = (int64_t)du.u - (int64_t)a.layer0 * per_layer;
-                bulk_g2s(smem + L.nrow, a.new_k + ui * RB, RB, &qfull[0]);
-                bulk_g2s(smem + L.nrow + RB, a.new_v + ui * RB, RB, &qfull[0]);
-            }
-            pre_q = true;
-        }
         if (v.home_pages && it0 < it1) {
             const DecUnit du = dec_unit(a, it0);
             int32_t t0, t1;
@@ -353,8 +345,27 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                 pre_issued = i + 1;
             }
         }
+        if (a.pdl_early) griddep_wait();   // q and the new rows may come from the previous grid
+        if (it0 < it1) {
+            const DecUnit du = dec_unit(a, it0);
+            const int32_t per_layer = v.batch * v.hkv;
+            const int32_t li = du.u / per_layer - a.layer0;
+            const int64_t qbase = (((int64_t)li * v.batch + (du.u / v.hkv) % v.batch) * v.hq +
+                                   (int64_t)(du.u % v.hkv) * G) * D;
+            mbar_arrive_expect_tx(&qfull[0], QB + (a.fused ? 2 * RB : 0));
+            bulk_g2s(smem + L.qraw, a.q + qbase * ESZ, QB, &qfull[0]);
+            if (a.fused) {
+                const int64_t ui = (int64_t)du.u - (int64_t)a.layer0 * per_layer;
+                bulk_g2s(smem + L.nrow, a.new_k + ui * RB, RB, &qfull[0]);
+                bulk_g2s(smem + L.nrow + RB, a.new_v + ui * RB, RB, &qfull[0]);
+            }
+            pre_q = true;
+        }
     }
     __syncthreads();
+    // every thread is now past the wait (the producer's lane 0 waited before
+    // the sync): the next grid may start, and overlaps at most this one
+    griddep_launch_dependents();
     // every CTA's barriers must be initialised before any partner arrives on
     // them: arrive here, wait before this CTA's first remote access (the
     // CTA-local ring starts at once)
@@ -1117,8 +1128,10 @@ cudaLaunchConfig_t decode_config(int cs, int n_clusters, size_t smem, cudaStream
     attr[0].val.clusterDim.x = (unsigned)cs;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cfg;
 }
 
@@ -1127,8 +1140,9 @@ cudaLaunchConfig_t decode_config(int cs, int n_clusters, size_t smem, cudaStream
 template <typename T, int D, int G, bool SM>
 int decode_active_clusters(int cs, size_t smem) {
     if (decode_prepare<T, D, G, SM>(smem) != cudaSuccess) return 0;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = decode_config<T, D, G>(cs, 1, smem, nullptr, attr);
+    cfg.numAttrs = 1;   // the cluster shape alone decides residency
     return func_active_clusters(reinterpret_cast<const void*>(k_decode<T, D, G, SM>), cs, cfg);
 }
 
@@ -1142,7 +1156,7 @@ cudaError_t decode_launch_one(const DecodeArgs& a, const CUtensorMap& tmap, size
     DecodeArgs b = a;
     const int active = decode_active_clusters<T, D, G, SM>(a.cs, smem);
     if (active > 0 && b.n_clusters > active) b.n_clusters = active;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = decode_config<T, D, G>(b.cs, b.n_clusters, smem, s, attr);
     return cudaLaunchKernelEx(&cfg, k_decode<T, D, G, SM>, b, tmap);
 }
