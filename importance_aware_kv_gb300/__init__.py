@@ -31,7 +31,8 @@ ABI_FUNCTIONS = ("hikv_create_cache", "hikv_destroy_cache", "hikv_append", "hikv
                  "hikv_device_status", "hikv_last_error", "hikv_score_window_noalloc",
                  "hikv_decode_step_fused", "hikv_kernel_launches", "hikv_budgets_pyramid",
                  "hikv_budgets_duo", "hikv_selftest_timeout", "hikv_element_rows",
-                 "hikv_last_decode_config", "hikv_score_band", "hikv_read_floor")
+                 "hikv_last_decode_config", "hikv_score_band", "hikv_read_floor",
+                 "hikv_read_slot")
 
 
 class HikvError(RuntimeError):
@@ -79,6 +80,7 @@ def _load():
         "hikv_budgets_duo": ([I32, I32, P, I32, I32, I32, P], S),
         "hikv_selftest_timeout": ([P, I32, P], S),
         "hikv_read_floor": ([P, I64, I32, P, P], S),
+        "hikv_read_slot": ([P, I32, I32, P, P, P, P], S),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -425,6 +427,19 @@ class Cache:
         hikv_gather_retained(self.h, layer0, nl, cap, lengths, positions, importance, k_out, v_out,
                              stream)
         return lengths, positions, importance, k_out, v_out
+
+    def read_slot(self, unit: int, slot: int):
+        """Raw contents of one slot (diagnostic, synchronous): K row, V row
+        (numpy, bf16 as uint16 bit patterns), importance, position."""
+        c = self.cfg
+        dt = np.uint16 if c.dtype == "bf16" else np.float32
+        k = np.empty(c.head_dim, dt)
+        vv = np.empty(c.head_dim, dt)
+        imp = ctypes.c_float()
+        pos = ctypes.c_int32()
+        _check(_lib.hikv_read_slot(self.h, unit, slot, k.ctypes.data, vv.ctypes.data, ctypes.byref(imp),
+                                   ctypes.byref(pos)))
+        return k, vv, imp.value, pos.value
 
     def device_status(self):
         hikv_device_status(self.h)

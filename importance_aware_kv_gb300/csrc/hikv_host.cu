@@ -307,6 +307,7 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
     // compute a slot's page instead of loading it, and appends and evictions
     // move no pages.  A smaller pool shares its pages through the free stack.
     v.home_pages = c->pool_pages >= (int64_t)c->units * c->max_pages ? 1 : 0;
+    if (const char* e = std::getenv("HIKV_DEBUG")) v.debug = std::atoi(e) != 0 ? 1 : 0;
 
     const size_t U = (size_t)c->units;
     // hole lists: a unit cut from n <= cap to B leaves at most min(B, cap - B) holes
@@ -436,6 +437,14 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
                     cudaSuccess &&
                 cudaMemcpy(v.mapped, home_mapped.data(), U * 4, cudaMemcpyHostToDevice) == cudaSuccess)) &&
               cudaDeviceSynchronize() == cudaSuccess;
+    if (ok && v.debug) {
+        // debug mode: every slot starts dead -- NaN rows and importance
+        const uint32_t nan_word = c->esz == 2 ? 0x7FC07FC0u : 0x7FC00000u;
+        ok = launch_fill_u32(reinterpret_cast<uint32_t*>(v.pool), (size_t)c->pool_pages * v.page_bytes / 4, nan_word,
+                             nullptr) == cudaSuccess &&
+             launch_fill_u32(reinterpret_cast<uint32_t*>(v.imp), U * c->cap, 0x7FC00000u, nullptr) == cudaSuccess &&
+             cudaDeviceSynchronize() == cudaSuccess;
+    }
     if (!ok) {
         e = cudaGetLastError();
         free_all(c);
@@ -1081,6 +1090,29 @@ hikv_status hikv_element_rows(const hikv_cache* c, int64_t* rows_host) {
     cudaError_t e = cudaMemcpy(&r, c->d_erows, 8, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e, "element_rows: read");
     *rows_host = (int64_t)r;
+    return HIKV_OK;
+}
+
+hikv_status hikv_read_slot(const hikv_cache* c, int32_t unit, int32_t slot, void* k_host, void* v_host,
+                           float* imp_host, int32_t* pos_host) {
+    g_err.clear();
+    if (!c || unit < 0 || unit >= c->units || slot < 0 || slot >= c->cap)
+        return fail(HIKV_ERR_INVALID_ARG, "read_slot: bad cache, unit or slot");
+    int32_t pg = -1;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess)
+        e = cudaMemcpy(&pg, c->v.page_table + (int64_t)unit * c->max_pages + (slot >> c->page_shift), 4,
+                       cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "read_slot");
+    if (pg < 0 || pg >= c->pool_pages) return fail(HIKV_ERR_STATE, "read_slot: slot %d of unit %d has no page", slot, unit);
+    const uint8_t* kr = c->v.pool + (int64_t)pg * c->v.page_bytes + (int64_t)(slot & (c->P - 1)) * c->v.row_bytes;
+    const int64_t m = (int64_t)unit * c->cap + slot;
+    if ((k_host && (e = cudaMemcpy(k_host, kr, c->v.row_bytes, cudaMemcpyDeviceToHost)) != cudaSuccess) ||
+        (v_host && (e = cudaMemcpy(v_host, kr + (int64_t)c->P * c->v.row_bytes, c->v.row_bytes,
+                                   cudaMemcpyDeviceToHost)) != cudaSuccess) ||
+        (imp_host && (e = cudaMemcpy(imp_host, c->v.imp + m, 4, cudaMemcpyDeviceToHost)) != cudaSuccess) ||
+        (pos_host && (e = cudaMemcpy(pos_host, c->v.pos + m, 4, cudaMemcpyDeviceToHost)) != cudaSuccess))
+        return cuda_fail(e, "read_slot");
     return HIKV_OK;
 }
 

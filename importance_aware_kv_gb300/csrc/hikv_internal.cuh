@@ -52,6 +52,8 @@ struct View {
     int32_t recent_only;  // HiKV Stage I: decode steps add mass only to pos >= t - window
     int32_t home_pages;   // 1: page k of unit u is u * max_pages + k, mapped at create for good
                           // (the pool holds every unit's max_tokens); 0: pages from the free stack
+    int32_t debug;        // 1: vacated slots and freed pages are overwritten with NaN, slot
+                          // indices taken from data are range-checked (HIKV_DEBUG at create)
 };
 
 #ifndef HIKV_G8_GROUPS
@@ -114,6 +116,31 @@ __host__ __device__ inline int32_t ceil_div(int32_t a, int32_t b) { return (a + 
 __device__ __forceinline__ int32_t unit_page(const View& v, int32_t u, int32_t s) {
     return v.home_pages ? u * v.max_pages + (s >> v.page_shift)
                         : v.page_table[(int64_t)u * v.max_pages + (s >> v.page_shift)];
+}
+
+// Debug mode: overwrite slot s of unit u -- its K and V rows with NaN, its
+// importance with NaN, its position with -1 -- so that a kernel that reads
+// a dead slot poisons the outputs it feeds.  Lanes [0, nlanes) share it.
+__device__ __forceinline__ void poison_slot(const View& v, int32_t u, int32_t s, int lane, int nlanes) {
+    if (s < 0 || s >= v.cap) {
+        if (lane == 0) atomicOr(v.err, DEVERR_STATE);
+        return;
+    }
+    const int32_t pg = v.home_pages ? u * v.max_pages + (s >> v.page_shift)
+                                    : v.page_table[(int64_t)u * v.max_pages + (s >> v.page_shift)];
+    if (pg >= 0 && pg < v.pool_pages) {
+        const uint32_t w = v.row_bytes == 2 * v.d ? 0x7FC07FC0u : 0x7FC00000u;   // bf16 pair / fp32 NaN
+        const int32_t vec = v.row_bytes / 16;
+        uint8_t* kr = v.pool + (int64_t)pg * v.page_bytes + (int64_t)(s & (v.page_tokens - 1)) * v.row_bytes;
+        for (int32_t i = lane; i < 2 * vec; i += nlanes) {
+            uint8_t* row = i < vec ? kr : kr + (int64_t)v.page_tokens * v.row_bytes;
+            reinterpret_cast<uint4*>(row)[i < vec ? i : i - vec] = make_uint4(w, w, w, w);
+        }
+    }
+    if (lane == 0) {
+        v.imp[(int64_t)u * v.cap + s] = __int_as_float(0x7FC00000);
+        v.pos[(int64_t)u * v.cap + s] = -1;
+    }
 }
 
 // Address of the K (or V) row of slot s of unit u; nullptr if the page is bad.
@@ -561,6 +588,8 @@ struct GatherArgs {
 };
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s);
 cudaError_t launch_selftest_timeout(const View& v, uint64_t limit_ns, cudaStream_t s);
+// fill n 32-bit words at p with `word` (debug mode's NaN pool at create)
+cudaError_t launch_fill_u32(uint32_t* p, size_t n, uint32_t word, cudaStream_t s);
 
 // HiKV Stage II element-level decode (k_elem.cu): sort, span and merge kernels.
 struct ElemArgs {

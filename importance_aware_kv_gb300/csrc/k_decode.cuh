@@ -1100,6 +1100,11 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                     v.pos[(int64_t)u * v.cap + vs] = du.tnew;
                 }
             }
+            if (v.debug && vs >= 0) {
+                if (vs > sn && lane == 0) atomicOr(v.err, DEVERR_STATE);   // a victim past the new slot
+                __syncwarp();
+                poison_slot(v, u, sn, lane, 32);   // the last slot is vacated
+            }
         }
         named_bar_sync(1, NCT);   // shared buffers of this unit are free for the next
         if (ctid == 0) mbar_arrive(&qempty[xb]);

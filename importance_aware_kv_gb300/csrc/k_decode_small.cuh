@@ -396,6 +396,10 @@ __global__ void __launch_bounds__(kSmallThreads, 2)
                     pos[vs] = tnew;
                 }
             }
+            if (v.debug && cut) {
+                __syncwarp();
+                poison_slot(v, u, sn, lane, 32);   // the last slot is vacated
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&qempty[warp * 2 + qb]);   // q, staged rows and S are free

@@ -408,6 +408,10 @@ __device__ void merge_unit(const ElemArgs& a, int32_t uu, int32_t u, int32_t n, 
             v.pos[(int64_t)u * v.cap + vs] = v.pos[(int64_t)u * v.cap + n - 1];
         }
     }
+    if (v.debug && cut) {
+        __syncthreads();
+        if (tid < 32) poison_slot(v, u, n - 1, tid, 32);   // the last slot is vacated
+    }
     if (tid == 0) {
         v.victim[u] = cut ? -1 : vs;
         v.len[u] = cut ? n - 1 : n;

@@ -31,6 +31,10 @@ __device__ __forceinline__ unsigned long long mk_key(float imp, int32_t pos) {
 }
 
 __device__ void move_slot(const View& v, int32_t u, int32_t src, int32_t dst, int lane, int nlanes) {
+    if (v.debug && (src < 0 || src >= v.cap || dst < 0 || dst >= v.cap)) {
+        if (lane == 0) atomicOr(v.err, DEVERR_STATE);
+        return;
+    }
     const int32_t vec = v.row_bytes / 16;
     for (int32_t i = lane; i < 2 * vec; i += nlanes) {
         const bool isv = i >= vec;
@@ -64,6 +68,10 @@ __global__ void k_evict_fast(EvictArgs a) {
     }
     if (vs != n - 1) move_slot(v, u, n - 1, vs, lane, 32);
     __syncwarp();
+    if (v.debug) {
+        poison_slot(v, u, n - 1, lane, 32);   // the last slot is vacated
+        __syncwarp();
+    }
     if (lane == 0) {
         v.len[u] = B;
         v.victim[u] = -1;
@@ -227,6 +235,24 @@ __global__ void __launch_bounds__(kEvThreads) k_evict_general(EvictArgs a) {
         __syncthreads();   // the mover list is rewritten by the next batch
     }
     __syncthreads();
+    if (v.debug) {
+        // every slot in [B, n) is vacated (moved down or evicted) ...
+        for (int32_t s = B + warp; s < n; s += kEvWarps) poison_slot(v, u, s, lane, 32);
+        // ... and every row of the pages about to return to a shared pool
+        const int32_t keep = pages_kept(B, v.page_tokens, v.max_pages);
+        const int32_t m = v.mapped[u];
+        if (!v.home_pages && m > keep) {
+            const uint32_t w = v.row_bytes == 2 * v.d ? 0x7FC07FC0u : 0x7FC00000u;
+            const int64_t words = v.page_bytes / 16;
+            for (int32_t k = keep; k < m; ++k) {
+                const int32_t pg = v.page_table[(int64_t)u * v.max_pages + k];
+                if (pg < 0 || pg >= v.pool_pages) continue;
+                uint4* p = reinterpret_cast<uint4*>(v.pool + (int64_t)pg * v.page_bytes);
+                for (int64_t i = threadIdx.x; i < words; i += kEvThreads) p[i] = make_uint4(w, w, w, w);
+            }
+        }
+        __syncthreads();
+    }
     if (threadIdx.x == 0) {
         if (base != nholes) atomicOr(v.err, DEVERR_STATE);
         v.len[u] = B;

@@ -5,6 +5,8 @@
 // position: positions are unique in [0, next_pos), so a bitmap of present
 // positions and a prefix count over its words give every slot its rank
 // directly.  The bitmap covers 2^16 positions at a time.
+#include <algorithm>
+
 #include "hikv_internal.cuh"
 
 namespace hikv {
@@ -117,6 +119,20 @@ __global__ void k_selftest_timeout(View v, uint64_t limit_ns) {
 
 cudaError_t launch_selftest_timeout(const View& v, uint64_t limit_ns, cudaStream_t s) {
     k_selftest_timeout<<<1, 32, 0, s>>>(v, limit_ns);
+    return cudaGetLastError();
+}
+
+namespace {
+__global__ void k_fill_u32(uint32_t* p, size_t n, uint32_t word) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+        p[i] = word;
+}
+}  // namespace
+
+cudaError_t launch_fill_u32(uint32_t* p, size_t n, uint32_t word, cudaStream_t s) {
+    if (n == 0) return cudaSuccess;
+    const size_t blocks = std::min<size_t>((n + 255) / 256, 65536);
+    k_fill_u32<<<(unsigned)blocks, 256, 0, s>>>(p, n, word);
     return cudaGetLastError();
 }
 

@@ -228,6 +228,20 @@ hikv_status hikv_last_decode_config(const hikv_cache* cache, int32_t* out_host);
  * stream).  Errors: INVALID_ARG, CUDA. */
 hikv_status hikv_element_rows(const hikv_cache* cache, int64_t* rows_host);
 
+/* Diagnostic: the raw contents of slot `slot` of unit `unit` -- K row and V
+ * row (d elements of the cache dtype each), importance, position -- copied
+ * to HOST buffers (any may be NULL), whether the slot is live or not.
+ * Synchronises the device.  With the environment variable HIKV_DEBUG=1 set
+ * when the cache is created, slots that no token holds read as NaN rows,
+ * NaN importance and position -1: the pool starts that way, and every slot
+ * an eviction vacates and every page returned to a shared pool is
+ * overwritten so, so a kernel reading a dead slot turns its outputs into
+ * NaN; slot indices taken from data are also range-checked and reported as
+ * HIKV_ERR_STATE by hikv_device_status.
+ * Errors: INVALID_ARG, STATE (no page mapped for the slot), CUDA. */
+hikv_status hikv_read_slot(const hikv_cache* cache, int32_t unit, int32_t slot, void* k_host, void* v_host,
+                           float* imp_host, int32_t* pos_host);
+
 /* HOST copy of the host mirror of each unit's length (no device access):
  * lengths_host: [nlayers * batch * Hkv].  Errors: INVALID_ARG. */
 hikv_status hikv_get_lengths(const hikv_cache* cache, int32_t layer0, int32_t nlayers,
