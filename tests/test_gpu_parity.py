@@ -133,6 +133,25 @@ def test_more_units_than_resident_clusters(fused):
     _run(SMALL.with_(layers=1, batch=101, hq=8, hkv=4, steps=6), fused=fused)
 
 
+def test_last_round_60_percent_busy_runs_as_two_launches():
+    # 61 x 8 = 488 equal units of ~100 tokens: one round of 304 resident
+    # clusters (2 CTAs per SM on 152 SMs) and a last round 60 % busy, which
+    # the host launches separately at its own cluster size
+    from tests.lockstep import Lockstep
+    w = SMALL.with_(layers=1, batch=61, hq=32, hkv=8, prompt=120, steps=6)
+    ls = Lockstep(w)
+    ls.prefill()
+    rep = ls.decode(fused=True)
+    cfg = ls.cache.last_decode_config()
+    ls.cache.close()
+    assert rep.evictions_checked == w.units * (1 + w.steps)
+    assert len(cfg) == 2, cfg
+    first, rest = cfg
+    assert first["units"] + rest["units"] == w.units
+    assert first["units"] % first["clusters"] == 0          # full rounds only
+    assert 0.5 < rest["units"] / first["clusters"] <= 0.7   # the remainder's share of a round
+
+
 @FUSED
 def test_page_size_variants(fused):
     # 16-token pages: the cache grows a page every 16 steps before the
