@@ -764,6 +764,8 @@ def bench_gpu(args):
     w = W.WORKLOADS[args.workload]
     if args.layers:   # the workload cut to its first L layers (small cases for profiling)
         w = w.with_(layers=min(args.layers, w.layers), name=f"{w.name}-first{min(args.layers, w.layers)}layers")
+    if args.group:    # query heads per KV head: 1 runs the shape as multi-head attention
+        w = w.with_(hq=w.hkv * args.group, name=f"{w.name}-group{args.group}")
     seed = w.index if args.seed is None else args.seed
     cfg_w = w
     gw = global_workload(w, world, args.scaling)
@@ -843,7 +845,8 @@ def bench_gpu(args):
             line["cpu_baseline"]["sample_1thread"] = f"{single[1]} further steps of the same sample on one thread"
         stage("cpu baseline done")
     if rank == 0 and world == 1 and not args.no_other_workloads and args.workload == WORKLOAD_INDEX \
-            and not args.layers and not args.full_cache and not elem and args.schedule in (None, "", "workload"):
+            and not args.layers and not args.group and not args.full_cache and not elem \
+            and args.schedule in (None, "", "workload"):
         line["other_workloads"] = other_workloads(args, dev, peak, stage)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -871,6 +874,8 @@ def main():
                     help="workload index (default: the Llama-3-8B layer the metric is quoted on)")
     ap.add_argument("--layers", type=int, default=0,
                     help="cut the workload to its first L layers (profiling a smaller case; 0: all)")
+    ap.add_argument("--group", type=int, default=0, choices=[0, 1, 2, 4, 8],
+                    help="query heads per KV head (0: the workload's; 1: the shape as multi-head attention)")
     ap.add_argument("--spin-us", type=float, default=60.0)
     ap.add_argument("--impl", default="hikv", choices=["hikv", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")

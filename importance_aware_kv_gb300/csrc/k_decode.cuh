@@ -753,10 +753,9 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
             }   // half-row path
             __syncwarp();
             // ---- p.v over the tile's valid rows (unrolled; invalid rows skipped, their
-            // stale V bytes may hold any bit pattern) ----
-#pragma unroll
-            for (int r = 0; r < kDecTR; ++r) {
-                if (r < lo_r || r >= hi_r) continue;
+            // stale V bytes may hold any bit pattern).  A full tile, the common
+            // case, has no per-row test, so all of its loads can be issued ahead ----
+            auto pv_row = [&](int r) {
                 const Raw raw = *reinterpret_cast<const Raw*>(vtile + toff(r, pv_chunk) + pv_in);
                 float x[EPL];
                 Widen<T, EPL>::run(raw, x);
@@ -785,6 +784,14 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                     for (int e = 0; e < EPL / 2; ++e)
                         o2[h][e] = ffma2(make_float2(x[2 * e], x[2 * e + 1]), pp[h], o2[h][e]);
                 }
+            };
+            if (lo_r == 0 && hi_r == kDecTR) {
+#pragma unroll
+                for (int r = 0; r < kDecTR; ++r) pv_row(r);
+            } else {
+#pragma unroll
+                for (int r = 0; r < kDecTR; ++r)
+                    if (r >= lo_r && r < hi_r) pv_row(r);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[st]);

@@ -11,8 +11,9 @@
 //   producer warp   lane w streams the tiles of warp w's units into the two
 //                   ring stages {w, w + 4} that only warp w consumes, and
 //                   their q (and new rows) into warp w's double buffer;
-//   consumer warp w the tile loop of k_decode (half-row q.k, lazily rescaled
-//                   online softmax, lane-owns-dims p.v), then the output,
+//   consumer warp w the tile loop of k_decode (row-split q.k with q in
+//                   registers, lazily rescaled online softmax, lane-owns-dims
+//                   p.v), then the output,
 //                   the importance pass over the logits it kept in shared
 //                   memory, the victim by warp shuffles, and the fused move.
 // Units come from a per-warp list the host balances (largest first to the
@@ -49,11 +50,21 @@ __global__ void __launch_bounds__(kSmallThreads, 2)
     using Lay = SmallLayout<T, D, G>;
     constexpr int ESZ = (int)sizeof(T);
     constexpr int RB = Lay::RB, TB = Lay::TB, QB = Lay::QB;
-    constexpr int NBOX = RB / 128;
-    constexpr int CPR = RB / 16, CPL = CPR / 2, EPC = 16 / ESZ;
     constexpr int EPL = D / 32, LB = EPL * ESZ;
     constexpr int NCAP = small_unit_cap(G);
-    static_assert(EPL % 2 == 0 && EPC % 2 == 0, "pairs");
+    // row-split q.k, as in k_decode: QK_LPR lanes per row, one 16-byte chunk
+    // each against q in registers; per sub-block of QK_SUB warp steps the
+    // QK_NV (row, head) partial sums are reduce-scattered over the row's lanes
+    constexpr int QK_LPR = RB / 16;
+    constexpr int QK_RPW = 32 / QK_LPR;
+    constexpr int QK_STEPS = kDecTR / QK_RPW;
+    constexpr int QK_EPL = 16 / ESZ;
+    constexpr int QK_SUB = (QK_LPR / G) > QK_STEPS ? QK_STEPS : (QK_LPR / G);
+    constexpr int QK_NSUB = QK_STEPS / QK_SUB;
+    constexpr int QK_NV = QK_SUB * G;
+    constexpr int QK_DUP = QK_LPR / QK_NV;
+    static_assert(EPL % 2 == 0 && QK_EPL % 2 == 0, "pairs");
+    static_assert(QK_SUB >= 1 && QK_STEPS % QK_SUB == 0 && QK_LPR % QK_NV == 0, "one logit per lane and sub-block");
     using Raw = typename RawVec<LB>::type;
 
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -82,8 +93,6 @@ __global__ void __launch_bounds__(kSmallThreads, 2)
 
     if (warp == kSmallWarps) {
         // ======================= producer: lane w feeds warp w =======================
-        if (lane == 0) prefetch_tensormap(&tmap);
-        __syncwarp();
         if (lane < kSmallWarps) {
             const int w = lane;
             const int wi = blockIdx.x * kSmallWarps + w;
@@ -131,15 +140,9 @@ __global__ void __launch_bounds__(kSmallThreads, 2)
                         ++gj;
                         break;
                     }
-                    const int32_t yk = pg * 2 * v.page_tokens + (s0 & (v.page_tokens - 1));
                     uint8_t* dst = ring + st * 2 * TB;
                     mbar_arrive_expect_tx(&full[st], 2 * TB);
-#pragma unroll
-                    for (int bx = 0; bx < NBOX; ++bx) {
-                        tma_load_2d(dst + bx * (kDecTR * 128), &tmap, bx * (128 / ESZ), yk, &full[st]);
-                        tma_load_2d(dst + TB + bx * (kDecTR * 128), &tmap, bx * (128 / ESZ), yk + v.page_tokens,
-                                    &full[st]);
-                    }
+                    dec_load_tile<true, 1, ESZ, RB, TB>(dst, v, pg, s0, &tmap, &full[st]);
                 }
             }
             if (!ok) {
@@ -160,7 +163,9 @@ __global__ void __launch_bounds__(kSmallThreads, 2)
     float* q_s = reinterpret_cast<float*>(smem + Lay::QS) + warp * G * D;
     float* ps = reinterpret_cast<float*>(smem + Lay::PS) + warp * kDecTR * G;
     float* S = reinterpret_cast<float*>(smem + Lay::S) + warp * kSmallLogitFloats;
-    const int qr = lane & 15, qh = lane >> 4;
+    const int qk_c = lane % QK_LPR, qk_rg = lane / QK_LPR;
+    const int qk_k = qk_c / QK_DUP, qk_step = qk_k / G, hk = qk_k % G;
+    const bool qk_own = (qk_c % QK_DUP) == 0;
     const int pv_chunk = (lane * LB) >> 4, pv_in = (lane * LB) & 15;
     int gj = 0;
     bool ok = true;
@@ -194,12 +199,18 @@ __global__ void __launch_bounds__(kSmallThreads, 2)
         }
         __syncwarp();
 
-        float m_w[G], l_w[G];
+        float2 qreg[G][QK_EPL / 2];
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int e = 0; e < QK_EPL / 2; ++e)
+                qreg[h][e] = *reinterpret_cast<const float2*>(q_s + h * D + qk_c * QK_EPL + 2 * e);
+        float m_w[G];
+        float m_own = -INFINITY, l_own = 0.f;
         float2 o2[G][EPL / 2];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
             m_w[h] = -INFINITY;
-            l_w[h] = 0.f;
 #pragma unroll
             for (int e = 0; e < EPL / 2; ++e) o2[h][e] = make_float2(0.f, 0.f);
         }
@@ -219,8 +230,8 @@ __global__ void __launch_bounds__(kSmallThreads, 2)
                 const int r = sn - s0;
                 const Raw nk = *reinterpret_cast<const Raw*>(nrow + lane * LB);
                 const Raw nv = *reinterpret_cast<const Raw*>(nrow + RB + lane * LB);
-                *reinterpret_cast<Raw*>(ktile + swz(r, pv_chunk) + pv_in) = nk;
-                *reinterpret_cast<Raw*>(vtile + swz(r, pv_chunk) + pv_in) = nv;
+                *reinterpret_cast<Raw*>(ktile + lin<RB>(r, pv_chunk) + pv_in) = nk;
+                *reinterpret_cast<Raw*>(vtile + lin<RB>(r, pv_chunk) + pv_in) = nv;
                 fence_proxy_async_smem();
                 const int32_t pg = v.page_table[(int64_t)u * v.max_pages + (sn >> v.page_shift)];
                 if (pg >= 0 && pg < v.pool_pages) {
@@ -230,48 +241,50 @@ __global__ void __launch_bounds__(kSmallThreads, 2)
                 }
                 __syncwarp();
             }
-            // q.k: this lane's half row (chunks interleaved between the halves)
-            float2 acc[G];
+            // q.k: per sub-block, each lane's chunk of QK_SUB rows against q in
+            // registers, then the partial sums reduce-scattered
+            float sv[QK_NSUB];
 #pragma unroll
-            for (int h = 0; h < G; ++h) acc[h] = make_float2(0.f, 0.f);
+            for (int sb = 0; sb < QK_NSUB; ++sb) {
+                float part[QK_NV];
 #pragma unroll
-            for (int j = 0; j < CPL; ++j) {
-                const int cidx = 2 * j + qh;
-                const uint4 raw = *reinterpret_cast<const uint4*>(ktile + swz(qr, cidx));
-                float x[EPC];
-                Widen<T, EPC>::run(raw, x);
+                for (int j = 0; j < QK_SUB; ++j) {
+                    const int r = (sb * QK_SUB + j) * QK_RPW + qk_rg;
+                    const uint4 raw = *reinterpret_cast<const uint4*>(ktile + lin<RB>(r, qk_c));
+                    float x[QK_EPL];
+                    Widen<T, QK_EPL>::run(raw, x);
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    const float* qp = q_s + h * D + cidx * EPC;
+                    for (int h = 0; h < G; ++h) {
+                        float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int e = 0; e < EPC; e += 4) {
-                        const float4 q4 = *reinterpret_cast<const float4*>(qp + e);
-                        acc[h] = ffma2(make_float2(x[e], x[e + 1]), make_float2(q4.x, q4.y), acc[h]);
-                        acc[h] = ffma2(make_float2(x[e + 2], x[e + 3]), make_float2(q4.z, q4.w), acc[h]);
+                        for (int e = 0; e < QK_EPL / 2; ++e)
+                            acc = ffma2(make_float2(x[2 * e], x[2 * e + 1]), qreg[h][e], acc);
+                        part[j * G + h] = acc.x + acc.y;
                     }
                 }
-            }
-            const bool rv = qr < hi_r;
-            float s[G];
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                float tt = acc[h].x + acc[h].y;
-                tt += __shfl_xor_sync(0xffffffffu, tt, 16);
-                s[h] = rv ? tt : -INFINITY;
+                qk_reduce<QK_LPR / 2, QK_NV>(part, lane);
+                const int r = (sb * QK_SUB + qk_step) * QK_RPW + qk_rg;
+                sv[sb] = r < hi_r ? part[0] : -INFINITY;
             }
             bool big = false;
 #pragma unroll
-            for (int h = 0; h < G; ++h) big |= s[h] > m_w[h] + kDecLazy;
+            for (int sb = 0; sb < QK_NSUB; ++sb) big |= sv[sb] > m_own + kDecLazy;
             if (__any_sync(0xffffffffu, big)) {
+                float tmax = sv[0];
+#pragma unroll
+                for (int sb = 1; sb < QK_NSUB; ++sb) tmax = fmaxf(tmax, sv[sb]);
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
-                    float mt = s[h];
+                    float mt = hk == h ? tmax : -INFINITY;
 #pragma unroll
-                    for (int o = 8; o >= 1; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+                    for (int o = 16; o >= 1; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
                     const float mn = fmaxf(m_w[h], mt);
                     const float scl = exp2f(m_w[h] - mn);
                     m_w[h] = mn;
-                    l_w[h] *= scl;
+                    if (hk == h) {
+                        l_own *= scl;
+                        m_own = mn;
+                    }
 #pragma unroll
                     for (int e = 0; e < EPL / 2; ++e) {
                         o2[h][e].x *= scl;
@@ -279,21 +292,21 @@ __global__ void __launch_bounds__(kSmallThreads, 2)
                     }
                 }
             }
-            float p[G];
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                p[h] = rv ? exp2f(s[h] - m_w[h]) : 0.f;
-                l_w[h] += p[h];
-            }
-            if (qh == 0) {
-                store_group<G>(ps + qr * G, p);
-                if (rv && s0 + qr < NCAP) store_group<G>(S + (s0 + qr) * G, s);
+            for (int sb = 0; sb < QK_NSUB; ++sb) {
+                const int r = (sb * QK_SUB + qk_step) * QK_RPW + qk_rg;
+                const bool rv = sv[sb] > -INFINITY;
+                const float p = rv ? exp2f(sv[sb] - m_own) : 0.f;
+                if (qk_own) {
+                    l_own += p;
+                    ps[r * G + hk] = p;
+                    if (rv && s0 + r < NCAP) S[(s0 + r) * G + hk] = sv[sb];
+                }
             }
             __syncwarp();
-#pragma unroll
-            for (int r = 0; r < kDecTR; ++r) {
-                if (r >= hi_r) continue;
-                const Raw raw = *reinterpret_cast<const Raw*>(vtile + swz(r, pv_chunk) + pv_in);
+            // p.v; a full tile has no per-row test, so its loads can be issued ahead
+            auto pv_row = [&](int r) {
+                const Raw raw = *reinterpret_cast<const Raw*>(vtile + lin<RB>(r, pv_chunk) + pv_in);
                 float x[EPL];
                 Widen<T, EPL>::run(raw, x);
                 const float* pr = ps + r * G;
@@ -305,6 +318,14 @@ __global__ void __launch_bounds__(kSmallThreads, 2)
 #pragma unroll
                     for (int e = 0; e < EPL / 2; ++e)
                         o2[h][e] = ffma2(make_float2(x[2 * e], x[2 * e + 1]), pp[h], o2[h][e]);
+            };
+            if (hi_r == kDecTR) {
+#pragma unroll
+                for (int r = 0; r < kDecTR; ++r) pv_row(r);
+            } else {
+#pragma unroll
+                for (int r = 0; r < kDecTR; ++r)
+                    if (r < hi_r) pv_row(r);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[st]);
@@ -315,9 +336,10 @@ __global__ void __launch_bounds__(kSmallThreads, 2)
         float li_[G];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
+            float t = (qk_own && hk == h) ? l_own : 0.f;
 #pragma unroll
-            for (int o = 8; o >= 1; o >>= 1) l_w[h] += __shfl_xor_sync(0xffffffffu, l_w[h], o);
-            li_[h] = 1.0f / l_w[h];
+            for (int o = 16; o >= 1; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+            li_[h] = 1.0f / t;
         }
         {
             T* outp = reinterpret_cast<T*>(a.out) + (((int64_t)li * v.batch + b) * v.hq + (int64_t)g * G) * D;
