@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(kEvThreads) k_evict_general(EvictArgs a) {
 
     __shared__ uint32_t hist[kEvWarps][256];   // per-warp histograms
     __shared__ unsigned long long s_prefix, s_mask;
-    __shared__ int32_t s_rem;
+    __shared__ int32_t s_rem, s_done;
     __shared__ int32_t wsum[kEvWarps];
     __shared__ int32_t mv_src[kEvThreads], mv_dst[kEvThreads];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -124,6 +124,7 @@ __global__ void __launch_bounds__(kEvThreads) k_evict_general(EvictArgs a) {
         s_prefix = 0ull;
         s_mask = 0ull;
         s_rem = kmid;
+        s_done = 0;
     }
     __syncthreads();
     if (kmid > 0) {
@@ -169,11 +170,12 @@ __global__ void __launch_bounds__(kEvThreads) k_evict_general(EvictArgs a) {
                 const int32_t above = incl - tot;   // bins of lanes > this one
                 const int32_t rem = s_rem;
                 if (above < rem && rem <= incl) {
-                    int32_t cum = above, sel = 8 * lane, r = rem;
+                    int32_t cum = above, sel = 8 * lane, r = rem, csel = 0;
                     for (int j = 7; j >= 0; --j) {
                         if (cum + (int32_t)c[j] >= rem) {
                             sel = 8 * lane + j;
                             r = rem - cum;
+                            csel = (int32_t)c[j];
                             break;
                         }
                         cum += (int32_t)c[j];
@@ -181,9 +183,14 @@ __global__ void __launch_bounds__(kEvThreads) k_evict_general(EvictArgs a) {
                     s_rem = r;
                     s_prefix = prefix | ((unsigned long long)sel << shift);
                     s_mask = mask | (255ull << shift);
+                    // every key of the chosen bin survives: then the bin's
+                    // lowest possible key (the prefix, low bits zero) already
+                    // splits the kmid largest from the rest
+                    s_done = r == csel;
                 }
             }
             __syncthreads();
+            if (s_done) break;
         }
     }
     const unsigned long long T = s_prefix;
