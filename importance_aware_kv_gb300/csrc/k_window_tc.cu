@@ -25,6 +25,8 @@
 // query-major (row = query * G + head), so the G heads of a query sit in
 // lanes that differ only in lane bits 2.. and pass 2 sums them with G - 1
 // shuffles before staging one increment per (query, token).
+#include <type_traits>
+
 #include "hikv_internal.cuh"
 
 namespace hikv {
@@ -193,6 +195,7 @@ __global__ void __launch_bounds__(kTcThreads, NQV <= 64 ? 3 : 2) k_window_tc(con
         af[ks][3] = ld(row1, k0 + 8);
     }
     // causal limit of each of this lane's two rows (query i sits at tnew - nq + 1 + i)
+    const int32_t qfirst = tnew - nq + 1;
     const int32_t qpos0 = row0 < nqv ? tnew - nq + 1 + row0 / G : INT32_MIN;
     const int32_t qpos1 = row1 < nqv ? tnew - nq + 1 + row1 / G : INT32_MIN;
 
@@ -238,7 +241,14 @@ __global__ void __launch_bounds__(kTcThreads, NQV <= 64 ? 3 : 2) k_window_tc(con
         // one thread waits for the tile (bounded); the CTA barrier then orders
         // every thread's reads after the copy, and all take the same branch
         if (tid == 0) *landed = mbar_wait_bounded(&bar[st], (uint32_t)(i / C::STAGES) & 1u, v.err, kWaitFull, (uint32_t)i);
-        __syncthreads();
+        // a full tile whose tokens all precede the first window query is seen
+        // whole by every query: no causal mask (all tiles but the last few).
+        // Only with 128 query rows: with fewer, the two compiled bodies cost
+        // more in register spills than the mask does (measured on the 32-layer
+        // stack's 64 rows)
+        bool all_vis = false;
+        if constexpr (NQV >= 128) all_vis = __syncthreads_and(tid >= kTcTok || Pi[tid] <= qfirst) != 0;
+        else __syncthreads();
         if (!*landed) {
             // give up; let the copies already queued for the following tiles land first
             if (tid == 0)
@@ -274,6 +284,8 @@ __global__ void __launch_bounds__(kTcThreads, NQV <= 64 ? 3 : 2) k_window_tc(con
         }
         // logits (log2 domain) and causal visibility: value j of block nb is
         // row (j < 2 ? row0 : row1), token cslice*COLS + nb*8 + 2t + (j & 1)
+        auto tile_math = [&](auto masked_tag) {
+        constexpr bool kMasked = decltype(masked_tag)::value;
         float s[C::NB][4];
         bool vis[C::NB][4];
 #pragma unroll
@@ -281,8 +293,7 @@ __global__ void __launch_bounds__(kTcThreads, NQV <= 64 ? 3 : 2) k_window_tc(con
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int col = cslice * C::COLS + nb * 8 + 2 * t + (j & 1);
-                const int32_t p = Pi[col];
-                vis[nb][j] = p <= (j < 2 ? qpos0 : qpos1);
+                vis[nb][j] = kMasked ? Pi[col] <= (j < 2 ? qpos0 : qpos1) : true;
                 s[nb][j] = acc[nb][j] * qscale;
             }
         if (!PASS2) {
@@ -342,6 +353,13 @@ __global__ void __launch_bounds__(kTcThreads, NQV <= 64 ? 3 : 2) k_window_tc(con
                 for (int qi = 0; qi < nq; ++qi) imp = imp + Pt[qi * PT + tid];
                 v.imp[(int64_t)u * v.cap + s0 + tid] = imp;
             }
+        }
+        };
+        if constexpr (NQV >= 128) {
+            if (all_vis) tile_math(std::integral_constant<bool, false>{});
+            else tile_math(std::integral_constant<bool, true>{});
+        } else {
+            tile_math(std::integral_constant<bool, true>{});
         }
         __syncthreads();   // the tile buffer, Ps and Pt are free again
     }
