@@ -318,7 +318,12 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
         holes_total += std::max(0, std::min(c->budget_unit[u], c->cap - c->budget_unit[u]));
     }
     c->wchunks = ceil_div(c->cap, kWindowChunk);
-    const bool need_logits = dec_chunk_max(c->cap, kMaxCS) > c->max_smem_chunk;
+    // the decode kernel's global logits (a CTA's chunk too large for shared
+    // memory): always there (G floats a slot, about 6 % of the K/V bytes at
+    // d = 128), so that the cluster size is chosen by cost, not by what fits
+    // shared memory -- one CTA per unit with global logits beats two with
+    // shared-memory logits on ragged budgets (HeadKV workload: 157 vs 183 us)
+    const bool need_logits = true;
 
 #define ALLOC(ptr, n)                                                       \
     if ((e = dalloc(c, &(ptr), (n))) != cudaSuccess) {                      \
