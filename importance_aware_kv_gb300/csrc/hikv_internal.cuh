@@ -106,7 +106,17 @@ __host__ __device__ constexpr int dec_consumer_warps(int /*row_bytes*/, int /*gr
 // one per half of the group's query heads (two sets of dec_consumer_warps
 // warps rotating over the same tiles), so a warp carries the state of four
 // heads and twice the warps hide the tile loop's latency.
-__host__ __device__ constexpr int dec_head_groups(int group) { return group == 8 ? HIKV_G8_GROUPS : 1; }
+// Groups of eight query heads on bf16 rows of d = 128 run q.k and p.v on
+// the tensor cores (mma.sync m16n8k16, the eight heads in one warp's n = 8),
+// with one head group.  Measured on the 70B shape (640 units of 4,097
+// tokens) 312 us against 404 us for the two CUDA-core head groups; with four
+// heads the CUDA-core row-split path is as fast or slightly faster (the
+// Llama-3-8B layer 20.9 us both, the 32-layer stack 259.7 against 261.6 us),
+// so smaller groups stay on it.
+__host__ __device__ constexpr bool dec_tc(int elem_bytes, int d, int group) {
+    return elem_bytes == 2 && d == 128 && group == 8;
+}
+__host__ __device__ constexpr int dec_head_groups(int group, bool tc) { return group == 8 && !tc ? HIKV_G8_GROUPS : 1; }
 __host__ __device__ constexpr int dec_stages(int /*row_bytes*/, int /*group*/) { return 8; }
 
 __host__ __device__ inline int32_t ceil_div(int32_t a, int32_t b) { return (a + b - 1) / b; }
@@ -321,6 +331,50 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
 
 // 1-D bulk copy global -> shared (TMA engine), completion counted on `bar`.
 // dst, src 16-byte aligned; bytes a multiple of 16.
+// mma.sync m16n8k16, bf16 operands, fp32 accumulate: D = A * B + D with A
+// 16 x 16 row-major (4 registers), B 16 x 8 column-major (2 registers).
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Four 8x8 b16 matrices from shared memory: lane l gives the address of row
+// (l mod 8) of matrix l / 8 (16 contiguous bytes); register i receives
+// matrix i, each lane holding row lane / 4, columns 2 (lane mod 4) and + 1.
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t saddr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(saddr));
+}
+// the same, each matrix transposed: lane l receives column l / 4, rows
+// 2 (l mod 4) and + 1 of the stored matrix
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t saddr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(saddr));
+}
+
+// two floats as a bf16 pair (round to nearest even), the first in the low half
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&p);
+}
+
+// x0, x1 as three bf16 pairs whose sums give back their fp32 values: hi =
+// x rounded to bf16, mid = the remainder (exact in fp32) rounded, lo = what
+// is left of it rounded; 3 x 8 significant bits cover fp32's 24
+__device__ __forceinline__ void split3_bf16(float x0, float x1, uint32_t& hi, uint32_t& mid, uint32_t& lo) {
+    const float h0 = __bfloat162float(__float2bfloat16_rn(x0)), h1 = __bfloat162float(__float2bfloat16_rn(x1));
+    const float r0 = x0 - h0, r1 = x1 - h1;
+    const float m0 = __bfloat162float(__float2bfloat16_rn(r0)), m1 = __bfloat162float(__float2bfloat16_rn(r1));
+    hi = pack_bf16x2(h0, h1);
+    mid = pack_bf16x2(m0, m1);
+    lo = pack_bf16x2(r0 - m0, r1 - m1);
+}
+
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(

@@ -48,7 +48,9 @@ namespace hikv {
 
 // threads of a decode CTA: the consumer warps and one producer warp
 template <typename T, int D, int G>
-constexpr int dec_threads() { return (dec_consumer_warps(D * (int)sizeof(T), G) * dec_head_groups(G) + 1) * 32; }
+constexpr int dec_threads() {
+    return (dec_consumer_warps(D * (int)sizeof(T), G) * dec_head_groups(G, dec_tc((int)sizeof(T), D, G)) + 1) * 32;
+}
 constexpr int kDecTR = 16;                       // slots per tile
 constexpr float kDecLazy = 8.f;                  // softmax reference slack (log2 units)
 constexpr int kDecMaxPg = 256;                   // page ids cached in shared memory
@@ -78,7 +80,8 @@ __host__ __device__ inline DecSmem dec_layout(bool smem_s, int chunk_cap) {
     L.q = off;                                    // q * scale * log2 e, fp32 [G][D]
     off += G * D * 4;
     L.ps = off;                                   // per-warp p of the tile [NCW * HG][16][G / HG]
-    off += kDecNGW * kDecTR * G * 4;              // (= NCW * HG * 16 * G / HG)
+    // (= NCW * HG * 16 * G / HG; on the tensor cores [NCW][16][8], the heads padded to the mma's n = 8)
+    off += kDecNGW * kDecTR * (dec_tc((int)sizeof(T), D, G) ? 8 : G) * 4;
     L.red = off;                                  // warp O partials [NGW][G][D]
     off += kDecNGW * G * D * 4;
     // exchange buffer per unit parity: m [kMaxCS][G], l [kMaxCS][G], O slices [G*D + kMaxCS]
@@ -199,7 +202,8 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
     k_decode(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap) {
     constexpr int ESZ = (int)sizeof(T);
     constexpr int kDecNGW = dec_consumer_warps(D * ESZ, G);   // warps of a head group (the tile rotation)
-    constexpr int kHG = dec_head_groups(G);                   // head groups
+    constexpr bool kTC = dec_tc(ESZ, D, G);                      // q.k and p.v on the tensor cores
+    constexpr int kHG = dec_head_groups(G, kTC);              // head groups
     constexpr int kDecNCW = kDecNGW * kHG;                    // consumer warps
     constexpr int GW = G / kHG;                               // query heads of a warp
     constexpr int RB = D * ESZ;              // row bytes: 128, 256 or 512
@@ -227,6 +231,10 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
     // (lane = tile row and half of it, q read from shared memory) over
     // 128-byte-swizzled tiles that 2-D TMA boxes lay down
     constexpr bool kRS = kHG == 1;
+    // tiles laid down as plain rows by 1-D bulk copies (the row-split CUDA-
+    // core path), else as 128-byte-swizzled 2-D TMA boxes (the half-row path,
+    // and the tensor cores, whose ldmatrix row reads then hit distinct banks)
+    constexpr bool kLin = kRS && !kTC;
     constexpr int CPL = CPR / 2;             // half-row q.k: chunks per lane
     constexpr int QK_LPR = RB / 16;
     constexpr int QK_RPW = 32 / QK_LPR;
@@ -341,7 +349,7 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                 }
                 uint8_t* dst = ring + i * 2 * TB;
                 mbar_arrive_expect_tx(&full[i], 2 * TB);
-                dec_load_tile<kRS, NBOX, ESZ, RB, TB>(dst, v, pg, s0, &tmap, &full[i]);
+                dec_load_tile<kLin, NBOX, ESZ, RB, TB>(dst, v, pg, s0, &tmap, &full[i]);
                 pre_issued = i + 1;
             }
         }
@@ -374,7 +382,7 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
 
     if (warp == kDecNCW) {
         // ======================= producer =======================
-        if (!kRS && lane == 0) prefetch_tensormap(&tmap);
+        if (!kLin && lane == 0) prefetch_tensormap(&tmap);
         int gi = pre_issued;   // running tile counter of this CTA (lane 0's copy is authoritative)
         for (int k = 0, idx = it0; idx < it1; ++k, idx += istep) {
             if (*abort_flag) break;
@@ -455,7 +463,7 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                     if (pf > 0 && i + pf < nt) prefetch_tile(i + pf);
                     uint8_t* dst = ring + st * 2 * TB;
                     mbar_arrive_expect_tx(&full[st], 2 * TB);
-                    dec_load_tile<kRS, NBOX, ESZ, RB, TB>(dst, v, pg, s0, &tmap, &full[st]);
+                    dec_load_tile<kLin, NBOX, ESZ, RB, TB>(dst, v, pg, s0, &tmap, &full[st]);
                 }
             }
             gi = __shfl_sync(0xffffffffu, gi, 0);
@@ -476,7 +484,7 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
     const int ctid = tid;  // consumer thread 0 .. NCT-1
     const int wg = warp / kDecNGW, wi = warp % kDecNGW;   // head group, place in the tile rotation
     const int h0 = wg * GW;                               // this warp's heads: h0 .. h0 + GW - 1
-    float* ps = ps_all + warp * (kDecTR * GW);     // [16][GW] p of the tile
+    float* ps = ps_all + warp * (kDecTR * (kTC ? 8 : GW));   // [16][GW] p of the tile ([16][8] on the tensor cores)
     const int qr = lane & 15;                       // half-row q.k: tile row of this lane
     const int qh = lane >> 4;                       //               half of the row
     const int qk_c = lane % QK_LPR;                 // q.k: chunk of the row this lane reads
@@ -488,9 +496,13 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
     const int pv_chunk = (lane * LB) >> 4, pv_in = (lane * LB) & 15;
     // byte offset of 16-byte chunk c of tile row r in a ring stage
     auto toff = [](int r, int c) -> uint32_t {
-        if constexpr (kRS) return lin<RB>(r, c);
+        if constexpr (kLin) return lin<RB>(r, c);
         else return swz(r, c);
     };
+    // tensor-core fragments: this lane's row group (token or d offset) and
+    // column pair (heads 2 tc_t, 2 tc_t + 1)
+    const int tc_g = lane >> 2, tc_t = lane & 3;
+    const int tc_hA = 2 * tc_t, tc_hB = tc_hA + 1;
     int gi_base = 0;
 
     for (int k = 0, idx = it0; idx < it1; ++k, idx += istep) {
@@ -562,8 +574,24 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
         named_bar_sync(1, NCT);
 
         // q of this warp's heads at this lane's chunk, in registers
-        float2 qreg[kRS ? GW : 1][QK_EPL / 2];
-        if constexpr (kRS) {
+        float2 qreg[(kRS && !kTC) ? GW : 1][QK_EPL / 2];
+        // tensor cores: q as the B operand of S = K q^T (k = dimension, n =
+        // head), this lane's head tc_g and dimensions 16 ks + 2 tc_t (+ 1, + 8,
+        // + 9) of each k-step, split into three bf16 parts (hi + mid + lo
+        // carries q's 24-bit mantissa; K is bf16, so each partial product is
+        // exact and the logits keep fp32 accuracy)
+        uint32_t qb[kTC ? 3 : 1][kTC ? D / 16 : 1][2];
+        if constexpr (kTC) {
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks)
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const int d0 = ks * 16 + 2 * tc_t + 8 * r;
+                    const float x0 = tc_g < G ? q_s[tc_g * D + d0] : 0.f;
+                    const float x1 = tc_g < G ? q_s[tc_g * D + d0 + 1] : 0.f;
+                    split3_bf16(x0, x1, qb[0][ks][r], qb[1][ks][r], qb[2][ks][r]);
+                }
+        } else if constexpr (kRS) {
 #pragma unroll
             for (int h = 0; h < GW; ++h)
 #pragma unroll
@@ -576,14 +604,23 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
         float m_w[GW], l_tail[GW];
         float l_row[GW];   // half-row path: this lane's row sums of every head
         float m_own = -INFINITY, l_own = 0.f;
-        float2 o2[GW][EPL / 2];
+        float2 o2[kTC ? 1 : GW][EPL / 2];
+        // tensor cores: the reference and this lane's row-sum share of heads
+        // tc_hA, tc_hB, and O^T in the mma's C layout (d-block mb: d = 16 mb +
+        // tc_g (+ 8), heads tc_hA, tc_hB)
+        float tc_m[2] = {-INFINITY, -INFINITY}, tc_l[2] = {0.f, 0.f};
+        float tc_o[kTC ? D / 16 : 1][4];
+#pragma unroll
+        for (int mb = 0; mb < (kTC ? D / 16 : 1); ++mb) tc_o[mb][0] = tc_o[mb][1] = tc_o[mb][2] = tc_o[mb][3] = 0.f;
 #pragma unroll
         for (int h = 0; h < GW; ++h) {
             m_w[h] = -INFINITY;
             l_tail[h] = 0.f;
             l_row[h] = 0.f;
+            if constexpr (!kTC) {
 #pragma unroll
-            for (int e = 0; e < EPL / 2; ++e) o2[h][e] = make_float2(0.f, 0.f);
+                for (int e = 0; e < EPL / 2; ++e) o2[h][e] = make_float2(0.f, 0.f);
+            }
         }
 
         for (int i = wi; i < nt; i += kDecNGW) {
@@ -619,6 +656,116 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                 __syncwarp();
             }
 
+            if constexpr (kTC) {
+            // ---- S = K q^T on the tensor cores: m = the tile's 16 tokens,
+            // n = the group's heads (padded to 8), k = d; q in three parts ----
+            // Each mma sums from zero and the partial sums are added in fp32
+            // (round to nearest): chaining the accumulator through the mma
+            // would round every step toward zero, a bias that large logits
+            // turn into a visible error in p
+            float sc[4] = {0.f, 0.f, 0.f, 0.f};
+            {
+                const uint32_t kb = smem_u32(ktile);
+                const int mi = lane >> 3;
+                const int row = (mi & 1) * 8 + (lane & 7);   // ldmatrix: this lane's row of matrix mi
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    uint32_t af[4];
+                    ldmatrix_x4(af, kb + swz(row, 2 * ks + (mi >> 1)));
+#pragma unroll
+                    for (int pt = 0; pt < 3; ++pt) {
+                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                        mma_bf16_16816(acc, af, qb[pt][ks][0], qb[pt][ks][1]);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) sc[j] += acc[j];
+                    }
+                }
+            }
+            // sc: (token tc_g, head tc_hA), (tc_g, tc_hB), (tc_g + 8, tc_hA), (tc_g + 8, tc_hB)
+            const bool r0v = tc_g >= lo_r && tc_g < hi_r, r1v = tc_g + 8 >= lo_r && tc_g + 8 < hi_r;
+            const bool vA = tc_hA < G, vB = tc_hB < G;
+            float s4[4];
+            s4[0] = (r0v && vA) ? sc[0] : -INFINITY;
+            s4[1] = (r0v && vB) ? sc[1] : -INFINITY;
+            s4[2] = (r1v && vA) ? sc[2] : -INFINITY;
+            s4[3] = (r1v && vB) ? sc[3] : -INFINITY;
+            // ---- online softmax over this tile, lazily rescaled (as below) ----
+            const bool big = fmaxf(s4[0], s4[2]) > tc_m[0] + kDecLazy || fmaxf(s4[1], s4[3]) > tc_m[1] + kDecLazy;
+            if (__any_sync(0xffffffffu, big)) {
+                float mA = fmaxf(s4[0], s4[2]), mB = fmaxf(s4[1], s4[3]);
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) {   // over the lanes of the same heads
+                    mA = fmaxf(mA, __shfl_xor_sync(0xffffffffu, mA, o));
+                    mB = fmaxf(mB, __shfl_xor_sync(0xffffffffu, mB, o));
+                }
+                const float nA = fmaxf(tc_m[0], mA), nB = fmaxf(tc_m[1], mB);
+                // 1 when unchanged, 0 from -inf; a head without a logit yet stays at -inf
+                const float sA = nA == -INFINITY ? 1.f : exp2f(tc_m[0] - nA);
+                const float sB = nB == -INFINITY ? 1.f : exp2f(tc_m[1] - nB);
+                tc_m[0] = nA;
+                tc_m[1] = nB;
+                tc_l[0] *= sA;
+                tc_l[1] *= sB;
+#pragma unroll
+                for (int mb = 0; mb < D / 16; ++mb) {
+                    tc_o[mb][0] *= sA;
+                    tc_o[mb][2] *= sA;
+                    tc_o[mb][1] *= sB;
+                    tc_o[mb][3] *= sB;
+                }
+            }
+            float p4[4];
+            p4[0] = s4[0] == -INFINITY ? 0.f : exp2f(s4[0] - tc_m[0]);
+            p4[1] = s4[1] == -INFINITY ? 0.f : exp2f(s4[1] - tc_m[1]);
+            p4[2] = s4[2] == -INFINITY ? 0.f : exp2f(s4[2] - tc_m[0]);
+            p4[3] = s4[3] == -INFINITY ? 0.f : exp2f(s4[3] - tc_m[1]);
+            tc_l[0] += p4[0] + p4[2];
+            tc_l[1] += p4[1] + p4[3];
+            auto keep_s = [&](int r, int h, float x) {   // for the importance pass
+                if (r >= lo_r && r < hi_r && h < G && (!SMEM_S || s0 + r - s_off < a.chunk_cap))
+                    Sb[(int64_t)(s0 + r - s_off) * G + h] = x;
+            };
+            keep_s(tc_g, tc_hA, sc[0]);
+            keep_s(tc_g, tc_hB, sc[1]);
+            keep_s(tc_g + 8, tc_hA, sc[2]);
+            keep_s(tc_g + 8, tc_hB, sc[3]);
+            // ---- P into the B layout of O^T += V^T P (k = token, n = head)
+            // through this warp's [16][8] scratch, in three bf16 parts ----
+            *reinterpret_cast<float2*>(ps + tc_g * 8 + tc_hA) = make_float2(p4[0], p4[1]);
+            *reinterpret_cast<float2*>(ps + (tc_g + 8) * 8 + tc_hA) = make_float2(p4[2], p4[3]);
+            __syncwarp();
+            uint32_t pb[3][2];
+            split3_bf16(ps[(2 * tc_t) * 8 + tc_g], ps[(2 * tc_t + 1) * 8 + tc_g], pb[0][0], pb[1][0], pb[2][0]);
+            split3_bf16(ps[(2 * tc_t + 8) * 8 + tc_g], ps[(2 * tc_t + 9) * 8 + tc_g], pb[0][1], pb[1][1], pb[2][1]);
+            if (lo_r > 0 || hi_r < kDecTR) {
+                // a partial tile's other rows hold stale bytes (any bit
+                // pattern, which p = 0 would not cancel): zero their V
+                for (int i = lane; i < kDecTR * CPR; i += 32) {
+                    const int r = i / CPR;
+                    if (r < lo_r || r >= hi_r) *reinterpret_cast<uint4*>(vtile + swz(r, i % CPR)) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();   // the stage is refilled by TMA later
+                __syncwarp();
+            }
+            {
+                const uint32_t vb = smem_u32(vtile);
+                const int mi = lane >> 3;
+                const int trow = (mi >> 1) * 8 + (lane & 7);   // ldmatrix: this lane's token row of matrix mi
+                // likewise every mma from zero, added to O in fp32
+#pragma unroll
+                for (int mb = 0; mb < D / 16; ++mb) {
+                    uint32_t af[4];
+                    ldmatrix_x4_trans(af, vb + swz(trow, 2 * mb + (mi & 1)));
+#pragma unroll
+                    for (int pt = 0; pt < 3; ++pt) {
+                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                        mma_bf16_16816(acc, af, pb[pt][0], pb[pt][1]);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) tc_o[mb][j] += acc[j];
+                    }
+                }
+            }
+            } else {   // CUDA cores
             if constexpr (kRS) {
             // ---- q.k: per sub-block, each lane's chunk of QK_SUB rows against
             // q in registers, then the partial sums reduce-scattered ----
@@ -793,6 +940,7 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                 for (int r = 0; r < kDecTR; ++r)
                     if (r >= lo_r && r < hi_r) pv_row(r);
             }
+            }   // CUDA cores
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[st]);
         }
@@ -819,6 +967,55 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                 s[h] = t;
                 big |= t > m_w[h] + kDecLazy;
             }
+            if constexpr (kTC) {
+                // this lane's heads tc_hA, tc_hB in the mma's C layout (each
+                // head's reference moves on its own: the result does not depend
+                // on the reference); V through this warp's scratch as floats
+                float sA = -INFINITY, sB = -INFINITY;
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    if (h == tc_hA) sA = s[h];
+                    if (h == tc_hB) sB = s[h];
+                }
+                if (sA > tc_m[0] + kDecLazy) {
+                    const float sc_ = exp2f(tc_m[0] - sA);
+                    tc_m[0] = sA;
+                    tc_l[0] *= sc_;
+#pragma unroll
+                    for (int mb = 0; mb < D / 16; ++mb) {
+                        tc_o[mb][0] *= sc_;
+                        tc_o[mb][2] *= sc_;
+                    }
+                }
+                if (sB > tc_m[1] + kDecLazy) {
+                    const float sc_ = exp2f(tc_m[1] - sB);
+                    tc_m[1] = sB;
+                    tc_l[1] *= sc_;
+#pragma unroll
+                    for (int mb = 0; mb < D / 16; ++mb) {
+                        tc_o[mb][1] *= sc_;
+                        tc_o[mb][3] *= sc_;
+                    }
+                }
+                const float pA = sA == -INFINITY ? 0.f : exp2f(sA - tc_m[0]);
+                const float pB = sB == -INFINITY ? 0.f : exp2f(sB - tc_m[1]);
+                if (tc_g == 0) {   // the tail row, once in the warp's row sums
+                    tc_l[0] += pA;
+                    tc_l[1] += pB;
+                }
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) ps[lane * EPL + e] = xv[e];
+                __syncwarp();
+#pragma unroll
+                for (int mb = 0; mb < D / 16; ++mb) {
+                    const float v0 = ps[mb * 16 + tc_g], v1 = ps[mb * 16 + tc_g + 8];
+                    tc_o[mb][0] = fmaf(pA, v0, tc_o[mb][0]);
+                    tc_o[mb][1] = fmaf(pB, v0, tc_o[mb][1]);
+                    tc_o[mb][2] = fmaf(pA, v1, tc_o[mb][2]);
+                    tc_o[mb][3] = fmaf(pB, v1, tc_o[mb][3]);
+                }
+                __syncwarp();
+            } else {
             if (big) {   // warp-uniform: s is
 #pragma unroll
                 for (int h = 0; h < GW; ++h) {
@@ -852,6 +1049,7 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
                 for (int e = 0; e < EPL / 2; ++e)
                     o2[h][e] = ffma2(make_float2(xv[2 * e], xv[2 * e + 1]), make_float2(p, p), o2[h][e]);
             }
+            }   // CUDA cores
             if (lane == 0 && (!SMEM_S || ts - s_off < a.chunk_cap)) store_group<GW>(Sb + (int64_t)(ts - s_off) * G + h0, s);
             if (tail_staged && wg == 0) {   // the new token's rows into the pool for later steps
                 const int32_t pg = unit_page(v, u, sn);
@@ -882,6 +1080,31 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
         // ---- CTA merge of the warp states ----
         // (state of head h0 + h of rotation place wi at [wi][h0 + h]: a head's
         // partials come from the kDecNGW warps of its head group)
+        if constexpr (kTC) {
+            float lA = tc_l[0], lB = tc_l[1];
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {   // over the lanes of the same heads
+                lA += __shfl_xor_sync(0xffffffffu, lA, o);
+                lB += __shfl_xor_sync(0xffffffffu, lB, o);
+            }
+            if (tc_g == 0) {
+                if (tc_hA < G) {
+                    mw_s[wi * G + tc_hA] = tc_m[0];
+                    lw_s[wi * G + tc_hA] = lA;
+                }
+                if (tc_hB < G) {
+                    mw_s[wi * G + tc_hB] = tc_m[1];
+                    lw_s[wi * G + tc_hB] = lB;
+                }
+            }
+#pragma unroll
+            for (int mb = 0; mb < D / 16; ++mb)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int h = (j & 1) ? tc_hB : tc_hA;
+                    if (h < G) red[(wi * G + h) * D + mb * 16 + tc_g + (j >> 1) * 8] = tc_o[mb][j];
+                }
+        } else {
         float l_w[GW];   // each head's row sum over this warp's rows
 #pragma unroll
         for (int h = 0; h < GW; ++h) {
@@ -904,6 +1127,7 @@ __global__ void __launch_bounds__(dec_threads<T, D, G>(), dec_occupancy(D * size
 #pragma unroll
             for (int e = 0; e < EPL / 2; ++e)
                 *reinterpret_cast<float2*>(&red[(wi * G + h0 + h) * D + lane * EPL + 2 * e]) = o2[h][e];
+        }   // CUDA cores
         named_bar_sync(1, NCT);
         if (ctid < G) {
             float m = -INFINITY;

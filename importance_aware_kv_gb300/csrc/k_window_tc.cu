@@ -38,24 +38,6 @@ constexpr int kMaxTcChunk = 1024;          // tokens per CTA at most
 constexpr int kMaxChunkPages = kMaxTcChunk / 16 + 1;   // pages such a chunk can touch (pages hold >= 16 tokens)
 constexpr int kTcGroups = kTcTok / 16;     // 16-row TMA row groups per tile
 
-__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%0, %1, %2, %3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// Four 8x8 b16 matrices from shared memory: lane l gives the address of row
-// (l mod 8) of matrix l / 8 (16 contiguous bytes); register i receives matrix
-// i, each lane holding row lane / 4, columns 2 (lane mod 4) and + 1 -- for a
-// token-major K tile that is the B fragment of mma m16n8k16 (col-major B).
-__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t saddr) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(saddr));
-}
-
 template <int D, int NQV>
 struct WinTc {
     static constexpr int RB = NQV / 16;            // row blocks
