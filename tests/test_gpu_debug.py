@@ -65,6 +65,15 @@ def test_debug_ragged_budgets(debug, fused, small_mode):
     _run(SMALL.with_(sink=1, window=16), budgets=b, fused=fused, small_mode=small_mode)
 
 
+@FUSED
+@pytest.mark.parametrize("cs", [None, 3])
+def test_debug_group_of_eight_on_the_tensor_cores(debug, fused, cs):
+    # G = 8 runs q.k and p.v as mma over whole tiles: a partial tile's rows
+    # outside the CTA's slots (chunk edges, the ragged tail) hold NaN in this
+    # mode, so they must be zeroed before the product, not just weighted by 0
+    _run(SMALL.with_(hq=16, hkv=2, prompt=700, budget=250, window=24), fused=fused, cs=cs)
+
+
 def test_debug_batched_eviction_compaction(debug):
     _run(SMALL.with_(evict_every=16, steps=48, budget=120, window=20), fused=True)
 
