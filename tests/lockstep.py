@@ -178,9 +178,12 @@ class Lockstep:
         qs = np.ascontiguousarray(np.moveaxis(q, 3, 0))
         return ks, vs, qs
 
-    def decode(self, steps=None, compare_every=1, fused=False):
+    def decode(self, steps=None, compare_every=1, fused=False, per_layer=False):
         """Run the decode steps; fused=True drives each step through the
-        single append+decode+evict call instead of the three calls."""
+        single append+decode+evict call instead of the three calls;
+        per_layer=True makes that one fused call per layer, back to back on
+        the stream, as a model's layers issue them (consecutive launches on
+        disjoint units may overlap by programmatic dependent launch)."""
         w = self.w
         steps = w.steps if steps is None else steps
         ks, vs, qs = self._decode_inputs()
@@ -189,7 +192,11 @@ class Lockstep:
         for s in range(steps):
             evict_now = (s + 1) % w.evict_every == 0
             for ls in self._all():
-                if fused:
+                if fused and per_layer:
+                    for l in range(w.layers):
+                        ls.cache.step(dks[s][l:l + 1], dvs[s][l:l + 1], dqs[s][l:l + 1], out[l:l + 1],
+                                      evict=evict_now, layer0=l)
+                elif fused:
                     ls.cache.step(dks[s], dvs[s], dqs[s], out, evict=evict_now)
                 else:
                     ls.cache.append(dks[s], dvs[s])

@@ -434,3 +434,21 @@ def test_host_errors_leave_cache_usable():
     assert list(c.lengths()) == [17, 17]
     c.device_status()
     c.close()
+
+
+# One fused call per layer, back to back on the stream: each launch may start
+# while the previous one runs (programmatic dependent launch), loading its own
+# layer's tiles (and, for small calls, prefetching them into L2) before the
+# previous grid completes, and reading q and the new rows only after.
+@pytest.mark.parametrize("kw", [
+    dict(layers=6),                                          # G = 4, one eviction a step
+    dict(layers=5, hq=16, hkv=2, budget=250, window=24),     # G = 8 (tensor cores)
+    dict(layers=4, evict_every=4, steps=24),                 # batched evictions between the layer calls
+], ids=["g4", "g8", "evict_every4"])
+def test_per_layer_launches(kw):
+    w = SMALL.with_(**kw)
+    ls = _ls(w)
+    ls.prefill()
+    rep = ls.decode(fused=True, per_layer=True)
+    ls.cache.close()
+    assert rep.evictions_checked > 0
