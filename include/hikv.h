@@ -116,7 +116,11 @@ typedef struct {
 
 /* Create a cache: allocates the page pool, page tables, per-slot importance
  * (fp32) and position (int32) arrays, and the work buffers, with cudaMalloc
- * on the current device.  Synchronous.  On success *out owns all of it.
+ * on the current device.  The work buffers include the decode kernel's
+ * logits for chunks too long for shared memory, G fp32 per slot of every
+ * unit (max_tokens x G x 4 bytes a unit, about 6 % of the K/V pool at d =
+ * 128 in bf16), so that no call allocates.  Synchronous.  On success *out
+ * owns all of it.
  * Errors: INVALID_ARG (config), UNSUPPORTED (G or d or dtype), OUT_OF_MEMORY. */
 hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out);
 
