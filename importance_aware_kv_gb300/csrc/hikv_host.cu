@@ -319,8 +319,8 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
     }
     c->wchunks = ceil_div(c->cap, kWindowChunk);
     // the decode kernel's global logits (a CTA's chunk too large for shared
-    // memory): always there (G floats a slot, about 6 % of the K/V bytes at
-    // d = 128), so that the cluster size is chosen by cost, not by what fits
+    // memory): always there (G floats a slot, 3-6 % of the K/V bytes at
+    // d = 128 in bf16), so that the cluster size is chosen by cost, not by what fits
     // shared memory -- one CTA per unit with global logits beats two with
     // shared-memory logits on ragged budgets (HeadKV workload: 157 vs 183 us)
     const bool need_logits = true;

@@ -118,9 +118,9 @@ typedef struct {
  * (fp32) and position (int32) arrays, and the work buffers, with cudaMalloc
  * on the current device.  The work buffers include the decode kernel's
  * logits for chunks too long for shared memory, G fp32 per slot of every
- * unit (max_tokens x G x 4 bytes a unit, about 6 % of the K/V pool at d =
- * 128 in bf16), so that no call allocates.  Synchronous.  On success *out
- * owns all of it.
+ * unit (max_tokens x G x 4 bytes a unit: 3 % of the K/V pool at G = 4, 6 %
+ * at G = 8, with d = 128 in bf16), so that no call allocates.  Synchronous.
+ * On success *out owns all of it.
  * Errors: INVALID_ARG (config), UNSUPPORTED (G or d or dtype), OUT_OF_MEMORY. */
 hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out);
 
