@@ -123,6 +123,7 @@ struct hikv_cache {
     std::vector<uint64_t> sasg_key;     // [L]
     int small_mode = 1;                 // HIKV_DECODE_SMALL (tuning): 0 never, 1 auto, 2 always when eligible
     int first_burst = 4;                // one tile per consumer warp first (HIKV_DECODE_BURST: tuning)
+    int prefetch_override = -1;         // HIKV_DECODE_PREFETCH (tuning): L2 prefetch distance in tiles, -1 auto
     CUtensorMap tmap;                   // the pool as rows of d elements, 16 x 128-byte swizzled boxes
     std::vector<void*> allocs;
     // host mirror
@@ -278,6 +279,7 @@ hikv_status hikv_create_cache(const hikv_config* cfg, hikv_cache** out) {
     if (const char* e = std::getenv("HIKV_DECODE_CS")) c->cs_override = std::atoi(e);
     if (const char* e = std::getenv("HIKV_DECODE_SMALL")) c->small_mode = std::atoi(e);
     if (const char* e = std::getenv("HIKV_DECODE_BURST")) c->first_burst = std::atoi(e);
+    if (const char* e = std::getenv("HIKV_DECODE_PREFETCH")) c->prefetch_override = std::atoi(e);
     if (const char* e = std::getenv("HIKV_PDL")) c->pdl_on = std::atoi(e) != 0;
 
     cudaError_t e = cudaGetDevice(&c->device);
@@ -765,7 +767,7 @@ hikv_status launch_clusters(hikv_cache* c, int32_t layer0, int32_t nl, const std
     a.assign_off = d_assign_off;
     // small calls fit in L2: prefetch each CTA's tiles there ahead of the ring
     const int64_t call_bytes = total * 2 * c->d * c->esz;
-    a.prefetch_tiles = call_bytes <= (48ll << 20) ? 16 : 0;
+    a.prefetch_tiles = c->prefetch_override >= 0 ? c->prefetch_override : (call_bytes <= (48ll << 20) ? 16 : 0);
     a.first_burst = c->first_burst;
     a.fused = fused;
     a.evict = evict;
