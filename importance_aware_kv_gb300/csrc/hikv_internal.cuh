@@ -102,20 +102,25 @@ __host__ __device__ inline int32_t pages_kept(int32_t B, int32_t page_tokens, in
 __host__ __device__ constexpr int dec_occupancy(int /*row_bytes*/, int /*group*/) { return 2; }
 // consumer warps of one head group
 __host__ __device__ constexpr int dec_consumer_warps(int /*row_bytes*/, int /*group*/) { return 4; }
+// Tensor-core decode (HIKV_DECODE_TC=1 at compile time): groups of eight
+// query heads on bf16 rows of d = 128 run q.k and p.v as mma.sync m16n8k16
+// (the eight heads in one warp's n = 8), with one head group.  Measured on
+// the 70B shape (640 units of 4,097 tokens): 312 us against 404 us for the
+// two CUDA-core head groups.  Off by default: on that shape's heavy-hitter
+// logits it failed the one-ulp bf16 output check in one full test run of
+// three (two-ulp errors on outputs of the first head of a group), and the
+// cause -- the mma's accumulation precision or a fault in this path -- was
+// not found.  With four heads the CUDA-core row-split path is as fast.
+#ifndef HIKV_DECODE_TC
+#define HIKV_DECODE_TC 0
+#endif
+__host__ __device__ constexpr bool dec_tc(int elem_bytes, int d, int group) {
+    return HIKV_DECODE_TC != 0 && elem_bytes == 2 && d == 128 && group == 8;
+}
 // Head groups of a decode CTA: with G = 8 each tile is consumed by two warps,
 // one per half of the group's query heads (two sets of dec_consumer_warps
 // warps rotating over the same tiles), so a warp carries the state of four
 // heads and twice the warps hide the tile loop's latency.
-// Groups of eight query heads on bf16 rows of d = 128 run q.k and p.v on
-// the tensor cores (mma.sync m16n8k16, the eight heads in one warp's n = 8),
-// with one head group.  Measured on the 70B shape (640 units of 4,097
-// tokens) 312 us against 404 us for the two CUDA-core head groups; with four
-// heads the CUDA-core row-split path is as fast or slightly faster (the
-// Llama-3-8B layer 20.9 us both, the 32-layer stack 259.7 against 261.6 us),
-// so smaller groups stay on it.
-__host__ __device__ constexpr bool dec_tc(int elem_bytes, int d, int group) {
-    return elem_bytes == 2 && d == 128 && group == 8;
-}
 __host__ __device__ constexpr int dec_head_groups(int group, bool tc) { return group == 8 && !tc ? HIKV_G8_GROUPS : 1; }
 __host__ __device__ constexpr int dec_stages(int /*row_bytes*/, int /*group*/) { return 8; }
 

@@ -67,10 +67,10 @@ def test_debug_ragged_budgets(debug, fused, small_mode):
 
 @FUSED
 @pytest.mark.parametrize("cs", [None, 3])
-def test_debug_group_of_eight_on_the_tensor_cores(debug, fused, cs):
-    # G = 8 runs q.k and p.v as mma over whole tiles: a partial tile's rows
-    # outside the CTA's slots (chunk edges, the ragged tail) hold NaN in this
-    # mode, so they must be zeroed before the product, not just weighted by 0
+def test_debug_group_of_eight_partial_tiles(debug, fused, cs):
+    # G = 8 with partial tiles: their rows outside the CTA's slots (chunk
+    # edges, the ragged tail) hold NaN in this mode, and must be skipped (or,
+    # on the tensor-core path, zeroed before the mma) rather than weighted by 0
     _run(SMALL.with_(hq=16, hkv=2, prompt=700, budget=250, window=24), fused=fused, cs=cs)
 
 
