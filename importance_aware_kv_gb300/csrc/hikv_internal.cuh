@@ -108,9 +108,11 @@ __host__ __device__ constexpr int dec_consumer_warps(int /*row_bytes*/, int /*gr
 // the 70B shape (640 units of 4,097 tokens): 312 us against 404 us for the
 // two CUDA-core head groups.  Off by default: on that shape's heavy-hitter
 // logits it failed the one-ulp bf16 output check in one full test run of
-// three (two-ulp errors on outputs of the first head of a group), and the
-// cause -- the mma's accumulation precision or a fault in this path -- was
-// not found.  With four heads the CUDA-core row-split path is as fast.
+// three (two-ulp errors on outputs of the first head of a group) with the
+// same code and data that passed the other two: not deterministic, so more
+// likely a race in this path than the mma's accumulation precision; the
+// cause was not found.  With four heads the CUDA-core row-split path is as
+// fast.
 #ifndef HIKV_DECODE_TC
 #define HIKV_DECODE_TC 0
 #endif
