@@ -2,7 +2,7 @@
 //
 // A decode step reads its retained K/V rows once.  The fastest any kernel can
 // touch that many bytes from HBM in one launch -- ramp-up and tail included --
-// is the floor the step's time is judged against.  This kernel does nothing
+// is the floor the step's time is compared with.  This kernel does nothing
 // else: every thread issues eight independent 16-byte streaming loads per
 // round (a grid-stride sweep, so a warp reads 512 contiguous bytes per load),
 // folds them into a register, and stores nothing unless the fold hits one

@@ -10,8 +10,7 @@ head) and indexed by token position, so any subset of units or positions can
 be regenerated on its own (the oracle checks sampled layers of the big
 workloads this way).
 
-Workload shapes follow the five evaluation settings of the benchmark spec:
-tiny fp32 (GQA group 2), a Llama-3-8B-shaped layer, a 32-layer 32K-context
+Five workload shapes: tiny fp32 (GQA group 2), a Llama-3-8B-shaped layer, a 32-layer 32K-context
 stack evicting every 16 steps, HeadKV-style Dirichlet budgets, and a
 Llama-3-70B-shaped 128K context.  Heavy-hitter keys stand in for the
 observation (KV cache compression blog, sec. 2 "Heavy Hitter Tokens") that
